@@ -1,0 +1,467 @@
+#!/usr/bin/env python
+"""Decode-step benchmark of the QSA sparse-attention path on GB300.
+
+A step is one decode step of one QSA layer: pooled-key cache update, index score of every
+pooled row, block-domain top-k, cell list, sparse attention over the selected cells.
+Each step appends one token to its layer; steps rotate over ``--layers`` independent
+layer sets (12 QSA layers per token in the pages' model), so successive steps never
+re-read the same pooled cache from L2.
+
+Prints one JSON line: decode steps/s at the primary context (255,181 tokens by default),
+with the 61,789 / 126,253 / 255,181-token sweep, the HBM roofline of the score scan, an
+end-to-end figure with host buffers, SM clocks sampled during the timed region and the
+fp64 CPU oracle timed on a bounded sample as a baseline.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun every rank runs an independent replica ("replicas only": the decode path
+of one sequence does not shard); value = steps of all ranks / max time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "sparse-attn decode steps/s at 64k/128k/256k ctx; achieved HBM GB/s vs roofline"
+CONTEXTS = {"64k": "decode_64k", "128k": "decode_128k", "256k": "decode_256k"}
+SCORE_SRC = os.path.join(ROOT, "gather_qsa_pool_gb300", "csrc", "index_score.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "score_rows_256k_traffic.txt")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3072)
+    ap.add_argument("--warmup", type=int, default=24)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--contexts", default="64k,128k,256k")
+    ap.add_argument("--primary", default="256k")
+    ap.add_argument("--layers", type=int, default=12)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------------------- plumbing
+
+def dist_setup():
+    import torch
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampled every 20 ms while the timed region runs."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "20"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def mark(self):
+        return time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self, t0: float, t1: float):
+        rows = []
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                frac = float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+                rows.append((ts + frac, float(parts[2]), float(parts[3]), parts[6:10]))
+            except Exception:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sel = [r for r in rows if t0 - 0.05 <= r[0] <= t1 + 0.05] or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in sel for i, v in enumerate(r[3]) if v == "Active"})
+        return {"sm_mhz": statistics.median(r[1] for r in sel),
+                "sm_max_mhz": max(r[2] for r in sel), "reasons": reasons, "samples": len(sel)}
+
+
+def traffic_per_launch(n_rows_primary: int):
+    """DRAM bytes per score launch from the committed ncu summary, if it was taken on the
+    current kernel source (else None)."""
+    try:
+        with open(SCORE_SRC, "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()[:16]
+        kv = {}
+        with open(TRAFFIC_FILE) as f:
+            for ln in f:
+                if "=" in ln and not ln.startswith("#"):
+                    k, v = ln.split("=", 1)
+                    kv[k.strip()] = v.strip()
+        if kv.get("kernel_source_sha256_16") != sha:
+            return None
+        per_row = float(kv["dram_bytes_per_row"])
+        return per_row * n_rows_primary
+    except Exception:
+        return None
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+def run_context(name, args, world, rank, local, want_clocks):
+    import torch
+
+    import gather_qsa_pool_gb300 as qsa
+    import qsa_synth
+
+    shape = qsa_synth.CONFIGS[CONTEXTS[name]]
+    L = args.layers
+    K, W = args.steps, args.warmup
+    k_kernel = max(L, min(K, 4 * L * 16))
+    k_e2e = max(L, min(K, 1024))
+    total_steps = W + K + k_e2e + 2
+    extra = total_steps // L + 2
+    dev = torch.device("cuda", local)
+    n_q_pool = 32
+
+    layers, caches = [], []
+    for li in range(L):
+        inp = qsa_synth.decode_inputs_torch(shape, seed=1000 * (rank + 1) + li, device=dev,
+                                            extra_tokens=extra, n_steps=n_q_pool)
+        lay = qsa.DecodeLayer(cap_tokens=shape.n_ctx + extra, H_idx=shape.H_idx,
+                              d_idx=shape.d_idx, H_q=shape.H_q, H_kv=shape.H_kv, d=shape.d,
+                              top_k_tokens=shape.top_k_tokens, eps=shape.eps,
+                              rope_base=shape.rope_base, device=dev)
+        lay.rebuild(inp["raw_k"], inp["norm_w"], shape.n_ctx - 1)
+        lay.bind(inp["raw_k"], inp["norm_w"], inp["K"], inp["V"])
+        layers.append(lay)
+        caches.append(inp)
+        del inp
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    sp = stream.cuda_stream
+    n_ctx = [shape.n_ctx] * L  # context length of each layer's next step
+    q_ptrs = [([c["q_idx"][j].data_ptr() for j in range(n_q_pool)],
+               [c["q"][j].data_ptr() for j in range(n_q_pool)]) for c in caches]
+
+    def step(s):
+        li = s % L
+        j = (s // L) % n_q_pool
+        layers[li].step_ptr(n_ctx[li], q_ptrs[li][0][j], q_ptrs[li][1][j], sp)
+        n_ctx[li] += 1
+
+    s = 0
+    for _ in range(W):
+        step(s)
+        s += 1
+    torch.cuda.synchronize()
+    barrier(world)
+    sampler = None
+    if want_clocks:
+        sampler = ClockSampler(local)
+        sampler.start()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    barrier(world)
+    t_wall0 = time.time()
+    ev0.record(stream)
+    for _ in range(K):
+        step(s)
+        s += 1
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    barrier(world)
+    ms = ev0.elapsed_time(ev1)
+    clocks = None
+    if sampler is not None:
+        sampler.stop()
+        clocks = sampler.summary(t_wall0, t_wall1)
+    ms_max = max_over_ranks(ms, world)
+
+    # score kernel alone, back to back over the rotating layers (its average duration)
+    n_rows = [(c + 3) // 4 for c in n_ctx]
+    for li in range(L):
+        qsa.index_score(caches[li]["q_idx"][0].view(1, -1), layers[li].pooled, n_rows[li],
+                        shape.H_idx, shape.d_idx, 1.0 / math.sqrt(shape.d_idx), layers[li].scores)
+    torch.cuda.synchronize()
+    ev2, ev3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev2.record(stream)
+    for i in range(k_kernel):
+        li = i % L
+        qsa.index_score(caches[li]["q_idx"][i % n_q_pool].view(1, -1), layers[li].pooled,
+                        n_rows[li], shape.H_idx, shape.d_idx, 1.0 / math.sqrt(shape.d_idx),
+                        layers[li].scores)
+    ev3.record(stream)
+    torch.cuda.synchronize()
+    score_us = ev2.elapsed_time(ev3) * 1e3 / k_kernel
+    score_rows = sum(n_rows[i % L] for i in range(k_kernel)) / k_kernel
+
+    # end to end: per step, copy the new token's rows and the queries from pinned host
+    # memory into the caches, run the step, read the output back
+    hd = shape.H_idx * shape.d_idx
+    kvd = shape.H_kv * shape.d
+    h_raw = torch.randn(hd).to(caches[0]["raw_k"].dtype).pin_memory()
+    h_k = torch.randn(kvd).to(caches[0]["K"].dtype).pin_memory()
+    h_v = torch.randn(kvd).to(caches[0]["V"].dtype).pin_memory()
+    h_qidx = torch.randn(hd).pin_memory()
+    h_q = torch.randn(shape.H_q * shape.d).pin_memory()
+    h_out = torch.empty(shape.H_q * shape.d).pin_memory()
+    d_qidx = torch.empty(hd, device=dev)
+    d_q = torch.empty(shape.H_q * shape.d, device=dev)
+    h2d = (h_raw.numel() * h_raw.element_size() + h_k.numel() * h_k.element_size()
+           + h_v.numel() * h_v.element_size() + h_qidx.numel() * 4 + h_q.numel() * 4)
+    d2h = h_out.numel() * 4
+    torch.cuda.synchronize()
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(k_e2e):
+        li = s % L
+        c = caches[li]
+        p = n_ctx[li] - 1
+        c["raw_k"][p].view(-1).copy_(h_raw, non_blocking=True)
+        c["K"][p].view(-1).copy_(h_k, non_blocking=True)
+        c["V"][p].view(-1).copy_(h_v, non_blocking=True)
+        d_qidx.copy_(h_qidx, non_blocking=True)
+        d_q.copy_(h_q, non_blocking=True)
+        layers[li].step_ptr(n_ctx[li], d_qidx.data_ptr(), d_q.data_ptr(), sp)
+        n_ctx[li] += 1
+        s += 1
+        h_out.copy_(layers[li].out.view(-1), non_blocking=True)
+        stream.synchronize()
+    t_e2e = time.perf_counter() - t0
+    t_e2e = max_over_ranks(t_e2e, world)
+
+    splits = qsa._binding.load()  # noqa: F841  (library already loaded)
+    n_cells_last = int(layers[(s - 1) % L].n_cells.item())
+    res = {
+        "ms": ms_max, "K": K, "W": W, "score_us": score_us, "score_rows": score_rows,
+        "t_e2e": t_e2e, "k_e2e": k_e2e, "h2d": h2d, "d2h": d2h, "clocks": clocks,
+        "n_cells": n_cells_last, "shape": shape, "n_ctx_end": max(n_ctx),
+    }
+    del layers, caches
+    torch.cuda.empty_cache()
+    return res
+
+
+def algorithmic_bytes(shape, n_rows, n_cells):
+    """Pooled-cache scan (fp32) + the selected K/V rows (bf16), per decode step."""
+    esize = 2 if shape.dtype == "bf16" else 4
+    return n_rows * shape.H_idx * shape.d_idx * 4 + n_cells * shape.H_kv * 2 * shape.d * esize
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+
+def oracle_decode_sample(shape, n_steps: int, budget_s: float, seed: int = 7):
+    """Time the fp64 oracle's decode step (incremental pool update of the new rows, score
+    of every row, full sort, attention) for up to n_steps steps or budget_s seconds, after
+    an untimed build of its pooled cache.  Returns (steps, seconds)."""
+    from oracle import oracle
+    import qsa_synth
+
+    inp = qsa_synth.decode_inputs(shape, seed=seed, extra_tokens=n_steps + 1, n_steps=4)
+    n0 = shape.n_ctx - 1
+    cap = (shape.n_ctx + n_steps + 4) // 4
+    pooled = np.zeros((cap, shape.H_idx * shape.d_idx), np.float32)
+    oracle.pool_rows(inp["raw_k"], n0, shape.H_idx, shape.d_idx, inp["norm_w"], shape.eps,
+                     shape.rope_base, 0, (n0 + 3) // 4, pooled)
+    valid = n0 // 4
+    done, t = 0, 0.0
+    while done < n_steps and t < budget_s:
+        n_ctx = shape.n_ctx + done
+        t0 = time.perf_counter()
+        oracle.decode_step(inp["raw_k"], n_ctx, shape.H_idx, shape.d_idx, inp["norm_w"], shape.eps,
+                           shape.rope_base, pooled, valid, inp["q_idx"][done % 4],
+                           shape.top_k_tokens, inp["q"][done % 4], inp["K"], inp["V"], shape.H_q,
+                           shape.H_kv, shape.d)
+        t += time.perf_counter() - t0
+        valid = n_ctx // 4
+        done += 1
+    return done, t
+
+
+def config_for(shape, layers):
+    return {
+        "workload": (f"bf16 decode, one QSA layer per step at {shape.n_ctx:,}-token context, "
+                     f"+1 token per step, {layers} rotating layer sets"),
+        "n_ctx": shape.n_ctx, "indexer": f"{shape.H_idx} heads x {shape.d_idx}",
+        "attention": f"{shape.H_q} q heads / {shape.H_kv} kv heads x {shape.d}",
+        "top_k_tokens": shape.top_k_tokens, "layers": layers,
+        "storage": "bf16 K/V and raw indexer keys, fp32 pooled-key cache",
+        "l2": (f"inputs larger than L2: {layers} rotating layer sets of "
+               f"{shape.n_rows * shape.H_idx * shape.d_idx * 4 / 1e6:.0f} MB pooled cache each"),
+    }
+
+
+def main():
+    args = parse_args()
+    import qsa_synth
+
+    primary = qsa_synth.CONFIGS[CONTEXTS[args.primary]]
+
+    if args.impl == "reference":
+        world = int(os.environ.get("WORLD_SIZE", "1"))
+        rank = int(os.environ.get("RANK", "0"))
+        if rank != 0:
+            return
+        W = min(args.warmup, 1)
+        n_done, t = oracle_decode_sample(primary, n_steps=max(1, args.steps) + W, budget_s=90.0)
+        steps = max(n_done - W, 1)
+        value = n_done / t
+        line = {
+            "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world,
+            "steps": steps, "warmup": W, "ms_per_step": 1e3 * t / n_done,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": config_for(primary, args.layers), "impl": "reference",
+            "cpu_baseline": {"value": value, "unit": "steps/s", "cores": 1, "kind": "oracle",
+                             "sample": f"{n_done} consecutive oracle decode steps of one layer "
+                                       f"at {primary.n_ctx:,} tokens (bounded to ~90 s), after "
+                                       f"an untimed build of its pooled cache"},
+            "e2e": {"value": value, "unit": "steps/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+        }
+        print(json.dumps(line))
+        return
+
+    world, rank, local = dist_setup()
+    import torch
+
+    import gather_qsa_pool_gb300 as qsa
+
+    qsa.load()
+    names = [c for c in args.contexts.split(",") if c]
+    if args.primary not in names:
+        names.append(args.primary)
+    results = {}
+    for name in names:
+        results[name] = run_context(name, args, world, rank, local,
+                                    want_clocks=(name == args.primary and rank == 0))
+    peak, peak_kind = load_peaks()
+
+    sweep = {}
+    for name, r in results.items():
+        sh = r["shape"]
+        n_rows_avg = (sh.n_ctx + sh.n_ctx + r["K"] // args.layers) // 2 // 4
+        steps_s = world * r["K"] / (r["ms"] / 1e3)
+        bytes_step = algorithmic_bytes(sh, n_rows_avg, r["n_cells"])
+        sweep[name] = {
+            "n_ctx": sh.n_ctx, "steps_per_s": steps_s, "us_per_step": r["ms"] * 1e3 / r["K"],
+            "tokens_per_s_12_layers": steps_s / 12.0,
+            "algorithmic_MB_per_step": bytes_step / 1e6,
+            "achieved_GBps_step": bytes_step * steps_s / world / 1e9,
+            "frac_of_hbm_peak_step": bytes_step * steps_s / world / 1e9 / peak,
+            "score_kernel_us": r["score_us"],
+            "score_kernel_GBps": r["score_rows"] * sh.H_idx * sh.d_idx * 4 / r["score_us"] / 1e3,
+            "e2e_steps_per_s": world * r["k_e2e"] / r["t_e2e"],
+        }
+    r = results[args.primary]
+    sh = r["shape"]
+    value = sweep[args.primary]["steps_per_s"]
+    score_bytes = r["score_rows"] * sh.H_idx * sh.d_idx * 4 + r["score_rows"] * 4
+    achieved = score_bytes / (r["score_us"] * 1e-6) / 1e9
+    traffic = traffic_per_launch(int(r["score_rows"]))
+
+    cpu_baseline = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        n_done, t = oracle_decode_sample(sh, n_steps=40, budget_s=20.0)
+        cpu_baseline = {"value": n_done / t, "unit": "steps/s", "cores": 1, "kind": "oracle",
+                        "sample": f"{n_done} consecutive fp64 oracle decode steps of one layer at "
+                                  f"{sh.n_ctx:,} tokens (pool update, score of all "
+                                  f"{sh.n_rows:,} rows, full sort, attention), after an untimed "
+                                  f"build of its pooled cache; single-threaded C"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world,
+        "steps": r["K"], "warmup": r["W"], "ms_per_step": r["ms"] / r["K"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded N(0,1) keys/values/queries, 1% of blocks +3 on raw indexer keys)",
+        "config": config_for(sh, args.layers),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "kernel": "score_rows_kernel (qsa_index_score, decode)",
+                     "peak_source": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_kind == "measured" else "fallback 6.8 TB/s"},
+        "e2e": {"value": sweep[args.primary]["e2e_steps_per_s"], "unit": "steps/s",
+                "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
+        "gpu_launches": r["K"] * 6,
+        "clocks": r["clocks"],
+        "sweep": sweep,
+        "cpu_baseline": cpu_baseline,
+    }
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

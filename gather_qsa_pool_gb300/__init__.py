@@ -1,0 +1,28 @@
+"""GB300 (sm_103a) QSA two-stage sparse attention.
+
+The compute lives in ``libqsa.so`` (hand-written CUDA kernels behind a C ABI declared in
+``include/qsa.h``); this package is its ctypes binding plus a small decode-step driver
+that owns the per-layer device buffers.  There is no CPU or PyTorch fallback.
+"""
+from ._binding import (  # noqa: F401
+    QSA_BF16,
+    QSA_F32,
+    QSA_PREC_BF16_TC,
+    QSA_PREC_F32,
+    QSAError,
+    decode_step,
+    gather_kv,
+    header_functions,
+    index_score,
+    index_score_workspace_size,
+    load,
+    mask_sparse_eligible,
+    mask_to_list,
+    pool_update,
+    sparse_attn,
+    sparse_attn_workspace_size,
+    status_str,
+    topk_blocks,
+    topk_max_candidates,
+)
+from .decode import DecodeLayer  # noqa: F401

@@ -1,0 +1,215 @@
+"""ctypes binding of ``libqsa.so``: argument marshalling only.
+
+Every function here has the name of the C entry point it calls (without the ``qsa_``
+prefix), takes torch tensors that already live on the GPU, passes their data pointers,
+sizes and the current CUDA stream, and raises :class:`QSAError` when the call returns a
+non-OK status.  All computation happens in the library's CUDA kernels; there is no
+fallback of any kind: if the library is missing or fails to load, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "_build", "libqsa.so")
+HEADER = os.path.join(os.path.dirname(HERE), "include", "qsa.h")
+
+QSA_OK, QSA_ERR_INVALID_ARG, QSA_ERR_UNSUPPORTED, QSA_ERR_CUDA, QSA_ERR_TIMEOUT = range(5)
+QSA_F32, QSA_BF16 = 0, 1
+QSA_PREC_F32, QSA_PREC_BF16_TC = 0, 1
+
+_p = ctypes.c_void_p
+_i64 = ctypes.c_int64
+_int = ctypes.c_int
+_f = ctypes.c_float
+_d = ctypes.c_double
+_sz = ctypes.c_size_t
+
+_SIGNATURES = {
+    "qsa_status_str": (ctypes.c_char_p, [_int]),
+    "qsa_version": (_int, []),
+    "qsa_pool_update": (_int, [_p, _int, _i64, _int, _int, _p, _f, _d, _p, _i64, _i64, _p]),
+    "qsa_index_score": (_int, [_p, _i64, _i64, _p, _p, _i64, _int, _int, _f, _p, _i64, _int,
+                               _p, _sz, _p]),
+    "qsa_index_score_workspace_size": (_sz, [_i64, _i64, _int, _int, _int]),
+    "qsa_topk_blocks": (_int, [_p, _i64, _i64, _p, _i64, _i64, _p, _p, _p]),
+    "qsa_topk_max_candidates": (_i64, []),
+    "qsa_gather_kv": (_int, [_p, _p, _int, _i64, _int, _int, _int, _i64, _i64, _p, _p, _i64,
+                             _i64, _p, _i64, _p, _p, _p, _p, _i64, _p]),
+    "qsa_sparse_attn": (_int, [_p, _i64, _int, _int, _int, _int, _f, _p, _p, _int, _i64, _i64,
+                               _i64, _p, _p, _i64, _p, _p, _p, _sz, _p]),
+    "qsa_sparse_attn_workspace_size": (_sz, [_i64, _int, _int, _int, _i64]),
+    "qsa_decode_step": (_int, [_p, _int, _i64, _int, _int, _p, _f, _d, _p, _i64, _i64, _p, _f,
+                               _p, _i64, _p, _p, _p, _p, _int, _i64, _int, _int, _i64, _p, _p,
+                               _i64, _p, _int, _f, _p, _p, _p, _sz, _p]),
+    "qsa_mask_to_list": (_int, [_p, _i64, _i64, _i64, _i64, _p, _p, _p, _p]),
+    "qsa_mask_sparse_eligible": (_int, [_int, _f, _f, _i64, _i64]),
+}
+
+_lib = None
+
+
+class QSAError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn} returned {status_str(status)}")
+
+
+def header_functions() -> list[str]:
+    """Names of every function that include/qsa.h declares."""
+    with open(HEADER) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"^\s*(?:[\w\s\*]+?)\b(qsa_\w+)\s*\(", text, re.M)))
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Load the library (building it first when its sources are newer)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if path is None:
+        from . import build as _build
+
+        path = _build.build()
+    if not os.path.exists(path):
+        raise RuntimeError(f"QSA CUDA library not found at {path}")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in _SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def status_str(status: int) -> str:
+    return load().qsa_status_str(status).decode()
+
+
+def _check(fn: str, status: int):
+    if status != QSA_OK:
+        raise QSAError(fn, status)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dtype(t) -> int:
+    import torch
+
+    if t.dtype == torch.float32:
+        return QSA_F32
+    if t.dtype == torch.bfloat16:
+        return QSA_BF16
+    raise TypeError(f"QSA tensors are float32 or bfloat16, got {t.dtype}")
+
+
+# --------------------------------------------------------------------------- entry points
+
+def pool_update(raw_k, n_ctx, H, d, norm_w, eps, rope_base, pooled, n_valid_full, stream=None):
+    """qsa_pool_update: recompute pooled rows [n_valid_full, ceil(n_ctx/4))."""
+    _check("qsa_pool_update", load().qsa_pool_update(
+        _ptr(raw_k), _dtype(raw_k), n_ctx, H, d, _ptr(norm_w), eps, rope_base, _ptr(pooled),
+        pooled.shape[0], n_valid_full, _stream(stream)))
+
+
+def index_score_workspace_size(n_q, n_rows, H, d, precision=QSA_PREC_F32) -> int:
+    return int(load().qsa_index_score_workspace_size(n_q, n_rows, H, d, precision))
+
+
+def index_score(q, pooled, n_rows, H, d, scale, scores, q_pos=None, precision=QSA_PREC_F32,
+                workspace=None, stream=None):
+    """qsa_index_score: scores[i][b] for b < n_rows (q: [n_q][>= H*d] fp32)."""
+    n_q = q.shape[0] if q.dim() > 1 else 1
+    ld_q = q.stride(0) if q.dim() > 1 else H * d
+    ld_s = scores.stride(0) if scores.dim() > 1 else n_rows
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("qsa_index_score", load().qsa_index_score(
+        _ptr(q), n_q, ld_q, _ptr(q_pos), _ptr(pooled), n_rows, H, d, scale, _ptr(scores), ld_s,
+        precision, _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def topk_max_candidates() -> int:
+    return int(load().qsa_topk_max_candidates())
+
+
+def topk_blocks(scores, n_full, k_blk, blocks_out, counts_out, q_pos=None, stream=None):
+    """qsa_topk_blocks over the first n_full columns of each score row."""
+    n_q = scores.shape[0] if scores.dim() > 1 else 1
+    ld = scores.stride(0) if scores.dim() > 1 else scores.shape[0]
+    _check("qsa_topk_blocks", load().qsa_topk_blocks(
+        _ptr(scores), n_q, ld, _ptr(q_pos), n_full, k_blk, _ptr(blocks_out), _ptr(counts_out),
+        _stream(stream)))
+
+
+def gather_kv(blocks, counts, k_blk, pos_out, n_cells_out, max_cells, n_ctx=-1, q_pos=None,
+              K=None, V=None, K_out=None, V_out=None, H_kv=0, d_k=0, d_v=0, n_kv=None,
+              stream=None):
+    """qsa_gather_kv: cell positions (and compact K/V rows when K_out / V_out are given)."""
+    n_q = counts.shape[0]
+    dt = _dtype(K) if K is not None else QSA_BF16
+    if n_kv is None:
+        n_kv = K.shape[0] if K is not None else (1 << 62)
+    ld_k = K.stride(0) if K is not None else H_kv * d_k
+    ld_v = V.stride(0) if V is not None else H_kv * d_v
+    _check("qsa_gather_kv", load().qsa_gather_kv(
+        _ptr(K), _ptr(V), dt, n_kv, H_kv, d_k, d_v, ld_k, ld_v, _ptr(blocks), _ptr(counts), n_q,
+        k_blk, _ptr(q_pos), n_ctx, _ptr(K_out), _ptr(V_out), _ptr(pos_out), _ptr(n_cells_out),
+        max_cells, _stream(stream)))
+
+
+def sparse_attn_workspace_size(n_q, H_q, H_kv, d_v, max_cells) -> int:
+    return int(load().qsa_sparse_attn_workspace_size(n_q, H_q, H_kv, d_v, max_cells))
+
+
+def sparse_attn(q, K, V, n_cells, max_cells, out, H_kv, d_k, d_v, scale, pos=None, lse=None,
+                workspace=None, ld_k=None, ld_v=None, n_kv=None, stream=None):
+    """qsa_sparse_attn: q [n_q][H_q][d_k] fp32 over listed cells of K/V."""
+    n_q, H_q = q.shape[0], q.shape[1]
+    ld_k = K.stride(0) if ld_k is None else ld_k
+    ld_v = V.stride(0) if ld_v is None else ld_v
+    n_kv = K.shape[0] if n_kv is None else n_kv
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("qsa_sparse_attn", load().qsa_sparse_attn(
+        _ptr(q), n_q, H_q, H_kv, d_k, d_v, scale, _ptr(K), _ptr(V), _dtype(K), n_kv, ld_k, ld_v,
+        _ptr(pos), _ptr(n_cells), max_cells, _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes,
+        _stream(stream)))
+
+
+def decode_step(raw_k, n_ctx, H_idx, d_idx, norm_w, eps, rope_base, pooled, n_valid_full,
+                q_idx, scale_idx, scores, k_blk, blocks, counts, K, V, H_kv, d, pos, n_cells,
+                max_cells, q, H_q, scale, out, lse=None, workspace=None, stream=None):
+    """qsa_decode_step: pool update, score, top-k, cell list and attention in one call."""
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("qsa_decode_step", load().qsa_decode_step(
+        _ptr(raw_k), _dtype(raw_k), n_ctx, H_idx, d_idx, _ptr(norm_w), eps, rope_base,
+        _ptr(pooled), pooled.shape[0], n_valid_full, _ptr(q_idx), scale_idx, _ptr(scores), k_blk,
+        _ptr(blocks), _ptr(counts), _ptr(K), _ptr(V), _dtype(K), K.shape[0], H_kv, d,
+        K.stride(0), _ptr(pos), _ptr(n_cells), max_cells, _ptr(q), H_q, scale, _ptr(out),
+        _ptr(lse), _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def mask_to_list(mask, max_list, pos_out, counts_out, bits_out=None, n_kv=None, stream=None):
+    """qsa_mask_to_list over every row of a uint8 mask [n_rows][ld]."""
+    n_rows = mask.shape[0]
+    n_kv = mask.shape[1] if n_kv is None else n_kv
+    _check("qsa_mask_to_list", load().qsa_mask_to_list(
+        _ptr(mask), n_rows, n_kv, mask.stride(0), max_list, _ptr(pos_out), _ptr(counts_out),
+        _ptr(bits_out), _stream(stream)))
+
+
+def mask_sparse_eligible(has_mask, max_bias, softcap, n_kv, max_list) -> bool:
+    st = load().qsa_mask_sparse_eligible(int(bool(has_mask)), max_bias, softcap, n_kv, max_list)
+    if st not in (QSA_OK, QSA_ERR_UNSUPPORTED):
+        raise QSAError("qsa_mask_sparse_eligible", st)
+    return st == QSA_OK

@@ -1,0 +1,301 @@
+// capi.cu -- the extern "C" entry points: argument validation on the host, then one
+// launcher call per operation.  No entry point allocates, synchronises or keeps state
+// beyond cached kernel attributes.
+#include <math.h>
+
+#include "qsa_internal.cuh"
+
+namespace qsa {
+
+int device_sm_count()
+{
+    static int cached_dev = -1;
+    static int cached_sms = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return kTargetSMs;
+    if (dev != cached_dev) {
+        int sms = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            sms <= 0)
+            sms = kTargetSMs;
+        cached_sms = sms;
+        cached_dev = dev;
+    }
+    return cached_sms;
+}
+
+}  // namespace qsa
+
+using namespace qsa;
+
+namespace {
+
+constexpr size_t kMaxSmem = 227 * 1024;
+
+inline qsa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? QSA_OK : QSA_ERR_CUDA; }
+inline bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+inline bool valid_dtype(qsa_dtype d) { return d == QSA_F32 || d == QSA_BF16; }
+inline int esize_of(qsa_dtype d) { return d == QSA_BF16 ? 2 : 4; }
+
+}  // namespace
+
+extern "C" {
+
+const char *qsa_status_str(qsa_status s)
+{
+    switch (s) {
+        case QSA_OK: return "QSA_OK";
+        case QSA_ERR_INVALID_ARG: return "QSA_ERR_INVALID_ARG";
+        case QSA_ERR_UNSUPPORTED: return "QSA_ERR_UNSUPPORTED";
+        case QSA_ERR_CUDA: return "QSA_ERR_CUDA";
+        case QSA_ERR_TIMEOUT: return "QSA_ERR_TIMEOUT";
+    }
+    return "QSA_ERR_UNKNOWN";
+}
+
+int qsa_version(void) { return (1 << 16) | 0; }
+
+static qsa_status check_pool_update(const void *raw_k, qsa_dtype raw_dtype, int64_t n_ctx, int H,
+                                    int d, const float *norm_w, float eps, double rope_base,
+                                    float *pooled, int64_t cap_rows, int64_t n_valid_full)
+{
+    if (!raw_k || !norm_w || !pooled) return QSA_ERR_INVALID_ARG;
+    if (!valid_dtype(raw_dtype) || n_ctx < 0 || H < 1 || d < 2 || (d & 1) || n_valid_full < 0 ||
+        cap_rows < 0 || !(eps >= 0.0f) || !(rope_base > 0.0))
+        return QSA_ERR_INVALID_ARG;
+    if (!aligned(raw_k, esize_of(raw_dtype)) || !aligned(norm_w, 4) || !aligned(pooled, 4))
+        return QSA_ERR_INVALID_ARG;
+    const int64_t n_rows = (n_ctx + 3) / 4;
+    const int64_t n_full = n_ctx / 4;
+    if (n_rows > cap_rows) return QSA_ERR_INVALID_ARG;
+    if ((int64_t)H * d > 48 * 1024) return QSA_ERR_UNSUPPORTED;  // row staged in shared memory
+    const int64_t row0 = n_valid_full < n_full ? n_valid_full : n_full;
+    if (n_rows - row0 > 0x7fffffffLL) return QSA_ERR_UNSUPPORTED;
+    return QSA_OK;
+}
+
+static cudaError_t run_pool_update(const void *raw_k, qsa_dtype raw_dtype, int64_t n_ctx, int H,
+                                   int d, const float *norm_w, float eps, double rope_base,
+                                   float *pooled, int64_t n_valid_full, cudaStream_t st)
+{
+    const int64_t n_rows = (n_ctx + 3) / 4;
+    const int64_t n_full = n_ctx / 4;
+    const int64_t row0 = n_valid_full < n_full ? n_valid_full : n_full;
+    return launch_pool_update(raw_k, raw_dtype, n_ctx, H, d, norm_w, eps, rope_base, pooled, row0,
+                              n_rows, st);
+}
+
+qsa_status qsa_pool_update(const void *raw_k, qsa_dtype raw_dtype, int64_t n_ctx, int H, int d,
+                           const float *norm_w, float eps, double rope_base, float *pooled,
+                           int64_t cap_rows, int64_t n_valid_full, qsa_stream_t stream)
+{
+    const qsa_status v = check_pool_update(raw_k, raw_dtype, n_ctx, H, d, norm_w, eps, rope_base,
+                                           pooled, cap_rows, n_valid_full);
+    if (v != QSA_OK) return v;
+    return from_cuda(run_pool_update(raw_k, raw_dtype, n_ctx, H, d, norm_w, eps, rope_base, pooled,
+                                     n_valid_full, (cudaStream_t)stream));
+}
+
+size_t qsa_index_score_workspace_size(int64_t n_q, int64_t n_rows, int H, int d,
+                                      qsa_precision precision)
+{
+    if (precision != QSA_PREC_BF16_TC || n_q <= 0 || n_rows <= 0 || H < 1 || d < 1) return 0;
+    return index_score_tc_workspace(n_q, n_rows, H, d);
+}
+
+static qsa_status check_index_score(const float *q, int64_t n_q, int64_t ld_q, const float *pooled,
+                                    int64_t n_rows, int H, int d, float *scores, int64_t ld_scores)
+{
+    if (!q || !pooled || !scores) return QSA_ERR_INVALID_ARG;
+    if (n_q < 0 || n_rows < 0 || H < 1 || d < 1 || ld_q < (int64_t)H * d || ld_scores < n_rows)
+        return QSA_ERR_INVALID_ARG;
+    if (!aligned(q, 4) || !aligned(pooled, 4) || !aligned(scores, 4)) return QSA_ERR_INVALID_ARG;
+    if ((n_q + 63) / 64 > 65535) return QSA_ERR_UNSUPPORTED;
+    return QSA_OK;
+}
+
+qsa_status qsa_index_score(const float *q, int64_t n_q, int64_t ld_q, const int32_t *q_pos,
+                           const float *pooled, int64_t n_rows, int H, int d, float scale,
+                           float *scores, int64_t ld_scores, qsa_precision precision,
+                           void *workspace, size_t workspace_bytes, qsa_stream_t stream)
+{
+    const qsa_status v = check_index_score(q, n_q, ld_q, pooled, n_rows, H, d, scores, ld_scores);
+    if (v != QSA_OK) return v;
+    if (precision == QSA_PREC_F32) {
+        return from_cuda(launch_index_score(q, n_q, ld_q, q_pos, pooled, n_rows, H, d, scale,
+                                            scores, ld_scores, (cudaStream_t)stream));
+    }
+    if (precision == QSA_PREC_BF16_TC) {
+        const size_t need = qsa_index_score_workspace_size(n_q, n_rows, H, d, precision);
+        if (workspace_bytes < need || (need > 0 && !workspace)) return QSA_ERR_INVALID_ARG;
+        return launch_index_score_tc(q, n_q, ld_q, q_pos, pooled, n_rows, H, d, scale, scores,
+                                     ld_scores, workspace, workspace_bytes, (cudaStream_t)stream);
+    }
+    return QSA_ERR_INVALID_ARG;
+}
+
+int64_t qsa_topk_max_candidates(void) { return topk_max_candidates(); }
+
+static qsa_status check_topk(const float *scores, int64_t n_q, int64_t ld_scores, int64_t n_full,
+                             int64_t k_blk, int32_t *blocks_out, int32_t *counts_out)
+{
+    if (!scores || !blocks_out || !counts_out) return QSA_ERR_INVALID_ARG;
+    if (n_q < 0 || k_blk < 1 || n_full < 0 || ld_scores < n_full) return QSA_ERR_INVALID_ARG;
+    if (k_blk > 0x7fffffffLL) return QSA_ERR_UNSUPPORTED;
+    if (n_full > topk_max_candidates()) return QSA_ERR_UNSUPPORTED;
+    if (n_q * (int64_t)kTopkCluster > 0x7fffffffLL) return QSA_ERR_UNSUPPORTED;
+    return QSA_OK;
+}
+
+qsa_status qsa_topk_blocks(const float *scores, int64_t n_q, int64_t ld_scores,
+                           const int32_t *q_pos, int64_t n_full, int64_t k_blk,
+                           int32_t *blocks_out, int32_t *counts_out, qsa_stream_t stream)
+{
+    const qsa_status v = check_topk(scores, n_q, ld_scores, n_full, k_blk, blocks_out, counts_out);
+    if (v != QSA_OK) return v;
+    return from_cuda(launch_topk(scores, n_q, ld_scores, q_pos, n_full, k_blk, blocks_out,
+                                 counts_out, (cudaStream_t)stream));
+}
+
+static qsa_status check_gather(const void *K, const void *V, qsa_dtype dtype, int64_t n_kv,
+                               int H_kv, int d_k, int d_v, int64_t ld_k, int64_t ld_v,
+                               const int32_t *blocks, const int32_t *counts, int64_t n_q,
+                               int64_t k_blk, const int32_t *q_pos, int64_t n_ctx, void *K_out,
+                               void *V_out, int32_t *pos_out, int32_t *n_cells_out,
+                               int64_t max_cells)
+{
+    if (!blocks || !counts || !pos_out || !n_cells_out) return QSA_ERR_INVALID_ARG;
+    if ((K_out && !K) || (V_out && !V)) return QSA_ERR_INVALID_ARG;
+    if (!valid_dtype(dtype) || n_kv < 0 || n_q < 0 || k_blk < 1 || max_cells < 4 * k_blk + 3)
+        return QSA_ERR_INVALID_ARG;
+    if (!q_pos && n_ctx < 0) return QSA_ERR_INVALID_ARG;
+    if ((K_out || V_out) && (H_kv < 1 || d_k < 1 || d_v < 1 || ld_k < (int64_t)H_kv * d_k ||
+                             ld_v < (int64_t)H_kv * d_v))
+        return QSA_ERR_INVALID_ARG;
+    if (n_q > 65535 || max_cells > 0x7fffffffLL) return QSA_ERR_UNSUPPORTED;
+    return QSA_OK;
+}
+
+qsa_status qsa_gather_kv(const void *K, const void *V, qsa_dtype dtype, int64_t n_kv, int H_kv,
+                         int d_k, int d_v, int64_t ld_k, int64_t ld_v, const int32_t *blocks,
+                         const int32_t *counts, int64_t n_q, int64_t k_blk,
+                         const int32_t *q_pos, int64_t n_ctx, void *K_out, void *V_out,
+                         int32_t *pos_out, int32_t *n_cells_out, int64_t max_cells,
+                         qsa_stream_t stream)
+{
+    const qsa_status v = check_gather(K, V, dtype, n_kv, H_kv, d_k, d_v, ld_k, ld_v, blocks, counts,
+                                      n_q, k_blk, q_pos, n_ctx, K_out, V_out, pos_out, n_cells_out,
+                                      max_cells);
+    if (v != QSA_OK) return v;
+    return from_cuda(launch_gather(K, V, dtype, n_kv, H_kv, d_k, d_v, ld_k, ld_v, blocks, counts,
+                                   n_q, k_blk, q_pos, n_ctx, K_out, V_out, pos_out, n_cells_out,
+                                   max_cells, (cudaStream_t)stream));
+}
+
+size_t qsa_sparse_attn_workspace_size(int64_t n_q, int H_q, int H_kv, int d_v, int64_t max_cells)
+{
+    if (n_q <= 0 || H_q < 1 || H_kv < 1 || d_v < 1 || max_cells < 0 || H_q % H_kv) return 0;
+    return attn_workspace_bytes(n_q, H_q, H_kv, d_v, max_cells);
+}
+
+static qsa_status check_attn(const float *q, int64_t n_q, int H_q, int H_kv, int d_k, int d_v,
+                             const void *K, const void *V, qsa_dtype dtype, int64_t n_kv,
+                             int64_t ld_k, int64_t ld_v, const int32_t *n_cells,
+                             int64_t max_cells, float *out, void *workspace,
+                             size_t workspace_bytes)
+{
+    if (!q || !K || !V || !n_cells || !out) return QSA_ERR_INVALID_ARG;
+    if (!valid_dtype(dtype) || n_q < 0 || H_q < 1 || H_kv < 1 || H_q % H_kv || d_k < 8 ||
+        d_v < 8 || d_k % 8 || d_v % 8 || n_kv < 0 || max_cells < 0 || ld_k % 8 || ld_v % 8)
+        return QSA_ERR_INVALID_ARG;
+    if (ld_k < (int64_t)H_kv * d_k || ld_v < (int64_t)H_kv * d_v) return QSA_ERR_INVALID_ARG;
+    if (!aligned(K, 16) || !aligned(V, 16) || !aligned(q, 4) || !aligned(out, 4))
+        return QSA_ERR_INVALID_ARG;
+    const int G = H_q / H_kv;
+    if (G != 1 && G != 2 && G != 4 && G != 8 && G != 16) return QSA_ERR_UNSUPPORTED;
+    if (attn_smem_bytes_host(G, d_k, d_v, esize_of(dtype)) > kMaxSmem) return QSA_ERR_UNSUPPORTED;
+    if (n_q > 65535 || H_kv > 65535) return QSA_ERR_UNSUPPORTED;
+    const size_t need = qsa_sparse_attn_workspace_size(n_q, H_q, H_kv, d_v, max_cells);
+    if (workspace_bytes < need || (need > 0 && !workspace)) return QSA_ERR_INVALID_ARG;
+    if (need > 0 && !aligned(workspace, 16)) return QSA_ERR_INVALID_ARG;
+    return QSA_OK;
+}
+
+qsa_status qsa_sparse_attn(const float *q, int64_t n_q, int H_q, int H_kv, int d_k, int d_v,
+                           float scale, const void *K, const void *V, qsa_dtype dtype,
+                           int64_t n_kv, int64_t ld_k, int64_t ld_v, const int32_t *pos,
+                           const int32_t *n_cells, int64_t max_cells, float *out,
+                           float *lse_out, void *workspace, size_t workspace_bytes,
+                           qsa_stream_t stream)
+{
+    const qsa_status v = check_attn(q, n_q, H_q, H_kv, d_k, d_v, K, V, dtype, n_kv, ld_k, ld_v,
+                                    n_cells, max_cells, out, workspace, workspace_bytes);
+    if (v != QSA_OK) return v;
+    return from_cuda(launch_sparse_attn(q, n_q, H_q, H_kv, d_k, d_v, scale, K, V, dtype, n_kv,
+                                        ld_k, ld_v, pos, n_cells, max_cells, out, lse_out,
+                                        (float *)workspace, (cudaStream_t)stream));
+}
+
+qsa_status qsa_decode_step(const void *raw_k, qsa_dtype raw_dtype, int64_t n_ctx, int H_idx,
+                           int d_idx, const float *norm_w, float eps, double rope_base,
+                           float *pooled, int64_t cap_rows, int64_t n_valid_full,
+                           const float *q_idx, float scale_idx, float *scores, int64_t k_blk,
+                           int32_t *blocks, int32_t *counts, const void *K, const void *V,
+                           qsa_dtype kv_dtype, int64_t n_kv, int H_kv, int d, int64_t ld_kv,
+                           int32_t *pos, int32_t *n_cells, int64_t max_cells, const float *q,
+                           int H_q, float scale, float *out, float *lse_out, void *workspace,
+                           size_t workspace_bytes, qsa_stream_t stream)
+{
+    const int64_t n_rows = (n_ctx + 3) / 4;
+    const int64_t n_full = n_ctx / 4;
+    qsa_status v = check_pool_update(raw_k, raw_dtype, n_ctx, H_idx, d_idx, norm_w, eps,
+                                     rope_base, pooled, cap_rows, n_valid_full);
+    if (v == QSA_OK)
+        v = check_index_score(q_idx, 1, (int64_t)H_idx * d_idx, pooled, n_rows, H_idx, d_idx,
+                              scores, n_rows);
+    if (v == QSA_OK) v = check_topk(scores, 1, n_rows, n_full, k_blk, blocks, counts);
+    if (v == QSA_OK)
+        v = check_gather(K, V, kv_dtype, n_kv, H_kv, d, d, ld_kv, ld_kv, blocks, counts, 1,
+                         k_blk, nullptr, n_ctx, nullptr, nullptr, pos, n_cells, max_cells);
+    if (v == QSA_OK)
+        v = check_attn(q, 1, H_q, H_kv, d, d, K, V, kv_dtype, n_kv, ld_kv, ld_kv, n_cells,
+                       max_cells, out, workspace, workspace_bytes);
+    if (v != QSA_OK) return v;
+    const cudaStream_t st = (cudaStream_t)stream;
+    cudaError_t e = run_pool_update(raw_k, raw_dtype, n_ctx, H_idx, d_idx, norm_w, eps, rope_base,
+                                    pooled, n_valid_full, st);
+    if (e == cudaSuccess)
+        e = launch_index_score(q_idx, 1, (int64_t)H_idx * d_idx, nullptr, pooled, n_rows, H_idx,
+                               d_idx, scale_idx, scores, n_rows, st);
+    if (e == cudaSuccess) e = launch_topk(scores, 1, n_rows, nullptr, n_full, k_blk, blocks, counts, st);
+    if (e == cudaSuccess)
+        e = launch_gather(K, V, kv_dtype, n_kv, H_kv, d, d, ld_kv, ld_kv, blocks, counts, 1, k_blk,
+                          nullptr, n_ctx, nullptr, nullptr, pos, n_cells, max_cells, st);
+    if (e == cudaSuccess)
+        e = launch_sparse_attn(q, 1, H_q, H_kv, d, d, scale, K, V, kv_dtype, n_kv, ld_kv, ld_kv,
+                               pos, n_cells, max_cells, out, lse_out, (float *)workspace, st);
+    return from_cuda(e);
+}
+
+qsa_status qsa_mask_to_list(const uint8_t *mask, int64_t n_rows, int64_t n_kv, int64_t ld_mask,
+                            int64_t max_list, int32_t *pos_out, int32_t *counts_out,
+                            uint64_t *bits_out, qsa_stream_t stream)
+{
+    if (!mask || !counts_out || (!pos_out && max_list > 0)) return QSA_ERR_INVALID_ARG;
+    if (n_rows < 0 || n_kv < 0 || ld_mask < n_kv || max_list < 0) return QSA_ERR_INVALID_ARG;
+    if (bits_out && !aligned(bits_out, 8)) return QSA_ERR_INVALID_ARG;
+    if (n_kv > 0x7fffffffLL || n_rows > 0x7fffffffLL) return QSA_ERR_UNSUPPORTED;
+    return from_cuda(launch_mask_to_list(mask, n_rows, n_kv, ld_mask, max_list, pos_out,
+                                         counts_out, bits_out, (cudaStream_t)stream));
+}
+
+qsa_status qsa_mask_sparse_eligible(int has_mask, float max_bias, float softcap, int64_t n_kv,
+                                    int64_t max_list)
+{
+    if (n_kv < 0 || max_list < 0) return QSA_ERR_INVALID_ARG;
+    if (!has_mask || max_bias != 0.0f || softcap != 0.0f) return QSA_ERR_UNSUPPORTED;
+    if (n_kv < 4096 || n_kv < 2 * max_list) return QSA_ERR_UNSUPPORTED;
+    return QSA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,141 @@
+// qsa_internal.cuh -- shared device helpers and launcher declarations of the sm_103a
+// QSA library.  Only the library's own .cu files include this header.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <utility>
+
+#include "../../include/qsa.h"
+
+namespace qsa {
+
+// GB300: 152 SMs.  Split counts that must be known without a device (workspace sizes)
+// are derived from this constant; launch grids query the device.
+constexpr int kTargetSMs = 152;
+
+// ------------------------------------------------------------------ element loads
+
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+// 16-byte streaming load: read once, do not keep in L1, ask L2 for 256-byte sectors.
+__device__ __forceinline__ float4 ld_stream_f4(const float4 *p)
+{
+    float4 v;
+    asm("ld.global.nc.L1::no_allocate.L2::256B.v4.f32 {%0,%1,%2,%3}, [%4];"
+        : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+        : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ float warp_max(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+// ------------------------------------------------------------------ programmatic launch
+// Every kernel waits for the preceding grid in the stream before touching global memory
+// (a no-op when it was launched without the programmatic-serialisation attribute), then
+// lets its successor launch: the successor's CTAs become resident as this grid's CTAs
+// retire and block in their own wait until this grid has completed and flushed, which
+// hides the launch gap between the small kernels of a decode step.
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                   cudaStream_t stream, int cluster_x, Args &&...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    int n = 0;
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+    if (cluster_x > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = (unsigned)cluster_x;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = (unsigned)n;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args...);
+    if (e == cudaErrorNotSupported || e == cudaErrorInvalidValue) {
+        // a stream that does not take programmatic serialisation: launch plainly
+        (void)cudaGetLastError();
+        cfg.attrs = attr + 1;
+        cfg.numAttrs = (unsigned)(n - 1);
+        e = cudaLaunchKernelEx(&cfg, kernel, args...);
+    }
+    return e;
+}
+
+int device_sm_count();
+
+// ------------------------------------------------------------------ launchers
+// Host-side launchers, one per kernel family; arguments are already validated.
+
+cudaError_t launch_pool_update(const void *raw_k, qsa_dtype dt, int64_t n_ctx, int H, int d,
+                               const float *norm_w, float eps, double rope_base,
+                               float *pooled, int64_t row0, int64_t row1, cudaStream_t st);
+
+cudaError_t launch_index_score(const float *q, int64_t n_q, int64_t ld_q, const int32_t *q_pos,
+                               const float *pooled, int64_t n_rows, int H, int d, float scale,
+                               float *scores, int64_t ld_scores, cudaStream_t st);
+
+qsa_status launch_index_score_tc(const float *q, int64_t n_q, int64_t ld_q,
+                                 const int32_t *q_pos, const float *pooled, int64_t n_rows,
+                                 int H, int d, float scale, float *scores, int64_t ld_scores,
+                                 void *workspace, size_t ws_bytes, cudaStream_t st);
+size_t index_score_tc_workspace(int64_t n_q, int64_t n_rows, int H, int d);
+
+constexpr int kTopkCluster = 8;
+constexpr int kTopkThreads = 512;
+int64_t topk_max_candidates();
+cudaError_t launch_topk(const float *scores, int64_t n_q, int64_t ld, const int32_t *q_pos,
+                        int64_t n_full, int64_t k_blk, int32_t *blocks_out, int32_t *counts_out,
+                        cudaStream_t st);
+
+cudaError_t launch_gather(const void *K, const void *V, qsa_dtype dt, int64_t n_kv, int H_kv,
+                          int d_k, int d_v, int64_t ld_k, int64_t ld_v, const int32_t *blocks,
+                          const int32_t *counts, int64_t n_q, int64_t k_blk,
+                          const int32_t *q_pos, int64_t n_ctx, void *K_out, void *V_out,
+                          int32_t *pos_out, int32_t *n_cells_out, int64_t max_cells,
+                          cudaStream_t st);
+
+int attn_num_splits(int64_t n_q, int H_kv, int64_t max_cells);
+size_t attn_smem_bytes_host(int G, int d_k, int d_v, int esize);
+size_t attn_workspace_bytes(int64_t n_q, int H_q, int H_kv, int d_v, int64_t max_cells);
+cudaError_t launch_sparse_attn(const float *q, int64_t n_q, int H_q, int H_kv, int d_k, int d_v,
+                               float scale, const void *K, const void *V, qsa_dtype dt,
+                               int64_t n_kv, int64_t ld_k, int64_t ld_v, const int32_t *pos,
+                               const int32_t *n_cells, int64_t max_cells, float *out,
+                               float *lse, float *partials, cudaStream_t st);
+
+cudaError_t launch_mask_to_list(const uint8_t *mask, int64_t n_rows, int64_t n_kv,
+                                int64_t ld_mask, int64_t max_list, int32_t *pos_out,
+                                int32_t *counts_out, uint64_t *bits_out, cudaStream_t st);
+
+}  // namespace qsa

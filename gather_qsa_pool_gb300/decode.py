@@ -1,0 +1,108 @@
+"""One QSA layer's decode step through the C ABI.
+
+``DecodeLayer`` owns the device buffers of one QSA layer (the persistent pooled-key
+cache, scores, selected blocks, cell list, split-K workspace, output) and issues the
+five library calls of a decode step on the current stream:
+
+    qsa_pool_update -> qsa_index_score -> qsa_topk_blocks -> qsa_gather_kv
+                    -> qsa_sparse_attn
+
+The raw indexer-key cache and the K/V cache belong to the caller (the model writes the
+new token's rows before the step).  The gather call only builds the cell list; the
+attention kernel stages the listed K/V rows straight from the cache.
+"""
+from __future__ import annotations
+
+import math
+
+from . import _binding as qb
+
+
+class DecodeLayer:
+    def __init__(self, *, cap_tokens, H_idx, d_idx, H_q, H_kv, d, top_k_tokens,
+                 eps=1e-6, rope_base=10000.0, device="cuda"):
+        import torch
+
+        self.H_idx, self.d_idx = H_idx, d_idx
+        self.H_q, self.H_kv, self.d = H_q, H_kv, d
+        self.k_blk = top_k_tokens // 4
+        self.eps, self.rope_base = eps, rope_base
+        self.max_cells = 4 * self.k_blk + 3
+        self.cap_rows = (cap_tokens + 3) // 4
+        f32, i32 = torch.float32, torch.int32
+        self.pooled = torch.zeros(self.cap_rows, H_idx * d_idx, dtype=f32, device=device)
+        self.scores = torch.zeros(1, self.cap_rows, dtype=f32, device=device)
+        self.blocks = torch.zeros(1, self.k_blk, dtype=i32, device=device)
+        self.counts = torch.zeros(1, dtype=i32, device=device)
+        self.pos = torch.zeros(1, self.max_cells, dtype=i32, device=device)
+        self.n_cells = torch.zeros(1, dtype=i32, device=device)
+        self.out = torch.zeros(1, H_q, d, dtype=f32, device=device)
+        self.lse = torch.zeros(1, H_q, dtype=f32, device=device)
+        ws = qb.sparse_attn_workspace_size(1, H_q, H_kv, d, self.max_cells)
+        self.workspace = torch.empty(max(ws // 4, 1), dtype=f32, device=device)
+        self.n_valid_full = 0
+
+    def rebuild(self, raw_k, norm_w, n_ctx, stream=None):
+        """Recompute every pooled row (state load / sequence edit)."""
+        qb.pool_update(raw_k, n_ctx, self.H_idx, self.d_idx, norm_w, self.eps, self.rope_base,
+                       self.pooled, 0, stream)
+        self.n_valid_full = n_ctx // 4
+
+    def invalidate(self, first_changed_token):
+        """Rows from the block holding ``first_changed_token`` on are recomputed next step."""
+        self.n_valid_full = min(self.n_valid_full, first_changed_token // 4)
+
+    def step(self, raw_k, norm_w, K, V, n_ctx, q_idx, q, stream=None):
+        """Decode step at context length n_ctx (the current token is position n_ctx-1).
+
+        q_idx: [H_idx*d_idx] fp32, q: [H_q][d] fp32.  Returns the output [1][H_q][d]
+        (a view into this layer's buffer, overwritten by the next step)."""
+        qb.decode_step(raw_k, n_ctx, self.H_idx, self.d_idx, norm_w, self.eps, self.rope_base,
+                       self.pooled, self.n_valid_full, q_idx, 1.0 / math.sqrt(self.d_idx),
+                       self.scores, self.k_blk, self.blocks, self.counts, K, V, self.H_kv,
+                       self.d, self.pos, self.n_cells, self.max_cells, q, self.H_q,
+                       1.0 / math.sqrt(self.d), self.out, self.lse, self.workspace, stream)
+        self.n_valid_full = n_ctx // 4
+        return self.out
+
+    def bind(self, raw_k, norm_w, K, V):
+        """Fix the caller-owned caches for ``step_ptr`` (pointers resolved once)."""
+        self._lib = qb.load()
+        self._fixed = (raw_k.data_ptr(), qb._dtype(raw_k), norm_w.data_ptr(),
+                       self.pooled.data_ptr(), self.pooled.shape[0], self.scores.data_ptr(),
+                       self.blocks.data_ptr(), self.counts.data_ptr(), K.data_ptr(), V.data_ptr(),
+                       qb._dtype(K), K.shape[0], K.stride(0), self.pos.data_ptr(),
+                       self.n_cells.data_ptr(), self.out.data_ptr(), self.lse.data_ptr(),
+                       self.workspace.data_ptr(), self.workspace.numel() * 4)
+
+    def step_ptr(self, n_ctx, q_idx_ptr, q_ptr, stream_ptr):
+        """Decode step on caches fixed by ``bind``; q_idx / q given as device pointers."""
+        (raw, raw_dt, w, pooled, cap, scores, blocks, counts, K, V, kv_dt, n_kv, ld, pos,
+         n_cells, out, lse, ws, ws_bytes) = self._fixed
+        st = self._lib.qsa_decode_step(
+            raw, raw_dt, n_ctx, self.H_idx, self.d_idx, w, self.eps, self.rope_base, pooled,
+            cap, self.n_valid_full, q_idx_ptr, 1.0 / math.sqrt(self.d_idx), scores, self.k_blk,
+            blocks, counts, K, V, kv_dt, n_kv, self.H_kv, self.d, ld, pos, n_cells,
+            self.max_cells, q_ptr, self.H_q, 1.0 / math.sqrt(self.d), out, lse, ws, ws_bytes,
+            stream_ptr)
+        if st != 0:
+            raise qb.QSAError("qsa_decode_step", st)
+        self.n_valid_full = n_ctx // 4
+
+    def step_separate_calls(self, raw_k, norm_w, K, V, n_ctx, q_idx, q, stream=None):
+        """The same step issued as the five individual C calls."""
+        n_rows = (n_ctx + 3) // 4
+        n_full = n_ctx // 4
+        qb.pool_update(raw_k, n_ctx, self.H_idx, self.d_idx, norm_w, self.eps, self.rope_base,
+                       self.pooled, self.n_valid_full, stream)
+        self.n_valid_full = n_full
+        qb.index_score(q_idx.view(1, -1), self.pooled, n_rows, self.H_idx, self.d_idx,
+                       1.0 / math.sqrt(self.d_idx), self.scores, stream=stream)
+        qb.topk_blocks(self.scores, n_full, self.k_blk, self.blocks, self.counts, stream=stream)
+        qb.gather_kv(self.blocks, self.counts, self.k_blk, self.pos, self.n_cells,
+                     self.max_cells, n_ctx=n_ctx, n_kv=K.shape[0], stream=stream)
+        qb.sparse_attn(q.view(1, self.H_q, self.d), K, V, self.n_cells, self.max_cells,
+                       self.out, self.H_kv, self.d, self.d, 1.0 / math.sqrt(self.d),
+                       pos=self.pos, lse=self.lse, workspace=self.workspace,
+                       ld_k=self.H_kv * self.d, ld_v=self.H_kv * self.d, stream=stream)
+        return self.out

@@ -1,0 +1,290 @@
+/*
+ * qsa.h -- C ABI of the GB300 (sm_103a) QSA two-stage sparse-attention library.
+ *
+ * QSA ("Qwen Sparse Attention") first runs a light indexer that picks the important
+ * 4-token blocks of a long context, then runs attention over the selected cells only
+ * (Qiita, ariera, EVO-X2 + Qwen3.8-Flash-Next llama.cpp series part 10, section
+ * "QSA and the QSA indexer").  One decode step of one QSA layer is the call sequence
+ *
+ *   qsa_pool_update -> qsa_index_score -> qsa_topk_blocks -> qsa_gather_kv
+ *                   -> qsa_sparse_attn
+ *
+ * and the mask-driven variant is qsa_mask_to_list -> qsa_sparse_attn.
+ *
+ * Conventions shared by every entry point
+ *   - Every tensor pointer is device memory owned by the caller; the library never
+ *     allocates, frees or keeps a pointer past the call.  Scratch memory comes from a
+ *     caller buffer whose size the matching *_workspace_size() function returns.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and never synchronises with the host.
+ *   - The returned status is decided on the host from the arguments before anything is
+ *     launched: QSA_ERR_INVALID_ARG / QSA_ERR_UNSUPPORTED mean nothing was enqueued.
+ *     QSA_ERR_CUDA means a launch failed (the CUDA error is left for
+ *     cudaGetLastError()).  Data-dependent conditions (a list longer than its capacity)
+ *     are reported in device outputs, never by a trap.
+ *   - Layouts are row-major.  "ld" arguments are element strides between consecutive
+ *     rows.  Pointers to fp32 / bf16 data must be aligned to their element size.
+ *   - Dtype QSA_BF16 means bfloat16 storage; all arithmetic accumulates in fp32.
+ *   - Block b of a context covers tokens 4b .. 4b+3.  With n_ctx tokens there are
+ *     n_full = floor(n_ctx/4) complete blocks and n_rows = ceil(n_ctx/4) pooled rows;
+ *     the last row is the open (partial) block when n_ctx is not a multiple of 4.
+ */
+#ifndef QSA_H
+#define QSA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *qsa_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+    QSA_OK = 0,
+    QSA_ERR_INVALID_ARG = 1, /* a pointer, size, stride or alignment is invalid */
+    QSA_ERR_UNSUPPORTED = 2, /* valid, but outside what this build implements */
+    QSA_ERR_CUDA = 3,        /* a CUDA launch or query failed */
+    QSA_ERR_TIMEOUT = 4      /* reserved: a bounded device wait gave up */
+} qsa_status;
+
+typedef enum { QSA_F32 = 0, QSA_BF16 = 1 } qsa_dtype;
+
+typedef enum {
+    QSA_PREC_F32 = 0,    /* fp32 operands, fp32 accumulation (CUDA cores) */
+    QSA_PREC_BF16_TC = 1 /* operands rounded to bf16 (nearest even), fp32 accumulation
+                            on the tcgen05 tensor cores; for multi-query chunks */
+} qsa_precision;
+
+/* Human-readable name of a status code (static storage). */
+const char *qsa_status_str(qsa_status s);
+
+/* Library ABI version: (major << 16) | minor. */
+int qsa_version(void);
+
+/*
+ * qsa_pool_update -- incremental pooled-key cache update.
+ *
+ * Source: same page, sections "QSA and the QSA indexer" (4-token average pooling ->
+ * RMS norm -> RoPE of the pooled summary) and "incremental pooled-key cache
+ * (COMMON-004)" (a persistent cache of completed-block rows; only newly completed or
+ * invalidated blocks, and the open block, are recomputed).
+ *
+ * For every block b in [n_valid_full, n_rows):
+ *   p   = mean of the raw indexer keys of the tokens of block b present in n_ctx
+ *   y_h = p_h / sqrt(mean_j p_h[j]^2 + eps) * norm_w        (each indexer head h)
+ *   z_h = RoPE(y_h, position 4b): dims i and i + d/2 rotate by 4b * base^(-2i/d)
+ *   pooled[b][h*d .. h*d+d) = z_h  (fp32; the angle is formed in fp64)
+ * Rows below n_valid_full are not touched.  Invalidation after a state load, a
+ * sequence edit or a rolled-back speculative write is done by passing a smaller
+ * n_valid_full (e.g. floor(first_changed_position / 4)).
+ *
+ *   raw_k      [n_ctx][H][d] raw indexer keys, dtype raw_dtype (row stride H*d)
+ *   norm_w     [d] fp32 RMS-norm weight shared by all indexer heads
+ *   pooled     [cap_rows][H*d] fp32 cache, updated in place
+ *   n_valid_full  rows [0, n_valid_full) are known to be valid; 0 <= n_valid_full
+ *              (values above n_full are clamped to n_full)
+ * Errors: INVALID_ARG for null pointers, n_ctx < 0, H < 1, d < 2 or odd d,
+ * n_valid_full < 0, or n_rows > cap_rows.
+ */
+qsa_status qsa_pool_update(const void *raw_k, qsa_dtype raw_dtype, int64_t n_ctx, int H, int d,
+                           const float *norm_w, float eps, double rope_base, float *pooled,
+                           int64_t cap_rows, int64_t n_valid_full, qsa_stream_t stream);
+
+/*
+ * qsa_index_score -- indexer score of every pooled row against each query.
+ *
+ * Source: same page, section "QSA and the QSA indexer" (the query is scored against
+ * every pooled block summary; the top blocks are then selected).
+ *
+ *   scores[i][b] = scale * sum_{h,j} q[i][h*d+j] * pooled[b][h*d+j],  b < n_rows
+ * When q_pos is not NULL (prefill chunk), row b is visible to query i only if the
+ * block is complete at the query's position (4b + 3 <= q_pos[i]); other rows get
+ * -inf.  When q_pos is NULL (decode), every row including the open one is scored.
+ *
+ *   q          [n_q][ld_q] fp32 indexer queries (already position-encoded by the caller)
+ *   q_pos      [n_q] int32 device positions, or NULL
+ *   pooled     [n_rows][H*d] fp32
+ *   scores     [n_q][ld_scores] fp32 output, ld_scores >= n_rows
+ *   precision  QSA_PREC_F32 or QSA_PREC_BF16_TC (the latter needs the workspace)
+ *   workspace  caller scratch of qsa_index_score_workspace_size() bytes (may be NULL
+ *              when that size is 0)
+ * Errors: INVALID_ARG for null pointers, sizes < 0, ld_q < H*d, ld_scores < n_rows, or
+ * a workspace smaller than required.
+ */
+qsa_status qsa_index_score(const float *q, int64_t n_q, int64_t ld_q, const int32_t *q_pos,
+                           const float *pooled, int64_t n_rows, int H, int d, float scale,
+                           float *scores, int64_t ld_scores, qsa_precision precision,
+                           void *workspace, size_t workspace_bytes, qsa_stream_t stream);
+
+size_t qsa_index_score_workspace_size(int64_t n_q, int64_t n_rows, int H, int d,
+                                      qsa_precision precision);
+
+/*
+ * qsa_topk_blocks -- block-domain top-k.
+ *
+ * Source: same page, section "block-domain top-k (COMMON-006)" (top-k is taken over
+ * the block scores and only the chosen blocks are expanded to cells) and section
+ * "QSA and the QSA indexer" (indexer_top_k = 2048 tokens = 512 blocks).
+ *
+ * For each query i, the candidates are the complete blocks b < n_full_i, where
+ * n_full_i = n_full when q_pos is NULL, else min(n_full, floor((q_pos[i]+1)/4)).
+ * The open block never competes (it is appended as the tail by qsa_gather_kv).
+ * Output: the min(k_blk, n_full_i) best candidates by score, ties to the lower block
+ * index, NaN ranked as -inf, written in ascending block order to
+ * blocks_out[i][0 .. count), count to counts_out[i].  Entries past the count are not
+ * written.
+ *
+ *   scores     [n_q][ld_scores] fp32 (as written by qsa_index_score)
+ *   blocks_out [n_q][k_blk] int32;  counts_out [n_q] int32
+ * Errors: INVALID_ARG for null pointers, n_q < 0, k_blk < 1, n_full < 0,
+ * ld_scores < n_full; UNSUPPORTED when n_full exceeds qsa_topk_max_candidates().
+ */
+qsa_status qsa_topk_blocks(const float *scores, int64_t n_q, int64_t ld_scores,
+                           const int32_t *q_pos, int64_t n_full, int64_t k_blk,
+                           int32_t *blocks_out, int32_t *counts_out, qsa_stream_t stream);
+
+int64_t qsa_topk_max_candidates(void);
+
+/*
+ * qsa_gather_kv -- expand selected blocks to KV cells and (optionally) copy the rows.
+ *
+ * Source: same page, section "selected K/V gather (COMMON-005)" (get_rows of K, V and
+ * mask at the ~2051 selected cells into compact tensors) and section "block-domain
+ * top-k (COMMON-006)" (expand only the selected blocks to cell indices, then append
+ * the tail indices); section "why Flash Attention scaled" gives 2048 + 4 - 1 = 2051.
+ *
+ * For query i at position p_i (q_pos[i], or n_ctx - 1 when q_pos is NULL):
+ *   cells = 4b, 4b+1, 4b+2, 4b+3 for each b in blocks[i][0 .. counts[i]) in order,
+ *           then the tail 4*floor((p_i+1)/4) .. p_i
+ *   pos_out[i][j] = cells[j];  n_cells_out[i] = 4*counts[i] + tail length
+ * If K_out / V_out are not NULL, row j of query i is copied:
+ *   K_out[(i*max_cells + j)][0 .. H_kv*d_k) = K[cells[j]*ld_k + 0 .. H_kv*d_k)
+ *   V_out likewise with d_v and ld_v (K_out / V_out are packed: row stride H_kv*d_k,
+ *   H_kv*d_v).  Entries past n_cells_out[i] are not written.
+ *
+ *   K, V       [n_kv][ld] caches, dtype `dtype` (may be NULL when K_out/V_out are NULL)
+ *   blocks     [n_q][k_blk] int32; counts [n_q] int32 (from qsa_topk_blocks)
+ *   max_cells  capacity per query; must be >= 4*k_blk + 3
+ * Errors: INVALID_ARG for null required pointers, bad sizes or max_cells too small.
+ * Block indices outside [0, n_kv/4) produce position -1 rows that are not copied.
+ */
+qsa_status qsa_gather_kv(const void *K, const void *V, qsa_dtype dtype, int64_t n_kv, int H_kv,
+                         int d_k, int d_v, int64_t ld_k, int64_t ld_v, const int32_t *blocks,
+                         const int32_t *counts, int64_t n_q, int64_t k_blk,
+                         const int32_t *q_pos, int64_t n_ctx, void *K_out, void *V_out,
+                         int32_t *pos_out, int32_t *n_cells_out, int64_t max_cells,
+                         qsa_stream_t stream);
+
+/*
+ * qsa_sparse_attn -- attention of each query token over its listed cells only.
+ *
+ * Source: same page, section "selected K/V gather (COMMON-005)" (attention over the
+ * compact ~2051 rows; the Flash Attention kernel then no longer scales with context)
+ * and devotd.net, "llama.cpp CDNA sparse attention", sections 2-3 (attention over the
+ * listed key positions only; DKQ 576 with 16 query columns per KV head).
+ *
+ * For query i and head h (KV head g = floor(h*H_kv/H_q)), over j < n_cells[i]:
+ *   c_j    = pos[i*max_cells + j]  (pos != NULL: rows of the full cache K, V)
+ *          = i*max_cells + j       (pos == NULL: K, V are already compact)
+ *   logit_j = scale * sum_t q[i][h][t] * K[c_j*ld_k + g*d_k + t]
+ *   out[i][h][:] = sum_j softmax(logit)_j * V[c_j*ld_v + g*d_v + :]
+ *   lse_out[i][h] = log(sum_j exp(logit_j))   (natural log; optional)
+ * Computed as split-K flash decoding (online softmax per split, then a log-sum-exp
+ * combine).  Cells whose position is outside [0, n_kv) are skipped.  An empty list
+ * gives out = 0 and lse = -inf.  n_cells[i] > max_cells (a truncated list, e.g. a
+ * mask with more set positions than the list holds) gives out = NaN and lse = NaN for
+ * that query: the result must not be used.
+ *
+ *   q        [n_q][H_q][d_k] fp32;  out [n_q][H_q][d_v] fp32;  lse_out [n_q][H_q] or NULL
+ *   K, V     dtype `dtype`, row strides ld_k, ld_v (V may alias K, e.g. V = K[:, :d_v])
+ *   n_cells  [n_q] int32 device counts
+ * Requirements: H_q % H_kv == 0, d_k and d_v multiples of 8, ld_k and ld_v multiples
+ * of 8, K and V 16-byte aligned (checked: INVALID_ARG otherwise).
+ */
+qsa_status qsa_sparse_attn(const float *q, int64_t n_q, int H_q, int H_kv, int d_k, int d_v,
+                           float scale, const void *K, const void *V, qsa_dtype dtype,
+                           int64_t n_kv, int64_t ld_k, int64_t ld_v, const int32_t *pos,
+                           const int32_t *n_cells, int64_t max_cells, float *out,
+                           float *lse_out, void *workspace, size_t workspace_bytes,
+                           qsa_stream_t stream);
+
+size_t qsa_sparse_attn_workspace_size(int64_t n_q, int H_q, int H_kv, int d_v,
+                                      int64_t max_cells);
+
+/*
+ * qsa_decode_step -- one decode step of one QSA layer: the five calls above in order,
+ * validated together before anything is enqueued, issued from one host call.
+ *
+ * Source: same page as qsa_pool_update, sections "incremental pooled-key cache
+ * (COMMON-004)", "selected K/V gather (COMMON-005)" and "block-domain top-k
+ * (COMMON-006)" (the decode path: cached pooled keys -> scores -> block top-k -> selected
+ * cells -> attention over them).
+ *
+ * Equivalent to, on `stream`:
+ *   qsa_pool_update(raw_k, raw_dtype, n_ctx, H_idx, d_idx, norm_w, eps, rope_base, pooled,
+ *                   cap_rows, n_valid_full)
+ *   qsa_index_score(q_idx, 1, H_idx*d_idx, NULL, pooled, n_rows, H_idx, d_idx, scale_idx,
+ *                   scores, n_rows, QSA_PREC_F32)
+ *   qsa_topk_blocks(scores, 1, n_rows, NULL, n_full, k_blk, blocks, counts)
+ *   qsa_gather_kv(K, V, kv_dtype, n_kv, H_kv, d, d, ld_kv, ld_kv, blocks, counts, 1, k_blk,
+ *                 NULL, n_ctx, NULL, NULL, pos, n_cells, max_cells)     (cell list only)
+ *   qsa_sparse_attn(q, 1, H_q, H_kv, d, d, scale, K, V, kv_dtype, n_kv, ld_kv, ld_kv, pos,
+ *                   n_cells, max_cells, out, lse_out, workspace, workspace_bytes)
+ * with n_rows = ceil(n_ctx/4), n_full = floor(n_ctx/4).  scores holds >= n_rows floats,
+ * blocks k_blk ints, pos max_cells ints; the attention kernel reads the listed K/V rows in
+ * place.  Returns the first failing validation status without enqueuing anything.
+ */
+qsa_status qsa_decode_step(const void *raw_k, qsa_dtype raw_dtype, int64_t n_ctx, int H_idx,
+                           int d_idx, const float *norm_w, float eps, double rope_base,
+                           float *pooled, int64_t cap_rows, int64_t n_valid_full,
+                           const float *q_idx, float scale_idx, float *scores, int64_t k_blk,
+                           int32_t *blocks, int32_t *counts, const void *K, const void *V,
+                           qsa_dtype kv_dtype, int64_t n_kv, int H_kv, int d, int64_t ld_kv,
+                           int32_t *pos, int32_t *n_cells, int64_t max_cells, const float *q,
+                           int H_q, float scale, float *out, float *lse_out, void *workspace,
+                           size_t workspace_bytes, qsa_stream_t stream);
+
+/*
+ * qsa_mask_to_list -- build each mask row's list of attendable key positions.
+ *
+ * Source: devotd.net, "llama.cpp CDNA sparse attention", section 2 (attendable key
+ * positions are gathered from the mask into a list before the sparse kernel runs; the
+ * per-lane selection is kept as a 64-bit mask and the count uses the same words).
+ *
+ * For row r: bit t of word w is (mask[r*ld_mask + 64w + t] != 0), least significant
+ * bit first (each 64-bit word is built from two 32-lane warp ballots); the set
+ * positions are written in ascending order to pos_out[r][0 .. min(count, max_list));
+ * counts_out[r] = the true number of set positions, even when it exceeds max_list.
+ *
+ *   mask      [n_rows][ld_mask] uint8, nonzero = attend
+ *   pos_out   [n_rows][max_list] int32;  counts_out [n_rows] int32
+ *   bits_out  [n_rows][ceil(n_kv/64)] uint64, or NULL
+ * Errors: INVALID_ARG for null required pointers, n_kv < 0, ld_mask < n_kv,
+ * max_list < 0; UNSUPPORTED for n_kv > 2^31 - 1.
+ */
+qsa_status qsa_mask_to_list(const uint8_t *mask, int64_t n_rows, int64_t n_kv, int64_t ld_mask,
+                            int64_t max_list, int32_t *pos_out, int32_t *counts_out,
+                            uint64_t *bits_out, qsa_stream_t stream);
+
+/*
+ * qsa_mask_sparse_eligible -- host-side check of when the mask-driven sparse path
+ * applies.
+ *
+ * Source: devotd.net, "llama.cpp CDNA sparse attention", section 3 (the sparse path is
+ * a candidate when a mask is present and bias and softcap are 0; on CDNA the key length
+ * must be at least 4096 and at least twice the maximum list length).
+ *
+ * Returns QSA_OK when has_mask != 0, max_bias == 0, softcap == 0, n_kv >= 4096 and
+ * n_kv >= 2*max_list; QSA_ERR_UNSUPPORTED otherwise (this library has no dense
+ * fallback: the caller runs its own dense attention).  Launches nothing.
+ */
+qsa_status qsa_mask_sparse_eligible(int has_mask, float max_bias, float softcap, int64_t n_kv,
+                                    int64_t max_list);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QSA_H */

@@ -18,6 +18,8 @@ where multi-GB inputs would take minutes on the host).
 """
 from __future__ import annotations
 
+import os
+from concurrent.futures import ThreadPoolExecutor
 from dataclasses import dataclass, replace
 
 import numpy as np
@@ -128,11 +130,29 @@ def shrink(shape, **kw):
 
 # --------------------------------------------------------------------------- helpers
 
+_CHUNK = 1 << 22  # elements per generator stream / conversion chunk
+
+
+def _pool():
+    return ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 1))
+
+
+def _to_bf16_chunk(u: np.ndarray, out: np.ndarray):
+    t = (u >> np.uint32(16)) & np.uint32(1)
+    t += np.uint32(0x7FFF)
+    t += u
+    t >>= np.uint32(16)
+    out[...] = t
+
+
 def to_bf16_bits(x: np.ndarray) -> np.ndarray:
     """fp32 -> bf16 bit patterns, round to nearest even (inputs hold no NaN)."""
-    u = np.ascontiguousarray(x, np.float32).view(np.uint32)
-    r = (u + np.uint32(0x7FFF) + ((u >> np.uint32(16)) & np.uint32(1))) >> np.uint32(16)
-    return r.astype(np.uint16)
+    u = np.ascontiguousarray(x, np.float32).reshape(-1).view(np.uint32)
+    out = np.empty(u.shape[0], np.uint16)
+    with _pool() as ex:
+        list(ex.map(lambda i: _to_bf16_chunk(u[i:i + _CHUNK], out[i:i + _CHUNK]),
+                    range(0, u.shape[0], _CHUNK)))
+    return out.reshape(np.shape(x))
 
 
 def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
@@ -140,7 +160,22 @@ def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
 
 
 def _normal(rng, shape):
-    return rng.standard_normal(size=shape, dtype=np.float32)
+    """N(0,1) float32 of the given shape.  Large draws are split into fixed-size chunks,
+    each with its own stream seeded from ``rng`` (deterministic for any thread count)."""
+    n = int(np.prod(shape))
+    if n <= _CHUNK:
+        return rng.standard_normal(size=shape, dtype=np.float32)
+    out = np.empty(n, np.float32)
+    starts = list(range(0, n, _CHUNK))
+    seeds = rng.integers(0, 2 ** 63 - 1, size=len(starts))
+
+    def fill(k):
+        g = np.random.Generator(np.random.PCG64(int(seeds[k])))
+        g.standard_normal(out=out[starts[k]:starts[k] + _CHUNK], dtype=np.float32)
+
+    with _pool() as ex:
+        list(ex.map(fill, range(len(starts))))
+    return out.reshape(shape)
 
 
 def _store(x: np.ndarray, dtype: str) -> np.ndarray:

@@ -1,0 +1,117 @@
+"""Host-only checks of the C ABI: the library builds for sm_103a, loads without a GPU,
+exports every function include/qsa.h declares, and rejects bad arguments before it
+launches anything (no call here reaches a kernel)."""
+import ctypes
+
+import pytest
+
+import gather_qsa_pool_gb300 as qsa
+from gather_qsa_pool_gb300 import _binding as qb
+
+P = ctypes.c_void_p
+FAKE = P(0x10000)  # never dereferenced: every call below fails validation first
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return qsa.load()
+
+
+def test_library_exports_every_declared_function(lib):
+    names = qb.header_functions()
+    assert len(names) >= 12
+    for n in ["qsa_pool_update", "qsa_index_score", "qsa_topk_blocks", "qsa_gather_kv",
+              "qsa_sparse_attn", "qsa_mask_to_list"]:
+        assert n in names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings_and_version(lib):
+    assert qsa.status_str(0) == "QSA_OK"
+    assert qsa.status_str(1) == "QSA_ERR_INVALID_ARG"
+    assert qsa.status_str(4) == "QSA_ERR_TIMEOUT"
+    assert lib.qsa_version() >> 16 == 1
+
+
+def test_pool_update_rejects(lib):
+    s = None
+    assert lib.qsa_pool_update(None, 0, 10, 4, 64, FAKE, 1e-6, 1e4, FAKE, 10, 0, s) == 1
+    assert lib.qsa_pool_update(FAKE, 0, 10, 4, 63, FAKE, 1e-6, 1e4, FAKE, 10, 0, s) == 1  # odd d
+    assert lib.qsa_pool_update(FAKE, 0, 41, 4, 64, FAKE, 1e-6, 1e4, FAKE, 10, 0, s) == 1  # cap
+    assert lib.qsa_pool_update(FAKE, 0, 10, 4, 64, FAKE, 1e-6, 1e4, FAKE, 10, -1, s) == 1
+    assert lib.qsa_pool_update(FAKE, 7, 10, 4, 64, FAKE, 1e-6, 1e4, FAKE, 10, 0, s) == 1  # dtype
+    assert lib.qsa_pool_update(FAKE, 0, 10, 4, 64, FAKE, 1e-6, -1.0, FAKE, 10, 0, s) == 1
+
+
+def test_index_score_rejects(lib):
+    s = None
+    assert lib.qsa_index_score(None, 1, 256, None, FAKE, 10, 4, 64, 1.0, FAKE, 10, 0, None, 0, s) == 1
+    assert lib.qsa_index_score(FAKE, 1, 255, None, FAKE, 10, 4, 64, 1.0, FAKE, 10, 0, None, 0, s) == 1
+    assert lib.qsa_index_score(FAKE, 1, 256, None, FAKE, 10, 4, 64, 1.0, FAKE, 9, 0, None, 0, s) == 1
+    assert lib.qsa_index_score(FAKE, 1, 256, None, FAKE, 10, 4, 64, 1.0, FAKE, 10, 9, None, 0, s) == 1
+
+
+def test_topk_rejects(lib):
+    s = None
+    assert lib.qsa_topk_blocks(FAKE, 1, 10, None, 10, 0, FAKE, FAKE, s) == 1      # k < 1
+    assert lib.qsa_topk_blocks(FAKE, 1, 9, None, 10, 4, FAKE, FAKE, s) == 1       # ld < n_full
+    assert lib.qsa_topk_blocks(None, 1, 10, None, 10, 4, FAKE, FAKE, s) == 1
+    big = lib.qsa_topk_max_candidates() + 1
+    assert lib.qsa_topk_blocks(FAKE, 1, big, None, big, 4, FAKE, FAKE, s) == 2
+    assert lib.qsa_topk_max_candidates() >= 64052  # a 256k-token context fits
+
+
+def test_gather_rejects(lib):
+    s = None
+    # max_cells < 4*k_blk + 3
+    assert lib.qsa_gather_kv(None, None, 1, 100, 4, 128, 128, 512, 512, FAKE, FAKE, 1, 16, None,
+                             100, None, None, FAKE, FAKE, 66, s) == 1
+    # K_out without K
+    assert lib.qsa_gather_kv(None, None, 1, 100, 4, 128, 128, 512, 512, FAKE, FAKE, 1, 16, None,
+                             100, FAKE, None, FAKE, FAKE, 67, s) == 1
+    # decode without n_ctx
+    assert lib.qsa_gather_kv(None, None, 1, 100, 4, 128, 128, 512, 512, FAKE, FAKE, 1, 16, None,
+                             -1, None, None, FAKE, FAKE, 67, s) == 1
+
+
+def test_sparse_attn_rejects(lib):
+    s = None
+    a = P(0x10000)
+    ok = dict(q=a, n_q=1, H_q=32, H_kv=4, d_k=128, d_v=128, scale=0.1, K=a, V=a, dt=1, n_kv=100,
+              ld_k=512, ld_v=512, pos=None, n_cells=a, max_cells=2051, out=a, lse=None,
+              ws=a, ws_bytes=1 << 30, st=s)
+
+    def call(**kw):
+        v = dict(ok, **kw)
+        return lib.qsa_sparse_attn(*v.values())
+
+    assert call(H_kv=3) == 1                 # H_q % H_kv
+    assert call(d_k=100) == 1                # not a multiple of 8
+    assert call(ld_k=500) == 1               # ld_k < H_kv*d_k
+    assert call(K=P(0x10008)) == 1           # K not 16-byte aligned
+    assert call(ws_bytes=0) == 1             # workspace too small
+    assert call(H_q=96) == 2                 # 24 heads per KV head: not built
+    assert call(H_q=16, H_kv=1, d_k=576, d_v=512, ld_k=576, ld_v=576, dt=0) == 2  # smem
+    need = lib.qsa_sparse_attn_workspace_size(1, 32, 4, 128, 2051)
+    assert need > 0
+    assert lib.qsa_sparse_attn_workspace_size(1024, 32, 4, 128, 2051) == 0  # one split
+
+
+def test_mask_to_list_rejects(lib):
+    s = None
+    assert lib.qsa_mask_to_list(None, 1, 64, 64, 8, FAKE, FAKE, None, s) == 1
+    assert lib.qsa_mask_to_list(FAKE, 1, 64, 63, 8, FAKE, FAKE, None, s) == 1
+    assert lib.qsa_mask_to_list(FAKE, 1, 64, 64, 8, FAKE, FAKE, P(0x10004), s) == 1
+    assert lib.qsa_mask_to_list(FAKE, 1, 1 << 31, 1 << 31, 8, FAKE, FAKE, None, s) == 2
+
+
+def test_mask_sparse_eligibility_rule():
+    # devotd.net, section 3: mask present, no bias, no softcap, n_kv >= 4096, n_kv >= 2*max
+    assert qsa.mask_sparse_eligible(True, 0.0, 0.0, 32768, 2048)
+    assert not qsa.mask_sparse_eligible(False, 0.0, 0.0, 32768, 2048)
+    assert not qsa.mask_sparse_eligible(True, 8.0, 0.0, 32768, 2048)
+    assert not qsa.mask_sparse_eligible(True, 0.0, 30.0, 32768, 2048)
+    assert not qsa.mask_sparse_eligible(True, 0.0, 0.0, 4095, 16)
+    assert not qsa.mask_sparse_eligible(True, 0.0, 0.0, 4096, 2049)
+    assert qsa.mask_sparse_eligible(True, 0.0, 0.0, 4096, 2048)

@@ -1,0 +1,144 @@
+"""GPU parity of the mask-driven variant (mask -> position list, attention over the list)
+and of the prefill-chunk path (per-query causal scores, per-query top-k, gathered
+attention) against the fp64 oracle."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import gather_qsa_pool_gb300 as qsa
+import qsa_synth
+from oracle import oracle
+from gpu_helpers import ATOL_ATTN_BF16, ATOL_ATTN_F32, check_topk, to_dev, to_host
+
+pytestmark = pytest.mark.gpu
+
+
+# ------------------------------------------------------------------ a7 mask -> list
+
+@pytest.mark.parametrize("n_kv", [32768, 100_000, 1000, 64, 63, 1])
+def test_mask_to_list(n_kv):
+    n_rows, max_list = 3, 2048
+    m = qsa_synth.mask_rows(n_rows, n_kv, seed=n_kv)
+    if n_kv >= 64:
+        m[1, :] = 0            # empty row
+    pos = torch.full((n_rows, max_list), -3, dtype=torch.int32, device="cuda")
+    counts = torch.zeros(n_rows, dtype=torch.int32, device="cuda")
+    bits = torch.zeros((n_rows, (n_kv + 63) // 64), dtype=torch.int64, device="cuda")
+    qsa.mask_to_list(to_dev(m), max_list, pos, counts, bits)
+    g_pos, g_cnt, g_bits = to_host(pos), to_host(counts), to_host(bits).view(np.uint64)
+    for r in range(n_rows):
+        w_pos, w_cnt, w_bits = oracle.mask_to_list(m[r], max_list)
+        assert g_cnt[r] == w_cnt
+        np.testing.assert_array_equal(g_pos[r, :min(w_cnt, max_list)], w_pos)
+        assert np.all(g_pos[r, min(w_cnt, max_list):] == -3)
+        np.testing.assert_array_equal(g_bits[r], w_bits)
+
+
+def test_mask_to_list_overflow_keeps_true_count():
+    m = np.ones((2, 5000), np.uint8)
+    m[1, ::3] = 0
+    pos = torch.zeros((2, 2048), dtype=torch.int32, device="cuda")
+    counts = torch.zeros(2, dtype=torch.int32, device="cuda")
+    qsa.mask_to_list(to_dev(m), 2048, pos, counts)
+    for r in range(2):
+        w_pos, w_cnt, _ = oracle.mask_to_list(m[r], 2048)
+        assert int(to_host(counts)[r]) == w_cnt > 2048
+        np.testing.assert_array_equal(to_host(pos)[r], w_pos)
+
+
+# ------------------------------------------------------------------ a8 mask-mode attention
+
+def test_mask_mode_attention_dkq576():
+    """DKQ 576 / d_v 512, 16 query heads on one KV head, V = first 512 columns of each
+    K row, bf16; list from the mask; one row overflowing its list gives NaN."""
+    shape = qsa_synth.CONFIGS["mask_32k"]
+    inp = qsa_synth.mask_attn_inputs(shape, seed=4)
+    m = qsa_synth.mask_rows(shape.n_q, shape.n_kv, seed=5)
+    m[3, :] = 0
+    m[3, 100:100 + 3000] = 1   # 3000 set positions: more than the 2048-entry list
+    assert qsa.mask_sparse_eligible(True, 0.0, 0.0, shape.n_kv, shape.max_list)
+    KV = to_dev(inp["KV"])
+    pos = torch.zeros((shape.n_q, shape.max_list), dtype=torch.int32, device="cuda")
+    counts = torch.zeros(shape.n_q, dtype=torch.int32, device="cuda")
+    qsa.mask_to_list(to_dev(m), shape.max_list, pos, counts)
+    out = torch.zeros((shape.n_q, shape.H_q, shape.d_v), device="cuda")
+    lse = torch.zeros((shape.n_q, shape.H_q), device="cuda")
+    ws_n = qsa.sparse_attn_workspace_size(shape.n_q, shape.H_q, 1, shape.d_v, shape.max_list)
+    ws = torch.empty(max(ws_n // 4, 1), device="cuda")
+    scale = 1.0 / math.sqrt(shape.d_k)
+    qsa.sparse_attn(to_dev(inp["q"]), KV, KV, counts, shape.max_list, out, 1, shape.d_k,
+                    shape.d_v, scale, pos=pos, lse=lse, workspace=ws, ld_k=shape.d_k,
+                    ld_v=shape.d_k)
+    g_out, g_lse = to_host(out), to_host(lse)
+    for r in range(shape.n_q):
+        w_pos, w_cnt, _ = oracle.mask_to_list(m[r], shape.max_list)
+        if w_cnt > shape.max_list:
+            assert np.all(np.isnan(g_out[r])) and np.all(np.isnan(g_lse[r]))
+            continue
+        want, want_lse = oracle.attention(inp["q"][r], inp["KV"], inp["KV"], shape.H_q, 1,
+                                          shape.d_k, shape.d_v, shape.d_k, shape.d_k, w_pos, scale)
+        np.testing.assert_allclose(g_out[r], want, rtol=0, atol=ATOL_ATTN_BF16)
+        np.testing.assert_allclose(g_lse[r], want_lse, rtol=1e-5, atol=1e-4)
+
+
+# ------------------------------------------------------------------ a6 prefill chunk
+
+def _prefill_case(dtype, depth, n_q, k_tokens, seed):
+    shape = qsa_synth.PrefillShape("prefill_small", depth, n_q, 4, 64, 8, 2, 128, k_tokens,
+                                   dtype=dtype)
+    return shape, qsa_synth.prefill_inputs(shape, seed)
+
+
+@pytest.mark.parametrize("dtype,depth,n_q,k_tokens", [("f32", 3001, 64, 256),
+                                                      ("bf16", 700, 130, 1024)])
+def test_prefill_chunk_fp32_scores(dtype, depth, n_q, k_tokens):
+    shape, inp = _prefill_case(dtype, depth, n_q, k_tokens, seed=21)
+    H, d, n_ctx = shape.H_idx, shape.d_idx, shape.n_ctx
+    n_rows, k_blk, max_cells = shape.n_rows, shape.k_blk, shape.max_cells
+    scale_idx = 1.0 / math.sqrt(d)
+    # oracle
+    o_pooled = oracle.pool_rows(inp["raw_k"], n_ctx, H, d, inp["norm_w"], shape.eps,
+                                shape.rope_base, 0, n_rows)
+    o_scores = oracle.scores(inp["q_idx"], o_pooled, n_rows, H, d, scale_idx, q_pos=inp["q_pos"])
+    # GPU
+    pooled = torch.zeros(n_rows, H * d, device="cuda")
+    qsa.pool_update(to_dev(inp["raw_k"]), n_ctx, H, d, to_dev(inp["norm_w"]), shape.eps,
+                    shape.rope_base, pooled, 0)
+    q_pos = to_dev(inp["q_pos"])
+    scores = torch.zeros(n_q, n_rows, device="cuda")
+    qsa.index_score(to_dev(inp["q_idx"]), pooled, n_rows, H, d, scale_idx, scores, q_pos=q_pos)
+    blocks = torch.zeros(n_q, k_blk, dtype=torch.int32, device="cuda")
+    counts = torch.zeros(n_q, dtype=torch.int32, device="cuda")
+    qsa.topk_blocks(scores, n_ctx // 4, k_blk, blocks, counts, q_pos=q_pos)
+    pos = torch.zeros(n_q, max_cells, dtype=torch.int32, device="cuda")
+    n_cells = torch.zeros(n_q, dtype=torch.int32, device="cuda")
+    K, V = to_dev(inp["K"]), to_dev(inp["V"])
+    qsa.gather_kv(blocks, counts, k_blk, pos, n_cells, max_cells, q_pos=q_pos, n_kv=n_ctx)
+    out = torch.zeros(n_q, shape.H_q, shape.d, device="cuda")
+    ws = torch.empty(max(qsa.sparse_attn_workspace_size(n_q, shape.H_q, shape.H_kv, shape.d,
+                                                        max_cells) // 4, 1), device="cuda")
+    qsa.sparse_attn(to_dev(inp["q"]), K, V, n_cells, max_cells, out, shape.H_kv, shape.d,
+                    shape.d, 1.0 / math.sqrt(shape.d), pos=pos, workspace=ws)
+    g_scores, g_blocks, g_counts = to_host(scores), to_host(blocks), to_host(counts)
+    g_out, g_pos, g_nc = to_host(out), to_host(pos), to_host(n_cells)
+    atol = ATOL_ATTN_BF16 if dtype == "bf16" else ATOL_ATTN_F32
+    checked = 0
+    for i in range(n_q):
+        p = int(inp["q_pos"][i])
+        nf = (p + 1) // 4
+        assert np.all(np.isneginf(g_scores[i, nf:n_rows]))
+        n_band = check_topk(g_blocks[i], int(g_counts[i]), o_scores[i], nf, k_blk)
+        w_blocks = oracle.topk(o_scores[i], nf, k_blk)
+        if not np.array_equal(g_blocks[i, :g_counts[i]], w_blocks):
+            assert n_band > 0
+            continue
+        cells = oracle.cells(w_blocks, p)
+        np.testing.assert_array_equal(g_pos[i, :g_nc[i]], cells)
+        want, _ = oracle.attention(inp["q"][i], inp["K"], inp["V"], shape.H_q, shape.H_kv,
+                                   shape.d, shape.d, shape.H_kv * shape.d, shape.H_kv * shape.d,
+                                   cells, 1.0 / math.sqrt(shape.d))
+        np.testing.assert_allclose(g_out[i], want, rtol=0, atol=atol)
+        checked += 1
+    assert checked >= n_q - 2
