@@ -232,9 +232,11 @@ def run_context(name, args, world, rank, local, want_clocks):
     barrier(world)
     t_wall0 = time.time()
     ev0.record(stream)
+    t_issue0 = time.perf_counter()
     for _ in range(K):
         step(s)
         s += 1
+    t_issue = time.perf_counter() - t_issue0
     ev1.record(stream)
     torch.cuda.synchronize()
     t_wall1 = time.time()
@@ -303,7 +305,7 @@ def run_context(name, args, world, rank, local, want_clocks):
     n_cells_last = int(layers[(s - 1) % L].n_cells.item())
     res = {
         "ms": ms_max, "K": K, "W": W, "score_us": score_us, "score_rows": score_rows,
-        "t_e2e": t_e2e, "k_e2e": k_e2e, "h2d": h2d, "d2h": d2h, "clocks": clocks,
+        "t_e2e": t_e2e, "k_e2e": k_e2e, "host_issue_us": t_issue * 1e6 / K, "h2d": h2d, "d2h": d2h, "clocks": clocks,
         "n_cells": n_cells_last, "shape": shape, "n_ctx_end": max(n_ctx),
     }
     del layers, caches
@@ -420,6 +422,7 @@ def main():
             "score_kernel_us": r["score_us"],
             "score_kernel_GBps": r["score_rows"] * sh.H_idx * sh.d_idx * 4 / r["score_us"] / 1e3,
             "e2e_steps_per_s": world * r["k_e2e"] / r["t_e2e"],
+            "host_issue_us_per_step": r["host_issue_us"],
         }
     r = results[args.primary]
     sh = r["shape"]

@@ -11,6 +11,7 @@ from ._binding import (  # noqa: F401
     QSA_PREC_F32,
     QSAError,
     decode_step,
+    decode_step_workspace_size,
     gather_kv,
     header_functions,
     index_score,

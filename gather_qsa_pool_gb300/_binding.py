@@ -44,6 +44,7 @@ _SIGNATURES = {
     "qsa_decode_step": (_int, [_p, _int, _i64, _int, _int, _p, _f, _d, _p, _i64, _i64, _p, _f,
                                _p, _i64, _p, _p, _p, _p, _int, _i64, _int, _int, _i64, _p, _p,
                                _i64, _p, _int, _f, _p, _p, _p, _sz, _p]),
+    "qsa_decode_step_workspace_size": (_sz, [_int, _int, _int, _i64]),
     "qsa_mask_to_list": (_int, [_p, _i64, _i64, _i64, _i64, _p, _p, _p, _p]),
     "qsa_mask_sparse_eligible": (_int, [_int, _f, _f, _i64, _i64]),
 }
@@ -104,6 +105,14 @@ def _stream(stream):
     return ctypes.c_void_p(s.cuda_stream)
 
 
+def _ld(t) -> int:
+    """Element stride between rows of a row-major tensor (a single-row tensor may carry an
+    arbitrary stride on its size-1 leading dim: use its row length)."""
+    if t.dim() < 2 or t.shape[0] <= 1:
+        return t[0].numel() if t.dim() >= 2 else t.numel()
+    return t.stride(0)
+
+
 def _dtype(t) -> int:
     import torch
 
@@ -131,8 +140,8 @@ def index_score(q, pooled, n_rows, H, d, scale, scores, q_pos=None, precision=QS
                 workspace=None, stream=None):
     """qsa_index_score: scores[i][b] for b < n_rows (q: [n_q][>= H*d] fp32)."""
     n_q = q.shape[0] if q.dim() > 1 else 1
-    ld_q = q.stride(0) if q.dim() > 1 else H * d
-    ld_s = scores.stride(0) if scores.dim() > 1 else n_rows
+    ld_q = _ld(q) if q.dim() > 1 else H * d
+    ld_s = _ld(scores) if scores.dim() > 1 else n_rows
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check("qsa_index_score", load().qsa_index_score(
         _ptr(q), n_q, ld_q, _ptr(q_pos), _ptr(pooled), n_rows, H, d, scale, _ptr(scores), ld_s,
@@ -146,7 +155,7 @@ def topk_max_candidates() -> int:
 def topk_blocks(scores, n_full, k_blk, blocks_out, counts_out, q_pos=None, stream=None):
     """qsa_topk_blocks over the first n_full columns of each score row."""
     n_q = scores.shape[0] if scores.dim() > 1 else 1
-    ld = scores.stride(0) if scores.dim() > 1 else scores.shape[0]
+    ld = _ld(scores)
     _check("qsa_topk_blocks", load().qsa_topk_blocks(
         _ptr(scores), n_q, ld, _ptr(q_pos), n_full, k_blk, _ptr(blocks_out), _ptr(counts_out),
         _stream(stream)))
@@ -160,8 +169,8 @@ def gather_kv(blocks, counts, k_blk, pos_out, n_cells_out, max_cells, n_ctx=-1, 
     dt = _dtype(K) if K is not None else QSA_BF16
     if n_kv is None:
         n_kv = K.shape[0] if K is not None else (1 << 62)
-    ld_k = K.stride(0) if K is not None else H_kv * d_k
-    ld_v = V.stride(0) if V is not None else H_kv * d_v
+    ld_k = _ld(K) if K is not None else H_kv * d_k
+    ld_v = _ld(V) if V is not None else H_kv * d_v
     _check("qsa_gather_kv", load().qsa_gather_kv(
         _ptr(K), _ptr(V), dt, n_kv, H_kv, d_k, d_v, ld_k, ld_v, _ptr(blocks), _ptr(counts), n_q,
         k_blk, _ptr(q_pos), n_ctx, _ptr(K_out), _ptr(V_out), _ptr(pos_out), _ptr(n_cells_out),
@@ -176,8 +185,8 @@ def sparse_attn(q, K, V, n_cells, max_cells, out, H_kv, d_k, d_v, scale, pos=Non
                 workspace=None, ld_k=None, ld_v=None, n_kv=None, stream=None):
     """qsa_sparse_attn: q [n_q][H_q][d_k] fp32 over listed cells of K/V."""
     n_q, H_q = q.shape[0], q.shape[1]
-    ld_k = K.stride(0) if ld_k is None else ld_k
-    ld_v = V.stride(0) if ld_v is None else ld_v
+    ld_k = _ld(K) if ld_k is None else ld_k
+    ld_v = _ld(V) if ld_v is None else ld_v
     n_kv = K.shape[0] if n_kv is None else n_kv
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check("qsa_sparse_attn", load().qsa_sparse_attn(
@@ -195,8 +204,12 @@ def decode_step(raw_k, n_ctx, H_idx, d_idx, norm_w, eps, rope_base, pooled, n_va
         _ptr(raw_k), _dtype(raw_k), n_ctx, H_idx, d_idx, _ptr(norm_w), eps, rope_base,
         _ptr(pooled), pooled.shape[0], n_valid_full, _ptr(q_idx), scale_idx, _ptr(scores), k_blk,
         _ptr(blocks), _ptr(counts), _ptr(K), _ptr(V), _dtype(K), K.shape[0], H_kv, d,
-        K.stride(0), _ptr(pos), _ptr(n_cells), max_cells, _ptr(q), H_q, scale, _ptr(out),
+        _ld(K), _ptr(pos), _ptr(n_cells), max_cells, _ptr(q), H_q, scale, _ptr(out),
         _ptr(lse), _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def decode_step_workspace_size(H_q, H_kv, d, max_cells) -> int:
+    return int(load().qsa_decode_step_workspace_size(H_q, H_kv, d, max_cells))
 
 
 def mask_to_list(mask, max_list, pos_out, counts_out, bits_out=None, n_kv=None, stream=None):
@@ -204,7 +217,7 @@ def mask_to_list(mask, max_list, pos_out, counts_out, bits_out=None, n_kv=None, 
     n_rows = mask.shape[0]
     n_kv = mask.shape[1] if n_kv is None else n_kv
     _check("qsa_mask_to_list", load().qsa_mask_to_list(
-        _ptr(mask), n_rows, n_kv, mask.stride(0), max_list, _ptr(pos_out), _ptr(counts_out),
+        _ptr(mask), n_rows, n_kv, _ld(mask), max_list, _ptr(pos_out), _ptr(counts_out),
         _ptr(bits_out), _stream(stream)))
 
 

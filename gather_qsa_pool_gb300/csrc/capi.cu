@@ -69,6 +69,7 @@ static qsa_status check_pool_update(const void *raw_k, qsa_dtype raw_dtype, int6
     const int64_t n_full = n_ctx / 4;
     if (n_rows > cap_rows) return QSA_ERR_INVALID_ARG;
     if ((int64_t)H * d > 48 * 1024) return QSA_ERR_UNSUPPORTED;  // row staged in shared memory
+    if (d / 2 > kRopeMaxHalf) return QSA_ERR_UNSUPPORTED;
     const int64_t row0 = n_valid_full < n_full ? n_valid_full : n_full;
     if (n_rows - row0 > 0x7fffffffLL) return QSA_ERR_UNSUPPORTED;
     return QSA_OK;
@@ -76,13 +77,14 @@ static qsa_status check_pool_update(const void *raw_k, qsa_dtype raw_dtype, int6
 
 static cudaError_t run_pool_update(const void *raw_k, qsa_dtype raw_dtype, int64_t n_ctx, int H,
                                    int d, const float *norm_w, float eps, double rope_base,
-                                   float *pooled, int64_t n_valid_full, cudaStream_t st)
+                                   float *pooled, int64_t n_valid_full, uint32_t *zero_hist,
+                                   cudaStream_t st)
 {
     const int64_t n_rows = (n_ctx + 3) / 4;
     const int64_t n_full = n_ctx / 4;
     const int64_t row0 = n_valid_full < n_full ? n_valid_full : n_full;
     return launch_pool_update(raw_k, raw_dtype, n_ctx, H, d, norm_w, eps, rope_base, pooled, row0,
-                              n_rows, st);
+                              n_rows, zero_hist, st);
 }
 
 qsa_status qsa_pool_update(const void *raw_k, qsa_dtype raw_dtype, int64_t n_ctx, int H, int d,
@@ -93,7 +95,7 @@ qsa_status qsa_pool_update(const void *raw_k, qsa_dtype raw_dtype, int64_t n_ctx
                                            pooled, cap_rows, n_valid_full);
     if (v != QSA_OK) return v;
     return from_cuda(run_pool_update(raw_k, raw_dtype, n_ctx, H, d, norm_w, eps, rope_base, pooled,
-                                     n_valid_full, (cudaStream_t)stream));
+                                     n_valid_full, nullptr, (cudaStream_t)stream));
 }
 
 size_t qsa_index_score_workspace_size(int64_t n_q, int64_t n_rows, int H, int d,
@@ -123,7 +125,7 @@ qsa_status qsa_index_score(const float *q, int64_t n_q, int64_t ld_q, const int3
     if (v != QSA_OK) return v;
     if (precision == QSA_PREC_F32) {
         return from_cuda(launch_index_score(q, n_q, ld_q, q_pos, pooled, n_rows, H, d, scale,
-                                            scores, ld_scores, (cudaStream_t)stream));
+                                            scores, ld_scores, nullptr, 0, (cudaStream_t)stream));
     }
     if (precision == QSA_PREC_BF16_TC) {
         const size_t need = qsa_index_score_workspace_size(n_q, n_rows, H, d, precision);
@@ -143,7 +145,7 @@ static qsa_status check_topk(const float *scores, int64_t n_q, int64_t ld_scores
     if (n_q < 0 || k_blk < 1 || n_full < 0 || ld_scores < n_full) return QSA_ERR_INVALID_ARG;
     if (k_blk > 0x7fffffffLL) return QSA_ERR_UNSUPPORTED;
     if (n_full > topk_max_candidates()) return QSA_ERR_UNSUPPORTED;
-    if (n_q * (int64_t)kTopkCluster > 0x7fffffffLL) return QSA_ERR_UNSUPPORTED;
+    if (n_q > 0x7fffffffLL) return QSA_ERR_UNSUPPORTED;
     return QSA_OK;
 }
 
@@ -154,7 +156,7 @@ qsa_status qsa_topk_blocks(const float *scores, int64_t n_q, int64_t ld_scores,
     const qsa_status v = check_topk(scores, n_q, ld_scores, n_full, k_blk, blocks_out, counts_out);
     if (v != QSA_OK) return v;
     return from_cuda(launch_topk(scores, n_q, ld_scores, q_pos, n_full, k_blk, blocks_out,
-                                 counts_out, (cudaStream_t)stream));
+                                 counts_out, 0, nullptr, nullptr, 0, nullptr, (cudaStream_t)stream));
 }
 
 static qsa_status check_gather(const void *K, const void *V, qsa_dtype dtype, int64_t n_kv,
@@ -215,6 +217,7 @@ static qsa_status check_attn(const float *q, int64_t n_q, int H_q, int H_kv, int
     if (G != 1 && G != 2 && G != 4 && G != 8 && G != 16) return QSA_ERR_UNSUPPORTED;
     if (attn_smem_bytes_host(G, d_k, d_v, esize_of(dtype)) > kMaxSmem) return QSA_ERR_UNSUPPORTED;
     if (n_q > 65535 || H_kv > 65535) return QSA_ERR_UNSUPPORTED;
+    if (n_kv > 0x7fffffffLL || n_q * max_cells > 0x7fffffffLL) return QSA_ERR_UNSUPPORTED;
     const size_t need = qsa_sparse_attn_workspace_size(n_q, H_q, H_kv, d_v, max_cells);
     if (workspace_bytes < need || (need > 0 && !workspace)) return QSA_ERR_INVALID_ARG;
     if (need > 0 && !aligned(workspace, 16)) return QSA_ERR_INVALID_ARG;
@@ -236,6 +239,14 @@ qsa_status qsa_sparse_attn(const float *q, int64_t n_q, int H_q, int H_kv, int d
                                         (float *)workspace, (cudaStream_t)stream));
 }
 
+static size_t align256(size_t b) { return (b + 255) & ~(size_t)255; }
+
+size_t qsa_decode_step_workspace_size(int H_q, int H_kv, int d, int64_t max_cells)
+{
+    if (H_q < 1 || H_kv < 1 || d < 1 || max_cells < 0 || H_q % H_kv) return 0;
+    return align256(attn_workspace_bytes(1, H_q, H_kv, d, max_cells)) + kTopkHistBytes;
+}
+
 qsa_status qsa_decode_step(const void *raw_k, qsa_dtype raw_dtype, int64_t n_ctx, int H_idx,
                            int d_idx, const float *norm_w, float eps, double rope_base,
                            float *pooled, int64_t cap_rows, int64_t n_valid_full,
@@ -248,6 +259,10 @@ qsa_status qsa_decode_step(const void *raw_k, qsa_dtype raw_dtype, int64_t n_ctx
 {
     const int64_t n_rows = (n_ctx + 3) / 4;
     const int64_t n_full = n_ctx / 4;
+    const size_t need = qsa_decode_step_workspace_size(H_q, H_kv, d, max_cells);
+    if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return QSA_ERR_INVALID_ARG;
+    const size_t attn_bytes = align256(attn_workspace_bytes(1, H_q, H_kv, d, max_cells));
+    uint32_t *hist = reinterpret_cast<uint32_t *>(static_cast<char *>(workspace) + attn_bytes);
     qsa_status v = check_pool_update(raw_k, raw_dtype, n_ctx, H_idx, d_idx, norm_w, eps,
                                      rope_base, pooled, cap_rows, n_valid_full);
     if (v == QSA_OK)
@@ -259,18 +274,21 @@ qsa_status qsa_decode_step(const void *raw_k, qsa_dtype raw_dtype, int64_t n_ctx
                          k_blk, nullptr, n_ctx, nullptr, nullptr, pos, n_cells, max_cells);
     if (v == QSA_OK)
         v = check_attn(q, 1, H_q, H_kv, d, d, K, V, kv_dtype, n_kv, ld_kv, ld_kv, n_cells,
-                       max_cells, out, workspace, workspace_bytes);
+                       max_cells, out, workspace, attn_bytes);
     if (v != QSA_OK) return v;
     const cudaStream_t st = (cudaStream_t)stream;
+    // 1. pooled rows of the new / open block; clears the top-k histogram
     cudaError_t e = run_pool_update(raw_k, raw_dtype, n_ctx, H_idx, d_idx, norm_w, eps, rope_base,
-                                    pooled, n_valid_full, st);
+                                    pooled, n_valid_full, hist, st);
+    // 2. scores of every row; full blocks also enter the histogram of their top key bits
     if (e == cudaSuccess)
         e = launch_index_score(q_idx, 1, (int64_t)H_idx * d_idx, nullptr, pooled, n_rows, H_idx,
-                               d_idx, scale_idx, scores, n_rows, st);
-    if (e == cudaSuccess) e = launch_topk(scores, 1, n_rows, nullptr, n_full, k_blk, blocks, counts, st);
+                               d_idx, scale_idx, scores, n_rows, hist, n_full, st);
+    // 3. top-k from that histogram; its epilogue writes the cell list (qsa_gather_kv's job)
     if (e == cudaSuccess)
-        e = launch_gather(K, V, kv_dtype, n_kv, H_kv, d, d, ld_kv, ld_kv, blocks, counts, 1, k_blk,
-                          nullptr, n_ctx, nullptr, nullptr, pos, n_cells, max_cells, st);
+        e = launch_topk(scores, 1, n_rows, nullptr, n_full, k_blk, blocks, counts, n_ctx, pos,
+                        n_cells, max_cells, hist, st);
+    // 4. attention over the listed cells, read in place from the cache
     if (e == cudaSuccess)
         e = launch_sparse_attn(q, 1, H_q, H_kv, d, d, scale, K, V, kv_dtype, n_kv, ld_kv, ld_kv,
                                pos, n_cells, max_cells, out, lse_out, (float *)workspace, st);

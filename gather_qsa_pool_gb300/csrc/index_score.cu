@@ -23,7 +23,8 @@ constexpr int kScoreThreads = 256;
 template <int NV, int R>
 __global__ void __launch_bounds__(kScoreThreads)
 score_rows_kernel(const float *__restrict__ q, const float *__restrict__ pooled,
-                  int64_t n_rows, float scale, float *__restrict__ scores)
+                  int64_t n_rows, float scale, float *__restrict__ scores,
+                  uint32_t *__restrict__ hist, int64_t n_hist)
 {
     __shared__ float4 q_s[NV * 32];
     pdl_wait();
@@ -61,7 +62,11 @@ score_rows_kernel(const float *__restrict__ q, const float *__restrict__ pooled,
                     a3 = fmaf(v[r][j].w, qq.w, a3);
                 }
                 const float acc = warp_sum((a0 + a1) + (a2 + a3));
-                if (lane == 0) scores[row] = acc * scale;
+                if (lane == 0) {
+                    const float sc = acc * scale;
+                    scores[row] = sc;
+                    if (hist && row < n_hist) atomicAdd(&hist[score_key(sc) >> (32 - kTopkHistBits)], 1u);
+                }
             }
         }
     }
@@ -75,7 +80,7 @@ __global__ void __launch_bounds__(256)
 score_tiled_kernel(const float *__restrict__ q, int64_t n_q, int64_t ld_q,
                    const int32_t *__restrict__ q_pos, const float *__restrict__ pooled,
                    int64_t n_rows, int hd, float scale, float *__restrict__ scores,
-                   int64_t ld_scores)
+                   int64_t ld_scores, uint32_t *__restrict__ hist, int64_t n_hist)
 {
     __shared__ float a_s[kBK][kBM + 4];
     __shared__ float b_s[kBK][kBN + 4];
@@ -118,14 +123,17 @@ score_tiled_kernel(const float *__restrict__ q, int64_t n_q, int64_t ld_q,
             const int64_t gn = n0 + tx * 4 + j;
             if (gn >= n_rows) continue;
             const bool visible = q_pos == nullptr || 4 * gn + 3 <= p;
-            scores[gm * ld_scores + gn] = visible ? acc[i][j] * scale : -INFINITY;
+            const float sc = visible ? acc[i][j] * scale : -INFINITY;
+            scores[gm * ld_scores + gn] = sc;
+            if (hist && visible && gn < n_hist)
+                atomicAdd(&hist[gm * (1 << kTopkHistBits) + (score_key(sc) >> (32 - kTopkHistBits))], 1u);
         }
     }
 }
 
 template <int NV, int R>
 cudaError_t launch_rows(const float *q, const float *pooled, int64_t n_rows, float scale,
-                        float *scores, cudaStream_t st)
+                        float *scores, uint32_t *hist, int64_t n_hist, cudaStream_t st)
 {
     static int blocks_per_sm = 0;
     auto k = score_rows_kernel<NV, R>;
@@ -141,14 +149,15 @@ cudaError_t launch_rows(const float *q, const float *pooled, int64_t n_rows, flo
     if (grid > grid_needed) grid = grid_needed;
     if (grid < 1) grid = 1;
     return launch(k, dim3((unsigned)grid), dim3(kScoreThreads), 0, st, 1, q, pooled, n_rows,
-                  scale, scores);
+                  scale, scores, hist, n_hist);
 }
 
 }  // namespace
 
 cudaError_t launch_index_score(const float *q, int64_t n_q, int64_t ld_q, const int32_t *q_pos,
                                const float *pooled, int64_t n_rows, int H, int d, float scale,
-                               float *scores, int64_t ld_scores, cudaStream_t st)
+                               float *scores, int64_t ld_scores, uint32_t *hist, int64_t n_hist,
+                               cudaStream_t st)
 {
     if (n_q == 0 || n_rows == 0) return cudaSuccess;
     const int hd = H * d;
@@ -156,17 +165,17 @@ cudaError_t launch_index_score(const float *q, int64_t n_q, int64_t ld_q, const 
                          (reinterpret_cast<uintptr_t>(pooled) % 16 == 0);
     if (n_q == 1 && q_pos == nullptr && aligned && hd % 128 == 0) {
         switch (hd / 128) {
-            case 1: return launch_rows<1, 4>(q, pooled, n_rows, scale, scores, st);
-            case 2: return launch_rows<2, 4>(q, pooled, n_rows, scale, scores, st);
-            case 4: return launch_rows<4, 2>(q, pooled, n_rows, scale, scores, st);
-            case 8: return launch_rows<8, 2>(q, pooled, n_rows, scale, scores, st);
-            case 16: return launch_rows<16, 1>(q, pooled, n_rows, scale, scores, st);
+            case 1: return launch_rows<1, 4>(q, pooled, n_rows, scale, scores, hist, n_hist, st);
+            case 2: return launch_rows<2, 4>(q, pooled, n_rows, scale, scores, hist, n_hist, st);
+            case 4: return launch_rows<4, 2>(q, pooled, n_rows, scale, scores, hist, n_hist, st);
+            case 8: return launch_rows<8, 2>(q, pooled, n_rows, scale, scores, hist, n_hist, st);
+            case 16: return launch_rows<16, 1>(q, pooled, n_rows, scale, scores, hist, n_hist, st);
             default: break;
         }
     }
     const dim3 grid((unsigned)((n_rows + kBN - 1) / kBN), (unsigned)((n_q + kBM - 1) / kBM));
     return launch(score_tiled_kernel, grid, dim3(256), 0, st, 1, q, n_q, ld_q, q_pos, pooled,
-                  n_rows, hd, scale, scores, ld_scores);
+                  n_rows, hd, scale, scores, ld_scores, hist, n_hist);
 }
 
 }  // namespace qsa

@@ -7,17 +7,26 @@
 // block are recomputed each step; completed rows are reused).
 //
 // In decode this touches one or two rows (<= 4 raw rows read, 8 KB written), so it is
-// latency-bound; a full rebuild (n_valid_full = 0) streams the raw indexer keys once.
+// latency-bound: every thread issues all of its raw-key loads before using any, and the
+// rotation angles avoid device fp64 transcendentals (slow on this part): the inverse
+// frequencies base^(-2i/d) come from the host in fp64, the angle 4b * theta_i is formed
+// and reduced modulo 2*pi in fp64 (exact to ~1e-11 rad at a million tokens), and only
+// the reduced angle, |r| <= pi, goes through fp32 sincosf.
+#include <math.h>
+
 #include "qsa_internal.cuh"
 
 namespace qsa {
 namespace {
 
+constexpr int kPoolThreads = 512;
+
 template <typename T>
-__global__ void __launch_bounds__(512)
+__global__ void __launch_bounds__(kPoolThreads)
 pool_update_kernel(const T *__restrict__ raw, int64_t n_ctx, int H, int d,
-                   const float *__restrict__ w, float eps, double base,
-                   float *__restrict__ pooled, int64_t row0)
+                   const float *__restrict__ w, float eps, const RopeTable tab,
+                   float *__restrict__ pooled, int64_t row0, int64_t row1,
+                   uint32_t *__restrict__ zero_hist)
 {
     extern __shared__ float smem[];
     const int hd = H * d;
@@ -28,26 +37,31 @@ pool_update_kernel(const T *__restrict__ raw, int64_t n_ctx, int H, int d,
 
     pdl_wait();
     pdl_trigger();
+    if (zero_hist && blockIdx.x == 0)
+        for (int i = threadIdx.x; i < (1 << kTopkHistBits); i += kPoolThreads) zero_hist[i] = 0u;
 
     const int64_t b = row0 + blockIdx.x;
+    if (b >= row1) return;
     const int64_t t0 = 4 * b;
     const int c = (int)min((int64_t)4, n_ctx - t0);  // tokens present in this block (1..4)
     const float inv_c = 1.0f / (float)c;
+    const T *rb = raw + t0 * hd;
 
-    for (int e = threadIdx.x; e < hd; e += blockDim.x) {
-        float s = 0.0f;
-        for (int t = 0; t < c; ++t) s += to_f32(raw[(t0 + t) * hd + e]);
-        p_s[e] = s * inv_c;
+#pragma unroll 4
+    for (int e = threadIdx.x; e < hd; e += kPoolThreads) {
+        float v[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) v[t] = t < c ? to_f32(rb[(int64_t)t * hd + e]) : 0.0f;
+        p_s[e] = ((v[0] + v[1]) + (v[2] + v[3])) * inv_c;
     }
-    // Rotation angles depend on (b, i) only: form them once per row, in fp64, so that
-    // positions up to millions keep full angle accuracy.
-    for (int i = threadIdx.x; i < half; i += blockDim.x) {
-        const double theta = pow(base, -2.0 * (double)i / (double)d);
-        const double phi = (4.0 * (double)b) * theta;
-        double sv, cv;
-        sincos(phi, &sv, &cv);
-        cos_s[i] = (float)cv;
-        sin_s[i] = (float)sv;
+    for (int i = threadIdx.x; i < half; i += kPoolThreads) {
+        const double phi = (4.0 * (double)b) * tab.theta[i];
+        const double k = rint(phi * kInvTwoPi);
+        const float r = (float)fma(-k, kTwoPi, phi);
+        float sv, cv;
+        sincosf(r, &sv, &cv);
+        cos_s[i] = cv;
+        sin_s[i] = sv;
     }
     __syncthreads();
 
@@ -72,14 +86,31 @@ pool_update_kernel(const T *__restrict__ raw, int64_t n_ctx, int H, int d,
 
 }  // namespace
 
+void make_rope_table(RopeTable *tab, int d, double base)
+{
+    for (int i = 0; i < d / 2 && i < kRopeMaxHalf; ++i)
+        tab->theta[i] = pow(base, -2.0 * (double)i / (double)d);
+}
+
 cudaError_t launch_pool_update(const void *raw_k, qsa_dtype dt, int64_t n_ctx, int H, int d,
                                const float *norm_w, float eps, double rope_base,
-                               float *pooled, int64_t row0, int64_t row1, cudaStream_t st)
+                               float *pooled, int64_t row0, int64_t row1, uint32_t *zero_hist,
+                               cudaStream_t st)
 {
-    const int64_t n = row1 - row0;
-    if (n <= 0) return cudaSuccess;
-    const int warps = H < 16 ? H : 16;
-    const dim3 block(32 * warps);
+    int64_t n = row1 - row0;
+    if (n <= 0) {
+        if (!zero_hist) return cudaSuccess;
+        n = 1;  // one CTA clears the histogram
+    }
+    // the table depends on (d, base) only: rebuild it when they change
+    thread_local RopeTable tab;
+    thread_local int tab_d = -1;
+    thread_local double tab_base = 0.0;
+    if (tab_d != d || tab_base != rope_base) {
+        make_rope_table(&tab, d, rope_base);
+        tab_d = d;
+        tab_base = rope_base;
+    }
     const size_t smem = sizeof(float) * ((size_t)H * d + (size_t)d);
     static bool attr_set[2] = {false, false};
     if (dt == QSA_BF16) {
@@ -88,17 +119,17 @@ cudaError_t launch_pool_update(const void *raw_k, qsa_dtype dt, int64_t n_ctx, i
             cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
             attr_set[1] = true;
         }
-        return launch(k, dim3((unsigned)n), block, smem, st, 1,
-                      (const __nv_bfloat16 *)raw_k, n_ctx, H, d, norm_w, eps, rope_base, pooled,
-                      row0);
+        return launch(k, dim3((unsigned)n), dim3(kPoolThreads), smem, st, 1,
+                      (const __nv_bfloat16 *)raw_k, n_ctx, H, d, norm_w, eps, tab, pooled, row0,
+                      row1, zero_hist);
     }
     auto k = pool_update_kernel<float>;
     if (smem > 48 * 1024 && !attr_set[0]) {
         cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
         attr_set[0] = true;
     }
-    return launch(k, dim3((unsigned)n), block, smem, st, 1, (const float *)raw_k, n_ctx, H, d,
-                  norm_w, eps, rope_base, pooled, row0);
+    return launch(k, dim3((unsigned)n), dim3(kPoolThreads), smem, st, 1, (const float *)raw_k,
+                  n_ctx, H, d, norm_w, eps, tab, pooled, row0, row1, zero_hist);
 }
 
 }  // namespace qsa

@@ -94,16 +94,33 @@ cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
 
 int device_sm_count();
 
+// ------------------------------------------------------------------ RoPE frequencies
+// Inverse frequencies theta_i = base^(-2i/d), i < d/2, computed on the host in fp64 and
+// passed by value as a kernel parameter.
+constexpr int kRopeMaxHalf = 256;  // d <= 512
+struct RopeTable {
+    double theta[kRopeMaxHalf];
+};
+constexpr double kTwoPi = 6.283185307179586;
+constexpr double kInvTwoPi = 0.15915494309189535;
+void make_rope_table(RopeTable *tab, int d, double base);
+
 // ------------------------------------------------------------------ launchers
 // Host-side launchers, one per kernel family; arguments are already validated.
 
+// zero_hist (nullable): a top-k histogram that the kernel clears (the launch then has at
+// least one CTA even when no row needs recomputing).
 cudaError_t launch_pool_update(const void *raw_k, qsa_dtype dt, int64_t n_ctx, int H, int d,
                                const float *norm_w, float eps, double rope_base,
-                               float *pooled, int64_t row0, int64_t row1, cudaStream_t st);
+                               float *pooled, int64_t row0, int64_t row1, uint32_t *zero_hist,
+                               cudaStream_t st);
 
+// hist (nullable, decode only): also add each row b < n_hist to a histogram of the top
+// kTopkHistBits bits of its score key, for qsa_topk_blocks' first radix digit.
 cudaError_t launch_index_score(const float *q, int64_t n_q, int64_t ld_q, const int32_t *q_pos,
                                const float *pooled, int64_t n_rows, int H, int d, float scale,
-                               float *scores, int64_t ld_scores, cudaStream_t st);
+                               float *scores, int64_t ld_scores, uint32_t *hist, int64_t n_hist,
+                               cudaStream_t st);
 
 qsa_status launch_index_score_tc(const float *q, int64_t n_q, int64_t ld_q,
                                  const int32_t *q_pos, const float *pooled, int64_t n_rows,
@@ -111,12 +128,26 @@ qsa_status launch_index_score_tc(const float *q, int64_t n_q, int64_t ld_q,
                                  void *workspace, size_t ws_bytes, cudaStream_t st);
 size_t index_score_tc_workspace(int64_t n_q, int64_t n_rows, int H, int d);
 
-constexpr int kTopkCluster = 8;
-constexpr int kTopkThreads = 512;
+// Order-preserving key of a score: higher score <=> larger key.  NaN ranks as -inf;
+// -0 and +0 are the same score.
+__device__ __forceinline__ uint32_t score_key(float s)
+{
+    uint32_t u = __float_as_uint(s);
+    if ((u & 0x7fffffffu) > 0x7f800000u) u = 0xff800000u;  // NaN -> -inf
+    if (u == 0x80000000u) u = 0u;                           // -0 -> +0
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+constexpr int kTopkThreads = 1024;
+constexpr int kTopkHistBits = 12;  // first radix digit: histogram of key >> 20
+constexpr size_t kTopkHistBytes = sizeof(uint32_t) << kTopkHistBits;
 int64_t topk_max_candidates();
+// pos_out / n_cells_out (nullable): also write each query's cell list -- the selected
+// blocks' 4 cells in order, then the open tail of the query (q_pos[i], or n_ctx - 1).
 cudaError_t launch_topk(const float *scores, int64_t n_q, int64_t ld, const int32_t *q_pos,
                         int64_t n_full, int64_t k_blk, int32_t *blocks_out, int32_t *counts_out,
-                        cudaStream_t st);
+                        int64_t n_ctx, int32_t *pos_out, int32_t *n_cells_out,
+                        int64_t max_cells, uint32_t *ext_hist, cudaStream_t st);
 
 cudaError_t launch_gather(const void *K, const void *V, qsa_dtype dt, int64_t n_kv, int H_kv,
                           int d_k, int d_v, int64_t ld_k, int64_t ld_v, const int32_t *blocks,

@@ -1,44 +1,53 @@
-// topk.cu -- block-domain top-k by cluster-wide radix select.
+// topk.cu -- block-domain top-k: one CTA per query, radix select over score keys.
 //
 // Source: Qiita, ariera, EVO-X2 + Qwen3.8-Flash-Next llama.cpp series part 10, section
 // "block-domain top-k (COMMON-006)": select over the block scores instead of expanding
 // every block score to its cells first (the expansion cost grew with context:
-// 0.45 -> 0.91 ms per layer from 128k to 256k on the pages' GPU).
+// 0.45 -> 0.91 ms per layer from 128k to 256k on the pages' GPU), then expand only the
+// selected blocks to cell indices and append the tail.
 //
-// One thread-block cluster of 8 CTAs per query.  Each CTA keeps 1/8 of the candidates
-// (contiguous block indices) as order-preserving 32-bit keys in shared memory.  Three
-// radix passes (11 + 11 + 10 bits) find the k-th largest key T: every CTA histograms its
-// slice, the histograms are summed across the cluster through distributed shared memory,
-// and every CTA picks the same bucket.  The final pass keeps keys > T and the first
-// (lowest-index) keys == T until k are taken, writing them in ascending block order from
-// a cluster-wide exclusive scan of per-thread counts.  No grid-wide synchronisation and no
-// global scratch: cluster barriers are hardware barriers.
-#include <cooperative_groups.h>
-
+// Scores become order-preserving 32-bit keys.  The k-th largest key T is found by radix
+// select in three digits (12 + 10 + 10 bits):
+//   1. a 4096-bin histogram of the top 12 bits -- either accumulated by the score kernel
+//      as it writes the scores (decode step, no extra pass) or built here from one read;
+//   2. one read of the scores classifies every candidate: above the threshold bucket
+//      (selected: a bit in a shared-memory bitmap), inside it (appended to a candidate
+//      list in shared memory), or below (dropped);
+//   3. the remaining digits are resolved on the candidate list alone (a few hundred to a
+//      few thousand keys), stopping early once a bucket holds exactly the keys still
+//      needed;
+//   4. the candidates above T join the bitmap, the ones equal to T go to a tie bitmap;
+//   5. a block-wide scan over the bitmap words writes the selected blocks in ascending
+//      order -- ties taken lowest index first -- and, when asked, their cells and the
+//      open tail.
+// If the candidate list would overflow shared memory (pathological score
+// distributions), steps 3-4 re-read the scores instead.  No inter-CTA communication,
+// no global scratch beyond the optional histogram, no spin-waits.
 #include "qsa_internal.cuh"
-
-namespace cg = cooperative_groups;
 
 namespace qsa {
 namespace {
 
-constexpr int CL = kTopkCluster;
 constexpr int NT = kTopkThreads;
-constexpr int kBins = 2048;
-constexpr int kSmemFixedWords = 2 * kBins + 64 + 2 * NT;
+constexpr int kBins1 = 1 << kTopkHistBits;  // 4096
 constexpr int kMaxSmemBytes = 220 * 1024;
-constexpr int64_t kMaxSlice = (kMaxSmemBytes / 4) - kSmemFixedWords;
+constexpr int kFixedWords = kBins1 + 2 * (NT / 32) + 32;
+constexpr int64_t kMaxN = 640 * 1024;           // candidates per query
+constexpr int kCandCapMax = 16384;
 
-// Higher score <=> larger key.  NaN ranks as -inf; -0 and +0 are the same score.
-__device__ __forceinline__ uint32_t score_key(float s)
+__device__ __forceinline__ void put_cells(int32_t *dst, int32_t b, bool vec)
 {
-    uint32_t u = __float_as_uint(s);
-    if ((u & 0x7fffffffu) > 0x7f800000u) u = 0xff800000u;  // NaN -> -inf
-    if (u == 0x80000000u) u = 0u;                           // -0 -> +0
-    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    if (vec) {
+        *reinterpret_cast<int4 *>(dst) = make_int4(4 * b, 4 * b + 1, 4 * b + 2, 4 * b + 3);
+    } else {
+        dst[0] = 4 * b;
+        dst[1] = 4 * b + 1;
+        dst[2] = 4 * b + 2;
+        dst[3] = 4 * b + 3;
+    }
 }
 
-// Exclusive prefix sum over the block (NT threads); returns the total in *total.
+// Exclusive prefix sum over the block (NT threads); *total gets the block total.
 __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t *warp_s, uint32_t *total)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -57,164 +66,284 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t *warp_s
             const uint32_t y = __shfl_up_sync(0xffffffffu, w, o);
             if (lane >= o) w += y;
         }
-        if (lane < NT / 32) warp_s[lane] = w;  // inclusive per-warp totals
+        if (lane < NT / 32) warp_s[lane] = w;
     }
     __syncthreads();
-    const uint32_t warp_before = warp == 0 ? 0u : warp_s[warp - 1];
+    const uint32_t r = (warp == 0 ? 0u : warp_s[warp - 1]) + x - v;
     *total = warp_s[NT / 32 - 1];
-    const uint32_t r = warp_before + x - v;
-    __syncthreads();  // warp_s is reused by the caller's next scan
+    __syncthreads();
     return r;
 }
 
-__global__ void __launch_bounds__(NT)
-topk_cluster_kernel(const float *__restrict__ scores, int64_t ld, const int32_t *__restrict__ q_pos,
-                    int64_t n_full_cap, int k_blk, int32_t *__restrict__ blocks_out,
-                    int32_t *__restrict__ counts_out)
+// Bucket holding the k_rem-th largest of the histogram h[0..nb) (bins scanned from the
+// top).  Returns via misc: [0] bin, [1] keys in higher bins, [2] keys in the bin.
+__device__ __forceinline__ void find_bucket(const uint32_t *h, int nb, uint32_t k_rem,
+                                            uint32_t *warp_s, uint32_t *misc)
 {
-    cg::cluster_group cluster = cg::this_cluster();
-    const int rank = (int)cluster.block_rank();
-    const int64_t qi = blockIdx.x / CL;
+    const int per = nb / NT;  // 4 or 1
+    uint32_t cnt[4];
+    uint32_t mine = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        cnt[j] = j < per ? h[nb - 1 - threadIdx.x * per - j] : 0u;
+        mine += cnt[j];
+    }
+    uint32_t tot;
+    uint32_t above = block_excl_scan(mine, warp_s, &tot);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        if (j < per) {
+            if (above < k_rem && above + cnt[j] >= k_rem) {
+                misc[0] = (uint32_t)(nb - 1 - threadIdx.x * per - j);
+                misc[1] = above;
+                misc[2] = cnt[j];
+            }
+            above += cnt[j];
+        }
+    }
+    __syncthreads();
+}
 
-    extern __shared__ uint32_t smem[];
-    uint32_t *hist = smem;              // [kBins] this CTA's histogram
-    uint32_t *ghist = hist + kBins;     // [kBins] cluster-summed histogram
-    uint32_t *misc = ghist + kBins;     // [64] bucket choice, CTA totals
-    uint32_t *warp_s = misc + 64;       // [NT/32] scan scratch (x2)
-    uint32_t *keys = warp_s + 2 * NT;   // [slice]
+// Apply f(key, index) to every score of the row (coalesced, 16-byte loads when aligned).
+template <typename F>
+__device__ __forceinline__ void for_each_key(const float *__restrict__ row, int64_t n, F f)
+{
+    if ((reinterpret_cast<uintptr_t>(row) & 15) == 0) {
+        const int64_t n4 = n / 4;
+        const float4 *r4 = reinterpret_cast<const float4 *>(row);
+#pragma unroll 4
+        for (int64_t i = threadIdx.x; i < n4; i += NT) {
+            const float4 v = r4[i];
+            f(score_key(v.x), 4 * i);
+            f(score_key(v.y), 4 * i + 1);
+            f(score_key(v.z), 4 * i + 2);
+            f(score_key(v.w), 4 * i + 3);
+        }
+        for (int64_t i = 4 * n4 + threadIdx.x; i < n; i += NT) f(score_key(row[i]), i);
+    } else {
+#pragma unroll 4
+        for (int64_t i = threadIdx.x; i < n; i += NT) f(score_key(row[i]), i);
+    }
+}
+
+__global__ void __launch_bounds__(NT)
+topk_kernel(const float *__restrict__ scores, int64_t ld, const int32_t *__restrict__ q_pos,
+            int64_t n_full_cap, int k_blk, int32_t *__restrict__ blocks_out,
+            int32_t *__restrict__ counts_out, int64_t n_ctx, int32_t *__restrict__ pos_out,
+            int32_t *__restrict__ n_cells_out, int64_t max_cells, uint32_t *__restrict__ ext_hist,
+            int cand_cap)
+{
+    extern __shared__ __align__(16) uint32_t smem[];
+    uint32_t *hist = smem;                      // [4096]
+    uint32_t *warp_s = hist + kBins1;           // [2][NT/32]
+    uint32_t *misc = warp_s + 2 * (NT / 32);    // [32]
+    uint32_t *selw = misc + 32;                 // [nw] selected blocks bitmap
+    const int64_t qi = blockIdx.x;
 
     pdl_wait();
     pdl_trigger();
 
+    const int64_t p = q_pos ? (int64_t)q_pos[qi] : n_ctx - 1;  // the query's position
     int64_t n = n_full_cap;
     if (q_pos) {
-        const int64_t p1 = ((int64_t)q_pos[qi] + 1) / 4;
+        const int64_t p1 = (p + 1) / 4;
         n = p1 < n ? p1 : n;
     }
     if (n < 0) n = 0;
     const int64_t k = (int64_t)k_blk < n ? (int64_t)k_blk : n;
     int32_t *out = blocks_out + qi * (int64_t)k_blk;
-    if (rank == 0 && threadIdx.x == 0) counts_out[qi] = (int32_t)k;
-
-    const int64_t slice = (n + CL - 1) / CL;
-    const int64_t lo = (int64_t)rank * slice;
-    const int64_t hi = lo + slice < n ? lo + slice : n;
-    const int64_t len = hi > lo ? hi - lo : 0;
-
-    if (n <= k_blk) {  // every candidate is selected (uniform across the cluster)
-        for (int64_t i = threadIdx.x; i < len; i += NT) out[lo + i] = (int32_t)(lo + i);
+    int32_t *pout = pos_out ? pos_out + qi * max_cells : nullptr;
+    const bool pvec = (reinterpret_cast<uintptr_t>(pout) & 15) == 0;
+    uint32_t *ehist = ext_hist ? ext_hist + qi * (int64_t)kBins1 : nullptr;
+    if (threadIdx.x < 4) {
+        const int64_t tail0 = 4 * ((p + 1) / 4);
+        const int64_t n_tail = p + 1 - tail0;
+        if (threadIdx.x == 0) counts_out[qi] = (int32_t)k;
+        if (pout) {
+            if (threadIdx.x == 0) n_cells_out[qi] = (int32_t)(4 * k + n_tail);
+            if (threadIdx.x < n_tail) pout[4 * k + threadIdx.x] = (int32_t)(tail0 + threadIdx.x);
+        }
+    }
+    if (n <= k_blk) {  // every candidate is selected
+        for (int64_t i = threadIdx.x; i < n; i += NT) {
+            out[i] = (int32_t)i;
+            if (pout) put_cells(pout + 4 * i, (int32_t)i, pvec);
+        }
         return;
     }
-
+    const int64_t nw = (n + 31) / 32;
+    uint32_t *eqw = selw + nw;                               // [nw] tie bitmap
+    uint32_t *cand_key = eqw + nw;                           // [cand_cap]
+    int32_t *cand_idx = reinterpret_cast<int32_t *>(cand_key + cand_cap);
     const float *srow = scores + qi * ld;
-    for (int64_t i = threadIdx.x; i < len; i += NT) keys[i] = score_key(srow[lo + i]);
 
-    uint32_t prefix = 0;     // bits of T fixed so far
-    int fixed = 0;           // number of fixed high bits
-    uint32_t k_rem = (uint32_t)k;
-#pragma unroll
-    for (int pass = 0; pass < 3; ++pass) {
-        const int bits = pass == 2 ? 10 : 11;
-        const int shift = 32 - fixed - bits;
-        const int nb = 1 << bits;
-        for (int i = threadIdx.x; i < nb; i += NT) hist[i] = 0u;
+    // ---- 1. histogram of the top 12 bits
+    if (ehist) {
+        for (int i = threadIdx.x; i < kBins1; i += NT) hist[i] = ehist[i];
+    } else {
+        for (int i = threadIdx.x; i < kBins1; i += NT) hist[i] = 0u;
         __syncthreads();
-        for (int64_t i = threadIdx.x; i < len; i += NT) {
-            const uint32_t key = keys[i];
-            const bool match = fixed == 0 || (key >> (32 - fixed)) == prefix;
-            if (match) atomicAdd(&hist[(key >> shift) & (uint32_t)(nb - 1)], 1u);
-        }
-        cluster.sync();  // every CTA's histogram is complete
-        for (int i = threadIdx.x; i < nb; i += NT) {
-            uint32_t s = 0;
-#pragma unroll
-            for (int r = 0; r < CL; ++r) s += cluster.map_shared_rank(hist, r)[i];
-            ghist[i] = s;
-        }
-        cluster.sync();  // remote reads of hist are done before it is cleared again
-        // Bucket of the k_rem-th largest key: scan bins from the top.  Thread t owns
-        // bins nb-1-t*per .. nb-per-t*per (per = nb/NT, descending).
-        const int per = nb / NT;
-        uint32_t mine = 0;
-        for (int j = 0; j < per; ++j) mine += ghist[nb - 1 - threadIdx.x * per - j];
-        uint32_t tot;
-        uint32_t above = block_excl_scan(mine, warp_s, &tot);
-        for (int j = 0; j < per; ++j) {
-            const int bin = nb - 1 - threadIdx.x * per - j;
-            const uint32_t c = ghist[bin];
-            if (above < k_rem && above + c >= k_rem) {
-                misc[0] = (uint32_t)bin;
-                misc[1] = above;
+        for_each_key(srow, n, [&](uint32_t key, int64_t) {
+            const uint32_t bin = key >> (32 - kTopkHistBits);
+            const unsigned peers = __match_any_sync(__activemask(), bin);
+            if ((__ffs(peers) - 1) == (int)(threadIdx.x & 31)) atomicAdd(&hist[bin], __popc(peers));
+        });
+    }
+    for (int64_t i = threadIdx.x; i < 2 * nw; i += NT) selw[i] = 0u;
+    if (threadIdx.x == 0) misc[8] = 0u;  // candidate count
+    __syncthreads();
+    find_bucket(hist, kBins1, (uint32_t)k, warp_s, misc);
+    uint32_t prefix = misc[0];
+    int fixed = kTopkHistBits;
+    uint32_t k_rem = (uint32_t)k - misc[1];
+    bool whole = misc[2] == k_rem;
+    __syncthreads();
+
+    // ---- 2. classify every candidate (one read)
+    const uint32_t B1 = prefix;
+    for_each_key(srow, n, [&](uint32_t key, int64_t i) {
+        const uint32_t d = key >> (32 - kTopkHistBits);
+        const bool take = d > B1 || (whole && d == B1);
+        if (take) atomicOr(&selw[i >> 5], 1u << (i & 31));
+        const bool cand = !whole && d == B1;
+        const unsigned am = __activemask();
+        const unsigned cm = __ballot_sync(am, cand);
+        if (cand) {
+            const int leader = __ffs(cm) - 1;
+            uint32_t base = 0;
+            if ((int)(threadIdx.x & 31) == leader) base = atomicAdd(&misc[8], (uint32_t)__popc(cm));
+            base = __shfl_sync(cm, base, leader);
+            const uint32_t slot = base + __popc(cm & ((1u << (threadIdx.x & 31)) - 1u));
+            if (slot < (uint32_t)cand_cap) {
+                cand_key[slot] = key;
+                cand_idx[slot] = (int32_t)i;
             }
-            above += c;
         }
-        __syncthreads();
-        const uint32_t bucket = misc[0];
-        k_rem -= misc[1];
-        prefix = (prefix << bits) | bucket;
-        fixed += bits;
-        __syncthreads();
-    }
-    const uint32_t T = prefix;   // the k-th largest key
-    const uint32_t k_eq = k_rem; // keys == T to take, lowest block index first
+    });
+    __syncthreads();
 
-    // Contiguous chunk per thread so that the output comes out in index order.
-    const int64_t chunk = (len + NT - 1) / NT;
-    const int64_t c0 = (int64_t)threadIdx.x * chunk;
-    const int64_t c1 = c0 + chunk < len ? c0 + chunk : len;
-    uint32_t n_gt = 0, n_eq = 0;
-    for (int64_t i = c0; i < c1; ++i) {
-        const uint32_t key = keys[i];
-        n_gt += key > T;
-        n_eq += key == T;
+    if (!whole) {
+        const uint32_t n_cand = misc[8];
+        const bool in_smem = n_cand <= (uint32_t)cand_cap;
+        // ---- 3. remaining digits on the candidates
+        bool exact = false;
+#pragma unroll 1
+        for (int pass = 0; pass < 2; ++pass) {
+            const int bits = 10;
+            const int shift = 32 - fixed - bits;
+            const int nb = 1 << bits;
+            for (int i = threadIdx.x; i < nb; i += NT) hist[i] = 0u;
+            __syncthreads();
+            const uint32_t pf = prefix;
+            const int fx = fixed;
+            auto add = [&](uint32_t key, int64_t) {
+                if ((key >> (32 - fx)) == pf) atomicAdd(&hist[(key >> shift) & (uint32_t)(nb - 1)], 1u);
+            };
+            if (in_smem) {
+                for (uint32_t c = threadIdx.x; c < n_cand; c += NT) add(cand_key[c], 0);
+            } else {
+                for_each_key(srow, n, add);
+            }
+            __syncthreads();
+            find_bucket(hist, nb, k_rem, warp_s, misc);
+            k_rem -= misc[1];
+            prefix = (prefix << bits) | misc[0];
+            fixed += bits;
+            exact = misc[2] == k_rem;
+            __syncthreads();
+            if (exact) break;
+        }
+        // ---- 4. mark the candidates above the threshold and the ties
+        const int drop = 32 - fixed;
+        const uint32_t T = prefix;
+        auto mark = [&](uint32_t key, int64_t i) {
+            if ((key >> (32 - kTopkHistBits)) != B1) return;
+            const uint32_t kp = key >> drop;
+            if (kp > T || (exact && kp == T)) atomicOr(&selw[i >> 5], 1u << (i & 31));
+            else if (kp == T) atomicOr(&eqw[i >> 5], 1u << (i & 31));
+        };
+        if (in_smem) {
+            for (uint32_t c = threadIdx.x; c < n_cand; c += NT) mark(cand_key[c], cand_idx[c]);
+        } else {
+            for_each_key(srow, n, mark);
+        }
+        if (exact) k_rem = 0;
+        __syncthreads();
+    } else {
+        k_rem = 0;
     }
-    uint32_t tot_gt, tot_eq;
-    uint32_t gt_before = block_excl_scan(n_gt, warp_s, &tot_gt);
-    uint32_t eq_before = block_excl_scan(n_eq, warp_s + NT, &tot_eq);
-    if (threadIdx.x == 0) {
-        misc[2] = tot_gt;
-        misc[3] = tot_eq;
-    }
-    cluster.sync();
-    for (int r = 0; r < rank; ++r) {
-        const uint32_t *rm = cluster.map_shared_rank(misc, r);
-        gt_before += rm[2];
-        eq_before += rm[3];
-    }
-    for (int64_t i = c0; i < c1; ++i) {
-        const uint32_t key = keys[i];
-        if (key > T) {
-            out[gt_before + (eq_before < k_eq ? eq_before : k_eq)] = (int32_t)(lo + i);
-            ++gt_before;
-        } else if (key == T) {
-            if (eq_before < k_eq) out[gt_before + eq_before] = (int32_t)(lo + i);
+
+    // ---- 5. ordered output: ties lowest index first, then a scan over bitmap words
+    const int64_t wpt = (nw + NT - 1) / NT;
+    const int64_t w0 = (int64_t)threadIdx.x * wpt;
+    const int64_t w1 = w0 + wpt < nw ? w0 + wpt : nw;
+    uint32_t n_eq = 0;
+    for (int64_t w = w0; w < w1; ++w) n_eq += __popc(eqw[w]);
+    uint32_t tot;
+    uint32_t eq_before = block_excl_scan(n_eq, warp_s, &tot);
+    uint32_t n_sel = 0;
+    for (int64_t w = w0; w < w1; ++w) {
+        uint32_t e = eqw[w];
+        uint32_t keep = 0;
+        while (e && eq_before < k_rem) {
+            const uint32_t bit = e & (0u - e);
+            keep |= bit;
+            e ^= bit;
             ++eq_before;
         }
+        const uint32_t f = selw[w] | keep;
+        selw[w] = f;
+        n_sel += __popc(f);
     }
-    cluster.sync();  // keep this CTA's shared memory alive until every remote read is done
+    uint32_t o = block_excl_scan(n_sel, warp_s + NT / 32, &tot);
+    for (int64_t w = w0; w < w1; ++w) {
+        uint32_t f = selw[w];
+        while (f) {
+            const int b = __ffs(f) - 1;
+            f &= f - 1;
+            const int32_t blk = (int32_t)(32 * w + b);
+            if (o < (uint32_t)k) {
+                out[o] = blk;
+                if (pout) put_cells(pout + 4 * o, blk, pvec);
+            }
+            ++o;
+        }
+    }
+}
+
+size_t topk_smem_bytes(int64_t n, int *cand_cap)
+{
+    const int64_t nw = (n + 31) / 32;
+    int64_t words = kFixedWords + 2 * nw;
+    int64_t cap = (kMaxSmemBytes / 4 - words) / 2;
+    if (cap > kCandCapMax) cap = kCandCapMax;
+    if (cap < 0) cap = 0;
+    *cand_cap = (int)cap;
+    return sizeof(uint32_t) * (size_t)(words + 2 * cap);
 }
 
 }  // namespace
 
-int64_t topk_max_candidates() { return kMaxSlice * CL; }
+int64_t topk_max_candidates() { return kMaxN; }
 
 cudaError_t launch_topk(const float *scores, int64_t n_q, int64_t ld, const int32_t *q_pos,
                         int64_t n_full, int64_t k_blk, int32_t *blocks_out, int32_t *counts_out,
-                        cudaStream_t st)
+                        int64_t n_ctx, int32_t *pos_out, int32_t *n_cells_out,
+                        int64_t max_cells, uint32_t *ext_hist, cudaStream_t st)
 {
     if (n_q == 0) return cudaSuccess;
-    const int64_t slice = (n_full + CL - 1) / CL;
-    const size_t smem = sizeof(uint32_t) * ((size_t)kSmemFixedWords + (size_t)slice);
-    static size_t attr_bytes = 0;
-    if (smem > 48 * 1024 && attr_bytes < smem) {
-        cudaError_t e = cudaFuncSetAttribute(topk_cluster_kernel,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+    int cand_cap = 0;
+    const size_t smem = topk_smem_bytes(n_full, &cand_cap);
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              kMaxSmemBytes);
         if (e != cudaSuccess) return e;
-        attr_bytes = kMaxSmemBytes;
+        attr = true;
     }
-    return launch(topk_cluster_kernel, dim3((unsigned)(n_q * CL)), dim3(NT), smem, st, CL,
-                  scores, ld, q_pos, n_full, (int)k_blk, blocks_out, counts_out);
+    return launch(topk_kernel, dim3((unsigned)n_q), dim3(NT), smem, st, 1, scores, ld, q_pos,
+                  n_full, (int)k_blk, blocks_out, counts_out, n_ctx, pos_out, n_cells_out,
+                  max_cells, ext_hist, cand_cap);
 }
 
 }  // namespace qsa

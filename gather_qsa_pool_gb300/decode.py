@@ -38,7 +38,7 @@ class DecodeLayer:
         self.n_cells = torch.zeros(1, dtype=i32, device=device)
         self.out = torch.zeros(1, H_q, d, dtype=f32, device=device)
         self.lse = torch.zeros(1, H_q, dtype=f32, device=device)
-        ws = qb.sparse_attn_workspace_size(1, H_q, H_kv, d, self.max_cells)
+        ws = qb.decode_step_workspace_size(H_q, H_kv, d, self.max_cells)
         self.workspace = torch.empty(max(ws // 4, 1), dtype=f32, device=device)
         self.n_valid_full = 0
 
@@ -71,7 +71,7 @@ class DecodeLayer:
         self._fixed = (raw_k.data_ptr(), qb._dtype(raw_k), norm_w.data_ptr(),
                        self.pooled.data_ptr(), self.pooled.shape[0], self.scores.data_ptr(),
                        self.blocks.data_ptr(), self.counts.data_ptr(), K.data_ptr(), V.data_ptr(),
-                       qb._dtype(K), K.shape[0], K.stride(0), self.pos.data_ptr(),
+                       qb._dtype(K), K.shape[0], qb._ld(K), self.pos.data_ptr(),
                        self.n_cells.data_ptr(), self.out.data_ptr(), self.lse.data_ptr(),
                        self.workspace.data_ptr(), self.workspace.numel() * 4)
 

@@ -233,8 +233,14 @@ size_t qsa_sparse_attn_workspace_size(int64_t n_q, int H_q, int H_kv, int d_v,
  *   qsa_sparse_attn(q, 1, H_q, H_kv, d, d, scale, K, V, kv_dtype, n_kv, ld_kv, ld_kv, pos,
  *                   n_cells, max_cells, out, lse_out, workspace, workspace_bytes)
  * with n_rows = ceil(n_ctx/4), n_full = floor(n_ctx/4).  scores holds >= n_rows floats,
- * blocks k_blk ints, pos max_cells ints; the attention kernel reads the listed K/V rows in
- * place.  Returns the first failing validation status without enqueuing anything.
+ * blocks k_blk ints, pos max_cells ints.  Results are identical to those calls; the work
+ * is fused differently: the score kernel also counts the top 12 bits of each full
+ * block's score key into a histogram kept in the workspace (cleared by the pool-update
+ * kernel at the start of every step), the top-k kernel starts from that histogram and
+ * writes the cell list itself, and the attention kernel reads the listed K/V rows in
+ * place.  workspace: qsa_decode_step_workspace_size() bytes, 256-byte aligned, contents
+ * need no initialisation; steps that share a workspace must not overlap in time.
+ * Returns the first failing validation status without enqueuing anything.
  */
 qsa_status qsa_decode_step(const void *raw_k, qsa_dtype raw_dtype, int64_t n_ctx, int H_idx,
                            int d_idx, const float *norm_w, float eps, double rope_base,
@@ -245,6 +251,8 @@ qsa_status qsa_decode_step(const void *raw_k, qsa_dtype raw_dtype, int64_t n_ctx
                            int32_t *pos, int32_t *n_cells, int64_t max_cells, const float *q,
                            int H_q, float scale, float *out, float *lse_out, void *workspace,
                            size_t workspace_bytes, qsa_stream_t stream);
+
+size_t qsa_decode_step_workspace_size(int H_q, int H_kv, int d, int64_t max_cells);
 
 /*
  * qsa_mask_to_list -- build each mask row's list of attendable key positions.

@@ -322,3 +322,27 @@ def test_decode_steps_end_to_end(shape, steps):
             np.testing.assert_allclose(to_host(out)[0], o_out, rtol=0, atol=_atol(shape))
         else:
             assert n_band > 0
+
+
+def test_decode_step_composite_equals_separate_calls():
+    """qsa_decode_step (cell list written by the top-k kernel) and the five separate calls
+    (cell list from qsa_gather_kv) give bit-identical outputs."""
+    shape = SMALL_BF16
+    inp = qsa_synth.decode_inputs(shape, seed=12, extra_tokens=3, n_steps=3)
+    raw, w = to_dev(inp["raw_k"]), to_dev(inp["norm_w"])
+    K, V = to_dev(inp["K"]), to_dev(inp["V"])
+    kw = dict(cap_tokens=shape.n_ctx + 3, H_idx=shape.H_idx, d_idx=shape.d_idx, H_q=shape.H_q,
+              H_kv=shape.H_kv, d=shape.d, top_k_tokens=shape.top_k_tokens)
+    a, b = qsa.DecodeLayer(**kw), qsa.DecodeLayer(**kw)
+    a.rebuild(raw, w, shape.n_ctx - 1)
+    b.rebuild(raw, w, shape.n_ctx - 1)
+    for s in range(3):
+        n_ctx = shape.n_ctx + s
+        oa = a.step(raw, w, K, V, n_ctx, to_dev(inp["q_idx"][s]), to_dev(inp["q"][s])).clone()
+        ob = b.step_separate_calls(raw, w, K, V, n_ctx, to_dev(inp["q_idx"][s]),
+                                   to_dev(inp["q"][s])).clone()
+        assert torch.equal(a.pooled, b.pooled)
+        assert torch.equal(a.blocks, b.blocks) and torch.equal(a.n_cells, b.n_cells)
+        nc = int(a.n_cells.item())
+        assert torch.equal(a.pos[0, :nc], b.pos[0, :nc])
+        assert torch.equal(oa, ob)
