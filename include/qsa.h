@@ -255,6 +255,42 @@ qsa_status qsa_decode_step(const void *raw_k, qsa_dtype raw_dtype, int64_t n_ctx
 size_t qsa_decode_step_workspace_size(int H_q, int H_kv, int d, int64_t max_cells);
 
 /*
+ * qsa_sparse_attn_noalloc -- qsa_sparse_attn for callers that cannot allocate device
+ * memory.
+ *
+ * The source pages have no counterpart of this call: it is a service of this library.
+ *
+ * qsa_sparse_attn needs a caller-provided workspace for its split-K partial results.
+ * Some callers cannot obtain one: a plugin running inside a host framework that owns
+ * every device allocation and hands its plugins no allocator, or a real-time loop that
+ * must not risk the latency or the failure of a cudaMalloc.  This entry point takes no
+ * workspace.  Its scratch is a fixed array of QSA_NOALLOC_SCRATCH_BYTES bytes that the
+ * library defines in device memory; every GPU that loads the library keeps that array
+ * until the process exits.
+ *
+ * Arguments, layouts and results are those of qsa_sparse_attn without workspace and
+ * workspace_bytes.  The call allocates nothing and calls no allocating routine.  The
+ * first call on each device looks the array's device address up (cudaGetSymbolAddress,
+ * with that device current) and remembers it; make that first call before any stream
+ * capture.  All calls share the one array, which keeps whatever the previous call wrote
+ * there; nothing in it has to start at zero, because every call writes each partial
+ * record before reading it.  Calls that run at the same time on the GPU (on different
+ * streams, or in parallel branches of a graph) race on the array: the caller must
+ * order them.
+ *
+ * Errors: those of qsa_sparse_attn, plus QSA_ERR_UNSUPPORTED when the scratch this shape
+ * needs -- qsa_sparse_attn_workspace_size(n_q, H_q, H_kv, d_v, max_cells) -- is larger
+ * than QSA_NOALLOC_SCRATCH_BYTES (decode shapes fit: 32 query heads, 4 KV heads, d 128,
+ * 2051 cells need 1.1 MB), and QSA_ERR_CUDA when the address lookup fails.
+ */
+#define QSA_NOALLOC_SCRATCH_BYTES ((size_t)4 << 20)
+qsa_status qsa_sparse_attn_noalloc(const float *q, int64_t n_q, int H_q, int H_kv, int d_k,
+                                   int d_v, float scale, const void *K, const void *V,
+                                   qsa_dtype dtype, int64_t n_kv, int64_t ld_k, int64_t ld_v,
+                                   const int32_t *pos, const int32_t *n_cells, int64_t max_cells,
+                                   float *out, float *lse_out, qsa_stream_t stream);
+
+/*
  * qsa_mask_to_list -- build each mask row's list of attendable key positions.
  *
  * Source: devotd.net, "llama.cpp CDNA sparse attention", section 2 (attendable key
