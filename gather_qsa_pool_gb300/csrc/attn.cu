@@ -13,7 +13,11 @@
 // overlap this tile's math.  Logits: one warp per cell, lanes split the head dim, one
 // warp reduction per query head of the group.  Softmax: one warp per head, one lane per
 // cell.  P.V: each thread owns G*d_v/128 output entries.  fp32 throughout.
+#include <cooperative_groups.h>
+
 #include "qsa_internal.cuh"
+
+namespace cg = cooperative_groups;
 
 namespace qsa {
 namespace {
@@ -488,18 +492,349 @@ size_t attn128_smem()
            4 * (size_t)G * (128 + 2) * sizeof(float);
 }
 
-// Combine the S split partials of one (query, head): log-sum-exp weighting.
+// ---------------------------------------------------------------------------------
+// bf16 K/V, head dim 128, 8 query heads per KV head: QK^T and P.V on the tensor cores
+// with warp-level mma.m16n8k16 (bf16 operands, fp32 accumulation).  The 16 rows of the A
+// operand are the 8 heads twice: rows 0-7 hold the bf16 rounding of the (pre-scaled)
+// query, rows 8-15 the bf16 rounding of what that left over, so row h + row h+8 carries
+// the fp32 query to ~2^-17 relative; K and V are exact bf16.  The probabilities are split
+// the same way for P.V.  Per 16 cells a warp issues 16 + 16 MMAs and 8 + 8 ldmatrix loads
+// (vs. ~2700 CUDA-core instructions).  K and V tiles live in shared memory with rows
+// padded to 272 bytes so that the 8 rows of every ldmatrix fall in distinct banks.
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi)
+{
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);  // .x = lo (low half), .y = hi
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+__device__ __forceinline__ void split_bf16(float x, float &hi, float &lo)
+{
+    hi = __bfloat162float(__float2bfloat16_rn(x));
+    lo = x - hi;
+}
+
+__device__ __forceinline__ void mma_16816(float *c, const uint32_t *a, uint32_t b0, uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t *r, const void *p)
+{
+    const unsigned s = (unsigned)__cvta_generic_to_shared(p);
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(s));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t *r, const void *p)
+{
+    const unsigned s = (unsigned)__cvta_generic_to_shared(p);
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(s));
+}
+
+constexpr int kMmaWarps = 8;
+constexpr int kMmaTC = 16 * kMmaWarps;  // cells per stage: 16 per warp
+constexpr int kMmaLd = 136;             // padded smem row in bf16 elements = 272 bytes
+constexpr int kMmaMaxCluster = 16;      // splits of one (query, KV head) merged in-cluster
+
+__host__ __device__ constexpr size_t attn_mma_smem()
+{
+    // K and V stages, cell rows, per-warp states, the CTA's merged state
+    return 2 * 2 * (size_t)kMmaTC * kMmaLd * 2 + 2 * kMmaTC * 4 +
+           (size_t)kMmaWarps * 8 * (128 + 2) * 4 + (size_t)8 * (128 + 2) * 4;
+}
+
+// Grid (S, H_kv, n_q).  With S > 1 the S CTAs of one (query, KV head) form a thread-block
+// cluster: each merges its warps into one (m, l, o) per head in shared memory, then every
+// CTA combines a slice of the 8 x 128 outputs from all S states through distributed shared
+// memory -- no partials in global memory and no second kernel.
+__global__ void __launch_bounds__(32 * kMmaWarps)
+attn_mma_kernel(const float *__restrict__ q, int H_q, int H_kv, float scale_log2,
+                const __nv_bfloat16 *__restrict__ K, const __nv_bfloat16 *__restrict__ V,
+                int64_t n_kv, int64_t ld_k, int64_t ld_v, const int32_t *__restrict__ pos,
+                const int32_t *__restrict__ n_cells, int64_t max_cells, float *__restrict__ out,
+                float *__restrict__ lse)
+{
+    constexpr int G = 8, D = 128, TC = kMmaTC, LD = kMmaLd, NW = kMmaWarps, NT = 32 * NW;
+    extern __shared__ __align__(16) char smem_raw[];
+    __nv_bfloat16 *Ks = reinterpret_cast<__nv_bfloat16 *>(smem_raw);  // [2][TC][LD]
+    __nv_bfloat16 *Vs = Ks + 2 * TC * LD;                                // [2][TC][LD]
+    int32_t *rows = reinterpret_cast<int32_t *>(Vs + 2 * TC * LD);      // [2][TC]
+    float *mrg = reinterpret_cast<float *>(rows + 2 * TC);               // [NW][G][D+2]
+    float *cta = mrg + NW * G * (D + 2);                                 // [G][D+2]: o, m, l
+
+    const int S = gridDim.x, s_idx = blockIdx.x, g = blockIdx.y;
+    const int64_t qi = blockIdx.z;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int hr = lane >> 2;       // head of this lane's fragment rows
+    const int qc = (lane & 3) * 2;  // first column of this lane's fragment pairs
+    const int mi = lane >> 3, mj = lane & 7;  // ldmatrix: matrix and row this lane addresses
+
+    pdl_wait();
+    pdl_trigger();
+
+    int64_t n = n_cells[qi];
+    const bool overflow = n > max_cells;  // truncated list: the result must not be used
+    if (overflow) n = 0;
+    if (n < 0) n = 0;
+    const int64_t chunk = (n + S - 1) / S;
+    const int64_t c0 = (int64_t)s_idx * chunk;
+    const int64_t c1 = c0 + chunk < n ? c0 + chunk : n;
+    const int ntiles = c1 > c0 ? (int)((c1 - c0 + TC - 1) / TC) : 0;
+
+    // A fragments of the query: rows 0-7 = hi, rows 8-15 = lo, for 8 k-steps of 16 dims
+    uint32_t qa[8][4];
+    {
+        const float *qh = q + (qi * H_q + (int64_t)g * G + hr) * D;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+            const float2 x0 = *reinterpret_cast<const float2 *>(qh + ks * 16 + qc);
+            const float2 x1 = *reinterpret_cast<const float2 *>(qh + ks * 16 + 8 + qc);
+            float h0, l0, h1, l1, h2, l2, h3, l3;
+            split_bf16(x0.x * scale_log2, h0, l0);
+            split_bf16(x0.y * scale_log2, h1, l1);
+            split_bf16(x1.x * scale_log2, h2, l2);
+            split_bf16(x1.y * scale_log2, h3, l3);
+            qa[ks][0] = pack_bf16(h0, h1);
+            qa[ks][1] = pack_bf16(l0, l1);
+            qa[ks][2] = pack_bf16(h2, h3);
+            qa[ks][3] = pack_bf16(l2, l3);
+        }
+    }
+    float o[16][4];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.0f;
+    float m = -INFINITY, lsum = 0.0f;
+
+    auto issue = [&](int it, int buf) {
+        const int64_t base = c0 + (int64_t)it * TC;
+        const int tc = (int)min((int64_t)TC, c1 - base);
+        int32_t *rb = rows + buf * TC;
+        for (int slot = tid; slot < TC; slot += NT) {
+            int64_t row = -1;
+            if (slot < tc) {
+                const int64_t cell = base + slot;
+                row = pos ? (int64_t)pos[qi * max_cells + cell] : qi * max_cells + cell;
+                if (row < 0 || row >= n_kv) row = -1;
+            }
+            rb[slot] = (int32_t)row;
+        }
+        __syncthreads();
+        __nv_bfloat16 *ks = Ks + buf * TC * LD;
+        __nv_bfloat16 *vs = Vs + buf * TC * LD;
+        // 16 K chunks + 16 V chunks per row.  A skipped row's K is never used (its logit is
+        // masked by a select), but its V row is multiplied by p = 0 inside the MMA, so it is
+        // zero-filled: stale shared memory could hold a NaN pattern.
+        for (int e = tid; e < TC * 32; e += NT) {
+            const int slot = e >> 5;
+            const int c = e & 31;
+            const int64_t row = rb[slot];
+            if (row < 0) {
+                if (c >= 16) cp_async16(vs + slot * LD + (c - 16) * 8, V, false);
+                continue;
+            }
+            if (c < 16)
+                cp_async16(ks + slot * LD + c * 8, K + row * ld_k + (int64_t)g * D + c * 8, true);
+            else
+                cp_async16(vs + slot * LD + (c - 16) * 8,
+                           V + row * ld_v + (int64_t)g * D + (c - 16) * 8, true);
+        }
+        cp_async_commit();
+    };
+
+    if (ntiles > 0) issue(0, 0);
+    for (int it = 0; it < ntiles; ++it) {
+        const int buf = it & 1;
+        if (it + 1 < ntiles) {
+            issue(it + 1, buf ^ 1);
+            cp_async_wait<1>();
+        } else {
+            cp_async_wait<0>();
+        }
+        __syncthreads();
+        const int tc = (int)min((int64_t)TC, c1 - (c0 + (int64_t)it * TC));
+        const __nv_bfloat16 *ks = Ks + buf * TC * LD;
+        const __nv_bfloat16 *vs = Vs + buf * TC * LD;
+        const int32_t *rw = rows + buf * TC;
+        const int s0 = warp * 16;  // this warp's 16 cells of the stage
+        if (s0 < tc) {
+            // S = Q K^T for cells s0..s0+15 as two n-tiles of 8 cells
+            float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                uint32_t b[4];
+                const int cell = s0 + (mi >> 1) * 8 + mj;
+                ldsm_x4(b, ks + cell * LD + kk * 16 + (mi & 1) * 8);
+                mma_16816(sc[0], qa[kk], b[0], b[1]);
+                mma_16816(sc[1], qa[kk], b[2], b[3]);
+            }
+            // logits of head hr for cells s0 + nt*8 + qc + {0,1}: hi row + lo row
+            float x[4];
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const int slot = s0 + nt * 8 + qc + u;
+                    const bool ok = slot < tc && rw[slot] >= 0;
+                    x[nt * 2 + u] = ok ? sc[nt][u] + sc[nt][u + 2] : -INFINITY;
+                }
+            }
+            float cmax = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+            cmax = fmaxf(cmax, __shfl_xor_sync(0xffffffffu, cmax, 1));
+            cmax = fmaxf(cmax, __shfl_xor_sync(0xffffffffu, cmax, 2));
+            const float m_new = fmaxf(m, cmax);
+            const bool live = m_new != -INFINITY;
+            // warp-uniform branch: every lane takes part in the MMAs below
+            if (__any_sync(0xffffffffu, live)) {
+                const float alpha = live ? exp2f(m - m_new) : 1.0f;
+                float p[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) p[u] = live ? exp2f(x[u] - m_new) : 0.0f;
+                if (live) {
+                    lsum = lsum * alpha + ((p[0] + p[1]) + (p[2] + p[3]));
+                    m = m_new;
+                }
+                if (alpha != 1.0f) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        o[j][0] *= alpha;
+                        o[j][1] *= alpha;
+                        o[j][2] *= alpha;
+                        o[j][3] *= alpha;
+                    }
+                }
+                // A fragment of P (rows 0-7 hi, 8-15 lo); the K dim is the 16 cells
+                float ph[4], pl[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) split_bf16(p[u], ph[u], pl[u]);
+                uint32_t pa[4];
+                pa[0] = pack_bf16(ph[0], ph[1]);
+                pa[1] = pack_bf16(pl[0], pl[1]);
+                pa[2] = pack_bf16(ph[2], ph[3]);
+                pa[3] = pack_bf16(pl[2], pl[3]);
+                // O += P V over 16 dim tiles of 8; ldmatrix.trans gives V^T fragments
+#pragma unroll
+                for (int dp = 0; dp < 8; ++dp) {
+                    uint32_t b[4];
+                    const int cell = s0 + (mi & 1) * 8 + mj;
+                    ldsm_x4_t(b, vs + cell * LD + dp * 16 + (mi >> 1) * 8);
+                    mma_16816(o[2 * dp], pa, b[0], b[1]);
+                    mma_16816(o[2 * dp + 1], pa, b[2], b[3]);
+                }
+            }
+        }
+        __syncthreads();  // this stage is refilled by the next issue()
+    }
+
+    // per-warp state -> shared memory: head hr, dims 8j + qc + {0,1}
+    float l4 = lsum;
+    l4 += __shfl_xor_sync(0xffffffffu, l4, 1);
+    l4 += __shfl_xor_sync(0xffffffffu, l4, 2);
+    float *mw = mrg + ((size_t)warp * G + hr) * (D + 2);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        mw[8 * j + qc] = o[j][0] + o[j][2];
+        mw[8 * j + qc + 1] = o[j][1] + o[j][3];
+    }
+    if ((lane & 3) == 0) {
+        mw[D] = m;
+        mw[D + 1] = l4;
+    }
+    __syncthreads();
+    // merge the warps: the CTA's (o unnormalised, m, l) per head
+    for (int e = tid; e < G * D; e += NT) {
+        const int h = e / D, c = e - h * D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) M = fmaxf(M, mrg[(w * G + h) * (D + 2) + D]);
+        float acc = 0.0f, L = 0.0f;
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < NW; ++w) {
+                const float *r = mrg + (w * G + h) * (D + 2);
+                const float f = exp2f(r[D] - M);
+                acc = fmaf(f, r[c], acc);
+                L = fmaf(f, r[D + 1], L);
+            }
+        }
+        if (S == 1) {
+            float v = L > 0.0f ? acc / L : 0.0f;
+            if (overflow) v = __int_as_float(0x7fc00000);
+            out[(qi * H_q + (int64_t)g * G + h) * D + c] = v;
+            if (lse && c == 0)
+                lse[qi * H_q + g * G + h] = overflow ? __int_as_float(0x7fc00000)
+                                           : (L > 0.0f ? (M + log2f(L)) * kLn2 : -INFINITY);
+        } else {
+            float *r = cta + h * (D + 2);
+            r[c] = acc;
+            if (c == 0) {
+                r[D] = M;
+                r[D + 1] = L;
+            }
+        }
+    }
+    if (S == 1) return;
+
+    // combine the S CTAs of the cluster: CTA s owns outputs [s*per, (s+1)*per) of G*D
+    cg::cluster_group cluster = cg::this_cluster();
+    cluster.sync();  // every CTA's merged state is in its shared memory
+    const int per = (G * D + S - 1) / S;
+    for (int e = s_idx * per + tid; e < (s_idx + 1) * per && e < G * D; e += NT) {
+        const int h = e / D, c = e - h * D;
+        float mv[kMmaMaxCluster], lv[kMmaMaxCluster], ov[kMmaMaxCluster];
+        float M = -INFINITY;
+#pragma unroll
+        for (int r = 0; r < kMmaMaxCluster; ++r) {
+            if (r < S) {
+                const float *rc = cluster.map_shared_rank(cta, r) + h * (D + 2);
+                mv[r] = rc[D];
+                lv[r] = rc[D + 1];
+                ov[r] = rc[c];
+                M = fmaxf(M, mv[r]);
+            }
+        }
+        float acc = 0.0f, L = 0.0f;
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int r = 0; r < kMmaMaxCluster; ++r) {
+                if (r < S) {
+                    const float f = exp2f(mv[r] - M);
+                    acc = fmaf(f, ov[r], acc);
+                    L = fmaf(f, lv[r], L);
+                }
+            }
+        }
+        float v = L > 0.0f ? acc / L : 0.0f;
+        if (overflow) v = __int_as_float(0x7fc00000);
+        out[(qi * H_q + (int64_t)g * G + h) * D + c] = v;
+        if (lse && c == 0)
+            lse[qi * H_q + g * G + h] = overflow ? __int_as_float(0x7fc00000)
+                                       : (L > 0.0f ? (M + log2f(L)) * kLn2 : -INFINITY);
+    }
+    cluster.sync();  // keep this CTA's state alive until every remote read is done
+}
+
+// Combine the S split partials of one (query, head): log-sum-exp weighting.  The split
+// maxima and weights go through shared memory once; every output dim then sums its S
+// partials with eight independent loads in flight.
 __global__ void __launch_bounds__(128)
 attn_combine_kernel(const float *__restrict__ part, int S, int H_q, int H_kv, int d_v,
                     const int32_t *__restrict__ n_cells, int64_t max_cells,
                     float *__restrict__ out, float *__restrict__ lse)
 {
-    extern __shared__ float wsm[];  // [S] weights, then [32] reduction scratch
+    extern __shared__ float wsm[];  // [S] weights, [S] sums, [8] reduction scratch
     const int h = blockIdx.x;
     const int64_t qi = blockIdx.y;
     const int G = H_q / H_kv;
     const int g = h / G, hh = h - g * G;
     const int rec = d_v + 4;
+    const int64_t stride = (int64_t)G * rec;
     pdl_wait();
     pdl_trigger();
     float *o = out + (qi * H_q + h) * (int64_t)d_v;
@@ -508,45 +843,79 @@ attn_combine_kernel(const float *__restrict__ part, int S, int H_q, int H_kv, in
         if (lse && threadIdx.x == 0) lse[qi * H_q + h] = __int_as_float(0x7fc00000);
         return;
     }
-    const float *pr = part + ((qi * H_kv + g) * (int64_t)S * G + hh) * rec;  // split s at + s*G*rec
-    float *red = wsm + S;
+    const float *pr = part + ((qi * H_kv + g) * (int64_t)S * G + hh) * rec;  // split s: + s*stride
+    float *ls = wsm + S;
+    float *red = wsm + 2 * S;
     float mx = -INFINITY;
-    for (int s = threadIdx.x; s < S; s += blockDim.x) mx = fmaxf(mx, pr[(int64_t)s * G * rec]);
+    for (int s = threadIdx.x; s < S; s += blockDim.x) {
+        const float mv = pr[s * stride];
+        wsm[s] = mv;
+        ls[s] = pr[s * stride + 1];
+        mx = fmaxf(mx, mv);
+    }
     mx = warp_max(mx);
     if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
     __syncthreads();
-    mx = red[0];
-    for (int w = 1; w < (int)(blockDim.x >> 5); ++w) mx = fmaxf(mx, red[w]);
+    mx = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
     __syncthreads();
-    float lsum = 0.0f;
     for (int s = threadIdx.x; s < S; s += blockDim.x) {
-        const float m = pr[(int64_t)s * G * rec];
-        const float w = (m == -INFINITY) ? 0.0f : exp2f(m - mx);
-        wsm[s] = w;
-        lsum += w * pr[(int64_t)s * G * rec + 1];
+        const float mv = wsm[s];
+        wsm[s] = mv == -INFINITY ? 0.0f : exp2f(mv - mx);
     }
-    lsum = warp_sum(lsum);
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = lsum;
     __syncthreads();
     float L = 0.0f;
-    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) L += red[w];
+    for (int s = 0; s < S; ++s) L = fmaf(wsm[s], ls[s], L);
     const float inv = L > 0.0f ? 1.0f / L : 0.0f;
     for (int c = threadIdx.x; c < d_v; c += blockDim.x) {
-        float acc0 = 0.0f, acc1 = 0.0f, acc2 = 0.0f, acc3 = 0.0f;
         const float *pc = pr + 4 + c;
-        const int64_t stride = (int64_t)G * rec;
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         int s = 0;
-#pragma unroll 2
-        for (; s + 4 <= S; s += 4) {
-            acc0 = fmaf(wsm[s], pc[s * stride], acc0);
-            acc1 = fmaf(wsm[s + 1], pc[(s + 1) * stride], acc1);
-            acc2 = fmaf(wsm[s + 2], pc[(s + 2) * stride], acc2);
-            acc3 = fmaf(wsm[s + 3], pc[(s + 3) * stride], acc3);
+        for (; s + 8 <= S; s += 8) {
+            float v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) v[u] = pc[(s + u) * stride];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) acc[u] = fmaf(wsm[s + u], v[u], acc[u]);
         }
-        for (; s < S; ++s) acc0 = fmaf(wsm[s], pc[s * stride], acc0);
-        o[c] = ((acc0 + acc1) + (acc2 + acc3)) * inv;
+        for (; s < S; ++s) acc[0] = fmaf(wsm[s], pc[s * stride], acc[0]);
+        o[c] = (((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]))) * inv;
     }
     if (lse && threadIdx.x == 0) lse[qi * H_q + h] = L > 0.0f ? (mx + log2f(L)) * kLn2 : -INFINITY;
+}
+
+// Splits for the tensor-core kernel: about one 128-cell stage per CTA, at most one
+// cluster (16 CTAs) per (query, KV head); one split per group when there are many groups.
+int attn_mma_splits(int64_t n_q, int H_kv, int64_t max_cells)
+{
+    const int64_t groups = n_q * (int64_t)H_kv;
+    if (groups >= kTargetSMs) return 1;
+    int64_t S = (max_cells + kMmaTC - 1) / kMmaTC;
+    if (S > kMmaMaxCluster) S = kMmaMaxCluster;
+    if (S < 1) S = 1;
+    return (int)S;
+}
+
+cudaError_t launch_attn_mma(const float *q, int64_t n_q, int H_q, int H_kv, float scale,
+                            const void *K, const void *V, int64_t n_kv, int64_t ld_k, int64_t ld_v,
+                            const int32_t *pos, const int32_t *n_cells, int64_t max_cells,
+                            float *out, float *lse, cudaStream_t st)
+{
+    const size_t smem = attn_mma_smem();
+    static bool set = false;
+    if (!set) {
+        cudaError_t e = cudaFuncSetAttribute(attn_mma_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(attn_mma_kernel,
+                                     cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return e;
+        set = true;
+    }
+    const int S = attn_mma_splits(n_q, H_kv, max_cells);
+    const dim3 grid((unsigned)S, (unsigned)H_kv, (unsigned)n_q);
+    return launch(attn_mma_kernel, grid, dim3(32 * kMmaWarps), smem, st, S > 1 ? S : 1, q, H_q,
+                  H_kv, scale * kLog2e, (const __nv_bfloat16 *)K, (const __nv_bfloat16 *)V, n_kv,
+                  ld_k, ld_v, pos, n_cells, max_cells, out, lse);
 }
 
 template <typename T, int G>
@@ -569,7 +938,7 @@ cudaError_t launch_attn128_t(const float *q, int64_t n_q, int H_q, int H_kv, flo
                            (const T *)K, (const T *)V, n_kv, ld_k, ld_v, pos, n_cells, max_cells,
                            out, lse, part);
     if (e != cudaSuccess || S == 1) return e;
-    const size_t csmem = sizeof(float) * ((size_t)S + 32);
+    const size_t csmem = sizeof(float) * (2 * (size_t)S + 8);
     return launch(attn_combine_kernel, dim3((unsigned)H_q, (unsigned)n_q), dim3(128), csmem, st,
                   1, (const float *)part, S, H_q, H_kv, 128, n_cells, max_cells, out, lse);
 }
@@ -595,7 +964,7 @@ cudaError_t launch_attn_t(const float *q, int64_t n_q, int H_q, int H_kv, int d_
                            scale * kLog2e, (const T *)K, (const T *)V, n_kv, ld_k, ld_v, pos,
                            n_cells, max_cells, out, lse, part);
     if (e != cudaSuccess || S == 1) return e;
-    const size_t csmem = sizeof(float) * ((size_t)S + 32);
+    const size_t csmem = sizeof(float) * (2 * (size_t)S + 8);
     return launch(attn_combine_kernel, dim3((unsigned)H_q, (unsigned)n_q), dim3(128), csmem, st,
                   1, (const float *)part, S, H_q, H_kv, d_v, n_cells, max_cells, out, lse);
 }
@@ -612,10 +981,15 @@ int attn_num_splits(int64_t n_q, int H_kv, int64_t max_cells)
     const int64_t groups = n_q * (int64_t)H_kv;
     if (groups <= 0) return 1;
     int64_t S = (2 * kTargetSMs + groups - 1) / groups;
-    const int64_t max_by_tiles = (max_cells + kTile - 1) / kTile;
+    const int64_t max_by_tiles = (max_cells + 63) / 64;  // at least ~64 cells per split
     if (S > max_by_tiles) S = max_by_tiles;
     if (S < 1) S = 1;
     return (int)S;
+}
+
+bool attn_uses_mma(qsa_dtype dt, int d_k, int d_v, int G)
+{
+    return dt == QSA_BF16 && d_k == 128 && d_v == 128 && G == 8;
 }
 
 size_t attn_workspace_bytes(int64_t n_q, int H_q, int H_kv, int d_v, int64_t max_cells)
@@ -635,6 +1009,9 @@ cudaError_t launch_sparse_attn(const float *q, int64_t n_q, int H_q, int H_kv, i
     if (n_q == 0) return cudaSuccess;
     const int S = attn_num_splits(n_q, H_kv, max_cells);
     const int G = H_q / H_kv;
+    if (attn_uses_mma(dt, d_k, d_v, G))
+        return launch_attn_mma(q, n_q, H_q, H_kv, scale, K, V, n_kv, ld_k, ld_v, pos, n_cells,
+                               max_cells, out, lse, st);
     if (d_k == 128 && d_v == 128 && G <= 8) {
 #define QSA_ATTN128_CASE(GG)                                                                   \
     case GG:                                                                                   \

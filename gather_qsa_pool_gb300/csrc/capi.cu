@@ -279,13 +279,27 @@ qsa_status qsa_decode_step(const void *raw_k, qsa_dtype raw_dtype, int64_t n_ctx
                        max_cells, out, workspace, attn_bytes);
     if (v != QSA_OK) return v;
     const cudaStream_t st = (cudaStream_t)stream;
-    // 1. pooled rows of the new / open block; clears the top-k histogram
-    cudaError_t e = run_pool_update(raw_k, raw_dtype, n_ctx, H_idx, d_idx, norm_w, eps, rope_base,
-                                    pooled, n_valid_full, hist, st);
-    // 2. scores of every row; full blocks also enter the histogram of their top key bits
-    if (e == cudaSuccess)
-        e = launch_index_score(q_idx, 1, (int64_t)H_idx * d_idx, nullptr, pooled, n_rows, H_idx,
-                               d_idx, scale_idx, scores, n_rows, hist, n_full, st);
+    // 1+2. pooled rows of the new / open block, then scores of every row; full blocks also
+    // enter the histogram of their top key bits.  One kernel when the rows to recompute are
+    // few (the decode case), else the pool-update kernel followed by the score kernel.
+    const int64_t row0 = n_valid_full < n_full ? n_valid_full : n_full;
+    PoolFuse pf;
+    pf.raw = raw_k;
+    pf.dt = raw_dtype;
+    pf.n_ctx = n_ctx;
+    pf.w = norm_w;
+    pf.eps = eps;
+    pf.row0 = row0;
+    pf.row1 = n_rows;
+    cudaError_t e = launch_score_pool_fused(q_idx, pooled, n_rows, H_idx, d_idx, scale_idx, scores,
+                                            hist, n_full, pf, rope_base, st);
+    if (e == cudaErrorNotSupported) {
+        e = run_pool_update(raw_k, raw_dtype, n_ctx, H_idx, d_idx, norm_w, eps, rope_base, pooled,
+                            n_valid_full, hist, st);
+        if (e == cudaSuccess)
+            e = launch_index_score(q_idx, 1, (int64_t)H_idx * d_idx, nullptr, pooled, n_rows,
+                                   H_idx, d_idx, scale_idx, scores, n_rows, hist, n_full, st);
+    }
     // 3. top-k from that histogram; its epilogue writes the cell list (qsa_gather_kv's job)
     if (e == cudaSuccess)
         e = launch_topk(scores, 1, n_rows, nullptr, n_full, k_blk, blocks, counts, n_ctx, pos,

@@ -18,25 +18,15 @@ namespace {
 
 constexpr int kScoreThreads = 256;
 
-// One query, H*d = NV*128 floats per row.  Each warp owns rows gw, gw + nw, ...; R rows
-// are loaded before any is reduced.
+// One query, H*d = NV*128 floats per row.  Warps gw, gw + nw, ... of the grid walk the
+// rows [0, n_rows); R rows are loaded before any is reduced.
 template <int NV, int R>
-__global__ void __launch_bounds__(kScoreThreads)
-score_rows_kernel(const float *__restrict__ q, const float *__restrict__ pooled,
-                  int64_t n_rows, float scale, float *__restrict__ scores,
-                  uint32_t *__restrict__ hist, int64_t n_hist)
+__device__ __forceinline__ void score_rows_loop(const float4 *q_s, const float *__restrict__ pooled,
+                                                int64_t n_rows, int64_t gw, int64_t nw,
+                                                float scale, float *__restrict__ scores,
+                                                uint32_t *__restrict__ hist, int64_t n_hist)
 {
-    __shared__ float4 q_s[NV * 32];
-    pdl_wait();
-    pdl_trigger();
-    for (int i = threadIdx.x; i < NV * 32; i += blockDim.x)
-        q_s[i] = reinterpret_cast<const float4 *>(q)[i];
-    __syncthreads();
-
     const int lane = threadIdx.x & 31;
-    const int64_t nw = (int64_t)gridDim.x * (kScoreThreads / 32);
-    const int64_t gw = (int64_t)blockIdx.x * (kScoreThreads / 32) + (threadIdx.x >> 5);
-
     for (int64_t r0 = gw; r0 < n_rows; r0 += nw * R) {
         float4 v[R][NV];
 #pragma unroll
@@ -70,6 +60,80 @@ score_rows_kernel(const float *__restrict__ q, const float *__restrict__ pooled,
             }
         }
     }
+}
+
+// The score of one row already in shared memory, with exactly the summation order of
+// score_rows_loop (called by one warp).
+template <int NV>
+__device__ __forceinline__ float score_row_smem(const float4 *q_s, const float *row_s)
+{
+    const int lane = threadIdx.x & 31;
+    const float4 *rp = reinterpret_cast<const float4 *>(row_s) + lane;
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+        const float4 v = rp[32 * j];
+        const float4 qq = q_s[lane + 32 * j];
+        a0 = fmaf(v.x, qq.x, a0);
+        a1 = fmaf(v.y, qq.y, a1);
+        a2 = fmaf(v.z, qq.z, a2);
+        a3 = fmaf(v.w, qq.w, a3);
+    }
+    return warp_sum((a0 + a1) + (a2 + a3));
+}
+
+template <int NV, int R>
+__global__ void __launch_bounds__(kScoreThreads)
+score_rows_kernel(const float *__restrict__ q, const float *__restrict__ pooled,
+                  int64_t n_rows, float scale, float *__restrict__ scores,
+                  uint32_t *__restrict__ hist, int64_t n_hist)
+{
+    __shared__ float4 q_s[NV * 32];
+    pdl_wait();
+    pdl_trigger();
+    for (int i = threadIdx.x; i < NV * 32; i += blockDim.x)
+        q_s[i] = reinterpret_cast<const float4 *>(q)[i];
+    __syncthreads();
+    const int64_t nw = (int64_t)gridDim.x * (kScoreThreads / 32);
+    const int64_t gw = (int64_t)blockIdx.x * (kScoreThreads / 32) + (threadIdx.x >> 5);
+    score_rows_loop<NV, R>(q_s, pooled, n_rows, gw, nw, scale, scores, hist, n_hist);
+}
+
+// Decode step with the pooled-row update folded in: CTA i < n_pool recomputes row
+// row0 + i (pool -> RMS norm -> rotation), stores it and scores it from shared memory;
+// the other CTAs stream the rows [0, row0) that were already valid.
+template <int NV, typename T>
+__global__ void __launch_bounds__(kScoreThreads)
+score_pool_kernel(const float *__restrict__ q, float *__restrict__ pooled, float scale,
+                  float *__restrict__ scores, uint32_t *__restrict__ hist, int64_t n_hist,
+                  const T *__restrict__ raw, int64_t n_ctx, int H, int d,
+                  const float *__restrict__ w, float eps, int64_t row0, int n_pool,
+                  const RopeTable tab)
+{
+    __shared__ float4 q_s[NV * 32];
+    __shared__ __align__(16) float p_s[NV * 128];
+    __shared__ float cs[kRopeMaxHalf], sn[kRopeMaxHalf];
+    pdl_wait();
+    pdl_trigger();
+    for (int i = threadIdx.x; i < NV * 32; i += blockDim.x)
+        q_s[i] = reinterpret_cast<const float4 *>(q)[i];
+    __syncthreads();
+    if ((int)blockIdx.x < n_pool) {
+        const int64_t b = row0 + blockIdx.x;
+        pool_row(raw, n_ctx, H, d, w, eps, tab, b, p_s, cs, sn, pooled + b * (int64_t)(NV * 128));
+        if (threadIdx.x < 32) {
+            const float acc = score_row_smem<NV>(q_s, p_s);
+            if (threadIdx.x == 0) {
+                const float sc = acc * scale;
+                scores[b] = sc;
+                if (hist && b < n_hist) atomicAdd(&hist[score_key(sc) >> (32 - kTopkHistBits)], 1u);
+            }
+        }
+        return;
+    }
+    const int64_t nw = (int64_t)(gridDim.x - n_pool) * (kScoreThreads / 32);
+    const int64_t gw = (int64_t)(blockIdx.x - n_pool) * (kScoreThreads / 32) + (threadIdx.x >> 5);
+    score_rows_loop<NV, (NV <= 8 ? 2 : 1)>(q_s, pooled, row0, gw, nw, scale, scores, hist, n_hist);
 }
 
 // General case: scores[i][b] = scale * <q_i, pooled_b>, 64 queries x 64 rows per CTA,
@@ -152,7 +216,59 @@ cudaError_t launch_rows(const float *q, const float *pooled, int64_t n_rows, flo
                   scale, scores, hist, n_hist);
 }
 
+template <int NV, typename T>
+cudaError_t launch_fused(const float *q, const float *pooled, int64_t n_rows, int H, int d,
+                         float scale, float *scores, uint32_t *hist, int64_t n_hist,
+                         const PoolFuse &pf, double rope_base, cudaStream_t st)
+{
+    static int blocks_per_sm = 0;
+    auto k = score_pool_kernel<NV, T>;
+    if (blocks_per_sm == 0) {
+        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks_per_sm, k,
+                                                                      kScoreThreads, 0);
+        if (e != cudaSuccess) return e;
+        if (blocks_per_sm < 1) blocks_per_sm = 1;
+    }
+    thread_local RopeTable tab;
+    thread_local int tab_d = -1;
+    thread_local double tab_base = 0.0;
+    if (tab_d != d || tab_base != rope_base) {
+        make_rope_table(&tab, d, rope_base);
+        tab_d = d;
+        tab_base = rope_base;
+    }
+    const int n_pool = (int)(pf.row1 - pf.row0);
+    int64_t grid = (int64_t)device_sm_count() * blocks_per_sm;
+    const int64_t warps_needed = pf.row0;
+    const int64_t grid_needed = n_pool + (warps_needed + kScoreThreads / 32 - 1) / (kScoreThreads / 32);
+    if (grid > grid_needed) grid = grid_needed;
+    if (grid < n_pool + 1) grid = n_pool + 1;
+    (void)n_rows;
+    return launch(k, dim3((unsigned)grid), dim3(kScoreThreads), 0, st, 1, q, (float *)pooled,
+                  scale, scores, hist, n_hist, (const T *)pf.raw, pf.n_ctx, H, d, pf.w, pf.eps,
+                  pf.row0, n_pool, tab);
+}
+
 }  // namespace
+
+cudaError_t launch_score_pool_fused(const float *q, const float *pooled, int64_t n_rows, int H,
+                                    int d, float scale, float *scores, uint32_t *hist,
+                                    int64_t n_hist, const PoolFuse &pf, double rope_base,
+                                    cudaStream_t st)
+{
+    const int hd = H * d;
+    const int64_t n_pool = pf.row1 - pf.row0;
+    const bool aligned = (reinterpret_cast<uintptr_t>(q) % 16 == 0) &&
+                         (reinterpret_cast<uintptr_t>(pooled) % 16 == 0);
+    if (!aligned || hd != 2048 || d / 2 > kRopeMaxHalf || n_pool < 0 || n_pool > kMaxFusedPoolRows ||
+        pf.row1 != n_rows)
+        return cudaErrorNotSupported;
+    if (pf.dt == QSA_BF16)
+        return launch_fused<16, __nv_bfloat16>(q, pooled, n_rows, H, d, scale, scores, hist,
+                                               n_hist, pf, rope_base, st);
+    return launch_fused<16, float>(q, pooled, n_rows, H, d, scale, scores, hist, n_hist, pf,
+                                   rope_base, st);
+}
 
 cudaError_t launch_index_score(const float *q, int64_t n_q, int64_t ld_q, const int32_t *q_pos,
                                const float *pooled, int64_t n_rows, int H, int d, float scale,

@@ -42,46 +42,8 @@ pool_update_kernel(const T *__restrict__ raw, int64_t n_ctx, int H, int d,
 
     const int64_t b = row0 + blockIdx.x;
     if (b >= row1) return;
-    const int64_t t0 = 4 * b;
-    const int c = (int)min((int64_t)4, n_ctx - t0);  // tokens present in this block (1..4)
-    const float inv_c = 1.0f / (float)c;
-    const T *rb = raw + t0 * hd;
-
-#pragma unroll 4
-    for (int e = threadIdx.x; e < hd; e += kPoolThreads) {
-        float v[4];
-#pragma unroll
-        for (int t = 0; t < 4; ++t) v[t] = t < c ? to_f32(rb[(int64_t)t * hd + e]) : 0.0f;
-        p_s[e] = ((v[0] + v[1]) + (v[2] + v[3])) * inv_c;
-    }
-    for (int i = threadIdx.x; i < half; i += kPoolThreads) {
-        const double phi = (4.0 * (double)b) * tab.theta[i];
-        const double k = rint(phi * kInvTwoPi);
-        const float r = (float)fma(-k, kTwoPi, phi);
-        float sv, cv;
-        sincosf(r, &sv, &cv);
-        cos_s[i] = cv;
-        sin_s[i] = sv;
-    }
-    __syncthreads();
-
-    const int lane = threadIdx.x & 31;
-    const int warp = threadIdx.x >> 5;
-    const int nwarps = blockDim.x >> 5;
-    for (int h = warp; h < H; h += nwarps) {
-        const float *ph = p_s + h * d;
-        float ss = 0.0f;
-        for (int j = lane; j < d; j += 32) ss = fmaf(ph[j], ph[j], ss);
-        ss = warp_sum(ss);
-        const float inv = 1.0f / sqrtf(ss / (float)d + eps);
-        float *out = pooled + b * (int64_t)hd + (int64_t)h * d;
-        for (int i = lane; i < half; i += 32) {
-            const float ya = ph[i] * inv * w[i];
-            const float yb = ph[i + half] * inv * w[i + half];
-            out[i] = ya * cos_s[i] - yb * sin_s[i];
-            out[i + half] = ya * sin_s[i] + yb * cos_s[i];
-        }
-    }
+    pool_row(raw, n_ctx, H, d, w, eps, tab, b, p_s, cos_s, sin_s,
+             pooled + b * (int64_t)(H * d));
 }
 
 }  // namespace

@@ -105,6 +105,65 @@ constexpr double kTwoPi = 6.283185307179586;
 constexpr double kInvTwoPi = 0.15915494309189535;
 void make_rope_table(RopeTable *tab, int d, double base);
 
+// One pooled-key row b, computed by the whole CTA: mean of the block's present raw keys
+// -> per-head RMS norm -> rotation at position 4b.  The row ends up both in p_s (shared,
+// [H*d]) and in out_row (global).  cs / sn: shared [d/2] scratch.  Every element's
+// arithmetic is independent of the CTA size, so every kernel that calls this produces the
+// same bits.  Contains __syncthreads().
+template <typename T>
+__device__ __forceinline__ void pool_row(const T *__restrict__ raw, int64_t n_ctx, int H, int d,
+                                         const float *__restrict__ w, float eps,
+                                         const RopeTable &tab, int64_t b, float *p_s, float *cs,
+                                         float *sn, float *__restrict__ out_row)
+{
+    const int hd = H * d;
+    const int half = d / 2;
+    const int64_t t0 = 4 * b;
+    const int c = (int)min((int64_t)4, n_ctx - t0);  // tokens present in this block (1..4)
+    const float inv_c = 1.0f / (float)c;
+    const T *rb = raw + t0 * hd;
+#pragma unroll 4
+    for (int e = threadIdx.x; e < hd; e += blockDim.x) {
+        float v[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) v[t] = t < c ? to_f32(rb[(int64_t)t * hd + e]) : 0.0f;
+        p_s[e] = ((v[0] + v[1]) + (v[2] + v[3])) * inv_c;
+    }
+    for (int i = threadIdx.x; i < half; i += blockDim.x) {
+        // the angle 4b * theta_i, formed and reduced modulo 2 pi in fp64; fp32 sincos of
+        // the reduced angle (|r| <= pi)
+        const double phi = (4.0 * (double)b) * tab.theta[i];
+        const double k = rint(phi * kInvTwoPi);
+        const float r = (float)fma(-k, kTwoPi, phi);
+        float sv, cv;
+        sincosf(r, &sv, &cv);
+        cs[i] = cv;
+        sn[i] = sv;
+    }
+    __syncthreads();
+    const int lane = threadIdx.x & 31;
+    const int nwarps = blockDim.x >> 5;
+    for (int h = threadIdx.x >> 5; h < H; h += nwarps) {
+        float *ph = p_s + h * d;
+        float ss = 0.0f;
+        for (int j = lane; j < d; j += 32) ss = fmaf(ph[j], ph[j], ss);
+        ss = warp_sum(ss);
+        const float inv = 1.0f / sqrtf(ss / (float)d + eps);
+        float *o = out_row + (int64_t)h * d;
+        for (int i = lane; i < half; i += 32) {
+            const float ya = ph[i] * inv * w[i];
+            const float yb = ph[i + half] * inv * w[i + half];
+            const float za = ya * cs[i] - yb * sn[i];
+            const float zb = ya * sn[i] + yb * cs[i];
+            ph[i] = za;
+            ph[i + half] = zb;
+            o[i] = za;
+            o[i + half] = zb;
+        }
+    }
+    __syncthreads();
+}
+
 // ------------------------------------------------------------------ launchers
 // Host-side launchers, one per kernel family; arguments are already validated.
 
@@ -114,6 +173,23 @@ cudaError_t launch_pool_update(const void *raw_k, qsa_dtype dt, int64_t n_ctx, i
                                const float *norm_w, float eps, double rope_base,
                                float *pooled, int64_t row0, int64_t row1, uint32_t *zero_hist,
                                cudaStream_t st);
+
+// Pooled-row recomputation fused into the decode score kernel (rows [row0, row1)).
+struct PoolFuse {
+    const void *raw;
+    qsa_dtype dt;
+    int64_t n_ctx;
+    const float *w;
+    float eps;
+    int64_t row0, row1;
+};
+constexpr int kMaxFusedPoolRows = 4;
+// Decode score kernel with the pool update of rows [pf.row0, pf.row1) folded in, when the
+// shape allows it (returns cudaErrorNotSupported otherwise, without launching).
+cudaError_t launch_score_pool_fused(const float *q, const float *pooled, int64_t n_rows, int H,
+                                    int d, float scale, float *scores, uint32_t *hist,
+                                    int64_t n_hist, const PoolFuse &pf, double rope_base,
+                                    cudaStream_t st);
 
 // hist (nullable, decode only): also add each row b < n_hist to a histogram of the top
 // kTopkHistBits bits of its score key, for qsa_topk_blocks' first radix digit.

@@ -9,7 +9,8 @@
 // Scores become order-preserving 32-bit keys.  The k-th largest key T is found by radix
 // select in three digits (12 + 10 + 10 bits):
 //   1. a 4096-bin histogram of the top 12 bits -- either accumulated by the score kernel
-//      as it writes the scores (decode step, no extra pass) or built here from one read;
+//      as it writes the scores (decode step, no extra pass; this kernel clears it again)
+//      or built here from one read;
 //   2. one read of the scores classifies every candidate: above the threshold bucket
 //      (selected: a bit in a shared-memory bitmap), inside it (appended to a candidate
 //      list in shared memory), or below (dropped);
@@ -104,25 +105,48 @@ __device__ __forceinline__ void find_bucket(const uint32_t *h, int nb, uint32_t 
     __syncthreads();
 }
 
-// Apply f(key, index) to every score of the row (coalesced, 16-byte loads when aligned).
+// Apply f(key, index) to every score of the row.  Each thread first loads 8 16-byte
+// vectors (all in flight at once), then applies f to their 32 keys.
 template <typename F>
 __device__ __forceinline__ void for_each_key(const float *__restrict__ row, int64_t n, F f)
 {
+    constexpr int U = 8;
     if ((reinterpret_cast<uintptr_t>(row) & 15) == 0) {
         const int64_t n4 = n / 4;
         const float4 *r4 = reinterpret_cast<const float4 *>(row);
-#pragma unroll 4
-        for (int64_t i = threadIdx.x; i < n4; i += NT) {
-            const float4 v = r4[i];
-            f(score_key(v.x), 4 * i);
-            f(score_key(v.y), 4 * i + 1);
-            f(score_key(v.z), 4 * i + 2);
-            f(score_key(v.w), 4 * i + 3);
+        for (int64_t base = threadIdx.x; base < n4; base += (int64_t)NT * U) {
+            float4 v[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t i = base + (int64_t)u * NT;
+                v[u] = i < n4 ? r4[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t i = base + (int64_t)u * NT;
+                if (i < n4) {
+                    f(score_key(v[u].x), 4 * i);
+                    f(score_key(v[u].y), 4 * i + 1);
+                    f(score_key(v[u].z), 4 * i + 2);
+                    f(score_key(v[u].w), 4 * i + 3);
+                }
+            }
         }
         for (int64_t i = 4 * n4 + threadIdx.x; i < n; i += NT) f(score_key(row[i]), i);
     } else {
-#pragma unroll 4
-        for (int64_t i = threadIdx.x; i < n; i += NT) f(score_key(row[i]), i);
+        for (int64_t base = threadIdx.x; base < n; base += (int64_t)NT * U) {
+            float v[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t i = base + (int64_t)u * NT;
+                v[u] = i < n ? row[i] : 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t i = base + (int64_t)u * NT;
+                if (i < n) f(score_key(v[u]), i);
+            }
+        }
     }
 }
 
@@ -169,6 +193,8 @@ topk_kernel(const float *__restrict__ scores, int64_t ld, const int32_t *__restr
             out[i] = (int32_t)i;
             if (pout) put_cells(pout + 4 * i, (int32_t)i, pvec);
         }
+        if (ehist)  // leave the histogram cleared for the next step
+            for (int i = threadIdx.x; i < kBins1; i += NT) ehist[i] = 0u;
         return;
     }
     const int64_t nw = (n + 31) / 32;
@@ -177,16 +203,27 @@ topk_kernel(const float *__restrict__ scores, int64_t ld, const int32_t *__restr
     int32_t *cand_idx = reinterpret_cast<int32_t *>(cand_key + cand_cap);
     const float *srow = scores + qi * ld;
 
-    // ---- 1. histogram of the top 12 bits
+    // ---- 1. histogram of the top 12 bits: take the one the score kernel accumulated (and
+    // clear it for the next step) unless its total disagrees with the candidate count --
+    // a workspace that was never cleared -- in which case build it here
+    bool have = false;
     if (ehist) {
-        for (int i = threadIdx.x; i < kBins1; i += NT) hist[i] = ehist[i];
-    } else {
+        uint32_t part = 0;
+        for (int i = threadIdx.x; i < kBins1; i += NT) {
+            const uint32_t v = ehist[i];
+            hist[i] = v;
+            ehist[i] = 0u;
+            part += v;
+        }
+        uint32_t tot;
+        block_excl_scan(part, warp_s, &tot);
+        have = tot == (uint32_t)n;
+    }
+    if (!have) {
         for (int i = threadIdx.x; i < kBins1; i += NT) hist[i] = 0u;
         __syncthreads();
         for_each_key(srow, n, [&](uint32_t key, int64_t) {
-            const uint32_t bin = key >> (32 - kTopkHistBits);
-            const unsigned peers = __match_any_sync(__activemask(), bin);
-            if ((__ffs(peers) - 1) == (int)(threadIdx.x & 31)) atomicAdd(&hist[bin], __popc(peers));
+            atomicAdd(&hist[key >> (32 - kTopkHistBits)], 1u);
         });
     }
     for (int64_t i = threadIdx.x; i < 2 * nw; i += NT) selw[i] = 0u;
@@ -201,19 +238,14 @@ topk_kernel(const float *__restrict__ scores, int64_t ld, const int32_t *__restr
 
     // ---- 2. classify every candidate (one read)
     const uint32_t B1 = prefix;
+    const uint32_t lo_key = B1 << (32 - kTopkHistBits);  // smallest key with digit B1
     for_each_key(srow, n, [&](uint32_t key, int64_t i) {
+        if (key < lo_key) return;  // below the threshold bucket: the common case
         const uint32_t d = key >> (32 - kTopkHistBits);
-        const bool take = d > B1 || (whole && d == B1);
-        if (take) atomicOr(&selw[i >> 5], 1u << (i & 31));
-        const bool cand = !whole && d == B1;
-        const unsigned am = __activemask();
-        const unsigned cm = __ballot_sync(am, cand);
-        if (cand) {
-            const int leader = __ffs(cm) - 1;
-            uint32_t base = 0;
-            if ((int)(threadIdx.x & 31) == leader) base = atomicAdd(&misc[8], (uint32_t)__popc(cm));
-            base = __shfl_sync(cm, base, leader);
-            const uint32_t slot = base + __popc(cm & ((1u << (threadIdx.x & 31)) - 1u));
+        if (d > B1 || whole) {
+            atomicOr(&selw[i >> 5], 1u << (i & 31));
+        } else {
+            const uint32_t slot = atomicAdd(&misc[8], 1u);
             if (slot < (uint32_t)cand_cap) {
                 cand_key[slot] = key;
                 cand_idx[slot] = (int32_t)i;

@@ -39,7 +39,8 @@ class DecodeLayer:
         self.out = torch.zeros(1, H_q, d, dtype=f32, device=device)
         self.lse = torch.zeros(1, H_q, dtype=f32, device=device)
         ws = qb.decode_step_workspace_size(H_q, H_kv, d, self.max_cells)
-        self.workspace = torch.empty(max(ws // 4, 1), dtype=f32, device=device)
+        # zero-filled once: the step keeps its top-k histogram cleared from then on
+        self.workspace = torch.zeros(max(ws // 4, 1), dtype=f32, device=device)
         self.n_valid_full = 0
 
     def rebuild(self, raw_k, norm_w, n_ctx, stream=None):

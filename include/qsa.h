@@ -234,12 +234,15 @@ size_t qsa_sparse_attn_workspace_size(int64_t n_q, int H_q, int H_kv, int d_v,
  *                   n_cells, max_cells, out, lse_out, workspace, workspace_bytes)
  * with n_rows = ceil(n_ctx/4), n_full = floor(n_ctx/4).  scores holds >= n_rows floats,
  * blocks k_blk ints, pos max_cells ints.  Results are identical to those calls; the work
- * is fused differently: the score kernel also counts the top 12 bits of each full
- * block's score key into a histogram kept in the workspace (cleared by the pool-update
- * kernel at the start of every step), the top-k kernel starts from that histogram and
- * writes the cell list itself, and the attention kernel reads the listed K/V rows in
- * place.  workspace: qsa_decode_step_workspace_size() bytes, 256-byte aligned, contents
- * need no initialisation; steps that share a workspace must not overlap in time.
+ * is fused differently: when at most 4 pooled rows need recomputing (every decode step),
+ * the score kernel recomputes them itself; it also counts the top 12 bits of each full
+ * block's score key into a histogram kept in the workspace, which the top-k kernel
+ * starts from (and clears for the next step); the top-k kernel writes the cell list
+ * itself, and the attention kernel reads the listed K/V rows in place.
+ * workspace: qsa_decode_step_workspace_size() bytes, 256-byte aligned.  Its contents need
+ * no initialisation: a histogram whose total disagrees with the block count (a workspace
+ * never cleared) is rebuilt from the scores, which only makes that call slower; filling
+ * it with zeros once avoids that.  Steps that share a workspace must not overlap in time.
  * Returns the first failing validation status without enqueuing anything.
  */
 qsa_status qsa_decode_step(const void *raw_k, qsa_dtype raw_dtype, int64_t n_ctx, int H_idx,

@@ -346,3 +346,28 @@ def test_decode_step_composite_equals_separate_calls():
         nc = int(a.n_cells.item())
         assert torch.equal(a.pos[0, :nc], b.pos[0, :nc])
         assert torch.equal(oa, ob)
+
+
+def test_decode_step_with_uninitialised_workspace():
+    """A workspace holding garbage (never cleared) still gives the same results: the top-k
+    kernel notices that the histogram's total disagrees with the block count and rebuilds
+    it from the scores."""
+    shape = SMALL_BF16
+    inp = qsa_synth.decode_inputs(shape, seed=13, extra_tokens=2, n_steps=2)
+    raw, w = to_dev(inp["raw_k"]), to_dev(inp["norm_w"])
+    K, V = to_dev(inp["K"]), to_dev(inp["V"])
+    kw = dict(cap_tokens=shape.n_ctx + 2, H_idx=shape.H_idx, d_idx=shape.d_idx, H_q=shape.H_q,
+              H_kv=shape.H_kv, d=shape.d, top_k_tokens=shape.top_k_tokens)
+    a, b = qsa.DecodeLayer(**kw), qsa.DecodeLayer(**kw)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(5)
+    a.workspace.view(torch.int32).random_(0, 1 << 20, generator=g)
+    for lay in (a, b):
+        lay.rebuild(raw, w, shape.n_ctx - 1)
+    for s in range(2):
+        n_ctx = shape.n_ctx + s
+        oa = a.step(raw, w, K, V, n_ctx, to_dev(inp["q_idx"][s]), to_dev(inp["q"][s])).clone()
+        ob = b.step_separate_calls(raw, w, K, V, n_ctx, to_dev(inp["q_idx"][s]),
+                                   to_dev(inp["q"][s])).clone()
+        assert torch.equal(a.blocks, b.blocks)
+        assert torch.equal(oa, ob)

@@ -13,7 +13,7 @@ import torch
 
 import gather_qsa_pool_gb300 as qsa
 import qsa_synth
-from gpu_helpers import ATOL_ATTN_BF16, to_dev, to_host
+from gpu_helpers import ATOL_ATTN_BF16, ATOL_ATTN_F32, to_dev, to_host
 from oracle import oracle
 
 pytestmark = pytest.mark.gpu
@@ -37,14 +37,17 @@ def _cells(rng, n_ctx, k_blk, max_cells):
     return pos, np.array([cl.shape[0]], np.int32)
 
 
-def test_noalloc_matches_workspace_call_on_two_calls_in_a_row():
+def _compare_two_calls(dtype, H_q, H_kv, d, n_ctx, k_blk, tol):
     fn = _entry()
-    rng = np.random.default_rng(2024)
-    H_q, H_kv, d, n_ctx, k_blk = 32, 4, 128, 61789, 512
+    rng = np.random.default_rng(2024 + H_q)
     max_cells = 4 * k_blk + 3
     scale = 1.0 / math.sqrt(d)
-    K = to_dev(qsa_synth.to_bf16_bits(rng.standard_normal((n_ctx, H_kv, d)).astype(np.float32)))
-    V = to_dev(qsa_synth.to_bf16_bits(rng.standard_normal((n_ctx, H_kv, d)).astype(np.float32)))
+
+    def store(x):
+        return qsa_synth.to_bf16_bits(x) if dtype == "bf16" else x
+
+    K = to_dev(store(rng.standard_normal((n_ctx, H_kv, d)).astype(np.float32)))
+    V = to_dev(store(rng.standard_normal((n_ctx, H_kv, d)).astype(np.float32)))
     cases = []
     for _ in range(2):  # two different queries and cell lists
         pos, n = _cells(rng, n_ctx, k_blk, max_cells)
@@ -63,20 +66,31 @@ def test_noalloc_matches_workspace_call_on_two_calls_in_a_row():
         want.append((to_host(out), to_host(lse)))
     # the entry point under test, called twice in a row through the C ABI
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    dt = 1 if dtype == "bf16" else 0
     got = []
     for q, pos, n in cases:
         out = torch.full((1, H_q, d), float("nan"), device="cuda")
         lse = torch.full((1, H_q), float("nan"), device="cuda")
-        st = fn(q.data_ptr(), 1, H_q, H_kv, d, d, scale, K.data_ptr(), V.data_ptr(), 1, n_ctx,
+        st = fn(q.data_ptr(), 1, H_q, H_kv, d, d, scale, K.data_ptr(), V.data_ptr(), dt, n_ctx,
                 H_kv * d, H_kv * d, pos.data_ptr(), n.data_ptr(), max_cells, out.data_ptr(),
                 lse.data_ptr(), stream)
         assert st == 0, qsa.status_str(st)
         got.append((out, lse))
     torch.cuda.synchronize()
     for (o, l), (wo, wl) in zip(got, want):
-        np.testing.assert_allclose(to_host(o), wo, rtol=0, atol=ATOL_ATTN_BF16)
+        np.testing.assert_allclose(to_host(o), wo, rtol=0, atol=tol)
         np.testing.assert_allclose(to_host(l), wl, rtol=1e-5, atol=1e-5)
     assert not np.allclose(want[0][0], want[1][0])  # the two calls really differ
+
+
+def test_noalloc_matches_workspace_call_fp32_split_k():
+    """fp32 K/V, 4 query heads per KV head: the split-K partials go through the scratch."""
+    _compare_two_calls("f32", 8, 2, 128, 2050, 16, ATOL_ATTN_F32)
+
+
+def test_noalloc_matches_workspace_call_bf16_decode():
+    """The 61,789-token decode shape (32 / 4 heads, 2,051 cells)."""
+    _compare_two_calls("bf16", 32, 4, 128, 61789, 512, ATOL_ATTN_BF16)
 
 
 def test_noalloc_rejects_shapes_beyond_its_scratch():
