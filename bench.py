@@ -49,6 +49,8 @@ def parse_args():
     ap.add_argument("--primary", default="256k")
     ap.add_argument("--layers", type=int, default=12)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--prefill-reps", type=int, default=5)
     return ap.parse_args()
 
 
@@ -313,6 +315,76 @@ def run_context(name, args, world, rank, local, want_clocks):
     return res
 
 
+def run_prefill(args, local):
+    """The prefill chunk: 1024 queries after 255,181 tokens.  Times (CUDA events, after a
+    warm-up) the tensor-core score contraction, the per-query top-k, the cell lists and the
+    gathered attention; returns per-kernel microseconds and the score kernel's TFLOP/s."""
+    import torch
+
+    import gather_qsa_pool_gb300 as qsa
+    import qsa_synth
+
+    shape = qsa_synth.CONFIGS["prefill_256k"]
+    dev = torch.device("cuda", local)
+    inp = qsa_synth.prefill_inputs_torch(shape, seed=4242, device=dev)
+    H, d, n_q, n_rows = shape.H_idx, shape.d_idx, shape.n_q, shape.n_rows
+    pooled = torch.zeros(n_rows, H * d, device=dev)
+    qsa.pool_update(inp["raw_k"], shape.n_ctx, H, d, inp["norm_w"], shape.eps, shape.rope_base,
+                    pooled, 0)
+    scores = torch.empty(n_q, n_rows, device=dev)
+    ws = torch.zeros(qsa.index_score_workspace_size(n_q, n_rows, H, d, qsa.QSA_PREC_BF16_TC),
+                     dtype=torch.uint8, device=dev)
+    blocks = torch.empty(n_q, shape.k_blk, dtype=torch.int32, device=dev)
+    counts = torch.empty(n_q, dtype=torch.int32, device=dev)
+    pos = torch.empty(n_q, shape.max_cells, dtype=torch.int32, device=dev)
+    n_cells = torch.empty(n_q, dtype=torch.int32, device=dev)
+    out = torch.empty(n_q, shape.H_q, shape.d, device=dev)
+    aws = torch.empty(max(qsa.sparse_attn_workspace_size(n_q, shape.H_q, shape.H_kv, shape.d,
+                                                          shape.max_cells) // 4, 1), device=dev)
+    scale_idx, scale = 1.0 / math.sqrt(d), 1.0 / math.sqrt(shape.d)
+
+    calls = [
+        ("score_tc", lambda: qsa.index_score(inp["q_idx"], pooled, n_rows, H, d, scale_idx, scores,
+                                              q_pos=inp["q_pos"], precision=qsa.QSA_PREC_BF16_TC,
+                                              workspace=ws)),
+        ("topk", lambda: qsa.topk_blocks(scores, n_rows, shape.k_blk, blocks, counts,
+                                         q_pos=inp["q_pos"])),
+        ("cells", lambda: qsa.gather_kv(blocks, counts, shape.k_blk, pos, n_cells, shape.max_cells,
+                                        q_pos=inp["q_pos"], n_kv=shape.n_ctx)),
+        ("attn", lambda: qsa.sparse_attn(inp["q"], inp["K"], inp["V"], n_cells, shape.max_cells,
+                                         out, shape.H_kv, shape.d, shape.d, scale, pos=pos,
+                                         workspace=aws)),
+    ]
+    for _ in range(2):
+        for _, fn in calls:
+            fn()
+    torch.cuda.synchronize()
+    res = {}
+    for name, fn in calls:
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(args.prefill_reps):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        res[name] = a.elapsed_time(b) * 1e3 / args.prefill_reps
+    flops = 2.0 * n_q * n_rows * H * d
+    attn_flops = 2.0 * 2.0 * n_q * shape.H_q * shape.d * float(n_cells.float().mean().item())
+    out_d = {
+        "workload": (f"prefill chunk: {n_q} queries at positions {shape.depth:,}..{shape.n_ctx - 1:,}, "
+                     f"indexer {H}x{d}, top-k {shape.top_k_tokens}, attention {shape.H_q}/"
+                     f"{shape.H_kv}x{shape.d} bf16"),
+        "us": {k: round(v, 1) for k, v in res.items()},
+        "chunk_us": round(sum(res.values()), 1),
+        "score_tc_tflops": flops / (res["score_tc"] * 1e-6) / 1e12,
+        "attn_tflops": attn_flops / (res["attn"] * 1e-6) / 1e12,
+        "tokens_per_s": n_q / (sum(res.values()) * 1e-6),
+    }
+    del inp, pooled, scores, ws, pos, out, aws
+    torch.cuda.empty_cache()
+    return out_d
+
+
 def algorithmic_bytes(shape, n_rows, n_cells):
     """Pooled-cache scan (fp32) + the selected K/V rows (bf16), per decode step."""
     esize = 2 if shape.dtype == "bf16" else 4
@@ -431,6 +503,8 @@ def main():
     achieved = score_bytes / (r["score_us"] * 1e-6) / 1e9
     traffic = traffic_per_launch(int(r["score_rows"]))
 
+    prefill = None if args.no_prefill else run_prefill(args, local)
+
     cpu_baseline = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         n_done, t = oracle_decode_sample(sh, n_steps=40, budget_s=20.0)
@@ -456,6 +530,7 @@ def main():
         "gpu_launches": r["K"] * 6,
         "clocks": r["clocks"],
         "sweep": sweep,
+        "prefill": prefill,
         "cpu_baseline": cpu_baseline,
     }
     if rank == 0:

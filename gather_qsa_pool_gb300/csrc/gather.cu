@@ -73,6 +73,35 @@ gather_kernel(const char *__restrict__ K, const char *__restrict__ V, int esize,
     (void)esize;
 }
 
+// Index-only form (no row copies): one thread per output cell.
+__global__ void __launch_bounds__(256)
+cells_kernel(int64_t n_kv, const int32_t *__restrict__ blocks, const int32_t *__restrict__ counts,
+             int64_t k_blk, const int32_t *__restrict__ q_pos, int64_t n_ctx,
+             int32_t *__restrict__ pos_out, int32_t *__restrict__ n_cells_out, int64_t max_cells)
+{
+    pdl_wait();
+    pdl_trigger();
+    const int64_t qi = blockIdx.y;
+    const int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t p = q_pos ? (int64_t)q_pos[qi] : n_ctx - 1;
+    const int64_t tail0 = 4 * ((p + 1) / 4);
+    int64_t cnt = counts[qi];
+    if (cnt < 0) cnt = 0;
+    if (cnt > k_blk) cnt = k_blk;
+    const int64_t n_cells = 4 * cnt + (p + 1 - tail0);
+    if (j == 0) n_cells_out[qi] = (int32_t)n_cells;
+    if (j >= n_cells) return;
+    int64_t cell;
+    if (j < 4 * cnt) {
+        const int64_t b = blocks[qi * k_blk + j / 4];
+        cell = b >= 0 ? 4 * b + (j & 3) : -1;
+    } else {
+        cell = tail0 + (j - 4 * cnt);
+    }
+    if (cell >= n_kv) cell = -1;
+    pos_out[qi * max_cells + j] = (int32_t)cell;
+}
+
 }  // namespace
 
 cudaError_t launch_gather(const void *K, const void *V, qsa_dtype dt, int64_t n_kv, int H_kv,
@@ -83,6 +112,11 @@ cudaError_t launch_gather(const void *K, const void *V, qsa_dtype dt, int64_t n_
                           cudaStream_t st)
 {
     if (n_q == 0) return cudaSuccess;
+    if (!K_out && !V_out) {
+        const dim3 grid((unsigned)((max_cells + 255) / 256), (unsigned)n_q);
+        return launch(cells_kernel, grid, dim3(256), 0, st, 1, n_kv, blocks, counts, k_blk, q_pos,
+                      n_ctx, pos_out, n_cells_out, max_cells);
+    }
     const int esize = dt == QSA_BF16 ? 2 : 4;
     const int warps = 8;
     const dim3 grid((unsigned)((max_cells + warps - 1) / warps), (unsigned)n_q);

@@ -10,7 +10,8 @@ import torch
 import gather_qsa_pool_gb300 as qsa
 import qsa_synth
 from oracle import oracle
-from gpu_helpers import ATOL_ATTN_BF16, ATOL_ATTN_F32, check_topk, to_dev, to_host
+from gpu_helpers import (ATOL_ATTN_BF16, ATOL_ATTN_F32, check_topk, score_tolerance, to_dev,
+                         to_host)
 
 pytestmark = pytest.mark.gpu
 
@@ -91,24 +92,64 @@ def _prefill_case(dtype, depth, n_q, k_tokens, seed):
     return shape, qsa_synth.prefill_inputs(shape, seed)
 
 
-@pytest.mark.parametrize("dtype,depth,n_q,k_tokens", [("f32", 3001, 64, 256),
-                                                      ("bf16", 700, 130, 1024)])
-def test_prefill_chunk_fp32_scores(dtype, depth, n_q, k_tokens):
+@pytest.mark.parametrize("H,d,depth,n_q", [(4, 64, 3001, 130), (16, 128, 10000, 600)])
+def test_prefill_scores_on_tensor_cores(H, d, depth, n_q):
+    """qsa_index_score with QSA_PREC_BF16_TC (tcgen05, bf16 operands, fp32 accumulation)
+    against the oracle with both operands rounded to bf16; rows a query cannot see are
+    -inf.  Shapes cover partial query and row tiles."""
+    shape = qsa_synth.PrefillShape("tc", depth, n_q, H, d, 8, 2, 128, 256, dtype="bf16")
+    inp = qsa_synth.prefill_inputs(shape, seed=31)
+    n_rows = shape.n_rows
+    o_pooled = oracle.pool_rows(inp["raw_k"], shape.n_ctx, H, d, inp["norm_w"], shape.eps,
+                                shape.rope_base, 0, n_rows)
+    scale = 1.0 / math.sqrt(d)
+    ws = torch.zeros(qsa.index_score_workspace_size(n_q, n_rows, H, d, qsa.QSA_PREC_BF16_TC),
+                     dtype=torch.uint8, device="cuda")
+    scores = torch.full((n_q, n_rows + 5), 7.0, device="cuda")
+    qsa.index_score(to_dev(inp["q_idx"]), to_dev(o_pooled), n_rows, H, d, scale, scores,
+                    q_pos=to_dev(inp["q_pos"]), precision=qsa.QSA_PREC_BF16_TC, workspace=ws)
+    got = to_host(scores)
+    assert np.all(got[:, n_rows:] == 7.0)
+    rows = np.arange(n_q) if n_q <= 130 else np.random.default_rng(3).choice(n_q, 48, replace=False)
+    want = oracle.scores(inp["q_idx"][rows], o_pooled, n_rows, H, d, scale,
+                         q_pos=inp["q_pos"][rows], round_bf16_operands=True)
+    qb = np.array([oracle.round_bf16(float(x)) for x in inp["q_idx"][rows].reshape(-1)],
+                  np.float32).reshape(len(rows), -1)
+    for j, i in enumerate(rows):
+        vis = np.isfinite(want[j])
+        assert np.array_equal(np.isneginf(got[i, :n_rows]), ~vis)
+        tol = score_tolerance(qb[j], o_pooled, n_rows, scale, chain=H * d)[vis]
+        assert np.all(np.abs(got[i, :n_rows][vis] - want[j][vis]) <= tol)
+
+
+@pytest.mark.parametrize("dtype,depth,n_q,k_tokens,prec", [("f32", 3001, 64, 256, "f32"),
+                                                           ("bf16", 700, 130, 1024, "f32"),
+                                                           ("bf16", 2900, 200, 512, "tc")])
+def test_prefill_chunk(dtype, depth, n_q, k_tokens, prec):
     shape, inp = _prefill_case(dtype, depth, n_q, k_tokens, seed=21)
+    tc = prec == "tc"
     H, d, n_ctx = shape.H_idx, shape.d_idx, shape.n_ctx
     n_rows, k_blk, max_cells = shape.n_rows, shape.k_blk, shape.max_cells
     scale_idx = 1.0 / math.sqrt(d)
     # oracle
     o_pooled = oracle.pool_rows(inp["raw_k"], n_ctx, H, d, inp["norm_w"], shape.eps,
                                 shape.rope_base, 0, n_rows)
-    o_scores = oracle.scores(inp["q_idx"], o_pooled, n_rows, H, d, scale_idx, q_pos=inp["q_pos"])
+    o_scores = oracle.scores(inp["q_idx"], o_pooled, n_rows, H, d, scale_idx, q_pos=inp["q_pos"],
+                             round_bf16_operands=tc)
     # GPU
     pooled = torch.zeros(n_rows, H * d, device="cuda")
     qsa.pool_update(to_dev(inp["raw_k"]), n_ctx, H, d, to_dev(inp["norm_w"]), shape.eps,
                     shape.rope_base, pooled, 0)
     q_pos = to_dev(inp["q_pos"])
     scores = torch.zeros(n_q, n_rows, device="cuda")
-    qsa.index_score(to_dev(inp["q_idx"]), pooled, n_rows, H, d, scale_idx, scores, q_pos=q_pos)
+    if tc:
+        ws = torch.zeros(qsa.index_score_workspace_size(n_q, n_rows, H, d, qsa.QSA_PREC_BF16_TC),
+                         dtype=torch.uint8, device="cuda")
+        qsa.index_score(to_dev(inp["q_idx"]), pooled, n_rows, H, d, scale_idx, scores,
+                        q_pos=q_pos, precision=qsa.QSA_PREC_BF16_TC, workspace=ws)
+    else:
+        qsa.index_score(to_dev(inp["q_idx"]), pooled, n_rows, H, d, scale_idx, scores,
+                        q_pos=q_pos)
     blocks = torch.zeros(n_q, k_blk, dtype=torch.int32, device="cuda")
     counts = torch.zeros(n_q, dtype=torch.int32, device="cuda")
     qsa.topk_blocks(scores, n_ctx // 4, k_blk, blocks, counts, q_pos=q_pos)
