@@ -44,7 +44,7 @@ _SIGNATURES = {
     "qsa_decode_step": (_int, [_p, _int, _i64, _int, _int, _p, _f, _d, _p, _i64, _i64, _p, _f,
                                _p, _i64, _p, _p, _p, _p, _int, _i64, _int, _int, _i64, _p, _p,
                                _i64, _p, _int, _f, _p, _p, _p, _sz, _p]),
-    "qsa_decode_step_workspace_size": (_sz, [_int, _int, _int, _i64]),
+    "qsa_decode_step_workspace_size": (_sz, [_int, _int, _int, _i64, _i64]),
     "qsa_mask_to_list": (_int, [_p, _i64, _i64, _i64, _i64, _p, _p, _p, _p]),
     "qsa_mask_sparse_eligible": (_int, [_int, _f, _f, _i64, _i64]),
 }
@@ -208,8 +208,8 @@ def decode_step(raw_k, n_ctx, H_idx, d_idx, norm_w, eps, rope_base, pooled, n_va
         _ptr(lse), _ptr(workspace), ws_bytes, _stream(stream)))
 
 
-def decode_step_workspace_size(H_q, H_kv, d, max_cells) -> int:
-    return int(load().qsa_decode_step_workspace_size(H_q, H_kv, d, max_cells))
+def decode_step_workspace_size(H_q, H_kv, d, max_cells, cap_rows) -> int:
+    return int(load().qsa_decode_step_workspace_size(H_q, H_kv, d, max_cells, cap_rows))
 
 
 def mask_to_list(mask, max_list, pos_out, counts_out, bits_out=None, n_kv=None, stream=None):

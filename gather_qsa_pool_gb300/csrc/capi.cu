@@ -243,10 +243,12 @@ qsa_status qsa_sparse_attn(const float *q, int64_t n_q, int H_q, int H_kv, int d
 
 static size_t align256(size_t b) { return (b + 255) & ~(size_t)255; }
 
-size_t qsa_decode_step_workspace_size(int H_q, int H_kv, int d, int64_t max_cells)
+size_t qsa_decode_step_workspace_size(int H_q, int H_kv, int d, int64_t max_cells,
+                                      int64_t cap_rows)
 {
-    if (H_q < 1 || H_kv < 1 || d < 1 || max_cells < 0 || H_q % H_kv) return 0;
-    return align256(attn_workspace_bytes(1, H_q, H_kv, d, max_cells)) + kTopkHistBytes;
+    if (H_q < 1 || H_kv < 1 || d < 1 || max_cells < 0 || H_q % H_kv || cap_rows < 0) return 0;
+    return align256(attn_workspace_bytes(1, H_q, H_kv, d, max_cells)) + kTopkHistBytes +
+           topk_pre_workspace_bytes(cap_rows);
 }
 
 qsa_status qsa_decode_step(const void *raw_k, qsa_dtype raw_dtype, int64_t n_ctx, int H_idx,
@@ -261,10 +263,20 @@ qsa_status qsa_decode_step(const void *raw_k, qsa_dtype raw_dtype, int64_t n_ctx
 {
     const int64_t n_rows = (n_ctx + 3) / 4;
     const int64_t n_full = n_ctx / 4;
-    const size_t need = qsa_decode_step_workspace_size(H_q, H_kv, d, max_cells);
+    const size_t need = qsa_decode_step_workspace_size(H_q, H_kv, d, max_cells, cap_rows);
     if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return QSA_ERR_INVALID_ARG;
     const size_t attn_bytes = align256(attn_workspace_bytes(1, H_q, H_kv, d, max_cells));
-    uint32_t *hist = reinterpret_cast<uint32_t *>(static_cast<char *>(workspace) + attn_bytes);
+    char *wsb = static_cast<char *>(workspace);
+    uint32_t *hist = reinterpret_cast<uint32_t *>(wsb + attn_bytes);
+    // top-k classify area: meta | per-CTA counts | per-CTA candidates | bitmap
+    const int64_t nw_cap = (cap_rows + 31) / 32;
+    const int64_t g_cap = (nw_cap + kClsWordsPerCta - 1) / kClsWordsPerCta;
+    char *pre_base = wsb + attn_bytes + kTopkHistBytes;
+    uint32_t *meta = reinterpret_cast<uint32_t *>(pre_base);
+    int32_t *cand_cnt = reinterpret_cast<int32_t *>(pre_base + 256);
+    uint2 *cand = reinterpret_cast<uint2 *>(pre_base + 256 + align256(4 * g_cap));
+    uint32_t *bitmap = reinterpret_cast<uint32_t *>(pre_base + 256 + align256(4 * g_cap) +
+                                                    align256(8 * g_cap * kClsCap));
     qsa_status v = check_pool_update(raw_k, raw_dtype, n_ctx, H_idx, d_idx, norm_w, eps,
                                      rope_base, pooled, cap_rows, n_valid_full);
     if (v == QSA_OK)
@@ -300,10 +312,16 @@ qsa_status qsa_decode_step(const void *raw_k, qsa_dtype raw_dtype, int64_t n_ctx
             e = launch_index_score(q_idx, 1, (int64_t)H_idx * d_idx, nullptr, pooled, n_rows,
                                    H_idx, d_idx, scale_idx, scores, n_rows, hist, n_full, st);
     }
-    // 3. top-k from that histogram; its epilogue writes the cell list (qsa_gather_kv's job)
+    // 3. top-k from that histogram: a many-CTA classify pass, then the one-CTA resolve pass,
+    // whose epilogue writes the cell list (qsa_gather_kv's job)
+    TopkPre pre;
+    if (e == cudaSuccess) {
+        e = launch_topk_classify(scores, n_full, k_blk, hist, meta, bitmap, cand, cand_cnt, &pre, st);
+        if (e == cudaErrorNotSupported) e = cudaSuccess;  // the resolve pass does it all
+    }
     if (e == cudaSuccess)
         e = launch_topk(scores, 1, n_rows, nullptr, n_full, k_blk, blocks, counts, n_ctx, pos,
-                        n_cells, max_cells, hist, st);
+                        n_cells, max_cells, hist, st, pre);
     // 4. attention over the listed cells, read in place from the cache
     if (e == cudaSuccess)
         e = launch_sparse_attn(q, 1, H_q, H_kv, d, d, scale, K, V, kv_dtype, n_kv, ld_kv, ld_kv,

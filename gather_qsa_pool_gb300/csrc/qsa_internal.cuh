@@ -218,12 +218,33 @@ constexpr int kTopkThreads = 1024;
 constexpr int kTopkHistBits = 12;  // first radix digit: histogram of key >> 20
 constexpr size_t kTopkHistBytes = sizeof(uint32_t) << kTopkHistBits;
 int64_t topk_max_candidates();
+// Decode top-k split in two: a many-CTA classify pass (threshold digit from the score
+// kernel's histogram; above-threshold bitmap words; threshold-bucket candidates in
+// per-CTA lists) feeding the one-CTA resolve pass.
+struct TopkPre {
+    const uint32_t *meta = nullptr;     // [4]: digit, keys above it, whole-bucket flag, valid
+    const uint32_t *bitmap = nullptr;   // [ceil(n/32)] above-threshold blocks
+    const uint2 *cand = nullptr;        // [n_cta][cap] (key, block) of the threshold bucket
+    const int32_t *cand_cnt = nullptr;  // [n_cta] true counts
+    int n_cta = 0;
+    int cap = 0;
+};
+constexpr int kClsWordsPerCta = 32;   // bitmap words (x 32 blocks) per classify CTA
+constexpr int kClsCap = 128;          // candidates kept per classify CTA
+
 // pos_out / n_cells_out (nullable): also write each query's cell list -- the selected
 // blocks' 4 cells in order, then the open tail of the query (q_pos[i], or n_ctx - 1).
 cudaError_t launch_topk(const float *scores, int64_t n_q, int64_t ld, const int32_t *q_pos,
                         int64_t n_full, int64_t k_blk, int32_t *blocks_out, int32_t *counts_out,
                         int64_t n_ctx, int32_t *pos_out, int32_t *n_cells_out,
-                        int64_t max_cells, uint32_t *ext_hist, cudaStream_t st);
+                        int64_t max_cells, uint32_t *ext_hist, cudaStream_t st,
+                        const TopkPre &pre = TopkPre());
+// The classify pass for one query (decode); returns cudaErrorNotSupported when the shape
+// does not take it (then the resolve pass runs its own full path).
+cudaError_t launch_topk_classify(const float *scores, int64_t n_full, int64_t k_blk,
+                                 const uint32_t *hist, uint32_t *meta, uint32_t *bitmap,
+                                 uint2 *cand, int32_t *cand_cnt, TopkPre *pre, cudaStream_t st);
+size_t topk_pre_workspace_bytes(int64_t n_full_cap);
 
 cudaError_t launch_gather(const void *K, const void *V, qsa_dtype dt, int64_t n_kv, int H_kv,
                           int d_k, int d_v, int64_t ld_k, int64_t ld_v, const int32_t *blocks,

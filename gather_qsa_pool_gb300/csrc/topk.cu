@@ -155,7 +155,7 @@ topk_kernel(const float *__restrict__ scores, int64_t ld, const int32_t *__restr
             int64_t n_full_cap, int k_blk, int32_t *__restrict__ blocks_out,
             int32_t *__restrict__ counts_out, int64_t n_ctx, int32_t *__restrict__ pos_out,
             int32_t *__restrict__ n_cells_out, int64_t max_cells, uint32_t *__restrict__ ext_hist,
-            int cand_cap)
+            int cand_cap, const TopkPre pre)
 {
     extern __shared__ __align__(16) uint32_t smem[];
     uint32_t *hist = smem;                      // [4096]
@@ -203,56 +203,94 @@ topk_kernel(const float *__restrict__ scores, int64_t ld, const int32_t *__restr
     int32_t *cand_idx = reinterpret_cast<int32_t *>(cand_key + cand_cap);
     const float *srow = scores + qi * ld;
 
-    // ---- 1. histogram of the top 12 bits: take the one the score kernel accumulated (and
-    // clear it for the next step) unless its total disagrees with the candidate count --
-    // a workspace that was never cleared -- in which case build it here
-    bool have = false;
-    if (ehist) {
-        uint32_t part = 0;
-        for (int i = threadIdx.x; i < kBins1; i += NT) {
-            const uint32_t v = ehist[i];
-            hist[i] = v;
-            ehist[i] = 0u;
-            part += v;
-        }
-        uint32_t tot;
-        block_excl_scan(part, warp_s, &tot);
-        have = tot == (uint32_t)n;
-    }
-    if (!have) {
-        for (int i = threadIdx.x; i < kBins1; i += NT) hist[i] = 0u;
-        __syncthreads();
-        for_each_key(srow, n, [&](uint32_t key, int64_t) {
-            atomicAdd(&hist[key >> (32 - kTopkHistBits)], 1u);
-        });
-    }
-    for (int64_t i = threadIdx.x; i < 2 * nw; i += NT) selw[i] = 0u;
-    if (threadIdx.x == 0) misc[8] = 0u;  // candidate count
-    __syncthreads();
-    find_bucket(hist, kBins1, (uint32_t)k, warp_s, misc);
-    uint32_t prefix = misc[0];
+    uint32_t prefix = 0, k_rem = 0;
     int fixed = kTopkHistBits;
-    uint32_t k_rem = (uint32_t)k - misc[1];
-    bool whole = misc[2] == k_rem;
-    __syncthreads();
-
-    // ---- 2. classify every candidate (one read)
-    const uint32_t B1 = prefix;
-    const uint32_t lo_key = B1 << (32 - kTopkHistBits);  // smallest key with digit B1
-    for_each_key(srow, n, [&](uint32_t key, int64_t i) {
-        if (key < lo_key) return;  // below the threshold bucket: the common case
-        const uint32_t d = key >> (32 - kTopkHistBits);
-        if (d > B1 || whole) {
-            atomicOr(&selw[i >> 5], 1u << (i & 31));
-        } else {
-            const uint32_t slot = atomicAdd(&misc[8], 1u);
-            if (slot < (uint32_t)cand_cap) {
-                cand_key[slot] = key;
-                cand_idx[slot] = (int32_t)i;
-            }
+    bool whole = false;
+    bool pre_ok = false;
+    if (pre.meta) {
+        // ---- 1-2 done by the classify pass: take its decision, bitmap and candidates
+        const int c = threadIdx.x;
+        uint32_t my = 0;
+        bool over = false;
+        if (c < pre.n_cta) {
+            my = (uint32_t)pre.cand_cnt[c];
+            over = my > (uint32_t)pre.cap;
         }
-    });
-    __syncthreads();
+        const bool any_over = __syncthreads_or(over);
+        uint32_t n_cand;
+        const uint32_t cbase = block_excl_scan(my, warp_s, &n_cand);
+        pre_ok = pre.meta[3] != 0 && !any_over && n_cand <= (uint32_t)cand_cap;
+        if (pre_ok) {
+            prefix = pre.meta[0];
+            k_rem = (uint32_t)k - pre.meta[1];
+            whole = pre.meta[2] != 0;
+            for (int64_t w = threadIdx.x; w < nw; w += NT) {
+                selw[w] = pre.bitmap[w];
+                eqw[w] = 0u;
+            }
+            for (uint32_t j = 0; j < my; ++j) {
+                const uint2 e = pre.cand[(int64_t)c * pre.cap + j];
+                cand_key[cbase + j] = e.x;
+                cand_idx[cbase + j] = (int32_t)e.y;
+            }
+            if (threadIdx.x == 0) misc[8] = n_cand;
+        }
+        if (ehist)  // leave the histogram cleared for the next step
+            for (int i = threadIdx.x; i < kBins1; i += NT) ehist[i] = 0u;
+        __syncthreads();
+    }
+    if (!pre_ok) {
+        // ---- 1. histogram of the top 12 bits: take the one the score kernel accumulated
+        // (and clear it for the next step) unless its total disagrees with the candidate
+        // count -- a workspace that was never cleared -- in which case build it here
+        bool have = false;
+        if (ehist && !pre.meta) {
+            uint32_t part = 0;
+            for (int i = threadIdx.x; i < kBins1; i += NT) {
+                const uint32_t v = ehist[i];
+                hist[i] = v;
+                ehist[i] = 0u;
+                part += v;
+            }
+            uint32_t tot;
+            block_excl_scan(part, warp_s, &tot);
+            have = tot == (uint32_t)n;
+        }
+        if (!have) {
+            for (int i = threadIdx.x; i < kBins1; i += NT) hist[i] = 0u;
+            __syncthreads();
+            for_each_key(srow, n, [&](uint32_t key, int64_t) {
+                atomicAdd(&hist[key >> (32 - kTopkHistBits)], 1u);
+            });
+        }
+        for (int64_t i = threadIdx.x; i < 2 * nw; i += NT) selw[i] = 0u;
+        if (threadIdx.x == 0) misc[8] = 0u;  // candidate count
+        __syncthreads();
+        find_bucket(hist, kBins1, (uint32_t)k, warp_s, misc);
+        prefix = misc[0];
+        k_rem = (uint32_t)k - misc[1];
+        whole = misc[2] == k_rem;
+        __syncthreads();
+
+        // ---- 2. classify every candidate (one read)
+        const uint32_t B1c = prefix;
+        const uint32_t lo_key = B1c << (32 - kTopkHistBits);  // smallest key with digit B1
+        for_each_key(srow, n, [&](uint32_t key, int64_t i) {
+            if (key < lo_key) return;  // below the threshold bucket: the common case
+            const uint32_t d = key >> (32 - kTopkHistBits);
+            if (d > B1c || whole) {
+                atomicOr(&selw[i >> 5], 1u << (i & 31));
+            } else {
+                const uint32_t slot = atomicAdd(&misc[8], 1u);
+                if (slot < (uint32_t)cand_cap) {
+                    cand_key[slot] = key;
+                    cand_idx[slot] = (int32_t)i;
+                }
+            }
+        });
+        __syncthreads();
+    }
+    const uint32_t B1 = prefix;
 
     if (!whole) {
         const uint32_t n_cand = misc[8];
@@ -343,6 +381,69 @@ topk_kernel(const float *__restrict__ scores, int64_t ld, const int32_t *__restr
     }
 }
 
+// Classify pass (decode, one query): every CTA derives the threshold digit from the score
+// kernel's histogram, then one warp per bitmap word classifies 32 consecutive blocks with
+// two ballots -- the word of blocks above the threshold bucket is written as is, blocks
+// inside it are appended to this CTA's candidate list.  CTA 0 publishes the decision.
+__global__ void __launch_bounds__(NT)
+topk_classify_kernel(const float *__restrict__ scores, int64_t n, int64_t k,
+                     const uint32_t *__restrict__ hist, uint32_t *__restrict__ meta,
+                     uint32_t *__restrict__ bitmap, uint2 *__restrict__ cand,
+                     int32_t *__restrict__ cand_cnt, int cap)
+{
+    __shared__ uint32_t h[kBins1];
+    __shared__ uint32_t warp_s[2 * (NT / 32)];
+    __shared__ uint32_t misc[32];
+    pdl_wait();
+    pdl_trigger();
+    uint32_t part = 0;
+    for (int i = threadIdx.x; i < kBins1; i += NT) {
+        const uint32_t v = hist[i];
+        h[i] = v;
+        part += v;
+    }
+    uint32_t tot;
+    block_excl_scan(part, warp_s, &tot);
+    if (threadIdx.x == 0) misc[8] = 0u;
+    if (tot != (uint32_t)n) {  // not this step's histogram: the resolve pass does it all
+        if (blockIdx.x == 0 && threadIdx.x == 0) meta[3] = 0u;
+        return;
+    }
+    find_bucket(h, kBins1, (uint32_t)k, warp_s, misc);
+    const uint32_t B1 = misc[0];
+    const uint32_t above_n = misc[1];
+    const bool whole = misc[2] == (uint32_t)k - above_n;
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        meta[0] = B1;
+        meta[1] = above_n;
+        meta[2] = whole ? 1u : 0u;
+        meta[3] = 1u;
+    }
+    const int lane = threadIdx.x & 31;
+    const int64_t nw = (n + 31) / 32;
+    const int64_t wi = (int64_t)blockIdx.x * kClsWordsPerCta + (threadIdx.x >> 5);
+    if (wi < nw) {
+        const int64_t i = wi * 32 + lane;
+        const bool valid = i < n;
+        const uint32_t key = valid ? score_key(scores[i]) : 0u;
+        const uint32_t d = key >> (32 - kTopkHistBits);
+        const bool above = valid && (d > B1 || (whole && d == B1));
+        const bool is_cand = valid && !whole && d == B1;
+        const uint32_t word = __ballot_sync(0xffffffffu, above);
+        if (lane == 0) bitmap[wi] = word;
+        const uint32_t cm = __ballot_sync(0xffffffffu, is_cand);
+        uint32_t base = 0;
+        if (lane == 0 && cm) base = atomicAdd(&misc[8], (uint32_t)__popc(cm));
+        base = __shfl_sync(0xffffffffu, base, 0);
+        if (is_cand) {
+            const uint32_t slot = base + __popc(cm & ((1u << lane) - 1u));
+            if (slot < (uint32_t)cap) cand[(int64_t)blockIdx.x * cap + slot] = make_uint2(key, (uint32_t)i);
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) cand_cnt[blockIdx.x] = (int32_t)misc[8];
+}
+
 size_t topk_smem_bytes(int64_t n, int *cand_cap)
 {
     const int64_t nw = (n + 31) / 32;
@@ -358,10 +459,39 @@ size_t topk_smem_bytes(int64_t n, int *cand_cap)
 
 int64_t topk_max_candidates() { return kMaxN; }
 
+size_t topk_pre_workspace_bytes(int64_t n_full_cap)
+{
+    const int64_t nw = (n_full_cap + 31) / 32;
+    const int64_t g = (nw + kClsWordsPerCta - 1) / kClsWordsPerCta;
+    // meta (256 B) | counts | candidates | bitmap, each 256-byte aligned
+    auto al = [](int64_t b) { return (b + 255) & ~(int64_t)255; };
+    return (size_t)(256 + al(4 * g) + al(8 * g * kClsCap) + al(4 * nw));
+}
+
+cudaError_t launch_topk_classify(const float *scores, int64_t n_full, int64_t k_blk,
+                                 const uint32_t *hist, uint32_t *meta, uint32_t *bitmap,
+                                 uint2 *cand, int32_t *cand_cnt, TopkPre *pre, cudaStream_t st)
+{
+    const int64_t nw = (n_full + 31) / 32;
+    const int64_t g = (nw + kClsWordsPerCta - 1) / kClsWordsPerCta;
+    if (n_full <= k_blk || g < 1 || g > NT) return cudaErrorNotSupported;
+    cudaError_t e = launch(topk_classify_kernel, dim3((unsigned)g), dim3(NT), 0, st, 1, scores,
+                           n_full, k_blk, hist, meta, bitmap, cand, cand_cnt, kClsCap);
+    if (e != cudaSuccess) return e;
+    pre->meta = meta;
+    pre->bitmap = bitmap;
+    pre->cand = cand;
+    pre->cand_cnt = cand_cnt;
+    pre->n_cta = (int)g;
+    pre->cap = kClsCap;
+    return cudaSuccess;
+}
+
 cudaError_t launch_topk(const float *scores, int64_t n_q, int64_t ld, const int32_t *q_pos,
                         int64_t n_full, int64_t k_blk, int32_t *blocks_out, int32_t *counts_out,
                         int64_t n_ctx, int32_t *pos_out, int32_t *n_cells_out,
-                        int64_t max_cells, uint32_t *ext_hist, cudaStream_t st)
+                        int64_t max_cells, uint32_t *ext_hist, cudaStream_t st,
+                        const TopkPre &pre)
 {
     if (n_q == 0) return cudaSuccess;
     int cand_cap = 0;
@@ -375,7 +505,7 @@ cudaError_t launch_topk(const float *scores, int64_t n_q, int64_t ld, const int3
     }
     return launch(topk_kernel, dim3((unsigned)n_q), dim3(NT), smem, st, 1, scores, ld, q_pos,
                   n_full, (int)k_blk, blocks_out, counts_out, n_ctx, pos_out, n_cells_out,
-                  max_cells, ext_hist, cand_cap);
+                  max_cells, ext_hist, cand_cap, pre);
 }
 
 }  // namespace qsa

@@ -38,7 +38,7 @@ class DecodeLayer:
         self.n_cells = torch.zeros(1, dtype=i32, device=device)
         self.out = torch.zeros(1, H_q, d, dtype=f32, device=device)
         self.lse = torch.zeros(1, H_q, dtype=f32, device=device)
-        ws = qb.decode_step_workspace_size(H_q, H_kv, d, self.max_cells)
+        ws = qb.decode_step_workspace_size(H_q, H_kv, d, self.max_cells, self.cap_rows)
         # zero-filled once: the step keeps its top-k histogram cleared from then on
         self.workspace = torch.zeros(max(ws // 4, 1), dtype=f32, device=device)
         self.n_valid_full = 0

@@ -238,7 +238,9 @@ size_t qsa_sparse_attn_workspace_size(int64_t n_q, int H_q, int H_kv, int d_v,
  * the score kernel recomputes them itself; it also counts the top 12 bits of each full
  * block's score key into a histogram kept in the workspace, which the top-k kernel
  * starts from (and clears for the next step); the top-k kernel writes the cell list
- * itself, and the attention kernel reads the listed K/V rows in place.
+ * itself (a many-CTA classify pass over the scores, then one CTA that settles the
+ * threshold bucket and orders the output), and the attention kernel reads the listed K/V
+ * rows in place.
  * workspace: qsa_decode_step_workspace_size() bytes, 256-byte aligned.  Its contents need
  * no initialisation: a histogram whose total disagrees with the block count (a workspace
  * never cleared) is rebuilt from the scores, which only makes that call slower; filling
@@ -255,7 +257,9 @@ qsa_status qsa_decode_step(const void *raw_k, qsa_dtype raw_dtype, int64_t n_ctx
                            int H_q, float scale, float *out, float *lse_out, void *workspace,
                            size_t workspace_bytes, qsa_stream_t stream);
 
-size_t qsa_decode_step_workspace_size(int H_q, int H_kv, int d, int64_t max_cells);
+/* Workspace bytes of qsa_decode_step for a cache of up to cap_rows pooled rows. */
+size_t qsa_decode_step_workspace_size(int H_q, int H_kv, int d, int64_t max_cells,
+                                      int64_t cap_rows);
 
 /*
  * qsa_sparse_attn_noalloc -- qsa_sparse_attn for callers that cannot allocate device
