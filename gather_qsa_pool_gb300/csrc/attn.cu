@@ -559,7 +559,7 @@ attn_mma_kernel(const float *__restrict__ q, int H_q, int H_kv, float scale_log2
                 const __nv_bfloat16 *__restrict__ K, const __nv_bfloat16 *__restrict__ V,
                 int64_t n_kv, int64_t ld_k, int64_t ld_v, const int32_t *__restrict__ pos,
                 const int32_t *__restrict__ n_cells, int64_t max_cells, float *__restrict__ out,
-                float *__restrict__ lse)
+                float *__restrict__ lse, int early_q)
 {
     constexpr int G = 8, D = 128, TC = kMmaTC, LD = kMmaLd, NW = kMmaWarps, NT = 32 * NW;
     extern __shared__ __align__(16) char smem_raw[];
@@ -576,18 +576,9 @@ attn_mma_kernel(const float *__restrict__ q, int H_q, int H_kv, float scale_log2
     const int qc = (lane & 3) * 2;  // first column of this lane's fragment pairs
     const int mi = lane >> 3, mj = lane & 7;  // ldmatrix: matrix and row this lane addresses
 
-    pdl_wait();
-    pdl_trigger();
-
-    int64_t n = n_cells[qi];
-    const bool overflow = n > max_cells;  // truncated list: the result must not be used
-    if (overflow) n = 0;
-    if (n < 0) n = 0;
-    const int64_t chunk = (n + S - 1) / S;
-    const int64_t c0 = (int64_t)s_idx * chunk;
-    const int64_t c1 = c0 + chunk < n ? c0 + chunk : n;
-    const int ntiles = c1 > c0 ? (int)((c1 - c0 + TC - 1) / TC) : 0;
-
+    // Inside a decode step the preceding kernel only produces the cell list, so the query
+    // fragments are built before waiting on it (early_q); a standalone call waits first.
+    if (!early_q) pdl_wait();
     // A fragments of the query: rows 0-7 = hi, rows 8-15 = lo, for 8 k-steps of 16 dims
     uint32_t qa[8][4];
     {
@@ -611,6 +602,17 @@ attn_mma_kernel(const float *__restrict__ q, int H_q, int H_kv, float scale_log2
 #pragma unroll
     for (int j = 0; j < 16; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.0f;
     float m = -INFINITY, lsum = 0.0f;
+
+    if (early_q) pdl_wait();  // the cell list is complete from here on
+    pdl_trigger();
+    int64_t n = n_cells[qi];
+    const bool overflow = n > max_cells;  // truncated list: the result must not be used
+    if (overflow) n = 0;
+    if (n < 0) n = 0;
+    const int64_t chunk = (n + S - 1) / S;
+    const int64_t c0 = (int64_t)s_idx * chunk;
+    const int64_t c1 = c0 + chunk < n ? c0 + chunk : n;
+    const int ntiles = c1 > c0 ? (int)((c1 - c0 + TC - 1) / TC) : 0;
 
     auto issue = [&](int it, int buf) {
         const int64_t base = c0 + (int64_t)it * TC;
@@ -898,7 +900,7 @@ int attn_mma_splits(int64_t n_q, int H_kv, int64_t max_cells)
 cudaError_t launch_attn_mma(const float *q, int64_t n_q, int H_q, int H_kv, float scale,
                             const void *K, const void *V, int64_t n_kv, int64_t ld_k, int64_t ld_v,
                             const int32_t *pos, const int32_t *n_cells, int64_t max_cells,
-                            float *out, float *lse, cudaStream_t st)
+                            float *out, float *lse, cudaStream_t st, bool early_q)
 {
     const size_t smem = attn_mma_smem();
     static bool set = false;
@@ -915,7 +917,7 @@ cudaError_t launch_attn_mma(const float *q, int64_t n_q, int H_q, int H_kv, floa
     const dim3 grid((unsigned)S, (unsigned)H_kv, (unsigned)n_q);
     return launch(attn_mma_kernel, grid, dim3(32 * kMmaWarps), smem, st, S > 1 ? S : 1, q, H_q,
                   H_kv, scale * kLog2e, (const __nv_bfloat16 *)K, (const __nv_bfloat16 *)V, n_kv,
-                  ld_k, ld_v, pos, n_cells, max_cells, out, lse);
+                  ld_k, ld_v, pos, n_cells, max_cells, out, lse, early_q ? 1 : 0);
 }
 
 template <typename T, int G>
@@ -1004,14 +1006,14 @@ cudaError_t launch_sparse_attn(const float *q, int64_t n_q, int H_q, int H_kv, i
                                float scale, const void *K, const void *V, qsa_dtype dt,
                                int64_t n_kv, int64_t ld_k, int64_t ld_v, const int32_t *pos,
                                const int32_t *n_cells, int64_t max_cells, float *out,
-                               float *lse, float *partials, cudaStream_t st)
+                               float *lse, float *partials, cudaStream_t st, bool early_q)
 {
     if (n_q == 0) return cudaSuccess;
     const int S = attn_num_splits(n_q, H_kv, max_cells);
     const int G = H_q / H_kv;
     if (attn_uses_mma(dt, d_k, d_v, G))
         return launch_attn_mma(q, n_q, H_q, H_kv, scale, K, V, n_kv, ld_k, ld_v, pos, n_cells,
-                               max_cells, out, lse, st);
+                               max_cells, out, lse, st, early_q);
     if (d_k == 128 && d_v == 128 && G <= 8) {
 #define QSA_ATTN128_CASE(GG)                                                                   \
     case GG:                                                                                   \

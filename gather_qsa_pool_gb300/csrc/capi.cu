@@ -325,7 +325,8 @@ qsa_status qsa_decode_step(const void *raw_k, qsa_dtype raw_dtype, int64_t n_ctx
     // 4. attention over the listed cells, read in place from the cache
     if (e == cudaSuccess)
         e = launch_sparse_attn(q, 1, H_q, H_kv, d, d, scale, K, V, kv_dtype, n_kv, ld_kv, ld_kv,
-                               pos, n_cells, max_cells, out, lse_out, (float *)workspace, st);
+                               pos, n_cells, max_cells, out, lse_out, (float *)workspace, st,
+                               true);
     return from_cuda(e);
 }
 

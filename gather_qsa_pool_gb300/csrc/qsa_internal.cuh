@@ -46,11 +46,14 @@ __device__ __forceinline__ float warp_max(float v)
 }
 
 // ------------------------------------------------------------------ programmatic launch
-// Every kernel waits for the preceding grid in the stream before touching global memory
-// (a no-op when it was launched without the programmatic-serialisation attribute), then
-// lets its successor launch: the successor's CTAs become resident as this grid's CTAs
-// retire and block in their own wait until this grid has completed and flushed, which
-// hides the launch gap between the small kernels of a decode step.
+// Every kernel waits for the preceding grid in the stream before touching memory that grid
+// may write (a no-op when it was launched without the programmatic-serialisation
+// attribute), then lets its successor launch: the successor's CTAs become resident as this
+// grid's CTAs retire and block in their own wait until this grid has completed and
+// flushed, which hides the launch gap between the small kernels of a decode step.  Since
+// every kernel triggers only after its own wait, a running kernel knows that all grids
+// before its immediate predecessor have completed: inputs written before that
+// predecessor may be read before the wait.
 
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger()
@@ -260,7 +263,8 @@ cudaError_t launch_sparse_attn(const float *q, int64_t n_q, int H_q, int H_kv, i
                                float scale, const void *K, const void *V, qsa_dtype dt,
                                int64_t n_kv, int64_t ld_k, int64_t ld_v, const int32_t *pos,
                                const int32_t *n_cells, int64_t max_cells, float *out,
-                               float *lse, float *partials, cudaStream_t st);
+                               float *lse, float *partials, cudaStream_t st,
+                               bool early_q = false);  // q written before the predecessor
 
 cudaError_t launch_mask_to_list(const uint8_t *mask, int64_t n_rows, int64_t n_kv,
                                 int64_t ld_mask, int64_t max_list, int32_t *pos_out,

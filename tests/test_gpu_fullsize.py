@@ -1,0 +1,177 @@
+"""Full-size GPU parity in the launch configuration bench.py times (one decode step through
+qsa_decode_step at the pages' context lengths; the 1024-query prefill chunk at 255,181
+tokens), against the fp64 oracle on sampled outputs or in full where the oracle is fast
+enough, and against properties that hold at any size.  Inputs come from qsa_synth only."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import gather_qsa_pool_gb300 as qsa
+import qsa_synth
+from oracle import oracle
+from gpu_helpers import (ATOL_ATTN_BF16, check_topk, score_tolerance, to_dev, to_host)
+
+pytestmark = pytest.mark.gpu
+
+
+def _layer(shape, steps):
+    return qsa.DecodeLayer(cap_tokens=shape.n_ctx + steps, H_idx=shape.H_idx, d_idx=shape.d_idx,
+                           H_q=shape.H_q, H_kv=shape.H_kv, d=shape.d,
+                           top_k_tokens=shape.top_k_tokens, eps=shape.eps,
+                           rope_base=shape.rope_base)
+
+
+def test_decode_61789_tokens_full_oracle():
+    """Every pooled row, every score, the selection and the attention output of two
+    appending decode steps at 61,789 tokens against the oracle."""
+    shape = qsa_synth.CONFIGS["decode_64k"]
+    steps = 2
+    inp = qsa_synth.decode_inputs(shape, seed=61, extra_tokens=steps, n_steps=steps)
+    H, d = shape.H_idx, shape.d_idx
+    raw, w, K, V = (to_dev(inp["raw_k"]), to_dev(inp["norm_w"]), to_dev(inp["K"]),
+                    to_dev(inp["V"]))
+    lay = _layer(shape, steps)
+    n0 = shape.n_ctx - 1
+    lay.rebuild(raw, w, n0)
+    o_pooled = np.zeros((lay.cap_rows, H * d), np.float32)
+    oracle.pool_rows(inp["raw_k"], n0, H, d, inp["norm_w"], shape.eps, shape.rope_base, 0,
+                     (n0 + 3) // 4, o_pooled)
+    o_valid = n0 // 4
+    for s in range(steps):
+        n_ctx = n0 + 1 + s
+        out = lay.step(raw, w, K, V, n_ctx, to_dev(inp["q_idx"][s]), to_dev(inp["q"][s]))
+        blocks, cells, o_out, _, o_scores = oracle.decode_step(
+            inp["raw_k"], n_ctx, H, d, inp["norm_w"], shape.eps, shape.rope_base, o_pooled,
+            o_valid, inp["q_idx"][s], shape.top_k_tokens, inp["q"][s], inp["K"], inp["V"],
+            shape.H_q, shape.H_kv, shape.d)
+        o_valid = n_ctx // 4
+        n_rows = (n_ctx + 3) // 4
+        g_pooled = to_host(lay.pooled)[:n_rows]
+        np.testing.assert_allclose(g_pooled, o_pooled[:n_rows], rtol=2e-5,
+                                   atol=2e-6 * float(np.abs(o_pooled[:n_rows]).max()))
+        g_scores = to_host(lay.scores)[0, :n_rows]
+        tol = score_tolerance(inp["q_idx"][s], o_pooled, n_rows, 1.0 / math.sqrt(d))
+        assert np.all(np.abs(g_scores - o_scores) <= tol)
+        g_count = int(to_host(lay.counts)[0])
+        g_blocks = to_host(lay.blocks)[0]
+        n_band = check_topk(g_blocks, g_count, o_scores, n_ctx // 4, shape.k_blk)
+        if np.array_equal(g_blocks[:g_count], blocks):
+            nc = int(to_host(lay.n_cells)[0])
+            np.testing.assert_array_equal(to_host(lay.pos)[0, :nc], cells)
+            np.testing.assert_allclose(to_host(out)[0], o_out, rtol=0, atol=ATOL_ATTN_BF16)
+        else:
+            assert n_band > 0
+
+
+def test_decode_255181_tokens_sampled():
+    """One decode step at 255,181 tokens: sampled pooled rows (including the open row) and
+    their scores against the oracle; the selection is the exact top-k of the scores the GPU
+    produced (ties to the lower block); the cell list is the selected blocks' cells in
+    order followed by the open tail."""
+    shape = qsa_synth.CONFIGS["decode_256k"]
+    inp = qsa_synth.decode_inputs(shape, seed=256, extra_tokens=1, n_steps=1)
+    H, d = shape.H_idx, shape.d_idx
+    raw, w, K, V = (to_dev(inp["raw_k"]), to_dev(inp["norm_w"]), to_dev(inp["K"]),
+                    to_dev(inp["V"]))
+    lay = _layer(shape, 1)
+    n_ctx = shape.n_ctx
+    lay.rebuild(raw, w, n_ctx - 1)
+    lay.step(raw, w, K, V, n_ctx, to_dev(inp["q_idx"][0]), to_dev(inp["q"][0]))
+    n_rows, n_full = (n_ctx + 3) // 4, n_ctx // 4
+    rng = np.random.default_rng(7)
+    rows = np.concatenate([rng.choice(n_full, 14, replace=False), [n_full - 1, n_rows - 1]])
+    g_pooled = to_host(lay.pooled)
+    g_scores = to_host(lay.scores)[0, :n_rows].astype(np.float64)
+    for b in rows:
+        z = oracle.pool_row_f64(inp["raw_k"], n_ctx, H, d, inp["norm_w"], shape.eps,
+                                shape.rope_base, int(b)).astype(np.float32)
+        np.testing.assert_allclose(g_pooled[b], z, rtol=2e-5, atol=2e-6 * float(np.abs(z).max()))
+        s = oracle.scores(inp["q_idx"][0], z[None], 1, H, d, 1.0 / math.sqrt(d))[0, 0]
+        tol = score_tolerance(inp["q_idx"][0], z[None], 1, 1.0 / math.sqrt(d))[0]
+        assert abs(g_scores[b] - s) <= tol
+    k = shape.k_blk
+    order = np.lexsort((np.arange(n_full), -g_scores[:n_full]))
+    np.testing.assert_array_equal(to_host(lay.blocks)[0], np.sort(order[:k]))
+    assert int(to_host(lay.counts)[0]) == k
+    nc = int(to_host(lay.n_cells)[0])
+    assert nc == 4 * k + n_ctx % 4
+    cells = to_host(lay.pos)[0, :nc]
+    want = np.concatenate([(4 * np.sort(order[:k])[:, None] + np.arange(4)).reshape(-1),
+                           np.arange(4 * n_full, n_ctx)])
+    np.testing.assert_array_equal(cells, want)
+    assert np.all(np.isfinite(to_host(lay.out)))
+
+
+def test_topk_at_maximum_candidates():
+    n_full = qsa.topk_max_candidates()
+    k_blk = 512
+    rng = np.random.default_rng(640)
+    s = rng.standard_normal(n_full).astype(np.float32)
+    s[rng.choice(n_full, 5000, replace=False)] = s[rng.choice(n_full, 5000)]
+    blocks = torch.zeros((1, k_blk), dtype=torch.int32, device="cuda")
+    counts = torch.zeros(1, dtype=torch.int32, device="cuda")
+    qsa.topk_blocks(to_dev(s[None]), n_full, k_blk, blocks, counts)
+    want = oracle.topk(s.astype(np.float64), n_full, k_blk)
+    np.testing.assert_array_equal(to_host(blocks)[0], want)
+
+
+def test_prefill_chunk_1024_queries_at_255181_sampled():
+    """The 1024-query chunk after 255,181 tokens: tensor-core scores of sampled queries
+    against the oracle's bf16-operand scores, their selections under the tie band rule,
+    and their attention outputs whenever the selections agree."""
+    shape = qsa_synth.CONFIGS["prefill_256k"]
+    inp = qsa_synth.prefill_inputs(shape, seed=1024)
+    H, d, n_q, n_rows, n_ctx = shape.H_idx, shape.d_idx, shape.n_q, shape.n_rows, shape.n_ctx
+    pooled = torch.zeros(n_rows, H * d, device="cuda")
+    qsa.pool_update(to_dev(inp["raw_k"]), n_ctx, H, d, to_dev(inp["norm_w"]), shape.eps,
+                    shape.rope_base, pooled, 0)
+    q_pos = to_dev(inp["q_pos"])
+    scale_idx = 1.0 / math.sqrt(d)
+    scores = torch.empty(n_q, n_rows, device="cuda")
+    ws = torch.zeros(qsa.index_score_workspace_size(n_q, n_rows, H, d, qsa.QSA_PREC_BF16_TC),
+                     dtype=torch.uint8, device="cuda")
+    qsa.index_score(to_dev(inp["q_idx"]), pooled, n_rows, H, d, scale_idx, scores, q_pos=q_pos,
+                    precision=qsa.QSA_PREC_BF16_TC, workspace=ws)
+    blocks = torch.empty(n_q, shape.k_blk, dtype=torch.int32, device="cuda")
+    counts = torch.empty(n_q, dtype=torch.int32, device="cuda")
+    qsa.topk_blocks(scores, n_ctx // 4, shape.k_blk, blocks, counts, q_pos=q_pos)
+    pos = torch.empty(n_q, shape.max_cells, dtype=torch.int32, device="cuda")
+    n_cells = torch.empty(n_q, dtype=torch.int32, device="cuda")
+    qsa.gather_kv(blocks, counts, shape.k_blk, pos, n_cells, shape.max_cells, q_pos=q_pos,
+                  n_kv=n_ctx)
+    out = torch.empty(n_q, shape.H_q, shape.d, device="cuda")
+    aws = torch.empty(max(qsa.sparse_attn_workspace_size(n_q, shape.H_q, shape.H_kv, shape.d,
+                                                          shape.max_cells) // 4, 1),
+                      device="cuda")
+    qsa.sparse_attn(to_dev(inp["q"]), to_dev(inp["K"]), to_dev(inp["V"]), n_cells,
+                    shape.max_cells, out, shape.H_kv, shape.d, shape.d, 1.0 / math.sqrt(shape.d),
+                    pos=pos, workspace=aws)
+    g_scores, g_blocks, g_counts = to_host(scores), to_host(blocks), to_host(counts)
+    g_out, g_pos = to_host(out), to_host(pos)
+    # the oracle's own pooled cache and scores for a few queries (first, last, random)
+    o_pooled = oracle.pool_rows(inp["raw_k"], n_ctx, H, d, inp["norm_w"], shape.eps,
+                                shape.rope_base, 0, n_rows)
+    sample = np.array([0, 1, 511, 1022, 1023] + list(np.random.default_rng(5).choice(1024, 3)))
+    o_scores = oracle.scores(inp["q_idx"][sample], o_pooled, n_rows, H, d, scale_idx,
+                             q_pos=inp["q_pos"][sample], round_bf16_operands=True)
+    agree = 0
+    for j, i in enumerate(sample):
+        p = int(inp["q_pos"][i])
+        nf = (p + 1) // 4
+        vis = np.isfinite(o_scores[j])
+        assert np.array_equal(np.isneginf(g_scores[i]), ~vis)
+        n_band = check_topk(g_blocks[i], int(g_counts[i]), o_scores[j], nf, shape.k_blk)
+        w_blocks = oracle.topk(o_scores[j], nf, shape.k_blk)
+        if np.array_equal(g_blocks[i, :g_counts[i]], w_blocks):
+            cells = oracle.cells(w_blocks, p)
+            np.testing.assert_array_equal(g_pos[i, :cells.shape[0]], cells)
+            want, _ = oracle.attention(inp["q"][i], inp["K"], inp["V"], shape.H_q, shape.H_kv,
+                                       shape.d, shape.d, shape.H_kv * shape.d,
+                                       shape.H_kv * shape.d, cells, 1.0 / math.sqrt(shape.d))
+            np.testing.assert_allclose(g_out[i], want, rtol=0, atol=ATOL_ATTN_BF16)
+            agree += 1
+        else:
+            assert n_band > 0
+    assert agree >= len(sample) - 1
