@@ -37,6 +37,10 @@ METRIC = "sparse-attn decode steps/s at 64k/128k/256k ctx; achieved HBM GB/s vs 
 CONTEXTS = {"64k": "decode_64k", "128k": "decode_128k", "256k": "decode_256k"}
 SCORE_SRC = os.path.join(ROOT, "gather_qsa_pool_gb300", "csrc", "index_score.cu")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "score_rows_256k_traffic.txt")
+# Kernels one qsa_decode_step launches when it appends a token: the fused pool-update +
+# score scan, the top-k classify pass, the top-k resolve pass (which also writes the cell
+# list) and the attention kernel (split-K with the combine inside its cluster).
+LAUNCHES_PER_DECODE_STEP = 4
 
 
 def parse_args():
@@ -50,6 +54,7 @@ def parse_args():
     ap.add_argument("--layers", type=int, default=12)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-mask", action="store_true")
     ap.add_argument("--prefill-reps", type=int, default=5)
     return ap.parse_args()
 
@@ -250,6 +255,37 @@ def run_context(name, args, world, rank, local, want_clocks):
         clocks = sampler.summary(t_wall0, t_wall1)
     ms_max = max_over_ranks(ms, world)
 
+    # the same steps replayed from a CUDA graph (one captured step per layer set, context
+    # lengths fixed at capture): launch issue leaves the host
+    graph_us, graph_err = None, None
+    try:
+        gs = torch.cuda.Stream(device=dev)
+        gs.wait_stream(stream)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(gs):
+            with torch.cuda.graph(graph, stream=gs):
+                for li in range(L):
+                    layers[li].step_ptr(n_ctx[li], q_ptrs[li][0][0], q_ptrs[li][1][0],
+                                        gs.cuda_stream)
+            for li in range(L):
+                layers[li].n_valid_full = (n_ctx[li] - 1) // 4
+        torch.cuda.synchronize()
+        reps = max(3, K // L)
+        for _ in range(3):
+            graph.replay()
+        torch.cuda.synchronize()
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        g0.record(torch.cuda.current_stream())
+        for _ in range(reps):
+            graph.replay()
+        g1.record(torch.cuda.current_stream())
+        torch.cuda.synchronize()
+        graph_us = g0.elapsed_time(g1) * 1e3 / (reps * L)
+        del graph
+    except Exception as e:  # capture unsupported on this driver: report why
+        graph_err = f"{type(e).__name__}: {e}"[:200]
+        torch.cuda.synchronize()
+
     # score kernel alone, back to back over the rotating layers (its average duration)
     n_rows = [(c + 3) // 4 for c in n_ctx]
     for li in range(L):
@@ -309,6 +345,7 @@ def run_context(name, args, world, rank, local, want_clocks):
         "ms": ms_max, "K": K, "W": W, "score_us": score_us, "score_rows": score_rows,
         "t_e2e": t_e2e, "k_e2e": k_e2e, "host_issue_us": t_issue * 1e6 / K, "h2d": h2d, "d2h": d2h, "clocks": clocks,
         "n_cells": n_cells_last, "shape": shape, "n_ctx_end": max(n_ctx),
+        "graph_us": graph_us, "graph_err": graph_err,
     }
     del layers, caches
     torch.cuda.empty_cache()
@@ -381,6 +418,76 @@ def run_prefill(args, local):
         "tokens_per_s": n_q / (sum(res.values()) * 1e-6),
     }
     del inp, pooled, scores, ws, pos, out, aws
+    torch.cuda.empty_cache()
+    return out_d
+
+
+def run_mask(args, local):
+    """The mask-driven variant at 32,768 keys: mask -> position list (qsa_mask_to_list) and
+    attention of 16 query heads over the listed keys (DKQ 576, d_v 512, bf16).  Eight
+    rotating input sets (about 300 MB of K/V) keep consecutive calls out of L2.  Returns
+    microseconds per call and GB/s of the bytes each call must read."""
+    import torch
+
+    import gather_qsa_pool_gb300 as qsa
+    import qsa_synth
+
+    shape = qsa_synth.CONFIGS["mask_32k"]
+    dev = torch.device("cuda", local)
+    n_sets = 8
+    g = torch.Generator(device=dev)
+    g.manual_seed(32768)
+    sets = []
+    for i in range(n_sets):
+        m = torch.from_numpy(qsa_synth.mask_rows(shape.n_q, shape.n_kv, seed=100 + i)).to(dev)
+        KV = torch.randn(shape.n_kv, shape.d_k, device=dev, generator=g).to(torch.bfloat16)
+        q = torch.randn(shape.n_q, shape.H_q, shape.d_k, device=dev, generator=g)
+        sets.append((m, KV, q))
+    pos = torch.empty(shape.n_q, shape.max_list, dtype=torch.int32, device=dev)
+    counts = torch.empty(shape.n_q, dtype=torch.int32, device=dev)
+    out = torch.empty(shape.n_q, shape.H_q, shape.d_v, device=dev)
+    ws_n = qsa.sparse_attn_workspace_size(shape.n_q, shape.H_q, 1, shape.d_v, shape.max_list)
+    ws = torch.empty(max(ws_n // 4, 1), device=dev)
+    scale = 1.0 / math.sqrt(shape.d_k)
+
+    def to_list(i):
+        qsa.mask_to_list(sets[i % n_sets][0], shape.max_list, pos, counts)
+
+    def attend(i):
+        _, KV, q = sets[i % n_sets]
+        qsa.sparse_attn(q, KV, KV, counts, shape.max_list, out, 1, shape.d_k, shape.d_v, scale,
+                        pos=pos, workspace=ws, ld_k=shape.d_k, ld_v=shape.d_k)
+
+    reps = 8 * n_sets
+    res = {}
+    for name, fns in (("mask_to_list", (to_list,)), ("attn", (attend,)),
+                      ("both", (to_list, attend))):
+        for i in range(n_sets):
+            for fn in fns:
+                fn(i)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for i in range(reps):
+            for fn in fns:
+                fn(i)
+        b.record()
+        torch.cuda.synchronize()
+        res[name] = a.elapsed_time(b) * 1e3 / reps
+    n_listed = float(counts.float().mean().item())
+    mask_bytes = shape.n_q * shape.n_kv
+    kv_bytes = shape.n_q * n_listed * (shape.d_k + shape.d_v) * 2
+    out_d = {
+        "workload": (f"mask mode: {shape.n_q} query tokens x {shape.H_q} heads, {shape.n_kv:,} "
+                     f"keys, DKQ {shape.d_k} / d_v {shape.d_v} bf16, list of {shape.max_list}, "
+                     f"{n_sets} rotating input sets"),
+        "mean_listed": n_listed,
+        "us": {k: round(v, 2) for k, v in res.items()},
+        "mask_to_list_GBps": mask_bytes / (res["mask_to_list"] * 1e-6) / 1e9,
+        "attn_GBps": kv_bytes / (res["attn"] * 1e-6) / 1e9,
+        "algorithmic_bytes": {"mask": mask_bytes, "kv": kv_bytes},
+    }
+    del sets, pos, out, ws
     torch.cuda.empty_cache()
     return out_d
 
@@ -495,7 +602,10 @@ def main():
             "score_kernel_GBps": r["score_rows"] * sh.H_idx * sh.d_idx * 4 / r["score_us"] / 1e3,
             "e2e_steps_per_s": world * r["k_e2e"] / r["t_e2e"],
             "host_issue_us_per_step": r["host_issue_us"],
+            "graph_us_per_step": r["graph_us"],
         }
+        if r["graph_err"]:
+            sweep[name]["graph_err"] = r["graph_err"]
     r = results[args.primary]
     sh = r["shape"]
     value = sweep[args.primary]["steps_per_s"]
@@ -504,6 +614,7 @@ def main():
     traffic = traffic_per_launch(int(r["score_rows"]))
 
     prefill = None if args.no_prefill else run_prefill(args, local)
+    mask = None if args.no_mask else run_mask(args, local)
 
     cpu_baseline = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -527,10 +638,11 @@ def main():
                      if peak_kind == "measured" else "fallback 6.8 TB/s"},
         "e2e": {"value": sweep[args.primary]["e2e_steps_per_s"], "unit": "steps/s",
                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
-        "gpu_launches": r["K"] * 6,
+        "gpu_launches": r["K"] * LAUNCHES_PER_DECODE_STEP,
         "clocks": r["clocks"],
         "sweep": sweep,
         "prefill": prefill,
+        "mask": mask,
         "cpu_baseline": cpu_baseline,
     }
     if rank == 0:

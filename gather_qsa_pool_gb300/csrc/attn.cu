@@ -109,6 +109,11 @@ sparse_attn_kernel(const float *__restrict__ q, int H_q, int H_kv, int d_k, int 
     AttnSmem sm = carve(smem_raw, G, d_k, d_v, (int)sizeof(T));
 
     pdl_wait();
+    QSA_AFTER_WAIT(q);
+    QSA_AFTER_WAIT(K);
+    QSA_AFTER_WAIT(V);
+    QSA_AFTER_WAIT(pos);
+    QSA_AFTER_WAIT(n_cells);
     pdl_trigger();
 
     int64_t n = n_cells[qi];
@@ -311,6 +316,11 @@ attn128_kernel(const float *__restrict__ q, int H_q, int H_kv, float scale_log2,
     const int hl = lane / LPH, sl = lane % LPH;
 
     pdl_wait();
+    QSA_AFTER_WAIT(q);
+    QSA_AFTER_WAIT(K);
+    QSA_AFTER_WAIT(V);
+    QSA_AFTER_WAIT(pos);
+    QSA_AFTER_WAIT(n_cells);
     pdl_trigger();
 
     int64_t n = n_cells[qi];
@@ -578,7 +588,10 @@ attn_mma_kernel(const float *__restrict__ q, int H_q, int H_kv, float scale_log2
 
     // Inside a decode step the preceding kernel only produces the cell list, so the query
     // fragments are built before waiting on it (early_q); a standalone call waits first.
-    if (!early_q) pdl_wait();
+    if (!early_q) {
+        pdl_wait();
+        QSA_AFTER_WAIT(q);
+    }
     // A fragments of the query: rows 0-7 = hi, rows 8-15 = lo, for 8 k-steps of 16 dims
     uint32_t qa[8][4];
     {
@@ -604,6 +617,10 @@ attn_mma_kernel(const float *__restrict__ q, int H_q, int H_kv, float scale_log2
     float m = -INFINITY, lsum = 0.0f;
 
     if (early_q) pdl_wait();  // the cell list is complete from here on
+    QSA_AFTER_WAIT(pos);
+    QSA_AFTER_WAIT(n_cells);
+    QSA_AFTER_WAIT(K);
+    QSA_AFTER_WAIT(V);
     pdl_trigger();
     int64_t n = n_cells[qi];
     const bool overflow = n > max_cells;  // truncated list: the result must not be used
@@ -838,6 +855,8 @@ attn_combine_kernel(const float *__restrict__ part, int S, int H_q, int H_kv, in
     const int rec = d_v + 4;
     const int64_t stride = (int64_t)G * rec;
     pdl_wait();
+    QSA_AFTER_WAIT(part);
+    QSA_AFTER_WAIT(n_cells);
     pdl_trigger();
     float *o = out + (qi * H_q + h) * (int64_t)d_v;
     if ((int64_t)n_cells[qi] > max_cells) {

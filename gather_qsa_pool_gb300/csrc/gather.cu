@@ -42,6 +42,11 @@ gather_kernel(const char *__restrict__ K, const char *__restrict__ V, int esize,
               int32_t *__restrict__ n_cells_out, int64_t max_cells)
 {
     pdl_wait();
+    QSA_AFTER_WAIT(K);
+    QSA_AFTER_WAIT(V);
+    QSA_AFTER_WAIT(blocks);
+    QSA_AFTER_WAIT(counts);
+    QSA_AFTER_WAIT(q_pos);
     pdl_trigger();
     const int64_t qi = blockIdx.y;
     const int lane = threadIdx.x & 31;
@@ -80,6 +85,9 @@ cells_kernel(int64_t n_kv, const int32_t *__restrict__ blocks, const int32_t *__
              int32_t *__restrict__ pos_out, int32_t *__restrict__ n_cells_out, int64_t max_cells)
 {
     pdl_wait();
+    QSA_AFTER_WAIT(blocks);
+    QSA_AFTER_WAIT(counts);
+    QSA_AFTER_WAIT(q_pos);
     pdl_trigger();
     const int64_t qi = blockIdx.y;
     const int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;

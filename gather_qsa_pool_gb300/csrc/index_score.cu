@@ -90,6 +90,8 @@ score_rows_kernel(const float *__restrict__ q, const float *__restrict__ pooled,
 {
     __shared__ float4 q_s[NV * 32];
     pdl_wait();
+    QSA_AFTER_WAIT(q);
+    QSA_AFTER_WAIT(pooled);
     pdl_trigger();
     for (int i = threadIdx.x; i < NV * 32; i += blockDim.x)
         q_s[i] = reinterpret_cast<const float4 *>(q)[i];
@@ -114,6 +116,10 @@ score_pool_kernel(const float *__restrict__ q, float *__restrict__ pooled, float
     __shared__ __align__(16) float p_s[NV * 128];
     __shared__ float cs[kRopeMaxHalf], sn[kRopeMaxHalf];
     pdl_wait();
+    QSA_AFTER_WAIT(q);
+    QSA_AFTER_WAIT(pooled);
+    QSA_AFTER_WAIT(raw);
+    QSA_AFTER_WAIT(w);
     pdl_trigger();
     for (int i = threadIdx.x; i < NV * 32; i += blockDim.x)
         q_s[i] = reinterpret_cast<const float4 *>(q)[i];
@@ -149,6 +155,9 @@ score_tiled_kernel(const float *__restrict__ q, int64_t n_q, int64_t ld_q,
     __shared__ float a_s[kBK][kBM + 4];
     __shared__ float b_s[kBK][kBN + 4];
     pdl_wait();
+    QSA_AFTER_WAIT(q);
+    QSA_AFTER_WAIT(q_pos);
+    QSA_AFTER_WAIT(pooled);
     pdl_trigger();
     const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
     const int64_t m0 = (int64_t)blockIdx.y * kBM;

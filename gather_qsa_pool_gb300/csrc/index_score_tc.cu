@@ -147,6 +147,7 @@ q_to_bf16_kernel(const float *__restrict__ q, int64_t n_q, int64_t ld_q, int K,
                  __nv_bfloat16 *__restrict__ qb)
 {
     pdl_wait();
+    QSA_AFTER_WAIT(q);
     pdl_trigger();
     const int64_t total = n_q * (int64_t)K;
     for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
@@ -174,6 +175,9 @@ score_tc_kernel(const __nv_bfloat16 *__restrict__ qb, int64_t n_q,
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     pdl_wait();
+    QSA_AFTER_WAIT(qb);
+    QSA_AFTER_WAIT(q_pos);
+    QSA_AFTER_WAIT(pooled);
     pdl_trigger();
 
     if (tid == 0) {

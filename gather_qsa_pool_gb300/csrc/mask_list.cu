@@ -28,6 +28,7 @@ mask_to_list_kernel(const uint8_t *__restrict__ mask, int64_t n_kv, int64_t ld_m
     __shared__ uint32_t warp_tot[kMaskThreads / 32];
     __shared__ uint32_t carry_s;
     pdl_wait();
+    QSA_AFTER_WAIT(mask);
     pdl_trigger();
 
     const int64_t r = blockIdx.x;

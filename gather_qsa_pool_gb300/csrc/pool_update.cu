@@ -36,6 +36,8 @@ pool_update_kernel(const T *__restrict__ raw, int64_t n_ctx, int H, int d,
     float *sin_s = cos_s + half;  // [d/2]
 
     pdl_wait();
+    QSA_AFTER_WAIT(raw);
+    QSA_AFTER_WAIT(w);
     pdl_trigger();
     if (zero_hist && blockIdx.x == 0)
         for (int i = threadIdx.x; i < (1 << kTopkHistBits); i += kPoolThreads) zero_hist[i] = 0u;

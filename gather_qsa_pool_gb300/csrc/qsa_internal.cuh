@@ -50,8 +50,8 @@ __device__ __forceinline__ float warp_max(float v)
 // may write (a no-op when it was launched without the programmatic-serialisation
 // attribute), then lets its successor launch: the successor's CTAs become resident as this
 // grid's CTAs retire and block in their own wait until this grid has completed and
-// flushed, which hides the launch gap between the small kernels of a decode step.  Since
-// every kernel triggers only after its own wait, a running kernel knows that all grids
+// flushed, which hides the launch gap between the small kernels of a decode step.  Every
+// kernel triggers right after its own wait, so a running kernel knows that all grids
 // before its immediate predecessor have completed: inputs written before that
 // predecessor may be read before the wait.
 
@@ -60,6 +60,13 @@ __device__ __forceinline__ void pdl_trigger()
 {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
+
+// A load through a const __restrict__ pointer may be compiled as an invariant load, which
+// the compiler is free to issue before griddepcontrol.wait (an asm with a memory clobber
+// does not order it).  QSA_AFTER_WAIT(p), placed after the wait, passes p through an
+// empty volatile asm: every later load through p then depends on a value produced after
+// the wait.  Each kernel applies it to every pointer it reads after its wait.
+#define QSA_AFTER_WAIT(p) asm volatile("" : "+l"(p))
 
 template <typename... KArgs, typename... Args>
 cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,

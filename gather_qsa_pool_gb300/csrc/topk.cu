@@ -163,8 +163,18 @@ topk_kernel(const float *__restrict__ scores, int64_t ld, const int32_t *__restr
     uint32_t *misc = warp_s + 2 * (NT / 32);    // [32]
     uint32_t *selw = misc + 32;                 // [nw] selected blocks bitmap
     const int64_t qi = blockIdx.x;
+    const uint32_t *pre_meta = pre.meta, *pre_bitmap = pre.bitmap;
+    const uint2 *pre_cand = pre.cand;
+    const int32_t *pre_cnt = pre.cand_cnt;
 
     pdl_wait();
+    QSA_AFTER_WAIT(scores);
+    QSA_AFTER_WAIT(q_pos);
+    QSA_AFTER_WAIT(ext_hist);
+    QSA_AFTER_WAIT(pre_meta);
+    QSA_AFTER_WAIT(pre_bitmap);
+    QSA_AFTER_WAIT(pre_cand);
+    QSA_AFTER_WAIT(pre_cnt);
     pdl_trigger();
 
     const int64_t p = q_pos ? (int64_t)q_pos[qi] : n_ctx - 1;  // the query's position
@@ -207,29 +217,29 @@ topk_kernel(const float *__restrict__ scores, int64_t ld, const int32_t *__restr
     int fixed = kTopkHistBits;
     bool whole = false;
     bool pre_ok = false;
-    if (pre.meta) {
+    if (pre_meta) {
         // ---- 1-2 done by the classify pass: take its decision, bitmap and candidates
         const int c = threadIdx.x;
         uint32_t my = 0;
         bool over = false;
         if (c < pre.n_cta) {
-            my = (uint32_t)pre.cand_cnt[c];
+            my = (uint32_t)pre_cnt[c];
             over = my > (uint32_t)pre.cap;
         }
         const bool any_over = __syncthreads_or(over);
         uint32_t n_cand;
         const uint32_t cbase = block_excl_scan(my, warp_s, &n_cand);
-        pre_ok = pre.meta[3] != 0 && !any_over && n_cand <= (uint32_t)cand_cap;
+        pre_ok = pre_meta[3] != 0 && !any_over && n_cand <= (uint32_t)cand_cap;
         if (pre_ok) {
-            prefix = pre.meta[0];
-            k_rem = (uint32_t)k - pre.meta[1];
-            whole = pre.meta[2] != 0;
+            prefix = pre_meta[0];
+            k_rem = (uint32_t)k - pre_meta[1];
+            whole = pre_meta[2] != 0;
             for (int64_t w = threadIdx.x; w < nw; w += NT) {
-                selw[w] = pre.bitmap[w];
+                selw[w] = pre_bitmap[w];
                 eqw[w] = 0u;
             }
             for (uint32_t j = 0; j < my; ++j) {
-                const uint2 e = pre.cand[(int64_t)c * pre.cap + j];
+                const uint2 e = pre_cand[(int64_t)c * pre.cap + j];
                 cand_key[cbase + j] = e.x;
                 cand_idx[cbase + j] = (int32_t)e.y;
             }
@@ -244,7 +254,7 @@ topk_kernel(const float *__restrict__ scores, int64_t ld, const int32_t *__restr
         // (and clear it for the next step) unless its total disagrees with the candidate
         // count -- a workspace that was never cleared -- in which case build it here
         bool have = false;
-        if (ehist && !pre.meta) {
+        if (ehist && !pre_meta) {
             uint32_t part = 0;
             for (int i = threadIdx.x; i < kBins1; i += NT) {
                 const uint32_t v = ehist[i];
@@ -395,6 +405,8 @@ topk_classify_kernel(const float *__restrict__ scores, int64_t n, int64_t k,
     __shared__ uint32_t warp_s[2 * (NT / 32)];
     __shared__ uint32_t misc[32];
     pdl_wait();
+    QSA_AFTER_WAIT(scores);
+    QSA_AFTER_WAIT(hist);
     pdl_trigger();
     uint32_t part = 0;
     for (int i = threadIdx.x; i < kBins1; i += NT) {
