@@ -38,9 +38,9 @@ CONTEXTS = {"64k": "decode_64k", "128k": "decode_128k", "256k": "decode_256k"}
 SCORE_SRC = os.path.join(ROOT, "gather_qsa_pool_gb300", "csrc", "index_score.cu")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "score_rows_256k_traffic.txt")
 # Kernels one qsa_decode_step launches when it appends a token: the fused pool-update +
-# score scan, the top-k classify pass, the top-k resolve pass (which also writes the cell
-# list) and the attention kernel (split-K with the combine inside its cluster).
-LAUNCHES_PER_DECODE_STEP = 4
+# score scan, the top-k (whose last CTA also writes the cell list) and the attention
+# kernel (split-K with the combine inside its cluster).
+LAUNCHES_PER_DECODE_STEP = 3
 
 
 def parse_args():

@@ -572,6 +572,7 @@ attn_mma_kernel(const float *__restrict__ q, int H_q, int H_kv, float scale_log2
                 float *__restrict__ lse, int early_q)
 {
     constexpr int G = 8, D = 128, TC = kMmaTC, LD = kMmaLd, NW = kMmaWarps, NT = 32 * NW;
+    static_assert(NT == 2 * TC, "one thread per cell of the first two stages");
     extern __shared__ __align__(16) char smem_raw[];
     __nv_bfloat16 *Ks = reinterpret_cast<__nv_bfloat16 *>(smem_raw);  // [2][TC][LD]
     __nv_bfloat16 *Vs = Ks + 2 * TC * LD;                                // [2][TC][LD]
@@ -622,16 +623,40 @@ attn_mma_kernel(const float *__restrict__ q, int H_q, int H_kv, float scale_log2
     QSA_AFTER_WAIT(K);
     QSA_AFTER_WAIT(V);
     pdl_trigger();
-    int64_t n = n_cells[qi];
-    const bool overflow = n > max_cells;  // truncated list: the result must not be used
-    if (overflow) n = 0;
-    if (n < 0) n = 0;
-    const int64_t chunk = (n + S - 1) / S;
+    // One barrier per stage buffer: a phase completes when every K and V row of the stage
+    // has landed (bulk copies count their bytes on it).
+    __shared__ __align__(8) uint64_t sbar[2];
+    if (tid == 0) {
+        mbar_init(&sbar[0], 1);
+        mbar_init(&sbar[1], 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    uint32_t sphase = 0;  // bit b: parity of buffer b's next phase
+    bool lost = false;    // a stage that never completed (its outputs become NaN)
+    uint32_t lost_at = 0;  // buffer | parity << 1 of that stage
+    // A split's cell range is fixed by max_cells, so the positions of its first two stages
+    // are loaded together with the list length; entries past the length are dropped once
+    // it arrives.
+    const int64_t chunk = (max_cells + S - 1) / S;
     const int64_t c0 = (int64_t)s_idx * chunk;
-    const int64_t c1 = c0 + chunk < n ? c0 + chunk : n;
+    const int64_t c1max = c0 + chunk < max_cells ? c0 + chunk : max_cells;
+    int64_t n = n_cells[qi];
+    int64_t first_row = -1;  // cell c0 + tid: stage tid / TC, slot tid % TC
+    if (c0 + tid < c1max)
+        first_row = pos ? (int64_t)pos[qi * max_cells + c0 + tid] : qi * max_cells + c0 + tid;
+    const bool overflow = n > max_cells;  // truncated list: the result must not be used
+    if (overflow || n < 0) n = 0;
+    const int64_t c1 = c1max < n ? c1max : n;
     const int ntiles = c1 > c0 ? (int)((c1 - c0 + TC - 1) / TC) : 0;
+    {
+        int64_t row = c0 + tid < c1 ? first_row : -1;
+        if (row < 0 || row >= n_kv) row = -1;
+        rows[tid] = (int32_t)row;
+    }
+    __syncthreads();
 
-    auto issue = [&](int it, int buf) {
+    // rows of stage `it` into row buffer `buf` (stages from the third on)
+    auto load_rows = [&](int it, int buf) {
         const int64_t base = c0 + (int64_t)it * TC;
         const int tc = (int)min((int64_t)TC, c1 - base);
         int32_t *rb = rows + buf * TC;
@@ -645,38 +670,50 @@ attn_mma_kernel(const float *__restrict__ q, int H_q, int H_kv, float scale_log2
             rb[slot] = (int32_t)row;
         }
         __syncthreads();
+    };
+    // K and V rows of buffer `buf` into shared memory: one bulk copy of this KV head's 256
+    // bytes per row and tensor, all counted on the buffer's barrier.  A skipped row's K is
+    // never used (its logit is masked by a select), but its V row is multiplied by p = 0
+    // inside the MMA, so it is zero-filled: stale shared memory could hold a NaN pattern.
+    auto copy_rows = [&](int buf) {
+        const int32_t *rb = rows + buf * TC;
         __nv_bfloat16 *ks = Ks + buf * TC * LD;
         __nv_bfloat16 *vs = Vs + buf * TC * LD;
-        // 16 K chunks + 16 V chunks per row.  A skipped row's K is never used (its logit is
-        // masked by a select), but its V row is multiplied by p = 0 inside the MMA, so it is
-        // zero-filled: stale shared memory could hold a NaN pattern.
-        for (int e = tid; e < TC * 32; e += NT) {
-            const int slot = e >> 5;
-            const int c = e & 31;
-            const int64_t row = rb[slot];
-            if (row < 0) {
-                if (c >= 16) cp_async16(vs + slot * LD + (c - 16) * 8, V, false);
-                continue;
-            }
-            if (c < 16)
-                cp_async16(ks + slot * LD + c * 8, K + row * ld_k + (int64_t)g * D + c * 8, true);
-            else
-                cp_async16(vs + slot * LD + (c - 16) * 8,
-                           V + row * ld_v + (int64_t)g * D + (c - 16) * 8, true);
+        for (int e = tid; e < TC * (D / 8); e += NT) {
+            const int slot = e / (D / 8), c = e - slot * (D / 8);
+            if (rb[slot] < 0) *reinterpret_cast<uint4 *>(vs + slot * LD + c * 8) = make_uint4(0u, 0u, 0u, 0u);
         }
-        cp_async_commit();
+        const int nv = __syncthreads_count(tid < TC && rb[tid] >= 0);
+        if (tid == 0) mbar_arrive_expect_tx(&sbar[buf], (uint32_t)nv * 2u * D * 2u);
+        const int slot = tid >> 1;  // NT = 2 * TC: one thread per row and tensor
+        const int64_t row = rb[slot];
+        if (row >= 0) {
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            if (tid & 1)
+                bulk_g2s(vs + slot * LD, V + row * ld_v + (int64_t)g * D, D * 2, &sbar[buf]);
+            else
+                bulk_g2s(ks + slot * LD, K + row * ld_k + (int64_t)g * D, D * 2, &sbar[buf]);
+        }
+    };
+    // Wait for buffer `buf`'s stage (bounded), then make its zero-filled rows visible.
+    auto wait_rows = [&](int buf) {
+        if (!lost && !mbar_wait(&sbar[buf], (sphase >> buf) & 1u)) {
+            lost = true;
+            lost_at = (uint32_t)buf | (((sphase >> buf) & 1u) << 1);
+        }
+        sphase ^= 1u << buf;
+        __syncthreads();
     };
 
-    if (ntiles > 0) issue(0, 0);
+    if (ntiles > 0) copy_rows(0);
+    if (ntiles > 1) copy_rows(1);
     for (int it = 0; it < ntiles; ++it) {
         const int buf = it & 1;
-        if (it + 1 < ntiles) {
-            issue(it + 1, buf ^ 1);
-            cp_async_wait<1>();
-        } else {
-            cp_async_wait<0>();
+        if (it >= 1 && it + 1 < ntiles) {
+            load_rows(it + 1, buf ^ 1);
+            copy_rows(buf ^ 1);
         }
-        __syncthreads();
+        wait_rows(buf);
         const int tc = (int)min((int64_t)TC, c1 - (c0 + (int64_t)it * TC));
         const __nv_bfloat16 *ks = Ks + buf * TC * LD;
         const __nv_bfloat16 *vs = Vs + buf * TC * LD;
@@ -751,6 +788,7 @@ attn_mma_kernel(const float *__restrict__ q, int H_q, int H_kv, float scale_log2
         __syncthreads();  // this stage is refilled by the next issue()
     }
 
+    lost = __syncthreads_or(lost);
     // per-warp state -> shared memory: head hr, dims 8j + qc + {0,1}
     float l4 = lsum;
     l4 += __shfl_xor_sync(0xffffffffu, l4, 1);
@@ -766,77 +804,117 @@ attn_mma_kernel(const float *__restrict__ q, int H_q, int H_kv, float scale_log2
         mw[D + 1] = l4;
     }
     __syncthreads();
-    // merge the warps: the CTA's (o unnormalised, m, l) per head
-    for (int e = tid; e < G * D; e += NT) {
-        const int h = e / D, c = e - h * D;
+    // merge the warps: per head the maximum M over the warps and each warp's weight
+    // 2^(m_w - M) once, then every output is one weighted sum over the warps
+    __shared__ float wf[NW * G];  // warp weights
+    __shared__ float hm[G], hl[G];  // per head: M and the weighted l
+    if (tid < G) {
         float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < NW; ++w) M = fmaxf(M, mrg[(w * G + h) * (D + 2) + D]);
-        float acc = 0.0f, L = 0.0f;
-        if (M != -INFINITY) {
+        for (int w = 0; w < NW; ++w) M = fmaxf(M, mrg[(w * G + tid) * (D + 2) + D]);
+        float L = 0.0f;
 #pragma unroll
-            for (int w = 0; w < NW; ++w) {
-                const float *r = mrg + (w * G + h) * (D + 2);
-                const float f = exp2f(r[D] - M);
-                acc = fmaf(f, r[c], acc);
-                L = fmaf(f, r[D + 1], L);
-            }
+        for (int w = 0; w < NW; ++w) {
+            const float *r = mrg + (w * G + tid) * (D + 2);
+            const float f = M != -INFINITY ? exp2f(r[D] - M) : 0.0f;
+            wf[w * G + tid] = f;
+            L = fmaf(f, r[D + 1], L);
         }
+        hm[tid] = M;
+        hl[tid] = L;
+    }
+    __syncthreads();
+    for (int e = tid; e < G * D; e += NT) {
+        const int h = e / D, c = e - h * D;
+        float acc = 0.0f;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) acc = fmaf(wf[w * G + h], mrg[(w * G + h) * (D + 2) + c], acc);
+        const float M = hm[h], L = hl[h];
         if (S == 1) {
             float v = L > 0.0f ? acc / L : 0.0f;
-            if (overflow) v = __int_as_float(0x7fc00000);
+            if (overflow || lost) v = __int_as_float(0x7fc00000);
             out[(qi * H_q + (int64_t)g * G + h) * D + c] = v;
             if (lse && c == 0)
-                lse[qi * H_q + g * G + h] = overflow ? __int_as_float(0x7fc00000)
+                lse[qi * H_q + g * G + h] = (overflow || lost) ? __int_as_float(0x7fc00000)
                                            : (L > 0.0f ? (M + log2f(L)) * kLn2 : -INFINITY);
         } else {
             float *r = cta + h * (D + 2);
             r[c] = acc;
             if (c == 0) {
                 r[D] = M;
-                r[D + 1] = L;
+                r[D + 1] = lost ? -1.0f : L;  // a negative weight sum marks a lost stage
             }
         }
     }
-    if (S == 1) return;
+    // a lost stage may still have copies in flight into this CTA's shared memory: give them
+    // one more bounded wait before the CTA retires
+    auto drain = [&]() {
+        if (lost) (void)mbar_wait(&sbar[lost_at & 1u], lost_at >> 1);
+    };
+    if (S == 1) {
+        drain();
+        return;
+    }
 
-    // combine the S CTAs of the cluster: CTA s owns outputs [s*per, (s+1)*per) of G*D
+    // combine the S CTAs of the cluster: CTA s owns outputs [s*per, (s+1)*per) of G*D.
+    // Four threads per output, each reading (m, l, o) of a quarter of the remote states in
+    // one round of distributed shared-memory loads; the maximum and the sums meet through
+    // two shuffles.
     cg::cluster_group cluster = cg::this_cluster();
     cluster.sync();  // every CTA's merged state is in its shared memory
     const int per = (G * D + S - 1) / S;
-    for (int e = s_idx * per + tid; e < (s_idx + 1) * per && e < G * D; e += NT) {
+    const int part = tid & 3;
+    for (int base = s_idx * per; base < (s_idx + 1) * per; base += NT / 4) {
+        const int e0 = base + (tid >> 2);
+        const bool live = e0 < (s_idx + 1) * per && e0 < G * D;
+        const int e = live ? e0 : 0;
         const int h = e / D, c = e - h * D;
-        float mv[kMmaMaxCluster], lv[kMmaMaxCluster], ov[kMmaMaxCluster];
+        constexpr int RQ = kMmaMaxCluster / 4;
+        float mv[RQ], lv[RQ], ov[RQ];
         float M = -INFINITY;
 #pragma unroll
-        for (int r = 0; r < kMmaMaxCluster; ++r) {
+        for (int j = 0; j < RQ; ++j) {
+            const int r = part + 4 * j;
+            mv[j] = -INFINITY;
+            lv[j] = ov[j] = 0.0f;
             if (r < S) {
                 const float *rc = cluster.map_shared_rank(cta, r) + h * (D + 2);
-                mv[r] = rc[D];
-                lv[r] = rc[D + 1];
-                ov[r] = rc[c];
-                M = fmaxf(M, mv[r]);
+                mv[j] = rc[D];
+                lv[j] = rc[D + 1];
+                ov[j] = rc[c];
             }
+            M = fmaxf(M, mv[j]);
         }
+        bool bad = false;
+#pragma unroll
+        for (int j = 0; j < RQ; ++j) bad = bad || lv[j] < 0.0f;
+        bad = __any_sync(0xffffffffu, bad && live) || overflow;  // any lost stage of the group
+        M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 1));
+        M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 2));
         float acc = 0.0f, L = 0.0f;
         if (M != -INFINITY) {
 #pragma unroll
-            for (int r = 0; r < kMmaMaxCluster; ++r) {
-                if (r < S) {
-                    const float f = exp2f(mv[r] - M);
-                    acc = fmaf(f, ov[r], acc);
-                    L = fmaf(f, lv[r], L);
-                }
+            for (int j = 0; j < RQ; ++j) {
+                const float f = exp2f(mv[j] - M);
+                acc = fmaf(f, ov[j], acc);
+                L = fmaf(f, lv[j], L);
             }
         }
-        float v = L > 0.0f ? acc / L : 0.0f;
-        if (overflow) v = __int_as_float(0x7fc00000);
-        out[(qi * H_q + (int64_t)g * G + h) * D + c] = v;
-        if (lse && c == 0)
-            lse[qi * H_q + g * G + h] = overflow ? __int_as_float(0x7fc00000)
-                                       : (L > 0.0f ? (M + log2f(L)) * kLn2 : -INFINITY);
+        acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+        acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+        L += __shfl_xor_sync(0xffffffffu, L, 1);
+        L += __shfl_xor_sync(0xffffffffu, L, 2);
+        if (part == 0 && live) {
+            float v = L > 0.0f ? acc / L : 0.0f;
+            if (bad) v = __int_as_float(0x7fc00000);
+            out[(qi * H_q + (int64_t)g * G + h) * D + c] = v;
+            if (lse && c == 0)
+                lse[qi * H_q + g * G + h] = bad ? __int_as_float(0x7fc00000)
+                                           : (L > 0.0f ? (M + log2f(L)) * kLn2 : -INFINITY);
+        }
     }
     cluster.sync();  // keep this CTA's state alive until every remote read is done
+    drain();
 }
 
 // Combine the S split partials of one (query, head): log-sum-exp weighting.  The split

@@ -127,7 +127,8 @@ qsa_status qsa_index_score(const float *q, int64_t n_q, int64_t ld_q, const int3
     if (v != QSA_OK) return v;
     if (precision == QSA_PREC_F32) {
         return from_cuda(launch_index_score(q, n_q, ld_q, q_pos, pooled, n_rows, H, d, scale,
-                                            scores, ld_scores, nullptr, 0, (cudaStream_t)stream));
+                                            scores, ld_scores, nullptr, 0, nullptr,
+                                            (cudaStream_t)stream));
     }
     if (precision == QSA_PREC_BF16_TC) {
         const size_t need = qsa_index_score_workspace_size(n_q, n_rows, H, d, precision);
@@ -248,7 +249,7 @@ size_t qsa_decode_step_workspace_size(int H_q, int H_kv, int d, int64_t max_cell
 {
     if (H_q < 1 || H_kv < 1 || d < 1 || max_cells < 0 || H_q % H_kv || cap_rows < 0) return 0;
     return align256(attn_workspace_bytes(1, H_q, H_kv, d, max_cells)) + kTopkHistBytes +
-           topk_pre_workspace_bytes(cap_rows);
+           topk_select_workspace_bytes(cap_rows);
 }
 
 qsa_status qsa_decode_step(const void *raw_k, qsa_dtype raw_dtype, int64_t n_ctx, int H_idx,
@@ -268,15 +269,9 @@ qsa_status qsa_decode_step(const void *raw_k, qsa_dtype raw_dtype, int64_t n_ctx
     const size_t attn_bytes = align256(attn_workspace_bytes(1, H_q, H_kv, d, max_cells));
     char *wsb = static_cast<char *>(workspace);
     uint32_t *hist = reinterpret_cast<uint32_t *>(wsb + attn_bytes);
-    // top-k classify area: meta | per-CTA counts | per-CTA candidates | bitmap
-    const int64_t nw_cap = (cap_rows + 31) / 32;
-    const int64_t g_cap = (nw_cap + kClsWordsPerCta - 1) / kClsWordsPerCta;
-    char *pre_base = wsb + attn_bytes + kTopkHistBytes;
-    uint32_t *meta = reinterpret_cast<uint32_t *>(pre_base);
-    int32_t *cand_cnt = reinterpret_cast<int32_t *>(pre_base + 256);
-    uint2 *cand = reinterpret_cast<uint2 *>(pre_base + 256 + align256(4 * g_cap));
-    uint32_t *bitmap = reinterpret_cast<uint32_t *>(pre_base + 256 + align256(4 * g_cap) +
-                                                    align256(8 * g_cap * kClsCap));
+    // top-k scratch: arrival ticket | per-CTA candidate counts | candidates | bitmap
+    void *sel = wsb + attn_bytes + kTopkHistBytes;
+    uint32_t *ticket = topk_select_ticket(sel);
     qsa_status v = check_pool_update(raw_k, raw_dtype, n_ctx, H_idx, d_idx, norm_w, eps,
                                      rope_base, pooled, cap_rows, n_valid_full);
     if (v == QSA_OK)
@@ -304,24 +299,28 @@ qsa_status qsa_decode_step(const void *raw_k, qsa_dtype raw_dtype, int64_t n_ctx
     pf.row0 = row0;
     pf.row1 = n_rows;
     cudaError_t e = launch_score_pool_fused(q_idx, pooled, n_rows, H_idx, d_idx, scale_idx, scores,
-                                            hist, n_full, pf, rope_base, st);
+                                            hist, n_full, ticket, pf, rope_base, st);
     if (e == cudaErrorNotSupported) {
         e = run_pool_update(raw_k, raw_dtype, n_ctx, H_idx, d_idx, norm_w, eps, rope_base, pooled,
                             n_valid_full, hist, st);
         if (e == cudaSuccess)
             e = launch_index_score(q_idx, 1, (int64_t)H_idx * d_idx, nullptr, pooled, n_rows,
-                                   H_idx, d_idx, scale_idx, scores, n_rows, hist, n_full, st);
+                                   H_idx, d_idx, scale_idx, scores, n_rows, hist, n_full, ticket,
+                                   st);
     }
-    // 3. top-k from that histogram: a many-CTA classify pass, then the one-CTA resolve pass,
-    // whose epilogue writes the cell list (qsa_gather_kv's job)
-    TopkPre pre;
+    // 3. top-k from that histogram; its last CTA also writes the cell list (qsa_gather_kv's
+    // job).  When every full block is selected, the one-CTA form does it.
     if (e == cudaSuccess) {
-        e = launch_topk_classify(scores, n_full, k_blk, hist, meta, bitmap, cand, cand_cnt, &pre, st);
-        if (e == cudaErrorNotSupported) e = cudaSuccess;  // the resolve pass does it all
+        const int64_t esize = kv_dtype == QSA_BF16 ? 2 : 4;
+        const int64_t row_bytes = (int64_t)H_kv * d * esize;
+        const bool contiguous = ld_kv == (int64_t)H_kv * d;
+        e = launch_topk_select(scores, n_full, k_blk, n_ctx, hist, sel, blocks, counts, pos,
+                               n_cells, contiguous ? K : nullptr, contiguous ? V : nullptr,
+                               row_bytes, st);
+        if (e == cudaErrorNotSupported)
+            e = launch_topk(scores, 1, n_rows, nullptr, n_full, k_blk, blocks, counts, n_ctx, pos,
+                            n_cells, max_cells, hist, st);
     }
-    if (e == cudaSuccess)
-        e = launch_topk(scores, 1, n_rows, nullptr, n_full, k_blk, blocks, counts, n_ctx, pos,
-                        n_cells, max_cells, hist, st, pre);
     // 4. attention over the listed cells, read in place from the cache
     if (e == cudaSuccess)
         e = launch_sparse_attn(q, 1, H_q, H_kv, d, d, scale, K, V, kv_dtype, n_kv, ld_kv, ld_kv,

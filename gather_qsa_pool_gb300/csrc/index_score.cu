@@ -86,13 +86,14 @@ template <int NV, int R>
 __global__ void __launch_bounds__(kScoreThreads)
 score_rows_kernel(const float *__restrict__ q, const float *__restrict__ pooled,
                   int64_t n_rows, float scale, float *__restrict__ scores,
-                  uint32_t *__restrict__ hist, int64_t n_hist)
+                  uint32_t *__restrict__ hist, int64_t n_hist, uint32_t *__restrict__ ticket)
 {
     __shared__ float4 q_s[NV * 32];
     pdl_wait();
     QSA_AFTER_WAIT(q);
     QSA_AFTER_WAIT(pooled);
     pdl_trigger();
+    if (ticket && blockIdx.x == 0 && threadIdx.x == 0) *ticket = 0u;
     for (int i = threadIdx.x; i < NV * 32; i += blockDim.x)
         q_s[i] = reinterpret_cast<const float4 *>(q)[i];
     __syncthreads();
@@ -108,7 +109,7 @@ template <int NV, typename T>
 __global__ void __launch_bounds__(kScoreThreads)
 score_pool_kernel(const float *__restrict__ q, float *__restrict__ pooled, float scale,
                   float *__restrict__ scores, uint32_t *__restrict__ hist, int64_t n_hist,
-                  const T *__restrict__ raw, int64_t n_ctx, int H, int d,
+                  uint32_t *__restrict__ ticket, const T *__restrict__ raw, int64_t n_ctx, int H, int d,
                   const float *__restrict__ w, float eps, int64_t row0, int n_pool,
                   const RopeTable tab)
 {
@@ -121,6 +122,7 @@ score_pool_kernel(const float *__restrict__ q, float *__restrict__ pooled, float
     QSA_AFTER_WAIT(raw);
     QSA_AFTER_WAIT(w);
     pdl_trigger();
+    if (ticket && blockIdx.x == 0 && threadIdx.x == 0) *ticket = 0u;
     for (int i = threadIdx.x; i < NV * 32; i += blockDim.x)
         q_s[i] = reinterpret_cast<const float4 *>(q)[i];
     __syncthreads();
@@ -150,7 +152,8 @@ __global__ void __launch_bounds__(256)
 score_tiled_kernel(const float *__restrict__ q, int64_t n_q, int64_t ld_q,
                    const int32_t *__restrict__ q_pos, const float *__restrict__ pooled,
                    int64_t n_rows, int hd, float scale, float *__restrict__ scores,
-                   int64_t ld_scores, uint32_t *__restrict__ hist, int64_t n_hist)
+                   int64_t ld_scores, uint32_t *__restrict__ hist, int64_t n_hist,
+                   uint32_t *__restrict__ ticket)
 {
     __shared__ float a_s[kBK][kBM + 4];
     __shared__ float b_s[kBK][kBN + 4];
@@ -159,6 +162,7 @@ score_tiled_kernel(const float *__restrict__ q, int64_t n_q, int64_t ld_q,
     QSA_AFTER_WAIT(q_pos);
     QSA_AFTER_WAIT(pooled);
     pdl_trigger();
+    if (ticket && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *ticket = 0u;
     const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
     const int64_t m0 = (int64_t)blockIdx.y * kBM;
     const int64_t n0 = (int64_t)blockIdx.x * kBN;
@@ -206,7 +210,8 @@ score_tiled_kernel(const float *__restrict__ q, int64_t n_q, int64_t ld_q,
 
 template <int NV, int R>
 cudaError_t launch_rows(const float *q, const float *pooled, int64_t n_rows, float scale,
-                        float *scores, uint32_t *hist, int64_t n_hist, cudaStream_t st)
+                        float *scores, uint32_t *hist, int64_t n_hist, uint32_t *ticket,
+                        cudaStream_t st)
 {
     static int blocks_per_sm = 0;
     auto k = score_rows_kernel<NV, R>;
@@ -222,12 +227,13 @@ cudaError_t launch_rows(const float *q, const float *pooled, int64_t n_rows, flo
     if (grid > grid_needed) grid = grid_needed;
     if (grid < 1) grid = 1;
     return launch(k, dim3((unsigned)grid), dim3(kScoreThreads), 0, st, 1, q, pooled, n_rows,
-                  scale, scores, hist, n_hist);
+                  scale, scores, hist, n_hist, ticket);
 }
 
 template <int NV, typename T>
 cudaError_t launch_fused(const float *q, const float *pooled, int64_t n_rows, int H, int d,
                          float scale, float *scores, uint32_t *hist, int64_t n_hist,
+                         uint32_t *ticket,
                          const PoolFuse &pf, double rope_base, cudaStream_t st)
 {
     static int blocks_per_sm = 0;
@@ -254,7 +260,7 @@ cudaError_t launch_fused(const float *q, const float *pooled, int64_t n_rows, in
     if (grid < n_pool + 1) grid = n_pool + 1;
     (void)n_rows;
     return launch(k, dim3((unsigned)grid), dim3(kScoreThreads), 0, st, 1, q, (float *)pooled,
-                  scale, scores, hist, n_hist, (const T *)pf.raw, pf.n_ctx, H, d, pf.w, pf.eps,
+                  scale, scores, hist, n_hist, ticket, (const T *)pf.raw, pf.n_ctx, H, d, pf.w, pf.eps,
                   pf.row0, n_pool, tab);
 }
 
@@ -262,7 +268,8 @@ cudaError_t launch_fused(const float *q, const float *pooled, int64_t n_rows, in
 
 cudaError_t launch_score_pool_fused(const float *q, const float *pooled, int64_t n_rows, int H,
                                     int d, float scale, float *scores, uint32_t *hist,
-                                    int64_t n_hist, const PoolFuse &pf, double rope_base,
+                                    int64_t n_hist, uint32_t *ticket, const PoolFuse &pf,
+                                    double rope_base,
                                     cudaStream_t st)
 {
     const int hd = H * d;
@@ -274,15 +281,15 @@ cudaError_t launch_score_pool_fused(const float *q, const float *pooled, int64_t
         return cudaErrorNotSupported;
     if (pf.dt == QSA_BF16)
         return launch_fused<16, __nv_bfloat16>(q, pooled, n_rows, H, d, scale, scores, hist,
-                                               n_hist, pf, rope_base, st);
-    return launch_fused<16, float>(q, pooled, n_rows, H, d, scale, scores, hist, n_hist, pf,
+                                               n_hist, ticket, pf, rope_base, st);
+    return launch_fused<16, float>(q, pooled, n_rows, H, d, scale, scores, hist, n_hist, ticket, pf,
                                    rope_base, st);
 }
 
 cudaError_t launch_index_score(const float *q, int64_t n_q, int64_t ld_q, const int32_t *q_pos,
                                const float *pooled, int64_t n_rows, int H, int d, float scale,
                                float *scores, int64_t ld_scores, uint32_t *hist, int64_t n_hist,
-                               cudaStream_t st)
+                               uint32_t *ticket, cudaStream_t st)
 {
     if (n_q == 0 || n_rows == 0) return cudaSuccess;
     const int hd = H * d;
@@ -290,17 +297,17 @@ cudaError_t launch_index_score(const float *q, int64_t n_q, int64_t ld_q, const 
                          (reinterpret_cast<uintptr_t>(pooled) % 16 == 0);
     if (n_q == 1 && q_pos == nullptr && aligned && hd % 128 == 0) {
         switch (hd / 128) {
-            case 1: return launch_rows<1, 4>(q, pooled, n_rows, scale, scores, hist, n_hist, st);
-            case 2: return launch_rows<2, 4>(q, pooled, n_rows, scale, scores, hist, n_hist, st);
-            case 4: return launch_rows<4, 2>(q, pooled, n_rows, scale, scores, hist, n_hist, st);
-            case 8: return launch_rows<8, 2>(q, pooled, n_rows, scale, scores, hist, n_hist, st);
-            case 16: return launch_rows<16, 1>(q, pooled, n_rows, scale, scores, hist, n_hist, st);
+            case 1: return launch_rows<1, 4>(q, pooled, n_rows, scale, scores, hist, n_hist, ticket, st);
+            case 2: return launch_rows<2, 4>(q, pooled, n_rows, scale, scores, hist, n_hist, ticket, st);
+            case 4: return launch_rows<4, 2>(q, pooled, n_rows, scale, scores, hist, n_hist, ticket, st);
+            case 8: return launch_rows<8, 2>(q, pooled, n_rows, scale, scores, hist, n_hist, ticket, st);
+            case 16: return launch_rows<16, 1>(q, pooled, n_rows, scale, scores, hist, n_hist, ticket, st);
             default: break;
         }
     }
     const dim3 grid((unsigned)((n_rows + kBN - 1) / kBN), (unsigned)((n_q + kBM - 1) / kBM));
     return launch(score_tiled_kernel, grid, dim3(256), 0, st, 1, q, n_q, ld_q, q_pos, pooled,
-                  n_rows, hd, scale, scores, ld_scores, hist, n_hist);
+                  n_rows, hd, scale, scores, ld_scores, hist, n_hist, ticket);
 }
 
 }  // namespace qsa

@@ -39,16 +39,10 @@ constexpr int kStages = 2;
 constexpr int kTileA = kMT * kBM * kBK * 2;  // 64 KB per stage
 constexpr int kTileB = kBN * kBK * 2;        // 16 KB per stage
 constexpr uint32_t kTmemCols = 512;
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // a wait that lasts 2 s is declared lost
 
 __host__ __device__ constexpr size_t tc_smem_bytes()
 {
     return 1024 /* alignment slack */ + (size_t)kStages * (kTileA + kTileB) + 64;
-}
-
-__device__ __forceinline__ uint32_t smem_u32(const void *p)
-{
-    return (uint32_t)__cvta_generic_to_shared(p);
 }
 
 // 64-bit shared-memory matrix descriptor of a K-major tile in the 128-byte swizzle:
@@ -70,43 +64,6 @@ __host__ __device__ constexpr uint32_t idesc_bf16_m128_n128()
 {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kBN >> 3) << 17) |
            ((uint32_t)(kBM >> 4) << 24);
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
-{
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
-                 : "memory");
-}
-
-__device__ __forceinline__ uint64_t global_ns()
-{
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-// Wait until the barrier's phase with the given parity has completed; false once the wait
-// has lasted kWaitLimitNs (the caller then records an error and winds down).
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
-{
-    const uint32_t a = smem_u32(bar);
-    uint64_t t0 = 0;
-    for (uint32_t i = 0;; ++i) {
-        uint32_t done;
-        asm volatile(
-            "{\n\t.reg .pred p;\n\t"
-            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-            "selp.u32 %0, 1, 0, p;\n\t}"
-            : "=r"(done)
-            : "r"(a), "r"(parity)
-            : "memory");
-        if (done) return true;
-        if ((i & 1023) == 0) {
-            const uint64_t t = global_ns();
-            if (t0 == 0) t0 = t;
-            else if (t - t0 > kWaitLimitNs) return false;
-        }
-    }
 }
 
 __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,

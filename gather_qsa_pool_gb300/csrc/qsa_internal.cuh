@@ -68,6 +68,75 @@ __device__ __forceinline__ void pdl_trigger()
 // the wait.  Each kernel applies it to every pointer it reads after its wait.
 #define QSA_AFTER_WAIT(p) asm volatile("" : "+l"(p))
 
+// ------------------------------------------------------------------ mbarrier / bulk copy
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // a wait that lasts 2 s is declared lost
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+                 : "memory");
+}
+
+__device__ __forceinline__ uint64_t global_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait until the barrier's phase with the given parity has completed; false once the wait
+// has lasted kWaitLimitNs (the caller then records an error and winds down).
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
+{
+    const uint32_t a = smem_u32(bar);
+    uint64_t t0 = 0;
+    for (uint32_t i = 0;; ++i) {
+        uint32_t done;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(done)
+            : "r"(a), "r"(parity)
+            : "memory");
+        if (done) return true;
+        if ((i & 1023) == 0) {
+            const uint64_t t = global_ns();
+            if (t0 == 0) t0 = t;
+            else if (t - t0 > kWaitLimitNs) return false;
+        }
+    }
+}
+
+// One arrival on the barrier that also expects `bytes` more transaction bytes this phase.
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+// Bulk copy global -> this CTA's shared memory, completing `bytes` transaction bytes on bar.
+// dst and src 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Bulk L2 prefetch of [p, p + bytes): p 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 template <typename... KArgs, typename... Args>
 cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
                    cudaStream_t stream, int cluster_x, Args &&...args)
@@ -196,17 +265,19 @@ struct PoolFuse {
 constexpr int kMaxFusedPoolRows = 4;
 // Decode score kernel with the pool update of rows [pf.row0, pf.row1) folded in, when the
 // shape allows it (returns cudaErrorNotSupported otherwise, without launching).
+// ticket (nullable): set to 0 once the kernel runs -- the decode top-k's arrival counter.
 cudaError_t launch_score_pool_fused(const float *q, const float *pooled, int64_t n_rows, int H,
                                     int d, float scale, float *scores, uint32_t *hist,
-                                    int64_t n_hist, const PoolFuse &pf, double rope_base,
-                                    cudaStream_t st);
+                                    int64_t n_hist, uint32_t *ticket, const PoolFuse &pf,
+                                    double rope_base, cudaStream_t st);
 
 // hist (nullable, decode only): also add each row b < n_hist to a histogram of the top
-// kTopkHistBits bits of its score key, for qsa_topk_blocks' first radix digit.
+// kTopkHistBits bits of its score key, for the top-k's first radix digit.  ticket
+// (nullable): set to 0 once the kernel runs.
 cudaError_t launch_index_score(const float *q, int64_t n_q, int64_t ld_q, const int32_t *q_pos,
                                const float *pooled, int64_t n_rows, int H, int d, float scale,
                                float *scores, int64_t ld_scores, uint32_t *hist, int64_t n_hist,
-                               cudaStream_t st);
+                               uint32_t *ticket, cudaStream_t st);
 
 qsa_status launch_index_score_tc(const float *q, int64_t n_q, int64_t ld_q,
                                  const int32_t *q_pos, const float *pooled, int64_t n_rows,
@@ -228,33 +299,30 @@ constexpr int kTopkThreads = 1024;
 constexpr int kTopkHistBits = 12;  // first radix digit: histogram of key >> 20
 constexpr size_t kTopkHistBytes = sizeof(uint32_t) << kTopkHistBits;
 int64_t topk_max_candidates();
-// Decode top-k split in two: a many-CTA classify pass (threshold digit from the score
-// kernel's histogram; above-threshold bitmap words; threshold-bucket candidates in
-// per-CTA lists) feeding the one-CTA resolve pass.
-struct TopkPre {
-    const uint32_t *meta = nullptr;     // [4]: digit, keys above it, whole-bucket flag, valid
-    const uint32_t *bitmap = nullptr;   // [ceil(n/32)] above-threshold blocks
-    const uint2 *cand = nullptr;        // [n_cta][cap] (key, block) of the threshold bucket
-    const int32_t *cand_cnt = nullptr;  // [n_cta] true counts
-    int n_cta = 0;
-    int cap = 0;
-};
-constexpr int kClsWordsPerCta = 32;   // bitmap words (x 32 blocks) per classify CTA
-constexpr int kClsCap = 128;          // candidates kept per classify CTA
 
 // pos_out / n_cells_out (nullable): also write each query's cell list -- the selected
 // blocks' 4 cells in order, then the open tail of the query (q_pos[i], or n_ctx - 1).
+// ext_hist (nullable): per-query histograms accumulated by the score kernel, cleared here.
 cudaError_t launch_topk(const float *scores, int64_t n_q, int64_t ld, const int32_t *q_pos,
                         int64_t n_full, int64_t k_blk, int32_t *blocks_out, int32_t *counts_out,
                         int64_t n_ctx, int32_t *pos_out, int32_t *n_cells_out,
-                        int64_t max_cells, uint32_t *ext_hist, cudaStream_t st,
-                        const TopkPre &pre = TopkPre());
-// The classify pass for one query (decode); returns cudaErrorNotSupported when the shape
-// does not take it (then the resolve pass runs its own full path).
-cudaError_t launch_topk_classify(const float *scores, int64_t n_full, int64_t k_blk,
-                                 const uint32_t *hist, uint32_t *meta, uint32_t *bitmap,
-                                 uint2 *cand, int32_t *cand_cnt, TopkPre *pre, cudaStream_t st);
-size_t topk_pre_workspace_bytes(int64_t n_full_cap);
+                        int64_t max_cells, uint32_t *ext_hist, cudaStream_t st);
+// The decode form of the top-k (one query whose n_full blocks outnumber k_blk): many CTAs
+// classify against the score kernel's histogram, the last to finish resolves and writes
+// blocks, count, cells and tail.  scratch: topk_select_workspace_bytes(n_full) bytes,
+// 256-byte aligned, whose first word (the ticket) the step's score kernel sets to 0.
+// Returns cudaErrorNotSupported, without launching, when n_full <= k_blk or n_full is
+// above topk_max_candidates().
+// kv_k / kv_v (nullable): K and V caches whose rows are contiguous (row stride = row
+// size = kv_row_bytes, a multiple of 16, bases 16-byte aligned); the K and V rows of the
+// blocks that clear the threshold bucket are then prefetched into L2 for the attention.
+cudaError_t launch_topk_select(const float *scores, int64_t n_full, int64_t k_blk, int64_t n_ctx,
+                               uint32_t *hist, void *scratch, int32_t *blocks_out,
+                               int32_t *counts_out, int32_t *pos_out, int32_t *n_cells_out,
+                               const void *kv_k, const void *kv_v, int64_t kv_row_bytes,
+                               cudaStream_t st);
+size_t topk_select_workspace_bytes(int64_t n_full_cap);
+uint32_t *topk_select_ticket(void *scratch);
 
 cudaError_t launch_gather(const void *K, const void *V, qsa_dtype dt, int64_t n_kv, int H_kv,
                           int d_k, int d_v, int64_t ld_k, int64_t ld_v, const int32_t *blocks,

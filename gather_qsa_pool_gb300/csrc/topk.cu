@@ -1,4 +1,4 @@
-// topk.cu -- block-domain top-k: one CTA per query, radix select over score keys.
+// topk.cu -- block-domain top-k: radix select over order-preserving score keys.
 //
 // Source: Qiita, ariera, EVO-X2 + Qwen3.8-Flash-Next llama.cpp series part 10, section
 // "block-domain top-k (COMMON-006)": select over the block scores instead of expanding
@@ -7,23 +7,33 @@
 // selected blocks to cell indices and append the tail.
 //
 // Scores become order-preserving 32-bit keys.  The k-th largest key T is found by radix
-// select in three digits (12 + 10 + 10 bits):
-//   1. a 4096-bin histogram of the top 12 bits -- either accumulated by the score kernel
-//      as it writes the scores (decode step, no extra pass; this kernel clears it again)
-//      or built here from one read;
-//   2. one read of the scores classifies every candidate: above the threshold bucket
-//      (selected: a bit in a shared-memory bitmap), inside it (appended to a candidate
-//      list in shared memory), or below (dropped);
-//   3. the remaining digits are resolved on the candidate list alone (a few hundred to a
-//      few thousand keys), stopping early once a bucket holds exactly the keys still
-//      needed;
+// select, first digit 12 bits (a 4096-bin histogram), then digits of 10 bits.
+//
+// General form (qsa_topk_blocks, prefill): one 1024-thread CTA per query.
+//   1. the 4096-bin histogram -- built here from one read of the scores, or taken from
+//      the score kernel when it accumulated one (and cleared again for the next step);
+//   2. one read of the scores classifies every block: above the threshold bucket
+//      (selected: a bit in a shared-memory bitmap), inside it (a candidate list in
+//      shared memory), or below (dropped);
+//   3. the remaining digits are resolved on the candidate list alone, stopping early
+//      once a bucket holds exactly the keys still needed;
 //   4. the candidates above T join the bitmap, the ones equal to T go to a tie bitmap;
 //   5. a block-wide scan over the bitmap words writes the selected blocks in ascending
 //      order -- ties taken lowest index first -- and, when asked, their cells and the
 //      open tail.
 // If the candidate list would overflow shared memory (pathological score
-// distributions), steps 3-4 re-read the scores instead.  No inter-CTA communication,
-// no global scratch beyond the optional histogram, no spin-waits.
+// distributions), steps 3-4 re-read the scores instead.
+//
+// Decode form (inside qsa_decode_step, one query): one kernel of ceil(n/1024) CTAs.
+// Every CTA finds the threshold bucket in the score kernel's histogram with a two-level
+// warp search, classifies its 1024 blocks with ballots (bitmap words for the blocks
+// above the bucket, a per-CTA list for the blocks inside it), then takes a ticket; the
+// last CTA to arrive resolves the bucket by ranking its candidates against each other
+// (key descending, index ascending), writes the selection, the cells and the tail, and
+// clears the histogram.  No CTA waits for another: the ticket decides which CTA
+// finishes the work, so there is no spin-wait.  A histogram whose total disagrees with
+// the block count (a workspace never cleared), or a bucket holding more than 1024
+// candidates, sends the last CTA through the general form instead.
 #include "qsa_internal.cuh"
 
 namespace qsa {
@@ -150,157 +160,133 @@ __device__ __forceinline__ void for_each_key(const float *__restrict__ row, int6
     }
 }
 
-__global__ void __launch_bounds__(NT)
-topk_kernel(const float *__restrict__ scores, int64_t ld, const int32_t *__restrict__ q_pos,
-            int64_t n_full_cap, int k_blk, int32_t *__restrict__ blocks_out,
-            int32_t *__restrict__ counts_out, int64_t n_ctx, int32_t *__restrict__ pos_out,
-            int32_t *__restrict__ n_cells_out, int64_t max_cells, uint32_t *__restrict__ ext_hist,
-            int cand_cap, const TopkPre pre)
+// Step 5 of the general form: fold the ties (lowest index first, k_rem of them) into the
+// selected bitmap, then write the selected blocks in ascending order.
+__device__ void write_selection(uint32_t *selw, const uint32_t *eqw, int64_t nw, uint32_t k_rem,
+                                int64_t k, int32_t *out, int32_t *pout, bool pvec,
+                                uint32_t *warp_s)
 {
-    extern __shared__ __align__(16) uint32_t smem[];
-    uint32_t *hist = smem;                      // [4096]
-    uint32_t *warp_s = hist + kBins1;           // [2][NT/32]
-    uint32_t *misc = warp_s + 2 * (NT / 32);    // [32]
-    uint32_t *selw = misc + 32;                 // [nw] selected blocks bitmap
-    const int64_t qi = blockIdx.x;
-    const uint32_t *pre_meta = pre.meta, *pre_bitmap = pre.bitmap;
-    const uint2 *pre_cand = pre.cand;
-    const int32_t *pre_cnt = pre.cand_cnt;
-
-    pdl_wait();
-    QSA_AFTER_WAIT(scores);
-    QSA_AFTER_WAIT(q_pos);
-    QSA_AFTER_WAIT(ext_hist);
-    QSA_AFTER_WAIT(pre_meta);
-    QSA_AFTER_WAIT(pre_bitmap);
-    QSA_AFTER_WAIT(pre_cand);
-    QSA_AFTER_WAIT(pre_cnt);
-    pdl_trigger();
-
-    const int64_t p = q_pos ? (int64_t)q_pos[qi] : n_ctx - 1;  // the query's position
-    int64_t n = n_full_cap;
-    if (q_pos) {
-        const int64_t p1 = (p + 1) / 4;
-        n = p1 < n ? p1 : n;
+    const int64_t wpt = (nw + NT - 1) / NT;
+    const int64_t w0 = (int64_t)threadIdx.x * wpt;
+    const int64_t w1 = w0 + wpt < nw ? w0 + wpt : nw;
+    uint32_t tot;
+    uint32_t n_sel = 0;
+    if (eqw) {
+        uint32_t n_eq = 0;
+        for (int64_t w = w0; w < w1; ++w) n_eq += __popc(eqw[w]);
+        uint32_t eq_before = block_excl_scan(n_eq, warp_s, &tot);
+        for (int64_t w = w0; w < w1; ++w) {
+            uint32_t e = eqw[w];
+            uint32_t keep = 0;
+            while (e && eq_before < k_rem) {
+                const uint32_t bit = e & (0u - e);
+                keep |= bit;
+                e ^= bit;
+                ++eq_before;
+            }
+            const uint32_t f = selw[w] | keep;
+            selw[w] = f;
+            n_sel += __popc(f);
+        }
+    } else {
+        for (int64_t w = w0; w < w1; ++w) n_sel += __popc(selw[w]);
     }
-    if (n < 0) n = 0;
-    const int64_t k = (int64_t)k_blk < n ? (int64_t)k_blk : n;
-    int32_t *out = blocks_out + qi * (int64_t)k_blk;
-    int32_t *pout = pos_out ? pos_out + qi * max_cells : nullptr;
-    const bool pvec = (reinterpret_cast<uintptr_t>(pout) & 15) == 0;
-    uint32_t *ehist = ext_hist ? ext_hist + qi * (int64_t)kBins1 : nullptr;
+    uint32_t o = block_excl_scan(n_sel, warp_s + NT / 32, &tot);
+    for (int64_t w = w0; w < w1; ++w) {
+        uint32_t f = selw[w];
+        while (f) {
+            const int b = __ffs(f) - 1;
+            f &= f - 1;
+            const int32_t blk = (int32_t)(32 * w + b);
+            if (o < (uint32_t)k) {
+                out[o] = blk;
+                if (pout) put_cells(pout + 4 * o, blk, pvec);
+            }
+            ++o;
+        }
+    }
+}
+
+// Counts and the open tail of one query (threads 0-3 of the CTA).
+__device__ __forceinline__ void write_count_tail(int64_t k, int64_t p, int32_t *count_out,
+                                                 int32_t *pout, int32_t *n_cells_out)
+{
     if (threadIdx.x < 4) {
         const int64_t tail0 = 4 * ((p + 1) / 4);
         const int64_t n_tail = p + 1 - tail0;
-        if (threadIdx.x == 0) counts_out[qi] = (int32_t)k;
+        if (threadIdx.x == 0) *count_out = (int32_t)k;
         if (pout) {
-            if (threadIdx.x == 0) n_cells_out[qi] = (int32_t)(4 * k + n_tail);
+            if (threadIdx.x == 0) *n_cells_out = (int32_t)(4 * k + n_tail);
             if (threadIdx.x < n_tail) pout[4 * k + threadIdx.x] = (int32_t)(tail0 + threadIdx.x);
         }
     }
-    if (n <= k_blk) {  // every candidate is selected
-        for (int64_t i = threadIdx.x; i < n; i += NT) {
-            out[i] = (int32_t)i;
-            if (pout) put_cells(pout + 4 * i, (int32_t)i, pvec);
-        }
-        if (ehist)  // leave the histogram cleared for the next step
-            for (int i = threadIdx.x; i < kBins1; i += NT) ehist[i] = 0u;
-        return;
-    }
+}
+
+// The general form for one query whose n candidates outnumber k (steps 1-5).  smem:
+// hist [4096] | warp_s [2][32] | misc [32] | selw [nw] | eqw [nw] | keys [cap] | idx [cap].
+// ehist (nullable): the score kernel's histogram of this query, cleared here.
+__device__ void topk_query(const float *srow, int64_t n, int64_t k, int32_t *out, int32_t *pout,
+                           bool pvec, uint32_t *ehist, int cand_cap, uint32_t *smem)
+{
+    uint32_t *hist = smem;
+    uint32_t *warp_s = hist + kBins1;
+    uint32_t *misc = warp_s + 2 * (NT / 32);
+    uint32_t *selw = misc + 32;
     const int64_t nw = (n + 31) / 32;
-    uint32_t *eqw = selw + nw;                               // [nw] tie bitmap
-    uint32_t *cand_key = eqw + nw;                           // [cand_cap]
+    uint32_t *eqw = selw + nw;
+    uint32_t *cand_key = eqw + nw;
     int32_t *cand_idx = reinterpret_cast<int32_t *>(cand_key + cand_cap);
-    const float *srow = scores + qi * ld;
 
-    uint32_t prefix = 0, k_rem = 0;
-    int fixed = kTopkHistBits;
-    bool whole = false;
-    bool pre_ok = false;
-    if (pre_meta) {
-        // ---- 1-2 done by the classify pass: take its decision, bitmap and candidates
-        const int c = threadIdx.x;
-        uint32_t my = 0;
-        bool over = false;
-        if (c < pre.n_cta) {
-            my = (uint32_t)pre_cnt[c];
-            over = my > (uint32_t)pre.cap;
+    // ---- 1. histogram of the top 12 bits: take the one the score kernel accumulated
+    // (and clear it for the next step) unless its total disagrees with the candidate
+    // count -- a workspace that was never cleared -- in which case build it here
+    bool have = false;
+    if (ehist) {
+        uint32_t part = 0;
+        for (int i = threadIdx.x; i < kBins1; i += NT) {
+            const uint32_t v = ehist[i];
+            hist[i] = v;
+            ehist[i] = 0u;
+            part += v;
         }
-        const bool any_over = __syncthreads_or(over);
-        uint32_t n_cand;
-        const uint32_t cbase = block_excl_scan(my, warp_s, &n_cand);
-        pre_ok = pre_meta[3] != 0 && !any_over && n_cand <= (uint32_t)cand_cap;
-        if (pre_ok) {
-            prefix = pre_meta[0];
-            k_rem = (uint32_t)k - pre_meta[1];
-            whole = pre_meta[2] != 0;
-            for (int64_t w = threadIdx.x; w < nw; w += NT) {
-                selw[w] = pre_bitmap[w];
-                eqw[w] = 0u;
-            }
-            for (uint32_t j = 0; j < my; ++j) {
-                const uint2 e = pre_cand[(int64_t)c * pre.cap + j];
-                cand_key[cbase + j] = e.x;
-                cand_idx[cbase + j] = (int32_t)e.y;
-            }
-            if (threadIdx.x == 0) misc[8] = n_cand;
-        }
-        if (ehist)  // leave the histogram cleared for the next step
-            for (int i = threadIdx.x; i < kBins1; i += NT) ehist[i] = 0u;
-        __syncthreads();
+        uint32_t tot;
+        block_excl_scan(part, warp_s, &tot);
+        have = tot == (uint32_t)n;
     }
-    if (!pre_ok) {
-        // ---- 1. histogram of the top 12 bits: take the one the score kernel accumulated
-        // (and clear it for the next step) unless its total disagrees with the candidate
-        // count -- a workspace that was never cleared -- in which case build it here
-        bool have = false;
-        if (ehist && !pre_meta) {
-            uint32_t part = 0;
-            for (int i = threadIdx.x; i < kBins1; i += NT) {
-                const uint32_t v = ehist[i];
-                hist[i] = v;
-                ehist[i] = 0u;
-                part += v;
-            }
-            uint32_t tot;
-            block_excl_scan(part, warp_s, &tot);
-            have = tot == (uint32_t)n;
-        }
-        if (!have) {
-            for (int i = threadIdx.x; i < kBins1; i += NT) hist[i] = 0u;
-            __syncthreads();
-            for_each_key(srow, n, [&](uint32_t key, int64_t) {
-                atomicAdd(&hist[key >> (32 - kTopkHistBits)], 1u);
-            });
-        }
-        for (int64_t i = threadIdx.x; i < 2 * nw; i += NT) selw[i] = 0u;
-        if (threadIdx.x == 0) misc[8] = 0u;  // candidate count
+    if (!have) {
+        for (int i = threadIdx.x; i < kBins1; i += NT) hist[i] = 0u;
         __syncthreads();
-        find_bucket(hist, kBins1, (uint32_t)k, warp_s, misc);
-        prefix = misc[0];
-        k_rem = (uint32_t)k - misc[1];
-        whole = misc[2] == k_rem;
-        __syncthreads();
-
-        // ---- 2. classify every candidate (one read)
-        const uint32_t B1c = prefix;
-        const uint32_t lo_key = B1c << (32 - kTopkHistBits);  // smallest key with digit B1
-        for_each_key(srow, n, [&](uint32_t key, int64_t i) {
-            if (key < lo_key) return;  // below the threshold bucket: the common case
-            const uint32_t d = key >> (32 - kTopkHistBits);
-            if (d > B1c || whole) {
-                atomicOr(&selw[i >> 5], 1u << (i & 31));
-            } else {
-                const uint32_t slot = atomicAdd(&misc[8], 1u);
-                if (slot < (uint32_t)cand_cap) {
-                    cand_key[slot] = key;
-                    cand_idx[slot] = (int32_t)i;
-                }
-            }
+        for_each_key(srow, n, [&](uint32_t key, int64_t) {
+            atomicAdd(&hist[key >> (32 - kTopkHistBits)], 1u);
         });
-        __syncthreads();
     }
+    for (int64_t i = threadIdx.x; i < 2 * nw; i += NT) selw[i] = 0u;
+    if (threadIdx.x == 0) misc[8] = 0u;  // candidate count
+    __syncthreads();
+    find_bucket(hist, kBins1, (uint32_t)k, warp_s, misc);
+    uint32_t prefix = misc[0];
+    uint32_t k_rem = (uint32_t)k - misc[1];
+    const bool whole = misc[2] == k_rem;
+    int fixed = kTopkHistBits;
+    __syncthreads();
+
+    // ---- 2. classify every candidate (one read)
     const uint32_t B1 = prefix;
+    const uint32_t lo_key = B1 << (32 - kTopkHistBits);  // smallest key with digit B1
+    for_each_key(srow, n, [&](uint32_t key, int64_t i) {
+        if (key < lo_key) return;  // below the threshold bucket: the common case
+        const uint32_t d = key >> (32 - kTopkHistBits);
+        if (d > B1 || whole) {
+            atomicOr(&selw[i >> 5], 1u << (i & 31));
+        } else {
+            const uint32_t slot = atomicAdd(&misc[8], 1u);
+            if (slot < (uint32_t)cand_cap) {
+                cand_key[slot] = key;
+                cand_idx[slot] = (int32_t)i;
+            }
+        }
+    });
+    __syncthreads();
 
     if (!whole) {
         const uint32_t n_cand = misc[8];
@@ -353,107 +339,228 @@ topk_kernel(const float *__restrict__ scores, int64_t ld, const int32_t *__restr
         k_rem = 0;
     }
 
-    // ---- 5. ordered output: ties lowest index first, then a scan over bitmap words
-    const int64_t wpt = (nw + NT - 1) / NT;
-    const int64_t w0 = (int64_t)threadIdx.x * wpt;
-    const int64_t w1 = w0 + wpt < nw ? w0 + wpt : nw;
-    uint32_t n_eq = 0;
-    for (int64_t w = w0; w < w1; ++w) n_eq += __popc(eqw[w]);
-    uint32_t tot;
-    uint32_t eq_before = block_excl_scan(n_eq, warp_s, &tot);
-    uint32_t n_sel = 0;
-    for (int64_t w = w0; w < w1; ++w) {
-        uint32_t e = eqw[w];
-        uint32_t keep = 0;
-        while (e && eq_before < k_rem) {
-            const uint32_t bit = e & (0u - e);
-            keep |= bit;
-            e ^= bit;
-            ++eq_before;
-        }
-        const uint32_t f = selw[w] | keep;
-        selw[w] = f;
-        n_sel += __popc(f);
-    }
-    uint32_t o = block_excl_scan(n_sel, warp_s + NT / 32, &tot);
-    for (int64_t w = w0; w < w1; ++w) {
-        uint32_t f = selw[w];
-        while (f) {
-            const int b = __ffs(f) - 1;
-            f &= f - 1;
-            const int32_t blk = (int32_t)(32 * w + b);
-            if (o < (uint32_t)k) {
-                out[o] = blk;
-                if (pout) put_cells(pout + 4 * o, blk, pvec);
-            }
-            ++o;
-        }
-    }
+    // ---- 5. ordered output
+    write_selection(selw, eqw, nw, k_rem, k, out, pout, pvec, warp_s);
 }
 
-// Classify pass (decode, one query): every CTA derives the threshold digit from the score
-// kernel's histogram, then one warp per bitmap word classifies 32 consecutive blocks with
-// two ballots -- the word of blocks above the threshold bucket is written as is, blocks
-// inside it are appended to this CTA's candidate list.  CTA 0 publishes the decision.
 __global__ void __launch_bounds__(NT)
-topk_classify_kernel(const float *__restrict__ scores, int64_t n, int64_t k,
-                     const uint32_t *__restrict__ hist, uint32_t *__restrict__ meta,
-                     uint32_t *__restrict__ bitmap, uint2 *__restrict__ cand,
-                     int32_t *__restrict__ cand_cnt, int cap)
+topk_kernel(const float *__restrict__ scores, int64_t ld, const int32_t *__restrict__ q_pos,
+            int64_t n_full_cap, int k_blk, int32_t *__restrict__ blocks_out,
+            int32_t *__restrict__ counts_out, int64_t n_ctx, int32_t *__restrict__ pos_out,
+            int32_t *__restrict__ n_cells_out, int64_t max_cells, uint32_t *__restrict__ ext_hist,
+            int cand_cap)
 {
-    __shared__ uint32_t h[kBins1];
-    __shared__ uint32_t warp_s[2 * (NT / 32)];
-    __shared__ uint32_t misc[32];
+    extern __shared__ __align__(16) uint32_t smem[];
+    const int64_t qi = blockIdx.x;
+    pdl_wait();
+    QSA_AFTER_WAIT(scores);
+    QSA_AFTER_WAIT(q_pos);
+    QSA_AFTER_WAIT(ext_hist);
+    pdl_trigger();
+
+    const int64_t p = q_pos ? (int64_t)q_pos[qi] : n_ctx - 1;  // the query's position
+    int64_t n = n_full_cap;
+    if (q_pos) {
+        const int64_t p1 = (p + 1) / 4;
+        n = p1 < n ? p1 : n;
+    }
+    if (n < 0) n = 0;
+    const int64_t k = (int64_t)k_blk < n ? (int64_t)k_blk : n;
+    int32_t *out = blocks_out + qi * (int64_t)k_blk;
+    int32_t *pout = pos_out ? pos_out + qi * max_cells : nullptr;
+    const bool pvec = (reinterpret_cast<uintptr_t>(pout) & 15) == 0;
+    uint32_t *ehist = ext_hist ? ext_hist + qi * (int64_t)kBins1 : nullptr;
+    write_count_tail(k, p, counts_out + qi, pout, n_cells_out ? n_cells_out + qi : nullptr);
+    if (n <= k_blk) {  // every candidate is selected
+        for (int64_t i = threadIdx.x; i < n; i += NT) {
+            out[i] = (int32_t)i;
+            if (pout) put_cells(pout + 4 * i, (int32_t)i, pvec);
+        }
+        if (ehist)  // leave the histogram cleared for the next step
+            for (int i = threadIdx.x; i < kBins1; i += NT) ehist[i] = 0u;
+        return;
+    }
+    topk_query(scores + qi * ld, n, k, out, pout, pvec, ehist, cand_cap, smem);
+}
+
+// The decode form (one query, n > k): see the file comment.  Grid ceil(n / 1024) CTAs of
+// 1024 threads; CTA c classifies blocks [1024c, 1024c + 1024).  hist: the score kernel's
+// histogram of the n full blocks; ticket: set to 0 by the score kernel of this step.
+// Scratch: bitmap [ceil(n/32)] words, cand [grid][1024] (key, block), cand_cnt [grid].
+__global__ void __launch_bounds__(NT)
+topk_select_kernel(const float *__restrict__ scores, int64_t n, int k_blk, int64_t n_ctx,
+                   uint32_t *__restrict__ hist, uint32_t *__restrict__ ticket,
+                   uint32_t *__restrict__ bitmap, uint2 *__restrict__ cand,
+                   int32_t *__restrict__ cand_cnt, int32_t *__restrict__ blocks_out,
+                   int32_t *__restrict__ counts_out, int32_t *__restrict__ pos_out,
+                   int32_t *__restrict__ n_cells_out, int cand_cap, const char *kv_k,
+                   const char *kv_v, uint32_t kv_block_bytes)
+{
+    extern __shared__ __align__(16) uint32_t smem[];
+    __shared__ uint32_t wtot[NT / 32];
+    __shared__ uint32_t sh[8];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0) sh[6] = 0u;  // this CTA's candidate count
     pdl_wait();
     QSA_AFTER_WAIT(scores);
     QSA_AFTER_WAIT(hist);
+    QSA_AFTER_WAIT(ticket);
+    QSA_AFTER_WAIT(bitmap);
+    QSA_AFTER_WAIT(cand);
+    QSA_AFTER_WAIT(cand_cnt);
+    QSA_AFTER_WAIT(kv_k);
+    QSA_AFTER_WAIT(kv_v);
     pdl_trigger();
-    uint32_t part = 0;
-    for (int i = threadIdx.x; i < kBins1; i += NT) {
-        const uint32_t v = hist[i];
-        h[i] = v;
-        part += v;
-    }
-    uint32_t tot;
-    block_excl_scan(part, warp_s, &tot);
-    if (threadIdx.x == 0) misc[8] = 0u;
-    if (tot != (uint32_t)n) {  // not this step's histogram: the resolve pass does it all
-        if (blockIdx.x == 0 && threadIdx.x == 0) meta[3] = 0u;
-        return;
-    }
-    find_bucket(h, kBins1, (uint32_t)k, warp_s, misc);
-    const uint32_t B1 = misc[0];
-    const uint32_t above_n = misc[1];
-    const bool whole = misc[2] == (uint32_t)k - above_n;
-    if (blockIdx.x == 0 && threadIdx.x == 0) {
-        meta[0] = B1;
-        meta[1] = above_n;
-        meta[2] = whole ? 1u : 0u;
-        meta[3] = 1u;
-    }
-    const int lane = threadIdx.x & 31;
+
+    const int64_t k = k_blk;
     const int64_t nw = (n + 31) / 32;
-    const int64_t wi = (int64_t)blockIdx.x * kClsWordsPerCta + (threadIdx.x >> 5);
-    if (wi < nw) {
-        const int64_t i = wi * 32 + lane;
-        const bool valid = i < n;
-        const uint32_t key = valid ? score_key(scores[i]) : 0u;
-        const uint32_t d = key >> (32 - kTopkHistBits);
-        const bool above = valid && (d > B1 || (whole && d == B1));
-        const bool is_cand = valid && !whole && d == B1;
-        const uint32_t word = __ballot_sync(0xffffffffu, above);
-        if (lane == 0) bitmap[wi] = word;
-        const uint32_t cm = __ballot_sync(0xffffffffu, is_cand);
-        uint32_t base = 0;
-        if (lane == 0 && cm) base = atomicAdd(&misc[8], (uint32_t)__popc(cm));
-        base = __shfl_sync(0xffffffffu, base, 0);
-        if (is_cand) {
-            const uint32_t slot = base + __popc(cm & ((1u << lane) - 1u));
-            if (slot < (uint32_t)cap) cand[(int64_t)blockIdx.x * cap + slot] = make_uint2(key, (uint32_t)i);
+    const int64_t i = (int64_t)blockIdx.x * NT + tid;  // this thread's block
+    const float sv = i < n ? scores[i] : 0.0f;
+    // ---- threshold bucket, two-level: thread t holds bins 4095-4t .. 4092-4t (top first)
+    uint32_t c[4], mine = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        c[j] = hist[kBins1 - 1 - 4 * tid - j];
+        mine += c[j];
+    }
+    uint32_t inc = mine;  // inclusive scan within the warp, top bins first
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += y;
+    }
+    if (lane == 31) wtot[warp] = inc;
+    __syncthreads();
+    if (warp == 0) {
+        const uint32_t w = wtot[lane];
+        uint32_t winc = w;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xffffffffu, winc, o);
+            if (lane >= o) winc += y;
+        }
+        const uint32_t ball = __ballot_sync(0xffffffffu, winc >= (uint32_t)k);
+        const int wl = ball ? __ffs(ball) - 1 : 0;
+        const uint32_t before = __shfl_sync(0xffffffffu, winc - w, wl);
+        const uint32_t total = __shfl_sync(0xffffffffu, winc, 31);
+        if (lane == 0) {
+            sh[0] = (total == (uint32_t)n && ball != 0u) ? 1u : 0u;  // the histogram is usable
+            sh[1] = (uint32_t)wl;
+            sh[2] = before;
         }
     }
     __syncthreads();
-    if (threadIdx.x == 0) cand_cnt[blockIdx.x] = (int32_t)misc[8];
+    const bool valid = sh[0] != 0u;
+    if (valid && warp == (int)sh[1]) {
+        uint32_t above = sh[2] + inc - mine;  // keys in the bins above this thread's
+        if (above < (uint32_t)k && above + mine >= (uint32_t)k) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                if (above + c[j] >= (uint32_t)k) {
+                    sh[3] = (uint32_t)(kBins1 - 1 - 4 * tid - j);
+                    sh[4] = above;
+                    sh[5] = c[j];
+                    break;
+                }
+                above += c[j];
+            }
+        }
+    }
+    __syncthreads();
+    const uint32_t B1 = sh[3], above_n = sh[4];
+    const uint32_t k_rem = (uint32_t)k - above_n;
+    const bool whole = valid && sh[5] == k_rem;
+
+    // ---- classify this CTA's 1024 blocks
+    const uint32_t key = score_key(sv);
+    const uint32_t dg = key >> (32 - kTopkHistBits);
+    const bool in = valid && i < n;
+    const bool above = in && (dg > B1 || (whole && dg == B1));
+    const bool is_cand = in && !whole && dg == B1;
+    // Blocks above the bucket are selected whatever the bucket resolves to: start pulling
+    // their K and V rows into L2 now, for the attention kernel that follows.
+    if (above && kv_k) {
+        prefetch_l2(kv_k + i * (int64_t)kv_block_bytes, kv_block_bytes);
+        prefetch_l2(kv_v + i * (int64_t)kv_block_bytes, kv_block_bytes);
+    }
+    const uint32_t word = __ballot_sync(0xffffffffu, above);
+    const int64_t wi = (int64_t)blockIdx.x * (NT / 32) + warp;
+    if (lane == 0 && wi < nw) bitmap[wi] = word;
+    const uint32_t cm = __ballot_sync(0xffffffffu, is_cand);
+    uint32_t base = 0;
+    if (lane == 0 && cm) base = atomicAdd(&sh[6], (uint32_t)__popc(cm));
+    base = __shfl_sync(0xffffffffu, base, 0);
+    if (is_cand)
+        cand[(int64_t)blockIdx.x * NT + base + __popc(cm & ((1u << lane) - 1u))] =
+            make_uint2(key, (uint32_t)i);
+    // Arrival: the barrier orders this CTA's writes before thread 0's device-scope fence,
+    // which publishes them before the ticket; the last arrival fences again before its
+    // threads read what the others wrote (the grid-barrier pattern, without the wait).
+    __syncthreads();
+    if (tid == 0) {
+        cand_cnt[blockIdx.x] = (int32_t)sh[6];
+        __threadfence();
+        sh[7] = atomicAdd(ticket, 1u) == gridDim.x - 1 ? 1u : 0u;
+        __threadfence();
+    }
+    __syncthreads();
+    if (!sh[7]) return;
+
+    // ---- the last CTA: every other CTA's bitmap words and candidates are visible
+    int32_t *pout = pos_out;
+    const bool pvec = (reinterpret_cast<uintptr_t>(pout) & 15) == 0;
+    write_count_tail(k, n_ctx - 1, counts_out, pout, n_cells_out);
+    // the general form's layout, its histogram area holding the candidates and the lists
+    // cp [1024]: candidates packed as key << 32 | ~block, so that one unsigned comparison
+    // orders them by key descending, then block ascending
+    unsigned long long *cp = reinterpret_cast<unsigned long long *>(smem);
+    uint32_t *lo = smem + 2 * NT;                               // [grid] list offsets
+    uint32_t *lc = smem + 3 * NT;                               // [grid] list lengths
+    uint32_t *warp_s = smem + kBins1;
+    uint32_t *selw = warp_s + 2 * (NT / 32) + 32;
+    uint32_t n_cand = 0;
+    if (valid) {
+        const int G = (int)gridDim.x;
+        const uint32_t my = tid < G ? (uint32_t)__ldcg(cand_cnt + tid) : 0u;
+        for (int64_t w = tid; w < nw; w += NT) selw[w] = __ldcg(bitmap + w);
+        const uint32_t off = block_excl_scan(my, warp_s, &n_cand);
+        if (tid < G) {
+            lo[tid] = off;
+            lc[tid] = my;
+        }
+        __syncthreads();
+        if (n_cand <= (uint32_t)NT) {
+            for (int cta = warp; cta < G; cta += NT / 32)
+                for (uint32_t j = lane; j < lc[cta]; j += 32) {
+                    const uint2 e = __ldcg(cand + (int64_t)cta * NT + j);
+                    cp[lo[cta] + j] = ((unsigned long long)e.x << 32) | (uint32_t)~e.y;
+                }
+            const uint32_t n8 = (n_cand + 7) & ~7u;  // padded with 0: below every candidate
+            if ((uint32_t)tid >= n_cand && (uint32_t)tid < n8) cp[tid] = 0ull;
+            __syncthreads();
+            // rank of each candidate: how many others order before it (broadcast reads,
+            // eight per step)
+            if ((uint32_t)tid < n_cand) {
+                const unsigned long long v = cp[tid];
+                uint32_t r = 0;
+                const ulonglong2 *c2 = reinterpret_cast<const ulonglong2 *>(cp);
+                for (uint32_t j = 0; j < n8 / 2; j += 4) {
+                    const ulonglong2 a = c2[j], b = c2[j + 1], c = c2[j + 2], e = c2[j + 3];
+                    r += (a.x > v) + (a.y > v) + (b.x > v) + (b.y > v) + (c.x > v) + (c.y > v) +
+                         (e.x > v) + (e.y > v);
+                }
+                const uint32_t it = ~(uint32_t)v;
+                if (r < k_rem) atomicOr(&selw[it >> 5], 1u << (it & 31));
+            }
+            __syncthreads();
+            write_selection(selw, nullptr, nw, 0u, k, blocks_out, pout, pvec, warp_s);
+            for (int j = tid; j < kBins1; j += NT) hist[j] = 0u;  // cleared for the next step
+            return;
+        }
+        __syncthreads();
+    }
+    // unusable histogram or an oversized bucket: the general form (clears the histogram)
+    topk_query(scores, n, k, blocks_out, pout, pvec, hist, cand_cap, smem);
 }
 
 size_t topk_smem_bytes(int64_t n, int *cand_cap)
@@ -467,57 +574,78 @@ size_t topk_smem_bytes(int64_t n, int *cand_cap)
     return sizeof(uint32_t) * (size_t)(words + 2 * cap);
 }
 
+cudaError_t set_max_smem()
+{
+    static bool done = false;
+    if (done) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kMaxSmemBytes);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(topk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kMaxSmemBytes);
+    if (e == cudaSuccess) done = true;
+    return e;
+}
+
 }  // namespace
 
 int64_t topk_max_candidates() { return kMaxN; }
 
-size_t topk_pre_workspace_bytes(int64_t n_full_cap)
+size_t topk_select_workspace_bytes(int64_t n_full_cap)
 {
     const int64_t nw = (n_full_cap + 31) / 32;
-    const int64_t g = (nw + kClsWordsPerCta - 1) / kClsWordsPerCta;
-    // meta (256 B) | counts | candidates | bitmap, each 256-byte aligned
+    const int64_t g = (n_full_cap + NT - 1) / NT;
+    // ticket (256 B) | counts | candidates | bitmap, each 256-byte aligned
     auto al = [](int64_t b) { return (b + 255) & ~(int64_t)255; };
-    return (size_t)(256 + al(4 * g) + al(8 * g * kClsCap) + al(4 * nw));
+    return (size_t)(256 + al(4 * g) + al(8 * g * NT) + al(4 * nw));
 }
 
-cudaError_t launch_topk_classify(const float *scores, int64_t n_full, int64_t k_blk,
-                                 const uint32_t *hist, uint32_t *meta, uint32_t *bitmap,
-                                 uint2 *cand, int32_t *cand_cnt, TopkPre *pre, cudaStream_t st)
+cudaError_t launch_topk_select(const float *scores, int64_t n_full, int64_t k_blk, int64_t n_ctx,
+                               uint32_t *hist, void *scratch, int32_t *blocks_out,
+                               int32_t *counts_out, int32_t *pos_out, int32_t *n_cells_out,
+                               const void *kv_k, const void *kv_v, int64_t kv_row_bytes,
+                               cudaStream_t st)
 {
+    if (n_full <= k_blk || n_full > kMaxN) return cudaErrorNotSupported;
+    if (!kv_k || !kv_v || kv_row_bytes <= 0 || kv_row_bytes % 16 || 4 * kv_row_bytes > (1 << 20) ||
+        (reinterpret_cast<uintptr_t>(kv_k) | reinterpret_cast<uintptr_t>(kv_v)) % 16)
+        kv_k = kv_v = nullptr;
     const int64_t nw = (n_full + 31) / 32;
-    const int64_t g = (nw + kClsWordsPerCta - 1) / kClsWordsPerCta;
-    if (n_full <= k_blk || g < 1 || g > NT) return cudaErrorNotSupported;
-    cudaError_t e = launch(topk_classify_kernel, dim3((unsigned)g), dim3(NT), 0, st, 1, scores,
-                           n_full, k_blk, hist, meta, bitmap, cand, cand_cnt, kClsCap);
+    const int64_t g = (n_full + NT - 1) / NT;
+    auto al = [](int64_t b) { return (b + 255) & ~(int64_t)255; };
+    char *b = static_cast<char *>(scratch);
+    uint32_t *ticket = reinterpret_cast<uint32_t *>(b);
+    int32_t *cand_cnt = reinterpret_cast<int32_t *>(b + 256);
+    uint2 *cand = reinterpret_cast<uint2 *>(b + 256 + al(4 * g));
+    uint32_t *bitmap = reinterpret_cast<uint32_t *>(b + 256 + al(4 * g) + al(8 * g * NT));
+    // Shared memory for the fast path and the general form without a candidate list (it
+    // re-reads the scores instead): every CTA of the grid carries this allocation, and a
+    // large one would shrink the L1 of SMs still running the score kernel.
+    const int cand_cap = 0;
+    const size_t smem = sizeof(uint32_t) * (size_t)(kFixedWords + 2 * nw);
+    cudaError_t e = set_max_smem();
     if (e != cudaSuccess) return e;
-    pre->meta = meta;
-    pre->bitmap = bitmap;
-    pre->cand = cand;
-    pre->cand_cnt = cand_cnt;
-    pre->n_cta = (int)g;
-    pre->cap = kClsCap;
-    return cudaSuccess;
+    return launch(topk_select_kernel, dim3((unsigned)g), dim3(NT), smem, st, 1, scores, n_full,
+                  (int)k_blk, n_ctx, hist, ticket, bitmap, cand, cand_cnt, blocks_out, counts_out,
+                  pos_out, n_cells_out, cand_cap, (const char *)kv_k, (const char *)kv_v,
+                  (uint32_t)(4 * kv_row_bytes));
 }
+
+uint32_t *topk_select_ticket(void *scratch) { return static_cast<uint32_t *>(scratch); }
 
 cudaError_t launch_topk(const float *scores, int64_t n_q, int64_t ld, const int32_t *q_pos,
                         int64_t n_full, int64_t k_blk, int32_t *blocks_out, int32_t *counts_out,
                         int64_t n_ctx, int32_t *pos_out, int32_t *n_cells_out,
-                        int64_t max_cells, uint32_t *ext_hist, cudaStream_t st,
-                        const TopkPre &pre)
+                        int64_t max_cells, uint32_t *ext_hist, cudaStream_t st)
 {
     if (n_q == 0) return cudaSuccess;
     int cand_cap = 0;
     const size_t smem = topk_smem_bytes(n_full, &cand_cap);
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             kMaxSmemBytes);
-        if (e != cudaSuccess) return e;
-        attr = true;
-    }
+    cudaError_t e = set_max_smem();
+    if (e != cudaSuccess) return e;
     return launch(topk_kernel, dim3((unsigned)n_q), dim3(NT), smem, st, 1, scores, ld, q_pos,
                   n_full, (int)k_blk, blocks_out, counts_out, n_ctx, pos_out, n_cells_out,
-                  max_cells, ext_hist, cand_cap, pre);
+                  max_cells, ext_hist, cand_cap);
 }
 
 }  // namespace qsa
