@@ -15,7 +15,7 @@
 // cell.  P.V: each thread owns G*d_v/128 output entries.  fp32 throughout.
 #include <cooperative_groups.h>
 
-#include "qsa_internal.cuh"
+#include "mma_frag.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -24,8 +24,6 @@ namespace {
 
 constexpr int kAttnThreads = 128;
 constexpr int kTile = 32;
-constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kLn2 = 0.6931471805599453f;
 
 __device__ __forceinline__ void cp_async16(void *smem_dst, const void *gsrc, bool valid)
 {
@@ -511,43 +509,6 @@ size_t attn128_smem()
 // the same way for P.V.  Per 16 cells a warp issues 16 + 16 MMAs and 8 + 8 ldmatrix loads
 // (vs. ~2700 CUDA-core instructions).  K and V tiles live in shared memory with rows
 // padded to 272 bytes so that the 8 rows of every ldmatrix fall in distinct banks.
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi)
-{
-    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);  // .x = lo (low half), .y = hi
-    return *reinterpret_cast<uint32_t *>(&v);
-}
-
-__device__ __forceinline__ void split_bf16(float x, float &hi, float &lo)
-{
-    hi = __bfloat162float(__float2bfloat16_rn(x));
-    lo = x - hi;
-}
-
-__device__ __forceinline__ void mma_16816(float *c, const uint32_t *a, uint32_t b0, uint32_t b1)
-{
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-        "{%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ void ldsm_x4(uint32_t *r, const void *p)
-{
-    const unsigned s = (unsigned)__cvta_generic_to_shared(p);
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(s));
-}
-
-__device__ __forceinline__ void ldsm_x4_t(uint32_t *r, const void *p)
-{
-    const unsigned s = (unsigned)__cvta_generic_to_shared(p);
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(s));
-}
-
 constexpr int kMmaWarps = 8;
 constexpr int kMmaTC = 16 * kMmaWarps;  // cells per stage: 16 per warp
 constexpr int kMmaLd = 136;             // padded smem row in bf16 elements = 272 bytes
@@ -1108,6 +1069,9 @@ cudaError_t launch_sparse_attn(const float *q, int64_t n_q, int H_q, int H_kv, i
     if (n_q == 0) return cudaSuccess;
     const int S = attn_num_splits(n_q, H_kv, max_cells);
     const int G = H_q / H_kv;
+    if (attn_uses_wide(dt, d_k, d_v, G, K, V, ld_k, ld_v))
+        return launch_attn_wide(q, n_q, H_q, H_kv, scale, K, n_kv, ld_k, pos, n_cells, max_cells,
+                                out, lse, st);
     if (attn_uses_mma(dt, d_k, d_v, G))
         return launch_attn_mma(q, n_q, H_q, H_kv, scale, K, V, n_kv, ld_k, ld_v, pos, n_cells,
                                max_cells, out, lse, st, early_q);

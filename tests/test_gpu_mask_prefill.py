@@ -183,3 +183,62 @@ def test_prefill_chunk(dtype, depth, n_q, k_tokens, prec):
         np.testing.assert_allclose(g_out[i], want, rtol=0, atol=atol)
         checked += 1
     assert checked >= n_q - 2
+
+
+@pytest.mark.parametrize("n_q,lens", [(1, [2048]), (4, [0, 1, 65, 2048]), (3, [63, 64, 129]),
+                                      (160, None)])
+def test_latent_attention_list_lengths(n_q, lens):
+    """The latent-KV form (DKQ 576, d_v 512, 16 heads, V = first 512 columns of the K row)
+    over position lists of many lengths: empty, one cell, stage edges, a full list; 160
+    queries take the one-CTA-per-query path.  Every output against the oracle."""
+    n_kv, d_k, d_v, H, max_list = 5000, 576, 512, 16, 2048
+    rng = np.random.default_rng(n_q)
+    KV = qsa_synth.to_bf16_bits(rng.standard_normal((n_kv, d_k)).astype(np.float32))
+    q = rng.standard_normal((n_q, H, d_k)).astype(np.float32)
+    if lens is None:
+        lens = list(rng.integers(0, 300, size=n_q))
+    pos = np.full((n_q, max_list), -7, np.int32)
+    for i, L in enumerate(lens):
+        pos[i, :L] = np.sort(rng.choice(n_kv, size=L, replace=False))
+    counts = np.array(lens, np.int32)
+    out = torch.zeros((n_q, H, d_v), device="cuda")
+    lse = torch.zeros((n_q, H), device="cuda")
+    scale = 1.0 / math.sqrt(d_k)
+    kv = to_dev(KV)
+    ws_n = qsa.sparse_attn_workspace_size(n_q, H, 1, d_v, max_list)
+    ws = torch.empty(max(ws_n // 4, 1), device="cuda")
+    qsa.sparse_attn(to_dev(q), kv, kv, to_dev(counts), max_list, out, 1, d_k, d_v, scale,
+                    pos=to_dev(pos), lse=lse, workspace=ws, ld_k=d_k, ld_v=d_k)
+    g_out, g_lse = to_host(out), to_host(lse)
+    for i, L in enumerate(lens):
+        if L == 0:
+            assert np.all(g_out[i] == 0.0) and np.all(np.isneginf(g_lse[i]))
+            continue
+        want, want_lse = oracle.attention(q[i], KV, KV, H, 1, d_k, d_v, d_k, d_k, pos[i, :L],
+                                          scale)
+        np.testing.assert_allclose(g_out[i], want, rtol=0, atol=ATOL_ATTN_BF16)
+        np.testing.assert_allclose(g_lse[i], want_lse, rtol=1e-5, atol=1e-4)
+
+
+def test_dkq576_with_separate_values():
+    """DKQ 576 / d_v 512 with a V tensor of its own (not the K row's first columns): the
+    general attention kernel, against the oracle."""
+    n_kv, d_k, d_v, H, max_list, n_q = 3000, 576, 512, 16, 512, 2
+    rng = np.random.default_rng(99)
+    K = qsa_synth.to_bf16_bits(rng.standard_normal((n_kv, d_k)).astype(np.float32))
+    V = qsa_synth.to_bf16_bits(rng.standard_normal((n_kv, d_v)).astype(np.float32))
+    q = rng.standard_normal((n_q, H, d_k)).astype(np.float32)
+    lens = [300, 512]
+    pos = np.zeros((n_q, max_list), np.int32)
+    for i, L in enumerate(lens):
+        pos[i, :L] = np.sort(rng.choice(n_kv, size=L, replace=False))
+    out = torch.zeros((n_q, H, d_v), device="cuda")
+    ws_n = qsa.sparse_attn_workspace_size(n_q, H, 1, d_v, max_list)
+    ws = torch.empty(max(ws_n // 4, 1), device="cuda")
+    scale = 1.0 / math.sqrt(d_k)
+    qsa.sparse_attn(to_dev(q), to_dev(K), to_dev(V), to_dev(np.array(lens, np.int32)), max_list,
+                    out, 1, d_k, d_v, scale, pos=to_dev(pos), workspace=ws, ld_k=d_k, ld_v=d_v)
+    g_out = to_host(out)
+    for i, L in enumerate(lens):
+        want, _ = oracle.attention(q[i], K, V, H, 1, d_k, d_v, d_k, d_v, pos[i, :L], scale)
+        np.testing.assert_allclose(g_out[i], want, rtol=0, atol=ATOL_ATTN_BF16)
