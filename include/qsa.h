@@ -237,10 +237,10 @@ size_t qsa_sparse_attn_workspace_size(int64_t n_q, int H_q, int H_kv, int d_v,
  * is fused differently: when at most 4 pooled rows need recomputing (every decode step),
  * the score kernel recomputes them itself; it also counts the top 12 bits of each full
  * block's score key into a histogram kept in the workspace, which the top-k kernel
- * starts from (and clears for the next step); the top-k kernel writes the cell list
- * itself (a many-CTA classify pass over the scores, then one CTA that settles the
- * threshold bucket and orders the output), and the attention kernel reads the listed K/V
- * rows in place.
+ * starts from (and clears for the next step); the top-k is one kernel whose CTAs each
+ * classify 1024 blocks against that histogram and whose last CTA to finish settles the
+ * threshold bucket, orders the output and writes the cell list itself; the attention
+ * kernel reads the listed K/V rows in place.  Three launches in all.
  * workspace: qsa_decode_step_workspace_size() bytes, 256-byte aligned.  Its contents need
  * no initialisation: a histogram whose total disagrees with the block count (a workspace
  * never cleared) is rebuilt from the scores, which only makes that call slower; filling
