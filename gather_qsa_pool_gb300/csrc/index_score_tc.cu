@@ -9,40 +9,40 @@
 // so the chunk form -- every query of a 1024-token ubatch against 64k pooled rows, a
 // [1024 x 2048] x [2048 x 64052] contraction -- is this library's.
 //
-// Design (one CTA per SM, persistent over work items):
-//   - a work item is 512 queries x 128 pooled rows; its four 128 x 128 fp32 accumulators
-//     fill the SM's 512 tensor-memory columns;
-//   - the K = H*d reduction runs in stages of 64: the query tile (bf16, converted once by a
-//     prologue kernel) arrives by cp.async, the pooled tile (fp32 in HBM) is loaded into
-//     registers one stage ahead, rounded to bf16 (nearest even) and stored; both tiles use
-//     the 128-byte-swizzled K-major layout the MMA descriptors describe;
-//   - one thread issues 16 tcgen05.mma (4 accumulators x 4 k-steps of 16) per stage and
-//     commits them to the stage's mbarrier, which releases the buffer two stages later;
-//   - after the last stage a commit to a second mbarrier hands the accumulators to the
-//     epilogue: every warp reads its 32 tensor-memory lanes (tcgen05.ld), scales, masks and
-//     writes the scores.
-// Work items alternate the two query halves on the same pooled tile so that the second
-// read of each pooled tile is an L2 hit.  Every mbarrier wait is bounded: on a timeout the
-// kernel records an error word and stops issuing work (no hang), and it always returns its
-// tensor memory.
+// Design:
+//   - two prologue kernels round the queries and the pooled rows to bf16 (nearest even)
+//     into the workspace, so that both operands can be staged by TMA;
+//   - the score kernel is persistent, one CTA per SM, warp-specialised: warp 0 issues the
+//     TMA copies (query tile 128 x 64 and pooled tile 256 x 64 per stage, 128-byte
+//     swizzle, four stages in flight), warp 1 issues tcgen05.mma (M 128, N 256, K 16; four
+//     per stage) into one of two 256-column accumulators, and warps 2-5 drain the other
+//     accumulator (tcgen05.ld, scale, causal mask, store) while the next tile computes;
+//   - tiles are ordered query-block-fastest, so the CTAs working at the same time share a
+//     pooled tile and all but the first read it from L2;
+//   - every mbarrier wait is bounded (2 s): on a timeout the kernel records an error word,
+//     stops issuing, waits (bounded) for what it already issued, and always returns its
+//     tensor memory.
+#include <cuda.h>
+
 #include "qsa_internal.cuh"
 
 namespace qsa {
 namespace {
 
-constexpr int kTcThreads = 128;
-constexpr int kBM = 128;          // rows per MMA (queries)
-constexpr int kMT = 4;            // accumulators per work item (512 queries)
-constexpr int kBN = 128;          // pooled rows per work item
-constexpr int kBK = 64;           // k per stage (one 128-byte swizzle row of bf16)
-constexpr int kStages = 2;
-constexpr int kTileA = kMT * kBM * kBK * 2;  // 64 KB per stage
-constexpr int kTileB = kBN * kBK * 2;        // 16 KB per stage
-constexpr uint32_t kTmemCols = 512;
+constexpr int kTcWarps = 6;
+constexpr int kTcThreads = 32 * kTcWarps;
+constexpr int kBM = 128;     // queries per tile (MMA M)
+constexpr int kBN = 256;     // pooled rows per tile (MMA N)
+constexpr int kBK = 64;      // k per stage: one 128-byte swizzle row of bf16
+constexpr int kStages = 4;
+constexpr int kTileA = kBM * kBK * 2;  // 16 KB
+constexpr int kTileB = kBN * kBK * 2;  // 32 KB
+constexpr uint32_t kTmemCols = 512;    // two accumulators of 256 columns
+constexpr int kEpiThreads = 128;       // warps 2-5
 
 __host__ __device__ constexpr size_t tc_smem_bytes()
 {
-    return 1024 /* alignment slack */ + (size_t)kStages * (kTileA + kTileB) + 64;
+    return 1024 /* alignment slack */ + (size_t)kStages * (kTileA + kTileB) + 256;
 }
 
 // 64-bit shared-memory matrix descriptor of a K-major tile in the 128-byte swizzle:
@@ -59,8 +59,8 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr)
     return d;
 }
 
-// Instruction descriptor: fp32 accumulator, bf16 A and B, both K-major, N = 128, M = 128.
-__host__ __device__ constexpr uint32_t idesc_bf16_m128_n128()
+// Instruction descriptor: fp32 accumulator, bf16 A and B, both K-major, N = 256, M = 128.
+__host__ __device__ constexpr uint32_t idesc_bf16_m128_n256()
 {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kBN >> 3) << 17) |
            ((uint32_t)(kBM >> 4) << 24);
@@ -85,11 +85,20 @@ __device__ __forceinline__ void umma_commit(uint64_t *bar)
         : "memory");
 }
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool valid)
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
 {
-    const int n = valid ? 16 : 0;
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(n)
-                 : "memory");
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// 2-D tiled TMA load of the box at (x, y) into this CTA's shared memory.
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y,
+                                            uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
 }
 
 __device__ __forceinline__ uint32_t bf16x2(float lo, float hi)
@@ -114,34 +123,57 @@ q_to_bf16_kernel(const float *__restrict__ q, int64_t n_q, int64_t ld_q, int K,
     }
 }
 
+// Prologue: the pooled rows (fp32, contiguous, n4 float4) -> bf16, nearest even.
+__global__ void __launch_bounds__(256)
+rows_to_bf16_kernel(const float4 *__restrict__ src, int64_t n4, uint2 *__restrict__ dst)
+{
+    pdl_wait();
+    QSA_AFTER_WAIT(src);
+    pdl_trigger();
+    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n4;
+         e += (int64_t)gridDim.x * blockDim.x) {
+        const float4 v = ld_stream_f4(src + e);
+        dst[e] = make_uint2(bf16x2(v.x, v.y), bf16x2(v.z, v.w));
+    }
+}
+
 __global__ void __launch_bounds__(kTcThreads, 1)
-score_tc_kernel(const __nv_bfloat16 *__restrict__ qb, int64_t n_q,
-                const int32_t *__restrict__ q_pos, const float *__restrict__ pooled,
-                int64_t n_rows, int K, float scale, float *__restrict__ scores, int64_t ld_scores,
-                int *__restrict__ err)
+score_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                int64_t n_q, const int32_t *__restrict__ q_pos, int64_t n_rows, int K,
+                float scale, float *__restrict__ scores, int64_t ld_scores, int *__restrict__ err)
 {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     // 1024-byte aligned operand area (the swizzle is a function of address bits 4-9)
     unsigned char *base = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-    unsigned char *sA = base;                             // [kStages][kMT*kBM rows][128 B]
-    unsigned char *sB = base + kStages * kTileA;          // [kStages][kBN rows][128 B]
-    uint64_t *bar = reinterpret_cast<uint64_t *>(sB + kStages * kTileB);  // [kStages] + acc
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + kStages + 1);
+    unsigned char *sA = base;                              // [kStages][128 rows][128 B]
+    unsigned char *sB = base + kStages * kTileA;           // [kStages][256 rows][128 B]
+    uint64_t *full = reinterpret_cast<uint64_t *>(sB + kStages * kTileB);  // [kStages]
+    uint64_t *empty = full + kStages;                      // [kStages]
+    uint64_t *accf = empty + kStages;                      // [2] accumulator ready
+    uint64_t *acce = accf + 2;                             // [2] accumulator drained
+    uint64_t *drain = acce + 2;                            // every MMA issued has finished
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     pdl_wait();
-    QSA_AFTER_WAIT(qb);
     QSA_AFTER_WAIT(q_pos);
-    QSA_AFTER_WAIT(pooled);
     pdl_trigger();
 
     if (tid == 0) {
-        for (int s = 0; s <= kStages; ++s) mbar_init(&bar[s], 1);
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int j = 0; j < 2; ++j) {
+            mbar_init(&accf[j], 1);
+            mbar_init(&acce[j], kEpiThreads);
+        }
+        mbar_init(drain, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (warp == 0) {
+    if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          smem_u32(tmem_slot)),
                      "r"(kTmemCols)
@@ -153,182 +185,179 @@ score_tc_kernel(const __nv_bfloat16 *__restrict__ qb, int64_t n_q,
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     const uint32_t tmem = *tmem_slot;
 
-    const int64_t n_mb = (n_q + kMT * kBM - 1) / (kMT * kBM);
-    const int64_t n_nt = (n_rows + kBN - 1) / kBN;
-    const int64_t n_items = n_mb * n_nt;
+    const int64_t n_mb = (n_q + kBM - 1) / kBM;
+    const int64_t n_nb = (n_rows + kBN - 1) / kBN;
+    const int64_t n_units = n_mb * n_nb;
     const int n_k = K / kBK;
-    constexpr uint32_t idesc = idesc_bf16_m128_n128();
-
-    uint32_t use_count[kStages] = {0, 0};  // commits issued to each stage barrier
-    uint32_t acc_count = 0;
     bool ok = true;
 
-    // The pooled tile of a stage is 128 rows x 16 float4; thread tid loads float4
-    // f = j*128 + tid (row f/16, column group f%16): coalesced, one stage ahead.
-    float4 breg[kBK / 4];
-    auto load_b = [&](int64_t it, int ks) {
-        const int64_t n0b = (it / n_mb) * kBN;
-#pragma unroll
-        for (int j = 0; j < kBK / 4; ++j) {
-            const int f = j * kTcThreads + tid;
-            const int64_t row = n0b + (f >> 4);
-            breg[j] = row < n_rows
-                          ? ld_stream_f4(reinterpret_cast<const float4 *>(
-                                pooled + row * (int64_t)K + (int64_t)ks * kBK) + (f & 15))
-                          : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-    };
-    // Fill buffer sb with stage (it, ks): query tile by cp.async, pooled tile from the
-    // registers (fp32 -> bf16, nearest even), both in the 128-byte swizzle; then load the
-    // pooled registers of the following stage.
-    auto fill = [&](int sb, int64_t it, int ks) {
-        unsigned char *a_s = sA + sb * kTileA;
-        unsigned char *b_s = sB + sb * kTileB;
-        const int64_t m0 = (it % n_mb) * (kMT * kBM);
-        for (int e = tid; e < kMT * kBM * 8; e += kTcThreads) {
-            const int r = e >> 3, c = e & 7;
-            const int64_t qi = m0 + r;
-            const bool valid = qi < n_q;
-            const __nv_bfloat16 *src = qb + (valid ? qi : 0) * (int64_t)K + (int64_t)ks * kBK + c * 8;
-            cp_async16(smem_u32(a_s + r * 128 + ((c ^ (r & 7)) << 4)), src, valid);
-        }
-        asm volatile("cp.async.commit_group;" ::: "memory");
-#pragma unroll
-        for (int j = 0; j < kBK / 4; ++j) {
-            const int f = j * kTcThreads + tid;
-            const int r = f >> 4, c4 = f & 15;
-            const uint2 v = make_uint2(bf16x2(breg[j].x, breg[j].y), bf16x2(breg[j].z, breg[j].w));
-            *reinterpret_cast<uint2 *>(b_s + r * 128 + (((c4 >> 1) ^ (r & 7)) << 4) + (c4 & 1) * 8) = v;
-        }
-        int64_t nit = it;
-        int nks = ks + 1;
-        if (nks == n_k) {
-            nit = it + gridDim.x;
-            nks = 0;
-        }
-        if (nit < n_items) load_b(nit, nks);
-    };
-
-    // Pipeline over the flattened (work item, k stage) sequence of this CTA: the copies of
-    // stage g+1 are in flight while the tensor cores run stage g.
-    int64_t item = blockIdx.x;
-    const int64_t my_items = item < n_items ? (n_items - 1 - item) / gridDim.x + 1 : 0;
-    const int64_t n_stages = my_items * n_k;
-    if (n_stages > 0) {
-        load_b(item, 0);
-        fill(0, item, 0);
-    }
-    for (int64_t gs = 0; gs < n_stages && ok; ++gs) {
-        const int sb = (int)(gs % kStages);
-        const int ks = (int)(gs % n_k);
-        const int64_t it = blockIdx.x + (gs / n_k) * gridDim.x;
-        asm volatile("cp.async.wait_group 0;" ::: "memory");  // this stage's query tile
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        __syncthreads();
-        if (tid == 0) {
-            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-            const uint32_t a0 = smem_u32(sA + sb * kTileA), b0 = smem_u32(sB + sb * kTileB);
-#pragma unroll
-            for (int mt = 0; mt < kMT; ++mt) {
-#pragma unroll
-                for (int k16 = 0; k16 < kBK / 16; ++k16) {
-                    const uint64_t ad = sw128_desc(a0 + mt * (kBM * 128) + k16 * 32);
-                    const uint64_t bd = sw128_desc(b0 + k16 * 32);
-                    umma_bf16(tmem + mt * kBN, ad, bd, idesc, (ks > 0 || k16 > 0) ? 1u : 0u);
+    if (warp == 0) {
+        // ---- producer: one thread issues the TMA copies of every stage
+        if (lane == 0) {
+            uint32_t uses[kStages] = {0, 0, 0, 0};
+            int stage = 0;
+            for (int64_t u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+                const int m0 = (int)((u % n_mb) * kBM), n0 = (int)((u / n_mb) * kBN);
+                for (int kb = 0; kb < n_k; ++kb) {
+                    if (uses[stage] > 0 && !mbar_wait(&empty[stage], (uses[stage] - 1) & 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&full[stage], kTileA + kTileB);
+                    tma_load_2d(sA + stage * kTileA, &tmA, kb * kBK, m0, &full[stage]);
+                    tma_load_2d(sB + stage * kTileB, &tmB, kb * kBK, n0, &full[stage]);
+                    ++uses[stage];
+                    stage = stage + 1 == kStages ? 0 : stage + 1;
                 }
             }
-            umma_commit(&bar[sb]);
-            if (ks == n_k - 1) umma_commit(&bar[kStages]);
+            // every copy issued has landed before the CTA may retire
+            for (int s = 0; s < kStages; ++s)
+                if (uses[s] > 0 && !mbar_wait(&full[s], (uses[s] - 1) & 1u)) ok = false;
         }
-        ++use_count[sb];
-        // refill the other buffer with stage gs+1 once the MMAs that last read it are done
-        if (gs + 1 < n_stages) {
-            const int nb = (int)((gs + 1) % kStages);
-            if (use_count[nb] > 0 && !mbar_wait(&bar[nb], (use_count[nb] - 1) & 1)) ok = false;
-            if (__syncthreads_or(!ok)) {
-                ok = false;
-                break;
+    } else if (warp == 1) {
+        // ---- MMA issuer: one thread, accumulators alternate between the two TMEM halves
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_bf16_m128_n256();
+            uint32_t uses[kStages] = {0, 0, 0, 0};
+            int stage = 0;
+            int64_t t = 0;
+            for (int64_t u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++t) {
+                const int j = (int)(t & 1);
+                if (t >= 2 && !mbar_wait(&acce[j], (uint32_t)((t >> 1) - 1) & 1u)) {
+                    ok = false;
+                    break;
+                }
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                for (int kb = 0; kb < n_k; ++kb) {
+                    if (!mbar_wait(&full[stage], uses[stage] & 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                    const uint32_t a0 = smem_u32(sA + stage * kTileA);
+                    const uint32_t b0 = smem_u32(sB + stage * kTileB);
+#pragma unroll
+                    for (int k16 = 0; k16 < kBK / 16; ++k16)
+                        umma_bf16(tmem + (uint32_t)(j * kBN), sw128_desc(a0 + k16 * 32),
+                                  sw128_desc(b0 + k16 * 32), idesc, (kb | k16) ? 1u : 0u);
+                    umma_commit(&empty[stage]);  // the stage is free once these MMAs finish
+                    ++uses[stage];
+                    stage = stage + 1 == kStages ? 0 : stage + 1;
+                }
+                if (!ok) break;
+                umma_commit(&accf[j]);
             }
-            if (ks + 1 < n_k) fill(nb, it, ks + 1);
-            else fill(nb, it + gridDim.x, 0);
+            umma_commit(drain);
+            if (!mbar_wait(drain, 0)) ok = false;
         }
-        if (ks == n_k - 1) {
-            // epilogue of work item `it`: wait for its accumulators, read this warp's lanes
-            const int64_t m0 = (it % n_mb) * (kMT * kBM), n0 = (it / n_mb) * kBN;
-            if (!mbar_wait(&bar[kStages], acc_count & 1)) ok = false;
-            ++acc_count;
-            if (__syncthreads_or(!ok)) {
+    } else {
+        // ---- epilogue: warp w reads tensor-memory lanes 32*(w%4) .. +31 (its queries)
+        const int quarter = warp & 3;
+        int64_t t = 0;
+        for (int64_t u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++t) {
+            const int j = (int)(t & 1);
+            if (!mbar_wait(&accf[j], (uint32_t)(t >> 1) & 1u)) {
                 ok = false;
                 break;
             }
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            const int64_t m0 = (u % n_mb) * kBM, n0 = (u / n_mb) * kBN;
+            const int64_t qi = m0 + quarter * 32 + lane;
+            const int64_t p = (qi < n_q && q_pos) ? (int64_t)q_pos[qi] : INT64_MAX;
 #pragma unroll 1
-            for (int mt = 0; mt < kMT; ++mt) {
-                const int64_t qi = m0 + mt * kBM + warp * 32 + lane;
-                const int64_t p = (qi < n_q && q_pos) ? (int64_t)q_pos[qi] : INT64_MAX;
-#pragma unroll 1
-                for (int cc = 0; cc < kBN / 32; ++cc) {
-                    uint32_t v[32];
-                    const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(mt * kBN + cc * 32);
-                    asm volatile(
-                        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-                        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-                        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-                        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]),
-                          "=r"(v[6]), "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]),
-                          "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]),
-                          "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]),
-                          "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]),
-                          "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
-                        : "r"(taddr));
-                    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-                    if (qi < n_q) {
-                        float *dst = scores + qi * ld_scores + n0 + cc * 32;
-                        const int64_t b0 = n0 + cc * 32;
-                        float o[32];
+            for (int cc = 0; cc < kBN / 32; ++cc) {
+                uint32_t v[32];
+                const uint32_t taddr =
+                    tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(j * kBN + cc * 32);
+                asm volatile(
+                    "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+                    "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+                    "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+                    : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]),
+                      "=r"(v[6]), "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]),
+                      "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]),
+                      "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]),
+                      "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]),
+                      "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+                    : "r"(taddr));
+                asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+                if (qi < n_q) {
+                    float *dst = scores + qi * ld_scores + n0 + cc * 32;
+                    const int64_t b0 = n0 + cc * 32;
+                    float o[32];
 #pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            o[j] = 4 * (b0 + j) + 3 <= p ? __uint_as_float(v[j]) * scale : -INFINITY;
-                        if (b0 + 32 <= n_rows && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
+                    for (int e = 0; e < 32; ++e)
+                        o[e] = 4 * (b0 + e) + 3 <= p ? __uint_as_float(v[e]) * scale : -INFINITY;
+                    if (b0 + 32 <= n_rows && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
 #pragma unroll
-                            for (int j = 0; j < 32; j += 4)
-                                *reinterpret_cast<float4 *>(dst + j) = make_float4(o[j], o[j + 1], o[j + 2], o[j + 3]);
-                        } else {
+                        for (int e = 0; e < 32; e += 4)
+                            *reinterpret_cast<float4 *>(dst + e) =
+                                make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
+                    } else {
 #pragma unroll
-                            for (int j = 0; j < 32; ++j)
-                                if (b0 + j < n_rows) dst[j] = o[j];
-                        }
+                        for (int e = 0; e < 32; ++e)
+                            if (b0 + e < n_rows) dst[e] = o[e];
                     }
                 }
             }
             asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-            __syncthreads();  // accumulators read: the next item's MMAs may overwrite them
+            mbar_arrive(&acce[j]);  // this half of tensor memory may be overwritten
         }
     }
-    if (!ok && tid == 0) atomicExch(err, 1);
-    // drain: the last commits must have landed before tensor memory is returned
-    __syncthreads();
-    if (tid == 0) {
-        for (int s = 0; s < kStages; ++s)
-            if (use_count[s] > 0) mbar_wait(&bar[s], (use_count[s] - 1) & 1);
-    }
+
+    if (!ok) atomicExch(err, 1);
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncthreads();
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-    if (warp == 0)
+    if (warp == 1)
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                      "r"(kTmemCols)
                      : "memory");
 }
 
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled()
+{
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+// Tensor map of a row-major bf16 matrix [rows][K]: boxes of 64 x box_rows, 128-byte
+// swizzle, zero fill outside the matrix.
+bool make_map(CUtensorMap *m, const void *base, int64_t rows, int K, uint32_t box_rows)
+{
+    EncodeTiledFn fn = encode_tiled();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)kBK, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+size_t al256(size_t b) { return (b + 255) & ~(size_t)255; }
+
 }  // namespace
 
 size_t index_score_tc_workspace(int64_t n_q, int64_t n_rows, int H, int d)
 {
-    (void)n_rows;
-    // bf16 copy of the queries, then one error word (256-byte aligned)
-    const size_t qb = ((size_t)n_q * (size_t)H * (size_t)d * 2 + 255) & ~(size_t)255;
-    return qb + 256;
+    // bf16 copies of the queries and of the pooled rows, then one error word
+    const size_t K = (size_t)H * (size_t)d;
+    return al256((size_t)n_q * K * 2) + al256((size_t)n_rows * K * 2) + 256;
 }
 
 qsa_status launch_index_score_tc(const float *q, int64_t n_q, int64_t ld_q,
@@ -341,11 +370,22 @@ qsa_status launch_index_score_tc(const float *q, int64_t n_q, int64_t ld_q,
     if ((reinterpret_cast<uintptr_t>(pooled) & 15) || (reinterpret_cast<uintptr_t>(workspace) & 255))
         return QSA_ERR_INVALID_ARG;
     if (n_q == 0 || n_rows == 0) return QSA_OK;
+    if (n_q > 0x7fffffffLL || n_rows > 0x7fffffffLL) return QSA_ERR_UNSUPPORTED;
     const size_t need = index_score_tc_workspace(n_q, n_rows, H, d);
     if (ws_bytes < need) return QSA_ERR_INVALID_ARG;
-    __nv_bfloat16 *qb = static_cast<__nv_bfloat16 *>(workspace);
-    int *err = reinterpret_cast<int *>(static_cast<char *>(workspace) + need - 256);
+    char *ws = static_cast<char *>(workspace);
+    __nv_bfloat16 *qb = reinterpret_cast<__nv_bfloat16 *>(ws);
+    __nv_bfloat16 *pb = reinterpret_cast<__nv_bfloat16 *>(ws + al256((size_t)n_q * K * 2));
+    int *err = reinterpret_cast<int *>(ws + need - 256);
+    CUtensorMap tmA, tmB;
+    if (!make_map(&tmA, qb, n_q, K, kBM) || !make_map(&tmB, pb, n_rows, K, kBN))
+        return QSA_ERR_CUDA;
     cudaError_t e = launch(q_to_bf16_kernel, dim3(1024), dim3(256), 0, st, 1, q, n_q, ld_q, K, qb);
+    if (e == cudaSuccess) {
+        const int64_t n4 = n_rows * (int64_t)K / 4;
+        e = launch(rows_to_bf16_kernel, dim3((unsigned)(device_sm_count() * 8)), dim3(256), 0, st,
+                   1, reinterpret_cast<const float4 *>(pooled), n4, reinterpret_cast<uint2 *>(pb));
+    }
     if (e != cudaSuccess) return QSA_ERR_CUDA;
     static bool attr = false;
     if (!attr) {
@@ -354,12 +394,11 @@ qsa_status launch_index_score_tc(const float *q, int64_t n_q, int64_t ld_q,
             return QSA_ERR_CUDA;
         attr = true;
     }
-    const int64_t n_items = ((n_q + kMT * kBM - 1) / (kMT * kBM)) * ((n_rows + kBN - 1) / kBN);
+    const int64_t n_units = ((n_q + kBM - 1) / kBM) * ((n_rows + kBN - 1) / kBN);
     int64_t grid = device_sm_count();
-    if (grid > n_items) grid = n_items;
+    if (grid > n_units) grid = n_units;
     e = launch(score_tc_kernel, dim3((unsigned)grid), dim3(kTcThreads), tc_smem_bytes(), st, 1,
-               (const __nv_bfloat16 *)qb, n_q, q_pos, pooled, n_rows, K, scale, scores, ld_scores,
-               err);
+               tmA, tmB, n_q, q_pos, n_rows, K, scale, scores, ld_scores, err);
     return e == cudaSuccess ? QSA_OK : QSA_ERR_CUDA;
 }
 
