@@ -535,24 +535,50 @@ topk_select_kernel(const float *__restrict__ scores, int64_t n, int k_blk, int64
                     const uint2 e = __ldcg(cand + (int64_t)cta * NT + j);
                     cp[lo[cta] + j] = ((unsigned long long)e.x << 32) | (uint32_t)~e.y;
                 }
-            const uint32_t n8 = (n_cand + 7) & ~7u;  // padded with 0: below every candidate
-            if ((uint32_t)tid >= n_cand && (uint32_t)tid < n8) cp[tid] = 0ull;
             __syncthreads();
-            // rank of each candidate: how many others order before it (broadcast reads,
-            // eight per step)
-            if ((uint32_t)tid < n_cand) {
-                const unsigned long long v = cp[tid];
-                uint32_t r = 0;
-                const ulonglong2 *c2 = reinterpret_cast<const ulonglong2 *>(cp);
-                for (uint32_t j = 0; j < n8 / 2; j += 4) {
-                    const ulonglong2 a = c2[j], b = c2[j + 1], c = c2[j + 2], e = c2[j + 3];
-                    r += (a.x > v) + (a.y > v) + (b.x > v) + (b.y > v) + (c.x > v) + (c.y > v) +
-                         (e.x > v) + (e.y > v);
+            // Second digit (key bits 12-19) over the candidates: a 256-bin histogram, then
+            // the bin holding the k_rem-th; candidates above it are in, the ones inside it
+            // (few) are ranked against each other by (key, index).
+            uint32_t *h2 = lo;                                     // [256]
+            uint32_t *sub = lc;                                    // [n_cand] indices into cp
+            if (tid < 256) h2[tid] = 0u;
+            if (tid == 0) sh[5] = 0u;
+            __syncthreads();
+            if ((uint32_t)tid < n_cand) atomicAdd(&h2[(uint32_t)(cp[tid] >> 44) & 255u], 1u);
+            __syncthreads();
+            {
+                const uint32_t c2n = tid < 256 ? h2[255 - tid] : 0u;  // top bin first
+                uint32_t tot;
+                const uint32_t above2 = block_excl_scan(c2n, warp_s, &tot);
+                if (tid < 256 && above2 < k_rem && above2 + c2n >= k_rem) {
+                    sh[0] = 255u - (uint32_t)tid;
+                    sh[1] = above2;
+                    sh[2] = c2n;
                 }
-                const uint32_t it = ~(uint32_t)v;
-                if (r < k_rem) atomicOr(&selw[it >> 5], 1u << (it & 31));
             }
             __syncthreads();
+            const uint32_t F = sh[0], k_rem2 = k_rem - sh[1];
+            const bool whole2 = sh[2] == k_rem2;
+            if ((uint32_t)tid < n_cand) {
+                const unsigned long long v = cp[tid];
+                const uint32_t d2 = (uint32_t)(v >> 44) & 255u, it = ~(uint32_t)v;
+                if (d2 > F || (whole2 && d2 == F)) atomicOr(&selw[it >> 5], 1u << (it & 31));
+                else if (d2 == F) sub[atomicAdd(&sh[5], 1u)] = (uint32_t)tid;
+            }
+            __syncthreads();
+            if (!whole2) {
+                const uint32_t m = sh[5];
+                if ((uint32_t)tid < m) {
+                    const unsigned long long v = cp[sub[tid]];
+                    uint32_t r = 0;
+                    for (uint32_t j = 0; j < m; ++j) r += cp[sub[j]] > v ? 1u : 0u;
+                    if (r < k_rem2) {
+                        const uint32_t it = ~(uint32_t)v;
+                        atomicOr(&selw[it >> 5], 1u << (it & 31));
+                    }
+                }
+                __syncthreads();
+            }
             write_selection(selw, nullptr, nw, 0u, k, blocks_out, pout, pvec, warp_s);
             for (int j = tid; j < kBins1; j += NT) hist[j] = 0u;  // cleared for the next step
             return;
