@@ -493,15 +493,18 @@ topk_select_kernel(const float *__restrict__ scores, int64_t n, int k_blk, int64
     if (is_cand)
         cand[(int64_t)blockIdx.x * NT + base + __popc(cm & ((1u << lane) - 1u))] =
             make_uint2(key, (uint32_t)i);
-    // Arrival: the barrier orders this CTA's writes before thread 0's device-scope fence,
-    // which publishes them before the ticket; the last arrival fences again before its
-    // threads read what the others wrote (the grid-barrier pattern, without the wait).
+    // Arrival: the barrier orders this CTA's writes before thread 0's ticket, an
+    // acquire-release atomic at device scope: it publishes them, and the last arrival
+    // acquires everything the others published (the grid-barrier pattern, without the wait).
     __syncthreads();
     if (tid == 0) {
         cand_cnt[blockIdx.x] = (int32_t)sh[6];
-        __threadfence();
-        sh[7] = atomicAdd(ticket, 1u) == gridDim.x - 1 ? 1u : 0u;
-        __threadfence();
+        uint32_t old;
+        asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;"
+                     : "=r"(old)
+                     : "l"(ticket)
+                     : "memory");
+        sh[7] = old == gridDim.x - 1 ? 1u : 0u;
     }
     __syncthreads();
     if (!sh[7]) return;
@@ -522,6 +525,15 @@ topk_select_kernel(const float *__restrict__ scores, int64_t n, int k_blk, int64
     if (valid) {
         const int G = (int)gridDim.x;
         const uint32_t my = tid < G ? (uint32_t)__ldcg(cand_cnt + tid) : 0u;
+        // Lists warp and warp + 32 (all of them when the grid has at most 64 CTAs): their
+        // first 32 entries are read together with the counts, before the offsets exist.
+        constexpr int kSpec = 2;
+        uint2 spec[kSpec];
+#pragma unroll
+        for (int r = 0; r < kSpec; ++r) {
+            const int cta = warp + 32 * r;
+            spec[r] = cta < G ? __ldcg(cand + (int64_t)cta * NT + lane) : make_uint2(0u, 0u);
+        }
         for (int64_t w = tid; w < nw; w += NT) selw[w] = __ldcg(bitmap + w);
         const uint32_t off = block_excl_scan(my, warp_s, &n_cand);
         if (tid < G) {
@@ -530,11 +542,19 @@ topk_select_kernel(const float *__restrict__ scores, int64_t n, int k_blk, int64
         }
         __syncthreads();
         if (n_cand <= (uint32_t)NT) {
-            for (int cta = warp; cta < G; cta += NT / 32)
-                for (uint32_t j = lane; j < lc[cta]; j += 32) {
+#pragma unroll
+            for (int r = 0; r < kSpec; ++r) {
+                const int cta = warp + 32 * r;
+                if (cta < G && (uint32_t)lane < lc[cta])
+                    cp[lo[cta] + lane] = ((unsigned long long)spec[r].x << 32) | (uint32_t)~spec[r].y;
+            }
+            for (int cta = warp; cta < G; cta += NT / 32) {
+                const uint32_t j0 = cta < 32 * kSpec ? 32u : 0u;  // entries already placed
+                for (uint32_t j = j0 + lane; j < lc[cta]; j += 32) {
                     const uint2 e = __ldcg(cand + (int64_t)cta * NT + j);
                     cp[lo[cta] + j] = ((unsigned long long)e.x << 32) | (uint32_t)~e.y;
                 }
+            }
             __syncthreads();
             // Second digit (key bits 12-19) over the candidates: a 256-bin histogram, then
             // the bin holding the k_rem-th; candidates above it are in, the ones inside it
