@@ -331,6 +331,15 @@ cudaError_t launch_gather(const void *K, const void *V, qsa_dtype dt, int64_t n_
                           int32_t *pos_out, int32_t *n_cells_out, int64_t max_cells,
                           cudaStream_t st);
 
+// Many queries (a prefill chunk) of the bf16 128-dim form with 4 KV heads x 8 query heads
+// and a position list: one CTA per query stages whole cell rows (all four heads).
+bool attn_uses_rows4(qsa_dtype dt, int64_t n_q, int H_q, int H_kv, int d_k, int d_v,
+                     const void *K, const void *V, int64_t ld_k, int64_t ld_v,
+                     const int32_t *pos, int64_t max_cells);
+cudaError_t launch_attn_rows4(const float *q, int64_t n_q, int H_q, float scale, const void *K,
+                              const void *V, int64_t n_kv, int64_t ld_k, int64_t ld_v,
+                              const int32_t *pos, const int32_t *n_cells, int64_t max_cells,
+                              float *out, float *lse, cudaStream_t st);
 // The latent-KV form (bf16, DKQ 576, d_v 512, 16 query heads per KV head, V the first
 // 512 columns of each K row: K == V, same stride) has its own tensor-core kernel.
 bool attn_uses_wide(qsa_dtype dt, int d_k, int d_v, int G, const void *K, const void *V,

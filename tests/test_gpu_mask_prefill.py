@@ -242,3 +242,40 @@ def test_dkq576_with_separate_values():
     for i, L in enumerate(lens):
         want, _ = oracle.attention(q[i], K, V, H, 1, d_k, d_v, d_k, d_v, pos[i, :L], scale)
         np.testing.assert_allclose(g_out[i], want, rtol=0, atol=ATOL_ATTN_BF16)
+
+
+def test_prefill_attention_all_heads_per_query():
+    """Many queries with 4 KV heads x 8 query heads (bf16, 128 dims) and position lists: one
+    CTA per query stages whole cell rows.  List lengths cover empty, one cell, the 32-cell
+    stage edges, the three-stage ring and a full 2051-cell list; every output and log-sum-exp
+    against the oracle."""
+    n_q, H_kv, G, d, n_kv, max_cells = 48, 4, 8, 128, 9000, 2051
+    H_q = H_kv * G
+    rng = np.random.default_rng(2051)
+    K = qsa_synth.to_bf16_bits(rng.standard_normal((n_kv, H_kv * d)).astype(np.float32))
+    V = qsa_synth.to_bf16_bits(rng.standard_normal((n_kv, H_kv * d)).astype(np.float32))
+    q = rng.standard_normal((n_q, H_q, d)).astype(np.float32)
+    edge = [0, 1, 31, 32, 33, 63, 64, 65, 95, 96, 97, 129, 2051]
+    lens = edge + list(rng.integers(1, max_cells + 1, size=n_q - len(edge)))
+    pos = np.full((n_q, max_cells), -9, np.int32)
+    for i, L in enumerate(lens):
+        pos[i, :L] = np.sort(rng.choice(n_kv, size=L, replace=False))
+    pos[5, 3] = -1  # a skipped entry inside a list
+    out = torch.zeros((n_q, H_q, d), device="cuda")
+    lse = torch.zeros((n_q, H_q), device="cuda")
+    ws_n = qsa.sparse_attn_workspace_size(n_q, H_q, H_kv, d, max_cells)
+    ws = torch.empty(max(ws_n // 4, 1), device="cuda")
+    scale = 1.0 / math.sqrt(d)
+    qsa.sparse_attn(to_dev(q), to_dev(K), to_dev(V), to_dev(np.array(lens, np.int32)), max_cells,
+                    out, H_kv, d, d, scale, pos=to_dev(pos), lse=lse, workspace=ws)
+    g_out, g_lse = to_host(out), to_host(lse)
+    for i, L in enumerate(lens):
+        if L == 0:
+            assert np.all(g_out[i] == 0.0) and np.all(np.isneginf(g_lse[i]))
+            continue
+        cells = pos[i, :L]
+        cells = cells[cells >= 0]
+        want, want_lse = oracle.attention(q[i], K, V, H_q, H_kv, d, d, H_kv * d, H_kv * d, cells,
+                                          scale)
+        np.testing.assert_allclose(g_out[i], want, rtol=0, atol=ATOL_ATTN_BF16)
+        np.testing.assert_allclose(g_lse[i], want_lse, rtol=1e-5, atol=1e-4)
