@@ -45,6 +45,7 @@ constexpr int kMaxSmemBytes = 220 * 1024;
 constexpr int kFixedWords = kBins1 + 2 * (NT / 32) + 32;
 constexpr int64_t kMaxN = 640 * 1024;           // candidates per query
 constexpr int kCandCapMax = 16384;
+constexpr int64_t kSampledMinN = 16384;  // below this the sampled form saves nothing
 
 __device__ __forceinline__ void put_cells(int32_t *dst, int32_t b, bool vec)
 {
@@ -343,6 +344,135 @@ __device__ void topk_query(const float *srow, int64_t n, int64_t k, int32_t *out
     write_selection(selw, eqw, nw, k_rem, k, out, pout, pvec, warp_s);
 }
 
+// The general form for one query when n is large and no histogram comes with the scores:
+// a strided sample of 1024 keys sets a threshold T at the 12-bit digit that holds the
+// sample's r-th largest key (r a margin above the k/n share); one pass keeps every key >= T
+// as a candidate (the top k are among them whenever at least k are); the candidates are
+// then selected exactly: first 12-bit digit, second 8-bit digit, and a (key, index) rank
+// inside the last bin.  Returns false (nothing written) when the sample missed -- fewer
+// than k or more than cand_cap candidates -- and the caller runs topk_query instead.
+// smem: the layout of topk_query.
+__device__ bool topk_query_sampled(const float *srow, int64_t n, int64_t k, int32_t *out,
+                                   int32_t *pout, bool pvec, int cand_cap, uint32_t *smem)
+{
+    uint32_t *hist = smem;
+    uint32_t *warp_s = hist + kBins1;
+    uint32_t *misc = warp_s + 2 * (NT / 32);
+    uint32_t *selw = misc + 32;
+    const int64_t nw = (n + 31) / 32;
+    uint32_t *cand_key = selw + 2 * nw;
+    int32_t *cand_idx = reinterpret_cast<int32_t *>(cand_key + cand_cap);
+    const int tid = threadIdx.x, lane = tid & 31;
+
+    // ---- 1. the sample's histogram and the threshold digit
+    for (int i = tid; i < kBins1; i += NT) hist[i] = 0u;
+    for (int64_t w = tid; w < nw; w += NT) selw[w] = 0u;
+    if (tid == 0) misc[8] = 0u;
+    __syncthreads();
+    {
+        const int64_t i = ((int64_t)tid * n) >> 10;  // NT = 1024 samples, strided
+        atomicAdd(&hist[score_key(srow[i]) >> (32 - kTopkHistBits)], 1u);
+    }
+    __syncthreads();
+    int64_t r = (k * 1024 + n - 1) / n + 8;
+    if (r > NT) r = NT;
+    find_bucket(hist, kBins1, (uint32_t)r, warp_s, misc);
+    const uint32_t T = misc[0] << (32 - kTopkHistBits);
+    __syncthreads();
+
+    // ---- 2. one pass: every key >= T is a candidate (warp-aggregated appends)
+    for_each_key(srow, n, [&](uint32_t key, int64_t i) {
+        if (key >= T) {
+            const uint32_t slot = atomicAdd(&misc[8], 1u);
+            if (slot < (uint32_t)cand_cap) {
+                cand_key[slot] = key;
+                cand_idx[slot] = (int32_t)i;
+            }
+        }
+    });
+    __syncthreads();
+    const uint32_t m = misc[8];
+    if (m < (uint32_t)k || m > (uint32_t)cand_cap) return false;  // uniform
+
+    // ---- 3. first digit over the candidates
+    for (int i = tid; i < kBins1; i += NT) hist[i] = 0u;
+    __syncthreads();
+    for (uint32_t c = tid; c < m; c += NT) atomicAdd(&hist[cand_key[c] >> (32 - kTopkHistBits)], 1u);
+    __syncthreads();
+    find_bucket(hist, kBins1, (uint32_t)k, warp_s, misc);
+    const uint32_t B1 = misc[0];
+    const uint32_t k_rem = (uint32_t)k - misc[1];
+    const bool whole1 = misc[2] == k_rem;
+    __syncthreads();
+    // ---- 4. above the bucket: selected; inside it: the second digit
+    if (tid < 256) hist[tid] = 0u;
+    __syncthreads();
+    for (uint32_t c = tid; c < m; c += NT) {
+        const uint32_t key = cand_key[c];
+        const uint32_t d1 = key >> (32 - kTopkHistBits);
+        if (d1 > B1 || (whole1 && d1 == B1)) {
+            const int32_t i = cand_idx[c];
+            atomicOr(&selw[i >> 5], 1u << (i & 31));
+        } else if (d1 == B1) {
+            atomicAdd(&hist[(key >> 12) & 255u], 1u);
+        }
+    }
+    __syncthreads();
+    if (!whole1) {
+        {
+            const uint32_t c2 = tid < 256 ? hist[255 - tid] : 0u;  // top bin first
+            uint32_t tot;
+            const uint32_t above2 = block_excl_scan(c2, warp_s, &tot);
+            if (tid < 256 && above2 < k_rem && above2 + c2 >= k_rem) {
+                misc[3] = 255u - (uint32_t)tid;
+                misc[4] = above2;
+                misc[5] = c2;
+            }
+        }
+        __syncthreads();
+        const uint32_t F = misc[3], k_rem2 = k_rem - misc[4], n_last = misc[5];
+        const bool whole2 = n_last == k_rem2;
+        if (n_last > (uint32_t)kBins1) return false;  // uniform: the general form takes it
+        // ---- 5. above the last bin: selected; its members (the histogram area holds their
+        // candidate slots) are ranked by (key descending, index ascending) among themselves
+        uint32_t *last = hist;
+        if (tid == 0) misc[9] = 0u;
+        __syncthreads();
+        for (uint32_t c = tid; c < m; c += NT) {
+            const uint32_t key = cand_key[c];
+            if ((key >> (32 - kTopkHistBits)) != B1) continue;
+            const uint32_t d2 = (key >> 12) & 255u;
+            if (d2 > F || (whole2 && d2 == F)) {
+                const int32_t i = cand_idx[c];
+                atomicOr(&selw[i >> 5], 1u << (i & 31));
+            } else if (d2 == F) {
+                const uint32_t slot = atomicAdd(&misc[9], 1u);
+                if (slot < (uint32_t)kBins1) last[slot] = c;
+            }
+        }
+        __syncthreads();
+        if (!whole2) {
+            for (uint32_t t = tid; t < n_last; t += NT) {
+                const uint32_t c = last[t];
+                const uint32_t key = cand_key[c];
+                const int32_t i = cand_idx[c];
+                uint32_t rank = 0;
+                for (uint32_t u = 0; u < n_last; ++u) {
+                    const uint32_t c2 = last[u];
+                    const uint32_t k2 = cand_key[c2];
+                    rank += (k2 > key || (k2 == key && cand_idx[c2] < i)) ? 1u : 0u;
+                }
+                if (rank < k_rem2) atomicOr(&selw[i >> 5], 1u << (i & 31));
+            }
+            __syncthreads();
+        }
+    }
+    (void)lane;
+    // ---- 6. ordered output
+    write_selection(selw, nullptr, nw, 0u, k, out, pout, pvec, warp_s);
+    return true;
+}
+
 __global__ void __launch_bounds__(NT)
 topk_kernel(const float *__restrict__ scores, int64_t ld, const int32_t *__restrict__ q_pos,
             int64_t n_full_cap, int k_blk, int32_t *__restrict__ blocks_out,
@@ -380,6 +510,9 @@ topk_kernel(const float *__restrict__ scores, int64_t ld, const int32_t *__restr
             for (int i = threadIdx.x; i < kBins1; i += NT) ehist[i] = 0u;
         return;
     }
+    if (!ehist && n >= kSampledMinN &&
+        topk_query_sampled(scores + qi * ld, n, k, out, pout, pvec, cand_cap, smem))
+        return;
     topk_query(scores + qi * ld, n, k, out, pout, pvec, ehist, cand_cap, smem);
 }
 

@@ -169,6 +169,33 @@ def test_topk_all_equal_scores():
     np.testing.assert_array_equal(to_host(blocks)[0], np.arange(100))
 
 
+@pytest.mark.parametrize("case", ["equal", "few_levels", "heavy_tail", "narrow"])
+def test_topk_large_rows_many_queries(case):
+    """Several queries of 20k-70k blocks (the sampled-threshold form of the general kernel):
+    all-equal rows (too many candidates: the full form), a few distinct levels (ties across
+    the threshold), a heavy tail and a narrow band of values.  Exact against the oracle."""
+    rng = np.random.default_rng(len(case))
+    n_q, n_full, k = 5, 70000, 512
+    if case == "equal":
+        s = np.full((n_q, n_full), 0.25, np.float32)
+    elif case == "few_levels":
+        s = rng.integers(0, 40, size=(n_q, n_full)).astype(np.float32) * 0.5
+    elif case == "heavy_tail":
+        s = rng.standard_cauchy((n_q, n_full)).astype(np.float32)
+    else:
+        s = (1.0 + 1e-6 * rng.standard_normal((n_q, n_full))).astype(np.float32)
+    n_each = np.array([70000, 20000, 16384, 16383, 50001], np.int64)
+    q_pos = (4 * n_each - 1).astype(np.int32)  # query i sees exactly n_each[i] full blocks
+    blocks = torch.full((n_q, k), -3, dtype=torch.int32, device="cuda")
+    counts = torch.zeros(n_q, dtype=torch.int32, device="cuda")
+    qsa.topk_blocks(to_dev(s), n_full, k, blocks, counts, q_pos=to_dev(q_pos))
+    g_blocks, g_counts = to_host(blocks), to_host(counts)
+    for i in range(n_q):
+        want = _oracle_topk_on_f32(s[i], int(n_each[i]), k)
+        assert g_counts[i] == want.shape[0]
+        np.testing.assert_array_equal(g_blocks[i, :g_counts[i]], want)
+
+
 def test_topk_per_query_positions():
     """With q_pos, query i ranks only blocks complete at its position."""
     rng = np.random.default_rng(6)
