@@ -61,12 +61,14 @@ def _load():
         lib = ctypes.CDLL(build())
         sig = {
             "oracle_round_bf16": (ctypes.c_float, [ctypes.c_float]),
+            "oracle_bf16_bits_from_f64": (ctypes.c_uint16, [_d]),
             "oracle_pool_mean": (_i32, [_p, _i32, _i64, _i32, _i32, _i64, _p]),
             "oracle_rmsnorm": (None, [_p, _i32, _p, _d, _p]),
             "oracle_rope": (None, [_p, _i32, _d, _d]),
             "oracle_pool_row_f64": (None, [_p, _i32, _i64, _i32, _i32, _p, _d, _d, _i64, _p]),
-            "oracle_pool_rows": (None, [_p, _i32, _i64, _i32, _i32, _p, _d, _d, _i64, _i64, _p]),
-            "oracle_scores": (None, [_p, _i64, _p, _i64, _i32, _i32, _d, _p, _i32, _p]),
+            "oracle_pool_rows": (None, [_p, _i32, _i64, _i32, _i32, _p, _d, _d, _i64, _i64, _i32,
+                                        _p]),
+            "oracle_scores": (None, [_p, _i64, _p, _i32, _i64, _i32, _i32, _d, _p, _i32, _p]),
             "oracle_topk": (_i64, [_p, _i64, _i64, _p]),
             "oracle_cells": (_i64, [_p, _i64, _i64, _p]),
             "oracle_get_rows": (None, [_p, _i32, _i64, _i64, _p, _i64, _p]),
@@ -105,6 +107,11 @@ def round_bf16(x: float) -> float:
     return float(_load().oracle_round_bf16(ctypes.c_float(x)))
 
 
+def bf16_bits_from_f64(x: float) -> int:
+    """Bit pattern of the bf16 value nearest to the fp64 value x (ties to even)."""
+    return int(_load().oracle_bf16_bits_from_f64(float(x)))
+
+
 def pool_mean(raw: np.ndarray, n_ctx: int, H: int, d: int, b: int):
     """Mean of the present raw indexer keys of block b; returns (p [H*d] f64, count)."""
     raw = np.ascontiguousarray(raw)
@@ -136,28 +143,29 @@ def pool_row_f64(raw, n_ctx, H, d, w, eps, base, b) -> np.ndarray:
     return z
 
 
-def pool_rows(raw, n_ctx, H, d, w, eps, base, row_begin, row_end, pooled=None):
-    """Recompute pooled-cache rows [row_begin, row_end) into ``pooled`` (fp32)."""
+def pool_rows(raw, n_ctx, H, d, w, eps, base, row_begin, row_end, pooled=None, store="f32"):
+    """Recompute pooled-cache rows [row_begin, row_end) into ``pooled``: an fp32 array, or
+    a uint16 array of bf16 bit patterns (``store="bf16"`` when a new one is made)."""
     raw = np.ascontiguousarray(raw)
     w = _c(w, np.float32)
     if pooled is None:
-        pooled = np.zeros((row_end, H * d), np.float32)
-    assert pooled.dtype == np.float32 and pooled.flags.c_contiguous
+        pooled = np.zeros((row_end, H * d), np.uint16 if store == "bf16" else np.float32)
+    assert pooled.flags.c_contiguous
     assert pooled.shape[0] >= row_end and pooled.shape[1] == H * d
     _load().oracle_pool_rows(_ptr(raw), _raw_dtype(raw), n_ctx, H, d, _ptr(w), eps, base,
-                             row_begin, row_end, _ptr(pooled))
+                             row_begin, row_end, _raw_dtype(pooled), _ptr(pooled))
     return pooled
 
 
 def scores(q, pooled, n_rows, H, d, scale, q_pos=None, round_bf16_operands=False):
-    """Index scores [n_q][n_rows] in fp64."""
+    """Index scores [n_q][n_rows] in fp64 (pooled: fp32, or uint16 bf16 bit patterns)."""
     q = _c(q, np.float32).reshape(-1, H * d)
-    pooled = _c(pooled, np.float32).reshape(-1, H * d)
+    pooled = np.ascontiguousarray(pooled).reshape(-1, H * d)
     assert pooled.shape[0] >= n_rows
     n_q = q.shape[0]
     out = np.zeros((n_q, n_rows), np.float64)
     qp = None if q_pos is None else _c(q_pos, np.int32)
-    _load().oracle_scores(_ptr(q), n_q, _ptr(pooled), n_rows, H, d, scale,
+    _load().oracle_scores(_ptr(q), n_q, _ptr(pooled), _raw_dtype(pooled), n_rows, H, d, scale,
                           None if qp is None else _ptr(qp), int(bool(round_bf16_operands)),
                           _ptr(out))
     return out
@@ -233,3 +241,34 @@ def decode_step(raw_k, n_ctx, H_idx, d_idx, w, eps, base, pooled, n_valid_full,
     ld = H_kv * d if kv_dtype_ld is None else kv_dtype_ld
     out, lse = attention(q, K, V, H_q, H_kv, d, d, ld, ld, cl, 1.0 / np.sqrt(d))
     return blocks, cl, out, lse, s
+
+
+def decode_step_multi(raw_k, n_ctx, H_idx, d_idx, w, eps, base, pooled, n_valid_full,
+                      q_idx, top_k_tokens, q, K, V, H_q, H_kv, d):
+    """A decode step for n_q query tokens at once: the last n_q tokens of the context,
+    positions n_ctx - n_q .. n_ctx - 1 (a token and the draft tokens that follow it,
+    verified together), sharing one pooled-cache update.
+
+    Every query scores every pooled row (as the one-query step does), but query i at
+    position p_i = n_ctx - n_q + i only selects among what is causal for it: the blocks
+    complete at p_i (b < floor((p_i+1)/4)) compete in its top-k, and its tail is
+    4*floor((p_i+1)/4) .. p_i.  Returns per-query lists (blocks, cells, out, lse) and
+    the score matrix [n_q][n_rows].
+    """
+    q_idx = _c(q_idx, np.float32).reshape(-1, H_idx * d_idx)
+    n_q = q_idx.shape[0]
+    q = _c(q, np.float32).reshape(n_q, H_q, d)
+    n_full = n_ctx // 4
+    n_rows = (n_ctx + 3) // 4
+    pool_rows(raw_k, n_ctx, H_idx, d_idx, w, eps, base, n_valid_full, n_rows, pooled)
+    q_pos = np.arange(n_ctx - n_q, n_ctx, dtype=np.int32)
+    s = scores(q_idx, pooled, n_rows, H_idx, d_idx, 1.0 / np.sqrt(d_idx))
+    res = []
+    for i in range(n_q):
+        p = int(q_pos[i])
+        blocks = topk(s[i], min(n_full, (p + 1) // 4), top_k_tokens // 4)
+        cl = cells(blocks, p)
+        out, lse = attention(q[i], K, V, H_q, H_kv, d, d, H_kv * d, H_kv * d, cl,
+                             1.0 / np.sqrt(d))
+        res.append((blocks, cl, out, lse))
+    return res, s

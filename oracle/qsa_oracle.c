@@ -11,9 +11,9 @@
  *   4-token block -> average pooling -> RMS norm -> RoPE -> score against the query
  *   -> top-k over blocks -> expand selected blocks to cells, append the open tail
  *   -> attention over the selected cells only.
- * All arithmetic is fp64; only the pooled-key cache is rounded to fp32 on store
- * (the cache is an fp32 tensor), and the tensor-core scoring mirror rounds its two
- * operands to bf16 when asked.
+ * All arithmetic is fp64; only the pooled-key cache is rounded on store, to fp32 or
+ * to bf16 (the storage type of the cache tensor), and the tensor-core scoring mirror
+ * rounds its two operands to bf16 when asked.
  *
  * Readings where the pages are silent (each one is listed with its reason in the
  * design notes): partial block divided by the number of present tokens; RMS norm per
@@ -72,6 +72,33 @@ static float round_to_bf16(float x)
 }
 
 float oracle_round_bf16(float x) { return round_to_bf16(x); }
+
+/*
+ * Round an fp64 value to the nearest bf16 value, ties to even, in one step (not through
+ * fp32: a value just above a bf16 midpoint must not first land on the midpoint).
+ * bf16 keeps 8 significant bits, exponents down to 2^-126 and subnormals spaced 2^-133;
+ * values at or beyond the midpoint above the largest finite bf16, (2 - 2^-7) * 2^127,
+ * become infinite.  Returns the bit pattern.
+ */
+uint16_t oracle_bf16_bits_from_f64(double x)
+{
+    uint16_t sign = signbit(x) ? 0x8000u : 0u;
+    if (isnan(x)) return 0x7fc0u;
+    if (isinf(x)) return (uint16_t)(sign | 0x7f80u);
+    double ax = fabs(x);
+    if (ax == 0.0) return sign;
+    int ex;
+    frexp(ax, &ex);             /* ax = m * 2^ex with 0.5 <= m < 1 */
+    int e_unit = ex - 8;        /* value of the last of the 8 significant bits */
+    if (e_unit < -133) e_unit = -133;
+    double r = nearbyint(ldexp(ax, -e_unit)); /* default rounding mode: ties to even */
+    double v = ldexp(r, e_unit);
+    if (v > 3.3895313892515355e38) return (uint16_t)(sign | 0x7f80u);
+    float f = (float)v;         /* exact: v has at most 8 significant bits */
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    return (uint16_t)(sign | (u >> 16));
+}
 
 /* ------------------------------------------------------------------ step 1: pool */
 
@@ -150,18 +177,24 @@ void oracle_pool_row_f64(const void *raw, int dtype, int64_t n_ctx, int H, int d
  * The incremental pooled-key cache update (p1, "incremental pooled-key cache
  * (COMMON-004)": only newly completed or invalidated blocks are recomputed; the open
  * partial block is recomputed every step).  Writes rows [row_begin, row_end) of
- * `pooled` ([rows][H*d], fp32 storage) and leaves every other row untouched.
+ * `pooled` ([rows][H*d]) and leaves every other row untouched.  store_dtype: the cache
+ * holds fp32 (ORC_F32, each value rounded to nearest fp32) or bf16 bits (ORC_BF16, each
+ * value rounded to nearest bf16 directly from fp64).
  */
 void oracle_pool_rows(const void *raw, int dtype, int64_t n_ctx, int H, int d,
                       const float *w, double eps, double base, int64_t row_begin,
-                      int64_t row_end, float *pooled)
+                      int64_t row_end, int store_dtype, void *pooled)
 {
     int64_t hd = (int64_t)H * d;
     double *z = (double *)malloc(sizeof(double) * (size_t)hd);
     for (int64_t b = row_begin; b < row_end; ++b) {
         oracle_pool_row_f64(raw, dtype, n_ctx, H, d, w, eps, base, b, z);
-        for (int64_t e = 0; e < hd; ++e)
-            pooled[b * hd + e] = (float)z[e];
+        for (int64_t e = 0; e < hd; ++e) {
+            if (store_dtype == ORC_BF16)
+                ((uint16_t *)pooled)[b * hd + e] = oracle_bf16_bits_from_f64(z[e]);
+            else
+                ((float *)pooled)[b * hd + e] = (float)z[e];
+        }
     }
     free(z);
 }
@@ -171,14 +204,15 @@ void oracle_pool_rows(const void *raw, int dtype, int64_t n_ctx, int H, int d,
 /*
  * Index scores (p1, "QSA indexer": score every pooled block against the query):
  *   s[i][b] = scale * sum_{h,j} q[i][h*d+j] * z[b][h*d+j]
- * q: [n_q][H*d] fp32; pooled: [n_rows][H*d] fp32; scores: [n_q][n_rows] fp64.
+ * q: [n_q][H*d] fp32; pooled: [n_rows][H*d] fp32 or bf16 bits (pooled_dtype);
+ * scores: [n_q][n_rows] fp64.
  * q_pos (nullable): position of query i; row b is visible to query i only when the
  * block is complete at that position (4b+3 <= q_pos[i]); other rows get -inf.
  * round_bf16 != 0: both operands are first rounded to bf16 (tensor-core mirror).
  */
-void oracle_scores(const float *q, int64_t n_q, const float *pooled, int64_t n_rows,
-                   int H, int d, double scale, const int32_t *q_pos, int round_bf16,
-                   double *scores)
+void oracle_scores(const float *q, int64_t n_q, const void *pooled, int pooled_dtype,
+                   int64_t n_rows, int H, int d, double scale, const int32_t *q_pos,
+                   int round_bf16, double *scores)
 {
     int64_t hd = (int64_t)H * d;
     for (int64_t i = 0; i < n_q; ++i) {
@@ -189,7 +223,7 @@ void oracle_scores(const float *q, int64_t n_q, const float *pooled, int64_t n_r
             }
             double s = 0.0;
             for (int64_t e = 0; e < hd; ++e) {
-                float qa = q[i * hd + e], zb = pooled[b * hd + e];
+                float qa = q[i * hd + e], zb = (float)elem(pooled, pooled_dtype, b * hd + e);
                 if (round_bf16) {
                     qa = round_to_bf16(qa);
                     zb = round_to_bf16(zb);
