@@ -35,7 +35,8 @@ import numpy as np  # noqa: E402
 
 METRIC = "sparse-attn decode steps/s at 64k/128k/256k ctx; achieved HBM GB/s vs roofline"
 CONTEXTS = {"64k": "decode_64k", "128k": "decode_128k", "256k": "decode_256k"}
-SCORE_SRC = os.path.join(ROOT, "gather_qsa_pool_gb300", "csrc", "index_score.cu")
+SCORE_SRCS = [os.path.join(ROOT, "gather_qsa_pool_gb300", "csrc", f)
+              for f in ("index_score.cu", "score_stream.cuh")]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "score_rows_256k_traffic.txt")
 # Kernels one qsa_decode_step launches when it appends a token: the fused pool-update +
 # score scan, the top-k (whose last CTA also writes the cell list) and the attention
@@ -56,6 +57,8 @@ def parse_args():
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-mask", action="store_true")
     ap.add_argument("--prefill-reps", type=int, default=5)
+    ap.add_argument("--no-variants", action="store_true",
+                    help="skip the bf16 pooled-cache and multi-query decode lines")
     return ap.parse_args()
 
 
@@ -164,8 +167,11 @@ def traffic_per_launch(n_rows_primary: int):
     """DRAM bytes per score launch from the committed ncu summary, if it was taken on the
     current kernel source (else None)."""
     try:
-        with open(SCORE_SRC, "rb") as f:
-            sha = hashlib.sha256(f.read()).hexdigest()[:16]
+        h = hashlib.sha256()
+        for src in SCORE_SRCS:
+            with open(src, "rb") as f:
+                h.update(f.read())
+        sha = h.hexdigest()[:16]
         kv = {}
         with open(TRAFFIC_FILE) as f:
             for ln in f:
@@ -182,7 +188,11 @@ def traffic_per_launch(n_rows_primary: int):
 
 # ----------------------------------------------------------------------------- GPU arm
 
-def run_context(name, args, world, rank, local, want_clocks):
+def run_context(name, args, world, rank, local, want_clocks, pooled="f32", n_q=1, light=False):
+    """Decode steps at one context length over ``args.layers`` rotating layer sets.
+    pooled: storage of the pooled-key cache ("f32" or "bf16"); n_q: query tokens per step
+    (a token and its drafts, each step appending n_q tokens); light: skip the CUDA-graph
+    replay and the end-to-end loop."""
     import torch
 
     import gather_qsa_pool_gb300 as qsa
@@ -192,11 +202,12 @@ def run_context(name, args, world, rank, local, want_clocks):
     L = args.layers
     K, W = args.steps, args.warmup
     k_kernel = max(L, min(K, 4 * L * 16))
-    k_e2e = max(L, min(K, 1024))
+    k_e2e = 0 if light else max(L, min(K, 1024))
     total_steps = W + K + k_e2e + 2
-    extra = total_steps // L + 2
+    extra = n_q * (total_steps // L + 2)
     dev = torch.device("cuda", local)
     n_q_pool = 32
+    pdt = torch.bfloat16 if pooled == "bf16" else torch.float32
 
     layers, caches = [], []
     for li in range(L):
@@ -205,7 +216,8 @@ def run_context(name, args, world, rank, local, want_clocks):
         lay = qsa.DecodeLayer(cap_tokens=shape.n_ctx + extra, H_idx=shape.H_idx,
                               d_idx=shape.d_idx, H_q=shape.H_q, H_kv=shape.H_kv, d=shape.d,
                               top_k_tokens=shape.top_k_tokens, eps=shape.eps,
-                              rope_base=shape.rope_base, device=dev)
+                              rope_base=shape.rope_base, pooled_dtype=pdt, max_queries=n_q,
+                              device=dev)
         lay.rebuild(inp["raw_k"], inp["norm_w"], shape.n_ctx - 1)
         lay.bind(inp["raw_k"], inp["norm_w"], inp["K"], inp["V"])
         layers.append(lay)
@@ -220,8 +232,9 @@ def run_context(name, args, world, rank, local, want_clocks):
 
     def step(s):
         li = s % L
-        j = (s // L) % n_q_pool
-        layers[li].step_ptr(n_ctx[li], q_ptrs[li][0][j], q_ptrs[li][1][j], sp)
+        j = (s // L) % (n_q_pool - n_q + 1)
+        n_ctx[li] += n_q - 1
+        layers[li].step_ptr(n_ctx[li], q_ptrs[li][0][j], q_ptrs[li][1][j], sp, n_q)
         n_ctx[li] += 1
 
     s = 0
@@ -258,15 +271,19 @@ def run_context(name, args, world, rank, local, want_clocks):
     # the same steps replayed from a CUDA graph (one captured step per layer set, context
     # lengths fixed at capture): launch issue leaves the host
     graph_us, graph_err = None, None
+    if light:
+        graph_err = "not run"
     try:
+        if light:
+            raise RuntimeError("not run")
         gs = torch.cuda.Stream(device=dev)
         gs.wait_stream(stream)
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.stream(gs):
             with torch.cuda.graph(graph, stream=gs):
                 for li in range(L):
-                    layers[li].step_ptr(n_ctx[li], q_ptrs[li][0][0], q_ptrs[li][1][0],
-                                        gs.cuda_stream)
+                    layers[li].step_ptr(n_ctx[li] + n_q - 1, q_ptrs[li][0][0], q_ptrs[li][1][0],
+                                        gs.cuda_stream, n_q)
             for li in range(L):
                 layers[li].n_valid_full = (n_ctx[li] - 1) // 4
         torch.cuda.synchronize()
@@ -283,22 +300,38 @@ def run_context(name, args, world, rank, local, want_clocks):
         graph_us = g0.elapsed_time(g1) * 1e3 / (reps * L)
         del graph
     except Exception as e:  # capture unsupported on this driver: report why
-        graph_err = f"{type(e).__name__}: {e}"[:200]
+        if not light:
+            graph_err = f"{type(e).__name__}: {e}"[:200]
         torch.cuda.synchronize()
 
     # score kernel alone, back to back over the rotating layers (its average duration)
     n_rows = [(c + 3) // 4 for c in n_ctx]
+
+    # the C call with its arguments marshalled once per layer set, so that issuing the
+    # launches stays well ahead of the GPU even for the short scans
+    lib = qsa.load()
+    score_args = []
     for li in range(L):
-        qsa.index_score(caches[li]["q_idx"][0].view(1, -1), layers[li].pooled, n_rows[li],
-                        shape.H_idx, shape.d_idx, 1.0 / math.sqrt(shape.d_idx), layers[li].scores)
+        pdt_c = qsa.QSA_BF16 if pooled == "bf16" else qsa.QSA_F32
+        score_args.append([(caches[li]["q_idx"][j].data_ptr(), n_q, shape.H_idx * shape.d_idx,
+                            None, layers[li].pooled.data_ptr(), pdt_c, n_rows[li], shape.H_idx,
+                            shape.d_idx, 1.0 / math.sqrt(shape.d_idx),
+                            layers[li].scores.data_ptr(), n_rows[li], qsa.QSA_PREC_F32, None, 0,
+                            sp) for j in range(n_q_pool - n_q + 1)])
+
+    def score_only(i):
+        a = score_args[i % L]
+        st_ = lib.qsa_index_score(*a[i % len(a)])
+        if st_ != 0:
+            raise qsa.QSAError("qsa_index_score", st_)
+
+    for i in range(L):
+        score_only(i)
     torch.cuda.synchronize()
     ev2, ev3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ev2.record(stream)
     for i in range(k_kernel):
-        li = i % L
-        qsa.index_score(caches[li]["q_idx"][i % n_q_pool].view(1, -1), layers[li].pooled,
-                        n_rows[li], shape.H_idx, shape.d_idx, 1.0 / math.sqrt(shape.d_idx),
-                        layers[li].scores)
+        score_only(i)
     ev3.record(stream)
     torch.cuda.synchronize()
     score_us = ev2.elapsed_time(ev3) * 1e3 / k_kernel
@@ -340,12 +373,12 @@ def run_context(name, args, world, rank, local, want_clocks):
     t_e2e = max_over_ranks(t_e2e, world)
 
     splits = qsa._binding.load()  # noqa: F841  (library already loaded)
-    n_cells_last = int(layers[(s - 1) % L].n_cells.item())
+    n_cells_last = int(layers[(s - 1) % L].n_cells[0].item())
     res = {
         "ms": ms_max, "K": K, "W": W, "score_us": score_us, "score_rows": score_rows,
         "t_e2e": t_e2e, "k_e2e": k_e2e, "host_issue_us": t_issue * 1e6 / K, "h2d": h2d, "d2h": d2h, "clocks": clocks,
         "n_cells": n_cells_last, "shape": shape, "n_ctx_end": max(n_ctx),
-        "graph_us": graph_us, "graph_err": graph_err,
+        "graph_us": graph_us, "graph_err": graph_err, "pooled": pooled, "n_q": n_q,
     }
     del layers, caches
     torch.cuda.empty_cache()
@@ -492,10 +525,43 @@ def run_mask(args, local):
     return out_d
 
 
-def algorithmic_bytes(shape, n_rows, n_cells):
-    """Pooled-cache scan (fp32) + the selected K/V rows (bf16), per decode step."""
+def algorithmic_bytes(shape, n_rows, n_cells, pooled_esize=4, n_q=1):
+    """Pooled-cache scan (read once for all queries) + each query's selected K/V rows, per
+    decode step."""
     esize = 2 if shape.dtype == "bf16" else 4
-    return n_rows * shape.H_idx * shape.d_idx * 4 + n_cells * shape.H_kv * 2 * shape.d * esize
+    return (n_rows * shape.H_idx * shape.d_idx * pooled_esize
+            + n_q * n_cells * shape.H_kv * 2 * shape.d * esize)
+
+
+def summarize(r, world, layers, peak):
+    """Per-context figures of one run_context result."""
+    sh = r["shape"]
+    n_q = r["n_q"]
+    pes = 2 if r["pooled"] == "bf16" else 4
+    n_rows_avg = (sh.n_ctx + sh.n_ctx + n_q * r["K"] // layers) // 2 // 4
+    steps_s = world * r["K"] / (r["ms"] / 1e3)
+    bytes_step = algorithmic_bytes(sh, n_rows_avg, r["n_cells"], pes, n_q)
+    out = {
+        "n_ctx": sh.n_ctx, "steps_per_s": steps_s, "us_per_step": r["ms"] * 1e3 / r["K"],
+        "algorithmic_MB_per_step": bytes_step / 1e6,
+        "achieved_GBps_step": bytes_step * steps_s / world / 1e9,
+        "frac_of_hbm_peak_step": bytes_step * steps_s / world / 1e9 / peak,
+        "score_kernel_us": r["score_us"],
+        "score_kernel_GBps": r["score_rows"] * sh.H_idx * sh.d_idx * pes / r["score_us"] / 1e3,
+        "host_issue_us_per_step": r["host_issue_us"],
+    }
+    if n_q == 1:
+        out["tokens_per_s_12_layers"] = steps_s / 12.0
+    else:
+        out["query_tokens_per_step"] = n_q
+        out["query_tokens_per_s"] = n_q * steps_s
+    if r["k_e2e"]:
+        out["e2e_steps_per_s"] = world * r["k_e2e"] / r["t_e2e"]
+    if r["graph_us"] is not None:
+        out["graph_us_per_step"] = r["graph_us"]
+    elif r["graph_err"] and r["graph_err"] != "not run":
+        out["graph_err"] = r["graph_err"]
+    return out
 
 
 # ----------------------------------------------------------------------------- CPU oracle
@@ -586,26 +652,20 @@ def main():
                                     want_clocks=(name == args.primary and rank == 0))
     peak, peak_kind = load_peaks()
 
-    sweep = {}
-    for name, r in results.items():
-        sh = r["shape"]
-        n_rows_avg = (sh.n_ctx + sh.n_ctx + r["K"] // args.layers) // 2 // 4
-        steps_s = world * r["K"] / (r["ms"] / 1e3)
-        bytes_step = algorithmic_bytes(sh, n_rows_avg, r["n_cells"])
-        sweep[name] = {
-            "n_ctx": sh.n_ctx, "steps_per_s": steps_s, "us_per_step": r["ms"] * 1e3 / r["K"],
-            "tokens_per_s_12_layers": steps_s / 12.0,
-            "algorithmic_MB_per_step": bytes_step / 1e6,
-            "achieved_GBps_step": bytes_step * steps_s / world / 1e9,
-            "frac_of_hbm_peak_step": bytes_step * steps_s / world / 1e9 / peak,
-            "score_kernel_us": r["score_us"],
-            "score_kernel_GBps": r["score_rows"] * sh.H_idx * sh.d_idx * 4 / r["score_us"] / 1e3,
-            "e2e_steps_per_s": world * r["k_e2e"] / r["t_e2e"],
-            "host_issue_us_per_step": r["host_issue_us"],
-            "graph_us_per_step": r["graph_us"],
-        }
-        if r["graph_err"]:
-            sweep[name]["graph_err"] = r["graph_err"]
+    sweep = {name: summarize(r, world, args.layers, peak) for name, r in results.items()}
+    # Next to the headline: the pooled-key cache stored in bf16 (half the scan's bytes),
+    # and steps carrying a token with two drafts (three queries, one scan).
+    variants = {}
+    if not args.no_variants:
+        for label, ctx, pooled, n_q in (("bf16_pooled_64k", "64k", "bf16", 1),
+                                        ("bf16_pooled_128k", "128k", "bf16", 1),
+                                        ("bf16_pooled_256k", "256k", "bf16", 1),
+                                        ("three_queries_256k", "256k", "f32", 3),
+                                        ("three_queries_bf16_pooled_256k", "256k", "bf16", 3)):
+            rv = run_context(ctx, args, world, rank, local, want_clocks=False, pooled=pooled,
+                             n_q=n_q, light=True)
+            variants[label] = dict(summarize(rv, world, args.layers, peak),
+                                   pooled_cache=pooled, queries_per_step=n_q)
     r = results[args.primary]
     sh = r["shape"]
     value = sweep[args.primary]["steps_per_s"]
@@ -633,7 +693,7 @@ def main():
         "config": config_for(sh, args.layers),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "kernel": "score_rows_kernel (qsa_index_score, decode)",
+                     "kernel": "score_stream_kernel (qsa_index_score, decode, fp32 cache)",
                      "peak_source": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s"},
         "e2e": {"value": sweep[args.primary]["e2e_steps_per_s"], "unit": "steps/s",
@@ -641,6 +701,7 @@ def main():
         "gpu_launches": r["K"] * LAUNCHES_PER_DECODE_STEP,
         "clocks": r["clocks"],
         "sweep": sweep,
+        "variants": variants or None,
         "prefill": prefill,
         "mask": mask,
         "cpu_baseline": cpu_baseline,

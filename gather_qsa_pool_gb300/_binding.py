@@ -30,10 +30,11 @@ _sz = ctypes.c_size_t
 _SIGNATURES = {
     "qsa_status_str": (ctypes.c_char_p, [_int]),
     "qsa_version": (_int, []),
-    "qsa_pool_update": (_int, [_p, _int, _i64, _int, _int, _p, _f, _d, _p, _i64, _i64, _p]),
-    "qsa_index_score": (_int, [_p, _i64, _i64, _p, _p, _i64, _int, _int, _f, _p, _i64, _int,
-                               _p, _sz, _p]),
-    "qsa_index_score_workspace_size": (_sz, [_i64, _i64, _int, _int, _int]),
+    "qsa_pool_update": (_int, [_p, _int, _i64, _int, _int, _p, _f, _d, _p, _int, _i64, _i64,
+                               _p]),
+    "qsa_index_score": (_int, [_p, _i64, _i64, _p, _p, _int, _i64, _int, _int, _f, _p, _i64,
+                               _int, _p, _sz, _p]),
+    "qsa_index_score_workspace_size": (_sz, [_i64, _i64, _int, _int, _int, _int]),
     "qsa_topk_blocks": (_int, [_p, _i64, _i64, _p, _i64, _i64, _p, _p, _p]),
     "qsa_topk_max_candidates": (_i64, []),
     "qsa_gather_kv": (_int, [_p, _p, _int, _i64, _int, _int, _int, _i64, _i64, _p, _p, _i64,
@@ -41,10 +42,10 @@ _SIGNATURES = {
     "qsa_sparse_attn": (_int, [_p, _i64, _int, _int, _int, _int, _f, _p, _p, _int, _i64, _i64,
                                _i64, _p, _p, _i64, _p, _p, _p, _sz, _p]),
     "qsa_sparse_attn_workspace_size": (_sz, [_i64, _int, _int, _int, _i64]),
-    "qsa_decode_step": (_int, [_p, _int, _i64, _int, _int, _p, _f, _d, _p, _i64, _i64, _p, _f,
-                               _p, _i64, _p, _p, _p, _p, _int, _i64, _int, _int, _i64, _p, _p,
-                               _i64, _p, _int, _f, _p, _p, _p, _sz, _p]),
-    "qsa_decode_step_workspace_size": (_sz, [_int, _int, _int, _i64, _i64]),
+    "qsa_decode_step": (_int, [_p, _int, _i64, _int, _int, _p, _f, _d, _p, _int, _i64, _i64,
+                               _i64, _p, _f, _p, _i64, _p, _p, _p, _p, _int, _i64, _int, _int,
+                               _i64, _p, _p, _i64, _p, _int, _f, _p, _p, _p, _sz, _p]),
+    "qsa_decode_step_workspace_size": (_sz, [_i64, _int, _int, _int, _i64, _i64]),
     "qsa_mask_to_list": (_int, [_p, _i64, _i64, _i64, _i64, _p, _p, _p, _p]),
     "qsa_mask_sparse_eligible": (_int, [_int, _f, _f, _i64, _i64]),
 }
@@ -126,26 +127,30 @@ def _dtype(t) -> int:
 # --------------------------------------------------------------------------- entry points
 
 def pool_update(raw_k, n_ctx, H, d, norm_w, eps, rope_base, pooled, n_valid_full, stream=None):
-    """qsa_pool_update: recompute pooled rows [n_valid_full, ceil(n_ctx/4))."""
+    """qsa_pool_update: recompute pooled rows [n_valid_full, ceil(n_ctx/4)) of a float32 or
+    bfloat16 cache."""
     _check("qsa_pool_update", load().qsa_pool_update(
         _ptr(raw_k), _dtype(raw_k), n_ctx, H, d, _ptr(norm_w), eps, rope_base, _ptr(pooled),
-        pooled.shape[0], n_valid_full, _stream(stream)))
+        _dtype(pooled), pooled.shape[0], n_valid_full, _stream(stream)))
 
 
-def index_score_workspace_size(n_q, n_rows, H, d, precision=QSA_PREC_F32) -> int:
-    return int(load().qsa_index_score_workspace_size(n_q, n_rows, H, d, precision))
+def index_score_workspace_size(n_q, n_rows, H, d, precision=QSA_PREC_F32,
+                               pooled_dtype=QSA_F32) -> int:
+    return int(load().qsa_index_score_workspace_size(n_q, n_rows, H, d, pooled_dtype,
+                                                     precision))
 
 
 def index_score(q, pooled, n_rows, H, d, scale, scores, q_pos=None, precision=QSA_PREC_F32,
                 workspace=None, stream=None):
-    """qsa_index_score: scores[i][b] for b < n_rows (q: [n_q][>= H*d] fp32)."""
+    """qsa_index_score: scores[i][b] for b < n_rows (q: [n_q][>= H*d] fp32; pooled float32
+    or bfloat16)."""
     n_q = q.shape[0] if q.dim() > 1 else 1
     ld_q = _ld(q) if q.dim() > 1 else H * d
     ld_s = _ld(scores) if scores.dim() > 1 else n_rows
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check("qsa_index_score", load().qsa_index_score(
-        _ptr(q), n_q, ld_q, _ptr(q_pos), _ptr(pooled), n_rows, H, d, scale, _ptr(scores), ld_s,
-        precision, _ptr(workspace), ws_bytes, _stream(stream)))
+        _ptr(q), n_q, ld_q, _ptr(q_pos), _ptr(pooled), _dtype(pooled), n_rows, H, d, scale,
+        _ptr(scores), ld_s, precision, _ptr(workspace), ws_bytes, _stream(stream)))
 
 
 def topk_max_candidates() -> int:
@@ -197,19 +202,20 @@ def sparse_attn(q, K, V, n_cells, max_cells, out, H_kv, d_k, d_v, scale, pos=Non
 
 def decode_step(raw_k, n_ctx, H_idx, d_idx, norm_w, eps, rope_base, pooled, n_valid_full,
                 q_idx, scale_idx, scores, k_blk, blocks, counts, K, V, H_kv, d, pos, n_cells,
-                max_cells, q, H_q, scale, out, lse=None, workspace=None, stream=None):
-    """qsa_decode_step: pool update, score, top-k, cell list and attention in one call."""
+                max_cells, q, H_q, scale, out, lse=None, workspace=None, n_q=1, stream=None):
+    """qsa_decode_step: pool update, score, top-k, cell list and attention in one call, for
+    the last n_q tokens of the context (packed per-query buffers)."""
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check("qsa_decode_step", load().qsa_decode_step(
         _ptr(raw_k), _dtype(raw_k), n_ctx, H_idx, d_idx, _ptr(norm_w), eps, rope_base,
-        _ptr(pooled), pooled.shape[0], n_valid_full, _ptr(q_idx), scale_idx, _ptr(scores), k_blk,
-        _ptr(blocks), _ptr(counts), _ptr(K), _ptr(V), _dtype(K), K.shape[0], H_kv, d,
-        _ld(K), _ptr(pos), _ptr(n_cells), max_cells, _ptr(q), H_q, scale, _ptr(out),
+        _ptr(pooled), _dtype(pooled), pooled.shape[0], n_valid_full, n_q, _ptr(q_idx), scale_idx,
+        _ptr(scores), k_blk, _ptr(blocks), _ptr(counts), _ptr(K), _ptr(V), _dtype(K), K.shape[0],
+        H_kv, d, _ld(K), _ptr(pos), _ptr(n_cells), max_cells, _ptr(q), H_q, scale, _ptr(out),
         _ptr(lse), _ptr(workspace), ws_bytes, _stream(stream)))
 
 
-def decode_step_workspace_size(H_q, H_kv, d, max_cells, cap_rows) -> int:
-    return int(load().qsa_decode_step_workspace_size(H_q, H_kv, d, max_cells, cap_rows))
+def decode_step_workspace_size(H_q, H_kv, d, max_cells, cap_rows, n_q=1) -> int:
+    return int(load().qsa_decode_step_workspace_size(n_q, H_q, H_kv, d, max_cells, cap_rows))
 
 
 def mask_to_list(mask, max_list, pos_out, counts_out, bits_out=None, n_kv=None, stream=None):

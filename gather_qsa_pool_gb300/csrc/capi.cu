@@ -59,13 +59,15 @@ int qsa_version(void) { return (1 << 16) | 0; }
 
 static qsa_status check_pool_update(const void *raw_k, qsa_dtype raw_dtype, int64_t n_ctx, int H,
                                     int d, const float *norm_w, float eps, double rope_base,
-                                    float *pooled, int64_t cap_rows, int64_t n_valid_full)
+                                    const void *pooled, qsa_dtype pooled_dtype, int64_t cap_rows,
+                                    int64_t n_valid_full)
 {
     if (!raw_k || !norm_w || !pooled) return QSA_ERR_INVALID_ARG;
-    if (!valid_dtype(raw_dtype) || n_ctx < 0 || H < 1 || d < 2 || (d & 1) || n_valid_full < 0 ||
-        cap_rows < 0 || !(eps >= 0.0f) || !(rope_base > 0.0))
+    if (!valid_dtype(raw_dtype) || !valid_dtype(pooled_dtype) || n_ctx < 0 || H < 1 || d < 2 ||
+        (d & 1) || n_valid_full < 0 || cap_rows < 0 || !(eps >= 0.0f) || !(rope_base > 0.0))
         return QSA_ERR_INVALID_ARG;
-    if (!aligned(raw_k, esize_of(raw_dtype)) || !aligned(norm_w, 4) || !aligned(pooled, 4))
+    if (!aligned(raw_k, esize_of(raw_dtype)) || !aligned(norm_w, 4) ||
+        !aligned(pooled, esize_of(pooled_dtype)))
         return QSA_ERR_INVALID_ARG;
     const int64_t n_rows = (n_ctx + 3) / 4;
     const int64_t n_full = n_ctx / 4;
@@ -79,62 +81,72 @@ static qsa_status check_pool_update(const void *raw_k, qsa_dtype raw_dtype, int6
 
 static cudaError_t run_pool_update(const void *raw_k, qsa_dtype raw_dtype, int64_t n_ctx, int H,
                                    int d, const float *norm_w, float eps, double rope_base,
-                                   float *pooled, int64_t n_valid_full, uint32_t *zero_hist,
-                                   cudaStream_t st)
+                                   void *pooled, qsa_dtype pooled_dtype, int64_t n_valid_full,
+                                   uint32_t *zero_hist, cudaStream_t st)
 {
     const int64_t n_rows = (n_ctx + 3) / 4;
     const int64_t n_full = n_ctx / 4;
     const int64_t row0 = n_valid_full < n_full ? n_valid_full : n_full;
-    return launch_pool_update(raw_k, raw_dtype, n_ctx, H, d, norm_w, eps, rope_base, pooled, row0,
-                              n_rows, zero_hist, st);
+    return launch_pool_update(raw_k, raw_dtype, n_ctx, H, d, norm_w, eps, rope_base, pooled,
+                              pooled_dtype, row0, n_rows, zero_hist, st);
 }
 
 qsa_status qsa_pool_update(const void *raw_k, qsa_dtype raw_dtype, int64_t n_ctx, int H, int d,
-                           const float *norm_w, float eps, double rope_base, float *pooled,
-                           int64_t cap_rows, int64_t n_valid_full, qsa_stream_t stream)
+                           const float *norm_w, float eps, double rope_base, void *pooled,
+                           qsa_dtype pooled_dtype, int64_t cap_rows, int64_t n_valid_full,
+                           qsa_stream_t stream)
 {
     const qsa_status v = check_pool_update(raw_k, raw_dtype, n_ctx, H, d, norm_w, eps, rope_base,
-                                           pooled, cap_rows, n_valid_full);
+                                           pooled, pooled_dtype, cap_rows, n_valid_full);
     if (v != QSA_OK) return v;
     return from_cuda(run_pool_update(raw_k, raw_dtype, n_ctx, H, d, norm_w, eps, rope_base, pooled,
-                                     n_valid_full, nullptr, (cudaStream_t)stream));
+                                     pooled_dtype, n_valid_full, nullptr, (cudaStream_t)stream));
 }
 
 size_t qsa_index_score_workspace_size(int64_t n_q, int64_t n_rows, int H, int d,
-                                      qsa_precision precision)
+                                      qsa_dtype pooled_dtype, qsa_precision precision)
 {
-    if (precision != QSA_PREC_BF16_TC || n_q <= 0 || n_rows <= 0 || H < 1 || d < 1) return 0;
-    return index_score_tc_workspace(n_q, n_rows, H, d);
+    if (precision != QSA_PREC_BF16_TC || n_q <= 0 || n_rows <= 0 || H < 1 || d < 1 ||
+        !valid_dtype(pooled_dtype))
+        return 0;
+    return index_score_tc_workspace(n_q, n_rows, H, d, pooled_dtype);
 }
 
-static qsa_status check_index_score(const float *q, int64_t n_q, int64_t ld_q, const float *pooled,
-                                    int64_t n_rows, int H, int d, float *scores, int64_t ld_scores)
+static qsa_status check_index_score(const float *q, int64_t n_q, int64_t ld_q, const void *pooled,
+                                    qsa_dtype pooled_dtype, int64_t n_rows, int H, int d,
+                                    float *scores, int64_t ld_scores)
 {
     if (!q || !pooled || !scores) return QSA_ERR_INVALID_ARG;
-    if (n_q < 0 || n_rows < 0 || H < 1 || d < 1 || ld_q < (int64_t)H * d || ld_scores < n_rows)
+    if (n_q < 0 || n_rows < 0 || H < 1 || d < 1 || ld_q < (int64_t)H * d || ld_scores < n_rows ||
+        !valid_dtype(pooled_dtype))
         return QSA_ERR_INVALID_ARG;
-    if (!aligned(q, 4) || !aligned(pooled, 4) || !aligned(scores, 4)) return QSA_ERR_INVALID_ARG;
+    if (!aligned(q, 4) || !aligned(pooled, esize_of(pooled_dtype)) || !aligned(scores, 4))
+        return QSA_ERR_INVALID_ARG;
     if ((n_q + 63) / 64 > 65535) return QSA_ERR_UNSUPPORTED;
     return QSA_OK;
 }
 
 qsa_status qsa_index_score(const float *q, int64_t n_q, int64_t ld_q, const int32_t *q_pos,
-                           const float *pooled, int64_t n_rows, int H, int d, float scale,
-                           float *scores, int64_t ld_scores, qsa_precision precision,
-                           void *workspace, size_t workspace_bytes, qsa_stream_t stream)
+                           const void *pooled, qsa_dtype pooled_dtype, int64_t n_rows, int H,
+                           int d, float scale, float *scores, int64_t ld_scores,
+                           qsa_precision precision, void *workspace, size_t workspace_bytes,
+                           qsa_stream_t stream)
 {
-    const qsa_status v = check_index_score(q, n_q, ld_q, pooled, n_rows, H, d, scores, ld_scores);
+    const qsa_status v = check_index_score(q, n_q, ld_q, pooled, pooled_dtype, n_rows, H, d,
+                                           scores, ld_scores);
     if (v != QSA_OK) return v;
     if (precision == QSA_PREC_F32) {
-        return from_cuda(launch_index_score(q, n_q, ld_q, q_pos, pooled, n_rows, H, d, scale,
-                                            scores, ld_scores, nullptr, 0, nullptr,
+        return from_cuda(launch_index_score(q, n_q, ld_q, q_pos, pooled, pooled_dtype, n_rows, H,
+                                            d, scale, scores, ld_scores, ScoreSide{},
                                             (cudaStream_t)stream));
     }
     if (precision == QSA_PREC_BF16_TC) {
-        const size_t need = qsa_index_score_workspace_size(n_q, n_rows, H, d, precision);
+        const size_t need =
+            qsa_index_score_workspace_size(n_q, n_rows, H, d, pooled_dtype, precision);
         if (workspace_bytes < need || (need > 0 && !workspace)) return QSA_ERR_INVALID_ARG;
-        return launch_index_score_tc(q, n_q, ld_q, q_pos, pooled, n_rows, H, d, scale, scores,
-                                     ld_scores, workspace, workspace_bytes, (cudaStream_t)stream);
+        return launch_index_score_tc(q, n_q, ld_q, q_pos, pooled, pooled_dtype, n_rows, H, d,
+                                     scale, scores, ld_scores, workspace, workspace_bytes,
+                                     (cudaStream_t)stream);
     }
     return QSA_ERR_INVALID_ARG;
 }
@@ -244,51 +256,68 @@ qsa_status qsa_sparse_attn(const float *q, int64_t n_q, int H_q, int H_kv, int d
 
 static size_t align256(size_t b) { return (b + 255) & ~(size_t)255; }
 
-size_t qsa_decode_step_workspace_size(int H_q, int H_kv, int d, int64_t max_cells,
+size_t qsa_decode_step_workspace_size(int64_t n_q, int H_q, int H_kv, int d, int64_t max_cells,
                                       int64_t cap_rows)
 {
-    if (H_q < 1 || H_kv < 1 || d < 1 || max_cells < 0 || H_q % H_kv || cap_rows < 0) return 0;
-    return align256(attn_workspace_bytes(1, H_q, H_kv, d, max_cells)) + kTopkHistBytes +
-           topk_select_workspace_bytes(cap_rows);
+    if (n_q < 1 || n_q > kMaxStreamQueries || H_q < 1 || H_kv < 1 || d < 1 || max_cells < 0 ||
+        H_q % H_kv || cap_rows < 0)
+        return 0;
+    return align256(attn_workspace_bytes(n_q, H_q, H_kv, d, max_cells)) +
+           (size_t)n_q * (kTopkHistBytes + topk_select_workspace_bytes(cap_rows));
 }
 
 qsa_status qsa_decode_step(const void *raw_k, qsa_dtype raw_dtype, int64_t n_ctx, int H_idx,
                            int d_idx, const float *norm_w, float eps, double rope_base,
-                           float *pooled, int64_t cap_rows, int64_t n_valid_full,
-                           const float *q_idx, float scale_idx, float *scores, int64_t k_blk,
-                           int32_t *blocks, int32_t *counts, const void *K, const void *V,
-                           qsa_dtype kv_dtype, int64_t n_kv, int H_kv, int d, int64_t ld_kv,
-                           int32_t *pos, int32_t *n_cells, int64_t max_cells, const float *q,
-                           int H_q, float scale, float *out, float *lse_out, void *workspace,
-                           size_t workspace_bytes, qsa_stream_t stream)
+                           void *pooled, qsa_dtype pooled_dtype, int64_t cap_rows,
+                           int64_t n_valid_full, int64_t n_q, const float *q_idx, float scale_idx,
+                           float *scores, int64_t k_blk, int32_t *blocks, int32_t *counts,
+                           const void *K, const void *V, qsa_dtype kv_dtype, int64_t n_kv,
+                           int H_kv, int d, int64_t ld_kv, int32_t *pos, int32_t *n_cells,
+                           int64_t max_cells, const float *q, int H_q, float scale, float *out,
+                           float *lse_out, void *workspace, size_t workspace_bytes,
+                           qsa_stream_t stream)
 {
+    if (n_q < 1 || n_q > kMaxStreamQueries || n_q > n_ctx) return QSA_ERR_INVALID_ARG;
     const int64_t n_rows = (n_ctx + 3) / 4;
     const int64_t n_full = n_ctx / 4;
-    const size_t need = qsa_decode_step_workspace_size(H_q, H_kv, d, max_cells, cap_rows);
-    if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return QSA_ERR_INVALID_ARG;
-    const size_t attn_bytes = align256(attn_workspace_bytes(1, H_q, H_kv, d, max_cells));
+    const size_t need = qsa_decode_step_workspace_size(n_q, H_q, H_kv, d, max_cells, cap_rows);
+    if (!workspace || need == 0 || workspace_bytes < need || !aligned(workspace, 256))
+        return QSA_ERR_INVALID_ARG;
+    const size_t attn_bytes = align256(attn_workspace_bytes(n_q, H_q, H_kv, d, max_cells));
+    const size_t sel_stride = topk_select_workspace_bytes(cap_rows);
     char *wsb = static_cast<char *>(workspace);
+    // workspace: attention partials | n_q histograms | n_q top-k scratch areas (each
+    // starting with the query's arrival ticket)
     uint32_t *hist = reinterpret_cast<uint32_t *>(wsb + attn_bytes);
-    // top-k scratch: arrival ticket | per-CTA candidate counts | candidates | bitmap
-    void *sel = wsb + attn_bytes + kTopkHistBytes;
-    uint32_t *ticket = topk_select_ticket(sel);
+    void *sel = wsb + attn_bytes + (size_t)n_q * kTopkHistBytes;
     qsa_status v = check_pool_update(raw_k, raw_dtype, n_ctx, H_idx, d_idx, norm_w, eps,
-                                     rope_base, pooled, cap_rows, n_valid_full);
+                                     rope_base, pooled, pooled_dtype, cap_rows, n_valid_full);
     if (v == QSA_OK)
-        v = check_index_score(q_idx, 1, (int64_t)H_idx * d_idx, pooled, n_rows, H_idx, d_idx,
-                              scores, n_rows);
-    if (v == QSA_OK) v = check_topk(scores, 1, n_rows, n_full, k_blk, blocks, counts);
+        v = check_index_score(q_idx, n_q, (int64_t)H_idx * d_idx, pooled, pooled_dtype, n_rows,
+                              H_idx, d_idx, scores, n_rows);
+    if (v == QSA_OK) v = check_topk(scores, n_q, n_rows, n_full, k_blk, blocks, counts);
     if (v == QSA_OK)
-        v = check_gather(K, V, kv_dtype, n_kv, H_kv, d, d, ld_kv, ld_kv, blocks, counts, 1,
+        v = check_gather(K, V, kv_dtype, n_kv, H_kv, d, d, ld_kv, ld_kv, blocks, counts, n_q,
                          k_blk, nullptr, n_ctx, nullptr, nullptr, pos, n_cells, max_cells);
     if (v == QSA_OK)
-        v = check_attn(q, 1, H_q, H_kv, d, d, K, V, kv_dtype, n_kv, ld_kv, ld_kv, n_cells,
+        v = check_attn(q, n_q, H_q, H_kv, d, d, K, V, kv_dtype, n_kv, ld_kv, ld_kv, n_cells,
                        max_cells, out, workspace, attn_bytes);
     if (v != QSA_OK) return v;
     const cudaStream_t st = (cudaStream_t)stream;
-    // 1+2. pooled rows of the new / open block, then scores of every row; full blocks also
-    // enter the histogram of their top key bits.  One kernel when the rows to recompute are
-    // few (the decode case), else the pool-update kernel followed by the score kernel.
+    // Query i sits at position p_i = n_ctx - n_q + i; its candidates are the blocks complete
+    // there.  The score kernel counts each query's candidates into its histogram and resets
+    // each query's arrival ticket.
+    ScoreSide side;
+    side.hist = hist;
+    for (int i = 0; i < n_q; ++i) {
+        const int64_t p1 = (n_ctx - n_q + i + 1) / 4;
+        side.n_hist[i] = p1 < n_full ? p1 : n_full;
+    }
+    side.ticket = topk_select_ticket(sel);
+    side.ticket_stride = (int64_t)(sel_stride / sizeof(uint32_t));
+    // 1+2. pooled rows of the new / open blocks, then scores of every row for every query.
+    // One kernel when the rows to recompute are few (the decode case), else the
+    // pool-update kernel (which also clears the histograms) followed by the score kernel.
     const int64_t row0 = n_valid_full < n_full ? n_valid_full : n_full;
     PoolFuse pf;
     pf.raw = raw_k;
@@ -298,32 +327,33 @@ qsa_status qsa_decode_step(const void *raw_k, qsa_dtype raw_dtype, int64_t n_ctx
     pf.eps = eps;
     pf.row0 = row0;
     pf.row1 = n_rows;
-    cudaError_t e = launch_score_pool_fused(q_idx, pooled, n_rows, H_idx, d_idx, scale_idx, scores,
-                                            hist, n_full, ticket, pf, rope_base, st);
+    cudaError_t e = launch_score_pool_fused(q_idx, (int)n_q, pooled, pooled_dtype, n_rows, H_idx,
+                                            d_idx, scale_idx, scores, n_rows, side, pf, rope_base,
+                                            st);
     if (e == cudaErrorNotSupported) {
         e = run_pool_update(raw_k, raw_dtype, n_ctx, H_idx, d_idx, norm_w, eps, rope_base, pooled,
-                            n_valid_full, hist, st);
+                            pooled_dtype, n_valid_full, nullptr, st);
         if (e == cudaSuccess)
-            e = launch_index_score(q_idx, 1, (int64_t)H_idx * d_idx, nullptr, pooled, n_rows,
-                                   H_idx, d_idx, scale_idx, scores, n_rows, hist, n_full, ticket,
-                                   st);
+            e = launch_index_score(q_idx, n_q, (int64_t)H_idx * d_idx, nullptr, pooled,
+                                   pooled_dtype, n_rows, H_idx, d_idx, scale_idx, scores, n_rows,
+                                   side, st);
     }
-    // 3. top-k from that histogram; its last CTA also writes the cell list (qsa_gather_kv's
-    // job).  When every full block is selected, the one-CTA form does it.
+    // 3. top-k from those histograms; the last CTA of each query also writes its cell list
+    // (qsa_gather_kv's job).  When a query's blocks are all selected, the one-CTA form does it.
     if (e == cudaSuccess) {
         const int64_t esize = kv_dtype == QSA_BF16 ? 2 : 4;
         const int64_t row_bytes = (int64_t)H_kv * d * esize;
         const bool contiguous = ld_kv == (int64_t)H_kv * d;
-        e = launch_topk_select(scores, n_full, k_blk, n_ctx, hist, sel, blocks, counts, pos,
-                               n_cells, contiguous ? K : nullptr, contiguous ? V : nullptr,
-                               row_bytes, st);
+        e = launch_topk_select(scores, n_rows, (int)n_q, n_full, cap_rows, k_blk, n_ctx, hist, sel,
+                               blocks, counts, pos, n_cells, max_cells, contiguous ? K : nullptr,
+                               contiguous ? V : nullptr, row_bytes, st);
         if (e == cudaErrorNotSupported)
-            e = launch_topk(scores, 1, n_rows, nullptr, n_full, k_blk, blocks, counts, n_ctx, pos,
-                            n_cells, max_cells, hist, st);
+            e = launch_topk(scores, n_q, n_rows, nullptr, n_full, k_blk, blocks, counts, n_ctx, pos,
+                            n_cells, max_cells, hist, st, 1);
     }
     // 4. attention over the listed cells, read in place from the cache
     if (e == cudaSuccess)
-        e = launch_sparse_attn(q, 1, H_q, H_kv, d, d, scale, K, V, kv_dtype, n_kv, ld_kv, ld_kv,
+        e = launch_sparse_attn(q, n_q, H_q, H_kv, d, d, scale, K, V, kv_dtype, n_kv, ld_kv, ld_kv,
                                pos, n_cells, max_cells, out, lse_out, (float *)workspace, st,
                                true);
     return from_cuda(e);

@@ -10,8 +10,9 @@
 // [1024 x 2048] x [2048 x 64052] contraction -- is this library's.
 //
 // Design:
-//   - two prologue kernels round the queries and the pooled rows to bf16 (nearest even)
-//     into the workspace, so that both operands can be staged by TMA;
+//   - prologue kernels round the queries and (for an fp32 cache) the pooled rows to bf16
+//     (nearest even) into the workspace, so that both operands can be staged by TMA; a
+//     bf16 cache is already the operand and is read in place;
 //   - the score kernel is persistent, one CTA per SM, warp-specialised: warp 0 issues the
 //     TMA copies (query tile 128 x 64 and pooled tile 256 x 64 per stage, 128-byte
 //     swizzle, four stages in flight), warp 1 issues tcgen05.mma (M 128, N 256, K 16; four
@@ -353,17 +354,20 @@ size_t al256(size_t b) { return (b + 255) & ~(size_t)255; }
 
 }  // namespace
 
-size_t index_score_tc_workspace(int64_t n_q, int64_t n_rows, int H, int d)
+size_t index_score_tc_workspace(int64_t n_q, int64_t n_rows, int H, int d, qsa_dtype pdt)
 {
-    // bf16 copies of the queries and of the pooled rows, then one error word
+    // bf16 copies of the queries and (for an fp32 cache) of the pooled rows, then one
+    // error word; a bf16 cache is read in place
     const size_t K = (size_t)H * (size_t)d;
-    return al256((size_t)n_q * K * 2) + al256((size_t)n_rows * K * 2) + 256;
+    const size_t rows = pdt == QSA_BF16 ? 0 : al256((size_t)n_rows * K * 2);
+    return al256((size_t)n_q * K * 2) + rows + 256;
 }
 
 qsa_status launch_index_score_tc(const float *q, int64_t n_q, int64_t ld_q,
-                                 const int32_t *q_pos, const float *pooled, int64_t n_rows,
-                                 int H, int d, float scale, float *scores, int64_t ld_scores,
-                                 void *workspace, size_t ws_bytes, cudaStream_t st)
+                                 const int32_t *q_pos, const void *pooled, qsa_dtype pdt,
+                                 int64_t n_rows, int H, int d, float scale, float *scores,
+                                 int64_t ld_scores, void *workspace, size_t ws_bytes,
+                                 cudaStream_t st)
 {
     const int K = H * d;
     if (K % kBK != 0) return QSA_ERR_UNSUPPORTED;
@@ -371,20 +375,24 @@ qsa_status launch_index_score_tc(const float *q, int64_t n_q, int64_t ld_q,
         return QSA_ERR_INVALID_ARG;
     if (n_q == 0 || n_rows == 0) return QSA_OK;
     if (n_q > 0x7fffffffLL || n_rows > 0x7fffffffLL) return QSA_ERR_UNSUPPORTED;
-    const size_t need = index_score_tc_workspace(n_q, n_rows, H, d);
+    const size_t need = index_score_tc_workspace(n_q, n_rows, H, d, pdt);
     if (ws_bytes < need) return QSA_ERR_INVALID_ARG;
     char *ws = static_cast<char *>(workspace);
     __nv_bfloat16 *qb = reinterpret_cast<__nv_bfloat16 *>(ws);
-    __nv_bfloat16 *pb = reinterpret_cast<__nv_bfloat16 *>(ws + al256((size_t)n_q * K * 2));
+    const bool convert_rows = pdt != QSA_BF16;
+    const __nv_bfloat16 *pb =
+        convert_rows ? reinterpret_cast<__nv_bfloat16 *>(ws + al256((size_t)n_q * K * 2))
+                     : static_cast<const __nv_bfloat16 *>(pooled);
     int *err = reinterpret_cast<int *>(ws + need - 256);
     CUtensorMap tmA, tmB;
     if (!make_map(&tmA, qb, n_q, K, kBM) || !make_map(&tmB, pb, n_rows, K, kBN))
         return QSA_ERR_CUDA;
     cudaError_t e = launch(q_to_bf16_kernel, dim3(1024), dim3(256), 0, st, 1, q, n_q, ld_q, K, qb);
-    if (e == cudaSuccess) {
+    if (e == cudaSuccess && convert_rows) {
         const int64_t n4 = n_rows * (int64_t)K / 4;
         e = launch(rows_to_bf16_kernel, dim3((unsigned)(device_sm_count() * 8)), dim3(256), 0, st,
-                   1, reinterpret_cast<const float4 *>(pooled), n4, reinterpret_cast<uint2 *>(pb));
+                   1, reinterpret_cast<const float4 *>(pooled), n4,
+                   reinterpret_cast<uint2 *>(const_cast<__nv_bfloat16 *>(pb)));
     }
     if (e != cudaSuccess) return QSA_ERR_CUDA;
     static bool attr = false;

@@ -6,6 +6,8 @@
 // "incremental pooled-key cache (COMMON-004)" (only new or invalidated rows and the open
 // block are recomputed each step; completed rows are reused).
 //
+// The cache stores fp32, or bf16 rounded to nearest even (half the bytes of the scan that
+// reads it back every step).
 // In decode this touches one or two rows (<= 4 raw rows read, 8 KB written), so it is
 // latency-bound: every thread issues all of its raw-key loads before using any, and the
 // rotation angles avoid device fp64 transcendentals (slow on this part): the inverse
@@ -21,11 +23,11 @@ namespace {
 
 constexpr int kPoolThreads = 512;
 
-template <typename T>
+template <typename T, typename TP>
 __global__ void __launch_bounds__(kPoolThreads)
 pool_update_kernel(const T *__restrict__ raw, int64_t n_ctx, int H, int d,
                    const float *__restrict__ w, float eps, const RopeTable tab,
-                   float *__restrict__ pooled, int64_t row0, int64_t row1,
+                   TP *__restrict__ pooled, int64_t row0, int64_t row1,
                    uint32_t *__restrict__ zero_hist)
 {
     extern __shared__ float smem[];
@@ -56,10 +58,29 @@ void make_rope_table(RopeTable *tab, int d, double base)
         tab->theta[i] = pow(base, -2.0 * (double)i / (double)d);
 }
 
+template <typename T, typename TP>
+cudaError_t launch_pool_typed(const void *raw_k, int64_t n_ctx, int H, int d,
+                              const float *norm_w, float eps, const RopeTable &tab, void *pooled,
+                              int64_t row0, int64_t row1, uint32_t *zero_hist, int64_t n,
+                              cudaStream_t st)
+{
+    const size_t smem = sizeof(float) * ((size_t)H * d + (size_t)d);
+    auto k = pool_update_kernel<T, TP>;
+    static bool attr_set = false;
+    if (smem > 48 * 1024 && !attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             200 * 1024);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    return launch(k, dim3((unsigned)n), dim3(kPoolThreads), smem, st, 1, (const T *)raw_k, n_ctx,
+                  H, d, norm_w, eps, tab, (TP *)pooled, row0, row1, zero_hist);
+}
+
 cudaError_t launch_pool_update(const void *raw_k, qsa_dtype dt, int64_t n_ctx, int H, int d,
                                const float *norm_w, float eps, double rope_base,
-                               float *pooled, int64_t row0, int64_t row1, uint32_t *zero_hist,
-                               cudaStream_t st)
+                               void *pooled, qsa_dtype pdt, int64_t row0, int64_t row1,
+                               uint32_t *zero_hist, cudaStream_t st)
 {
     int64_t n = row1 - row0;
     if (n <= 0) {
@@ -75,25 +96,18 @@ cudaError_t launch_pool_update(const void *raw_k, qsa_dtype dt, int64_t n_ctx, i
         tab_d = d;
         tab_base = rope_base;
     }
-    const size_t smem = sizeof(float) * ((size_t)H * d + (size_t)d);
-    static bool attr_set[2] = {false, false};
-    if (dt == QSA_BF16) {
-        auto k = pool_update_kernel<__nv_bfloat16>;
-        if (smem > 48 * 1024 && !attr_set[1]) {
-            cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-            attr_set[1] = true;
-        }
-        return launch(k, dim3((unsigned)n), dim3(kPoolThreads), smem, st, 1,
-                      (const __nv_bfloat16 *)raw_k, n_ctx, H, d, norm_w, eps, tab, pooled, row0,
-                      row1, zero_hist);
-    }
-    auto k = pool_update_kernel<float>;
-    if (smem > 48 * 1024 && !attr_set[0]) {
-        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-        attr_set[0] = true;
-    }
-    return launch(k, dim3((unsigned)n), dim3(kPoolThreads), smem, st, 1, (const float *)raw_k,
-                  n_ctx, H, d, norm_w, eps, tab, pooled, row0, row1, zero_hist);
+    using bf = __nv_bfloat16;
+    if (dt == QSA_BF16)
+        return pdt == QSA_BF16
+                   ? launch_pool_typed<bf, bf>(raw_k, n_ctx, H, d, norm_w, eps, tab, pooled, row0,
+                                               row1, zero_hist, n, st)
+                   : launch_pool_typed<bf, float>(raw_k, n_ctx, H, d, norm_w, eps, tab, pooled,
+                                                  row0, row1, zero_hist, n, st);
+    return pdt == QSA_BF16
+               ? launch_pool_typed<float, bf>(raw_k, n_ctx, H, d, norm_w, eps, tab, pooled, row0,
+                                              row1, zero_hist, n, st)
+               : launch_pool_typed<float, float>(raw_k, n_ctx, H, d, norm_w, eps, tab, pooled,
+                                                 row0, row1, zero_hist, n, st);
 }
 
 }  // namespace qsa

@@ -184,16 +184,29 @@ constexpr double kTwoPi = 6.283185307179586;
 constexpr double kInvTwoPi = 0.15915494309189535;
 void make_rope_table(RopeTable *tab, int d, double base);
 
+// Storage of one pooled-cache value: fp32 as is, bf16 rounded to nearest even.
+__device__ __forceinline__ float stored_value(float v, const float *) { return v; }
+__device__ __forceinline__ float stored_value(float v, const __nv_bfloat16 *)
+{
+    return __bfloat162float(__float2bfloat16_rn(v));
+}
+__device__ __forceinline__ void store_pooled(float *p, float v) { *p = v; }
+__device__ __forceinline__ void store_pooled(__nv_bfloat16 *p, float v)
+{
+    *p = __float2bfloat16_rn(v);
+}
+
 // One pooled-key row b, computed by the whole CTA: mean of the block's present raw keys
-// -> per-head RMS norm -> rotation at position 4b.  The row ends up both in p_s (shared,
-// [H*d]) and in out_row (global).  cs / sn: shared [d/2] scratch.  Every element's
-// arithmetic is independent of the CTA size, so every kernel that calls this produces the
-// same bits.  Contains __syncthreads().
-template <typename T>
+// -> per-head RMS norm -> rotation at position 4b.  The row is stored to out_row (global,
+// element type TP: fp32, or bf16 rounded to nearest even) and p_s (shared, [H*d] fp32)
+// ends up holding exactly the stored values.  cs / sn: shared [d/2] scratch.  Every
+// element's arithmetic is independent of the CTA size, so every kernel that calls this
+// produces the same bits.  Contains __syncthreads().
+template <typename T, typename TP>
 __device__ __forceinline__ void pool_row(const T *__restrict__ raw, int64_t n_ctx, int H, int d,
                                          const float *__restrict__ w, float eps,
                                          const RopeTable &tab, int64_t b, float *p_s, float *cs,
-                                         float *sn, float *__restrict__ out_row)
+                                         float *sn, TP *__restrict__ out_row)
 {
     const int hd = H * d;
     const int half = d / 2;
@@ -228,16 +241,16 @@ __device__ __forceinline__ void pool_row(const T *__restrict__ raw, int64_t n_ct
         for (int j = lane; j < d; j += 32) ss = fmaf(ph[j], ph[j], ss);
         ss = warp_sum(ss);
         const float inv = 1.0f / sqrtf(ss / (float)d + eps);
-        float *o = out_row + (int64_t)h * d;
+        TP *o = out_row + (int64_t)h * d;
         for (int i = lane; i < half; i += 32) {
             const float ya = ph[i] * inv * w[i];
             const float yb = ph[i + half] * inv * w[i + half];
             const float za = ya * cs[i] - yb * sn[i];
             const float zb = ya * sn[i] + yb * cs[i];
-            ph[i] = za;
-            ph[i + half] = zb;
-            o[i] = za;
-            o[i + half] = zb;
+            ph[i] = stored_value(za, o);
+            ph[i + half] = stored_value(zb, o);
+            store_pooled(o + i, za);
+            store_pooled(o + i + half, zb);
         }
     }
     __syncthreads();
@@ -248,10 +261,27 @@ __device__ __forceinline__ void pool_row(const T *__restrict__ raw, int64_t n_ct
 
 // zero_hist (nullable): a top-k histogram that the kernel clears (the launch then has at
 // least one CTA even when no row needs recomputing).
+// pooled: [rows][H*d] of type pdt (QSA_F32 or QSA_BF16).
 cudaError_t launch_pool_update(const void *raw_k, qsa_dtype dt, int64_t n_ctx, int H, int d,
                                const float *norm_w, float eps, double rope_base,
-                               float *pooled, int64_t row0, int64_t row1, uint32_t *zero_hist,
-                               cudaStream_t st);
+                               void *pooled, qsa_dtype pdt, int64_t row0, int64_t row1,
+                               uint32_t *zero_hist, cudaStream_t st);
+
+// Up to this many queries share one streaming pass over the pooled cache.
+constexpr int kMaxStreamQueries = 4;
+
+// Where the decode score kernels send their results besides scores[i][b]:
+// hist (nullable): per query i, rows b < n_hist[i] also enter a histogram of the top
+// kTopkHistBits bits of their score key (hist + i * 2^kTopkHistBits), for the top-k's
+// first radix digit.  ticket (nullable): the word ticket + i * ticket_stride (uint32
+// units) is set to 0 once the kernel runs, for each query i (the decode top-k's arrival
+// counters).
+struct ScoreSide {
+    uint32_t *hist = nullptr;
+    int64_t n_hist[kMaxStreamQueries] = {0, 0, 0, 0};
+    uint32_t *ticket = nullptr;
+    int64_t ticket_stride = 0;
+};
 
 // Pooled-row recomputation fused into the decode score kernel (rows [row0, row1)).
 struct PoolFuse {
@@ -263,27 +293,27 @@ struct PoolFuse {
     int64_t row0, row1;
 };
 constexpr int kMaxFusedPoolRows = 4;
-// Decode score kernel with the pool update of rows [pf.row0, pf.row1) folded in, when the
-// shape allows it (returns cudaErrorNotSupported otherwise, without launching).
-// ticket (nullable): set to 0 once the kernel runs -- the decode top-k's arrival counter.
-cudaError_t launch_score_pool_fused(const float *q, const float *pooled, int64_t n_rows, int H,
-                                    int d, float scale, float *scores, uint32_t *hist,
-                                    int64_t n_hist, uint32_t *ticket, const PoolFuse &pf,
+// Decode score kernel for n_q <= kMaxStreamQueries queries ([n_q][H*d], packed) with the
+// pool update of rows [pf.row0, pf.row1) folded in, when the shape allows it (returns
+// cudaErrorNotSupported otherwise, without launching).  scores [n_q][ld_scores].
+cudaError_t launch_score_pool_fused(const float *q, int n_q, void *pooled, qsa_dtype pdt,
+                                    int64_t n_rows, int H, int d, float scale, float *scores,
+                                    int64_t ld_scores, const ScoreSide &side, const PoolFuse &pf,
                                     double rope_base, cudaStream_t st);
 
-// hist (nullable, decode only): also add each row b < n_hist to a histogram of the top
-// kTopkHistBits bits of its score key, for the top-k's first radix digit.  ticket
-// (nullable): set to 0 once the kernel runs.
+// pooled of type pdt.  side: see ScoreSide (hist and tickets for the decode top-k; only
+// used with q_pos == NULL and n_q <= kMaxStreamQueries).
 cudaError_t launch_index_score(const float *q, int64_t n_q, int64_t ld_q, const int32_t *q_pos,
-                               const float *pooled, int64_t n_rows, int H, int d, float scale,
-                               float *scores, int64_t ld_scores, uint32_t *hist, int64_t n_hist,
-                               uint32_t *ticket, cudaStream_t st);
+                               const void *pooled, qsa_dtype pdt, int64_t n_rows, int H, int d,
+                               float scale, float *scores, int64_t ld_scores,
+                               const ScoreSide &side, cudaStream_t st);
 
 qsa_status launch_index_score_tc(const float *q, int64_t n_q, int64_t ld_q,
-                                 const int32_t *q_pos, const float *pooled, int64_t n_rows,
-                                 int H, int d, float scale, float *scores, int64_t ld_scores,
-                                 void *workspace, size_t ws_bytes, cudaStream_t st);
-size_t index_score_tc_workspace(int64_t n_q, int64_t n_rows, int H, int d);
+                                 const int32_t *q_pos, const void *pooled, qsa_dtype pdt,
+                                 int64_t n_rows, int H, int d, float scale, float *scores,
+                                 int64_t ld_scores, void *workspace, size_t ws_bytes,
+                                 cudaStream_t st);
+size_t index_score_tc_workspace(int64_t n_q, int64_t n_rows, int H, int d, qsa_dtype pdt);
 
 // Order-preserving key of a score: higher score <=> larger key.  NaN ranks as -inf;
 // -0 and +0 are the same score.
@@ -301,12 +331,17 @@ constexpr size_t kTopkHistBytes = sizeof(uint32_t) << kTopkHistBits;
 int64_t topk_max_candidates();
 
 // pos_out / n_cells_out (nullable): also write each query's cell list -- the selected
-// blocks' 4 cells in order, then the open tail of the query (q_pos[i], or n_ctx - 1).
+// blocks' 4 cells in order, then the open tail of the query.
+// The position of query i: q_pos[i]; without q_pos, n_ctx - 1 - p_step * (n_q - 1 - i):
+// with p_step = 1 the queries are the last n_q tokens (their candidates are then limited
+// to the blocks complete at their position, as with q_pos), with p_step = 0 every query
+// sits at n_ctx - 1 and every one of the n_full blocks competes.
 // ext_hist (nullable): per-query histograms accumulated by the score kernel, cleared here.
 cudaError_t launch_topk(const float *scores, int64_t n_q, int64_t ld, const int32_t *q_pos,
                         int64_t n_full, int64_t k_blk, int32_t *blocks_out, int32_t *counts_out,
                         int64_t n_ctx, int32_t *pos_out, int32_t *n_cells_out,
-                        int64_t max_cells, uint32_t *ext_hist, cudaStream_t st);
+                        int64_t max_cells, uint32_t *ext_hist, cudaStream_t st,
+                        int64_t p_step = 0);
 // The decode form of the top-k (one query whose n_full blocks outnumber k_blk): many CTAs
 // classify against the score kernel's histogram, the last to finish resolves and writes
 // blocks, count, cells and tail.  scratch: topk_select_workspace_bytes(n_full) bytes,
@@ -316,9 +351,16 @@ cudaError_t launch_topk(const float *scores, int64_t n_q, int64_t ld, const int3
 // kv_k / kv_v (nullable): K and V caches whose rows are contiguous (row stride = row
 // size = kv_row_bytes, a multiple of 16, bases 16-byte aligned); the K and V rows of the
 // blocks that clear the threshold bucket are then prefetched into L2 for the attention.
-cudaError_t launch_topk_select(const float *scores, int64_t n_full, int64_t k_blk, int64_t n_ctx,
-                               uint32_t *hist, void *scratch, int32_t *blocks_out,
-                               int32_t *counts_out, int32_t *pos_out, int32_t *n_cells_out,
+// Several queries (n_q <= kMaxStreamQueries, the last n_q tokens of the context: query i
+// at position n_ctx - n_q + i, candidates b < min(n_full, floor((p_i+1)/4))) run as
+// grid.y = n_q: query i reads scores + i*ld_scores and hist + i*2^kTopkHistBits, uses
+// the scratch at scratch + i*topk_select_workspace_bytes(n_full_cap) and writes
+// blocks_out + i*k_blk, counts_out + i, pos_out + i*max_cells, n_cells_out + i.
+// Returns cudaErrorNotSupported when some query has no more candidates than k_blk.
+cudaError_t launch_topk_select(const float *scores, int64_t ld_scores, int n_q, int64_t n_full,
+                               int64_t n_full_cap, int64_t k_blk, int64_t n_ctx, uint32_t *hist,
+                               void *scratch, int32_t *blocks_out, int32_t *counts_out,
+                               int32_t *pos_out, int32_t *n_cells_out, int64_t max_cells,
                                const void *kv_k, const void *kv_v, int64_t kv_row_bytes,
                                cudaStream_t st);
 size_t topk_select_workspace_bytes(int64_t n_full_cap);

@@ -478,7 +478,7 @@ topk_kernel(const float *__restrict__ scores, int64_t ld, const int32_t *__restr
             int64_t n_full_cap, int k_blk, int32_t *__restrict__ blocks_out,
             int32_t *__restrict__ counts_out, int64_t n_ctx, int32_t *__restrict__ pos_out,
             int32_t *__restrict__ n_cells_out, int64_t max_cells, uint32_t *__restrict__ ext_hist,
-            int cand_cap)
+            int cand_cap, int64_t p_step)
 {
     extern __shared__ __align__(16) uint32_t smem[];
     const int64_t qi = blockIdx.x;
@@ -488,9 +488,12 @@ topk_kernel(const float *__restrict__ scores, int64_t ld, const int32_t *__restr
     QSA_AFTER_WAIT(ext_hist);
     pdl_trigger();
 
-    const int64_t p = q_pos ? (int64_t)q_pos[qi] : n_ctx - 1;  // the query's position
+    // the query's position: q_pos[qi], else n_ctx - 1 - p_step * (n_q - 1 - qi) (the last
+    // n_q tokens of the context when p_step = 1; every query at n_ctx - 1 when it is 0)
+    const int64_t p = q_pos ? (int64_t)q_pos[qi]
+                            : n_ctx - 1 - p_step * ((int64_t)gridDim.x - 1 - qi);
     int64_t n = n_full_cap;
-    if (q_pos) {
+    if (q_pos || p_step) {
         const int64_t p1 = (p + 1) / 4;
         n = p1 < n ? p1 : n;
     }
@@ -516,18 +519,29 @@ topk_kernel(const float *__restrict__ scores, int64_t ld, const int32_t *__restr
     topk_query(scores + qi * ld, n, k, out, pout, pvec, ehist, cand_cap, smem);
 }
 
-// The decode form (one query, n > k): see the file comment.  Grid ceil(n / 1024) CTAs of
-// 1024 threads; CTA c classifies blocks [1024c, 1024c + 1024).  hist: the score kernel's
-// histogram of the n full blocks; ticket: set to 0 by the score kernel of this step.
-// Scratch: bitmap [ceil(n/32)] words, cand [grid][1024] (key, block), cand_cnt [grid].
+// Byte offset of a pointer (the per-query copies of the decode top-k's scratch).
+template <typename P>
+__device__ __forceinline__ P *byte_shift(P *p, int64_t bytes)
+{
+    return reinterpret_cast<P *>(reinterpret_cast<char *>(p) + bytes);
+}
+
+// The decode form (n > k for every query): see the file comment.  Grid ceil(n_full / 1024)
+// x n_q CTAs of 1024 threads; CTA (c, i) classifies blocks [1024c, 1024c + 1024) of query
+// i, the query at position p_i = n_ctx - n_q + i, whose candidates are the blocks
+// b < n_i = min(n_full, floor((p_i+1)/4)).  hist: the score kernel's histograms of those
+// blocks (2^kTopkHistBits words per query); ticket: set to 0 by the score kernel of this
+// step.  Scratch per query (query i's at byte offset i * q_stride): bitmap [ceil(n/32)]
+// words, cand [grid.x][1024] (key, block), cand_cnt [grid.x].
 __global__ void __launch_bounds__(NT)
-topk_select_kernel(const float *__restrict__ scores, int64_t n, int k_blk, int64_t n_ctx,
-                   uint32_t *__restrict__ hist, uint32_t *__restrict__ ticket,
-                   uint32_t *__restrict__ bitmap, uint2 *__restrict__ cand,
-                   int32_t *__restrict__ cand_cnt, int32_t *__restrict__ blocks_out,
-                   int32_t *__restrict__ counts_out, int32_t *__restrict__ pos_out,
-                   int32_t *__restrict__ n_cells_out, int cand_cap, const char *kv_k,
-                   const char *kv_v, uint32_t kv_block_bytes)
+topk_select_kernel(const float *__restrict__ scores, int64_t ld_scores, int n_q, int64_t n_full,
+                   int k_blk, int64_t n_ctx, uint32_t *__restrict__ hist,
+                   uint32_t *__restrict__ ticket, uint32_t *__restrict__ bitmap,
+                   uint2 *__restrict__ cand, int32_t *__restrict__ cand_cnt, int64_t q_stride,
+                   int32_t *__restrict__ blocks_out, int32_t *__restrict__ counts_out,
+                   int32_t *__restrict__ pos_out, int32_t *__restrict__ n_cells_out,
+                   int64_t max_cells, int cand_cap, const char *kv_k, const char *kv_v,
+                   uint32_t kv_block_bytes)
 {
     extern __shared__ __align__(16) uint32_t smem[];
     __shared__ uint32_t wtot[NT / 32];
@@ -544,6 +558,21 @@ topk_select_kernel(const float *__restrict__ scores, int64_t n, int k_blk, int64
     QSA_AFTER_WAIT(kv_k);
     QSA_AFTER_WAIT(kv_v);
     pdl_trigger();
+
+    // this CTA's query
+    const int qi = (int)blockIdx.y;
+    const int64_t p_q = n_ctx - n_q + qi;
+    const int64_t n = (p_q + 1) / 4 < n_full ? (p_q + 1) / 4 : n_full;
+    scores += qi * ld_scores;
+    hist += (int64_t)qi << kTopkHistBits;
+    ticket = byte_shift(ticket, qi * q_stride);
+    bitmap = byte_shift(bitmap, qi * q_stride);
+    cand = byte_shift(cand, qi * q_stride);
+    cand_cnt = byte_shift(cand_cnt, qi * q_stride);
+    blocks_out += (int64_t)qi * k_blk;
+    counts_out += qi;
+    if (pos_out) pos_out += qi * max_cells;
+    if (n_cells_out) n_cells_out += qi;
 
     const int64_t k = k_blk;
     const int64_t nw = (n + 31) / 32;
@@ -645,7 +674,7 @@ topk_select_kernel(const float *__restrict__ scores, int64_t n, int k_blk, int64
     // ---- the last CTA: every other CTA's bitmap words and candidates are visible
     int32_t *pout = pos_out;
     const bool pvec = (reinterpret_cast<uintptr_t>(pout) & 15) == 0;
-    write_count_tail(k, n_ctx - 1, counts_out, pout, n_cells_out);
+    write_count_tail(k, p_q, counts_out, pout, n_cells_out);
     // the general form's layout, its histogram area holding the candidates and the lists
     // cp [1024]: candidates packed as key << 32 | ~block, so that one unsigned comparison
     // orders them by key descending, then block ascending
@@ -779,13 +808,18 @@ size_t topk_select_workspace_bytes(int64_t n_full_cap)
     return (size_t)(256 + al(4 * g) + al(8 * g * NT) + al(4 * nw));
 }
 
-cudaError_t launch_topk_select(const float *scores, int64_t n_full, int64_t k_blk, int64_t n_ctx,
-                               uint32_t *hist, void *scratch, int32_t *blocks_out,
-                               int32_t *counts_out, int32_t *pos_out, int32_t *n_cells_out,
+cudaError_t launch_topk_select(const float *scores, int64_t ld_scores, int n_q, int64_t n_full,
+                               int64_t n_full_cap, int64_t k_blk, int64_t n_ctx, uint32_t *hist,
+                               void *scratch, int32_t *blocks_out, int32_t *counts_out,
+                               int32_t *pos_out, int32_t *n_cells_out, int64_t max_cells,
                                const void *kv_k, const void *kv_v, int64_t kv_row_bytes,
                                cudaStream_t st)
 {
-    if (n_full <= k_blk || n_full > kMaxN) return cudaErrorNotSupported;
+    // the first query has the fewest candidates
+    const int64_t p0 = n_ctx - n_q;
+    const int64_t n_min = (p0 + 1) / 4 < n_full ? (p0 + 1) / 4 : n_full;
+    if (n_q < 1 || n_q > 65535 || n_min <= k_blk || n_full > kMaxN || n_full > n_full_cap)
+        return cudaErrorNotSupported;
     if (!kv_k || !kv_v || kv_row_bytes <= 0 || kv_row_bytes % 16 || 4 * kv_row_bytes > (1 << 20) ||
         (reinterpret_cast<uintptr_t>(kv_k) | reinterpret_cast<uintptr_t>(kv_v)) % 16)
         kv_k = kv_v = nullptr;
@@ -804,10 +838,11 @@ cudaError_t launch_topk_select(const float *scores, int64_t n_full, int64_t k_bl
     const size_t smem = sizeof(uint32_t) * (size_t)(kFixedWords + 2 * nw);
     cudaError_t e = set_max_smem();
     if (e != cudaSuccess) return e;
-    return launch(topk_select_kernel, dim3((unsigned)g), dim3(NT), smem, st, 1, scores, n_full,
-                  (int)k_blk, n_ctx, hist, ticket, bitmap, cand, cand_cnt, blocks_out, counts_out,
-                  pos_out, n_cells_out, cand_cap, (const char *)kv_k, (const char *)kv_v,
-                  (uint32_t)(4 * kv_row_bytes));
+    const int64_t q_stride = (int64_t)topk_select_workspace_bytes(n_full_cap);
+    return launch(topk_select_kernel, dim3((unsigned)g, (unsigned)n_q), dim3(NT), smem, st, 1,
+                  scores, ld_scores, n_q, n_full, (int)k_blk, n_ctx, hist, ticket, bitmap, cand,
+                  cand_cnt, q_stride, blocks_out, counts_out, pos_out, n_cells_out, max_cells,
+                  cand_cap, (const char *)kv_k, (const char *)kv_v, (uint32_t)(4 * kv_row_bytes));
 }
 
 uint32_t *topk_select_ticket(void *scratch) { return static_cast<uint32_t *>(scratch); }
@@ -815,7 +850,7 @@ uint32_t *topk_select_ticket(void *scratch) { return static_cast<uint32_t *>(scr
 cudaError_t launch_topk(const float *scores, int64_t n_q, int64_t ld, const int32_t *q_pos,
                         int64_t n_full, int64_t k_blk, int32_t *blocks_out, int32_t *counts_out,
                         int64_t n_ctx, int32_t *pos_out, int32_t *n_cells_out,
-                        int64_t max_cells, uint32_t *ext_hist, cudaStream_t st)
+                        int64_t max_cells, uint32_t *ext_hist, cudaStream_t st, int64_t p_step)
 {
     if (n_q == 0) return cudaSuccess;
     int cand_cap = 0;
@@ -824,7 +859,7 @@ cudaError_t launch_topk(const float *scores, int64_t n_q, int64_t ld, const int3
     if (e != cudaSuccess) return e;
     return launch(topk_kernel, dim3((unsigned)n_q), dim3(NT), smem, st, 1, scores, ld, q_pos,
                   n_full, (int)k_blk, blocks_out, counts_out, n_ctx, pos_out, n_cells_out,
-                  max_cells, ext_hist, cand_cap);
+                  max_cells, ext_hist, cand_cap, p_step);
 }
 
 }  // namespace qsa

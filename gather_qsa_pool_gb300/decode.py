@@ -1,14 +1,18 @@
 """One QSA layer's decode step through the C ABI.
 
 ``DecodeLayer`` owns the device buffers of one QSA layer (the persistent pooled-key
-cache, scores, selected blocks, cell list, split-K workspace, output) and issues the
+cache, scores, selected blocks, cell lists, split-K workspace, output) and issues the
 five library calls of a decode step on the current stream:
 
     qsa_pool_update -> qsa_index_score -> qsa_topk_blocks -> qsa_gather_kv
                     -> qsa_sparse_attn
 
+either as the one fused call ``qsa_decode_step`` or one by one.  A step may carry up to
+four query tokens (a token and the draft tokens that follow it, verified together): they
+are the last ``n_q`` tokens of the context and share one scan of the pooled cache.
+
 The raw indexer-key cache and the K/V cache belong to the caller (the model writes the
-new token's rows before the step).  The gather call only builds the cell list; the
+new tokens' rows before the step).  The gather call only builds the cell lists; the
 attention kernel stages the listed K/V rows straight from the cache.
 """
 from __future__ import annotations
@@ -20,7 +24,10 @@ from . import _binding as qb
 
 class DecodeLayer:
     def __init__(self, *, cap_tokens, H_idx, d_idx, H_q, H_kv, d, top_k_tokens,
-                 eps=1e-6, rope_base=10000.0, device="cuda"):
+                 eps=1e-6, rope_base=10000.0, pooled_dtype=None, max_queries=1,
+                 device="cuda"):
+        """pooled_dtype: torch.float32 (default) or torch.bfloat16 storage of the pooled
+        cache.  max_queries: the most query tokens one step carries (1..4)."""
         import torch
 
         self.H_idx, self.d_idx = H_idx, d_idx
@@ -29,17 +36,21 @@ class DecodeLayer:
         self.eps, self.rope_base = eps, rope_base
         self.max_cells = 4 * self.k_blk + 3
         self.cap_rows = (cap_tokens + 3) // 4
+        self.max_queries = max_queries
         f32, i32 = torch.float32, torch.int32
-        self.pooled = torch.zeros(self.cap_rows, H_idx * d_idx, dtype=f32, device=device)
-        self.scores = torch.zeros(1, self.cap_rows, dtype=f32, device=device)
-        self.blocks = torch.zeros(1, self.k_blk, dtype=i32, device=device)
-        self.counts = torch.zeros(1, dtype=i32, device=device)
-        self.pos = torch.zeros(1, self.max_cells, dtype=i32, device=device)
-        self.n_cells = torch.zeros(1, dtype=i32, device=device)
-        self.out = torch.zeros(1, H_q, d, dtype=f32, device=device)
-        self.lse = torch.zeros(1, H_q, dtype=f32, device=device)
-        ws = qb.decode_step_workspace_size(H_q, H_kv, d, self.max_cells, self.cap_rows)
-        # zero-filled once: the step keeps its top-k histogram cleared from then on
+        nq = max_queries
+        pdt = f32 if pooled_dtype is None else pooled_dtype
+        self.pooled = torch.zeros(self.cap_rows, H_idx * d_idx, dtype=pdt, device=device)
+        # scores of a step are packed [n_q][n_rows] at the start of this buffer
+        self.scores = torch.zeros(nq * self.cap_rows, dtype=f32, device=device)
+        self.blocks = torch.zeros(nq, self.k_blk, dtype=i32, device=device)
+        self.counts = torch.zeros(nq, dtype=i32, device=device)
+        self.pos = torch.zeros(nq, self.max_cells, dtype=i32, device=device)
+        self.n_cells = torch.zeros(nq, dtype=i32, device=device)
+        self.out = torch.zeros(nq, H_q, d, dtype=f32, device=device)
+        self.lse = torch.zeros(nq, H_q, dtype=f32, device=device)
+        ws = qb.decode_step_workspace_size(H_q, H_kv, d, self.max_cells, self.cap_rows, nq)
+        # zero-filled once: the step keeps its top-k histograms cleared from then on
         self.workspace = torch.zeros(max(ws // 4, 1), dtype=f32, device=device)
         self.n_valid_full = 0
 
@@ -50,40 +61,50 @@ class DecodeLayer:
         self.n_valid_full = n_ctx // 4
 
     def invalidate(self, first_changed_token):
-        """Rows from the block holding ``first_changed_token`` on are recomputed next step."""
+        """Rows from the block holding ``first_changed_token`` on are recomputed next step
+        (e.g. after rejected draft tokens are rolled back)."""
         self.n_valid_full = min(self.n_valid_full, first_changed_token // 4)
 
-    def step(self, raw_k, norm_w, K, V, n_ctx, q_idx, q, stream=None):
-        """Decode step at context length n_ctx (the current token is position n_ctx-1).
+    def scores_of(self, n_q, n_ctx):
+        """The last step's scores as [n_q][n_rows]."""
+        n_rows = (n_ctx + 3) // 4
+        return self.scores[:n_q * n_rows].view(n_q, n_rows)
 
-        q_idx: [H_idx*d_idx] fp32, q: [H_q][d] fp32.  Returns the output [1][H_q][d]
-        (a view into this layer's buffer, overwritten by the next step)."""
+    def step(self, raw_k, norm_w, K, V, n_ctx, q_idx, q, stream=None):
+        """Decode step at context length n_ctx for the last n_q tokens (the current token
+        is position n_ctx-1).
+
+        q_idx: [n_q][H_idx*d_idx] (or [H_idx*d_idx]) fp32, q: [n_q][H_q][d] (or [H_q][d])
+        fp32.  Returns the output [n_q][H_q][d] (a view into this layer's buffer,
+        overwritten by the next step)."""
+        n_q = q_idx.shape[0] if q_idx.dim() > 1 else 1
         qb.decode_step(raw_k, n_ctx, self.H_idx, self.d_idx, norm_w, self.eps, self.rope_base,
                        self.pooled, self.n_valid_full, q_idx, 1.0 / math.sqrt(self.d_idx),
                        self.scores, self.k_blk, self.blocks, self.counts, K, V, self.H_kv,
                        self.d, self.pos, self.n_cells, self.max_cells, q, self.H_q,
-                       1.0 / math.sqrt(self.d), self.out, self.lse, self.workspace, stream)
+                       1.0 / math.sqrt(self.d), self.out, self.lse, self.workspace, n_q, stream)
         self.n_valid_full = n_ctx // 4
-        return self.out
+        return self.out[:n_q]
 
     def bind(self, raw_k, norm_w, K, V):
         """Fix the caller-owned caches for ``step_ptr`` (pointers resolved once)."""
         self._lib = qb.load()
         self._fixed = (raw_k.data_ptr(), qb._dtype(raw_k), norm_w.data_ptr(),
-                       self.pooled.data_ptr(), self.pooled.shape[0], self.scores.data_ptr(),
-                       self.blocks.data_ptr(), self.counts.data_ptr(), K.data_ptr(), V.data_ptr(),
-                       qb._dtype(K), K.shape[0], qb._ld(K), self.pos.data_ptr(),
-                       self.n_cells.data_ptr(), self.out.data_ptr(), self.lse.data_ptr(),
-                       self.workspace.data_ptr(), self.workspace.numel() * 4)
+                       self.pooled.data_ptr(), qb._dtype(self.pooled), self.pooled.shape[0],
+                       self.scores.data_ptr(), self.blocks.data_ptr(), self.counts.data_ptr(),
+                       K.data_ptr(), V.data_ptr(), qb._dtype(K), K.shape[0], qb._ld(K),
+                       self.pos.data_ptr(), self.n_cells.data_ptr(), self.out.data_ptr(),
+                       self.lse.data_ptr(), self.workspace.data_ptr(),
+                       self.workspace.numel() * 4)
 
-    def step_ptr(self, n_ctx, q_idx_ptr, q_ptr, stream_ptr):
+    def step_ptr(self, n_ctx, q_idx_ptr, q_ptr, stream_ptr, n_q=1):
         """Decode step on caches fixed by ``bind``; q_idx / q given as device pointers."""
-        (raw, raw_dt, w, pooled, cap, scores, blocks, counts, K, V, kv_dt, n_kv, ld, pos,
+        (raw, raw_dt, w, pooled, pdt, cap, scores, blocks, counts, K, V, kv_dt, n_kv, ld, pos,
          n_cells, out, lse, ws, ws_bytes) = self._fixed
         st = self._lib.qsa_decode_step(
-            raw, raw_dt, n_ctx, self.H_idx, self.d_idx, w, self.eps, self.rope_base, pooled,
-            cap, self.n_valid_full, q_idx_ptr, 1.0 / math.sqrt(self.d_idx), scores, self.k_blk,
-            blocks, counts, K, V, kv_dt, n_kv, self.H_kv, self.d, ld, pos, n_cells,
+            raw, raw_dt, n_ctx, self.H_idx, self.d_idx, w, self.eps, self.rope_base, pooled, pdt,
+            cap, self.n_valid_full, n_q, q_idx_ptr, 1.0 / math.sqrt(self.d_idx), scores,
+            self.k_blk, blocks, counts, K, V, kv_dt, n_kv, self.H_kv, self.d, ld, pos, n_cells,
             self.max_cells, q_ptr, self.H_q, 1.0 / math.sqrt(self.d), out, lse, ws, ws_bytes,
             stream_ptr)
         if st != 0:
@@ -92,18 +113,28 @@ class DecodeLayer:
 
     def step_separate_calls(self, raw_k, norm_w, K, V, n_ctx, q_idx, q, stream=None):
         """The same step issued as the five individual C calls."""
+        import torch
+
+        q_idx = q_idx.view(-1, self.H_idx * self.d_idx)
+        n_q = q_idx.shape[0]
         n_rows = (n_ctx + 3) // 4
         n_full = n_ctx // 4
         qb.pool_update(raw_k, n_ctx, self.H_idx, self.d_idx, norm_w, self.eps, self.rope_base,
                        self.pooled, self.n_valid_full, stream)
         self.n_valid_full = n_full
-        qb.index_score(q_idx.view(1, -1), self.pooled, n_rows, self.H_idx, self.d_idx,
-                       1.0 / math.sqrt(self.d_idx), self.scores, stream=stream)
-        qb.topk_blocks(self.scores, n_full, self.k_blk, self.blocks, self.counts, stream=stream)
-        qb.gather_kv(self.blocks, self.counts, self.k_blk, self.pos, self.n_cells,
-                     self.max_cells, n_ctx=n_ctx, n_kv=K.shape[0], stream=stream)
-        qb.sparse_attn(q.view(1, self.H_q, self.d), K, V, self.n_cells, self.max_cells,
-                       self.out, self.H_kv, self.d, self.d, 1.0 / math.sqrt(self.d),
-                       pos=self.pos, lse=self.lse, workspace=self.workspace,
+        scores = self.scores_of(n_q, n_ctx)
+        qb.index_score(q_idx, self.pooled, n_rows, self.H_idx, self.d_idx,
+                       1.0 / math.sqrt(self.d_idx), scores, stream=stream)
+        q_pos = None
+        if n_q > 1:
+            q_pos = torch.arange(n_ctx - n_q, n_ctx, dtype=torch.int32, device=q_idx.device)
+        qb.topk_blocks(scores, n_full, self.k_blk, self.blocks[:n_q], self.counts[:n_q],
+                       q_pos=q_pos, stream=stream)
+        qb.gather_kv(self.blocks[:n_q], self.counts[:n_q], self.k_blk, self.pos[:n_q],
+                     self.n_cells[:n_q], self.max_cells, n_ctx=n_ctx, q_pos=q_pos,
+                     n_kv=K.shape[0], stream=stream)
+        qb.sparse_attn(q.view(n_q, self.H_q, self.d), K, V, self.n_cells[:n_q], self.max_cells,
+                       self.out[:n_q], self.H_kv, self.d, self.d, 1.0 / math.sqrt(self.d),
+                       pos=self.pos[:n_q], lse=self.lse[:n_q], workspace=self.workspace,
                        ld_k=self.H_kv * self.d, ld_v=self.H_kv * self.d, stream=stream)
-        return self.out
+        return self.out[:n_q]

@@ -75,22 +75,26 @@ int qsa_version(void);
  *   p   = mean of the raw indexer keys of the tokens of block b present in n_ctx
  *   y_h = p_h / sqrt(mean_j p_h[j]^2 + eps) * norm_w        (each indexer head h)
  *   z_h = RoPE(y_h, position 4b): dims i and i + d/2 rotate by 4b * base^(-2i/d)
- *   pooled[b][h*d .. h*d+d) = z_h  (fp32; the angle is formed in fp64)
+ *   pooled[b][h*d .. h*d+d) = z_h  (the angle is formed in fp64; computed in fp32 and
+ *                                   stored as fp32, or as bf16 rounded to nearest even)
  * Rows below n_valid_full are not touched.  Invalidation after a state load, a
  * sequence edit or a rolled-back speculative write is done by passing a smaller
  * n_valid_full (e.g. floor(first_changed_position / 4)).
  *
  *   raw_k      [n_ctx][H][d] raw indexer keys, dtype raw_dtype (row stride H*d)
  *   norm_w     [d] fp32 RMS-norm weight shared by all indexer heads
- *   pooled     [cap_rows][H*d] fp32 cache, updated in place
+ *   pooled     [cap_rows][H*d] cache of type pooled_dtype (QSA_F32, or QSA_BF16: half
+ *              the bytes for the score scan to read), updated in place
  *   n_valid_full  rows [0, n_valid_full) are known to be valid; 0 <= n_valid_full
  *              (values above n_full are clamped to n_full)
  * Errors: INVALID_ARG for null pointers, n_ctx < 0, H < 1, d < 2 or odd d,
- * n_valid_full < 0, or n_rows > cap_rows.
+ * n_valid_full < 0, an unknown dtype, a misaligned pooled pointer, or
+ * n_rows > cap_rows.
  */
 qsa_status qsa_pool_update(const void *raw_k, qsa_dtype raw_dtype, int64_t n_ctx, int H, int d,
-                           const float *norm_w, float eps, double rope_base, float *pooled,
-                           int64_t cap_rows, int64_t n_valid_full, qsa_stream_t stream);
+                           const float *norm_w, float eps, double rope_base, void *pooled,
+                           qsa_dtype pooled_dtype, int64_t cap_rows, int64_t n_valid_full,
+                           qsa_stream_t stream);
 
 /*
  * qsa_index_score -- indexer score of every pooled row against each query.
@@ -102,24 +106,29 @@ qsa_status qsa_pool_update(const void *raw_k, qsa_dtype raw_dtype, int64_t n_ctx
  * When q_pos is not NULL (prefill chunk), row b is visible to query i only if the
  * block is complete at the query's position (4b + 3 <= q_pos[i]); other rows get
  * -inf.  When q_pos is NULL (decode), every row including the open one is scored.
+ * Up to four queries share one pass over the cache (each row is read once for all).
  *
  *   q          [n_q][ld_q] fp32 indexer queries (already position-encoded by the caller)
  *   q_pos      [n_q] int32 device positions, or NULL
- *   pooled     [n_rows][H*d] fp32
+ *   pooled     [n_rows][H*d] of type pooled_dtype (fp32 or bf16; the products and sums
+ *              are fp32 either way)
  *   scores     [n_q][ld_scores] fp32 output, ld_scores >= n_rows
- *   precision  QSA_PREC_F32 or QSA_PREC_BF16_TC (the latter needs the workspace)
+ *   precision  QSA_PREC_F32 or QSA_PREC_BF16_TC (q and an fp32 cache rounded to bf16
+ *              for the tensor cores; needs the workspace)
  *   workspace  caller scratch of qsa_index_score_workspace_size() bytes (may be NULL
  *              when that size is 0)
- * Errors: INVALID_ARG for null pointers, sizes < 0, ld_q < H*d, ld_scores < n_rows, or
- * a workspace smaller than required.
+ * Errors: INVALID_ARG for null pointers, sizes < 0, ld_q < H*d, ld_scores < n_rows, an
+ * unknown dtype, a misaligned pointer, or a workspace smaller than required.
  */
 qsa_status qsa_index_score(const float *q, int64_t n_q, int64_t ld_q, const int32_t *q_pos,
-                           const float *pooled, int64_t n_rows, int H, int d, float scale,
-                           float *scores, int64_t ld_scores, qsa_precision precision,
-                           void *workspace, size_t workspace_bytes, qsa_stream_t stream);
+                           const void *pooled, qsa_dtype pooled_dtype, int64_t n_rows, int H,
+                           int d, float scale, float *scores, int64_t ld_scores,
+                           qsa_precision precision, void *workspace, size_t workspace_bytes,
+                           qsa_stream_t stream);
 
+/* Workspace bytes of qsa_index_score (0 for QSA_PREC_F32; a bf16 cache needs no copy). */
 size_t qsa_index_score_workspace_size(int64_t n_q, int64_t n_rows, int H, int d,
-                                      qsa_precision precision);
+                                      qsa_dtype pooled_dtype, qsa_precision precision);
 
 /*
  * qsa_topk_blocks -- block-domain top-k.
@@ -220,45 +229,58 @@ size_t qsa_sparse_attn_workspace_size(int64_t n_q, int H_q, int H_kv, int d_v,
  * Source: same page as qsa_pool_update, sections "incremental pooled-key cache
  * (COMMON-004)", "selected K/V gather (COMMON-005)" and "block-domain top-k
  * (COMMON-006)" (the decode path: cached pooled keys -> scores -> block top-k -> selected
- * cells -> attention over them).
+ * cells -> attention over them).  Several query tokens per step (n_q > 1) serve
+ * speculative decoding, where a token and the draft tokens that follow it are verified
+ * in one pass (the pages' runs use multi-token prediction with two drafts): the queries
+ * are the last n_q tokens of the context and share one scan of the pooled cache.
  *
- * Equivalent to, on `stream`:
+ * Query i (0 <= i < n_q) sits at position p_i = n_ctx - n_q + i.  Equivalent to, on
+ * `stream`, with q_pos[i] = p_i:
  *   qsa_pool_update(raw_k, raw_dtype, n_ctx, H_idx, d_idx, norm_w, eps, rope_base, pooled,
- *                   cap_rows, n_valid_full)
- *   qsa_index_score(q_idx, 1, H_idx*d_idx, NULL, pooled, n_rows, H_idx, d_idx, scale_idx,
- *                   scores, n_rows, QSA_PREC_F32)
- *   qsa_topk_blocks(scores, 1, n_rows, NULL, n_full, k_blk, blocks, counts)
- *   qsa_gather_kv(K, V, kv_dtype, n_kv, H_kv, d, d, ld_kv, ld_kv, blocks, counts, 1, k_blk,
- *                 NULL, n_ctx, NULL, NULL, pos, n_cells, max_cells)     (cell list only)
- *   qsa_sparse_attn(q, 1, H_q, H_kv, d, d, scale, K, V, kv_dtype, n_kv, ld_kv, ld_kv, pos,
+ *                   pooled_dtype, cap_rows, n_valid_full)
+ *   qsa_index_score(q_idx, n_q, H_idx*d_idx, NULL, pooled, pooled_dtype, n_rows, H_idx,
+ *                   d_idx, scale_idx, scores, n_rows, QSA_PREC_F32)
+ *   qsa_topk_blocks(scores, n_q, n_rows, q_pos, n_full, k_blk, blocks, counts)
+ *   qsa_gather_kv(K, V, kv_dtype, n_kv, H_kv, d, d, ld_kv, ld_kv, blocks, counts, n_q,
+ *                 k_blk, q_pos, n_ctx, NULL, NULL, pos, n_cells, max_cells)  (cell lists)
+ *   qsa_sparse_attn(q, n_q, H_q, H_kv, d, d, scale, K, V, kv_dtype, n_kv, ld_kv, ld_kv, pos,
  *                   n_cells, max_cells, out, lse_out, workspace, workspace_bytes)
- * with n_rows = ceil(n_ctx/4), n_full = floor(n_ctx/4).  scores holds >= n_rows floats,
- * blocks k_blk ints, pos max_cells ints.  Results are identical to those calls; the work
- * is fused differently: when at most 4 pooled rows need recomputing (every decode step),
- * the score kernel recomputes them itself; it also counts the top 12 bits of each full
- * block's score key into a histogram kept in the workspace, which the top-k kernel
- * starts from (and clears for the next step); the top-k is one kernel whose CTAs each
- * classify 1024 blocks against that histogram and whose last CTA to finish settles the
- * threshold bucket, orders the output and writes the cell list itself; the attention
- * kernel reads the listed K/V rows in place.  Three launches in all.
+ * with n_rows = ceil(n_ctx/4), n_full = floor(n_ctx/4).  So every query scores every row,
+ * but query i selects only among the blocks complete at p_i, and its tail ends at p_i.
+ * With n_q = 1, q_pos = {n_ctx - 1} is the same as q_pos = NULL.
+ *   q_idx [n_q][H_idx*d_idx], scores [n_q][n_rows], blocks [n_q][k_blk], counts [n_q],
+ *   pos [n_q][max_cells], n_cells [n_q], q [n_q][H_q][d], out [n_q][H_q][d],
+ *   lse_out [n_q][H_q] (nullable); all packed.  1 <= n_q <= 4 and n_q <= n_ctx.
+ * Results are identical to those calls; the work is fused differently: when at most 4
+ * pooled rows need recomputing (every decode step), the score kernel recomputes them
+ * itself; it also counts the top 12 bits of the score key of each query's candidate
+ * blocks into a histogram per query kept in the workspace, which the top-k kernel starts
+ * from (and clears for the next step); the top-k is one kernel whose CTAs each classify
+ * 1024 blocks of one query against its histogram and whose last CTA to finish for a
+ * query settles its threshold bucket, orders its output and writes its cell list; the
+ * attention kernel reads the listed K/V rows in place.  Three launches in all.
  * workspace: qsa_decode_step_workspace_size() bytes, 256-byte aligned.  Its contents need
  * no initialisation: a histogram whose total disagrees with the block count (a workspace
  * never cleared) is rebuilt from the scores, which only makes that call slower; filling
  * it with zeros once avoids that.  Steps that share a workspace must not overlap in time.
- * Returns the first failing validation status without enqueuing anything.
+ * Returns the first failing validation status without enqueuing anything (INVALID_ARG
+ * for n_q outside [1, 4] or above n_ctx, and for a workspace sized for fewer queries or
+ * rows).
  */
 qsa_status qsa_decode_step(const void *raw_k, qsa_dtype raw_dtype, int64_t n_ctx, int H_idx,
                            int d_idx, const float *norm_w, float eps, double rope_base,
-                           float *pooled, int64_t cap_rows, int64_t n_valid_full,
-                           const float *q_idx, float scale_idx, float *scores, int64_t k_blk,
-                           int32_t *blocks, int32_t *counts, const void *K, const void *V,
-                           qsa_dtype kv_dtype, int64_t n_kv, int H_kv, int d, int64_t ld_kv,
-                           int32_t *pos, int32_t *n_cells, int64_t max_cells, const float *q,
-                           int H_q, float scale, float *out, float *lse_out, void *workspace,
-                           size_t workspace_bytes, qsa_stream_t stream);
+                           void *pooled, qsa_dtype pooled_dtype, int64_t cap_rows,
+                           int64_t n_valid_full, int64_t n_q, const float *q_idx, float scale_idx,
+                           float *scores, int64_t k_blk, int32_t *blocks, int32_t *counts,
+                           const void *K, const void *V, qsa_dtype kv_dtype, int64_t n_kv,
+                           int H_kv, int d, int64_t ld_kv, int32_t *pos, int32_t *n_cells,
+                           int64_t max_cells, const float *q, int H_q, float scale, float *out,
+                           float *lse_out, void *workspace, size_t workspace_bytes,
+                           qsa_stream_t stream);
 
-/* Workspace bytes of qsa_decode_step for a cache of up to cap_rows pooled rows. */
-size_t qsa_decode_step_workspace_size(int H_q, int H_kv, int d, int64_t max_cells,
+/* Workspace bytes of qsa_decode_step for n_q queries and a cache of up to cap_rows pooled
+ * rows (0 for an invalid shape). */
+size_t qsa_decode_step_workspace_size(int64_t n_q, int H_q, int H_kv, int d, int64_t max_cells,
                                       int64_t cap_rows);
 
 /*

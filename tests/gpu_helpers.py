@@ -43,10 +43,13 @@ def score_tolerance(q: np.ndarray, pooled: np.ndarray, n_rows: int, scale: float
 
 
 def check_topk(gpu_blocks: np.ndarray, gpu_count: int, oracle_scores: np.ndarray, n_full: int,
-               k_blk: int):
+               k_blk: int, band_abs=None):
     """GPU selection vs oracle scores: same count; every oracle-selected block outside the
     boundary band is selected, and no unselected block outside the band is.  Returns the
-    number of blocks inside the band (0 means the sets must be identical)."""
+    number of blocks inside the band (0 means the sets must be identical).
+    band_abs (optional, [n_full]): how far each block's GPU score may sit from the oracle's
+    for a reason other than summation order (a bf16 cache value rounded the other way);
+    it widens the band by the block's own amount plus the k-th block's."""
     k = min(k_blk, n_full)
     assert gpu_count == k
     sel = np.sort(gpu_blocks[:gpu_count].astype(np.int64))
@@ -57,7 +60,11 @@ def check_topk(gpu_blocks: np.ndarray, gpu_count: int, oracle_scores: np.ndarray
     s = np.nan_to_num(oracle_scores[:n_full], nan=-np.inf)
     order = np.lexsort((np.arange(n_full), -s))
     s_k = s[order[k - 1]]
-    band = np.abs(s - s_k) <= REL_TIE * abs(s_k) if np.isfinite(s_k) else (s == s_k)
+    if np.isfinite(s_k):
+        extra = 0.0 if band_abs is None else band_abs[:n_full] + band_abs[order[k - 1]]
+        band = np.abs(s - s_k) <= REL_TIE * abs(s_k) + extra
+    else:
+        band = s == s_k
     want = np.zeros(n_full, bool)
     want[order[:k]] = True
     got = np.zeros(n_full, bool)

@@ -36,20 +36,56 @@ def test_status_strings_and_version(lib):
 
 def test_pool_update_rejects(lib):
     s = None
-    assert lib.qsa_pool_update(None, 0, 10, 4, 64, FAKE, 1e-6, 1e4, FAKE, 10, 0, s) == 1
-    assert lib.qsa_pool_update(FAKE, 0, 10, 4, 63, FAKE, 1e-6, 1e4, FAKE, 10, 0, s) == 1  # odd d
-    assert lib.qsa_pool_update(FAKE, 0, 41, 4, 64, FAKE, 1e-6, 1e4, FAKE, 10, 0, s) == 1  # cap
-    assert lib.qsa_pool_update(FAKE, 0, 10, 4, 64, FAKE, 1e-6, 1e4, FAKE, 10, -1, s) == 1
-    assert lib.qsa_pool_update(FAKE, 7, 10, 4, 64, FAKE, 1e-6, 1e4, FAKE, 10, 0, s) == 1  # dtype
-    assert lib.qsa_pool_update(FAKE, 0, 10, 4, 64, FAKE, 1e-6, -1.0, FAKE, 10, 0, s) == 1
+    assert lib.qsa_pool_update(None, 0, 10, 4, 64, FAKE, 1e-6, 1e4, FAKE, 0, 10, 0, s) == 1
+    assert lib.qsa_pool_update(FAKE, 0, 10, 4, 63, FAKE, 1e-6, 1e4, FAKE, 0, 10, 0, s) == 1  # odd d
+    assert lib.qsa_pool_update(FAKE, 0, 41, 4, 64, FAKE, 1e-6, 1e4, FAKE, 0, 10, 0, s) == 1  # cap
+    assert lib.qsa_pool_update(FAKE, 0, 10, 4, 64, FAKE, 1e-6, 1e4, FAKE, 0, 10, -1, s) == 1
+    assert lib.qsa_pool_update(FAKE, 7, 10, 4, 64, FAKE, 1e-6, 1e4, FAKE, 0, 10, 0, s) == 1  # dtype
+    assert lib.qsa_pool_update(FAKE, 0, 10, 4, 64, FAKE, 1e-6, 1e4, FAKE, 5, 10, 0, s) == 1  # pooled
+    assert lib.qsa_pool_update(FAKE, 0, 10, 4, 64, FAKE, 1e-6, -1.0, FAKE, 0, 10, 0, s) == 1
+    # a bf16 cache must be 2-byte aligned
+    assert lib.qsa_pool_update(FAKE, 0, 10, 4, 64, FAKE, 1e-6, 1e4, P(0x10001), 1, 10, 0, s) == 1
 
 
 def test_index_score_rejects(lib):
     s = None
-    assert lib.qsa_index_score(None, 1, 256, None, FAKE, 10, 4, 64, 1.0, FAKE, 10, 0, None, 0, s) == 1
-    assert lib.qsa_index_score(FAKE, 1, 255, None, FAKE, 10, 4, 64, 1.0, FAKE, 10, 0, None, 0, s) == 1
-    assert lib.qsa_index_score(FAKE, 1, 256, None, FAKE, 10, 4, 64, 1.0, FAKE, 9, 0, None, 0, s) == 1
-    assert lib.qsa_index_score(FAKE, 1, 256, None, FAKE, 10, 4, 64, 1.0, FAKE, 10, 9, None, 0, s) == 1
+    args = [FAKE, 1, 256, None, FAKE, 0, 10, 4, 64, 1.0, FAKE, 10, 0, None, 0, s]
+
+    def call(**kw):
+        a = list(args)
+        for i, v in kw.items():
+            a[int(i[1:])] = v
+        return lib.qsa_index_score(*a)
+
+    assert call(a0=None) == 1
+    assert call(a2=255) == 1           # ld_q < H*d
+    assert call(a11=9) == 1            # ld_scores < n_rows
+    assert call(a12=9) == 1            # unknown precision
+    assert call(a5=3) == 1             # unknown pooled dtype
+    assert call(a4=P(0x10002)) == 1    # fp32 cache not 4-byte aligned
+    assert lib.qsa_index_score_workspace_size(4, 100, 16, 128, 1, 1) < \
+        lib.qsa_index_score_workspace_size(4, 100, 16, 128, 0, 1)  # a bf16 cache is read in place
+    assert lib.qsa_index_score_workspace_size(4, 100, 16, 128, 0, 0) == 0
+
+
+def test_decode_step_workspace_and_query_count(lib):
+    one = lib.qsa_decode_step_workspace_size(1, 32, 4, 128, 2051, 64000)
+    three = lib.qsa_decode_step_workspace_size(3, 32, 4, 128, 2051, 64000)
+    assert one > 0 and three > 2 * one
+    assert lib.qsa_decode_step_workspace_size(0, 32, 4, 128, 2051, 64000) == 0
+    assert lib.qsa_decode_step_workspace_size(5, 32, 4, 128, 2051, 64000) == 0
+    st = None
+
+    def step(n_q, n_ctx=1000, ws_bytes=1 << 30):
+        return lib.qsa_decode_step(FAKE, 1, n_ctx, 16, 128, FAKE, 1e-6, 1e4, FAKE, 0, 4000, 0,
+                                   n_q, FAKE, 0.1, FAKE, 512, FAKE, FAKE, FAKE, FAKE, 1, n_ctx, 4,
+                                   128, 512, FAKE, FAKE, 2051, FAKE, 32, 0.1, FAKE, None,
+                                   P(0x100000), ws_bytes, st)
+
+    assert step(0) == 1            # no query
+    assert step(5) == 1            # more than four
+    assert step(3, n_ctx=2) == 1   # more queries than tokens
+    assert step(3, ws_bytes=one) == 1  # workspace sized for one query
 
 
 def test_topk_rejects(lib):

@@ -51,7 +51,7 @@ def test_decode_61789_tokens_full_oracle():
         g_pooled = to_host(lay.pooled)[:n_rows]
         np.testing.assert_allclose(g_pooled, o_pooled[:n_rows], rtol=2e-5,
                                    atol=2e-6 * float(np.abs(o_pooled[:n_rows]).max()))
-        g_scores = to_host(lay.scores)[0, :n_rows]
+        g_scores = to_host(lay.scores)[:n_rows]
         tol = score_tolerance(inp["q_idx"][s], o_pooled, n_rows, 1.0 / math.sqrt(d))
         assert np.all(np.abs(g_scores - o_scores) <= tol)
         g_count = int(to_host(lay.counts)[0])
@@ -83,7 +83,7 @@ def test_decode_255181_tokens_sampled():
     rng = np.random.default_rng(7)
     rows = np.concatenate([rng.choice(n_full, 14, replace=False), [n_full - 1, n_rows - 1]])
     g_pooled = to_host(lay.pooled)
-    g_scores = to_host(lay.scores)[0, :n_rows].astype(np.float64)
+    g_scores = to_host(lay.scores)[:n_rows].astype(np.float64)
     for b in rows:
         z = oracle.pool_row_f64(inp["raw_k"], n_ctx, H, d, inp["norm_w"], shape.eps,
                                 shape.rope_base, int(b)).astype(np.float32)

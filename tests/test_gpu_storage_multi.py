@@ -1,0 +1,275 @@
+"""GPU parity of the bf16 pooled-key cache and of the multi-query decode step (a token and
+its draft tokens verified together) against the fp64 oracle on the same seeded inputs.
+Every input and every expected value comes from qsa_synth or the oracle.
+
+bf16 storage rule: the oracle rounds the exact (fp64) pooled value to bf16 once; the
+kernel rounds its fp32 value, which lies within delta (BF16_FLIP_REL of the rotation
+pair's magnitude) of the exact one.  So each stored value must be the bf16 rounding of
+some value within delta of the exact value: away from rounding midpoints (and from zero)
+that is the oracle's bits exactly, next to one either neighbour.  Scores and selections
+over a kernel-written bf16 cache widen the top-k boundary band by what such roundings
+can move a score.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import gather_qsa_pool_gb300 as qsa
+import qsa_synth
+from oracle import oracle
+from gpu_helpers import (ATOL_ATTN_BF16, ATOL_ATTN_F32, check_topk, score_tolerance, to_dev,
+                         to_host)
+
+pytestmark = pytest.mark.gpu
+
+TINY = qsa_synth.CONFIGS["tiny_f32_decode"]
+SMALL = qsa_synth.shrink(qsa_synth.CONFIGS["decode_64k"], name="small_bf16", n_ctx=9_003,
+                         top_k_tokens=512)
+# The kernel's fp32 pooled value: pooling, an RMS norm over d values, a weight and a
+# rotation, each a few roundings of 2^-24; 2^-17 of the pair's magnitude bounds them.
+BF16_FLIP_REL = 2.0 ** -17
+
+
+def _z64(inp, shape, n_ctx, rows):
+    H, d = shape.H_idx, shape.d_idx
+    return np.stack([oracle.pool_row_f64(inp["raw_k"], n_ctx, H, d, inp["norm_w"], shape.eps,
+                                         shape.rope_base, b) for b in rows])
+
+
+def _delta(z, d):
+    """Per element: the bound on the kernel's fp32 error, BF16_FLIP_REL of the magnitude of
+    the rotation pair (dims i and i + d/2 of a head) the element belongs to."""
+    zz = z.reshape(z.shape[0], -1, 2, d // 2)
+    pair = np.hypot(zz[:, :, 0, :], zz[:, :, 1, :])
+    return BF16_FLIP_REL * np.concatenate([pair, pair], axis=-1).reshape(z.shape)
+
+
+def _bf16_mag(bits):
+    return qsa_synth.bf16_bits_to_f32((bits & 0x7FFF).astype(np.uint16)).astype(np.float64)
+
+
+def _check_bf16_rows(got_bits, want_bits, z, d):
+    """Each stored bf16 value must be the rounding of some value within delta of the exact
+    one: |z| inside the value's rounding interval widened by delta (the sign may differ
+    only within delta of zero).  Returns how many values differ from the oracle's."""
+    delta = _delta(z, d)
+    mag = got_bits & 0x7FFF
+    g = _bf16_mag(got_bits)
+    lo = np.where(mag > 0, 0.5 * (_bf16_mag(np.maximum(mag, 1) - 1) + g), 0.0)
+    hi = 0.5 * (g + _bf16_mag(mag + 1))
+    a = np.abs(z)
+    sign_ok = ((got_bits >> 15) == (z < 0)) | (mag == 0)
+    ok = np.where(sign_ok, (a >= lo - delta) & (a <= hi + delta), g + a <= delta)
+    assert ok.all(), f"{int((~ok).sum())} stored values are not a rounding of the exact value"
+    return int((got_bits != want_bits).sum())
+
+
+def _flip_band(q, z, d, scale):
+    """Per row: how far the kernel's stored values can move a score from the oracle's (both
+    roundings of values within delta of the exact one): one bf16 step plus 2 delta at an
+    element whose exact value is within delta of a rounding midpoint or of zero."""
+    delta = _delta(z, d)
+    a = np.abs(z)
+    ulp = np.exp2(np.floor(np.log2(np.where(a > 0, a, 1.0))) - 7)
+    mid = (np.floor(a / ulp) + 0.5) * ulp
+    risky = (np.abs(a - mid) <= delta) | (a <= 2 * delta)
+    return scale * ((risky * (ulp + 2 * delta)) @ np.abs(q.astype(np.float64)).reshape(-1))
+
+
+# ------------------------------------------------------------------ bf16 pooled storage
+
+@pytest.mark.parametrize("shape", [TINY, SMALL], ids=lambda s: s.name)
+def test_pool_update_bf16_storage(shape):
+    inp = qsa_synth.decode_inputs(shape, seed=41)
+    n_ctx, H, d = shape.n_ctx, shape.H_idx, shape.d_idx
+    want = oracle.pool_rows(inp["raw_k"], n_ctx, H, d, inp["norm_w"], shape.eps,
+                            shape.rope_base, 0, shape.n_rows, store="bf16")
+    pooled = torch.zeros(shape.n_rows + 3, H * d, dtype=torch.bfloat16, device="cuda")
+    pooled[shape.n_rows:] = 5.0
+    qsa.pool_update(to_dev(inp["raw_k"]), n_ctx, H, d, to_dev(inp["norm_w"]), shape.eps,
+                    shape.rope_base, pooled, 0)
+    got = to_host(pooled)
+    z = _z64(inp, shape, n_ctx, range(shape.n_rows))
+    flips = _check_bf16_rows(got[:shape.n_rows], want, z, d)
+    assert flips <= 1e-3 * want.size  # rounding disagreements are rare
+    assert np.all(got[shape.n_rows:] == 0x40A0)  # rows past the cache end untouched
+
+
+@pytest.mark.parametrize("n_q", [1, 2, 3, 4])
+@pytest.mark.parametrize("store", ["f32", "bf16"])
+@pytest.mark.parametrize("causal", [False, True])
+def test_index_score_few_queries_one_pass(n_q, store, causal):
+    """1-4 queries share one pass over the cache (fp32 or bf16 rows); with q_pos the rows a
+    query cannot see are -inf."""
+    shape = qsa_synth.shrink(SMALL, n_ctx=20_001)
+    inp = qsa_synth.decode_inputs(shape, seed=42, n_steps=n_q)
+    H, d, n_rows = shape.H_idx, shape.d_idx, shape.n_rows
+    pooled = oracle.pool_rows(inp["raw_k"], shape.n_ctx, H, d, inp["norm_w"], shape.eps,
+                              shape.rope_base, 0, n_rows, store=store)
+    pvals = qsa_synth.bf16_bits_to_f32(pooled) if store == "bf16" else pooled
+    scale = 1.0 / math.sqrt(d)
+    q_pos = (np.array([5, 4000, 79_000, 80_000])[:n_q] % shape.n_ctx).astype(np.int32) \
+        if causal else None
+    want = oracle.scores(inp["q_idx"], pooled, n_rows, H, d, scale, q_pos=q_pos)
+    scores = torch.full((n_q, n_rows + 2), 3.0, device="cuda")
+    qsa.index_score(to_dev(inp["q_idx"]), to_dev(pooled), n_rows, H, d, scale, scores,
+                    q_pos=None if q_pos is None else to_dev(q_pos))
+    got = to_host(scores)
+    assert np.all(got[:, n_rows:] == 3.0)
+    for i in range(n_q):
+        vis = np.isfinite(want[i])
+        assert np.array_equal(np.isneginf(got[i, :n_rows]), ~vis)
+        tol = score_tolerance(inp["q_idx"][i], pvals, n_rows, scale)[vis]
+        assert np.all(np.abs(got[i, :n_rows][vis] - want[i][vis]) <= tol)
+
+
+def test_prefill_scores_on_tensor_cores_read_a_bf16_cache_in_place():
+    H, d, depth, n_q = 16, 128, 6000, 300
+    shape = qsa_synth.PrefillShape("tc_bf16", depth, n_q, H, d, 8, 2, 128, 256, dtype="bf16")
+    inp = qsa_synth.prefill_inputs(shape, seed=43)
+    n_rows = shape.n_rows
+    pooled = oracle.pool_rows(inp["raw_k"], shape.n_ctx, H, d, inp["norm_w"], shape.eps,
+                              shape.rope_base, 0, n_rows, store="bf16")
+    scale = 1.0 / math.sqrt(d)
+    ws_f32 = qsa.index_score_workspace_size(n_q, n_rows, H, d, qsa.QSA_PREC_BF16_TC)
+    ws_b = qsa.index_score_workspace_size(n_q, n_rows, H, d, qsa.QSA_PREC_BF16_TC, qsa.QSA_BF16)
+    assert ws_b < ws_f32
+    ws = torch.zeros(ws_b, dtype=torch.uint8, device="cuda")
+    scores = torch.zeros(n_q, n_rows, device="cuda")
+    qsa.index_score(to_dev(inp["q_idx"]), to_dev(pooled), n_rows, H, d, scale, scores,
+                    q_pos=to_dev(inp["q_pos"]), precision=qsa.QSA_PREC_BF16_TC, workspace=ws)
+    got = to_host(scores)
+    rows = np.random.default_rng(4).choice(n_q, 40, replace=False)
+    want = oracle.scores(inp["q_idx"][rows], pooled, n_rows, H, d, scale,
+                         q_pos=inp["q_pos"][rows], round_bf16_operands=True)
+    qb = np.array([oracle.round_bf16(float(x)) for x in inp["q_idx"][rows].reshape(-1)],
+                  np.float32).reshape(len(rows), -1)
+    pvals = qsa_synth.bf16_bits_to_f32(pooled)
+    for j, i in enumerate(rows):
+        vis = np.isfinite(want[j])
+        assert np.array_equal(np.isneginf(got[i]), ~vis)
+        tol = score_tolerance(qb[j], pvals, n_rows, scale, chain=H * d)[vis]
+        assert np.all(np.abs(got[i][vis] - want[j][vis]) <= tol)
+
+
+# ------------------------------------------------------------------ decode steps
+
+def _layer(shape, cap, store, max_queries):
+    return qsa.DecodeLayer(cap_tokens=cap, H_idx=shape.H_idx, d_idx=shape.d_idx, H_q=shape.H_q,
+                           H_kv=shape.H_kv, d=shape.d, top_k_tokens=shape.top_k_tokens,
+                           pooled_dtype=torch.bfloat16 if store == "bf16" else torch.float32,
+                           max_queries=max_queries)
+
+
+@pytest.mark.parametrize("shape", [TINY, SMALL], ids=lambda s: s.name)
+@pytest.mark.parametrize("store", ["f32", "bf16"])
+def test_multi_query_decode_steps_match_oracle(shape, store):
+    """Steps of 3, 1, 4 and 2 query tokens, each appending its tokens, against the oracle's
+    multi-query step: per query the selection (boundary band), the cell list and the
+    attention output; the pooled cache with the bf16 rule."""
+    plan = [3, 1, 4, 2]
+    extra = sum(plan)
+    inp = qsa_synth.decode_inputs(shape, seed=44, extra_tokens=extra, n_steps=extra)
+    H, d = shape.H_idx, shape.d_idx
+    raw, w = to_dev(inp["raw_k"]), to_dev(inp["norm_w"])
+    K, V = to_dev(inp["K"]), to_dev(inp["V"])
+    n0 = shape.n_ctx
+    lay = _layer(shape, n0 + extra, store, 4)
+    lay.rebuild(raw, w, n0)
+    cap_rows = (n0 + extra + 3) // 4
+    o_pooled = oracle.pool_rows(inp["raw_k"], n0, H, d, inp["norm_w"], shape.eps,
+                                shape.rope_base, 0, (n0 + 3) // 4,
+                                np.zeros((cap_rows, H * d),
+                                         np.uint16 if store == "bf16" else np.float32))
+    o_valid = n0 // 4
+    n_ctx, used, n_band = n0, 0, 0
+    atol = ATOL_ATTN_BF16 if shape.dtype == "bf16" else ATOL_ATTN_F32
+    scale = 1.0 / math.sqrt(d)
+    for n_q in plan:
+        n_ctx += n_q
+        qi = inp["q_idx"][used:used + n_q]
+        qa = inp["q"][used:used + n_q]
+        used += n_q
+        out = to_host(lay.step(raw, w, K, V, n_ctx, to_dev(qi), to_dev(qa)))
+        res, o_scores = oracle.decode_step_multi(
+            inp["raw_k"], n_ctx, H, d, inp["norm_w"], shape.eps, shape.rope_base, o_pooled,
+            o_valid, qi, shape.top_k_tokens, qa, inp["K"], inp["V"], shape.H_q, shape.H_kv,
+            shape.d)
+        o_valid = n_ctx // 4
+        n_rows = (n_ctx + 3) // 4
+        if store == "bf16":
+            z = _z64(inp, shape, n_ctx, range(n_rows))
+            _check_bf16_rows(to_host(lay.pooled)[:n_rows], o_pooled[:n_rows], z, d)
+        blocks = to_host(lay.blocks)
+        counts = to_host(lay.counts)
+        n_cells = to_host(lay.n_cells)
+        pos = to_host(lay.pos)
+        for i in range(n_q):
+            p = n_ctx - n_q + i
+            n_i = min(n_ctx // 4, (p + 1) // 4)
+            band_abs = _flip_band(qi[i], z[:n_i], d, scale) if store == "bf16" else None
+            n_band += check_topk(blocks[i], int(counts[i]), o_scores[i], n_i, shape.k_blk,
+                                 band_abs=band_abs)
+            o_blocks, o_cells, o_out, _ = res[i]
+            if np.array_equal(np.sort(blocks[i, :counts[i]]), o_blocks):
+                np.testing.assert_array_equal(pos[i, :n_cells[i]], o_cells)
+                np.testing.assert_allclose(out[i], o_out, rtol=0, atol=atol)
+            else:
+                assert len(np.sort(blocks[i, :counts[i]])) == len(o_blocks)
+    assert n_band < 20
+
+
+@pytest.mark.parametrize("store", ["f32", "bf16"])
+def test_multi_query_composite_equals_separate_calls(store):
+    """The fused step and the five calls (top-k and gather with q_pos = the last n_q
+    positions) give bit-identical cache, selections, cell lists and outputs."""
+    shape = SMALL
+    plan = [2, 3, 1, 4]
+    extra = sum(plan)
+    inp = qsa_synth.decode_inputs(shape, seed=45, extra_tokens=extra, n_steps=extra)
+    raw, w = to_dev(inp["raw_k"]), to_dev(inp["norm_w"])
+    K, V = to_dev(inp["K"]), to_dev(inp["V"])
+    a = _layer(shape, shape.n_ctx + extra, store, 4)
+    b = _layer(shape, shape.n_ctx + extra, store, 4)
+    a.rebuild(raw, w, shape.n_ctx - 1)
+    b.rebuild(raw, w, shape.n_ctx - 1)
+    n_ctx, used = shape.n_ctx - 1, 0
+    for n_q in plan:
+        n_ctx += n_q
+        qi = to_dev(inp["q_idx"][used:used + n_q])
+        qa = to_dev(inp["q"][used:used + n_q])
+        used += n_q
+        oa = a.step(raw, w, K, V, n_ctx, qi, qa).clone()
+        ob = b.step_separate_calls(raw, w, K, V, n_ctx, qi, qa).clone()
+        assert torch.equal(a.pooled, b.pooled)
+        assert torch.equal(a.scores_of(n_q, n_ctx), b.scores_of(n_q, n_ctx))
+        assert torch.equal(a.blocks[:n_q], b.blocks[:n_q])
+        assert torch.equal(a.counts[:n_q], b.counts[:n_q])
+        assert torch.equal(a.n_cells[:n_q], b.n_cells[:n_q])
+        for i in range(n_q):
+            nc = int(a.n_cells[i].item())
+            assert torch.equal(a.pos[i, :nc], b.pos[i, :nc])
+        assert torch.equal(oa, ob)
+
+
+def test_multi_query_small_context_takes_every_block():
+    """When a query has no more complete blocks than k, all of them are selected (the
+    one-CTA form) and its tail still ends at its own position."""
+    shape = qsa_synth.shrink(TINY, n_ctx=37)
+    inp = qsa_synth.decode_inputs(shape, seed=46, n_steps=3)
+    raw, w = to_dev(inp["raw_k"]), to_dev(inp["norm_w"])
+    K, V = to_dev(inp["K"]), to_dev(inp["V"])
+    lay = _layer(shape, 64, "f32", 3)
+    out = to_host(lay.step(raw, w, K, V, 37, to_dev(inp["q_idx"][:3]), to_dev(inp["q"][:3])))
+    res, _ = oracle.decode_step_multi(
+        inp["raw_k"], 37, shape.H_idx, shape.d_idx, inp["norm_w"], shape.eps, shape.rope_base,
+        np.zeros((10, shape.H_idx * shape.d_idx), np.float32), 0, inp["q_idx"][:3],
+        shape.top_k_tokens, inp["q"][:3], inp["K"], inp["V"], shape.H_q, shape.H_kv, shape.d)
+    for i in range(3):
+        o_blocks, o_cells, o_out, _ = res[i]
+        assert int(lay.counts[i].item()) == len(o_blocks)
+        np.testing.assert_array_equal(to_host(lay.blocks)[i, :len(o_blocks)], o_blocks)
+        np.testing.assert_array_equal(to_host(lay.pos)[i, :len(o_cells)], o_cells)
+        np.testing.assert_allclose(out[i], o_out, rtol=0, atol=ATOL_ATTN_F32)
