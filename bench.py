@@ -37,7 +37,7 @@ METRIC = "sparse-attn decode steps/s at 64k/128k/256k ctx; achieved HBM GB/s vs 
 CONTEXTS = {"64k": "decode_64k", "128k": "decode_128k", "256k": "decode_256k"}
 SCORE_SRCS = [os.path.join(ROOT, "gather_qsa_pool_gb300", "csrc", f)
               for f in ("index_score.cu", "score_stream.cuh")]
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "score_rows_256k_traffic.txt")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "score_stream_256k_traffic.txt")
 # Kernels one qsa_decode_step launches when it appends a token: the fused pool-update +
 # score scan, the top-k (whose last CTA also writes the cell list) and the attention
 # kernel (split-K with the combine inside its cluster).
@@ -59,6 +59,10 @@ def parse_args():
     ap.add_argument("--prefill-reps", type=int, default=5)
     ap.add_argument("--no-variants", action="store_true",
                     help="skip the bf16 pooled-cache and multi-query decode lines")
+    ap.add_argument("--pooled", choices=["f32", "bf16"], default="f32",
+                    help="pooled-key cache storage of the main sweep")
+    ap.add_argument("--queries", type=int, default=1, choices=[1, 2, 3, 4],
+                    help="query tokens per decode step of the main sweep")
     return ap.parse_args()
 
 
@@ -594,16 +598,18 @@ def oracle_decode_sample(shape, n_steps: int, budget_s: float, seed: int = 7):
     return done, t
 
 
-def config_for(shape, layers):
+def config_for(shape, layers, pooled="f32", n_q=1):
+    pes = 2 if pooled == "bf16" else 4
+    step = "+1 token per step" if n_q == 1 else f"{n_q} query tokens (+{n_q} tokens) per step"
     return {
         "workload": (f"bf16 decode, one QSA layer per step at {shape.n_ctx:,}-token context, "
-                     f"+1 token per step, {layers} rotating layer sets"),
+                     f"{step}, {layers} rotating layer sets"),
         "n_ctx": shape.n_ctx, "indexer": f"{shape.H_idx} heads x {shape.d_idx}",
         "attention": f"{shape.H_q} q heads / {shape.H_kv} kv heads x {shape.d}",
-        "top_k_tokens": shape.top_k_tokens, "layers": layers,
-        "storage": "bf16 K/V and raw indexer keys, fp32 pooled-key cache",
+        "top_k_tokens": shape.top_k_tokens, "layers": layers, "queries_per_step": n_q,
+        "storage": f"bf16 K/V and raw indexer keys, {pooled} pooled-key cache",
         "l2": (f"inputs larger than L2: {layers} rotating layer sets of "
-               f"{shape.n_rows * shape.H_idx * shape.d_idx * 4 / 1e6:.0f} MB pooled cache each"),
+               f"{shape.n_rows * shape.H_idx * shape.d_idx * pes / 1e6:.0f} MB pooled cache each"),
     }
 
 
@@ -649,7 +655,9 @@ def main():
     results = {}
     for name in names:
         results[name] = run_context(name, args, world, rank, local,
-                                    want_clocks=(name == args.primary and rank == 0))
+                                    want_clocks=(name == args.primary and rank == 0),
+                                    pooled=args.pooled, n_q=args.queries,
+                                    light=args.queries > 1)
     peak, peak_kind = load_peaks()
 
     sweep = {name: summarize(r, world, args.layers, peak) for name, r in results.items()}
@@ -669,9 +677,12 @@ def main():
     r = results[args.primary]
     sh = r["shape"]
     value = sweep[args.primary]["steps_per_s"]
-    score_bytes = r["score_rows"] * sh.H_idx * sh.d_idx * 4 + r["score_rows"] * 4
+    pes = 2 if args.pooled == "bf16" else 4
+    score_bytes = (r["score_rows"] * sh.H_idx * sh.d_idx * pes
+                   + args.queries * r["score_rows"] * 4)
     achieved = score_bytes / (r["score_us"] * 1e-6) / 1e9
-    traffic = traffic_per_launch(int(r["score_rows"]))
+    default_form = args.pooled == "f32" and args.queries == 1
+    traffic = traffic_per_launch(int(r["score_rows"])) if default_form else None
 
     prefill = None if args.no_prefill else run_prefill(args, local)
     mask = None if args.no_mask else run_mask(args, local)
@@ -690,14 +701,16 @@ def main():
         "steps": r["K"], "warmup": r["W"], "ms_per_step": r["ms"] / r["K"],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded N(0,1) keys/values/queries, 1% of blocks +3 on raw indexer keys)",
-        "config": config_for(sh, args.layers),
+        "config": config_for(sh, args.layers, args.pooled, args.queries),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "kernel": "score_stream_kernel (qsa_index_score, decode, fp32 cache)",
+                     "kernel": f"score_stream_kernel (qsa_index_score, decode, {args.pooled} "
+                               f"cache, {args.queries} quer{'y' if args.queries == 1 else 'ies'})",
                      "peak_source": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s"},
-        "e2e": {"value": sweep[args.primary]["e2e_steps_per_s"], "unit": "steps/s",
-                "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
+        "e2e": ({"value": sweep[args.primary]["e2e_steps_per_s"], "unit": "steps/s",
+                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]}
+                if "e2e_steps_per_s" in sweep[args.primary] else None),
         "gpu_launches": r["K"] * LAUNCHES_PER_DECODE_STEP,
         "clocks": r["clocks"],
         "sweep": sweep,
