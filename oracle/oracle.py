@@ -71,6 +71,7 @@ def _load():
             "oracle_scores": (None, [_p, _i64, _p, _i32, _i64, _i32, _i32, _d, _p, _i32, _p]),
             "oracle_topk": (_i64, [_p, _i64, _i64, _p]),
             "oracle_cells": (_i64, [_p, _i64, _i64, _p]),
+            "oracle_expand_block_scores": (None, [_p, _i64, _p]),
             "oracle_get_rows": (None, [_p, _i32, _i64, _i64, _p, _i64, _p]),
             "oracle_attention": (None, [_p, _i32, _i32, _i32, _i32, _p, _p, _i32, _i64, _i64,
                                         _p, _i64, _d, _p, _p]),
@@ -178,6 +179,16 @@ def topk(score_row, n_full, k_blk) -> np.ndarray:
     out = np.zeros(max(min(k_blk, n_full), 1), np.int32)
     k = _load().oracle_topk(_ptr(s), n_full, k_blk, _ptr(out))
     return out[:k].copy()
+
+
+def expand_block_scores(score_row, n_full) -> np.ndarray:
+    """Each full block's score copied to its 4 cells (the selection path before the block
+    domain): [4*n_full] fp64."""
+    s = _c(score_row, np.float64)
+    assert s.shape[0] >= n_full
+    out = np.zeros(max(4 * n_full, 1), np.float64)
+    _load().oracle_expand_block_scores(_ptr(s), n_full, _ptr(out))
+    return out[:4 * n_full].copy()
 
 
 def cells(blocks, p) -> np.ndarray:

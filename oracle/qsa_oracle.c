@@ -282,6 +282,18 @@ int64_t oracle_topk(const double *scores, int64_t n_full, int64_t k_blk, int32_t
     return k;
 }
 
+/*
+ * The pages' earlier selection path, kept for A/B measurement (p1, "block-domain top-k
+ * (COMMON-006)": before it, each block's score was copied to its 4 cells and the top-k
+ * ran over cells).  cells[c] = scores[floor(c/4)] for c < 4*n_full.
+ */
+void oracle_expand_block_scores(const double *scores, int64_t n_full, double *cells)
+{
+    for (int64_t b = 0; b < n_full; ++b)
+        for (int t = 0; t < 4; ++t)
+            cells[4 * b + t] = scores[b];
+}
+
 /* ------------------------------------------------------------------ step 4: cells */
 
 /*

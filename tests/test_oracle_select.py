@@ -105,6 +105,20 @@ def test_topk_equals_pages_old_cell_level_path():
     np.testing.assert_array_equal(new_blocks, old_blocks)
 
 
+def test_expand_block_scores_matches_library_repeat_and_cell_topk():
+    """The expansion step of the old path equals numpy's repeat; the oracle's top-k over the
+    expanded cells (ties to the lower cell) then picks whole blocks, the block-domain set."""
+    rng = np.random.default_rng(31)
+    n_full = 777
+    s = rng.standard_normal(n_full)
+    cells = oracle.expand_block_scores(s, n_full)
+    np.testing.assert_array_equal(cells, np.repeat(s, 4))
+    assert oracle.expand_block_scores(s, 0).shape == (0,)
+    top_cells = oracle.topk(cells, 4 * n_full, 512)
+    np.testing.assert_array_equal(np.unique(top_cells // 4), oracle.topk(s, n_full, 128))
+    assert np.all(np.bincount(top_cells // 4)[np.unique(top_cells // 4)] == 4)
+
+
 def test_topk_ties_go_to_lower_index_and_nan_ranks_last():
     s = np.array([1.0, 2.0, 2.0, 2.0, np.nan, 2.0, -np.inf, 0.5])
     np.testing.assert_array_equal(oracle.topk(s, 8, 3), [1, 2, 3])
