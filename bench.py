@@ -56,6 +56,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-mask", action="store_true")
+    ap.add_argument("--no-ablation", action="store_true",
+                    help="skip the timing of the pages' earlier path, piece by piece")
     ap.add_argument("--prefill-reps", type=int, default=5)
     ap.add_argument("--no-variants", action="store_true",
                     help="skip the bf16 pooled-cache and multi-query decode lines")
@@ -459,6 +461,98 @@ def run_prefill(args, local):
     return out_d
 
 
+def run_ablation(args, local):
+    """The pages' A/B on this GPU at 255,181 tokens: each piece of the QSA decode step next
+    to the piece it replaced -- the full pooled-cache rebuild (before the incremental cache),
+    the block score expanded to cells and a cell-level top-k (before the block-domain
+    top-k), attention over every cell of the context (before the selected-K/V gather).
+    CUDA events over a few repetitions after a warm-up call; returns microseconds."""
+    import torch
+
+    import gather_qsa_pool_gb300 as qsa
+    import qsa_synth
+
+    shape = qsa_synth.CONFIGS["decode_256k"]
+    dev = torch.device("cuda", local)
+    inp = qsa_synth.decode_inputs_torch(shape, seed=777, device=dev)
+    H, d, n_ctx = shape.H_idx, shape.d_idx, shape.n_ctx
+    n_rows, n_full, k_blk = shape.n_rows, shape.n_full, shape.k_blk
+    lay = qsa.DecodeLayer(cap_tokens=n_ctx, H_idx=H, d_idx=d, H_q=shape.H_q, H_kv=shape.H_kv,
+                          d=shape.d, top_k_tokens=shape.top_k_tokens, eps=shape.eps,
+                          rope_base=shape.rope_base, device=dev)
+    raw, w, K, V = inp["raw_k"], inp["norm_w"], inp["K"], inp["V"]
+    lay.rebuild(raw, w, n_ctx - 1)
+    lay.step(raw, w, K, V, n_ctx, inp["q_idx"][0], inp["q"][0])
+    q = inp["q"][:1]
+    scores = lay.scores_of(1, n_ctx)
+    blocks = torch.empty(1, k_blk, dtype=torch.int32, device=dev)
+    counts = torch.empty(1, dtype=torch.int32, device=dev)
+    cells = torch.empty(1, 4 * n_full, device=dev)
+    cell_sel = torch.empty(1, 4 * k_blk, dtype=torch.int32, device=dev)
+    out = torch.empty(1, shape.H_q, shape.d, device=dev)
+    all_pos = torch.arange(n_ctx, dtype=torch.int32, device=dev).view(1, n_ctx)
+    all_n = torch.tensor([n_ctx], dtype=torch.int32, device=dev)
+    ws = torch.zeros(max(qsa.sparse_attn_workspace_size(1, shape.H_q, shape.H_kv, shape.d, n_ctx)
+                         // 4, 1), device=dev)
+    scale_idx, scale = 1.0 / math.sqrt(d), 1.0 / math.sqrt(shape.d)
+    pieces = [
+        ("pool_full_rebuild", lambda: qsa.pool_update(raw, n_ctx, H, d, w, shape.eps,
+                                                      shape.rope_base, lay.pooled, 0)),
+        ("pool_incremental", lambda: qsa.pool_update(raw, n_ctx, H, d, w, shape.eps,
+                                                     shape.rope_base, lay.pooled, n_full - 1)),
+        ("score_scan", lambda: qsa.index_score(inp["q_idx"][:1], lay.pooled, n_rows, H, d,
+                                               scale_idx, scores)),
+        ("block_topk", lambda: qsa.topk_blocks(scores, n_full, k_blk, blocks, counts)),
+        ("expand_to_cells", lambda: qsa.expand_block_scores(scores, n_full, cells)),
+        ("cell_topk", lambda: qsa.topk_blocks(cells, 4 * n_full, 4 * k_blk, cell_sel, counts)),
+        ("attn_listed_cells", lambda: qsa.sparse_attn(q, K, V, lay.n_cells[:1], lay.max_cells,
+                                                      out, shape.H_kv, shape.d, shape.d, scale,
+                                                      pos=lay.pos[:1], workspace=lay.workspace)),
+        ("attn_full_kv", lambda: qsa.sparse_attn(q, K, V, all_n, n_ctx, out, shape.H_kv, shape.d,
+                                                 shape.d, scale, pos=all_pos, workspace=ws)),
+    ]
+    # each piece captured (reps calls) into a CUDA graph and replayed, so the device time is
+    # measured rather than the Python wrapper's issue time
+    res = {}
+    reps = 5
+    gs = torch.cuda.Stream(device=dev)
+    for name, fn in pieces:
+        fn()
+        torch.cuda.synchronize()
+        gs.wait_stream(torch.cuda.current_stream())
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(gs):
+            with torch.cuda.graph(graph, stream=gs):
+                for _ in range(reps):
+                    fn()
+        torch.cuda.synchronize()
+        graph.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        graph.replay()
+        b.record()
+        torch.cuda.synchronize()
+        res[name] = round(a.elapsed_time(b) * 1e3 / reps, 1)
+        del graph
+    n_listed = int(lay.n_cells[0].item())
+    out_d = {
+        "workload": (f"one layer at {n_ctx:,} tokens: {n_rows:,} pooled rows, {n_listed} listed "
+                     f"cells of {n_ctx:,}"),
+        "us": res,
+        "old_path_us": round(res["pool_full_rebuild"] + res["score_scan"] + res["expand_to_cells"]
+                             + res["cell_topk"] + res["attn_full_kv"], 1),
+        "qsa_pieces_us": round(res["pool_incremental"] + res["score_scan"] + res["block_topk"]
+                               + res["attn_listed_cells"], 1),
+        "note": ("pieces timed one at a time from CUDA-graph replays (the fused decode step "
+                 "overlaps them and uses the histogram-fed top-k); the old path is the sum of "
+                 "the pieces it ran"),
+    }
+    del lay, inp, cells, ws
+    torch.cuda.empty_cache()
+    return out_d
+
+
 def run_mask(args, local):
     """The mask-driven variant at 32,768 keys: mask -> position list (qsa_mask_to_list) and
     attention of 16 query heads over the listed keys (DKQ 576, d_v 512, bf16).  Eight
@@ -686,6 +780,7 @@ def main():
 
     prefill = None if args.no_prefill else run_prefill(args, local)
     mask = None if args.no_mask else run_mask(args, local)
+    ablation = None if args.no_ablation else run_ablation(args, local)
 
     cpu_baseline = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -717,6 +812,7 @@ def main():
         "variants": variants or None,
         "prefill": prefill,
         "mask": mask,
+        "ablation": ablation,
         "cpu_baseline": cpu_baseline,
     }
     if rank == 0:

@@ -12,6 +12,7 @@ from ._binding import (  # noqa: F401
     QSAError,
     decode_step,
     decode_step_workspace_size,
+    expand_block_scores,
     gather_kv,
     header_functions,
     index_score,

@@ -37,6 +37,7 @@ _SIGNATURES = {
     "qsa_index_score_workspace_size": (_sz, [_i64, _i64, _int, _int, _int, _int]),
     "qsa_topk_blocks": (_int, [_p, _i64, _i64, _p, _i64, _i64, _p, _p, _p]),
     "qsa_topk_max_candidates": (_i64, []),
+    "qsa_expand_block_scores": (_int, [_p, _i64, _i64, _i64, _p, _i64, _p]),
     "qsa_gather_kv": (_int, [_p, _p, _int, _i64, _int, _int, _int, _i64, _i64, _p, _p, _i64,
                              _i64, _p, _i64, _p, _p, _p, _p, _i64, _p]),
     "qsa_sparse_attn": (_int, [_p, _i64, _int, _int, _int, _int, _f, _p, _p, _int, _i64, _i64,
@@ -164,6 +165,15 @@ def topk_blocks(scores, n_full, k_blk, blocks_out, counts_out, q_pos=None, strea
     _check("qsa_topk_blocks", load().qsa_topk_blocks(
         _ptr(scores), n_q, ld, _ptr(q_pos), n_full, k_blk, _ptr(blocks_out), _ptr(counts_out),
         _stream(stream)))
+
+
+def expand_block_scores(scores, n_full, cell_scores, stream=None):
+    """qsa_expand_block_scores: cell_scores[i][c] = scores[i][c // 4] for c < 4*n_full."""
+    n_q = scores.shape[0] if scores.dim() > 1 else 1
+    ld_s = _ld(scores) if scores.dim() > 1 else scores.numel()
+    ld_c = _ld(cell_scores) if cell_scores.dim() > 1 else cell_scores.numel()
+    _check("qsa_expand_block_scores", load().qsa_expand_block_scores(
+        _ptr(scores), n_q, ld_s, n_full, _ptr(cell_scores), ld_c, _stream(stream)))
 
 
 def gather_kv(blocks, counts, k_blk, pos_out, n_cells_out, max_cells, n_ctx=-1, q_pos=None,

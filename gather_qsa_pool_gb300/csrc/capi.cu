@@ -174,6 +174,19 @@ qsa_status qsa_topk_blocks(const float *scores, int64_t n_q, int64_t ld_scores,
                                  counts_out, 0, nullptr, nullptr, 0, nullptr, (cudaStream_t)stream));
 }
 
+qsa_status qsa_expand_block_scores(const float *scores, int64_t n_q, int64_t ld_scores,
+                                   int64_t n_full, float *cell_scores, int64_t ld_cells,
+                                   qsa_stream_t stream)
+{
+    if (!scores || !cell_scores) return QSA_ERR_INVALID_ARG;
+    if (n_q < 0 || n_full < 0 || ld_scores < n_full || ld_cells < 4 * n_full)
+        return QSA_ERR_INVALID_ARG;
+    if (!aligned(scores, 4) || !aligned(cell_scores, 4)) return QSA_ERR_INVALID_ARG;
+    if (n_q > 65535) return QSA_ERR_UNSUPPORTED;
+    return from_cuda(launch_expand_scores(scores, n_q, ld_scores, n_full, cell_scores, ld_cells,
+                                          (cudaStream_t)stream));
+}
+
 static qsa_status check_gather(const void *K, const void *V, qsa_dtype dtype, int64_t n_kv,
                                int H_kv, int d_k, int d_v, int64_t ld_k, int64_t ld_v,
                                const int32_t *blocks, const int32_t *counts, int64_t n_q,

@@ -366,6 +366,10 @@ cudaError_t launch_topk_select(const float *scores, int64_t ld_scores, int n_q, 
 size_t topk_select_workspace_bytes(int64_t n_full_cap);
 uint32_t *topk_select_ticket(void *scratch);
 
+// cells[i][c] = scores[i][c / 4] for c < 4 * n_full (the pre-block-domain selection input).
+cudaError_t launch_expand_scores(const float *scores, int64_t n_q, int64_t ld_s, int64_t n_full,
+                                 float *cells, int64_t ld_c, cudaStream_t st);
+
 cudaError_t launch_gather(const void *K, const void *V, qsa_dtype dt, int64_t n_kv, int H_kv,
                           int d_k, int d_v, int64_t ld_k, int64_t ld_v, const int32_t *blocks,
                           const int32_t *counts, int64_t n_q, int64_t k_blk,

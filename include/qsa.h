@@ -157,6 +157,30 @@ qsa_status qsa_topk_blocks(const float *scores, int64_t n_q, int64_t ld_scores,
 int64_t qsa_topk_max_candidates(void);
 
 /*
+ * qsa_expand_block_scores -- the selection input of the pages' earlier path, kept for A/B
+ * measurement: each full block's score copied to its four cells.
+ *
+ * Source: same page, section "block-domain top-k (COMMON-006)" (before it, block scores were
+ * expanded to every cell through a cell -> block map and the top-k ran over cells; that
+ * expansion cost 0.45 / 0.91 ms per layer at 128k / 256k on the pages' GPU).
+ *
+ *   cell_scores[i][c] = scores[i][floor(c / 4)]   for c < 4 * n_full
+ * qsa_topk_blocks over cell_scores with 4 * n_full candidates and k = 4 * k_blk then
+ * selects cells; since a block's four cells tie and ties go to the lower index, whole
+ * blocks are selected, the same ones as the block-domain top-k unless a tie straddles its
+ * boundary.  The decode path does not use this call.
+ *
+ *   scores       [n_q][ld_scores] fp32, ld_scores >= n_full
+ *   cell_scores  [n_q][ld_cells] fp32 output, ld_cells >= 4 * n_full; entries from 4*n_full
+ *                on are not written
+ * Errors: INVALID_ARG for null or misaligned pointers, negative sizes or short strides;
+ * UNSUPPORTED for n_q > 65535.
+ */
+qsa_status qsa_expand_block_scores(const float *scores, int64_t n_q, int64_t ld_scores,
+                                   int64_t n_full, float *cell_scores, int64_t ld_cells,
+                                   qsa_stream_t stream);
+
+/*
  * qsa_gather_kv -- expand selected blocks to KV cells and (optionally) copy the rows.
  *
  * Source: same page, section "selected K/V gather (COMMON-005)" (get_rows of K, V and

@@ -98,6 +98,15 @@ def test_topk_rejects(lib):
     assert lib.qsa_topk_max_candidates() >= 64052  # a 256k-token context fits
 
 
+def test_expand_block_scores_rejects(lib):
+    s = None
+    assert lib.qsa_expand_block_scores(None, 1, 10, 10, FAKE, 40, s) == 1
+    assert lib.qsa_expand_block_scores(FAKE, 1, 9, 10, FAKE, 40, s) == 1    # ld_scores < n_full
+    assert lib.qsa_expand_block_scores(FAKE, 1, 10, 10, FAKE, 39, s) == 1   # ld_cells < 4 n_full
+    assert lib.qsa_expand_block_scores(FAKE, -1, 10, 10, FAKE, 40, s) == 1
+    assert lib.qsa_expand_block_scores(FAKE, 70000, 10, 10, FAKE, 40, s) == 2
+
+
 def test_gather_rejects(lib):
     s = None
     # max_cells < 4*k_blk + 3
