@@ -391,10 +391,12 @@ def run_context(name, args, world, rank, local, want_clocks, pooled="f32", n_q=1
     return res
 
 
-def run_prefill(args, local):
+def run_prefill(args, local, pooled_kind="f32"):
     """The prefill chunk: 1024 queries after 255,181 tokens.  Times (CUDA events, after a
     warm-up) the tensor-core score contraction, the per-query top-k, the cell lists and the
-    gathered attention; returns per-kernel microseconds and the score kernel's TFLOP/s."""
+    gathered attention; returns per-kernel microseconds and the score kernel's TFLOP/s.
+    pooled_kind "bf16": the pooled cache is stored in bf16 and the contraction reads it in
+    place (no conversion pass)."""
     import torch
 
     import gather_qsa_pool_gb300 as qsa
@@ -404,12 +406,14 @@ def run_prefill(args, local):
     dev = torch.device("cuda", local)
     inp = qsa_synth.prefill_inputs_torch(shape, seed=4242, device=dev)
     H, d, n_q, n_rows = shape.H_idx, shape.d_idx, shape.n_q, shape.n_rows
-    pooled = torch.zeros(n_rows, H * d, device=dev)
+    pdt = torch.bfloat16 if pooled_kind == "bf16" else torch.float32
+    pooled = torch.zeros(n_rows, H * d, dtype=pdt, device=dev)
     qsa.pool_update(inp["raw_k"], shape.n_ctx, H, d, inp["norm_w"], shape.eps, shape.rope_base,
                     pooled, 0)
     scores = torch.empty(n_q, n_rows, device=dev)
-    ws = torch.zeros(qsa.index_score_workspace_size(n_q, n_rows, H, d, qsa.QSA_PREC_BF16_TC),
-                     dtype=torch.uint8, device=dev)
+    ws = torch.zeros(qsa.index_score_workspace_size(
+        n_q, n_rows, H, d, qsa.QSA_PREC_BF16_TC,
+        qsa.QSA_BF16 if pooled_kind == "bf16" else qsa.QSA_F32), dtype=torch.uint8, device=dev)
     blocks = torch.empty(n_q, shape.k_blk, dtype=torch.int32, device=dev)
     counts = torch.empty(n_q, dtype=torch.int32, device=dev)
     pos = torch.empty(n_q, shape.max_cells, dtype=torch.int32, device=dev)
@@ -448,8 +452,8 @@ def run_prefill(args, local):
     attn_flops = 2.0 * 2.0 * n_q * shape.H_q * shape.d * float(n_cells.float().mean().item())
     out_d = {
         "workload": (f"prefill chunk: {n_q} queries at positions {shape.depth:,}..{shape.n_ctx - 1:,}, "
-                     f"indexer {H}x{d}, top-k {shape.top_k_tokens}, attention {shape.H_q}/"
-                     f"{shape.H_kv}x{shape.d} bf16"),
+                     f"indexer {H}x{d} ({pooled_kind} pooled cache), top-k {shape.top_k_tokens}, "
+                     f"attention {shape.H_q}/{shape.H_kv}x{shape.d} bf16"),
         "us": {k: round(v, 1) for k, v in res.items()},
         "chunk_us": round(sum(res.values()), 1),
         "score_tc_tflops": flops / (res["score_tc"] * 1e-6) / 1e12,
@@ -768,6 +772,8 @@ def main():
                              n_q=n_q, light=True)
             variants[label] = dict(summarize(rv, world, args.layers, peak),
                                    pooled_cache=pooled, queries_per_step=n_q)
+        if not args.no_prefill:
+            variants["prefill_bf16_pooled"] = run_prefill(args, local, "bf16")
     r = results[args.primary]
     sh = r["shape"]
     value = sweep[args.primary]["steps_per_s"]

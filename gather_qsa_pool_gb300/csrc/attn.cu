@@ -597,10 +597,14 @@ attn_mma_kernel(const float *__restrict__ q, int H_q, int H_kv, float scale_log2
     uint32_t lost_at = 0;  // buffer | parity << 1 of that stage
     // A split's cell range is fixed by max_cells, so the positions of its first two stages
     // are loaded together with the list length; entries past the length are dropped once
-    // it arrives.
-    const int64_t chunk = (max_cells + S - 1) / S;
+    // it arrives.  A range a few cells longer than a stage (2,051 cells over 16 splits:
+    // 129) would cost every split a second stage: then every split but the last takes
+    // whole stages and the last the few cells left.
+    int64_t chunk = (max_cells + S - 1) / S;
+    if (chunk > TC && chunk % TC != 0 && chunk % TC <= 8) chunk -= chunk % TC;
     const int64_t c0 = (int64_t)s_idx * chunk;
-    const int64_t c1max = c0 + chunk < max_cells ? c0 + chunk : max_cells;
+    const int64_t c1max =
+        (s_idx == S - 1 || c0 + chunk >= max_cells) ? max_cells : c0 + chunk;
     int64_t n = n_cells[qi];
     int64_t first_row = -1;  // cell c0 + tid: stage tid / TC, slot tid % TC
     if (c0 + tid < c1max)

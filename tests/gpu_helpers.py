@@ -3,6 +3,9 @@ the acceptance rules the comparisons use."""
 import numpy as np
 import torch
 
+import qsa_synth
+from oracle import oracle
+
 DEV = "cuda"
 
 # Attention output tolerance (max abs error): bf16 K/V with fp32 accumulation, and fp32.
@@ -72,3 +75,56 @@ def check_topk(gpu_blocks: np.ndarray, gpu_count: int, oracle_scores: np.ndarray
     bad = (want != got) & ~band
     assert not bad.any(), f"blocks differ outside the tie band: {np.flatnonzero(bad)[:10]}"
     return int(band.sum())
+
+
+# ------------------------------------------------------------------ bf16 pooled storage
+# The kernel's fp32 pooled value: pooling, an RMS norm over d values, a weight and a
+# rotation, each a few roundings of 2^-24; 2^-17 of the pair's magnitude bounds them.
+BF16_FLIP_REL = 2.0 ** -17
+
+
+def pooled_f64(inp, shape, n_ctx, rows):
+    """The oracle's exact (fp64, unrounded) pooled rows."""
+    H, d = shape.H_idx, shape.d_idx
+    return np.stack([oracle.pool_row_f64(inp["raw_k"], n_ctx, H, d, inp["norm_w"], shape.eps,
+                                         shape.rope_base, b) for b in rows])
+
+
+def bf16_delta(z, d):
+    """Per element: the bound on the kernel's fp32 error, BF16_FLIP_REL of the magnitude of
+    the rotation pair (dims i and i + d/2 of a head) the element belongs to."""
+    zz = z.reshape(z.shape[0], -1, 2, d // 2)
+    pair = np.hypot(zz[:, :, 0, :], zz[:, :, 1, :])
+    return BF16_FLIP_REL * np.concatenate([pair, pair], axis=-1).reshape(z.shape)
+
+
+def _bf16_mag(bits):
+    return qsa_synth.bf16_bits_to_f32((bits & 0x7FFF).astype(np.uint16)).astype(np.float64)
+
+
+def check_bf16_rows(got_bits, want_bits, z, d):
+    """Each stored bf16 value must be the rounding of some value within delta of the exact
+    one: |z| inside the value's rounding interval widened by delta (the sign may differ
+    only within delta of zero).  Returns how many values differ from the oracle's."""
+    delta = bf16_delta(z, d)
+    mag = got_bits & 0x7FFF
+    g = _bf16_mag(got_bits)
+    lo = np.where(mag > 0, 0.5 * (_bf16_mag(np.maximum(mag, 1) - 1) + g), 0.0)
+    hi = 0.5 * (g + _bf16_mag(mag + 1))
+    a = np.abs(z)
+    sign_ok = ((got_bits >> 15) == (z < 0)) | (mag == 0)
+    ok = np.where(sign_ok, (a >= lo - delta) & (a <= hi + delta), g + a <= delta)
+    assert ok.all(), f"{int((~ok).sum())} stored values are not a rounding of the exact value"
+    return int((got_bits != want_bits).sum())
+
+
+def flip_band(q, z, d, scale):
+    """Per row: how far the kernel's stored values can move a score from the oracle's (both
+    roundings of values within delta of the exact one): one bf16 step plus 2 delta at an
+    element whose exact value is within delta of a rounding midpoint or of zero."""
+    delta = bf16_delta(z, d)
+    a = np.abs(z)
+    ulp = np.exp2(np.floor(np.log2(np.where(a > 0, a, 1.0))) - 7)
+    mid = (np.floor(a / ulp) + 0.5) * ulp
+    risky = (np.abs(a - mid) <= delta) | (a <= 2 * delta)
+    return scale * ((risky * (ulp + 2 * delta)) @ np.abs(q.astype(np.float64)).reshape(-1))

@@ -11,7 +11,8 @@ import torch
 import gather_qsa_pool_gb300 as qsa
 import qsa_synth
 from oracle import oracle
-from gpu_helpers import (ATOL_ATTN_BF16, check_topk, score_tolerance, to_dev, to_host)
+from gpu_helpers import (ATOL_ATTN_BF16, check_bf16_rows, check_topk, flip_band, pooled_f64,
+                         score_tolerance, to_dev, to_host)
 
 pytestmark = pytest.mark.gpu
 
@@ -21,6 +22,56 @@ def _layer(shape, steps):
                            H_q=shape.H_q, H_kv=shape.H_kv, d=shape.d,
                            top_k_tokens=shape.top_k_tokens, eps=shape.eps,
                            rope_base=shape.rope_base)
+
+
+def test_decode_61789_tokens_three_queries_bf16_pooled_full_oracle():
+    """A step carrying three query tokens (a token and two drafts) over a bf16 pooled cache
+    at 61,789 tokens, in the benchmark's launch configuration, against the oracle's
+    multi-query step: every stored pooled value (bf16 rule), every score of every query, each
+    query's selection (band widened by possible bf16 roundings), cell list and output."""
+    shape = qsa_synth.CONFIGS["decode_64k"]
+    n_q = 3
+    inp = qsa_synth.decode_inputs(shape, seed=62, extra_tokens=n_q, n_steps=n_q)
+    H, d = shape.H_idx, shape.d_idx
+    raw, w, K, V = (to_dev(inp["raw_k"]), to_dev(inp["norm_w"]), to_dev(inp["K"]),
+                    to_dev(inp["V"]))
+    lay = qsa.DecodeLayer(cap_tokens=shape.n_ctx + n_q, H_idx=H, d_idx=d, H_q=shape.H_q,
+                          H_kv=shape.H_kv, d=shape.d, top_k_tokens=shape.top_k_tokens,
+                          eps=shape.eps, rope_base=shape.rope_base,
+                          pooled_dtype=torch.bfloat16, max_queries=n_q)
+    n0 = shape.n_ctx
+    lay.rebuild(raw, w, n0)
+    o_pooled = np.zeros((lay.cap_rows, H * d), np.uint16)
+    oracle.pool_rows(inp["raw_k"], n0, H, d, inp["norm_w"], shape.eps, shape.rope_base, 0,
+                     (n0 + 3) // 4, o_pooled)
+    n_ctx = n0 + n_q
+    out = to_host(lay.step(raw, w, K, V, n_ctx, to_dev(inp["q_idx"]), to_dev(inp["q"])))
+    res, o_scores = oracle.decode_step_multi(
+        inp["raw_k"], n_ctx, H, d, inp["norm_w"], shape.eps, shape.rope_base, o_pooled,
+        n0 // 4, inp["q_idx"], shape.top_k_tokens, inp["q"], inp["K"], inp["V"], shape.H_q,
+        shape.H_kv, shape.d)
+    n_rows = (n_ctx + 3) // 4
+    z = pooled_f64(inp, shape, n_ctx, range(n_rows))
+    flips = check_bf16_rows(to_host(lay.pooled)[:n_rows], o_pooled[:n_rows], z, d)
+    assert flips <= 1e-3 * n_rows * H * d
+    g_scores = to_host(lay.scores_of(n_q, n_ctx))
+    scale = 1.0 / math.sqrt(d)
+    g_pooled_vals = qsa_synth.bf16_bits_to_f32(to_host(lay.pooled)[:n_rows])
+    blocks, counts = to_host(lay.blocks), to_host(lay.counts)
+    pos, n_cells = to_host(lay.pos), to_host(lay.n_cells)
+    for i in range(n_q):
+        # the GPU's scores of its own cache: the fp32 summation rule
+        ref = g_pooled_vals.astype(np.float64) @ inp["q_idx"][i].astype(np.float64) * scale
+        tol = score_tolerance(inp["q_idx"][i], g_pooled_vals, n_rows, scale)
+        assert np.all(np.abs(g_scores[i] - ref) <= tol)
+        p = n_ctx - n_q + i
+        n_i = min(n_ctx // 4, (p + 1) // 4)
+        check_topk(blocks[i], int(counts[i]), o_scores[i], n_i, shape.k_blk,
+                   band_abs=flip_band(inp["q_idx"][i], z[:n_i], d, scale))
+        o_blocks, o_cells, o_out, _ = res[i]
+        if np.array_equal(blocks[i, :counts[i]], o_blocks):
+            np.testing.assert_array_equal(pos[i, :n_cells[i]], o_cells)
+            np.testing.assert_allclose(out[i], o_out, rtol=0, atol=ATOL_ATTN_BF16)
 
 
 def test_decode_61789_tokens_full_oracle():

@@ -19,65 +19,14 @@ import torch
 import gather_qsa_pool_gb300 as qsa
 import qsa_synth
 from oracle import oracle
-from gpu_helpers import (ATOL_ATTN_BF16, ATOL_ATTN_F32, check_topk, score_tolerance, to_dev,
-                         to_host)
+from gpu_helpers import (ATOL_ATTN_BF16, ATOL_ATTN_F32, check_bf16_rows, check_topk, flip_band,
+                         pooled_f64, score_tolerance, to_dev, to_host)
 
 pytestmark = pytest.mark.gpu
 
 TINY = qsa_synth.CONFIGS["tiny_f32_decode"]
 SMALL = qsa_synth.shrink(qsa_synth.CONFIGS["decode_64k"], name="small_bf16", n_ctx=9_003,
                          top_k_tokens=512)
-# The kernel's fp32 pooled value: pooling, an RMS norm over d values, a weight and a
-# rotation, each a few roundings of 2^-24; 2^-17 of the pair's magnitude bounds them.
-BF16_FLIP_REL = 2.0 ** -17
-
-
-def _z64(inp, shape, n_ctx, rows):
-    H, d = shape.H_idx, shape.d_idx
-    return np.stack([oracle.pool_row_f64(inp["raw_k"], n_ctx, H, d, inp["norm_w"], shape.eps,
-                                         shape.rope_base, b) for b in rows])
-
-
-def _delta(z, d):
-    """Per element: the bound on the kernel's fp32 error, BF16_FLIP_REL of the magnitude of
-    the rotation pair (dims i and i + d/2 of a head) the element belongs to."""
-    zz = z.reshape(z.shape[0], -1, 2, d // 2)
-    pair = np.hypot(zz[:, :, 0, :], zz[:, :, 1, :])
-    return BF16_FLIP_REL * np.concatenate([pair, pair], axis=-1).reshape(z.shape)
-
-
-def _bf16_mag(bits):
-    return qsa_synth.bf16_bits_to_f32((bits & 0x7FFF).astype(np.uint16)).astype(np.float64)
-
-
-def _check_bf16_rows(got_bits, want_bits, z, d):
-    """Each stored bf16 value must be the rounding of some value within delta of the exact
-    one: |z| inside the value's rounding interval widened by delta (the sign may differ
-    only within delta of zero).  Returns how many values differ from the oracle's."""
-    delta = _delta(z, d)
-    mag = got_bits & 0x7FFF
-    g = _bf16_mag(got_bits)
-    lo = np.where(mag > 0, 0.5 * (_bf16_mag(np.maximum(mag, 1) - 1) + g), 0.0)
-    hi = 0.5 * (g + _bf16_mag(mag + 1))
-    a = np.abs(z)
-    sign_ok = ((got_bits >> 15) == (z < 0)) | (mag == 0)
-    ok = np.where(sign_ok, (a >= lo - delta) & (a <= hi + delta), g + a <= delta)
-    assert ok.all(), f"{int((~ok).sum())} stored values are not a rounding of the exact value"
-    return int((got_bits != want_bits).sum())
-
-
-def _flip_band(q, z, d, scale):
-    """Per row: how far the kernel's stored values can move a score from the oracle's (both
-    roundings of values within delta of the exact one): one bf16 step plus 2 delta at an
-    element whose exact value is within delta of a rounding midpoint or of zero."""
-    delta = _delta(z, d)
-    a = np.abs(z)
-    ulp = np.exp2(np.floor(np.log2(np.where(a > 0, a, 1.0))) - 7)
-    mid = (np.floor(a / ulp) + 0.5) * ulp
-    risky = (np.abs(a - mid) <= delta) | (a <= 2 * delta)
-    return scale * ((risky * (ulp + 2 * delta)) @ np.abs(q.astype(np.float64)).reshape(-1))
-
-
 # ------------------------------------------------------------------ bf16 pooled storage
 
 @pytest.mark.parametrize("shape", [TINY, SMALL], ids=lambda s: s.name)
@@ -91,8 +40,8 @@ def test_pool_update_bf16_storage(shape):
     qsa.pool_update(to_dev(inp["raw_k"]), n_ctx, H, d, to_dev(inp["norm_w"]), shape.eps,
                     shape.rope_base, pooled, 0)
     got = to_host(pooled)
-    z = _z64(inp, shape, n_ctx, range(shape.n_rows))
-    flips = _check_bf16_rows(got[:shape.n_rows], want, z, d)
+    z = pooled_f64(inp, shape, n_ctx, range(shape.n_rows))
+    flips = check_bf16_rows(got[:shape.n_rows], want, z, d)
     assert flips <= 1e-3 * want.size  # rounding disagreements are rare
     assert np.all(got[shape.n_rows:] == 0x40A0)  # rows past the cache end untouched
 
@@ -200,8 +149,8 @@ def test_multi_query_decode_steps_match_oracle(shape, store):
         o_valid = n_ctx // 4
         n_rows = (n_ctx + 3) // 4
         if store == "bf16":
-            z = _z64(inp, shape, n_ctx, range(n_rows))
-            _check_bf16_rows(to_host(lay.pooled)[:n_rows], o_pooled[:n_rows], z, d)
+            z = pooled_f64(inp, shape, n_ctx, range(n_rows))
+            check_bf16_rows(to_host(lay.pooled)[:n_rows], o_pooled[:n_rows], z, d)
         blocks = to_host(lay.blocks)
         counts = to_host(lay.counts)
         n_cells = to_host(lay.n_cells)
@@ -209,7 +158,7 @@ def test_multi_query_decode_steps_match_oracle(shape, store):
         for i in range(n_q):
             p = n_ctx - n_q + i
             n_i = min(n_ctx // 4, (p + 1) // 4)
-            band_abs = _flip_band(qi[i], z[:n_i], d, scale) if store == "bf16" else None
+            band_abs = flip_band(qi[i], z[:n_i], d, scale) if store == "bf16" else None
             n_band += check_topk(blocks[i], int(counts[i]), o_scores[i], n_i, shape.k_blk,
                                  band_abs=band_abs)
             o_blocks, o_cells, o_out, _ = res[i]
