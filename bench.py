@@ -226,6 +226,8 @@ def run_context(name, args, world, rank, local, want_clocks, pooled="f32", n_q=1
                               rope_base=shape.rope_base, pooled_dtype=pdt, max_queries=n_q,
                               device=dev)
         lay.rebuild(inp["raw_k"], inp["norm_w"], shape.n_ctx - 1)
+        if not light:
+            lay.enable_host_feed(inp["raw_k"].dtype, inp["K"].dtype)
         lay.bind(inp["raw_k"], inp["norm_w"], inp["K"], inp["V"])
         layers.append(lay)
         caches.append(inp)
@@ -344,37 +346,27 @@ def run_context(name, args, world, rank, local, want_clocks, pooled="f32", n_q=1
     score_us = ev2.elapsed_time(ev3) * 1e3 / k_kernel
     score_rows = sum(n_rows[i % L] for i in range(k_kernel)) / k_kernel
 
-    # end to end: per step, copy the new token's rows and the queries from pinned host
-    # memory into the caches, run the step, read the output back
-    hd = shape.H_idx * shape.d_idx
-    kvd = shape.H_kv * shape.d
-    h_raw = torch.randn(hd).to(caches[0]["raw_k"].dtype).pin_memory()
-    h_k = torch.randn(kvd).to(caches[0]["K"].dtype).pin_memory()
-    h_v = torch.randn(kvd).to(caches[0]["V"].dtype).pin_memory()
-    h_qidx = torch.randn(hd).pin_memory()
-    h_q = torch.randn(shape.H_q * shape.d).pin_memory()
-    h_out = torch.empty(shape.H_q * shape.d).pin_memory()
-    d_qidx = torch.empty(hd, device=dev)
-    d_q = torch.empty(shape.H_q * shape.d, device=dev)
-    h2d = (h_raw.numel() * h_raw.element_size() + h_k.numel() * h_k.element_size()
-           + h_v.numel() * h_v.element_size() + h_qidx.numel() * 4 + h_q.numel() * 4)
-    d2h = h_out.numel() * 4
+    # end to end through the C call with host buffers (qsa_decode_step_host): per step one
+    # copy of the new token's raw-key, K and V rows and both queries from pinned host memory,
+    # the step, one copy of the output back, and a wait for it
+    h2d = d2h = 0
+    if not light:
+        g = torch.Generator()
+        g.manual_seed(99)
+        for lay in layers:
+            hin = lay.host_inputs(1)
+            for key in ("raw", "k", "v", "q_idx", "q"):
+                hin[key].copy_(torch.randn(hin[key].shape, generator=g).to(hin[key].dtype))
+        h2d = layers[0].host_inputs(1)["bytes"]
+        d2h = shape.H_q * shape.d * 4
     torch.cuda.synchronize()
     barrier(world)
     t0 = time.perf_counter()
     for _ in range(k_e2e):
         li = s % L
-        c = caches[li]
-        p = n_ctx[li] - 1
-        c["raw_k"][p].view(-1).copy_(h_raw, non_blocking=True)
-        c["K"][p].view(-1).copy_(h_k, non_blocking=True)
-        c["V"][p].view(-1).copy_(h_v, non_blocking=True)
-        d_qidx.copy_(h_qidx, non_blocking=True)
-        d_q.copy_(h_q, non_blocking=True)
-        layers[li].step_ptr(n_ctx[li], d_qidx.data_ptr(), d_q.data_ptr(), sp)
+        layers[li].step_host(n_ctx[li], sp, 1)
         n_ctx[li] += 1
         s += 1
-        h_out.copy_(layers[li].out.view(-1), non_blocking=True)
         stream.synchronize()
     t_e2e = time.perf_counter() - t0
     t_e2e = max_over_ranks(t_e2e, world)

@@ -11,6 +11,8 @@ from ._binding import (  # noqa: F401
     QSA_PREC_F32,
     QSAError,
     decode_step,
+    decode_step_host_layout,
+    decode_step_host_workspace_size,
     decode_step_workspace_size,
     expand_block_scores,
     gather_kv,

@@ -47,6 +47,13 @@ _SIGNATURES = {
                                _i64, _p, _f, _p, _i64, _p, _p, _p, _p, _int, _i64, _int, _int,
                                _i64, _p, _p, _i64, _p, _int, _f, _p, _p, _p, _sz, _p]),
     "qsa_decode_step_workspace_size": (_sz, [_i64, _int, _int, _int, _i64, _i64]),
+    "qsa_decode_step_host": (_int, [_p, _p, _p, _p, _int, _i64, _int, _int, _p, _f, _d, _p, _int,
+                                    _i64, _i64, _i64, _f, _p, _i64, _p, _p, _p, _p, _int, _i64,
+                                    _int, _int, _i64, _p, _p, _i64, _int, _f, _p, _p, _p, _sz,
+                                    _p]),
+    "qsa_decode_step_host_layout": (_sz, [_i64, _int, _int, _int, _int, _int, _int, _int, _p]),
+    "qsa_decode_step_host_workspace_size": (_sz, [_i64, _int, _int, _int, _i64, _i64, _int, _int,
+                                                  _int, _int]),
     "qsa_mask_to_list": (_int, [_p, _i64, _i64, _i64, _i64, _p, _p, _p, _p]),
     "qsa_mask_sparse_eligible": (_int, [_int, _f, _f, _i64, _i64]),
 }
@@ -226,6 +233,20 @@ def decode_step(raw_k, n_ctx, H_idx, d_idx, norm_w, eps, rope_base, pooled, n_va
 
 def decode_step_workspace_size(H_q, H_kv, d, max_cells, cap_rows, n_q=1) -> int:
     return int(load().qsa_decode_step_workspace_size(n_q, H_q, H_kv, d, max_cells, cap_rows))
+
+
+def decode_step_host_layout(n_q, raw_dtype, H_idx, d_idx, kv_dtype, H_kv, d, H_q):
+    """(total bytes, [5] section offsets) of qsa_decode_step_host's packed input."""
+    off = (ctypes.c_int64 * 5)()
+    total = int(load().qsa_decode_step_host_layout(n_q, raw_dtype, H_idx, d_idx, kv_dtype, H_kv,
+                                                   d, H_q, off))
+    return total, list(off)
+
+
+def decode_step_host_workspace_size(n_q, H_q, H_kv, d, max_cells, cap_rows, raw_dtype, H_idx,
+                                    d_idx, kv_dtype) -> int:
+    return int(load().qsa_decode_step_host_workspace_size(n_q, H_q, H_kv, d, max_cells, cap_rows,
+                                                          raw_dtype, H_idx, d_idx, kv_dtype))
 
 
 def mask_to_list(mask, max_list, pos_out, counts_out, bits_out=None, n_kv=None, stream=None):

@@ -279,16 +279,28 @@ size_t qsa_decode_step_workspace_size(int64_t n_q, int H_q, int H_kv, int d, int
            (size_t)n_q * (kTopkHistBytes + topk_select_workspace_bytes(cap_rows));
 }
 
-qsa_status qsa_decode_step(const void *raw_k, qsa_dtype raw_dtype, int64_t n_ctx, int H_idx,
-                           int d_idx, const float *norm_w, float eps, double rope_base,
-                           void *pooled, qsa_dtype pooled_dtype, int64_t cap_rows,
-                           int64_t n_valid_full, int64_t n_q, const float *q_idx, float scale_idx,
-                           float *scores, int64_t k_blk, int32_t *blocks, int32_t *counts,
-                           const void *K, const void *V, qsa_dtype kv_dtype, int64_t n_kv,
-                           int H_kv, int d, int64_t ld_kv, int32_t *pos, int32_t *n_cells,
-                           int64_t max_cells, const float *q, int H_q, float scale, float *out,
-                           float *lse_out, void *workspace, size_t workspace_bytes,
-                           qsa_stream_t stream)
+// A decode step fed from host memory: the packed inputs go to `staging` in one copy, the new
+// tokens' rows are scattered into the caches, and the outputs come back to h_out / h_lse.
+struct HostFeed {
+    const void *h_in;
+    size_t in_bytes;
+    char *staging;
+    int64_t off[5];  // new raw rows, new K rows, new V rows, q_idx, q
+    float *h_out;
+    float *h_lse;
+};
+
+static qsa_status decode_step_impl(const void *raw_k, qsa_dtype raw_dtype, int64_t n_ctx, int H_idx,
+                                   int d_idx, const float *norm_w, float eps, double rope_base,
+                                   void *pooled, qsa_dtype pooled_dtype, int64_t cap_rows,
+                                   int64_t n_valid_full, int64_t n_q, const float *q_idx,
+                                   float scale_idx, float *scores, int64_t k_blk, int32_t *blocks,
+                                   int32_t *counts, const void *K, const void *V,
+                                   qsa_dtype kv_dtype, int64_t n_kv, int H_kv, int d, int64_t ld_kv,
+                                   int32_t *pos, int32_t *n_cells, int64_t max_cells,
+                                   const float *q, int H_q, float scale, float *out, float *lse_out,
+                                   void *workspace, size_t workspace_bytes, qsa_stream_t stream,
+                                   const HostFeed *feed)
 {
     if (n_q < 1 || n_q > kMaxStreamQueries || n_q > n_ctx) return QSA_ERR_INVALID_ARG;
     const int64_t n_rows = (n_ctx + 3) / 4;
@@ -317,6 +329,24 @@ qsa_status qsa_decode_step(const void *raw_k, qsa_dtype raw_dtype, int64_t n_ctx
                        max_cells, out, workspace, attn_bytes);
     if (v != QSA_OK) return v;
     const cudaStream_t st = (cudaStream_t)stream;
+    cudaError_t e = cudaSuccess;
+    if (feed) {
+        // 0. this step's inputs from host memory (one copy), the new rows into the caches
+        e = cudaMemcpyAsync(feed->staging, feed->h_in, feed->in_bytes, cudaMemcpyHostToDevice, st);
+        if (e == cudaSuccess) {
+            const int64_t re = raw_dtype == QSA_BF16 ? 2 : 4, ke = kv_dtype == QSA_BF16 ? 2 : 4;
+            const int64_t hd = (int64_t)H_idx * d_idx, p0 = n_ctx - n_q;
+            const void *src[3] = {feed->staging + feed->off[0], feed->staging + feed->off[1],
+                                  feed->staging + feed->off[2]};
+            void *dst[3] = {(char *)raw_k + p0 * hd * re, (char *)K + p0 * ld_kv * ke,
+                            (char *)V + p0 * ld_kv * ke};
+            const int64_t rb[3] = {hd * re, (int64_t)H_kv * d * ke, (int64_t)H_kv * d * ke};
+            const int64_t ld[3] = {hd * re, ld_kv * ke, ld_kv * ke};
+            const int rows[3] = {(int)n_q, (int)n_q, (int)n_q};
+            e = launch_scatter_rows(src, dst, rb, ld, rows, st);
+        }
+        if (e != cudaSuccess) return QSA_ERR_CUDA;
+    }
     // Query i sits at position p_i = n_ctx - n_q + i; its candidates are the blocks complete
     // there.  The score kernel counts each query's candidates into its histogram and resets
     // each query's arrival ticket.
@@ -340,9 +370,8 @@ qsa_status qsa_decode_step(const void *raw_k, qsa_dtype raw_dtype, int64_t n_ctx
     pf.eps = eps;
     pf.row0 = row0;
     pf.row1 = n_rows;
-    cudaError_t e = launch_score_pool_fused(q_idx, (int)n_q, pooled, pooled_dtype, n_rows, H_idx,
-                                            d_idx, scale_idx, scores, n_rows, side, pf, rope_base,
-                                            st);
+    e = launch_score_pool_fused(q_idx, (int)n_q, pooled, pooled_dtype, n_rows, H_idx, d_idx,
+                                scale_idx, scores, n_rows, side, pf, rope_base, st);
     if (e == cudaErrorNotSupported) {
         e = run_pool_update(raw_k, raw_dtype, n_ctx, H_idx, d_idx, norm_w, eps, rope_base, pooled,
                             pooled_dtype, n_valid_full, nullptr, st);
@@ -369,7 +398,105 @@ qsa_status qsa_decode_step(const void *raw_k, qsa_dtype raw_dtype, int64_t n_ctx
         e = launch_sparse_attn(q, n_q, H_q, H_kv, d, d, scale, K, V, kv_dtype, n_kv, ld_kv, ld_kv,
                                pos, n_cells, max_cells, out, lse_out, (float *)workspace, st,
                                true);
+    // 5. the outputs back to host memory
+    if (feed && e == cudaSuccess) {
+        e = cudaMemcpyAsync(feed->h_out, out, sizeof(float) * (size_t)n_q * H_q * d,
+                            cudaMemcpyDeviceToHost, st);
+        if (e == cudaSuccess && feed->h_lse)
+            e = cudaMemcpyAsync(feed->h_lse, lse_out, sizeof(float) * (size_t)n_q * H_q,
+                                cudaMemcpyDeviceToHost, st);
+    }
     return from_cuda(e);
+}
+
+qsa_status qsa_decode_step(const void *raw_k, qsa_dtype raw_dtype, int64_t n_ctx, int H_idx,
+                           int d_idx, const float *norm_w, float eps, double rope_base,
+                           void *pooled, qsa_dtype pooled_dtype, int64_t cap_rows,
+                           int64_t n_valid_full, int64_t n_q, const float *q_idx, float scale_idx,
+                           float *scores, int64_t k_blk, int32_t *blocks, int32_t *counts,
+                           const void *K, const void *V, qsa_dtype kv_dtype, int64_t n_kv,
+                           int H_kv, int d, int64_t ld_kv, int32_t *pos, int32_t *n_cells,
+                           int64_t max_cells, const float *q, int H_q, float scale, float *out,
+                           float *lse_out, void *workspace, size_t workspace_bytes,
+                           qsa_stream_t stream)
+{
+    return decode_step_impl(raw_k, raw_dtype, n_ctx, H_idx, d_idx, norm_w, eps, rope_base, pooled,
+                            pooled_dtype, cap_rows, n_valid_full, n_q, q_idx, scale_idx, scores,
+                            k_blk, blocks, counts, K, V, kv_dtype, n_kv, H_kv, d, ld_kv, pos,
+                            n_cells, max_cells, q, H_q, scale, out, lse_out, workspace,
+                            workspace_bytes, stream, nullptr);
+}
+
+static int64_t a16(int64_t b) { return (b + 15) & ~(int64_t)15; }
+
+size_t qsa_decode_step_host_layout(int64_t n_q, qsa_dtype raw_dtype, int H_idx, int d_idx,
+                                   qsa_dtype kv_dtype, int H_kv, int d, int H_q, int64_t *offsets)
+{
+    if (n_q < 1 || n_q > kMaxStreamQueries || !valid_dtype(raw_dtype) || !valid_dtype(kv_dtype) ||
+        H_idx < 1 || d_idx < 1 || H_kv < 1 || d < 1 || H_q < 1)
+        return 0;
+    const int64_t re = esize_of(raw_dtype), ke = esize_of(kv_dtype);
+    int64_t off[5];
+    off[0] = 0;
+    off[1] = a16(off[0] + n_q * H_idx * d_idx * re);
+    off[2] = a16(off[1] + n_q * H_kv * d * ke);
+    off[3] = a16(off[2] + n_q * H_kv * d * ke);
+    off[4] = a16(off[3] + n_q * H_idx * d_idx * 4);
+    const int64_t total = a16(off[4] + n_q * H_q * d * 4);
+    if (offsets)
+        for (int i = 0; i < 5; ++i) offsets[i] = off[i];
+    return (size_t)total;
+}
+
+size_t qsa_decode_step_host_workspace_size(int64_t n_q, int H_q, int H_kv, int d,
+                                           int64_t max_cells, int64_t cap_rows,
+                                           qsa_dtype raw_dtype, int H_idx, int d_idx,
+                                           qsa_dtype kv_dtype)
+{
+    const size_t ws = qsa_decode_step_workspace_size(n_q, H_q, H_kv, d, max_cells, cap_rows);
+    const size_t in = qsa_decode_step_host_layout(n_q, raw_dtype, H_idx, d_idx, kv_dtype, H_kv, d,
+                                                  H_q, nullptr);
+    if (ws == 0 || in == 0) return 0;
+    return align256(ws) + align256(in);
+}
+
+qsa_status qsa_decode_step_host(const void *h_in, float *h_out, float *h_lse, void *raw_k,
+                                qsa_dtype raw_dtype, int64_t n_ctx, int H_idx, int d_idx,
+                                const float *norm_w, float eps, double rope_base, void *pooled,
+                                qsa_dtype pooled_dtype, int64_t cap_rows, int64_t n_valid_full,
+                                int64_t n_q, float scale_idx, float *scores, int64_t k_blk,
+                                int32_t *blocks, int32_t *counts, void *K, void *V,
+                                qsa_dtype kv_dtype, int64_t n_kv, int H_kv, int d, int64_t ld_kv,
+                                int32_t *pos, int32_t *n_cells, int64_t max_cells, int H_q,
+                                float scale, float *out, float *lse_out, void *workspace,
+                                size_t workspace_bytes, qsa_stream_t stream)
+{
+    if (!h_in || !h_out || (h_lse && !lse_out) || !raw_k || !K || !V || !workspace)
+        return QSA_ERR_INVALID_ARG;
+    HostFeed feed;
+    feed.in_bytes = qsa_decode_step_host_layout(n_q, raw_dtype, H_idx, d_idx, kv_dtype, H_kv, d,
+                                                H_q, feed.off);
+    const size_t ws = qsa_decode_step_workspace_size(n_q, H_q, H_kv, d, max_cells, cap_rows);
+    if (feed.in_bytes == 0 || ws == 0) return QSA_ERR_INVALID_ARG;
+    if (workspace_bytes < align256(ws) + align256(feed.in_bytes) || !aligned(workspace, 256))
+        return QSA_ERR_INVALID_ARG;
+    // the new rows land inside the caches (rows n_ctx - n_q .. n_ctx - 1), 4-byte units
+    if (n_ctx > n_kv || n_q > n_ctx || ld_kv < (int64_t)H_kv * d) return QSA_ERR_INVALID_ARG;
+    const int64_t re = esize_of(raw_dtype), ke = esize_of(kv_dtype);
+    if ((H_idx * (int64_t)d_idx * re) % 4 || (H_kv * (int64_t)d * ke) % 4 || (ld_kv * ke) % 4 ||
+        !aligned(raw_k, 4) || !aligned(K, 4) || !aligned(V, 4))
+        return QSA_ERR_INVALID_ARG;
+    feed.h_in = h_in;
+    feed.staging = static_cast<char *>(workspace) + align256(ws);
+    feed.h_out = h_out;
+    feed.h_lse = h_lse;
+    const float *q_idx = reinterpret_cast<const float *>(feed.staging + feed.off[3]);
+    const float *q = reinterpret_cast<const float *>(feed.staging + feed.off[4]);
+    return decode_step_impl(raw_k, raw_dtype, n_ctx, H_idx, d_idx, norm_w, eps, rope_base, pooled,
+                            pooled_dtype, cap_rows, n_valid_full, n_q, q_idx, scale_idx, scores,
+                            k_blk, blocks, counts, K, V, kv_dtype, n_kv, H_kv, d, ld_kv, pos,
+                            n_cells, max_cells, q, H_q, scale, out, lse_out, workspace, ws, stream,
+                            &feed);
 }
 
 qsa_status qsa_mask_to_list(const uint8_t *mask, int64_t n_rows, int64_t n_kv, int64_t ld_mask,

@@ -366,6 +366,13 @@ cudaError_t launch_topk_select(const float *scores, int64_t ld_scores, int n_q, 
 size_t topk_select_workspace_bytes(int64_t n_full_cap);
 uint32_t *topk_select_ticket(void *scratch);
 
+// Three row blocks copied from contiguous sources to strided destinations (the new tokens'
+// raw indexer-key, K and V rows of a host-fed decode step).  Every address, row size and
+// stride must be a multiple of 4 bytes.
+cudaError_t launch_scatter_rows(const void *const src[3], void *const dst[3],
+                                const int64_t row_bytes[3], const int64_t dst_ld[3],
+                                const int rows[3], cudaStream_t st);
+
 // cells[i][c] = scores[i][c / 4] for c < 4 * n_full (the pre-block-domain selection input).
 cudaError_t launch_expand_scores(const float *scores, int64_t n_q, int64_t ld_s, int64_t n_full,
                                  float *cells, int64_t ld_c, cudaStream_t st);

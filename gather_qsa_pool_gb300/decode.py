@@ -94,13 +94,13 @@ class DecodeLayer:
                        self.scores.data_ptr(), self.blocks.data_ptr(), self.counts.data_ptr(),
                        K.data_ptr(), V.data_ptr(), qb._dtype(K), K.shape[0], qb._ld(K),
                        self.pos.data_ptr(), self.n_cells.data_ptr(), self.out.data_ptr(),
-                       self.lse.data_ptr(), self.workspace.data_ptr(),
-                       self.workspace.numel() * 4)
+                       self.lse.data_ptr(), None, None)
 
     def step_ptr(self, n_ctx, q_idx_ptr, q_ptr, stream_ptr, n_q=1):
         """Decode step on caches fixed by ``bind``; q_idx / q given as device pointers."""
         (raw, raw_dt, w, pooled, pdt, cap, scores, blocks, counts, K, V, kv_dt, n_kv, ld, pos,
-         n_cells, out, lse, ws, ws_bytes) = self._fixed
+         n_cells, out, lse, _, _) = self._fixed
+        ws, ws_bytes = self.workspace.data_ptr(), self.workspace.numel() * 4
         st = self._lib.qsa_decode_step(
             raw, raw_dt, n_ctx, self.H_idx, self.d_idx, w, self.eps, self.rope_base, pooled, pdt,
             cap, self.n_valid_full, n_q, q_idx_ptr, 1.0 / math.sqrt(self.d_idx), scores,
@@ -109,6 +109,68 @@ class DecodeLayer:
             stream_ptr)
         if st != 0:
             raise qb.QSAError("qsa_decode_step", st)
+        self.n_valid_full = n_ctx // 4
+
+    # ------------------------------------------------------------------ host-fed steps
+
+    def enable_host_feed(self, raw_dtype, kv_dtype):
+        """Prepare steps fed from host memory (qsa_decode_step_host): a workspace with room
+        for the staging area and page-locked input / output buffers.  raw_dtype, kv_dtype:
+        torch dtypes of the raw indexer-key and K/V caches."""
+        import torch
+
+        rd = qb.QSA_BF16 if raw_dtype == torch.bfloat16 else qb.QSA_F32
+        kd = qb.QSA_BF16 if kv_dtype == torch.bfloat16 else qb.QSA_F32
+        self._host_dtypes = (rd, kd, raw_dtype, kv_dtype)
+        nq = self.max_queries
+        ws = qb.decode_step_host_workspace_size(nq, self.H_q, self.H_kv, self.d, self.max_cells,
+                                                self.cap_rows, rd, self.H_idx, self.d_idx, kd)
+        dev = self.workspace.device
+        self.workspace = torch.zeros(max(ws // 4, 1), dtype=torch.float32, device=dev)
+        total, _ = qb.decode_step_host_layout(nq, rd, self.H_idx, self.d_idx, kd, self.H_kv,
+                                              self.d, self.H_q)
+        self.h_in = torch.zeros(total, dtype=torch.uint8).pin_memory()
+        self.h_out = torch.zeros(nq, self.H_q, self.d, dtype=torch.float32).pin_memory()
+        self.h_lse = torch.zeros(nq, self.H_q, dtype=torch.float32).pin_memory()
+
+    def host_inputs(self, n_q):
+        """Views of the packed host input for a step of n_q queries: dict with 'raw' [n_q]
+        [H_idx*d_idx], 'k' and 'v' [n_q][H_kv*d], 'q_idx' [n_q][H_idx*d_idx], 'q' [n_q][H_q]
+        [d]; fill them, then call step_host."""
+        import torch
+
+        rd, kd, rdt, kdt = self._host_dtypes
+        total, off = qb.decode_step_host_layout(n_q, rd, self.H_idx, self.d_idx, kd, self.H_kv,
+                                                self.d, self.H_q)
+        hd, kvd = self.H_idx * self.d_idx, self.H_kv * self.d
+
+        def view(o, dtype, shape):
+            n = 1
+            for x in shape:
+                n *= x
+            es = torch.tensor([], dtype=dtype).element_size()
+            return self.h_in[o:o + n * es].view(dtype).view(*shape)
+
+        return {"raw": view(off[0], rdt, (n_q, hd)), "k": view(off[1], kdt, (n_q, kvd)),
+                "v": view(off[2], kdt, (n_q, kvd)), "q_idx": view(off[3], torch.float32, (n_q, hd)),
+                "q": view(off[4], torch.float32, (n_q, self.H_q, self.d)), "bytes": total}
+
+    def step_host(self, n_ctx, stream_ptr, n_q=1, with_lse=False):
+        """Host-fed decode step on caches fixed by ``bind``: the new tokens' rows and the
+        queries come from ``h_in`` (see host_inputs), the output lands in ``h_out`` once the
+        stream has been synchronised."""
+        (raw, raw_dt, w, pooled, pdt, cap, scores, blocks, counts, K, V, kv_dt, n_kv, ld, pos,
+         n_cells, out, lse, _, _) = self._fixed
+        st = self._lib.qsa_decode_step_host(
+            self.h_in.data_ptr(), self.h_out.data_ptr(),
+            self.h_lse.data_ptr() if with_lse else None, raw, raw_dt, n_ctx, self.H_idx,
+            self.d_idx, w, self.eps, self.rope_base, pooled, pdt, cap, self.n_valid_full, n_q,
+            1.0 / math.sqrt(self.d_idx), scores, self.k_blk, blocks, counts, K, V, kv_dt, n_kv,
+            self.H_kv, self.d, ld, pos, n_cells, self.max_cells, self.H_q,
+            1.0 / math.sqrt(self.d), out, lse, self.workspace.data_ptr(),
+            self.workspace.numel() * 4, stream_ptr)
+        if st != 0:
+            raise qb.QSAError("qsa_decode_step_host", st)
         self.n_valid_full = n_ctx // 4
 
     def step_separate_calls(self, raw_k, norm_w, K, V, n_ctx, q_idx, q, stream=None):

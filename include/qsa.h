@@ -308,6 +308,56 @@ size_t qsa_decode_step_workspace_size(int64_t n_q, int H_q, int H_kv, int d, int
                                       int64_t cap_rows);
 
 /*
+ * qsa_decode_step_host -- qsa_decode_step fed from host memory: the step's new cache rows
+ * and queries come from one packed host buffer, and its output goes back to host memory.
+ *
+ * Source: same passages as qsa_decode_step (the decode step appends the new tokens, then
+ * scores, selects and attends); the host transfer is this library's service.
+ *
+ * On `stream`, in order: one host-to-device copy of h_in (qsa_decode_step_host_layout()
+ * bytes) into a staging area at the end of the workspace; a kernel writing the new tokens'
+ * rows into the caches -- raw indexer keys to raw_k rows n_ctx - n_q .. n_ctx - 1 (row
+ * stride H_idx*d_idx), K and V rows to the same rows of K and V (row stride ld_kv); then
+ * exactly qsa_decode_step with q_idx and q read from the staging area; then device-to-host
+ * copies of out (n_q*H_q*d floats) into h_out and, if h_lse is not NULL, of lse_out
+ * (n_q*H_q floats) into h_lse.  The call returns without waiting: synchronise the stream
+ * before reading h_out or reusing h_in.  Host buffers should be page-locked (pinned) for
+ * the copies to be asynchronous.
+ *
+ *   h_in    packed inputs, sections at the byte offsets qsa_decode_step_host_layout()
+ *           reports: [n_q][H_idx*d_idx] raw-key rows (raw_dtype), [n_q][H_kv*d] K rows and
+ *           [n_q][H_kv*d] V rows (kv_dtype), [n_q][H_idx*d_idx] fp32 q_idx, [n_q][H_q][d]
+ *           fp32 q
+ *   raw_k, K, V   the caches, written at the new tokens' rows (n_ctx <= n_kv)
+ *   workspace     qsa_decode_step_host_workspace_size() bytes, 256-byte aligned
+ * Other arguments, results and errors as qsa_decode_step, plus INVALID_ARG for null host
+ * pointers, h_lse without lse_out, rows that are not whole 4-byte units, n_ctx > n_kv, or a
+ * workspace without room for the staging area.
+ */
+qsa_status qsa_decode_step_host(const void *h_in, float *h_out, float *h_lse, void *raw_k,
+                                qsa_dtype raw_dtype, int64_t n_ctx, int H_idx, int d_idx,
+                                const float *norm_w, float eps, double rope_base, void *pooled,
+                                qsa_dtype pooled_dtype, int64_t cap_rows, int64_t n_valid_full,
+                                int64_t n_q, float scale_idx, float *scores, int64_t k_blk,
+                                int32_t *blocks, int32_t *counts, void *K, void *V,
+                                qsa_dtype kv_dtype, int64_t n_kv, int H_kv, int d, int64_t ld_kv,
+                                int32_t *pos, int32_t *n_cells, int64_t max_cells, int H_q,
+                                float scale, float *out, float *lse_out, void *workspace,
+                                size_t workspace_bytes, qsa_stream_t stream);
+
+/* Total bytes of qsa_decode_step_host's packed input (0 for an invalid shape); offsets
+ * (nullable, [5]) receives the byte offsets of its sections: raw-key rows, K rows, V rows,
+ * q_idx, q (each 16-byte aligned). */
+size_t qsa_decode_step_host_layout(int64_t n_q, qsa_dtype raw_dtype, int H_idx, int d_idx,
+                                   qsa_dtype kv_dtype, int H_kv, int d, int H_q, int64_t *offsets);
+
+/* Workspace bytes of qsa_decode_step_host: the decode step's, then the staging area. */
+size_t qsa_decode_step_host_workspace_size(int64_t n_q, int H_q, int H_kv, int d,
+                                           int64_t max_cells, int64_t cap_rows,
+                                           qsa_dtype raw_dtype, int H_idx, int d_idx,
+                                           qsa_dtype kv_dtype);
+
+/*
  * qsa_sparse_attn_noalloc -- qsa_sparse_attn for callers that cannot allocate device
  * memory.
  *

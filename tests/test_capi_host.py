@@ -160,3 +160,34 @@ def test_mask_sparse_eligibility_rule():
     assert not qsa.mask_sparse_eligible(True, 0.0, 0.0, 4095, 16)
     assert not qsa.mask_sparse_eligible(True, 0.0, 0.0, 4096, 2049)
     assert qsa.mask_sparse_eligible(True, 0.0, 0.0, 4096, 2048)
+
+
+def test_decode_step_host_layout_and_validation(lib):
+    import ctypes as C
+
+    off = (C.c_int64 * 5)()
+    # 3 queries, bf16 raw keys 16x128, bf16 K/V 4x128, 32 query heads
+    total = lib.qsa_decode_step_host_layout(3, 1, 16, 128, 1, 4, 128, 32, off)
+    assert list(off) == [0, 12288, 15360, 18432, 43008]
+    assert total == 43008 + 3 * 32 * 128 * 4
+    assert all(o % 16 == 0 for o in off)
+    assert lib.qsa_decode_step_host_layout(0, 1, 16, 128, 1, 4, 128, 32, None) == 0
+    assert lib.qsa_decode_step_host_layout(3, 9, 16, 128, 1, 4, 128, 32, None) == 0
+    ws = lib.qsa_decode_step_workspace_size(3, 32, 4, 128, 2051, 4000)
+    wsh = lib.qsa_decode_step_host_workspace_size(3, 32, 4, 128, 2051, 4000, 1, 16, 128, 1)
+    assert wsh == ((ws + 255) // 256) * 256 + ((total + 255) // 256) * 256
+    st = None
+    # every call below fails validation (cap_rows = 4000 matches the sizes above), so
+    # nothing is ever enqueued with the fake pointers
+
+    def step(h_in=FAKE, h_out=FAKE, h_lse=None, lse=None, n_ctx=1000, n_kv=1000, ws_bytes=wsh):
+        return lib.qsa_decode_step_host(h_in, h_out, h_lse, FAKE, 1, n_ctx, 16, 128, FAKE, 1e-6,
+                                        1e4, FAKE, 0, 4000, 0, 3, 0.1, FAKE, 512, FAKE, FAKE,
+                                        FAKE, FAKE, 1, n_kv, 4, 128, 512, FAKE, FAKE, 2051, 32,
+                                        0.1, FAKE, lse, P(0x100000), ws_bytes, st)
+
+    assert step(h_in=None) == 1
+    assert step(h_out=None) == 1
+    assert step(h_lse=FAKE) == 1              # host lse without a device lse
+    assert step(n_kv=999) == 1                # the new rows would land past the K/V cache
+    assert step(ws_bytes=ws) == 1             # no room for the staging area

@@ -222,3 +222,42 @@ def test_multi_query_small_context_takes_every_block():
         np.testing.assert_array_equal(to_host(lay.blocks)[i, :len(o_blocks)], o_blocks)
         np.testing.assert_array_equal(to_host(lay.pos)[i, :len(o_cells)], o_cells)
         np.testing.assert_allclose(out[i], o_out, rtol=0, atol=ATOL_ATTN_F32)
+
+
+@pytest.mark.parametrize("n_q,store", [(1, "f32"), (3, "bf16")])
+def test_host_fed_step_equals_device_step(n_q, store):
+    """qsa_decode_step_host (new rows and queries from one packed host buffer, output back
+    to host memory) writes the same cache rows and gives bit-identical results to
+    qsa_decode_step on caches that already hold the new rows."""
+    shape = SMALL
+    inp = qsa_synth.decode_inputs(shape, seed=47, extra_tokens=n_q, n_steps=n_q)
+    n0 = shape.n_ctx
+    n_ctx = n0 + n_q
+    raw, w, K, V = (to_dev(inp["raw_k"]), to_dev(inp["norm_w"]), to_dev(inp["K"]),
+                    to_dev(inp["V"]))
+    qi, qa = to_dev(inp["q_idx"]), to_dev(inp["q"])
+    a = _layer(shape, n_ctx, store, n_q)
+    a.rebuild(raw, w, n0)
+    out_a = a.step(raw, w, K, V, n_ctx, qi, qa).clone()
+    raw_b, K_b, V_b = raw.clone(), K.clone(), V.clone()
+    raw_b[n0:n_ctx] = 0
+    K_b[n0:n_ctx] = 0
+    V_b[n0:n_ctx] = 0
+    b = _layer(shape, n_ctx, store, n_q)
+    b.rebuild(raw_b, w, n0)
+    b.enable_host_feed(raw.dtype, K.dtype)
+    b.bind(raw_b, w, K_b, V_b)
+    hin = b.host_inputs(n_q)
+    hin["raw"].copy_(raw[n0:n_ctx].reshape(n_q, -1).cpu())
+    hin["k"].copy_(K[n0:n_ctx].reshape(n_q, -1).cpu())
+    hin["v"].copy_(V[n0:n_ctx].reshape(n_q, -1).cpu())
+    hin["q_idx"].copy_(qi.cpu())
+    hin["q"].copy_(qa.cpu())
+    b.step_host(n_ctx, torch.cuda.current_stream().cuda_stream, n_q, with_lse=True)
+    torch.cuda.synchronize()
+    assert torch.equal(raw_b, raw) and torch.equal(K_b, K) and torch.equal(V_b, V)
+    assert torch.equal(a.pooled, b.pooled)
+    assert torch.equal(a.blocks[:n_q], b.blocks[:n_q])
+    assert torch.equal(a.n_cells[:n_q], b.n_cells[:n_q])
+    assert torch.equal(b.h_out[:n_q], out_a.cpu())
+    assert torch.equal(b.h_lse[:n_q], a.lse[:n_q].cpu())
