@@ -689,6 +689,23 @@ def oracle_decode_sample(shape, n_steps: int, budget_s: float, seed: int = 7):
     return done, t
 
 
+def host_description() -> str:
+    """Core count and CPU model of this host (the CPU baseline's machine)."""
+    model = ""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.split(":")[0].strip() in ("Model name", "Model"):
+                model = ln.split(":", 1)[1].strip()
+                if ln.startswith("Model name"):
+                    break
+    except Exception:
+        pass
+    import platform
+
+    return f"host {os.cpu_count()} cores, {model or platform.processor() or platform.machine()}"
+
+
 def config_for(shape, layers, pooled="f32", n_q=1):
     pes = 2 if pooled == "bf16" else 4
     step = "+1 token per step" if n_q == 1 else f"{n_q} query tokens (+{n_q} tokens) per step"
@@ -727,7 +744,8 @@ def main():
             "cpu_baseline": {"value": value, "unit": "steps/s", "cores": 1, "kind": "oracle",
                              "sample": f"{n_done} consecutive oracle decode steps of one layer "
                                        f"at {primary.n_ctx:,} tokens (bounded to ~90 s), after "
-                                       f"an untimed build of its pooled cache"},
+                                       f"an untimed build of its pooled cache; single-threaded "
+                                       f"C; {host_description()}"},
             "e2e": {"value": value, "unit": "steps/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0},
         }
@@ -788,7 +806,8 @@ def main():
                         "sample": f"{n_done} consecutive fp64 oracle decode steps of one layer at "
                                   f"{sh.n_ctx:,} tokens (pool update, score of all "
                                   f"{sh.n_rows:,} rows, full sort, attention), after an untimed "
-                                  f"build of its pooled cache; single-threaded C"}
+                                  f"build of its pooled cache; single-threaded C; "
+                                  f"{host_description()}"}
 
     line = {
         "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world,
