@@ -514,32 +514,56 @@ constexpr int kMmaTC = 16 * kMmaWarps;  // cells per stage: 16 per warp
 constexpr int kMmaLd = 136;             // padded smem row in bf16 elements = 272 bytes
 constexpr int kMmaMaxCluster = 16;      // splits of one (query, KV head) merged in-cluster
 
+// Shared memory of the tensor-core kernel with NW warps (16 cells each per stage) and NB
+// stage buffers: K and V stages, cell rows, per-warp states, the CTA's merged state.  With
+// one stage buffer the per-warp states reuse the stage area once the cells are done.
+template <int NW, int NB>
+__host__ __device__ constexpr size_t attn_mma_stage_bytes()
+{
+    return 2 * (size_t)NB * (16 * NW) * kMmaLd * 2;
+}
+template <int NW>
+__host__ __device__ constexpr size_t attn_mma_merge_bytes()
+{
+    return (size_t)NW * 8 * (128 + 2) * 4;
+}
+template <int NW, int NB>
 __host__ __device__ constexpr size_t attn_mma_smem()
 {
-    // K and V stages, cell rows, per-warp states, the CTA's merged state
-    return 2 * 2 * (size_t)kMmaTC * kMmaLd * 2 + 2 * kMmaTC * 4 +
-           (size_t)kMmaWarps * 8 * (128 + 2) * 4 + (size_t)8 * (128 + 2) * 4;
+    return (NB == 1 ? (attn_mma_stage_bytes<NW, NB>() > attn_mma_merge_bytes<NW>()
+                           ? attn_mma_stage_bytes<NW, NB>()
+                           : attn_mma_merge_bytes<NW>())
+                    : attn_mma_stage_bytes<NW, NB>() + attn_mma_merge_bytes<NW>()) +
+           2 * (size_t)(16 * NW) * 4 + (size_t)8 * (128 + 2) * 4;
 }
 
 // Grid (S, H_kv, n_q).  With S > 1 the S CTAs of one (query, KV head) form a thread-block
 // cluster: each merges its warps into one (m, l, o) per head in shared memory, then every
 // CTA combines a slice of the 8 x 128 outputs from all S states through distributed shared
 // memory -- no partials in global memory and no second kernel.
-__global__ void __launch_bounds__(32 * kMmaWarps)
+// NW warps per CTA (stages of 16 * NW cells), NB stage buffers (2: the next stage's rows
+// load while this one computes; 1: every split is one stage, and two CTAs fit an SM).
+template <int NW, int NB>
+__global__ void __launch_bounds__(32 * NW, (NB == 1 ? 2 : 0))
 attn_mma_kernel(const float *__restrict__ q, int H_q, int H_kv, float scale_log2,
                 const __nv_bfloat16 *__restrict__ K, const __nv_bfloat16 *__restrict__ V,
                 int64_t n_kv, int64_t ld_k, int64_t ld_v, const int32_t *__restrict__ pos,
                 const int32_t *__restrict__ n_cells, int64_t max_cells, float *__restrict__ out,
                 float *__restrict__ lse, int early_q)
 {
-    constexpr int G = 8, D = 128, TC = kMmaTC, LD = kMmaLd, NW = kMmaWarps, NT = 32 * NW;
+    constexpr int G = 8, D = 128, TC = 16 * NW, LD = kMmaLd, NT = 32 * NW;
     static_assert(NT == 2 * TC, "one thread per cell of the first two stages");
+    static_assert(NB == 1 || NB == 2, "one or two stage buffers");
+    constexpr size_t kStage = attn_mma_stage_bytes<NW, NB>();
+    constexpr size_t kMerge = attn_mma_merge_bytes<NW>();
     extern __shared__ __align__(16) char smem_raw[];
-    __nv_bfloat16 *Ks = reinterpret_cast<__nv_bfloat16 *>(smem_raw);  // [2][TC][LD]
-    __nv_bfloat16 *Vs = Ks + 2 * TC * LD;                                // [2][TC][LD]
-    int32_t *rows = reinterpret_cast<int32_t *>(Vs + 2 * TC * LD);      // [2][TC]
-    float *mrg = reinterpret_cast<float *>(rows + 2 * TC);               // [NW][G][D+2]
-    float *cta = mrg + NW * G * (D + 2);                                 // [G][D+2]: o, m, l
+    __nv_bfloat16 *Ks = reinterpret_cast<__nv_bfloat16 *>(smem_raw);  // [NB][TC][LD]
+    __nv_bfloat16 *Vs = Ks + NB * TC * LD;                               // [NB][TC][LD]
+    char *tail = smem_raw + (NB == 1 ? (kStage > kMerge ? kStage : kMerge) : kStage + kMerge);
+    int32_t *rows = reinterpret_cast<int32_t *>(tail);                   // [2][TC]
+    // [NW][G][D+2] per-warp states: after the stages (two buffers) or over them (one)
+    float *mrg = reinterpret_cast<float *>(NB == 1 ? smem_raw : smem_raw + kStage);
+    float *cta = reinterpret_cast<float *>(rows + 2 * TC);               // [G][D+2]: o, m, l
 
     const int S = gridDim.x, s_idx = blockIdx.x, g = blockIdx.y;
     const int64_t qi = blockIdx.z;
@@ -671,12 +695,17 @@ attn_mma_kernel(const float *__restrict__ q, int H_q, int H_kv, float scale_log2
     };
 
     if (ntiles > 0) copy_rows(0);
-    if (ntiles > 1) copy_rows(1);
+    if (NB == 2 && ntiles > 1) copy_rows(1);
     for (int it = 0; it < ntiles; ++it) {
-        const int buf = it & 1;
-        if (it >= 1 && it + 1 < ntiles) {
-            load_rows(it + 1, buf ^ 1);
-            copy_rows(buf ^ 1);
+        const int buf = NB == 2 ? (it & 1) : 0;
+        if (NB == 2) {
+            if (it >= 1 && it + 1 < ntiles) {
+                load_rows(it + 1, buf ^ 1);
+                copy_rows(buf ^ 1);
+            }
+        } else if (it >= 1) {  // one buffer: the previous stage is done (barrier below)
+            load_rows(it, 0);
+            copy_rows(0);
         }
         wait_rows(buf);
         const int tc = (int)min((int64_t)TC, c1 - (c0 + (int64_t)it * TC));
@@ -959,27 +988,45 @@ int attn_mma_splits(int64_t n_q, int H_kv, int64_t max_cells)
     return (int)S;
 }
 
+template <int NW, int NB>
+cudaError_t launch_attn_mma_t(int S, const float *q, int64_t n_q, int H_q, int H_kv, float scale,
+                              const void *K, const void *V, int64_t n_kv, int64_t ld_k,
+                              int64_t ld_v, const int32_t *pos, const int32_t *n_cells,
+                              int64_t max_cells, float *out, float *lse, cudaStream_t st,
+                              bool early_q)
+{
+    auto k = attn_mma_kernel<NW, NB>;
+    const size_t smem = attn_mma_smem<NW, NB>();
+    static bool set = false;
+    if (!set) {
+        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)smem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return e;
+        set = true;
+    }
+    const dim3 grid((unsigned)S, (unsigned)H_kv, (unsigned)n_q);
+    return launch(k, grid, dim3(32 * NW), smem, st, S > 1 ? S : 1, q, H_q, H_kv,
+                  scale * kLog2e, (const __nv_bfloat16 *)K, (const __nv_bfloat16 *)V, n_kv, ld_k,
+                  ld_v, pos, n_cells, max_cells, out, lse, early_q ? 1 : 0);
+}
+
 cudaError_t launch_attn_mma(const float *q, int64_t n_q, int H_q, int H_kv, float scale,
                             const void *K, const void *V, int64_t n_kv, int64_t ld_k, int64_t ld_v,
                             const int32_t *pos, const int32_t *n_cells, int64_t max_cells,
                             float *out, float *lse, cudaStream_t st, bool early_q)
 {
-    const size_t smem = attn_mma_smem();
-    static bool set = false;
-    if (!set) {
-        cudaError_t e = cudaFuncSetAttribute(attn_mma_kernel,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(attn_mma_kernel,
-                                     cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-        if (e != cudaSuccess) return e;
-        set = true;
-    }
     const int S = attn_mma_splits(n_q, H_kv, max_cells);
-    const dim3 grid((unsigned)S, (unsigned)H_kv, (unsigned)n_q);
-    return launch(attn_mma_kernel, grid, dim3(32 * kMmaWarps), smem, st, S > 1 ? S : 1, q, H_q,
-                  H_kv, scale * kLog2e, (const __nv_bfloat16 *)K, (const __nv_bfloat16 *)V, n_kv,
-                  ld_k, ld_v, pos, n_cells, max_cells, out, lse, early_q ? 1 : 0);
+    // Several queries per step: n_q * H_kv clusters of S CTAs at one CTA per SM would need a
+    // second wave.  With one stage buffer (the splits are about one stage long) two CTAs
+    // share an SM and the step fits one wave.
+    const int64_t ctas = n_q * (int64_t)H_kv * S;
+    if (S > 1 && ctas > device_sm_count() && ctas <= 2 * (int64_t)device_sm_count())
+        return launch_attn_mma_t<kMmaWarps, 1>(S, q, n_q, H_q, H_kv, scale, K, V, n_kv, ld_k, ld_v,
+                                               pos, n_cells, max_cells, out, lse, st, early_q);
+    return launch_attn_mma_t<kMmaWarps, 2>(S, q, n_q, H_q, H_kv, scale, K, V, n_kv, ld_k, ld_v, pos,
+                                           n_cells, max_cells, out, lse, st, early_q);
 }
 
 template <typename T, int G>
