@@ -224,12 +224,12 @@ def test_multi_query_small_context_takes_every_block():
         np.testing.assert_allclose(out[i], o_out, rtol=0, atol=ATOL_ATTN_F32)
 
 
-@pytest.mark.parametrize("n_q,store", [(1, "f32"), (3, "bf16")])
-def test_host_fed_step_equals_device_step(n_q, store):
+@pytest.mark.parametrize("shape,n_q,store", [(SMALL, 1, "f32"), (SMALL, 3, "bf16"),
+                                             (TINY, 2, "f32")], ids=["bf16-1", "bf16-3", "f32-2"])
+def test_host_fed_step_equals_device_step(shape, n_q, store):
     """qsa_decode_step_host (new rows and queries from one packed host buffer, output back
     to host memory) writes the same cache rows and gives bit-identical results to
     qsa_decode_step on caches that already hold the new rows."""
-    shape = SMALL
     inp = qsa_synth.decode_inputs(shape, seed=47, extra_tokens=n_q, n_steps=n_q)
     n0 = shape.n_ctx
     n_ctx = n0 + n_q
