@@ -661,10 +661,8 @@ def summarize(r, world, layers, peak):
 
 # ----------------------------------------------------------------------------- CPU oracle
 
-def oracle_decode_sample(shape, n_steps: int, budget_s: float, seed: int = 7):
-    """Time the fp64 oracle's decode step (incremental pool update of the new rows, score
-    of every row, full sort, attention) for up to n_steps steps or budget_s seconds, after
-    an untimed build of its pooled cache.  Returns (steps, seconds)."""
+def oracle_prepare(shape, n_steps: int, seed: int = 7):
+    """The oracle's decode inputs and its pooled cache built up to the first step (untimed)."""
     from oracle import oracle
     import qsa_synth
 
@@ -674,19 +672,94 @@ def oracle_decode_sample(shape, n_steps: int, budget_s: float, seed: int = 7):
     pooled = np.zeros((cap, shape.H_idx * shape.d_idx), np.float32)
     oracle.pool_rows(inp["raw_k"], n0, shape.H_idx, shape.d_idx, inp["norm_w"], shape.eps,
                      shape.rope_base, 0, (n0 + 3) // 4, pooled)
-    valid = n0 // 4
+    return inp, pooled
+
+
+def oracle_steps(shape, inp, pooled, n_steps: int, budget_s: float, first_q: int = 0):
+    """Consecutive oracle decode steps (incremental pool update of the new rows, score of
+    every row, full sort, attention) on ``pooled`` for up to n_steps steps or budget_s
+    seconds.  Returns (steps, seconds)."""
+    from oracle import oracle
+
+    valid = (shape.n_ctx - 1) // 4
     done, t = 0, 0.0
     while done < n_steps and t < budget_s:
         n_ctx = shape.n_ctx + done
+        j = (first_q + done) % 4
         t0 = time.perf_counter()
         oracle.decode_step(inp["raw_k"], n_ctx, shape.H_idx, shape.d_idx, inp["norm_w"], shape.eps,
-                           shape.rope_base, pooled, valid, inp["q_idx"][done % 4],
-                           shape.top_k_tokens, inp["q"][done % 4], inp["K"], inp["V"], shape.H_q,
-                           shape.H_kv, shape.d)
+                           shape.rope_base, pooled, valid, inp["q_idx"][j], shape.top_k_tokens,
+                           inp["q"][j], inp["K"], inp["V"], shape.H_q, shape.H_kv, shape.d)
         t += time.perf_counter() - t0
         valid = n_ctx // 4
         done += 1
     return done, t
+
+
+def oracle_decode_sample(shape, n_steps: int, budget_s: float, seed: int = 7):
+    """Single-threaded oracle decode steps after an untimed build of its pooled cache."""
+    inp, pooled = oracle_prepare(shape, n_steps, seed)
+    return oracle_steps(shape, inp, pooled, n_steps, budget_s)
+
+
+def _oracle_worker(shape_name, folder, rank, n_steps, budget_s, start, results):
+    """One process of the all-cores oracle timing: its own copy of the pooled cache, the
+    shared inputs read from files."""
+    sys.path.insert(0, ROOT)
+    import qsa_synth
+
+    shape = qsa_synth.CONFIGS[shape_name]
+    inp = {k: np.load(os.path.join(folder, k + ".npy"), mmap_mode="r")
+           for k in ("raw_k", "norm_w", "K", "V", "q_idx", "q")}
+    inp = {k: np.ascontiguousarray(v) if k in ("norm_w", "q_idx", "q") else v
+           for k, v in inp.items()}
+    pooled = np.array(np.load(os.path.join(folder, "pooled.npy"), mmap_mode="r"))
+    start.wait(timeout=600)
+    done, _ = oracle_steps(shape, inp, pooled, n_steps, budget_s, first_q=rank)
+    results.put(done)
+
+
+def oracle_all_cores_sample(shape_name, n_proc: int, n_steps: int, budget_s: float):
+    """The oracle as it stands (single-threaded C) run as n_proc independent processes, one
+    per host core, each stepping its own copy of the same layer: aggregate steps/s over the
+    wall time from a common start.  Inputs are built once and shared through files."""
+    import multiprocessing as mp
+    import shutil
+    import tempfile
+
+    import qsa_synth
+
+    shape = qsa_synth.CONFIGS[shape_name]
+    inp, pooled = oracle_prepare(shape, n_steps)
+    base = "/dev/shm" if os.path.isdir("/dev/shm") else None
+    folder = tempfile.mkdtemp(prefix="qsa_oracle_", dir=base)
+    try:
+        for k in ("raw_k", "norm_w", "K", "V", "q_idx", "q"):
+            np.save(os.path.join(folder, k + ".npy"), inp[k])
+        np.save(os.path.join(folder, "pooled.npy"), pooled)
+        del inp, pooled
+        ctx = mp.get_context("spawn")
+        start = ctx.Barrier(n_proc + 1)
+        results = ctx.Queue()
+        procs = [ctx.Process(target=_oracle_worker,
+                             args=(shape_name, folder, r, n_steps, budget_s, start, results))
+                 for r in range(n_proc)]
+        for p in procs:
+            p.start()
+        try:
+            start.wait(timeout=600)
+            t0 = time.perf_counter()
+            total = sum(results.get(timeout=600) for _ in range(n_proc))
+            wall = time.perf_counter() - t0
+        except Exception:  # a worker that died or stalled: no all-cores figure
+            total, wall = None, None
+        for p in procs:
+            p.join(60)
+            if p.is_alive():
+                p.kill()
+        return total, wall
+    finally:
+        shutil.rmtree(folder, ignore_errors=True)
 
 
 def host_description() -> str:
@@ -800,6 +873,7 @@ def main():
     ablation = None if args.no_ablation else run_ablation(args, local)
 
     cpu_baseline = None
+    cpu_all_cores = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         n_done, t = oracle_decode_sample(sh, n_steps=40, budget_s=20.0)
         cpu_baseline = {"value": n_done / t, "unit": "steps/s", "cores": 1, "kind": "oracle",
@@ -808,6 +882,17 @@ def main():
                                   f"{sh.n_rows:,} rows, full sort, attention), after an untimed "
                                   f"build of its pooled cache; single-threaded C; "
                                   f"{host_description()}"}
+        n_proc = os.cpu_count() or 1
+        total = wall = None
+        if n_proc > 1:
+            total, wall = oracle_all_cores_sample(CONTEXTS[args.primary], n_proc, 40, 12.0)
+        if n_proc > 1 and total:
+            cpu_all_cores = {"value": total / wall, "unit": "steps/s", "cores": n_proc,
+                             "kind": "oracle",
+                             "sample": f"{n_proc} processes (one per host core), each running "
+                                       f"up to 40 of the same single-threaded oracle steps "
+                                       f"(or 12 s) on its own copy of the layer; {total} steps "
+                                       f"in {wall:.1f} s of wall time; {host_description()}"}
 
     line = {
         "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world,
@@ -832,6 +917,7 @@ def main():
         "mask": mask,
         "ablation": ablation,
         "cpu_baseline": cpu_baseline,
+        "cpu_baseline_all_cores": cpu_all_cores,
     }
     if rank == 0:
         print(json.dumps(line))
