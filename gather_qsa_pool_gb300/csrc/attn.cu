@@ -7,12 +7,18 @@
 // "llama.cpp CDNA sparse attention", sections 2-3 (attention over the listed key
 // positions; DKQ 576 with 16 query heads per KV head).
 //
-// Grid (split, kv head, query).  Each CTA stages 32 listed rows of K and V at a time from
-// the full cache into shared memory with 16-byte cp.async (the gather happens on the way
-// in: no compact copy round-trips through HBM), double-buffered so the next tile's loads
-// overlap this tile's math.  Logits: one warp per cell, lanes split the head dim, one
-// warp reduction per query head of the group.  Softmax: one warp per head, one lane per
-// cell.  P.V: each thread owns G*d_v/128 output entries.  fp32 throughout.
+// Every kernel here reads the listed rows straight from the full cache into shared memory
+// (the gather happens on the way in: no compact copy round-trips through HBM).
+//   - attn_mma_kernel: the decode form (bf16, head dim 128, 8 query heads per KV head):
+//     tensor-core mma.sync, bulk-copy staging, the splits of one (query, KV head) combined
+//     inside a thread-block cluster.  See the comment above it.
+//   - attn128_kernel: head dim 128 for other dtypes and group sizes.
+//   - sparse_attn_kernel: any shape.  Grid (split, kv head, query); each CTA stages 32
+//     listed rows of K and V at a time with 16-byte cp.async, double-buffered so the next
+//     tile's loads overlap this tile's math.  Logits: one warp per cell, lanes split the
+//     head dim, one warp reduction per query head of the group.  Softmax: one warp per
+//     head, one lane per cell.  P.V: each thread owns G*d_v/128 output entries.  fp32.
+//   - attn_combine_kernel: the log-sum-exp merge of the splits of the last two.
 #include <cooperative_groups.h>
 
 #include "mma_frag.cuh"

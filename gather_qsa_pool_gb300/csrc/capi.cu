@@ -55,7 +55,7 @@ const char *qsa_status_str(qsa_status s)
     return "QSA_ERR_UNKNOWN";
 }
 
-int qsa_version(void) { return (1 << 16) | 0; }
+int qsa_version(void) { return (2 << 16) | 0; }
 
 static qsa_status check_pool_update(const void *raw_k, qsa_dtype raw_dtype, int64_t n_ctx, int H,
                                     int d, const float *norm_w, float eps, double rope_base,

@@ -24,13 +24,13 @@
 // If the candidate list would overflow shared memory (pathological score
 // distributions), steps 3-4 re-read the scores instead.
 //
-// Decode form (inside qsa_decode_step, one query): one kernel of ceil(n/1024) CTAs.
-// Every CTA finds the threshold bucket in the score kernel's histogram with a two-level
-// warp search, classifies its 1024 blocks with ballots (bitmap words for the blocks
-// above the bucket, a per-CTA list for the blocks inside it), then takes a ticket; the
-// last CTA to arrive resolves the bucket by ranking its candidates against each other
-// (key descending, index ascending), writes the selection, the cells and the tail, and
-// clears the histogram.  No CTA waits for another: the ticket decides which CTA
+// Decode form (inside qsa_decode_step, 1-4 queries): one kernel of ceil(n/1024) CTAs per
+// query.  Every CTA finds the threshold bucket in its query's histogram (built by the
+// score kernel) with a two-level warp search, classifies its 1024 blocks with ballots
+// (bitmap words for the blocks above the bucket, a per-CTA list for the blocks inside it),
+// then takes its query's ticket; the last CTA to arrive settles the bucket with a second
+// 8-bit digit and ranks the few candidates left against each other (key descending, index
+// ascending), writes the selection, the cells and the tail, and clears the histogram.  No CTA waits for another: the ticket decides which CTA
 // finishes the work, so there is no spin-wait.  A histogram whose total disagrees with
 // the block count (a workspace never cleared), or a bucket holding more than 1024
 // candidates, sends the last CTA through the general form instead.

@@ -12,9 +12,10 @@
  * and the mask-driven variant is qsa_mask_to_list -> qsa_sparse_attn.
  *
  * Conventions shared by every entry point
- *   - Every tensor pointer is device memory owned by the caller; the library never
- *     allocates, frees or keeps a pointer past the call.  Scratch memory comes from a
- *     caller buffer whose size the matching *_workspace_size() function returns.
+ *   - Every tensor pointer is device memory owned by the caller (except the host buffers
+ *     of qsa_decode_step_host); the library never allocates, frees or keeps a pointer past
+ *     the call.  Scratch memory comes from a caller buffer whose size the matching
+ *     *_workspace_size() function returns.
  *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy default
  *     stream) and never synchronises with the host.
  *   - The returned status is decided on the host from the arguments before anything is
@@ -60,7 +61,8 @@ typedef enum {
 /* Human-readable name of a status code (static storage). */
 const char *qsa_status_str(qsa_status s);
 
-/* Library ABI version: (major << 16) | minor. */
+/* Library ABI version: (major << 16) | minor.  Major 2: pooled-cache dtype arguments,
+ * several queries per decode step, the host-fed decode step. */
 int qsa_version(void);
 
 /*

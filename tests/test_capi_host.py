@@ -31,7 +31,7 @@ def test_status_strings_and_version(lib):
     assert qsa.status_str(0) == "QSA_OK"
     assert qsa.status_str(1) == "QSA_ERR_INVALID_ARG"
     assert qsa.status_str(4) == "QSA_ERR_TIMEOUT"
-    assert lib.qsa_version() >> 16 == 1
+    assert lib.qsa_version() >> 16 == 2
 
 
 def test_pool_update_rejects(lib):
