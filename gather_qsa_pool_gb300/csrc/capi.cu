@@ -383,12 +383,8 @@ static qsa_status decode_step_impl(const void *raw_k, qsa_dtype raw_dtype, int64
     // 3. top-k from those histograms; the last CTA of each query also writes its cell list
     // (qsa_gather_kv's job).  When a query's blocks are all selected, the one-CTA form does it.
     if (e == cudaSuccess) {
-        const int64_t esize = kv_dtype == QSA_BF16 ? 2 : 4;
-        const int64_t row_bytes = (int64_t)H_kv * d * esize;
-        const bool contiguous = ld_kv == (int64_t)H_kv * d;
         e = launch_topk_select(scores, n_rows, (int)n_q, n_full, cap_rows, k_blk, n_ctx, hist, sel,
-                               blocks, counts, pos, n_cells, max_cells, contiguous ? K : nullptr,
-                               contiguous ? V : nullptr, row_bytes, st);
+                               blocks, counts, pos, n_cells, max_cells, st);
         if (e == cudaErrorNotSupported)
             e = launch_topk(scores, n_q, n_rows, nullptr, n_full, k_blk, blocks, counts, n_ctx, pos,
                             n_cells, max_cells, hist, st, 1);

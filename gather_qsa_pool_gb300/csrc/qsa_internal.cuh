@@ -131,12 +131,6 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
         : "memory");
 }
 
-// Bulk L2 prefetch of [p, p + bytes): p 16-byte aligned, bytes a multiple of 16.
-__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes)
-{
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
-
 template <typename... KArgs, typename... Args>
 cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
                    cudaStream_t stream, int cluster_x, Args &&...args)
@@ -348,9 +342,6 @@ cudaError_t launch_topk(const float *scores, int64_t n_q, int64_t ld, const int3
 // 256-byte aligned, whose first word (the ticket) the step's score kernel sets to 0.
 // Returns cudaErrorNotSupported, without launching, when n_full <= k_blk or n_full is
 // above topk_max_candidates().
-// kv_k / kv_v (nullable): K and V caches whose rows are contiguous (row stride = row
-// size = kv_row_bytes, a multiple of 16, bases 16-byte aligned); the K and V rows of the
-// blocks that clear the threshold bucket are then prefetched into L2 for the attention.
 // Several queries (n_q <= kMaxStreamQueries, the last n_q tokens of the context: query i
 // at position n_ctx - n_q + i, candidates b < min(n_full, floor((p_i+1)/4))) run as
 // grid.y = n_q: query i reads scores + i*ld_scores and hist + i*2^kTopkHistBits, uses
@@ -361,7 +352,6 @@ cudaError_t launch_topk_select(const float *scores, int64_t ld_scores, int n_q, 
                                int64_t n_full_cap, int64_t k_blk, int64_t n_ctx, uint32_t *hist,
                                void *scratch, int32_t *blocks_out, int32_t *counts_out,
                                int32_t *pos_out, int32_t *n_cells_out, int64_t max_cells,
-                               const void *kv_k, const void *kv_v, int64_t kv_row_bytes,
                                cudaStream_t st);
 size_t topk_select_workspace_bytes(int64_t n_full_cap);
 uint32_t *topk_select_ticket(void *scratch);

@@ -540,8 +540,7 @@ topk_select_kernel(const float *__restrict__ scores, int64_t ld_scores, int n_q,
                    uint2 *__restrict__ cand, int32_t *__restrict__ cand_cnt, int64_t q_stride,
                    int32_t *__restrict__ blocks_out, int32_t *__restrict__ counts_out,
                    int32_t *__restrict__ pos_out, int32_t *__restrict__ n_cells_out,
-                   int64_t max_cells, int cand_cap, const char *kv_k, const char *kv_v,
-                   uint32_t kv_block_bytes)
+                   int64_t max_cells, int cand_cap)
 {
     extern __shared__ __align__(16) uint32_t smem[];
     __shared__ uint32_t wtot[NT / 32];
@@ -555,8 +554,6 @@ topk_select_kernel(const float *__restrict__ scores, int64_t ld_scores, int n_q,
     QSA_AFTER_WAIT(bitmap);
     QSA_AFTER_WAIT(cand);
     QSA_AFTER_WAIT(cand_cnt);
-    QSA_AFTER_WAIT(kv_k);
-    QSA_AFTER_WAIT(kv_v);
     pdl_trigger();
 
     // this CTA's query
@@ -639,12 +636,6 @@ topk_select_kernel(const float *__restrict__ scores, int64_t ld_scores, int n_q,
     const bool in = valid && i < n;
     const bool above = in && (dg > B1 || (whole && dg == B1));
     const bool is_cand = in && !whole && dg == B1;
-    // Blocks above the bucket are selected whatever the bucket resolves to: start pulling
-    // their K and V rows into L2 now, for the attention kernel that follows.
-    if (above && kv_k) {
-        prefetch_l2(kv_k + i * (int64_t)kv_block_bytes, kv_block_bytes);
-        prefetch_l2(kv_v + i * (int64_t)kv_block_bytes, kv_block_bytes);
-    }
     const uint32_t word = __ballot_sync(0xffffffffu, above);
     const int64_t wi = (int64_t)blockIdx.x * (NT / 32) + warp;
     if (lane == 0 && wi < nw) bitmap[wi] = word;
@@ -812,7 +803,6 @@ cudaError_t launch_topk_select(const float *scores, int64_t ld_scores, int n_q, 
                                int64_t n_full_cap, int64_t k_blk, int64_t n_ctx, uint32_t *hist,
                                void *scratch, int32_t *blocks_out, int32_t *counts_out,
                                int32_t *pos_out, int32_t *n_cells_out, int64_t max_cells,
-                               const void *kv_k, const void *kv_v, int64_t kv_row_bytes,
                                cudaStream_t st)
 {
     // the first query has the fewest candidates
@@ -820,9 +810,6 @@ cudaError_t launch_topk_select(const float *scores, int64_t ld_scores, int n_q, 
     const int64_t n_min = (p0 + 1) / 4 < n_full ? (p0 + 1) / 4 : n_full;
     if (n_q < 1 || n_q > 65535 || n_min <= k_blk || n_full > kMaxN || n_full > n_full_cap)
         return cudaErrorNotSupported;
-    if (!kv_k || !kv_v || kv_row_bytes <= 0 || kv_row_bytes % 16 || 4 * kv_row_bytes > (1 << 20) ||
-        (reinterpret_cast<uintptr_t>(kv_k) | reinterpret_cast<uintptr_t>(kv_v)) % 16)
-        kv_k = kv_v = nullptr;
     const int64_t nw = (n_full + 31) / 32;
     const int64_t g = (n_full + NT - 1) / NT;
     auto al = [](int64_t b) { return (b + 255) & ~(int64_t)255; };
@@ -842,7 +829,7 @@ cudaError_t launch_topk_select(const float *scores, int64_t ld_scores, int n_q, 
     return launch(topk_select_kernel, dim3((unsigned)g, (unsigned)n_q), dim3(NT), smem, st, 1,
                   scores, ld_scores, n_q, n_full, (int)k_blk, n_ctx, hist, ticket, bitmap, cand,
                   cand_cnt, q_stride, blocks_out, counts_out, pos_out, n_cells_out, max_cells,
-                  cand_cap, (const char *)kv_k, (const char *)kv_v, (uint32_t)(4 * kv_row_bytes));
+                  cand_cap);
 }
 
 uint32_t *topk_select_ticket(void *scratch) { return static_cast<uint32_t *>(scratch); }
