@@ -1003,15 +1003,8 @@ cudaError_t launch_attn_mma_t(int S, const float *q, int64_t n_q, int H_q, int H
 {
     auto k = attn_mma_kernel<NW, NB>;
     const size_t smem = attn_mma_smem<NW, NB>();
-    static bool set = false;
-    if (!set) {
-        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)smem);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-        if (e != cudaSuccess) return e;
-        set = true;
-    }
+    cudaError_t ea = ensure_kernel_attrs<attn_mma_kernel<NW, NB>>(smem, true);
+    if (ea != cudaSuccess) return ea;
     const dim3 grid((unsigned)S, (unsigned)H_kv, (unsigned)n_q);
     return launch(k, grid, dim3(32 * NW), smem, st, S > 1 ? S : 1, q, H_q, H_kv,
                   scale * kLog2e, (const __nv_bfloat16 *)K, (const __nv_bfloat16 *)V, n_kv, ld_k,
@@ -1043,13 +1036,8 @@ cudaError_t launch_attn128_t(const float *q, int64_t n_q, int H_q, int H_kv, flo
 {
     auto k = attn128_kernel<T, G>;
     const size_t smem = attn128_smem<T, G>();
-    static bool set = false;
-    if (!set) {
-        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)smem);
-        if (e != cudaSuccess) return e;
-        set = true;
-    }
+    cudaError_t ea = ensure_kernel_attrs<attn128_kernel<T, G>>(smem);
+    if (ea != cudaSuccess) return ea;
     const dim3 grid((unsigned)S, (unsigned)H_kv, (unsigned)n_q);
     cudaError_t e = launch(k, grid, dim3(128), smem, st, 1, q, H_q, H_kv, scale * kLog2e,
                            (const T *)K, (const T *)V, n_kv, ld_k, ld_v, pos, n_cells, max_cells,
@@ -1069,13 +1057,8 @@ cudaError_t launch_attn_t(const float *q, int64_t n_q, int H_q, int H_kv, int d_
 {
     auto k = sparse_attn_kernel<T, G>;
     const size_t smem = attn_smem_bytes(G, d_k, d_v, (int)sizeof(T));
-    static size_t set_bytes = 0;
-    if (smem > 48 * 1024 && set_bytes < smem) {
-        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)smem);
-        if (e != cudaSuccess) return e;
-        set_bytes = smem;
-    }
+    cudaError_t ea = ensure_kernel_attrs<sparse_attn_kernel<T, G>>(smem);
+    if (ea != cudaSuccess) return ea;
     const dim3 grid((unsigned)S, (unsigned)H_kv, (unsigned)n_q);
     cudaError_t e = launch(k, grid, dim3(kAttnThreads), smem, st, 1, q, H_q, H_kv, d_k, d_v,
                            scale * kLog2e, (const T *)K, (const T *)V, n_kv, ld_k, ld_v, pos,

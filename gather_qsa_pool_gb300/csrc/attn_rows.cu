@@ -292,14 +292,8 @@ cudaError_t launch_attn_rows4(const float *q, int64_t n_q, int H_q, float scale,
                               const int32_t *pos, const int32_t *n_cells, int64_t max_cells,
                               float *out, float *lse, cudaStream_t st)
 {
-    static bool set = false;
-    if (!set) {
-        cudaError_t e = cudaFuncSetAttribute(attn_rows4_kernel,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)kRSmem);
-        if (e != cudaSuccess) return e;
-        set = true;
-    }
+    const cudaError_t e = ensure_kernel_attrs<attn_rows4_kernel>(kRSmem);
+    if (e != cudaSuccess) return e;
     return launch(attn_rows4_kernel, dim3((unsigned)n_q), dim3(kRNT), kRSmem, st, 1, q, H_q,
                   scale * kLog2e, (const __nv_bfloat16 *)K, (const __nv_bfloat16 *)V, n_kv, ld_k,
                   ld_v, pos, n_cells, max_cells, out, lse);

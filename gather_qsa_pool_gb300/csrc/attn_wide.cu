@@ -397,17 +397,8 @@ cudaError_t launch_attn_wide(const float *q, int64_t n_q, int H_q, int H_kv, flo
                              const int32_t *n_cells, int64_t max_cells, float *out, float *lse,
                              cudaStream_t st)
 {
-    static bool set = false;
-    if (!set) {
-        cudaError_t e = cudaFuncSetAttribute(attn_wide_kernel,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)kWSmem);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(attn_wide_kernel,
-                                     cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-        if (e != cudaSuccess) return e;
-        set = true;
-    }
+    const cudaError_t ea = ensure_kernel_attrs<attn_wide_kernel>(kWSmem, true);
+    if (ea != cudaSuccess) return ea;
     const int S = attn_wide_splits(n_q, H_kv, max_cells);
     const dim3 grid((unsigned)S, (unsigned)H_kv, (unsigned)n_q);
     return launch(attn_wide_kernel, grid, dim3(kWNT), kWSmem, st, S > 1 ? S : 1, q, H_q, H_kv,

@@ -395,13 +395,7 @@ qsa_status launch_index_score_tc(const float *q, int64_t n_q, int64_t ld_q,
                    reinterpret_cast<uint2 *>(const_cast<__nv_bfloat16 *>(pb)));
     }
     if (e != cudaSuccess) return QSA_ERR_CUDA;
-    static bool attr = false;
-    if (!attr) {
-        if (cudaFuncSetAttribute(score_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)tc_smem_bytes()) != cudaSuccess)
-            return QSA_ERR_CUDA;
-        attr = true;
-    }
+    if (ensure_kernel_attrs<score_tc_kernel>(tc_smem_bytes()) != cudaSuccess) return QSA_ERR_CUDA;
     const int64_t n_units = ((n_q + kBM - 1) / kBM) * ((n_rows + kBN - 1) / kBN);
     int64_t grid = device_sm_count();
     if (grid > n_units) grid = n_units;

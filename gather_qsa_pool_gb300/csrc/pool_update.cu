@@ -66,13 +66,8 @@ cudaError_t launch_pool_typed(const void *raw_k, int64_t n_ctx, int H, int d,
 {
     const size_t smem = sizeof(float) * ((size_t)H * d + (size_t)d);
     auto k = pool_update_kernel<T, TP>;
-    static bool attr_set = false;
-    if (smem > 48 * 1024 && !attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             200 * 1024);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+    const cudaError_t e = ensure_kernel_attrs<pool_update_kernel<T, TP>>(smem);
+    if (e != cudaSuccess) return e;
     return launch(k, dim3((unsigned)n), dim3(kPoolThreads), smem, st, 1, (const T *)raw_k, n_ctx,
                   H, d, norm_w, eps, tab, (TP *)pooled, row0, row1, zero_hist);
 }

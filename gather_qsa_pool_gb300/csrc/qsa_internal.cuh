@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <utility>
 
 #include "../../include/qsa.h"
@@ -166,6 +167,33 @@ cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
 }
 
 int device_sm_count();
+
+// Kernel attributes are per device: raise the kernel's dynamic shared-memory limit to at
+// least `smem` bytes (and, when asked, allow non-portable cluster sizes) on the current
+// device, once per (kernel, device) and size.
+template <auto Kernel>
+cudaError_t ensure_kernel_attrs(size_t smem, bool nonportable_cluster = false)
+{
+    constexpr int kMaxDevices = 64;
+    static std::atomic<size_t> smem_set[kMaxDevices];  // zero before first use (static)
+    static std::atomic<bool> cluster_set[kMaxDevices];
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) dev = -1;
+    if (dev >= 0 && smem_set[dev].load() >= smem && (!nonportable_cluster || cluster_set[dev].load()))
+        return cudaSuccess;
+    cudaError_t e = cudaSuccess;
+    if (smem > 48 * 1024)
+        e = cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e == cudaSuccess && nonportable_cluster)
+        e = cudaFuncSetAttribute(Kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e == cudaSuccess && dev >= 0) {
+        size_t cur = smem_set[dev].load();
+        while (cur < smem && !smem_set[dev].compare_exchange_weak(cur, smem)) {
+        }
+        if (nonportable_cluster) cluster_set[dev].store(true);
+    }
+    return e;
+}
 
 // ------------------------------------------------------------------ RoPE frequencies
 // Inverse frequencies theta_i = base^(-2i/d), i < d/2, computed on the host in fp64 and

@@ -775,14 +775,8 @@ size_t topk_smem_bytes(int64_t n, int *cand_cap)
 
 cudaError_t set_max_smem()
 {
-    static bool done = false;
-    if (done) return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kMaxSmemBytes);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(topk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kMaxSmemBytes);
-    if (e == cudaSuccess) done = true;
+    cudaError_t e = ensure_kernel_attrs<topk_kernel>(kMaxSmemBytes);
+    if (e == cudaSuccess) e = ensure_kernel_attrs<topk_select_kernel>(kMaxSmemBytes);
     return e;
 }
 
