@@ -523,10 +523,18 @@ constexpr int kMmaMaxCluster = 16;      // splits of one (query, KV head) merged
 // Shared memory of the tensor-core kernel with NW warps (16 cells each per stage) and NB
 // stage buffers: K and V stages, cell rows, per-warp states, the CTA's merged state.  With
 // one stage buffer the per-warp states reuse the stage area once the cells are done.
+// Rows of a stage buffer: 16 per warp, and with one buffer 16 more, so that a split a few
+// cells longer than a stage (the last of 2,051 cells over 16 splits holds 131) is still
+// one stage (its last warp takes the extra cells).
+template <int NW, int NB>
+__host__ __device__ constexpr int attn_mma_stage_rows()
+{
+    return 16 * NW + (NB == 1 ? 16 : 0);
+}
 template <int NW, int NB>
 __host__ __device__ constexpr size_t attn_mma_stage_bytes()
 {
-    return 2 * (size_t)NB * (16 * NW) * kMmaLd * 2;
+    return 2 * (size_t)NB * attn_mma_stage_rows<NW, NB>() * kMmaLd * 2;
 }
 template <int NW>
 __host__ __device__ constexpr size_t attn_mma_merge_bytes()
@@ -558,13 +566,15 @@ attn_mma_kernel(const float *__restrict__ q, int H_q, int H_kv, float scale_log2
                 float *__restrict__ lse, int early_q)
 {
     constexpr int G = 8, D = 128, TC = 16 * NW, LD = kMmaLd, NT = 32 * NW;
+    constexpr int TX = attn_mma_stage_rows<NW, NB>();  // rows of a stage buffer
     static_assert(NT == 2 * TC, "one thread per cell of the first two stages");
+    static_assert(TX <= 2 * TC, "the preloaded rows cover a whole stage buffer");
     static_assert(NB == 1 || NB == 2, "one or two stage buffers");
     constexpr size_t kStage = attn_mma_stage_bytes<NW, NB>();
     constexpr size_t kMerge = attn_mma_merge_bytes<NW>();
     extern __shared__ __align__(16) char smem_raw[];
-    __nv_bfloat16 *Ks = reinterpret_cast<__nv_bfloat16 *>(smem_raw);  // [NB][TC][LD]
-    __nv_bfloat16 *Vs = Ks + NB * TC * LD;                               // [NB][TC][LD]
+    __nv_bfloat16 *Ks = reinterpret_cast<__nv_bfloat16 *>(smem_raw);  // [NB][TX][LD]
+    __nv_bfloat16 *Vs = Ks + NB * TX * LD;                               // [NB][TX][LD]
     char *tail = smem_raw + (NB == 1 ? (kStage > kMerge ? kStage : kMerge) : kStage + kMerge);
     int32_t *rows = reinterpret_cast<int32_t *>(tail);                   // [2][TC]
     // [NW][G][D+2] per-warp states: after the stages (two buffers) or over them (one)
@@ -642,7 +652,9 @@ attn_mma_kernel(const float *__restrict__ q, int H_q, int H_kv, float scale_log2
     const bool overflow = n > max_cells;  // truncated list: the result must not be used
     if (overflow || n < 0) n = 0;
     const int64_t c1 = c1max < n ? c1max : n;
-    const int ntiles = c1 > c0 ? (int)((c1 - c0 + TC - 1) / TC) : 0;
+    // cells per stage: a split that fits the one-buffer form's wider buffer is one stage
+    const int SC = (NB == 1 && c1max - c0 <= TX) ? TX : TC;
+    const int ntiles = c1 > c0 ? (int)((c1 - c0 + SC - 1) / SC) : 0;
     {
         int64_t row = c0 + tid < c1 ? first_row : -1;
         if (row < 0 || row >= n_kv) row = -1;
@@ -652,8 +664,8 @@ attn_mma_kernel(const float *__restrict__ q, int H_q, int H_kv, float scale_log2
 
     // rows of stage `it` into row buffer `buf` (stages from the third on)
     auto load_rows = [&](int it, int buf) {
-        const int64_t base = c0 + (int64_t)it * TC;
-        const int tc = (int)min((int64_t)TC, c1 - base);
+        const int64_t base = c0 + (int64_t)it * SC;
+        const int tc = (int)min((int64_t)SC, c1 - base);
         int32_t *rb = rows + buf * TC;
         for (int slot = tid; slot < TC; slot += NT) {
             int64_t row = -1;
@@ -672,22 +684,26 @@ attn_mma_kernel(const float *__restrict__ q, int H_q, int H_kv, float scale_log2
     // inside the MMA, so it is zero-filled: stale shared memory could hold a NaN pattern.
     auto copy_rows = [&](int buf) {
         const int32_t *rb = rows + buf * TC;
-        __nv_bfloat16 *ks = Ks + buf * TC * LD;
-        __nv_bfloat16 *vs = Vs + buf * TC * LD;
-        for (int e = tid; e < TC * (D / 8); e += NT) {
+        __nv_bfloat16 *ks = Ks + buf * TX * LD;
+        __nv_bfloat16 *vs = Vs + buf * TX * LD;
+        for (int e = tid; e < SC * (D / 8); e += NT) {
             const int slot = e / (D / 8), c = e - slot * (D / 8);
             if (rb[slot] < 0) *reinterpret_cast<uint4 *>(vs + slot * LD + c * 8) = make_uint4(0u, 0u, 0u, 0u);
         }
-        const int nv = __syncthreads_count(tid < TC && rb[tid] >= 0);
+        const int nv = __syncthreads_count(tid < SC && rb[tid] >= 0);
         if (tid == 0) mbar_arrive_expect_tx(&sbar[buf], (uint32_t)nv * 2u * D * 2u);
-        const int slot = tid >> 1;  // NT = 2 * TC: one thread per row and tensor
-        const int64_t row = rb[slot];
-        if (row >= 0) {
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            if (tid & 1)
-                bulk_g2s(vs + slot * LD, V + row * ld_v + (int64_t)g * D, D * 2, &sbar[buf]);
-            else
-                bulk_g2s(ks + slot * LD, K + row * ld_k + (int64_t)g * D, D * 2, &sbar[buf]);
+        // one thread per row and tensor (NT = 2 * TC); the rows past TC of a wider stage
+        // go to the first threads once more
+        for (int t = tid; t < 2 * SC; t += NT) {
+            const int slot = t >> 1;
+            const int64_t row = rb[slot];
+            if (row >= 0) {
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                if (t & 1)
+                    bulk_g2s(vs + slot * LD, V + row * ld_v + (int64_t)g * D, D * 2, &sbar[buf]);
+                else
+                    bulk_g2s(ks + slot * LD, K + row * ld_k + (int64_t)g * D, D * 2, &sbar[buf]);
+            }
         }
     };
     // Wait for buffer `buf`'s stage (bounded), then make its zero-filled rows visible.
@@ -714,11 +730,12 @@ attn_mma_kernel(const float *__restrict__ q, int H_q, int H_kv, float scale_log2
             copy_rows(0);
         }
         wait_rows(buf);
-        const int tc = (int)min((int64_t)TC, c1 - (c0 + (int64_t)it * TC));
-        const __nv_bfloat16 *ks = Ks + buf * TC * LD;
-        const __nv_bfloat16 *vs = Vs + buf * TC * LD;
+        const int tc = (int)min((int64_t)SC, c1 - (c0 + (int64_t)it * SC));
+        const __nv_bfloat16 *ks = Ks + buf * TX * LD;
+        const __nv_bfloat16 *vs = Vs + buf * TX * LD;
         const int32_t *rw = rows + buf * TC;
-        const int s0 = warp * 16;  // this warp's 16 cells of the stage
+        // cells s0 .. s0+15 of the stage into this warp's online-softmax state
+        auto group = [&](const int s0) {
         if (s0 < tc) {
             // S = Q K^T for cells s0..s0+15 as two n-tiles of 8 cells
             float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
@@ -785,6 +802,9 @@ attn_mma_kernel(const float *__restrict__ q, int H_q, int H_kv, float scale_log2
                 }
             }
         }
+        };
+        group(warp * 16);
+        if (NB == 1 && warp == NW - 1) group(TC);  // the extra rows of a wider stage
         __syncthreads();  // this stage is refilled by the next issue()
     }
 
