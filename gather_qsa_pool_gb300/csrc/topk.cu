@@ -533,6 +533,8 @@ __device__ __forceinline__ P *byte_shift(P *p, int64_t bytes)
 // blocks (2^kTopkHistBits words per query); ticket: set to 0 by the score kernel of this
 // step.  Scratch per query (query i's at byte offset i * q_stride): bitmap [ceil(n/32)]
 // words, cand [grid.x][1024] (key, block), cand_cnt [grid.x].
+// BPT blocks per thread: CTA c classifies blocks [c * 1024 * BPT, (c + 1) * 1024 * BPT).
+template <int BPT>
 __global__ void __launch_bounds__(NT)
 topk_select_kernel(const float *__restrict__ scores, int64_t ld_scores, int n_q, int64_t n_full,
                    int k_blk, int64_t n_ctx, uint32_t *__restrict__ hist,
@@ -573,8 +575,11 @@ topk_select_kernel(const float *__restrict__ scores, int64_t ld_scores, int n_q,
 
     const int64_t k = k_blk;
     const int64_t nw = (n + 31) / 32;
-    const int64_t i = (int64_t)blockIdx.x * NT + tid;  // this thread's block
-    const float sv = i < n ? scores[i] : 0.0f;
+    constexpr int kSpan = NT * BPT;  // blocks of one CTA
+    const int64_t i0 = (int64_t)blockIdx.x * kSpan + tid;  // this thread's blocks: i0 + j*NT
+    float sv[BPT];
+#pragma unroll
+    for (int j = 0; j < BPT; ++j) sv[j] = i0 + j * NT < n ? scores[i0 + j * NT] : 0.0f;
     // ---- threshold bucket, two-level: thread t holds bins 4095-4t .. 4092-4t (top first)
     uint32_t c[4], mine = 0;
 #pragma unroll
@@ -630,22 +635,26 @@ topk_select_kernel(const float *__restrict__ scores, int64_t ld_scores, int n_q,
     const uint32_t k_rem = (uint32_t)k - above_n;
     const bool whole = valid && sh[5] == k_rem;
 
-    // ---- classify this CTA's 1024 blocks
-    const uint32_t key = score_key(sv);
-    const uint32_t dg = key >> (32 - kTopkHistBits);
-    const bool in = valid && i < n;
-    const bool above = in && (dg > B1 || (whole && dg == B1));
-    const bool is_cand = in && !whole && dg == B1;
-    const uint32_t word = __ballot_sync(0xffffffffu, above);
-    const int64_t wi = (int64_t)blockIdx.x * (NT / 32) + warp;
-    if (lane == 0 && wi < nw) bitmap[wi] = word;
-    const uint32_t cm = __ballot_sync(0xffffffffu, is_cand);
-    uint32_t base = 0;
-    if (lane == 0 && cm) base = atomicAdd(&sh[6], (uint32_t)__popc(cm));
-    base = __shfl_sync(0xffffffffu, base, 0);
-    if (is_cand)
-        cand[(int64_t)blockIdx.x * NT + base + __popc(cm & ((1u << lane) - 1u))] =
-            make_uint2(key, (uint32_t)i);
+    // ---- classify this CTA's blocks
+#pragma unroll
+    for (int j = 0; j < BPT; ++j) {
+        const int64_t i = i0 + j * NT;
+        const uint32_t key = score_key(sv[j]);
+        const uint32_t dg = key >> (32 - kTopkHistBits);
+        const bool in = valid && i < n;
+        const bool above = in && (dg > B1 || (whole && dg == B1));
+        const bool is_cand = in && !whole && dg == B1;
+        const uint32_t word = __ballot_sync(0xffffffffu, above);
+        const int64_t wi = (int64_t)blockIdx.x * (kSpan / 32) + j * (NT / 32) + warp;
+        if (lane == 0 && wi < nw) bitmap[wi] = word;
+        const uint32_t cm = __ballot_sync(0xffffffffu, is_cand);
+        uint32_t base = 0;
+        if (lane == 0 && cm) base = atomicAdd(&sh[6], (uint32_t)__popc(cm));
+        base = __shfl_sync(0xffffffffu, base, 0);
+        if (is_cand)
+            cand[(int64_t)blockIdx.x * kSpan + base + __popc(cm & ((1u << lane) - 1u))] =
+                make_uint2(key, (uint32_t)i);
+    }
     // Arrival: the barrier orders this CTA's writes before thread 0's ticket, an
     // acquire-release atomic at device scope: it publishes them, and the last arrival
     // acquires everything the others published (the grid-barrier pattern, without the wait).
@@ -685,7 +694,7 @@ topk_select_kernel(const float *__restrict__ scores, int64_t ld_scores, int n_q,
 #pragma unroll
         for (int r = 0; r < kSpec; ++r) {
             const int cta = warp + 32 * r;
-            spec[r] = cta < G ? __ldcg(cand + (int64_t)cta * NT + lane) : make_uint2(0u, 0u);
+            spec[r] = cta < G ? __ldcg(cand + (int64_t)cta * kSpan + lane) : make_uint2(0u, 0u);
         }
         for (int64_t w = tid; w < nw; w += NT) selw[w] = __ldcg(bitmap + w);
         const uint32_t off = block_excl_scan(my, warp_s, &n_cand);
@@ -704,7 +713,7 @@ topk_select_kernel(const float *__restrict__ scores, int64_t ld_scores, int n_q,
             for (int cta = warp; cta < G; cta += NT / 32) {
                 const uint32_t j0 = cta < 32 * kSpec ? 32u : 0u;  // entries already placed
                 for (uint32_t j = j0 + lane; j < lc[cta]; j += 32) {
-                    const uint2 e = __ldcg(cand + (int64_t)cta * NT + j);
+                    const uint2 e = __ldcg(cand + (int64_t)cta * kSpan + j);
                     cp[lo[cta] + j] = ((unsigned long long)e.x << 32) | (uint32_t)~e.y;
                 }
             }
@@ -776,7 +785,8 @@ size_t topk_smem_bytes(int64_t n, int *cand_cap)
 cudaError_t set_max_smem()
 {
     cudaError_t e = ensure_kernel_attrs<topk_kernel>(kMaxSmemBytes);
-    if (e == cudaSuccess) e = ensure_kernel_attrs<topk_select_kernel>(kMaxSmemBytes);
+    if (e == cudaSuccess) e = ensure_kernel_attrs<topk_select_kernel<1>>(kMaxSmemBytes);
+    if (e == cudaSuccess) e = ensure_kernel_attrs<topk_select_kernel<2>>(kMaxSmemBytes);
     return e;
 }
 
@@ -784,10 +794,13 @@ cudaError_t set_max_smem()
 
 int64_t topk_max_candidates() { return kMaxN; }
 
+// CTA slots of the decode top-k's scratch: enough for one or two blocks per thread.
+static int64_t select_slots(int64_t n) { return 2 * ((n + 2 * NT - 1) / (2 * NT)); }
+
 size_t topk_select_workspace_bytes(int64_t n_full_cap)
 {
     const int64_t nw = (n_full_cap + 31) / 32;
-    const int64_t g = (n_full_cap + NT - 1) / NT;
+    const int64_t g = select_slots(n_full_cap);
     // ticket (256 B) | counts | candidates | bitmap, each 256-byte aligned
     auto al = [](int64_t b) { return (b + 255) & ~(int64_t)255; };
     return (size_t)(256 + al(4 * g) + al(8 * g * NT) + al(4 * nw));
@@ -805,7 +818,7 @@ cudaError_t launch_topk_select(const float *scores, int64_t ld_scores, int n_q, 
     if (n_q < 1 || n_q > 65535 || n_min <= k_blk || n_full > kMaxN || n_full > n_full_cap)
         return cudaErrorNotSupported;
     const int64_t nw = (n_full + 31) / 32;
-    const int64_t g = (n_full + NT - 1) / NT;
+    const int64_t g = select_slots(n_full);
     auto al = [](int64_t b) { return (b + 255) & ~(int64_t)255; };
     char *b = static_cast<char *>(scratch);
     uint32_t *ticket = reinterpret_cast<uint32_t *>(b);
@@ -820,7 +833,17 @@ cudaError_t launch_topk_select(const float *scores, int64_t ld_scores, int n_q, 
     cudaError_t e = set_max_smem();
     if (e != cudaSuccess) return e;
     const int64_t q_stride = (int64_t)topk_select_workspace_bytes(n_full_cap);
-    return launch(topk_select_kernel, dim3((unsigned)g, (unsigned)n_q), dim3(NT), smem, st, 1,
+    // One CTA per SM (registers): when the queries' CTAs would need a second wave, each
+    // CTA takes two blocks per thread.
+    const int64_t g1 = (n_full + NT - 1) / NT;
+    if (n_q * g1 > device_sm_count()) {
+        const int64_t g2 = (n_full + 2 * NT - 1) / (2 * NT);
+        return launch(topk_select_kernel<2>, dim3((unsigned)g2, (unsigned)n_q), dim3(NT), smem,
+                      st, 1, scores, ld_scores, n_q, n_full, (int)k_blk, n_ctx, hist, ticket,
+                      bitmap, cand, cand_cnt, q_stride, blocks_out, counts_out, pos_out,
+                      n_cells_out, max_cells, cand_cap);
+    }
+    return launch(topk_select_kernel<1>, dim3((unsigned)g1, (unsigned)n_q), dim3(NT), smem, st, 1,
                   scores, ld_scores, n_q, n_full, (int)k_blk, n_ctx, hist, ticket, bitmap, cand,
                   cand_cnt, q_stride, blocks_out, counts_out, pos_out, n_cells_out, max_cells,
                   cand_cap);
