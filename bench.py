@@ -346,9 +346,10 @@ def run_context(name, args, world, rank, local, want_clocks, pooled="f32", n_q=1
     score_us = ev2.elapsed_time(ev3) * 1e3 / k_kernel
     score_rows = sum(n_rows[i % L] for i in range(k_kernel)) / k_kernel
 
-    # end to end through the C call with host buffers (qsa_decode_step_host): per step one
-    # copy of the new token's raw-key, K and V rows and both queries from pinned host memory,
-    # the step, one copy of the output back, and a wait for it
+    # end to end through the C call with host buffers (qsa_decode_plan_step_host): per step
+    # the new token's raw-key, K and V rows and both queries cross from page-locked host
+    # memory (a copy kernel reads them in place), the step, the output crosses back (a copy
+    # kernel writes it into page-locked host memory), and a wait for it
     h2d = d2h = 0
     if not light:
         g = torch.Generator()

@@ -54,6 +54,12 @@ _SIGNATURES = {
     "qsa_decode_step_host_layout": (_sz, [_i64, _int, _int, _int, _int, _int, _int, _int, _p]),
     "qsa_decode_step_host_workspace_size": (_sz, [_i64, _int, _int, _int, _i64, _i64, _int, _int,
                                                   _int, _int]),
+    "qsa_decode_plan_create": (_int, [ctypes.POINTER(_p), _p, _int, _int, _int, _p, _f, _d, _p,
+                                      _int, _i64, _i64, _f, _p, _i64, _p, _p, _p, _p, _int, _i64,
+                                      _int, _int, _i64, _p, _p, _i64, _int, _f, _p, _p, _p, _sz]),
+    "qsa_decode_plan_destroy": (None, [_p]),
+    "qsa_decode_plan_step": (_int, [_p, _i64, _i64, _i64, _p, _p, _p]),
+    "qsa_decode_plan_step_host": (_int, [_p, _i64, _i64, _i64, _p, _p, _p, _p]),
     "qsa_mask_to_list": (_int, [_p, _i64, _i64, _i64, _i64, _p, _p, _p, _p]),
     "qsa_mask_sparse_eligible": (_int, [_int, _f, _f, _i64, _i64]),
 }
@@ -247,6 +253,38 @@ def decode_step_host_workspace_size(n_q, H_q, H_kv, d, max_cells, cap_rows, raw_
                                     d_idx, kv_dtype) -> int:
     return int(load().qsa_decode_step_host_workspace_size(n_q, H_q, H_kv, d, max_cells, cap_rows,
                                                           raw_dtype, H_idx, d_idx, kv_dtype))
+
+
+class DecodePlan:
+    """A qsa_decode_plan: the fixed arguments of a sequence's decode steps bound once (the
+    tensors are kept alive with the plan, which is destroyed with this object)."""
+
+    def __init__(self, raw_k, norm_w, eps, rope_base, pooled, max_queries, scale_idx, scores,
+                 k_blk, blocks, counts, K, V, H_idx, d_idx, H_kv, d, pos, n_cells, max_cells, H_q,
+                 scale, out, lse, workspace):
+        lib = load()
+        handle = _p()
+        ws_bytes = workspace.numel() * workspace.element_size()
+        _check("qsa_decode_plan_create", lib.qsa_decode_plan_create(
+            ctypes.byref(handle), _ptr(raw_k), _dtype(raw_k), H_idx, d_idx, _ptr(norm_w), eps,
+            rope_base, _ptr(pooled), _dtype(pooled), pooled.shape[0], max_queries, scale_idx,
+            _ptr(scores), k_blk, _ptr(blocks), _ptr(counts), _ptr(K), _ptr(V), _dtype(K),
+            K.shape[0], H_kv, d, _ld(K), _ptr(pos), _ptr(n_cells), max_cells, H_q, scale,
+            _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes))
+        self._lib = lib
+        self.handle = handle.value
+        self._keep = (raw_k, norm_w, pooled, scores, blocks, counts, K, V, pos, n_cells, out, lse,
+                      workspace)
+        self.step = lib.qsa_decode_plan_step            # (handle, n_ctx, n_valid_full, n_q,
+        self.step_host = lib.qsa_decode_plan_step_host  #  ...) -> status, see qsa.h
+
+    def close(self):
+        if self.handle:
+            self._lib.qsa_decode_plan_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        self.close()
 
 
 def mask_to_list(mask, max_list, pos_out, counts_out, bits_out=None, n_kv=None, stream=None):

@@ -1,7 +1,9 @@
 // capi.cu -- the extern "C" entry points: argument validation on the host, then one
-// launcher call per operation.  No entry point allocates, synchronises or keeps state
-// beyond cached kernel attributes.
+// launcher call per operation.  No entry point allocates device memory, synchronises or
+// keeps state beyond cached kernel attributes; decode plans are host objects the caller
+// creates and destroys.
 #include <math.h>
+#include <stdlib.h>
 
 #include <mutex>
 
@@ -55,7 +57,7 @@ const char *qsa_status_str(qsa_status s)
     return "QSA_ERR_UNKNOWN";
 }
 
-int qsa_version(void) { return (2 << 16) | 0; }
+int qsa_version(void) { return (2 << 16) | 1; }
 
 static qsa_status check_pool_update(const void *raw_k, qsa_dtype raw_dtype, int64_t n_ctx, int H,
                                     int d, const float *norm_w, float eps, double rope_base,
@@ -279,8 +281,11 @@ size_t qsa_decode_step_workspace_size(int64_t n_q, int H_q, int H_kv, int d, int
            (size_t)n_q * (kTopkHistBytes + topk_select_workspace_bytes(cap_rows));
 }
 
-// A decode step fed from host memory: the packed inputs go to `staging` in one copy, the new
-// tokens' rows are scattered into the caches, and the outputs come back to h_out / h_lse.
+// A decode step fed from host memory: the new tokens' rows go into the caches and the
+// queries into `staging`, and the outputs come back to h_out / h_lse.  A host buffer that
+// is mapped into the device's address space is read / written in place by the copy kernel;
+// any other goes through a copy-engine transfer (inputs: one copy into `staging`, which the
+// copy kernel then scatters).
 struct HostFeed {
     const void *h_in;
     size_t in_bytes;
@@ -331,20 +336,26 @@ static qsa_status decode_step_impl(const void *raw_k, qsa_dtype raw_dtype, int64
     const cudaStream_t st = (cudaStream_t)stream;
     cudaError_t e = cudaSuccess;
     if (feed) {
-        // 0. this step's inputs from host memory (one copy), the new rows into the caches
-        e = cudaMemcpyAsync(feed->staging, feed->h_in, feed->in_bytes, cudaMemcpyHostToDevice, st);
-        if (e == cudaSuccess) {
-            const int64_t re = raw_dtype == QSA_BF16 ? 2 : 4, ke = kv_dtype == QSA_BF16 ? 2 : 4;
-            const int64_t hd = (int64_t)H_idx * d_idx, p0 = n_ctx - n_q;
-            const void *src[3] = {feed->staging + feed->off[0], feed->staging + feed->off[1],
-                                  feed->staging + feed->off[2]};
-            void *dst[3] = {(char *)raw_k + p0 * hd * re, (char *)K + p0 * ld_kv * ke,
-                            (char *)V + p0 * ld_kv * ke};
-            const int64_t rb[3] = {hd * re, (int64_t)H_kv * d * ke, (int64_t)H_kv * d * ke};
-            const int64_t ld[3] = {hd * re, ld_kv * ke, ld_kv * ke};
-            const int rows[3] = {(int)n_q, (int)n_q, (int)n_q};
-            e = launch_scatter_rows(src, dst, rb, ld, rows, st);
+        // 0. this step's inputs from host memory: the new rows into the caches, the queries
+        // into the staging area
+        const int64_t re = raw_dtype == QSA_BF16 ? 2 : 4, ke = kv_dtype == QSA_BF16 ? 2 : 4;
+        const int64_t hd = (int64_t)H_idx * d_idx, p0 = n_ctx - n_q;
+        const char *in = static_cast<const char *>(mapped_host_view(feed->h_in));
+        if (!in || !aligned(in, 4)) {
+            e = cudaMemcpyAsync(feed->staging, feed->h_in, feed->in_bytes,
+                                cudaMemcpyHostToDevice, st);
+            if (e != cudaSuccess) return QSA_ERR_CUDA;
+            in = feed->staging;
         }
+        RowCopy job[4];
+        job[0] = {in + feed->off[0], (char *)raw_k + p0 * hd * re, hd * re, hd * re, n_q};
+        job[1] = {in + feed->off[1], (char *)K + p0 * ld_kv * ke, (int64_t)H_kv * d * ke,
+                  ld_kv * ke, n_q};
+        job[2] = {in + feed->off[2], (char *)V + p0 * ld_kv * ke, (int64_t)H_kv * d * ke,
+                  ld_kv * ke, n_q};
+        const int64_t qb = (int64_t)feed->in_bytes - feed->off[3];
+        job[3] = {in + feed->off[3], feed->staging + feed->off[3], qb, qb, 1};
+        e = launch_copy_rows(job, in == feed->staging ? 3 : 4, st);
         if (e != cudaSuccess) return QSA_ERR_CUDA;
     }
     // Query i sits at position p_i = n_ctx - n_q + i; its candidates are the blocks complete
@@ -396,11 +407,21 @@ static qsa_status decode_step_impl(const void *raw_k, qsa_dtype raw_dtype, int64
                                true);
     // 5. the outputs back to host memory
     if (feed && e == cudaSuccess) {
-        e = cudaMemcpyAsync(feed->h_out, out, sizeof(float) * (size_t)n_q * H_q * d,
-                            cudaMemcpyDeviceToHost, st);
-        if (e == cudaSuccess && feed->h_lse)
-            e = cudaMemcpyAsync(feed->h_lse, lse_out, sizeof(float) * (size_t)n_q * H_q,
-                                cudaMemcpyDeviceToHost, st);
+        const int64_t ob = (int64_t)sizeof(float) * n_q * H_q * d;
+        const int64_t lb = (int64_t)sizeof(float) * n_q * H_q;
+        void *ho = mapped_host_view(feed->h_out);
+        void *hl = feed->h_lse ? mapped_host_view(feed->h_lse) : nullptr;
+        if (ho && aligned(ho, 4) && aligned(out, 4) &&
+            (!feed->h_lse || (hl && aligned(hl, 4) && aligned(lse_out, 4)))) {
+            RowCopy job[2];
+            job[0] = {out, ho, ob, ob, 1};
+            job[1] = {lse_out, hl, lb, lb, 1};
+            e = launch_copy_rows(job, hl ? 2 : 1, st);
+        } else {
+            e = cudaMemcpyAsync(feed->h_out, out, (size_t)ob, cudaMemcpyDeviceToHost, st);
+            if (e == cudaSuccess && feed->h_lse)
+                e = cudaMemcpyAsync(feed->h_lse, lse_out, (size_t)lb, cudaMemcpyDeviceToHost, st);
+        }
     }
     return from_cuda(e);
 }
@@ -493,6 +514,97 @@ qsa_status qsa_decode_step_host(const void *h_in, float *h_out, float *h_lse, vo
                             k_blk, blocks, counts, K, V, kv_dtype, n_kv, H_kv, d, ld_kv, pos,
                             n_cells, max_cells, q, H_q, scale, out, lse_out, workspace, ws, stream,
                             &feed);
+}
+
+struct qsa_decode_plan {
+    void *raw_k;
+    qsa_dtype raw_dtype;
+    int H_idx, d_idx;
+    const float *norm_w;
+    float eps;
+    double rope_base;
+    void *pooled;
+    qsa_dtype pooled_dtype;
+    int64_t cap_rows, max_queries;
+    float scale_idx;
+    float *scores;
+    int64_t k_blk;
+    int32_t *blocks, *counts;
+    void *K, *V;
+    qsa_dtype kv_dtype;
+    int64_t n_kv;
+    int H_kv, d;
+    int64_t ld_kv;
+    int32_t *pos, *n_cells;
+    int64_t max_cells;
+    int H_q;
+    float scale;
+    float *out, *lse_out;
+    void *workspace;
+    size_t workspace_bytes;
+    bool host;  // the workspace also holds the host-fed step's staging area
+};
+
+qsa_status qsa_decode_plan_create(qsa_decode_plan **plan, void *raw_k, qsa_dtype raw_dtype,
+                                  int H_idx, int d_idx, const float *norm_w, float eps,
+                                  double rope_base, void *pooled, qsa_dtype pooled_dtype,
+                                  int64_t cap_rows, int64_t max_queries, float scale_idx,
+                                  float *scores, int64_t k_blk, int32_t *blocks, int32_t *counts,
+                                  void *K, void *V, qsa_dtype kv_dtype, int64_t n_kv, int H_kv,
+                                  int d, int64_t ld_kv, int32_t *pos, int32_t *n_cells,
+                                  int64_t max_cells, int H_q, float scale, float *out,
+                                  float *lse_out, void *workspace, size_t workspace_bytes)
+{
+    if (!plan) return QSA_ERR_INVALID_ARG;
+    *plan = nullptr;
+    if (!raw_k || !norm_w || !pooled || !scores || !blocks || !counts || !K || !V || !pos ||
+        !n_cells || !out || !workspace || !valid_dtype(raw_dtype) ||
+        !valid_dtype(pooled_dtype) || !valid_dtype(kv_dtype) || max_queries < 1 ||
+        max_queries > kMaxStreamQueries || !aligned(workspace, 256))
+        return QSA_ERR_INVALID_ARG;
+    const size_t need = qsa_decode_step_workspace_size(max_queries, H_q, H_kv, d, max_cells,
+                                                       cap_rows);
+    if (need == 0 || workspace_bytes < need) return QSA_ERR_INVALID_ARG;
+    const size_t need_host = qsa_decode_step_host_workspace_size(
+        max_queries, H_q, H_kv, d, max_cells, cap_rows, raw_dtype, H_idx, d_idx, kv_dtype);
+    qsa_decode_plan *p = static_cast<qsa_decode_plan *>(malloc(sizeof(qsa_decode_plan)));
+    if (!p) return QSA_ERR_INVALID_ARG;
+    *p = qsa_decode_plan{raw_k, raw_dtype, H_idx, d_idx, norm_w, eps, rope_base, pooled,
+                         pooled_dtype, cap_rows, max_queries, scale_idx, scores, k_blk, blocks,
+                         counts, K, V, kv_dtype, n_kv, H_kv, d, ld_kv, pos, n_cells, max_cells,
+                         H_q, scale, out, lse_out, workspace, workspace_bytes,
+                         need_host != 0 && workspace_bytes >= need_host};
+    *plan = p;
+    return QSA_OK;
+}
+
+void qsa_decode_plan_destroy(qsa_decode_plan *plan) { free(plan); }
+
+qsa_status qsa_decode_plan_step(const qsa_decode_plan *p, int64_t n_ctx, int64_t n_valid_full,
+                                int64_t n_q, const float *q_idx, const float *q,
+                                qsa_stream_t stream)
+{
+    if (!p || n_q > p->max_queries) return QSA_ERR_INVALID_ARG;
+    return qsa_decode_step(p->raw_k, p->raw_dtype, n_ctx, p->H_idx, p->d_idx, p->norm_w, p->eps,
+                           p->rope_base, p->pooled, p->pooled_dtype, p->cap_rows, n_valid_full,
+                           n_q, q_idx, p->scale_idx, p->scores, p->k_blk, p->blocks, p->counts,
+                           p->K, p->V, p->kv_dtype, p->n_kv, p->H_kv, p->d, p->ld_kv, p->pos,
+                           p->n_cells, p->max_cells, q, p->H_q, p->scale, p->out, p->lse_out,
+                           p->workspace, p->workspace_bytes, stream);
+}
+
+qsa_status qsa_decode_plan_step_host(const qsa_decode_plan *p, int64_t n_ctx,
+                                     int64_t n_valid_full, int64_t n_q, const void *h_in,
+                                     float *h_out, float *h_lse, qsa_stream_t stream)
+{
+    if (!p || !p->host || n_q > p->max_queries) return QSA_ERR_INVALID_ARG;
+    return qsa_decode_step_host(h_in, h_out, h_lse, p->raw_k, p->raw_dtype, n_ctx, p->H_idx,
+                                p->d_idx, p->norm_w, p->eps, p->rope_base, p->pooled,
+                                p->pooled_dtype, p->cap_rows, n_valid_full, n_q, p->scale_idx,
+                                p->scores, p->k_blk, p->blocks, p->counts, p->K, p->V,
+                                p->kv_dtype, p->n_kv, p->H_kv, p->d, p->ld_kv, p->pos, p->n_cells,
+                                p->max_cells, p->H_q, p->scale, p->out, p->lse_out, p->workspace,
+                                p->workspace_bytes, stream);
 }
 
 qsa_status qsa_mask_to_list(const uint8_t *mask, int64_t n_rows, int64_t n_kv, int64_t ld_mask,

@@ -384,12 +384,22 @@ cudaError_t launch_topk_select(const float *scores, int64_t ld_scores, int n_q, 
 size_t topk_select_workspace_bytes(int64_t n_full_cap);
 uint32_t *topk_select_ticket(void *scratch);
 
-// Three row blocks copied from contiguous sources to strided destinations (the new tokens'
-// raw indexer-key, K and V rows of a host-fed decode step).  Every address, row size and
-// stride must be a multiple of 4 bytes.
-cudaError_t launch_scatter_rows(const void *const src[3], void *const dst[3],
-                                const int64_t row_bytes[3], const int64_t dst_ld[3],
-                                const int rows[3], cudaStream_t st);
+// Row blocks copied from contiguous sources to strided destinations, one per grid row (the
+// host transfers of a host-fed decode step).  Every address, row size and stride must be a
+// multiple of 4 bytes; src / dst may be device views of mapped host memory.
+constexpr int kMaxCopyJobs = 4;
+struct RowCopy {
+    const void *src;
+    void *dst;
+    int64_t row_bytes;  // bytes per row, rows contiguous in the source
+    int64_t dst_ld;     // bytes between rows in the destination
+    int64_t rows;
+};
+cudaError_t launch_copy_rows(const RowCopy *jobs, int n_jobs, cudaStream_t st);
+
+// The address through which kernels on the current device reach host buffer h, or NULL
+// when h is not page-locked memory mapped for it (pageable memory, another device's).
+void *mapped_host_view(const void *h);
 
 // cells[i][c] = scores[i][c / 4] for c < 4 * n_full (the pre-block-domain selection input).
 cudaError_t launch_expand_scores(const float *scores, int64_t n_q, int64_t ld_s, int64_t n_full,

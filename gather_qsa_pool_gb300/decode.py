@@ -87,36 +87,33 @@ class DecodeLayer:
         return self.out[:n_q]
 
     def bind(self, raw_k, norm_w, K, V):
-        """Fix the caller-owned caches for ``step_ptr`` (pointers resolved once)."""
-        self._lib = qb.load()
-        self._fixed = (raw_k.data_ptr(), qb._dtype(raw_k), norm_w.data_ptr(),
-                       self.pooled.data_ptr(), qb._dtype(self.pooled), self.pooled.shape[0],
-                       self.scores.data_ptr(), self.blocks.data_ptr(), self.counts.data_ptr(),
-                       K.data_ptr(), V.data_ptr(), qb._dtype(K), K.shape[0], qb._ld(K),
-                       self.pos.data_ptr(), self.n_cells.data_ptr(), self.out.data_ptr(),
-                       self.lse.data_ptr(), None, None)
+        """Bind the caller-owned caches and this layer's buffers into a qsa_decode_plan for
+        ``step_ptr`` / ``step_host`` (per step only the context length, the validity
+        watermark, the query count and the query pointers cross the C boundary)."""
+        self._bound = (raw_k, norm_w, K, V)
+        self._plan = qb.DecodePlan(raw_k, norm_w, self.eps, self.rope_base, self.pooled,
+                                   self.max_queries, 1.0 / math.sqrt(self.d_idx), self.scores,
+                                   self.k_blk, self.blocks, self.counts, K, V, self.H_idx,
+                                   self.d_idx, self.H_kv, self.d, self.pos, self.n_cells,
+                                   self.max_cells, self.H_q, 1.0 / math.sqrt(self.d), self.out,
+                                   self.lse, self.workspace)
 
     def step_ptr(self, n_ctx, q_idx_ptr, q_ptr, stream_ptr, n_q=1):
-        """Decode step on caches fixed by ``bind``; q_idx / q given as device pointers."""
-        (raw, raw_dt, w, pooled, pdt, cap, scores, blocks, counts, K, V, kv_dt, n_kv, ld, pos,
-         n_cells, out, lse, _, _) = self._fixed
-        ws, ws_bytes = self.workspace.data_ptr(), self.workspace.numel() * 4
-        st = self._lib.qsa_decode_step(
-            raw, raw_dt, n_ctx, self.H_idx, self.d_idx, w, self.eps, self.rope_base, pooled, pdt,
-            cap, self.n_valid_full, n_q, q_idx_ptr, 1.0 / math.sqrt(self.d_idx), scores,
-            self.k_blk, blocks, counts, K, V, kv_dt, n_kv, self.H_kv, self.d, ld, pos, n_cells,
-            self.max_cells, q_ptr, self.H_q, 1.0 / math.sqrt(self.d), out, lse, ws, ws_bytes,
-            stream_ptr)
+        """Decode step on the caches fixed by ``bind``; q_idx / q given as device pointers."""
+        plan = self._plan
+        st = plan.step(plan.handle, n_ctx, self.n_valid_full, n_q, q_idx_ptr, q_ptr, stream_ptr)
         if st != 0:
-            raise qb.QSAError("qsa_decode_step", st)
+            raise qb.QSAError("qsa_decode_plan_step", st)
         self.n_valid_full = n_ctx // 4
 
     # ------------------------------------------------------------------ host-fed steps
 
-    def enable_host_feed(self, raw_dtype, kv_dtype):
+    def enable_host_feed(self, raw_dtype, kv_dtype, pinned=True):
         """Prepare steps fed from host memory (qsa_decode_step_host): a workspace with room
-        for the staging area and page-locked input / output buffers.  raw_dtype, kv_dtype:
-        torch dtypes of the raw indexer-key and K/V caches."""
+        for the staging area and the host input / output buffers.  raw_dtype, kv_dtype:
+        torch dtypes of the raw indexer-key and K/V caches.  pinned: page-locked buffers,
+        which the library's kernels read and write in place; pageable ones go through
+        copy-engine transfers instead."""
         import torch
 
         rd = qb.QSA_BF16 if raw_dtype == torch.bfloat16 else qb.QSA_F32
@@ -129,9 +126,15 @@ class DecodeLayer:
         self.workspace = torch.zeros(max(ws // 4, 1), dtype=torch.float32, device=dev)
         total, _ = qb.decode_step_host_layout(nq, rd, self.H_idx, self.d_idx, kd, self.H_kv,
                                               self.d, self.H_q)
-        self.h_in = torch.zeros(total, dtype=torch.uint8).pin_memory()
-        self.h_out = torch.zeros(nq, self.H_q, self.d, dtype=torch.float32).pin_memory()
-        self.h_lse = torch.zeros(nq, self.H_q, dtype=torch.float32).pin_memory()
+        self.h_in = torch.zeros(total, dtype=torch.uint8)
+        self.h_out = torch.zeros(nq, self.H_q, self.d, dtype=torch.float32)
+        self.h_lse = torch.zeros(nq, self.H_q, dtype=torch.float32)
+        if pinned:
+            self.h_in, self.h_out, self.h_lse = (self.h_in.pin_memory(), self.h_out.pin_memory(),
+                                                 self.h_lse.pin_memory())
+        self._host_ptrs = (self.h_in.data_ptr(), self.h_out.data_ptr(), self.h_lse.data_ptr())
+        if getattr(self, "_bound", None) is not None:
+            self.bind(*self._bound)  # the plan must see the larger workspace
 
     def host_inputs(self, n_q):
         """Views of the packed host input for a step of n_q queries: dict with 'raw' [n_q]
@@ -156,21 +159,15 @@ class DecodeLayer:
                 "q": view(off[4], torch.float32, (n_q, self.H_q, self.d)), "bytes": total}
 
     def step_host(self, n_ctx, stream_ptr, n_q=1, with_lse=False):
-        """Host-fed decode step on caches fixed by ``bind``: the new tokens' rows and the
-        queries come from ``h_in`` (see host_inputs), the output lands in ``h_out`` once the
-        stream has been synchronised."""
-        (raw, raw_dt, w, pooled, pdt, cap, scores, blocks, counts, K, V, kv_dt, n_kv, ld, pos,
-         n_cells, out, lse, _, _) = self._fixed
-        st = self._lib.qsa_decode_step_host(
-            self.h_in.data_ptr(), self.h_out.data_ptr(),
-            self.h_lse.data_ptr() if with_lse else None, raw, raw_dt, n_ctx, self.H_idx,
-            self.d_idx, w, self.eps, self.rope_base, pooled, pdt, cap, self.n_valid_full, n_q,
-            1.0 / math.sqrt(self.d_idx), scores, self.k_blk, blocks, counts, K, V, kv_dt, n_kv,
-            self.H_kv, self.d, ld, pos, n_cells, self.max_cells, self.H_q,
-            1.0 / math.sqrt(self.d), out, lse, self.workspace.data_ptr(),
-            self.workspace.numel() * 4, stream_ptr)
+        """Host-fed decode step on the caches fixed by ``bind``: the new tokens' rows and the
+        queries come from ``h_in`` (see host_inputs), the output lands in ``h_out`` (and the
+        log-sum-exp in ``h_lse`` when with_lse) once the stream has been synchronised."""
+        plan = self._plan
+        h_in, h_out, h_lse = self._host_ptrs
+        st = plan.step_host(plan.handle, n_ctx, self.n_valid_full, n_q, h_in, h_out,
+                            h_lse if with_lse else None, stream_ptr)
         if st != 0:
-            raise qb.QSAError("qsa_decode_step_host", st)
+            raise qb.QSAError("qsa_decode_plan_step_host", st)
         self.n_valid_full = n_ctx // 4
 
     def step_separate_calls(self, raw_k, norm_w, K, V, n_ctx, q_idx, q, stream=None):

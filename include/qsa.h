@@ -62,7 +62,7 @@ typedef enum {
 const char *qsa_status_str(qsa_status s);
 
 /* Library ABI version: (major << 16) | minor.  Major 2: pooled-cache dtype arguments,
- * several queries per decode step, the host-fed decode step. */
+ * several queries per decode step, the host-fed decode step; minor 1: decode plans. */
 int qsa_version(void);
 
 /*
@@ -316,15 +316,18 @@ size_t qsa_decode_step_workspace_size(int64_t n_q, int H_q, int H_kv, int d, int
  * Source: same passages as qsa_decode_step (the decode step appends the new tokens, then
  * scores, selects and attends); the host transfer is this library's service.
  *
- * On `stream`, in order: one host-to-device copy of h_in (qsa_decode_step_host_layout()
- * bytes) into a staging area at the end of the workspace; a kernel writing the new tokens'
- * rows into the caches -- raw indexer keys to raw_k rows n_ctx - n_q .. n_ctx - 1 (row
- * stride H_idx*d_idx), K and V rows to the same rows of K and V (row stride ld_kv); then
- * exactly qsa_decode_step with q_idx and q read from the staging area; then device-to-host
- * copies of out (n_q*H_q*d floats) into h_out and, if h_lse is not NULL, of lse_out
- * (n_q*H_q floats) into h_lse.  The call returns without waiting: synchronise the stream
- * before reading h_out or reusing h_in.  Host buffers should be page-locked (pinned) for
- * the copies to be asynchronous.
+ * On `stream`, in order: a copy kernel writing the new tokens' rows into the caches --
+ * raw indexer keys to raw_k rows n_ctx - n_q .. n_ctx - 1 (row stride H_idx*d_idx), K and
+ * V rows to the same rows of K and V (row stride ld_kv) -- and the queries into a staging
+ * area at the end of the workspace; then exactly qsa_decode_step with q_idx and q read from
+ * the staging area; then out (n_q*H_q*d floats) into h_out and, if h_lse is not NULL,
+ * lse_out (n_q*H_q floats) into h_lse.  When h_in is page-locked memory mapped into the
+ * current device's address space (cudaHostAlloc'd or registered memory on a unified-address
+ * system; torch's pin_memory() buffers are), the copy kernel reads it in place over the
+ * host link; otherwise one host-to-device copy of h_in (qsa_decode_step_host_layout()
+ * bytes) into the staging area comes first.  Likewise mapped h_out / h_lse are written by
+ * a kernel after the attention, other host buffers by device-to-host copies.  The call
+ * returns without waiting: synchronise the stream before reading h_out or reusing h_in.
  *
  *   h_in    packed inputs, sections at the byte offsets qsa_decode_step_host_layout()
  *           reports: [n_q][H_idx*d_idx] raw-key rows (raw_dtype), [n_q][H_kv*d] K rows and
@@ -346,6 +349,54 @@ qsa_status qsa_decode_step_host(const void *h_in, float *h_out, float *h_lse, vo
                                 int32_t *pos, int32_t *n_cells, int64_t max_cells, int H_q,
                                 float scale, float *out, float *lse_out, void *workspace,
                                 size_t workspace_bytes, qsa_stream_t stream);
+
+/*
+ * qsa_decode_plan -- a sequence's decode steps with the arguments that stay the same from
+ * step to step bound once.
+ *
+ * Source: same passages as qsa_decode_step; the plan is this library's service (it only
+ * saves the caller from passing some thirty unchanged arguments per step).
+ *
+ * qsa_decode_plan_create checks and copies the fixed arguments -- those of qsa_decode_step
+ * other than n_ctx, n_valid_full, n_q, q_idx and q -- into a host object (allocated with
+ * malloc; nothing on the device), for steps of up to max_queries query tokens (1..4).
+ * The buffers stay the caller's and must outlive the plan; the plan keeps no state between
+ * steps (the caller passes n_valid_full each step, as to qsa_decode_step).
+ *   workspace  at least qsa_decode_step_workspace_size(max_queries, ...) bytes, 256-byte
+ *              aligned; qsa_decode_plan_step_host also needs the staging area, i.e.
+ *              qsa_decode_step_host_workspace_size(max_queries, ...) bytes.
+ *   scores     room for [max_queries][cap_rows] floats.
+ * qsa_decode_plan_step(plan, n_ctx, n_valid_full, n_q, q_idx, q, stream) is
+ * qsa_decode_step with the plan's fixed arguments; qsa_decode_plan_step_host(plan, n_ctx,
+ * n_valid_full, n_q, h_in, h_out, h_lse, stream) is qsa_decode_step_host likewise (raw_k, K
+ * and V are the caches the new rows go into).  Results, validation and errors are those of
+ * the two calls, plus INVALID_ARG for a null plan, n_q above max_queries, and a host step
+ * on a plan whose workspace has no staging area.  qsa_decode_plan_create returns
+ * INVALID_ARG (and sets *plan to NULL) for a null plan pointer, null required buffers,
+ * unknown dtypes, max_queries outside [1, 4], or a workspace too small or misaligned; it
+ * launches nothing.  qsa_decode_plan_destroy(NULL) does nothing.
+ */
+typedef struct qsa_decode_plan qsa_decode_plan;
+
+qsa_status qsa_decode_plan_create(qsa_decode_plan **plan, void *raw_k, qsa_dtype raw_dtype,
+                                  int H_idx, int d_idx, const float *norm_w, float eps,
+                                  double rope_base, void *pooled, qsa_dtype pooled_dtype,
+                                  int64_t cap_rows, int64_t max_queries, float scale_idx,
+                                  float *scores, int64_t k_blk, int32_t *blocks, int32_t *counts,
+                                  void *K, void *V, qsa_dtype kv_dtype, int64_t n_kv, int H_kv,
+                                  int d, int64_t ld_kv, int32_t *pos, int32_t *n_cells,
+                                  int64_t max_cells, int H_q, float scale, float *out,
+                                  float *lse_out, void *workspace, size_t workspace_bytes);
+
+void qsa_decode_plan_destroy(qsa_decode_plan *plan);
+
+qsa_status qsa_decode_plan_step(const qsa_decode_plan *plan, int64_t n_ctx, int64_t n_valid_full,
+                                int64_t n_q, const float *q_idx, const float *q,
+                                qsa_stream_t stream);
+
+qsa_status qsa_decode_plan_step_host(const qsa_decode_plan *plan, int64_t n_ctx,
+                                     int64_t n_valid_full, int64_t n_q, const void *h_in,
+                                     float *h_out, float *h_lse, qsa_stream_t stream);
 
 /* Total bytes of qsa_decode_step_host's packed input (0 for an invalid shape); offsets
  * (nullable, [5]) receives the byte offsets of its sections: raw-key rows, K rows, V rows,

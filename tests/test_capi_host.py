@@ -32,6 +32,7 @@ def test_status_strings_and_version(lib):
     assert qsa.status_str(1) == "QSA_ERR_INVALID_ARG"
     assert qsa.status_str(4) == "QSA_ERR_TIMEOUT"
     assert lib.qsa_version() >> 16 == 2
+    assert lib.qsa_version() & 0xFFFF >= 1  # decode plans
 
 
 def test_pool_update_rejects(lib):
@@ -191,3 +192,49 @@ def test_decode_step_host_layout_and_validation(lib):
     assert step(h_lse=FAKE) == 1              # host lse without a device lse
     assert step(n_kv=999) == 1                # the new rows would land past the K/V cache
     assert step(ws_bytes=ws) == 1             # no room for the staging area
+
+
+def test_decode_plan_create_and_validation(lib):
+    import ctypes as C
+
+    ws = lib.qsa_decode_step_workspace_size(3, 32, 4, 128, 2051, 4000)
+    wsh = lib.qsa_decode_step_host_workspace_size(3, 32, 4, 128, 2051, 4000, 1, 16, 128, 1)
+    WS = P(0x100000)
+
+    def create(handle, max_queries=3, ws_bytes=wsh, raw_dtype=1, K=FAKE, workspace=WS):
+        # bf16 raw keys 16x128, fp32 pooled cache of 4000 rows, bf16 K/V 4x128, 32 query heads
+        return lib.qsa_decode_plan_create(handle, FAKE, raw_dtype, 16, 128, FAKE, 1e-6, 1e4,
+                                          FAKE, 0, 4000, max_queries, 0.1, FAKE, 512, FAKE, FAKE,
+                                          K, FAKE, 1, 16000, 4, 128, 512, FAKE, FAKE, 2051, 32,
+                                          0.1, FAKE, FAKE, workspace, ws_bytes)
+
+    h = P(0x1234)
+    assert create(None) == 1
+    for bad in (dict(max_queries=0), dict(max_queries=5), dict(ws_bytes=ws - 1),
+                dict(raw_dtype=9), dict(K=None), dict(workspace=P(0x100010))):
+        assert create(C.byref(h), **bad) == 1, bad
+        assert h.value is None  # *plan is cleared on failure
+    lib.qsa_decode_plan_destroy(None)
+    # host objects only: creating and destroying a plan touches no device
+    plan, plan_dev_only = P(), P()
+    assert create(C.byref(plan)) == 0 and plan.value
+    assert create(C.byref(plan_dev_only), ws_bytes=ws) == 0 and plan_dev_only.value
+    st = None
+    try:
+        # every step below fails validation before anything is enqueued
+        assert lib.qsa_decode_plan_step(None, 1000, 0, 1, FAKE, FAKE, st) == 1
+        assert lib.qsa_decode_plan_step(plan, 1000, 0, 4, FAKE, FAKE, st) == 1  # > max_queries
+        assert lib.qsa_decode_plan_step(plan, 1000, 0, 0, FAKE, FAKE, st) == 1
+        assert lib.qsa_decode_plan_step(plan, 16004, 0, 1, FAKE, FAKE, st) == 1  # 4001 rows
+        assert lib.qsa_decode_plan_step(plan, 1000, 0, 1, None, FAKE, st) == 1  # no q_idx
+        assert lib.qsa_decode_plan_step_host(None, 1000, 0, 1, FAKE, FAKE, None, st) == 1
+        assert lib.qsa_decode_plan_step_host(plan, 1000, 0, 4, FAKE, FAKE, None, st) == 1
+        assert lib.qsa_decode_plan_step_host(plan, 1000, 0, 1, None, FAKE, None, st) == 1
+        assert lib.qsa_decode_plan_step_host(plan, 1000, 0, 1, FAKE, None, None, st) == 1
+        assert lib.qsa_decode_plan_step_host(plan, 16004, 0, 1, FAKE, FAKE, None, st) == 1
+        # a plan whose workspace holds no staging area takes no host-fed steps
+        assert lib.qsa_decode_plan_step_host(plan_dev_only, 1000, 0, 1, FAKE, FAKE, None,
+                                             st) == 1
+    finally:
+        lib.qsa_decode_plan_destroy(plan)
+        lib.qsa_decode_plan_destroy(plan_dev_only)

@@ -224,12 +224,16 @@ def test_multi_query_small_context_takes_every_block():
         np.testing.assert_allclose(out[i], o_out, rtol=0, atol=ATOL_ATTN_F32)
 
 
-@pytest.mark.parametrize("shape,n_q,store", [(SMALL, 1, "f32"), (SMALL, 3, "bf16"),
-                                             (TINY, 2, "f32")], ids=["bf16-1", "bf16-3", "f32-2"])
-def test_host_fed_step_equals_device_step(shape, n_q, store):
+@pytest.mark.parametrize("shape,n_q,store,pinned", [
+    (SMALL, 1, "f32", True), (SMALL, 3, "bf16", True), (TINY, 2, "f32", True),
+    (SMALL, 2, "bf16", False), (TINY, 1, "f32", False)],
+    ids=["bf16-1", "bf16-3", "f32-2", "bf16-2-pageable", "f32-1-pageable"])
+def test_host_fed_step_equals_device_step(shape, n_q, store, pinned):
     """qsa_decode_step_host (new rows and queries from one packed host buffer, output back
     to host memory) writes the same cache rows and gives bit-identical results to
-    qsa_decode_step on caches that already hold the new rows."""
+    qsa_decode_step on caches that already hold the new rows: with page-locked host buffers
+    (read and written in place by the copy kernels) and with pageable ones (copy-engine
+    transfers)."""
     inp = qsa_synth.decode_inputs(shape, seed=47, extra_tokens=n_q, n_steps=n_q)
     n0 = shape.n_ctx
     n_ctx = n0 + n_q
@@ -245,7 +249,8 @@ def test_host_fed_step_equals_device_step(shape, n_q, store):
     V_b[n0:n_ctx] = 0
     b = _layer(shape, n_ctx, store, n_q)
     b.rebuild(raw_b, w, n0)
-    b.enable_host_feed(raw.dtype, K.dtype)
+    b.enable_host_feed(raw.dtype, K.dtype, pinned=pinned)
+    assert b.h_in.is_pinned() == pinned
     b.bind(raw_b, w, K_b, V_b)
     hin = b.host_inputs(n_q)
     hin["raw"].copy_(raw[n0:n_ctx].reshape(n_q, -1).cpu())
@@ -261,3 +266,33 @@ def test_host_fed_step_equals_device_step(shape, n_q, store):
     assert torch.equal(a.n_cells[:n_q], b.n_cells[:n_q])
     assert torch.equal(b.h_out[:n_q], out_a.cpu())
     assert torch.equal(b.h_lse[:n_q], a.lse[:n_q].cpu())
+
+
+@pytest.mark.parametrize("n_q,store", [(1, "f32"), (3, "bf16")])
+def test_plan_steps_equal_decode_step(n_q, store):
+    """Steps through a qsa_decode_plan (the fixed arguments bound once) equal
+    qsa_decode_step with all arguments, bit for bit, over several consecutive steps."""
+    shape = SMALL
+    steps = 5
+    inp = qsa_synth.decode_inputs(shape, seed=61, extra_tokens=steps + n_q, n_steps=n_q)
+    raw, w, K, V = (to_dev(inp["raw_k"]), to_dev(inp["norm_w"]), to_dev(inp["K"]),
+                    to_dev(inp["V"]))
+    qi, qa = to_dev(inp["q_idx"]), to_dev(inp["q"])
+    n0 = shape.n_ctx
+    a = _layer(shape, n0 + steps + n_q, store, n_q)
+    b = _layer(shape, n0 + steps + n_q, store, n_q)
+    a.rebuild(raw, w, n0)
+    b.rebuild(raw, w, n0)
+    b.bind(raw, w, K, V)
+    sp = torch.cuda.current_stream().cuda_stream
+    for t in range(steps):
+        n_ctx = n0 + n_q + t
+        out_a = a.step(raw, w, K, V, n_ctx, qi, qa)
+        b.step_ptr(n_ctx, qi.data_ptr(), qa.data_ptr(), sp, n_q)
+        torch.cuda.synchronize()
+        assert torch.equal(a.pooled, b.pooled)
+        assert torch.equal(a.counts[:n_q], b.counts[:n_q])
+        assert torch.equal(a.blocks[:n_q], b.blocks[:n_q])
+        assert torch.equal(a.pos[:n_q], b.pos[:n_q])
+        assert torch.equal(out_a, b.out[:n_q])
+        assert torch.equal(a.lse[:n_q], b.lse[:n_q])
