@@ -13,12 +13,17 @@
 //   - prologue kernels round the queries and (for an fp32 cache) the pooled rows to bf16
 //     (nearest even) into the workspace, so that both operands can be staged by TMA; a
 //     bf16 cache is already the operand and is read in place;
-//   - the score kernel is persistent, one CTA per SM, warp-specialised: warp 0 issues the
-//     TMA copies (query tile 128 x 64 and pooled tile 256 x 64 per stage, 128-byte
-//     swizzle, four stages in flight), warp 1 issues tcgen05.mma (M 128, N 256, K 16; four
-//     per stage) into one of two 256-column accumulators, and warps 2-5 drain the other
-//     accumulator (tcgen05.ld, scale, causal mask, store) while the next tile computes;
-//   - tiles are ordered query-block-fastest, so the CTAs working at the same time share a
+//   - the score kernel is persistent and runs as CTA pairs (clusters of two, one CTA per
+//     SM) sharing each tcgen05.mma of M 256 (128 queries in each CTA), N 256, K 16: per
+//     stage each CTA stages by TMA its 128 x 64 query tile and half (128 x 64) of the pooled
+//     tile (128-byte swizzle, six stages in flight), both completing on the leader CTA's
+//     barrier; the leader's warp 1 issues the MMAs (four per stage) into one of two
+//     256-column accumulators held in both CTAs' tensor memory and frees each stage in both
+//     CTAs with a multicast commit; warps 2-5 of each CTA drain the other accumulator
+//     (tcgen05.ld, scale, causal mask, store) while the next tile computes.  Against one
+//     CTA per M 128 tile this halves the pooled bytes each SM stages per MMA (32 KB a stage
+//     instead of 48 KB), so the same shared memory keeps 1.5 times the MMA time in flight;
+//   - tiles are ordered query-block-fastest, so the pairs working at the same time share a
 //     pooled tile and all but the first read it from L2;
 //   - every mbarrier wait is bounded (2 s): on a timeout the kernel records an error word,
 //     stops issuing, waits (bounded) for what it already issued, and always returns its
@@ -32,14 +37,14 @@ namespace {
 
 constexpr int kTcWarps = 6;
 constexpr int kTcThreads = 32 * kTcWarps;
-constexpr int kBM = 128;     // queries per tile (MMA M)
-constexpr int kBN = 256;     // pooled rows per tile (MMA N)
+constexpr int kBM = 128;     // queries per CTA; the CTA pair's MMA covers 256
+constexpr int kBN = 256;     // pooled rows per tile (MMA N); each CTA stages half of them
 constexpr int kBK = 64;      // k per stage: one 128-byte swizzle row of bf16
-constexpr int kStages = 4;
-constexpr int kTileA = kBM * kBK * 2;  // 16 KB
-constexpr int kTileB = kBN * kBK * 2;  // 32 KB
-constexpr uint32_t kTmemCols = 512;    // two accumulators of 256 columns
-constexpr int kEpiThreads = 128;       // warps 2-5
+constexpr int kStages = 6;
+constexpr int kTileA = kBM * kBK * 2;        // 16 KB: this CTA's 128 queries
+constexpr int kTileB = (kBN / 2) * kBK * 2;  // 16 KB: this CTA's 128 pooled rows
+constexpr uint32_t kTmemCols = 512;          // two accumulators of 256 columns
+constexpr int kEpiWarps = 4;                 // warps 2-5
 
 __host__ __device__ constexpr size_t tc_smem_bytes()
 {
@@ -60,46 +65,75 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr)
     return d;
 }
 
-// Instruction descriptor: fp32 accumulator, bf16 A and B, both K-major, N = 256, M = 128.
-__host__ __device__ constexpr uint32_t idesc_bf16_m128_n256()
+// Instruction descriptor: fp32 accumulator, bf16 A and B, both K-major, N = 256, M = 256
+// (the CTA pair: 128 rows in each CTA's tensor memory).
+__host__ __device__ constexpr uint32_t idesc_bf16_m256_n256()
 {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kBN >> 3) << 17) |
-           ((uint32_t)(kBM >> 4) << 24);
+           ((uint32_t)((2 * kBM) >> 4) << 24);
 }
 
-__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                          uint32_t idesc, uint32_t accumulate)
+// One M256 x N256 x K16 MMA of the CTA pair: A and B are read from the same shared-memory
+// offsets in both CTAs, D is written to the same tensor-memory columns of both.
+__device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                               uint32_t idesc, uint32_t accumulate)
 {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 
-__device__ __forceinline__ void umma_commit(uint64_t *bar)
+// Arrive on the barrier at this shared-memory offset in every CTA of `mask` once the pair
+// MMAs issued so far by this thread have completed.
+__device__ __forceinline__ void umma_commit_pair(uint64_t *bar, uint16_t mask)
 {
     asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-            smem_u32(bar))
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(smem_u32(bar)),
+        "h"(mask)
         : "memory");
 }
 
-__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+__device__ __forceinline__ uint32_t cluster_rank()
 {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
 }
 
-// 2-D tiled TMA load of the box at (x, y) into this CTA's shared memory.
-__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y,
-                                            uint64_t *bar)
+// Address of the same shared-memory object in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_to_rank(const void *p, uint32_t rank)
+{
+    uint32_t a;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_u32(p)), "r"(rank));
+    return a;
+}
+
+__device__ __forceinline__ void cluster_sync_all()
+{
+    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
+// 2-D tiled TMA load of the box at (x, y) into this CTA's shared memory, completing its bytes
+// on the barrier at cluster address bar (the leader CTA's, for either CTA of the pair).
+__device__ __forceinline__ void tma_load_2d_pair(void *dst, const CUtensorMap *map, int x, int y,
+                                                 uint32_t bar)
 {
     asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
-        "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::"
+        "bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
         : "memory");
+}
+
+// Remote (or local) arrival on a barrier given by its cluster address.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar)
+                 : "memory");
 }
 
 __device__ __forceinline__ uint32_t bf16x2(float lo, float hi)
@@ -144,19 +178,22 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 float scale, float *__restrict__ scores, int64_t ld_scores, int *__restrict__ err)
 {
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    // 1024-byte aligned operand area (the swizzle is a function of address bits 4-9)
+    // 1024-byte aligned operand area (the swizzle is a function of address bits 4-9); the
+    // same offsets in both CTAs of the pair, as the pair MMA requires
     unsigned char *base = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-    unsigned char *sA = base;                              // [kStages][128 rows][128 B]
-    unsigned char *sB = base + kStages * kTileA;           // [kStages][256 rows][128 B]
-    uint64_t *full = reinterpret_cast<uint64_t *>(sB + kStages * kTileB);  // [kStages]
-    uint64_t *empty = full + kStages;                      // [kStages]
-    uint64_t *accf = empty + kStages;                      // [2] accumulator ready
-    uint64_t *acce = accf + 2;                             // [2] accumulator drained
+    unsigned char *sA = base;                              // [kStages][128 queries][128 B]
+    unsigned char *sB = base + kStages * kTileA;           // [kStages][128 rows][128 B]
+    uint64_t *full = reinterpret_cast<uint64_t *>(sB + kStages * kTileB);  // [kStages] leader
+    uint64_t *empty = full + kStages;                      // [kStages] both CTAs
+    uint64_t *accf = empty + kStages;                      // [2] accumulator ready, both CTAs
+    uint64_t *acce = accf + 2;                             // [2] accumulator drained, leader
     uint64_t *drain = acce + 2;                            // every MMA issued has finished
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t rank = cluster_rank();  // 0: the leader, which issues the pair's MMAs
+    const bool leader = rank == 0;
 
     pdl_wait();
     QSA_AFTER_WAIT(q_pos);
@@ -169,68 +206,78 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         }
         for (int j = 0; j < 2; ++j) {
             mbar_init(&accf[j], 1);
-            mbar_init(&acce[j], kEpiThreads);
+            mbar_init(&acce[j], 2 * kEpiWarps);
         }
         mbar_init(drain, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 1) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+        // both CTAs of the pair allocate together: the same columns in each
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          smem_u32(tmem_slot)),
                      "r"(kTmemCols)
                      : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
     }
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-    __syncthreads();
+    __syncwarp();
+    cluster_sync_all();  // barriers initialised and tensor memory allocated in both CTAs
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     const uint32_t tmem = *tmem_slot;
 
-    const int64_t n_mb = (n_q + kBM - 1) / kBM;
+    const int64_t n_mb = (n_q + 2 * kBM - 1) / (2 * kBM);
     const int64_t n_nb = (n_rows + kBN - 1) / kBN;
     const int64_t n_units = n_mb * n_nb;
+    const int64_t pair = blockIdx.x >> 1, n_pairs = gridDim.x >> 1;
     const int n_k = K / kBK;
     bool ok = true;
 
     if (warp == 0) {
-        // ---- producer: one thread issues the TMA copies of every stage
+        // ---- producer, in each CTA: its 128 queries and its 128 pooled rows of every stage,
+        // both completing on the leader's barrier of the stage
         if (lane == 0) {
-            uint32_t uses[kStages] = {0, 0, 0, 0};
-            int stage = 0;
-            for (int64_t u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-                const int m0 = (int)((u % n_mb) * kBM), n0 = (int)((u / n_mb) * kBN);
-                for (int kb = 0; kb < n_k; ++kb) {
-                    if (uses[stage] > 0 && !mbar_wait(&empty[stage], (uses[stage] - 1) & 1u)) {
+            // k-step `it` of this CTA's sequence uses stage it % kStages for the
+            // (it / kStages)-th time; both CTAs of the pair run the same sequence
+            uint32_t it = 0;
+            for (int64_t u = pair; u < n_units && ok; u += n_pairs) {
+                const int m0 = (int)((u % n_mb) * (2 * kBM) + rank * kBM);
+                const int n0 = (int)((u / n_mb) * kBN + rank * (kBN / 2));
+                for (int kb = 0; kb < n_k; ++kb, ++it) {
+                    const uint32_t stage = it % kStages, use = it / kStages;
+                    if (use > 0 && !mbar_wait(&empty[stage], (use - 1) & 1u)) {
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(&full[stage], kTileA + kTileB);
-                    tma_load_2d(sA + stage * kTileA, &tmA, kb * kBK, m0, &full[stage]);
-                    tma_load_2d(sB + stage * kTileB, &tmB, kb * kBK, n0, &full[stage]);
-                    ++uses[stage];
-                    stage = stage + 1 == kStages ? 0 : stage + 1;
+                    if (leader) mbar_arrive_expect_tx(&full[stage], 2 * (kTileA + kTileB));
+                    const uint32_t fb = map_to_rank(&full[stage], 0);
+                    tma_load_2d_pair(sA + stage * kTileA, &tmA, kb * kBK, m0, fb);
+                    tma_load_2d_pair(sB + stage * kTileB, &tmB, kb * kBK, n0, fb);
                 }
             }
-            // every copy issued has landed before the CTA may retire
-            for (int s = 0; s < kStages; ++s)
-                if (uses[s] > 0 && !mbar_wait(&full[s], (uses[s] - 1) & 1u)) ok = false;
+            // the leader sees every stage it armed complete: both CTAs' copies have landed
+            if (leader)
+                for (uint32_t s = 0; s < kStages; ++s) {
+                    const uint32_t uses = it / kStages + (s < it % kStages ? 1u : 0u);
+                    if (uses > 0 && !mbar_wait(&full[s], (uses - 1) & 1u)) ok = false;
+                }
         }
     } else if (warp == 1) {
-        // ---- MMA issuer: one thread, accumulators alternate between the two TMEM halves
-        if (lane == 0) {
-            constexpr uint32_t idesc = idesc_bf16_m128_n256();
-            uint32_t uses[kStages] = {0, 0, 0, 0};
-            int stage = 0;
+        // ---- MMA issuer: one thread of the leader; accumulators alternate between the two
+        // tensor-memory halves
+        if (leader && lane == 0) {
+            constexpr uint32_t idesc = idesc_bf16_m256_n256();
+            uint32_t it = 0;
             int64_t t = 0;
-            for (int64_t u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++t) {
+            for (int64_t u = pair; u < n_units && ok; u += n_pairs, ++t) {
                 const int j = (int)(t & 1);
                 if (t >= 2 && !mbar_wait(&acce[j], (uint32_t)((t >> 1) - 1) & 1u)) {
                     ok = false;
                     break;
                 }
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                for (int kb = 0; kb < n_k; ++kb) {
-                    if (!mbar_wait(&full[stage], uses[stage] & 1u)) {
+                for (int kb = 0; kb < n_k; ++kb, ++it) {
+                    const uint32_t stage = it % kStages;
+                    if (!mbar_wait(&full[stage], (it / kStages) & 1u)) {
                         ok = false;
                         break;
                     }
@@ -239,30 +286,30 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     const uint32_t b0 = smem_u32(sB + stage * kTileB);
 #pragma unroll
                     for (int k16 = 0; k16 < kBK / 16; ++k16)
-                        umma_bf16(tmem + (uint32_t)(j * kBN), sw128_desc(a0 + k16 * 32),
-                                  sw128_desc(b0 + k16 * 32), idesc, (kb | k16) ? 1u : 0u);
-                    umma_commit(&empty[stage]);  // the stage is free once these MMAs finish
-                    ++uses[stage];
-                    stage = stage + 1 == kStages ? 0 : stage + 1;
+                        umma_bf16_pair(tmem + (uint32_t)(j * kBN), sw128_desc(a0 + k16 * 32),
+                                       sw128_desc(b0 + k16 * 32), idesc, (kb | k16) ? 1u : 0u);
+                    umma_commit_pair(&empty[stage], 0x3);  // the stage is free in both CTAs
                 }
                 if (!ok) break;
-                umma_commit(&accf[j]);
+                umma_commit_pair(&accf[j], 0x3);
             }
-            umma_commit(drain);
+            umma_commit_pair(drain, 0x1);
             if (!mbar_wait(drain, 0)) ok = false;
         }
     } else {
-        // ---- epilogue: warp w reads tensor-memory lanes 32*(w%4) .. +31 (its queries)
+        // ---- epilogue, in each CTA: warp w reads tensor-memory lanes 32*(w%4) .. +31 (its
+        // queries), then reports the accumulator half drained to the leader
         const int quarter = warp & 3;
+        const uint32_t acce_leader[2] = {map_to_rank(&acce[0], 0), map_to_rank(&acce[1], 0)};
         int64_t t = 0;
-        for (int64_t u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++t) {
+        for (int64_t u = pair; u < n_units && ok; u += n_pairs, ++t) {
             const int j = (int)(t & 1);
             if (!mbar_wait(&accf[j], (uint32_t)(t >> 1) & 1u)) {
                 ok = false;
                 break;
             }
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-            const int64_t m0 = (u % n_mb) * kBM, n0 = (u / n_mb) * kBN;
+            const int64_t m0 = (u % n_mb) * (2 * kBM) + rank * kBM, n0 = (u / n_mb) * kBN;
             const int64_t qi = m0 + quarter * 32 + lane;
             const int64_t p = (qi < n_q && q_pos) ? (int64_t)q_pos[qi] : INT64_MAX;
 #pragma unroll 1
@@ -302,16 +349,20 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 }
             }
             asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-            mbar_arrive(&acce[j]);  // this half of tensor memory may be overwritten
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(acce_leader[j]);  // this half may be overwritten
         }
     }
 
     if (!ok) atomicExch(err, 1);
+    // neither CTA leaves (or frees its tensor memory) while the pair's MMAs, copies or
+    // remote arrivals may still touch it
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-    __syncthreads();
+    __syncwarp();
+    cluster_sync_all();
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     if (warp == 1)
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                      "r"(kTmemCols)
                      : "memory");
 }
@@ -385,7 +436,7 @@ qsa_status launch_index_score_tc(const float *q, int64_t n_q, int64_t ld_q,
                      : static_cast<const __nv_bfloat16 *>(pooled);
     int *err = reinterpret_cast<int *>(ws + need - 256);
     CUtensorMap tmA, tmB;
-    if (!make_map(&tmA, qb, n_q, K, kBM) || !make_map(&tmB, pb, n_rows, K, kBN))
+    if (!make_map(&tmA, qb, n_q, K, kBM) || !make_map(&tmB, pb, n_rows, K, kBN / 2))
         return QSA_ERR_CUDA;
     cudaError_t e = launch(q_to_bf16_kernel, dim3(1024), dim3(256), 0, st, 1, q, n_q, ld_q, K, qb);
     if (e == cudaSuccess && convert_rows) {
@@ -396,11 +447,31 @@ qsa_status launch_index_score_tc(const float *q, int64_t n_q, int64_t ld_q,
     }
     if (e != cudaSuccess) return QSA_ERR_CUDA;
     if (ensure_kernel_attrs<score_tc_kernel>(tc_smem_bytes()) != cudaSuccess) return QSA_ERR_CUDA;
-    const int64_t n_units = ((n_q + kBM - 1) / kBM) * ((n_rows + kBN - 1) / kBN);
-    int64_t grid = device_sm_count();
-    if (grid > n_units) grid = n_units;
-    e = launch(score_tc_kernel, dim3((unsigned)grid), dim3(kTcThreads), tc_smem_bytes(), st, 1,
-               tmA, tmB, n_q, q_pos, n_rows, K, scale, scores, ld_scores, err);
+    // CTA pairs (clusters of two), persistent: as many pairs as fit on the GPU at once
+    const int64_t n_units = ((n_q + 2 * kBM - 1) / (2 * kBM)) * ((n_rows + kBN - 1) / kBN);
+    int64_t pairs = device_sm_count() / 2;
+    {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)(2 * pairs));
+        cfg.blockDim = dim3(kTcThreads);
+        cfg.dynamicSmemBytes = tc_smem_bytes();
+        cudaLaunchAttribute a;
+        a.id = cudaLaunchAttributeClusterDimension;
+        a.val.clusterDim.x = 2;
+        a.val.clusterDim.y = 1;
+        a.val.clusterDim.z = 1;
+        cfg.attrs = &a;
+        cfg.numAttrs = 1;
+        int resident = 0;
+        if (cudaOccupancyMaxActiveClusters(&resident, score_tc_kernel, &cfg) != cudaSuccess)
+            (void)cudaGetLastError();
+        else if (resident > 0 && resident < pairs)
+            pairs = resident;
+    }
+    if (pairs > n_units) pairs = n_units;
+    if (pairs < 1) pairs = 1;
+    e = launch(score_tc_kernel, dim3((unsigned)(2 * pairs)), dim3(kTcThreads), tc_smem_bytes(), st,
+               2, tmA, tmB, n_q, q_pos, n_rows, K, scale, scores, ld_scores, err);
     return e == cudaSuccess ? QSA_OK : QSA_ERR_CUDA;
 }
 
