@@ -279,3 +279,48 @@ def test_prefill_attention_all_heads_per_query():
                                           scale)
         np.testing.assert_allclose(g_out[i], want, rtol=0, atol=ATOL_ATTN_BF16)
         np.testing.assert_allclose(g_lse[i], want_lse, rtol=1e-5, atol=1e-4)
+
+
+@pytest.mark.parametrize("ld_pad", [0, 64], ids=["contiguous", "strided"])
+def test_prefill_attention_block_lists(ld_pad):
+    """Lists made of whole 4-token blocks (the prefill selections) and a tail: groups of four
+    consecutive rows are staged by one copy when the cache rows are contiguous (ld_pad 0) and
+    row by row otherwise; lists whose groups are broken (a skipped entry, a two-cell shift, a
+    gap) take the row-by-row form.  Every output and log-sum-exp against the oracle."""
+    n_q, H_kv, G, d, n_kv, max_cells = 40, 4, 8, 128, 9000, 2051
+    H_q, ld = H_kv * G, H_kv * d + ld_pad
+    rng = np.random.default_rng(4096 + ld_pad)
+    K = qsa_synth.to_bf16_bits(rng.standard_normal((n_kv, ld)).astype(np.float32))
+    V = qsa_synth.to_bf16_bits(rng.standard_normal((n_kv, ld)).astype(np.float32))
+    q = rng.standard_normal((n_q, H_q, d)).astype(np.float32)
+    edge = [0, 1, 3, 4, 5, 31, 32, 33, 36, 64, 97, 2048, 2049, 2051]
+    lens = edge + list(rng.integers(1, max_cells + 1, size=n_q - len(edge)))
+    pos = np.full((n_q, max_cells), -9, np.int32)
+    n_blk = n_kv // 4
+    for i, L in enumerate(lens):
+        nb, tail = L // 4, L % 4
+        b = np.sort(rng.choice(n_blk - 1, size=nb, replace=False))
+        cells = (4 * b[:, None] + np.arange(4)).reshape(-1)
+        t0 = 4 * (n_blk - 1)
+        pos[i, :L] = np.concatenate([cells, t0 + np.arange(tail)]).astype(np.int32)
+    pos[20, 6] = -1                                   # a skipped entry inside a group
+    pos[21, :lens[21]] = np.sort(np.concatenate([[3, 7], pos[21, 2:lens[21]] + 8]))[:lens[21]]
+    pos[22, 5] += 1                                   # a gap: the group is not consecutive
+    pos[22, 6:8] += 1
+    out = torch.zeros((n_q, H_q, d), device="cuda")
+    lse = torch.zeros((n_q, H_q), device="cuda")
+    ws = torch.empty(max(qsa.sparse_attn_workspace_size(n_q, H_q, H_kv, d, max_cells) // 4, 1),
+                     device="cuda")
+    scale = 1.0 / math.sqrt(d)
+    qsa.sparse_attn(to_dev(q), to_dev(K), to_dev(V), to_dev(np.array(lens, np.int32)), max_cells,
+                    out, H_kv, d, d, scale, pos=to_dev(pos), lse=lse, workspace=ws)
+    g_out, g_lse = to_host(out), to_host(lse)
+    for i, L in enumerate(lens):
+        cells = pos[i, :L]
+        cells = cells[(cells >= 0) & (cells < n_kv)]
+        if len(cells) == 0:
+            assert np.all(g_out[i] == 0.0) and np.all(np.isneginf(g_lse[i]))
+            continue
+        want, want_lse = oracle.attention(q[i], K, V, H_q, H_kv, d, d, ld, ld, cells, scale)
+        np.testing.assert_allclose(g_out[i], want, rtol=0, atol=ATOL_ATTN_BF16)
+        np.testing.assert_allclose(g_lse[i], want_lse, rtol=1e-5, atol=1e-4)
