@@ -161,6 +161,55 @@ __device__ __forceinline__ void for_each_key(const float *__restrict__ row, int6
     }
 }
 
+// The float whose key is T, for a T above the key of -inf (score_key is monotone and maps
+// NaN to -inf and -0 to +0): for such T, score_key(x) >= T exactly when x >= key_float(T)
+// as floats (a NaN x compares false, and its key, that of -inf, is below T).  A T in the
+// NaN range above +inf gives a NaN, which no x reaches, as no key reaches T.
+__device__ __forceinline__ float key_float(uint32_t T)
+{
+    return __uint_as_float((T & 0x80000000u) ? (T & 0x7fffffffu) : ~T);
+}
+constexpr uint32_t kKeyNegInf = 0x007fffffu;  // score_key(-inf), also that of NaN
+
+// Apply f(key, index) to the scores of the row with key >= T, T > kKeyNegInf: one float
+// compare per score (four per vector on the common path) instead of a key per score.
+template <typename F>
+__device__ __forceinline__ void for_each_key_at_least(const float *__restrict__ row, int64_t n,
+                                                      uint32_t T, F f)
+{
+    constexpr int U = 8;
+    const float lo = key_float(T);
+    if ((reinterpret_cast<uintptr_t>(row) & 15) == 0) {
+        const int64_t n4 = n / 4;
+        const float4 *r4 = reinterpret_cast<const float4 *>(row);
+        for (int64_t base = threadIdx.x; base < n4; base += (int64_t)NT * U) {
+            float4 v[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t i = base + (int64_t)u * NT;
+                v[u] = i < n4 ? r4[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t i = base + (int64_t)u * NT;
+                const float4 x = v[u];
+                // fmaxf drops NaN operands, so the maximum reaches lo iff some lane does
+                if (i < n4 && fmaxf(fmaxf(x.x, x.y), fmaxf(x.z, x.w)) >= lo) {
+                    if (x.x >= lo) f(score_key(x.x), 4 * i);
+                    if (x.y >= lo) f(score_key(x.y), 4 * i + 1);
+                    if (x.z >= lo) f(score_key(x.z), 4 * i + 2);
+                    if (x.w >= lo) f(score_key(x.w), 4 * i + 3);
+                }
+            }
+        }
+        for (int64_t i = 4 * n4 + threadIdx.x; i < n; i += NT)
+            if (row[i] >= lo) f(score_key(row[i]), i);
+    } else {
+        for (int64_t i = threadIdx.x; i < n; i += NT)
+            if (row[i] >= lo) f(score_key(row[i]), i);
+    }
+}
+
 // Step 5 of the general form: fold the ties (lowest index first, k_rem of them) into the
 // selected bitmap, then write the selected blocks in ascending order.
 __device__ void write_selection(uint32_t *selw, const uint32_t *eqw, int64_t nw, uint32_t k_rem,
@@ -274,7 +323,7 @@ __device__ void topk_query(const float *srow, int64_t n, int64_t k, int32_t *out
     // ---- 2. classify every candidate (one read)
     const uint32_t B1 = prefix;
     const uint32_t lo_key = B1 << (32 - kTopkHistBits);  // smallest key with digit B1
-    for_each_key(srow, n, [&](uint32_t key, int64_t i) {
+    auto classify = [&](uint32_t key, int64_t i) {
         if (key < lo_key) return;  // below the threshold bucket: the common case
         const uint32_t d = key >> (32 - kTopkHistBits);
         if (d > B1 || whole) {
@@ -286,7 +335,9 @@ __device__ void topk_query(const float *srow, int64_t n, int64_t k, int32_t *out
                 cand_idx[slot] = (int32_t)i;
             }
         }
-    });
+    };
+    if (lo_key > kKeyNegInf) for_each_key_at_least(srow, n, lo_key, classify);
+    else for_each_key(srow, n, classify);
     __syncthreads();
 
     if (!whole) {
@@ -380,8 +431,8 @@ __device__ bool topk_query_sampled(const float *srow, int64_t n, int64_t k, int3
     const uint32_t T = misc[0] << (32 - kTopkHistBits);
     __syncthreads();
 
-    // ---- 2. one pass: every key >= T is a candidate (warp-aggregated appends)
-    for_each_key(srow, n, [&](uint32_t key, int64_t i) {
+    // ---- 2. one pass: every key >= T is a candidate
+    auto keep = [&](uint32_t key, int64_t i) {
         if (key >= T) {
             const uint32_t slot = atomicAdd(&misc[8], 1u);
             if (slot < (uint32_t)cand_cap) {
@@ -389,7 +440,9 @@ __device__ bool topk_query_sampled(const float *srow, int64_t n, int64_t k, int3
                 cand_idx[slot] = (int32_t)i;
             }
         }
-    });
+    };
+    if (T > kKeyNegInf) for_each_key_at_least(srow, n, T, keep);
+    else for_each_key(srow, n, keep);
     __syncthreads();
     const uint32_t m = misc[8];
     if (m < (uint32_t)k || m > (uint32_t)cand_cap) return false;  // uniform

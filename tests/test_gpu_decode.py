@@ -196,6 +196,39 @@ def test_topk_large_rows_many_queries(case):
         np.testing.assert_array_equal(g_blocks[i, :g_counts[i]], want)
 
 
+@pytest.mark.parametrize("case", ["normal", "equal", "few_levels", "heavy_tail", "narrow"])
+def test_topk_many_queries(case):
+    """A prefill-sized query count (more than two per SM: the general kernel's
+    two-CTAs-per-SM form) over rows of up to 40k blocks, each query seeing its own number
+    of complete blocks (sampled form, full form, fewer blocks than k).  Exact against the
+    oracle for every query; nothing written past each query's count."""
+    rng = np.random.default_rng(100 + len(case))
+    n_q, n_full, k = 320, 40000, 512
+    if case == "normal":
+        s = (4 * rng.standard_normal((n_q, n_full))).astype(np.float32)
+    elif case == "equal":
+        s = np.full((n_q, n_full), -1.5, np.float32)
+    elif case == "few_levels":
+        s = rng.integers(0, 40, size=(n_q, n_full)).astype(np.float32) * 0.5
+    elif case == "heavy_tail":
+        s = rng.standard_cauchy((n_q, n_full)).astype(np.float32)
+    else:
+        s = (1.0 + 1e-6 * rng.standard_normal((n_q, n_full))).astype(np.float32)
+    base = np.array([40000, 20000, 16384, 16383, 30001, 513, 512, 100, 0, 1], np.int64)
+    n_each = np.where(np.arange(n_q) < base.shape[0], base[np.arange(n_q) % base.shape[0]],
+                      rng.integers(16384, n_full + 1, size=n_q))
+    q_pos = (4 * n_each - 1 + (np.arange(n_q) % 4)).astype(np.int32)  # tails of 0-3 tokens
+    blocks = torch.full((n_q, k), -3, dtype=torch.int32, device="cuda")
+    counts = torch.zeros(n_q, dtype=torch.int32, device="cuda")
+    qsa.topk_blocks(to_dev(s), n_full, k, blocks, counts, q_pos=to_dev(q_pos))
+    g_blocks, g_counts = to_host(blocks), to_host(counts)
+    for i in range(n_q):
+        want = _oracle_topk_on_f32(s[i], int(n_each[i]), k)
+        assert g_counts[i] == want.shape[0], i
+        np.testing.assert_array_equal(g_blocks[i, :g_counts[i]], want)
+        assert np.all(g_blocks[i, g_counts[i]:] == -3)
+
+
 def test_topk_per_query_positions():
     """With q_pos, query i ranks only blocks complete at its position."""
     rng = np.random.default_rng(6)
