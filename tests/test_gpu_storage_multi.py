@@ -296,3 +296,38 @@ def test_plan_steps_equal_decode_step(n_q, store):
         assert torch.equal(a.pos[:n_q], b.pos[:n_q])
         assert torch.equal(out_a, b.out[:n_q])
         assert torch.equal(a.lse[:n_q], b.lse[:n_q])
+
+
+@pytest.mark.parametrize("n_q,n_rows", [(130, 45_000), (1024, 64_052)])
+def test_tensor_core_scores_fp32_cache_equal_bf16_cache(n_q, n_rows):
+    """An fp32 cache goes through the tensor-core contraction as its bf16 rounding: chunk
+    by chunk, rounded on a second stream while earlier chunks are contracted when the rows
+    span several chunks.  The result is bit-identical to the same call on a bf16 cache
+    holding that rounding (one pass, nothing to round), and rows invisible to a query stay
+    -inf.  (The oracle pins the bf16-cache path elsewhere.)"""
+    H, d = 16, 128
+    g = torch.Generator(device="cuda")
+    g.manual_seed(n_rows)
+    pooled = torch.randn(n_rows, H * d, device="cuda", generator=g)
+    q = torch.randn(n_q, H * d, device="cuda", generator=g)
+    depth = 4 * n_rows - n_q - 700  # the last queries see every row, the first do not
+    q_pos = torch.arange(depth, depth + n_q, dtype=torch.int32, device="cuda")
+    scale = 1.0 / math.sqrt(d)
+    out = {}
+    for dt in (qsa.QSA_F32, qsa.QSA_BF16):
+        src = pooled if dt == qsa.QSA_F32 else pooled.to(torch.bfloat16)
+        ws = torch.zeros(qsa.index_score_workspace_size(n_q, n_rows, H, d, qsa.QSA_PREC_BF16_TC,
+                                                        dt), dtype=torch.uint8, device="cuda")
+        scores = torch.full((n_q, n_rows + 3), 5.0, device="cuda")
+        qsa.index_score(q, src, n_rows, H, d, scale, scores, q_pos=q_pos,
+                        precision=qsa.QSA_PREC_BF16_TC, workspace=ws)
+        out[dt] = scores
+    torch.cuda.synchronize()
+    a, b = out[qsa.QSA_F32], out[qsa.QSA_BF16]
+    assert torch.equal(a, b)
+    assert torch.all(a[:, n_rows:] == 5.0)
+    lim = (q_pos.long() + 1) // 4
+    cols = torch.arange(n_rows, device="cuda")
+    invisible = cols[None, :] >= lim[:, None]
+    assert torch.all(torch.isneginf(a[:, :n_rows][invisible]))
+    assert torch.all(torch.isfinite(a[:, :n_rows][~invisible]))
