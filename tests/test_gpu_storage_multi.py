@@ -300,11 +300,10 @@ def test_plan_steps_equal_decode_step(n_q, store):
 
 @pytest.mark.parametrize("n_q,n_rows", [(130, 45_000), (1024, 64_052)])
 def test_tensor_core_scores_fp32_cache_equal_bf16_cache(n_q, n_rows):
-    """An fp32 cache goes through the tensor-core contraction as its bf16 rounding: chunk
-    by chunk, rounded on a second stream while earlier chunks are contracted when the rows
-    span several chunks.  The result is bit-identical to the same call on a bf16 cache
-    holding that rounding (one pass, nothing to round), and rows invisible to a query stay
-    -inf.  (The oracle pins the bf16-cache path elsewhere.)"""
+    """An fp32 cache goes through the tensor-core contraction as its bf16 rounding (a
+    rounding pass into the workspace, then the contraction): the result is bit-identical to
+    the same call on a bf16 cache holding that rounding (read in place), and rows invisible
+    to a query stay -inf.  (The oracle pins the bf16-cache path elsewhere.)"""
     H, d = 16, 128
     g = torch.Generator(device="cuda")
     g.manual_seed(n_rows)
