@@ -330,3 +330,41 @@ def test_tensor_core_scores_fp32_cache_equal_bf16_cache(n_q, n_rows):
     invisible = cols[None, :] >= lim[:, None]
     assert torch.all(torch.isneginf(a[:, :n_rows][invisible]))
     assert torch.all(torch.isfinite(a[:, :n_rows][~invisible]))
+
+
+@pytest.mark.parametrize("store", ["f32", "bf16"])
+def test_rejected_drafts_roll_back(store):
+    """Speculative decode: a step carries a token and two drafts; the drafts are rejected,
+    a different token is written in the first draft's place, the layer is told which rows
+    changed, and the next step runs one query.  Its cache, selection and output equal those
+    of a layer that never saw the drafts (rebuilt at the accepted length, then stepped)."""
+    shape = SMALL
+    n0 = shape.n_ctx + 2  # 9,005: the drafts straddle a block boundary (9,004 = 4 * 2,251)
+    inp = qsa_synth.decode_inputs(qsa_synth.shrink(shape, n_ctx=n0), seed=71, extra_tokens=4,
+                                  n_steps=4)
+    raw, w, K, V = (to_dev(inp["raw_k"]), to_dev(inp["norm_w"]), to_dev(inp["K"]),
+                    to_dev(inp["V"]))
+    qi, qa = to_dev(inp["q_idx"]), to_dev(inp["q"])
+    cap = n0 + 8
+    # speculative layer: three queries at n0+1 .. n0+3 (token n0, drafts n0+1, n0+2)
+    a = _layer(shape, cap, store, 3)
+    a.rebuild(raw, w, n0)
+    a.step(raw, w, K, V, n0 + 3, qi[:3], qa[:3])
+    # the drafts are rejected: token n0+1 is replaced, row n0+2 is dropped
+    raw2, K2, V2 = raw.clone(), K.clone(), V.clone()
+    raw2[n0 + 1] = raw[n0 + 3]
+    K2[n0 + 1], V2[n0 + 1] = K[n0 + 3], V[n0 + 3]
+    a.invalidate(n0 + 1)
+    out_a = a.step(raw2, w, K2, V2, n0 + 2, qi[3:4], qa[3:4]).clone()
+    # reference layer: the accepted context only
+    b = _layer(shape, cap, store, 3)
+    b.rebuild(raw2, w, n0 + 1)
+    out_b = b.step(raw2, w, K2, V2, n0 + 2, qi[3:4], qa[3:4]).clone()
+    torch.cuda.synchronize()
+    n_rows = (n0 + 2 + 3) // 4
+    assert torch.equal(a.pooled[:n_rows], b.pooled[:n_rows])
+    assert torch.equal(a.counts[:1], b.counts[:1])
+    assert torch.equal(a.blocks[:1], b.blocks[:1])
+    assert torch.equal(a.n_cells[:1], b.n_cells[:1])
+    assert torch.equal(a.pos[:1, :int(b.n_cells[0])], b.pos[:1, :int(b.n_cells[0])])
+    assert torch.equal(out_a, out_b)
