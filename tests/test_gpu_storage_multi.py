@@ -368,3 +368,33 @@ def test_rejected_drafts_roll_back(store):
     assert torch.equal(a.n_cells[:1], b.n_cells[:1])
     assert torch.equal(a.pos[:1, :int(b.n_cells[0])], b.pos[:1, :int(b.n_cells[0])])
     assert torch.equal(out_a, out_b)
+
+
+def test_plan_steps_with_changing_query_counts():
+    """One plan, steps of 1, 3, 1, 4 and 2 queries (the workspace layout moves with the
+    count, so the histogram kept for the next step is rebuilt when it no longer matches):
+    each equals qsa_decode_step with all arguments, bit for bit."""
+    shape = SMALL
+    seq = [1, 3, 1, 4, 2]
+    total = sum(seq)
+    inp = qsa_synth.decode_inputs(shape, seed=83, extra_tokens=total, n_steps=4)
+    raw, w, K, V = (to_dev(inp["raw_k"]), to_dev(inp["norm_w"]), to_dev(inp["K"]),
+                    to_dev(inp["V"]))
+    qi, qa = to_dev(inp["q_idx"]), to_dev(inp["q"])
+    n0 = shape.n_ctx
+    a = _layer(shape, n0 + total, "f32", 4)
+    b = _layer(shape, n0 + total, "f32", 4)
+    a.rebuild(raw, w, n0)
+    b.rebuild(raw, w, n0)
+    b.bind(raw, w, K, V)
+    sp = torch.cuda.current_stream().cuda_stream
+    n_ctx = n0
+    for n_q in seq:
+        n_ctx += n_q
+        out_a = a.step(raw, w, K, V, n_ctx, qi[:n_q], qa[:n_q])
+        b.step_ptr(n_ctx, qi.data_ptr(), qa.data_ptr(), sp, n_q)
+        torch.cuda.synchronize()
+        assert torch.equal(a.pooled, b.pooled)
+        assert torch.equal(a.blocks[:n_q], b.blocks[:n_q])
+        assert torch.equal(a.n_cells[:n_q], b.n_cells[:n_q])
+        assert torch.equal(out_a, b.out[:n_q])
