@@ -78,7 +78,8 @@ gather_kernel(const char *__restrict__ K, const char *__restrict__ V, int esize,
     (void)esize;
 }
 
-// Index-only form (no row copies): one thread per output cell.
+// Index-only form (no row copies): thread j writes the four cells of selected block j (one
+// 16-byte store when the row allows it); thread cnt writes the open tail.
 __global__ void __launch_bounds__(256)
 cells_kernel(int64_t n_kv, const int32_t *__restrict__ blocks, const int32_t *__restrict__ counts,
              int64_t k_blk, const int32_t *__restrict__ q_pos, int64_t n_ctx,
@@ -91,23 +92,35 @@ cells_kernel(int64_t n_kv, const int32_t *__restrict__ blocks, const int32_t *__
     pdl_trigger();
     const int64_t qi = blockIdx.y;
     const int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    int64_t cnt = counts[qi];
+    const int64_t b = j < k_blk ? (int64_t)blocks[qi * k_blk + j] : -1;  // issued with counts
     const int64_t p = q_pos ? (int64_t)q_pos[qi] : n_ctx - 1;
     const int64_t tail0 = 4 * ((p + 1) / 4);
-    int64_t cnt = counts[qi];
     if (cnt < 0) cnt = 0;
     if (cnt > k_blk) cnt = k_blk;
-    const int64_t n_cells = 4 * cnt + (p + 1 - tail0);
-    if (j == 0) n_cells_out[qi] = (int32_t)n_cells;
-    if (j >= n_cells) return;
-    int64_t cell;
-    if (j < 4 * cnt) {
-        const int64_t b = blocks[qi * k_blk + j / 4];
-        cell = b >= 0 ? 4 * b + (j & 3) : -1;
-    } else {
-        cell = tail0 + (j - 4 * cnt);
+    const int64_t n_tail = p + 1 - tail0;
+    int32_t *row = pos_out + qi * max_cells;
+    if (j == 0) n_cells_out[qi] = (int32_t)(4 * cnt + n_tail);
+    if (j < cnt) {
+        int32_t c[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int64_t cell = b >= 0 ? 4 * b + r : -1;
+            c[r] = cell >= n_kv ? -1 : (int32_t)cell;
+        }
+        int32_t *dst = row + 4 * j;
+        if ((reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
+            *reinterpret_cast<int4 *>(dst) = make_int4(c[0], c[1], c[2], c[3]);
+        } else {
+#pragma unroll
+            for (int r = 0; r < 4; ++r) dst[r] = c[r];
+        }
+    } else if (j == cnt) {
+        for (int64_t t = 0; t < n_tail; ++t) {
+            const int64_t cell = tail0 + t;
+            row[4 * cnt + t] = cell >= n_kv ? -1 : (int32_t)cell;
+        }
     }
-    if (cell >= n_kv) cell = -1;
-    pos_out[qi * max_cells + j] = (int32_t)cell;
 }
 
 }  // namespace
@@ -121,7 +134,7 @@ cudaError_t launch_gather(const void *K, const void *V, qsa_dtype dt, int64_t n_
 {
     if (n_q == 0) return cudaSuccess;
     if (!K_out && !V_out) {
-        const dim3 grid((unsigned)((max_cells + 255) / 256), (unsigned)n_q);
+        const dim3 grid((unsigned)((k_blk + 1 + 255) / 256), (unsigned)n_q);  // blocks + tail
         return launch(cells_kernel, grid, dim3(256), 0, st, 1, n_kv, blocks, counts, k_blk, q_pos,
                       n_ctx, pos_out, n_cells_out, max_cells);
     }
