@@ -284,7 +284,10 @@ class DecodePlan:
             self.handle = None
 
     def __del__(self):
-        self.close()
+        try:
+            self.close()
+        except Exception:  # interpreter shutdown: the library may already be gone
+            pass
 
 
 def mask_to_list(mask, max_list, pos_out, counts_out, bits_out=None, n_kv=None, stream=None):
