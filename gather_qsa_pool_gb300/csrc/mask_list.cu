@@ -6,8 +6,11 @@
 // the count is taken from the same words.
 //
 // On 32-lane warps each 64-bit word is two ballots: lanes read positions 64w + lane and
-// 64w + 32 + lane.  One CTA per mask row walks the row in chunks of 64 * 1024 positions:
-//   1. each warp ballots its words, keeps them in shared memory, popcounts them;
+// 64w + 32 + lane; when the row is whole 64-byte words, 16-byte aligned, each thread
+// instead reads its word's 64 bytes with four 16-byte loads and packs the nonzero flags
+// itself (the same word).  One CTA per mask row walks the row in chunks of 64 * 1024
+// positions:
+//   1. the words of the chunk go to shared memory;
 //   2. one block-wide exclusive scan of the word counts gives each word's list offset;
 //   3. the thread owning a word writes its set positions (lowest bit first).
 // The list is capped at max_list; the count written is the true count.
@@ -17,6 +20,14 @@ namespace qsa {
 namespace {
 
 constexpr int kMaskThreads = 1024;
+
+// Bit i (i < 4) set when byte i of x is nonzero: the bytes' nonzero flags (0 or 1 each), times
+// a constant that moves byte i's flag to bit 28 + i with no carry into those bits.
+__device__ __forceinline__ uint32_t nonzero_byte_bits(uint32_t x)
+{
+    const uint32_t m = __vcmpne4(x, 0u) & 0x01010101u;
+    return (m * 0x10204080u) >> 28;
+}
 constexpr int kWordsPerChunk = kMaskThreads;  // one word per thread per chunk
 
 __global__ void __launch_bounds__(kMaskThreads)
@@ -41,9 +52,30 @@ mask_to_list_kernel(const uint8_t *__restrict__ mask, int64_t n_kv, int64_t ld_m
     if (threadIdx.x == 0) carry_s = 0;
     __syncthreads();
 
+    // rows whose words are all whole and 16-byte aligned: thread t builds word w0 + t from its
+    // 64 mask bytes, four 16-byte loads issued together
+    const bool vec = n_kv % 64 == 0 && (reinterpret_cast<uintptr_t>(row) & 15) == 0;
     for (int64_t w0 = 0; w0 < n_words; w0 += kWordsPerChunk) {
+        if (vec) {
+            const int64_t w = w0 + threadIdx.x;
+            unsigned long long word = 0ull;
+            if (w < n_words) {
+                const uint4 *src = reinterpret_cast<const uint4 *>(row + 64 * w);
+                uint4 v[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) v[k] = src[k];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const uint32_t u[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+#pragma unroll
+                    for (int m = 0; m < 4; ++m)
+                        word |= (unsigned long long)nonzero_byte_bits(u[m]) << (16 * k + 4 * m);
+                }
+            }
+            words[threadIdx.x] = word;
+        }
         // 1. ballots: warp `warp` builds words w0 + warp, w0 + warp + NW, ...
-        for (int wi = warp; wi < kWordsPerChunk; wi += NW) {
+        for (int wi = warp; !vec && wi < kWordsPerChunk; wi += NW) {
             const int64_t w = w0 + wi;
             unsigned long long word = 0ull;
             if (w < n_words) {

@@ -18,16 +18,22 @@ pytestmark = pytest.mark.gpu
 
 # ------------------------------------------------------------------ a7 mask -> list
 
-@pytest.mark.parametrize("n_kv", [32768, 100_000, 1000, 64, 63, 1])
-def test_mask_to_list(n_kv):
+@pytest.mark.parametrize("n_kv,ld_pad", [(32768, 0), (100_000, 0), (1000, 0), (64, 0), (63, 0),
+                                         (1, 0), (65_600, 0), (4096, 4)])
+def test_mask_to_list(n_kv, ld_pad):
+    """Rows of whole 64-key words on 16-byte boundaries (read 64 bytes a thread), ragged rows
+    and rows whose stride breaks the alignment (ballots), one and two chunks of 65,536."""
     n_rows, max_list = 3, 2048
     m = qsa_synth.mask_rows(n_rows, n_kv, seed=n_kv)
     if n_kv >= 64:
         m[1, :] = 0            # empty row
+    wide = np.zeros((n_rows, n_kv + ld_pad), np.uint8)
+    wide[:, :n_kv] = m
+    wide[:, n_kv:] = 1         # past the row: never listed
     pos = torch.full((n_rows, max_list), -3, dtype=torch.int32, device="cuda")
     counts = torch.zeros(n_rows, dtype=torch.int32, device="cuda")
     bits = torch.zeros((n_rows, (n_kv + 63) // 64), dtype=torch.int64, device="cuda")
-    qsa.mask_to_list(to_dev(m), max_list, pos, counts, bits)
+    qsa.mask_to_list(to_dev(wide), max_list, pos, counts, bits, n_kv=n_kv)
     g_pos, g_cnt, g_bits = to_host(pos), to_host(counts), to_host(bits).view(np.uint64)
     for r in range(n_rows):
         w_pos, w_cnt, w_bits = oracle.mask_to_list(m[r], max_list)
