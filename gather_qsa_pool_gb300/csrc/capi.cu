@@ -5,6 +5,7 @@
 #include <math.h>
 #include <stdlib.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "qsa_internal.cuh"
@@ -13,19 +14,23 @@ namespace qsa {
 
 int device_sm_count()
 {
-    static int cached_dev = -1;
-    static int cached_sms = 0;
+    constexpr int kMaxDevices = 64;
+    static std::atomic<int> sms_of[kMaxDevices];  // 0: not yet asked (static: zero at start)
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return kTargetSMs;
-    if (dev != cached_dev) {
-        int sms = 0;
-        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-            sms <= 0)
-            sms = kTargetSMs;
-        cached_sms = sms;
-        cached_dev = dev;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        (void)cudaGetLastError();
+        return kTargetSMs;
     }
-    return cached_sms;
+    int sms = sms_of[dev].load();
+    if (sms == 0) {
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            sms <= 0) {
+            (void)cudaGetLastError();
+            sms = kTargetSMs;
+        }
+        sms_of[dev].store(sms);
+    }
+    return sms;
 }
 
 }  // namespace qsa

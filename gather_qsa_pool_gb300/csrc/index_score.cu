@@ -119,14 +119,8 @@ cudaError_t launch_stream(const float *q, int64_t ld_q, const int32_t *q_pos, co
                           int64_t n_rows, float scale, float *scores, int64_t ld_s,
                           const ScoreSide &side, cudaStream_t st)
 {
-    static int blocks_per_sm = 0;
     auto k = score_stream_kernel<TP, CH, NQ, R>;
-    if (blocks_per_sm == 0) {
-        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks_per_sm, k,
-                                                                      kScoreThreads, 0);
-        if (e != cudaSuccess) return e;
-        if (blocks_per_sm < 1) blocks_per_sm = 1;
-    }
+    const int blocks_per_sm = occupancy_blocks<score_stream_kernel<TP, CH, NQ, R>>(kScoreThreads, 0);
     const int64_t warps_needed = (n_rows + R - 1) / R;
     int64_t grid = (int64_t)device_sm_count() * blocks_per_sm;
     const int64_t grid_needed = (warps_needed + kScoreThreads / 32 - 1) / (kScoreThreads / 32);

@@ -201,6 +201,26 @@ cudaError_t ensure_kernel_attrs(size_t smem, bool nonportable_cluster = false)
     return e;
 }
 
+// Resident CTAs of Kernel per SM for `threads` threads and `smem` dynamic bytes, on the
+// current device (asked once per device; at least 1).
+template <auto Kernel>
+int occupancy_blocks(int threads, size_t smem)
+{
+    constexpr int kMaxDevices = 64;
+    static std::atomic<int> blocks_of[kMaxDevices];  // 0: not yet asked
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) dev = -1;
+    int b = dev >= 0 ? blocks_of[dev].load() : 0;
+    if (b > 0) return b;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, Kernel, threads, smem) != cudaSuccess) {
+        (void)cudaGetLastError();
+        b = 1;
+    }
+    if (b < 1) b = 1;
+    if (dev >= 0) blocks_of[dev].store(b);
+    return b;
+}
+
 // ------------------------------------------------------------------ RoPE frequencies
 // Inverse frequencies theta_i = base^(-2i/d), i < d/2, computed on the host in fp64 and
 // passed by value as a kernel parameter.

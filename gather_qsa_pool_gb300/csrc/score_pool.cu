@@ -68,13 +68,8 @@ cudaError_t launch_fused(const float *q, void *pooled, int H, int d, float scale
                          const RopeTable &tab, cudaStream_t st)
 {
     constexpr int R = stream_rows<TP, NQ>();
-    static int blocks_per_sm = 0;
     auto k = score_pool_kernel<T, TP, NQ>;
-    if (blocks_per_sm == 0) {
-        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks_per_sm, k, kThreads, 0);
-        if (e != cudaSuccess) return e;
-        if (blocks_per_sm < 1) blocks_per_sm = 1;
-    }
+    const int blocks_per_sm = occupancy_blocks<score_pool_kernel<T, TP, NQ>>(kThreads, 0);
     const int n_pool = (int)(pf.row1 - pf.row0);
     int64_t grid = (int64_t)device_sm_count() * blocks_per_sm;
     const int64_t warps_needed = (pf.row0 + R - 1) / R;
