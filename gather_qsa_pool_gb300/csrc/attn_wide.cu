@@ -86,20 +86,6 @@ attn_wide_kernel(const float *__restrict__ q, int H_q, int H_kv, float scale_log
     QSA_AFTER_WAIT(n_cells);
     pdl_trigger();
 
-    // the query: rows 0-15 = bf16(q * scale), rows 16-31 = bf16 of the remainder
-    {
-        const float *qh = q + (qi * H_q + (int64_t)g * G) * DK;
-        for (int e = tid; e < G * DK / 2; e += NT) {
-            const int h = (2 * e) / DK, c = 2 * e - h * DK;
-            const float2 x = *reinterpret_cast<const float2 *>(qh + (int64_t)h * DK + c);
-            float h0, l0, h1, l1;
-            split_bf16(x.x * scale_log2, h0, l0);
-            split_bf16(x.y * scale_log2, h1, l1);
-            *reinterpret_cast<uint32_t *>(Qs + h * LD + c) = pack_bf16(h0, h1);
-            *reinterpret_cast<uint32_t *>(Qs + (G + h) * LD + c) = pack_bf16(l0, l1);
-        }
-    }
-
     // this split's cells; positions of its first two stages load with the list length
     const int64_t chunk = (max_cells + S - 1) / S;
     const int64_t c0 = (int64_t)s_idx * chunk;
@@ -167,6 +153,22 @@ attn_wide_kernel(const float *__restrict__ q, int H_q, int H_kv, float scale_log
 
     if (ntiles > 0) copy_rows(0);
     if (ntiles > 1) copy_rows(1);
+    // the query, while the first rows are in flight: rows 0-15 = bf16(q * scale), rows 16-31
+    // = bf16 of the remainder
+    {
+        const float *qh = q + (qi * H_q + (int64_t)g * G) * DK;
+#pragma unroll 3
+        for (int e = tid; e < G * DK / 2; e += NT) {
+            const int h = (2 * e) / DK, c = 2 * e - h * DK;
+            const float2 x = *reinterpret_cast<const float2 *>(qh + (int64_t)h * DK + c);
+            float h0, l0, h1, l1;
+            split_bf16(x.x * scale_log2, h0, l0);
+            split_bf16(x.y * scale_log2, h1, l1);
+            *reinterpret_cast<uint32_t *>(Qs + h * LD + c) = pack_bf16(h0, h1);
+            *reinterpret_cast<uint32_t *>(Qs + (G + h) * LD + c) = pack_bf16(l0, l1);
+        }
+    }
+    __syncthreads();  // the query images are complete
     for (int it = 0; it < ntiles; ++it) {
         const int buf = it & 1;
         if (it >= 1 && it + 1 < ntiles) {
