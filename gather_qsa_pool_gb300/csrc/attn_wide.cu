@@ -157,13 +157,19 @@ attn_wide_kernel(const float *__restrict__ q, int H_q, int H_kv, float scale_log
     // = bf16 of the remainder
     {
         const float *qh = q + (qi * H_q + (int64_t)g * G) * DK;
-#pragma unroll 3
-        for (int e = tid; e < G * DK / 2; e += NT) {
+        constexpr int kPer = G * DK / 2 / NT;  // float pairs per thread, all loaded at once
+        static_assert(kPer * NT * 2 == G * DK, "the query splits evenly over the threads");
+        float2 x[kPer];
+#pragma unroll
+        for (int k = 0; k < kPer; ++k)
+            x[k] = *reinterpret_cast<const float2 *>(qh + 2 * (int64_t)(tid + k * NT));
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+            const int e = tid + k * NT;
             const int h = (2 * e) / DK, c = 2 * e - h * DK;
-            const float2 x = *reinterpret_cast<const float2 *>(qh + (int64_t)h * DK + c);
             float h0, l0, h1, l1;
-            split_bf16(x.x * scale_log2, h0, l0);
-            split_bf16(x.y * scale_log2, h1, l1);
+            split_bf16(x[k].x * scale_log2, h0, l0);
+            split_bf16(x[k].y * scale_log2, h1, l1);
             *reinterpret_cast<uint32_t *>(Qs + h * LD + c) = pack_bf16(h0, h1);
             *reinterpret_cast<uint32_t *>(Qs + (G + h) * LD + c) = pack_bf16(l0, l1);
         }
@@ -316,58 +322,63 @@ attn_wide_kernel(const float *__restrict__ q, int H_q, int H_kv, float scale_log
         return;
     }
 
-    // cluster combine: CTA s owns outputs [s*per, (s+1)*per) of G*DV; four threads per output
+    // cluster combine: CTA s owns outputs [s*per, (s+1)*per) of G*DV.  First the weights of
+    // the heads in that slice (one round of remote loads of every split's maximum and sum),
+    // then every output sums its S partials, all S remote loads in flight at once.
     cg::cluster_group cluster = cg::this_cluster();
     cluster.sync();
     const int per = (G * DV + S - 1) / S;
-    const int part = tid & 3;
-    for (int base = s_idx * per; base < (s_idx + 1) * per; base += NT / 4) {
-        const int e0 = base + (tid >> 2);
-        const bool live = e0 < (s_idx + 1) * per && e0 < G * DV;
-        const int e = live ? e0 : 0;
-        const int h = e / DV, c = e - h * DV;
-        constexpr int RQ = kWMaxCluster / 4;
-        float mv[RQ], lv[RQ], ov[RQ];
+    const int e_begin = s_idx * per, e_end = min((s_idx + 1) * per, G * DV);
+    const int h_first = e_begin / DV;
+    const int nh = e_end > e_begin ? (e_end - 1) / DV - h_first + 1 : 0;
+    // the query images are no longer read: their space holds the weights
+    float *wf = reinterpret_cast<float *>(Qs);   // [nh][kWMaxCluster] split weights
+    float *wm = wf + G * kWMaxCluster;           // [nh][kWMaxCluster] split maxima, then [nh] M
+    float *hM = wm + G * kWMaxCluster;           // [nh] head maximum
+    float *hL = hM + G;                          // [nh] head weight sum (< 0: a lost stage)
+    for (int x = tid; x < nh * S; x += NT) {
+        const int hh = x / S, r = x - hh * S;
+        const int h = h_first + hh;
+        wm[hh * kWMaxCluster + r] = cluster.map_shared_rank(run_m, r)[h];
+        wf[hh * kWMaxCluster + r] = cluster.map_shared_rank(run_l, r)[h];
+    }
+    __syncthreads();
+    if (tid < nh) {
         float M = -INFINITY;
-#pragma unroll
-        for (int j = 0; j < RQ; ++j) {
-            const int r = part + 4 * j;
-            mv[j] = -INFINITY;
-            lv[j] = ov[j] = 0.0f;
-            if (r < S) {
-                mv[j] = cluster.map_shared_rank(run_m, r)[h];
-                lv[j] = cluster.map_shared_rank(run_l, r)[h];
-                ov[j] = cluster.map_shared_rank(ost, r)[h * kWOLD + c];
-            }
-            M = fmaxf(M, mv[j]);
-        }
         bool bad = false;
-#pragma unroll
-        for (int j = 0; j < RQ; ++j) bad = bad || lv[j] < 0.0f;
-        bad = __any_sync(0xffffffffu, bad && live) || overflow;
-        M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 1));
-        M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 2));
-        float acc = 0.0f, L = 0.0f;
-        if (M != -INFINITY) {
-#pragma unroll
-            for (int j = 0; j < RQ; ++j) {
-                const float f = exp2f(mv[j] - M);
-                acc = fmaf(f, ov[j], acc);
-                L = fmaf(f, lv[j], L);
-            }
+        for (int r = 0; r < S; ++r) {
+            M = fmaxf(M, wm[tid * kWMaxCluster + r]);
+            bad = bad || wf[tid * kWMaxCluster + r] < 0.0f;
         }
-        acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-        acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-        L += __shfl_xor_sync(0xffffffffu, L, 1);
-        L += __shfl_xor_sync(0xffffffffu, L, 2);
-        if (part == 0 && live) {
-            float v = L > 0.0f ? acc / L : 0.0f;
-            if (bad) v = __int_as_float(0x7fc00000);
-            out[(qi * H_q + (int64_t)g * G + h) * DV + c] = v;
-            if (lse && c == 0)
-                lse[qi * H_q + g * G + h] = bad ? __int_as_float(0x7fc00000)
-                                           : (L > 0.0f ? (M + log2f(L)) * kLn2 : -INFINITY);
+        float L = 0.0f;
+        for (int r = 0; r < S; ++r) {
+            const float f = M != -INFINITY ? exp2f(wm[tid * kWMaxCluster + r] - M) : 0.0f;
+            L = fmaf(f, wf[tid * kWMaxCluster + r], L);
+            wf[tid * kWMaxCluster + r] = f;
         }
+        hM[tid] = M;
+        hL[tid] = bad ? -1.0f : L;
+    }
+    __syncthreads();
+    for (int e = e_begin + tid; e < e_end; e += NT) {
+        const int h = e / DV, c = e - h * DV, hh = h - h_first;
+        const float *f = wf + hh * kWMaxCluster;
+        float ov[kWMaxCluster];
+#pragma unroll
+        for (int r = 0; r < kWMaxCluster; ++r)
+            ov[r] = r < S ? cluster.map_shared_rank(ost, r)[h * kWOLD + c] : 0.0f;
+        float acc = 0.0f;
+#pragma unroll
+        for (int r = 0; r < kWMaxCluster; ++r)
+            if (r < S) acc = fmaf(f[r], ov[r], acc);
+        const float L = hL[hh];
+        const bool bad = L < 0.0f || overflow;
+        float v = L > 0.0f ? acc / L : 0.0f;
+        if (bad) v = __int_as_float(0x7fc00000);
+        out[(qi * H_q + (int64_t)g * G + h) * DV + c] = v;
+        if (lse && c == 0)
+            lse[qi * H_q + g * G + h] = bad ? __int_as_float(0x7fc00000)
+                                       : (L > 0.0f ? (hM[hh] + log2f(L)) * kLn2 : -INFINITY);
     }
     cluster.sync();  // keep this CTA's state alive until every remote read is done
     drain();
