@@ -210,6 +210,68 @@ __device__ __forceinline__ void for_each_key_at_least(const float *__restrict__ 
     }
 }
 
+// The sampled form's candidate pass over a 16-byte aligned row (T > kKeyNegInf): every
+// score >= key_float(T) goes to the candidate list (key, block), slots past cap counted
+// but not stored.  Each round a thread loads U vectors, folds them into a 4U-bit hit mask
+// and lets them die; a warp scan and one shared atomic per warp reserve the round's slots;
+// the hits are then read again (lines just fetched) and stored.  Keeping the vectors live
+// across the stores (a lambda per hit) measured 9.8 us per 64k-block row against 5.6 us
+// this way.  All threads of the CTA call it; the round loop is uniform (full-warp shuffles).
+__device__ __forceinline__ void collect_at_least(const float *__restrict__ row, int64_t n,
+                                                 uint32_t T, uint32_t *counter,
+                                                 uint32_t *cand_key, int32_t *cand_idx,
+                                                 uint32_t cap)
+{
+    constexpr int U = 8;
+    const float lo = key_float(T);
+    const int lane = threadIdx.x & 31;
+    const int n4 = (int)(n / 4);  // n <= kMaxN: int indices
+    const float4 *r4 = reinterpret_cast<const float4 *>(row);
+    const float4 pad = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);  // < lo
+    for (int b0 = 0; b0 < n4; b0 += NT * U) {
+        float4 v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int i = b0 + (int)threadIdx.x + u * NT;
+            v[u] = i < n4 ? r4[i] : pad;
+        }
+        uint32_t hit = 0;
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            hit |= ((uint32_t)(v[u].x >= lo) | ((uint32_t)(v[u].y >= lo) << 1) |
+                    ((uint32_t)(v[u].z >= lo) << 2) | ((uint32_t)(v[u].w >= lo) << 3)) << (4 * u);
+        const uint32_t c = __popc(hit);
+        uint32_t inc = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xffffffffu, inc, o);
+            if (lane >= o) inc += y;
+        }
+        const uint32_t tot = __shfl_sync(0xffffffffu, inc, 31);
+        uint32_t s = 0;
+        if (lane == 31 && tot) s = atomicAdd(counter, tot);
+        s = __shfl_sync(0xffffffffu, s, 31) + inc - c;
+        while (hit) {
+            const int bit = __ffs(hit) - 1;
+            hit &= hit - 1;
+            const int b = 4 * (b0 + (int)threadIdx.x + (bit >> 2) * NT) + (bit & 3);
+            if (s < cap) {
+                cand_key[s] = score_key(row[b]);
+                cand_idx[s] = b;
+            }
+            ++s;
+        }
+    }
+    for (int64_t i = 4 * (int64_t)n4 + threadIdx.x; i < n; i += NT)
+        if (row[i] >= lo) {
+            const uint32_t slot = atomicAdd(counter, 1u);
+            if (slot < cap) {
+                cand_key[slot] = score_key(row[i]);
+                cand_idx[slot] = (int32_t)i;
+            }
+        }
+}
+
 // Step 5 of the general form: fold the ties (lowest index first, k_rem of them) into the
 // selected bitmap, then write the selected blocks in ascending order.
 __device__ void write_selection(uint32_t *selw, const uint32_t *eqw, int64_t nw, uint32_t k_rem,
@@ -441,8 +503,12 @@ __device__ bool topk_query_sampled(const float *srow, int64_t n, int64_t k, int3
             }
         }
     };
-    if (T > kKeyNegInf) for_each_key_at_least(srow, n, T, keep);
-    else for_each_key(srow, n, keep);
+    if (T > kKeyNegInf && (reinterpret_cast<uintptr_t>(srow) & 15) == 0)
+        collect_at_least(srow, n, T, &misc[8], cand_key, cand_idx, (uint32_t)cand_cap);
+    else if (T > kKeyNegInf)
+        for_each_key_at_least(srow, n, T, keep);
+    else
+        for_each_key(srow, n, keep);
     __syncthreads();
     const uint32_t m = misc[8];
     if (m < (uint32_t)k || m > (uint32_t)cand_cap) return false;  // uniform

@@ -196,6 +196,23 @@ def test_topk_large_rows_many_queries(case):
         np.testing.assert_array_equal(g_blocks[i, :g_counts[i]], want)
 
 
+def test_topk_sampled_form_on_unaligned_rows():
+    """Rows 40,001 scores apart (row i starts 4i bytes past a 16-byte boundary, mod 16):
+    the sampled candidate pass takes its vector form on the aligned rows and its scalar
+    form on the others.  Exact against the oracle; a ragged column count (n mod 4 = 1)."""
+    rng = np.random.default_rng(77)
+    n_q, n_full, k = 6, 40001, 512
+    s = (4 * rng.standard_normal((n_q, n_full))).astype(np.float32)
+    blocks = torch.full((n_q, k), -3, dtype=torch.int32, device="cuda")
+    counts = torch.zeros(n_q, dtype=torch.int32, device="cuda")
+    qsa.topk_blocks(to_dev(s), n_full, k, blocks, counts)
+    g_blocks, g_counts = to_host(blocks), to_host(counts)
+    for i in range(n_q):
+        want = _oracle_topk_on_f32(s[i], n_full, k)
+        assert g_counts[i] == k
+        np.testing.assert_array_equal(g_blocks[i], want)
+
+
 @pytest.mark.parametrize("case", ["normal", "equal", "few_levels", "heavy_tail", "narrow"])
 def test_topk_many_queries(case):
     """A prefill-sized query count (more than two per SM: the general kernel's
