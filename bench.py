@@ -385,10 +385,40 @@ def run_context(name, args, world, rank, local, want_clocks, pooled="f32", n_q=1
     return res
 
 
+def graph_time_us(fns, reps, dev):
+    """Device time per repetition of the calls fns (in order), captured reps times into one
+    CUDA graph and replayed after a warm-up replay: the kernels' time, not the Python
+    wrappers' issue time."""
+    import torch
+
+    gs = torch.cuda.Stream(device=dev)
+    for fn in fns:
+        fn()
+    torch.cuda.synchronize()
+    gs.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(gs):
+        with torch.cuda.graph(graph, stream=gs):
+            for _ in range(reps):
+                for fn in fns:
+                    fn()
+    torch.cuda.synchronize()
+    graph.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    graph.replay()
+    b.record()
+    torch.cuda.synchronize()
+    del graph
+    return a.elapsed_time(b) * 1e3 / reps
+
+
 def run_prefill(args, local, pooled_kind="f32"):
-    """The prefill chunk: 1024 queries after 255,181 tokens.  Times (CUDA events, after a
+    """The prefill chunk: 1024 queries after 255,181 tokens.  Times (CUDA-graph replays after a
     warm-up) the tensor-core score contraction, the per-query top-k, the cell lists and the
-    gathered attention; returns per-kernel microseconds and the score kernel's TFLOP/s.
+    gathered attention, one at a time and as one chained chunk; returns per-kernel
+    microseconds, the chunk's and the score kernel's TFLOP/s.
     pooled_kind "bf16": the pooled cache is stored in bf16 and the contraction reads it in
     place (no conversion pass)."""
     import torch
@@ -433,15 +463,24 @@ def run_prefill(args, local, pooled_kind="f32"):
         for _, fn in calls:
             fn()
     torch.cuda.synchronize()
-    res = {}
-    for name, fn in calls:
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        for _ in range(args.prefill_reps):
-            fn()
-        b.record()
+    # each kernel's calls captured into a CUDA graph and replayed (device time), then the
+    # whole chunk as one graph; plain CUDA events around direct calls if capture fails
+    res, timing, chunk_graph = {}, "cuda graph replay", None
+    try:
+        for name, fn in calls:
+            res[name] = graph_time_us([fn], args.prefill_reps, dev)
+        chunk_graph = graph_time_us([fn for _, fn in calls], args.prefill_reps, dev)
+    except Exception as e:  # noqa: BLE001 -- reported in the JSON line
+        timing = f"cuda events around direct calls (graph capture failed: {type(e).__name__})"
         torch.cuda.synchronize()
-        res[name] = a.elapsed_time(b) * 1e3 / args.prefill_reps
+        for name, fn in calls:
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            for _ in range(args.prefill_reps):
+                fn()
+            b.record()
+            torch.cuda.synchronize()
+            res[name] = a.elapsed_time(b) * 1e3 / args.prefill_reps
     flops = 2.0 * n_q * n_rows * H * d
     attn_flops = 2.0 * 2.0 * n_q * shape.H_q * shape.d * float(n_cells.float().mean().item())
     out_d = {
@@ -450,9 +489,11 @@ def run_prefill(args, local, pooled_kind="f32"):
                      f"attention {shape.H_q}/{shape.H_kv}x{shape.d} bf16"),
         "us": {k: round(v, 1) for k, v in res.items()},
         "chunk_us": round(sum(res.values()), 1),
+        "chunk_graph_us": None if chunk_graph is None else round(chunk_graph, 1),
+        "timing": timing,
         "score_tc_tflops": flops / (res["score_tc"] * 1e-6) / 1e12,
         "attn_tflops": attn_flops / (res["attn"] * 1e-6) / 1e12,
-        "tokens_per_s": n_q / (sum(res.values()) * 1e-6),
+        "tokens_per_s": n_q / ((chunk_graph or sum(res.values())) * 1e-6),
     }
     del inp, pooled, scores, ws, pos, out, aws
     torch.cuda.empty_cache()
@@ -511,28 +552,7 @@ def run_ablation(args, local):
     ]
     # each piece captured (reps calls) into a CUDA graph and replayed, so the device time is
     # measured rather than the Python wrapper's issue time
-    res = {}
-    reps = 5
-    gs = torch.cuda.Stream(device=dev)
-    for name, fn in pieces:
-        fn()
-        torch.cuda.synchronize()
-        gs.wait_stream(torch.cuda.current_stream())
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.stream(gs):
-            with torch.cuda.graph(graph, stream=gs):
-                for _ in range(reps):
-                    fn()
-        torch.cuda.synchronize()
-        graph.replay()
-        torch.cuda.synchronize()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        graph.replay()
-        b.record()
-        torch.cuda.synchronize()
-        res[name] = round(a.elapsed_time(b) * 1e3 / reps, 1)
-        del graph
+    res = {name: round(graph_time_us([fn], 5, dev), 1) for name, fn in pieces}
     n_listed = int(lay.n_cells[0].item())
     out_d = {
         "workload": (f"one layer at {n_ctx:,} tokens: {n_rows:,} pooled rows, {n_listed} listed "

@@ -458,15 +458,17 @@ __device__ void topk_query(const float *srow, int64_t n, int64_t k, int32_t *out
 }
 
 // The general form for one query when n is large and no histogram comes with the scores:
-// a strided sample of 1024 keys sets a threshold T at the 12-bit digit that holds the
-// sample's r-th largest key (r a margin above the k/n share); one pass keeps every key >= T
+// a strided sample (1024 positions over the row's capacity n_cap, the ones below n kept)
+// sets a threshold T at the 12-bit digit that holds the sample's r-th largest key (r a
+// margin above the k/n share); one pass keeps every key >= T
 // as a candidate (the top k are among them whenever at least k are); the candidates are
 // then selected exactly: first 12-bit digit, second 8-bit digit, and a (key, index) rank
 // inside the last bin.  Returns false (nothing written) when the sample missed -- fewer
 // than k or more than cand_cap candidates -- and the caller runs topk_query instead.
 // smem: the layout of topk_query.
 __device__ bool topk_query_sampled(const float *srow, int64_t n, int64_t k, int32_t *out,
-                                   int32_t *pout, bool pvec, int cand_cap, uint32_t *smem)
+                                   int32_t *pout, bool pvec, int cand_cap, uint32_t *smem,
+                                   float sample, int64_t n_cap)
 {
     uint32_t *hist = smem;
     uint32_t *warp_s = hist + kBins1;
@@ -477,18 +479,18 @@ __device__ bool topk_query_sampled(const float *srow, int64_t n, int64_t k, int3
     int32_t *cand_idx = reinterpret_cast<int32_t *>(cand_key + cand_cap);
     const int tid = threadIdx.x, lane = tid & 31;
 
-    // ---- 1. the sample's histogram and the threshold digit
+    // ---- 1. the sample's histogram and the threshold digit.  sample: this thread's score at
+    // (tid * n_cap) >> 10, loaded by the caller before the query's block count n was known;
+    // the ns samples below n stand for the row (ns >= 1: thread 0 samples block 0).
     for (int i = tid; i < kBins1; i += NT) hist[i] = 0u;
     for (int64_t w = tid; w < nw; w += NT) selw[w] = 0u;
     if (tid == 0) misc[8] = 0u;
     __syncthreads();
-    {
-        const int64_t i = ((int64_t)tid * n) >> 10;  // NT = 1024 samples, strided
-        atomicAdd(&hist[score_key(srow[i]) >> (32 - kTopkHistBits)], 1u);
-    }
-    __syncthreads();
-    int64_t r = (k * 1024 + n - 1) / n + 8;
-    if (r > NT) r = NT;
+    const bool in_row = (((int64_t)tid * n_cap) >> 10) < n;
+    if (in_row) atomicAdd(&hist[score_key(sample) >> (32 - kTopkHistBits)], 1u);
+    const int64_t ns = __syncthreads_count(in_row);
+    int64_t r = (k * ns + n - 1) / n + 8;
+    if (r > ns) r = ns;
     find_bucket(hist, kBins1, (uint32_t)r, warp_s, misc);
     const uint32_t T = misc[0] << (32 - kTopkHistBits);
     __syncthreads();
@@ -606,6 +608,11 @@ topk_kernel(const float *__restrict__ scores, int64_t ld, const int32_t *__restr
     QSA_AFTER_WAIT(q_pos);
     QSA_AFTER_WAIT(ext_hist);
     pdl_trigger();
+    // the sampled form's strided sample over the row's capacity, in flight while the query's
+    // position is read (samples past its own block count are dropped there)
+    const float sample = (!ext_hist && n_full_cap >= kSampledMinN)
+                             ? scores[qi * ld + (((int64_t)threadIdx.x * n_full_cap) >> 10)]
+                             : 0.0f;
 
     // the query's position: q_pos[qi], else n_ctx - 1 - p_step * (n_q - 1 - qi) (the last
     // n_q tokens of the context when p_step = 1; every query at n_ctx - 1 when it is 0)
@@ -633,7 +640,8 @@ topk_kernel(const float *__restrict__ scores, int64_t ld, const int32_t *__restr
         return;
     }
     if (!ehist && n >= kSampledMinN &&
-        topk_query_sampled(scores + qi * ld, n, k, out, pout, pvec, cand_cap, smem))
+        topk_query_sampled(scores + qi * ld, n, k, out, pout, pvec, cand_cap, smem, sample,
+                           n_full_cap))
         return;
     topk_query(scores + qi * ld, n, k, out, pout, pvec, ehist, cand_cap, smem);
 }
