@@ -20,6 +20,7 @@ from ._binding import (  # noqa: F401
     index_score,
     index_score_workspace_size,
     load,
+    mask_sparse_attn,
     mask_sparse_eligible,
     mask_to_list,
     pool_update,

@@ -62,6 +62,8 @@ _SIGNATURES = {
     "qsa_decode_plan_step_host": (_int, [_p, _i64, _i64, _i64, _p, _p, _p, _p]),
     "qsa_mask_to_list": (_int, [_p, _i64, _i64, _i64, _i64, _p, _p, _p, _p]),
     "qsa_mask_sparse_eligible": (_int, [_int, _f, _f, _i64, _i64]),
+    "qsa_mask_sparse_attn": (_int, [_p, _i64, _int, _int, _int, _int, _f, _p, _int, _i64, _i64,
+                                    _p, _i64, _i64, _p, _p, _p, _p]),
 }
 
 _lib = None
@@ -297,6 +299,17 @@ def mask_to_list(mask, max_list, pos_out, counts_out, bits_out=None, n_kv=None, 
     _check("qsa_mask_to_list", load().qsa_mask_to_list(
         _ptr(mask), n_rows, n_kv, _ld(mask), max_list, _ptr(pos_out), _ptr(counts_out),
         _ptr(bits_out), _stream(stream)))
+
+
+def mask_sparse_attn(q, KV, mask, max_list, out, scale, counts_out=None, lse=None, n_kv=None,
+                     d_k=576, d_v=512, stream=None):
+    """qsa_mask_sparse_attn: q [n_q][16][576] fp32 over the set positions of each query's
+    mask row (mask [n_q][ld] uint8), the latent KV rows [n_kv][ld] bf16."""
+    n_q, H_q = q.shape[0], q.shape[1]
+    n_kv = KV.shape[0] if n_kv is None else n_kv
+    _check("qsa_mask_sparse_attn", load().qsa_mask_sparse_attn(
+        _ptr(q), n_q, H_q, 1, d_k, d_v, scale, _ptr(KV), _dtype(KV), n_kv, _ld(KV), _ptr(mask),
+        _ld(mask), max_list, _ptr(counts_out), _ptr(out), _ptr(lse), _stream(stream)))
 
 
 def mask_sparse_eligible(has_mask, max_bias, softcap, n_kv, max_list) -> bool:

@@ -1133,7 +1133,7 @@ cudaError_t launch_sparse_attn(const float *q, int64_t n_q, int H_q, int H_kv, i
     if (attn_uses_rows4(dt, n_q, H_q, H_kv, d_k, d_v, K, V, ld_k, ld_v, pos, max_cells))
         return launch_attn_rows4(q, n_q, H_q, scale, K, V, n_kv, ld_k, ld_v, pos, n_cells,
                                  max_cells, out, lse, st);
-    if (attn_uses_wide(dt, d_k, d_v, G, K, V, ld_k, ld_v))
+    if (H_kv == 1 && attn_uses_wide(dt, d_k, d_v, G, K, V, ld_k, ld_v))  // one latent KV head
         return launch_attn_wide(q, n_q, H_q, H_kv, scale, K, n_kv, ld_k, pos, n_cells, max_cells,
                                 out, lse, st);
     if (attn_uses_mma(dt, d_k, d_v, G))

@@ -46,11 +46,119 @@ constexpr size_t kWSmem = kWQBytes + 2 * kWStageBytes + kWPBytes;
 static_assert((size_t)kWG * kWOLD * 4 <= 2 * kWStageBytes, "output state fits the stages");
 static_assert(kWQBytes % 16 == 0 && kWStageBytes % 16 == 0, "16-byte aligned regions");
 
+// Mask mode: the mask row's 64-bit ballot words (bit t of word w: position 64w + t is set)
+// and their exclusive prefix counts, built by every CTA of the query in shared memory; the
+// list index L is the L-th set position in ascending order, the list the separate
+// mask-to-list call writes.  Rows of up to kWMaskWords * 64 positions.
+constexpr int kWMaskWords = 1024;
+constexpr int kWWordsPerThread = kWMaskWords / kWNT;  // 4
+
+// Builds words[0, nw) and pre[0, nw) of one mask row (all threads call it); returns the
+// row's set-position count.  Thread t owns words [t * wpt, (t + 1) * wpt).
+__device__ int64_t build_mask_words(const uint8_t *__restrict__ row, int64_t n_kv,
+                                    unsigned long long *words, uint32_t *pre, uint32_t *wsum)
+{
+    constexpr int NT = kWNT;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nw = (int)((n_kv + 63) / 64);
+    const int wpt = (nw + NT - 1) / NT;  // <= kWWordsPerThread
+    const int w0 = tid * wpt;
+    unsigned long long wv[kWWordsPerThread];
+    const bool vec = n_kv % 64 == 0 && (reinterpret_cast<uintptr_t>(row) & 15) == 0;
+    if (vec) {
+        // whole words: four 16-byte loads per word, all of the thread's loads in flight
+        uint4 u[kWWordsPerThread][4];
+#pragma unroll
+        for (int i = 0; i < kWWordsPerThread; ++i)
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                u[i][k] = (i < wpt && w0 + i < nw)
+                              ? reinterpret_cast<const uint4 *>(row + 64 * (int64_t)(w0 + i))[k]
+                              : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int i = 0; i < kWWordsPerThread; ++i) {
+            unsigned long long w = 0;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                w |= (unsigned long long)nonzero_byte_bits(u[i][k].x) << (16 * k);
+                w |= (unsigned long long)nonzero_byte_bits(u[i][k].y) << (16 * k + 4);
+                w |= (unsigned long long)nonzero_byte_bits(u[i][k].z) << (16 * k + 8);
+                w |= (unsigned long long)nonzero_byte_bits(u[i][k].w) << (16 * k + 12);
+            }
+            wv[i] = w;
+        }
+    } else {
+        // a ragged or unaligned row: byte loads, positions past n_kv read as zero
+#pragma unroll
+        for (int i = 0; i < kWWordsPerThread; ++i) {
+            unsigned long long w = 0;
+            if (i < wpt && w0 + i < nw) {
+                const int64_t p0 = 64 * (int64_t)(w0 + i);
+                uint8_t b[64];
+#pragma unroll
+                for (int t = 0; t < 64; ++t) b[t] = p0 + t < n_kv ? row[p0 + t] : (uint8_t)0;
+#pragma unroll
+                for (int t = 0; t < 64; ++t) w |= (unsigned long long)(b[t] != 0) << t;
+            }
+            wv[i] = w;
+        }
+    }
+    // exclusive scan of the per-thread counts (threads own consecutive words)
+    uint32_t c = 0;
+#pragma unroll
+    for (int i = 0; i < kWWordsPerThread; ++i) c += __popcll(wv[i]);
+    uint32_t x = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) wsum[warp] = x;
+    __syncthreads();
+    uint32_t before = 0, total = 0;
+#pragma unroll
+    for (int k = 0; k < NT / 32; ++k) {
+        before += k < warp ? wsum[k] : 0u;
+        total += wsum[k];
+    }
+    uint32_t run = before + x - c;
+#pragma unroll
+    for (int i = 0; i < kWWordsPerThread; ++i)
+        if (i < wpt && w0 + i < nw) {
+            words[w0 + i] = wv[i];
+            pre[w0 + i] = run;
+            run += __popcll(wv[i]);
+        }
+    __syncthreads();
+    return total;
+}
+
+// The L-th set position (L < the row's count): the last word whose prefix is <= L holds it.
+__device__ __forceinline__ int64_t mask_position(const unsigned long long *words,
+                                                 const uint32_t *pre, int nw, uint32_t L)
+{
+    int lo = 0, hi = nw - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (pre[mid] <= L) lo = mid;
+        else hi = mid - 1;
+    }
+    const unsigned long long w = words[lo];
+    int j = (int)(L - pre[lo]);
+    const uint32_t w_lo = (uint32_t)w;
+    const int c_lo = __popc(w_lo);
+    const int bit = j < c_lo ? select_set_bit(w_lo, j) : 32 + select_set_bit((uint32_t)(w >> 32), j - c_lo);
+    return 64 * (int64_t)lo + bit;
+}
+
+template <bool kMask>
 __global__ void __launch_bounds__(kWNT, 1)
 attn_wide_kernel(const float *__restrict__ q, int H_q, int H_kv, float scale_log2,
                  const __nv_bfloat16 *__restrict__ KV, int64_t n_kv, int64_t ld,
                  const int32_t *__restrict__ pos, const int32_t *__restrict__ n_cells,
-                 int64_t max_cells, float *__restrict__ out, float *__restrict__ lse)
+                 int64_t max_cells, float *__restrict__ out, float *__restrict__ lse,
+                 const uint8_t *__restrict__ mask, int64_t ld_mask,
+                 int32_t *__restrict__ counts_out)
 {
     constexpr int G = kWG, DK = kWDK, DV = kWDV, TC = kWTC, LD = kWLD, NT = kWNT;
     extern __shared__ __align__(16) char smem_raw[];
@@ -84,16 +192,29 @@ attn_wide_kernel(const float *__restrict__ q, int H_q, int H_kv, float scale_log
     QSA_AFTER_WAIT(KV);
     QSA_AFTER_WAIT(pos);
     QSA_AFTER_WAIT(n_cells);
+    QSA_AFTER_WAIT(mask);
     pdl_trigger();
 
     // this split's cells; positions of its first two stages load with the list length
     const int64_t chunk = (max_cells + S - 1) / S;
     const int64_t c0 = (int64_t)s_idx * chunk;
     const int64_t c1max = c0 + chunk < max_cells ? c0 + chunk : max_cells;
-    int64_t n = n_cells[qi];
+    __shared__ unsigned long long mwords[kMask ? kWMaskWords : 1];
+    __shared__ uint32_t mpre[kMask ? kWMaskWords : 1];
+    __shared__ uint32_t mwsum[kWWarps];
+    const int mnw = (int)((n_kv + 63) / 64);
+    int64_t n;
     int64_t first_row = -1;
-    if (tid < 2 * TC && c0 + tid < c1max)
-        first_row = pos ? (int64_t)pos[qi * max_cells + c0 + tid] : qi * max_cells + c0 + tid;
+    if constexpr (kMask) {
+        n = build_mask_words(mask + qi * ld_mask, n_kv, mwords, mpre, mwsum);
+        if (counts_out && s_idx == 0 && g == 0 && tid == 0) counts_out[qi] = (int32_t)n;
+        if (tid < 2 * TC && c0 + tid < c1max && c0 + tid < n)
+            first_row = mask_position(mwords, mpre, mnw, (uint32_t)(c0 + tid));
+    } else {
+        n = n_cells[qi];
+        if (tid < 2 * TC && c0 + tid < c1max)
+            first_row = pos ? (int64_t)pos[qi * max_cells + c0 + tid] : qi * max_cells + c0 + tid;
+    }
     const bool overflow = n > max_cells;  // truncated list: the result must not be used
     if (overflow || n < 0) n = 0;
     const int64_t c1 = c1max < n ? c1max : n;
@@ -115,7 +236,8 @@ attn_wide_kernel(const float *__restrict__ q, int H_q, int H_kv, float scale_log
             int64_t row = -1;
             if (tid < tc) {
                 const int64_t cell = base + tid;
-                row = pos ? (int64_t)pos[qi * max_cells + cell] : qi * max_cells + cell;
+                if constexpr (kMask) row = mask_position(mwords, mpre, mnw, (uint32_t)cell);
+                else row = pos ? (int64_t)pos[qi * max_cells + cell] : qi * max_cells + cell;
                 if (row < 0 || row >= n_kv) row = -1;
             }
             rows[buf * TC + tid] = (int32_t)row;
@@ -410,13 +532,30 @@ cudaError_t launch_attn_wide(const float *q, int64_t n_q, int H_q, int H_kv, flo
                              const int32_t *n_cells, int64_t max_cells, float *out, float *lse,
                              cudaStream_t st)
 {
-    const cudaError_t ea = ensure_kernel_attrs<attn_wide_kernel>(kWSmem, true);
+    const cudaError_t ea = ensure_kernel_attrs<attn_wide_kernel<false>>(kWSmem, true);
     if (ea != cudaSuccess) return ea;
     const int S = attn_wide_splits(n_q, H_kv, max_cells);
     const dim3 grid((unsigned)S, (unsigned)H_kv, (unsigned)n_q);
-    return launch(attn_wide_kernel, grid, dim3(kWNT), kWSmem, st, S > 1 ? S : 1, q, H_q, H_kv,
-                  scale * kLog2e, (const __nv_bfloat16 *)KV, n_kv, ld, pos, n_cells, max_cells,
-                  out, lse);
+    return launch(attn_wide_kernel<false>, grid, dim3(kWNT), kWSmem, st, S > 1 ? S : 1, q, H_q,
+                  H_kv, scale * kLog2e, (const __nv_bfloat16 *)KV, n_kv, ld, pos, n_cells,
+                  max_cells, out, lse, (const uint8_t *)nullptr, (int64_t)0, (int32_t *)nullptr);
+}
+
+int64_t attn_wide_mask_max_kv() { return (int64_t)kWMaskWords * 64; }
+
+cudaError_t launch_attn_wide_mask(const float *q, int64_t n_q, int H_q, int H_kv, float scale,
+                                  const void *KV, int64_t n_kv, int64_t ld, const uint8_t *mask,
+                                  int64_t ld_mask, int64_t max_list, int32_t *counts_out,
+                                  float *out, float *lse, cudaStream_t st)
+{
+    const cudaError_t ea = ensure_kernel_attrs<attn_wide_kernel<true>>(kWSmem, true);
+    if (ea != cudaSuccess) return ea;
+    const int S = attn_wide_splits(n_q, H_kv, max_list);
+    const dim3 grid((unsigned)S, (unsigned)H_kv, (unsigned)n_q);
+    return launch(attn_wide_kernel<true>, grid, dim3(kWNT), kWSmem, st, S > 1 ? S : 1, q, H_q,
+                  H_kv, scale * kLog2e, (const __nv_bfloat16 *)KV, n_kv, ld,
+                  (const int32_t *)nullptr, (const int32_t *)nullptr, max_list, out, lse, mask,
+                  ld_mask, counts_out);
 }
 
 }  // namespace qsa

@@ -62,7 +62,7 @@ const char *qsa_status_str(qsa_status s)
     return "QSA_ERR_UNKNOWN";
 }
 
-int qsa_version(void) { return (2 << 16) | 1; }
+int qsa_version(void) { return (2 << 16) | 2; }
 
 static qsa_status check_pool_update(const void *raw_k, qsa_dtype raw_dtype, int64_t n_ctx, int H,
                                     int d, const float *norm_w, float eps, double rope_base,
@@ -269,6 +269,10 @@ qsa_status qsa_sparse_attn(const float *q, int64_t n_q, int H_q, int H_kv, int d
     const qsa_status v = check_attn(q, n_q, H_q, H_kv, d_k, d_v, K, V, dtype, n_kv, ld_k, ld_v,
                                     n_cells, max_cells, out, workspace, workspace_bytes);
     if (v != QSA_OK) return v;
+    // the latent form reads the query in 8-byte pairs
+    if (H_kv == 1 && attn_uses_wide(dtype, d_k, d_v, H_q / H_kv, K, V, ld_k, ld_v) &&
+        !aligned(q, 8))
+        return QSA_ERR_INVALID_ARG;
     return from_cuda(launch_sparse_attn(q, n_q, H_q, H_kv, d_k, d_v, scale, K, V, dtype, n_kv,
                                         ld_k, ld_v, pos, n_cells, max_cells, out, lse_out,
                                         (float *)workspace, (cudaStream_t)stream));
@@ -622,6 +626,30 @@ qsa_status qsa_mask_to_list(const uint8_t *mask, int64_t n_rows, int64_t n_kv, i
     if (n_kv > 0x7fffffffLL || n_rows > 0x7fffffffLL) return QSA_ERR_UNSUPPORTED;
     return from_cuda(launch_mask_to_list(mask, n_rows, n_kv, ld_mask, max_list, pos_out,
                                          counts_out, bits_out, (cudaStream_t)stream));
+}
+
+qsa_status qsa_mask_sparse_attn(const float *q, int64_t n_q, int H_q, int H_kv, int d_k,
+                                int d_v, float scale, const void *KV, qsa_dtype dtype,
+                                int64_t n_kv, int64_t ld_kv, const uint8_t *mask, int64_t ld_mask,
+                                int64_t max_list, int32_t *counts_out, float *out, float *lse_out,
+                                qsa_stream_t stream)
+{
+    if (!q || !KV || !mask || !out) return QSA_ERR_INVALID_ARG;
+    if (n_q < 0 || H_q < 1 || H_kv < 1 || H_q % H_kv || n_kv < 0 || ld_kv < (int64_t)H_kv * d_k ||
+        ld_mask < n_kv || max_list < 0)
+        return QSA_ERR_INVALID_ARG;
+    if (!aligned(q, 8) || !aligned(out, 4) || (lse_out && !aligned(lse_out, 4)) ||
+        (counts_out && !aligned(counts_out, 4)))
+        return QSA_ERR_INVALID_ARG;
+    if (dtype != QSA_F32 && dtype != QSA_BF16) return QSA_ERR_INVALID_ARG;
+    if (H_kv != 1 || !attn_uses_wide(dtype, d_k, d_v, H_q, KV, KV, ld_kv, ld_kv))
+        return QSA_ERR_UNSUPPORTED;  // only the latent shape (bf16, 576 / 512, 16 heads, 1 KV)
+    if (n_kv > attn_wide_mask_max_kv() || n_q > 65535 || H_kv > 65535 || max_list > 0x7fffffffLL)
+        return QSA_ERR_UNSUPPORTED;
+    if (n_q == 0) return QSA_OK;
+    return from_cuda(launch_attn_wide_mask(q, n_q, H_q, H_kv, scale, KV, n_kv, ld_kv, mask,
+                                           ld_mask, max_list, counts_out, out, lse_out,
+                                           (cudaStream_t)stream));
 }
 
 qsa_status qsa_mask_sparse_eligible(int has_mask, float max_bias, float softcap, int64_t n_kv,

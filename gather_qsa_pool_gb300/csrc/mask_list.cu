@@ -21,13 +21,6 @@ namespace {
 
 constexpr int kMaskThreads = 1024;
 
-// Bit i (i < 4) set when byte i of x is nonzero: the bytes' nonzero flags (0 or 1 each), times
-// a constant that moves byte i's flag to bit 28 + i with no carry into those bits.
-__device__ __forceinline__ uint32_t nonzero_byte_bits(uint32_t x)
-{
-    const uint32_t m = __vcmpne4(x, 0u) & 0x01010101u;
-    return (m * 0x10204080u) >> 28;
-}
 constexpr int kWordsPerChunk = kMaskThreads;  // one word per thread per chunk
 
 __global__ void __launch_bounds__(kMaskThreads)

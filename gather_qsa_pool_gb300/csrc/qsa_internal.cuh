@@ -56,6 +56,29 @@ __device__ __forceinline__ float warp_max(float v)
 // before its immediate predecessor have completed: inputs written before that
 // predecessor may be read before the wait.
 
+// Bit i (i < 4) set when byte i of x is nonzero: the bytes' nonzero flags (0 or 1 each), times
+// a constant that moves byte i's flag to bit 28 + i with no carry into those bits.
+__device__ __forceinline__ uint32_t nonzero_byte_bits(uint32_t x)
+{
+    const uint32_t m = __vcmpne4(x, 0u) & 0x01010101u;
+    return (m * 0x10204080u) >> 28;
+}
+
+// Index (0-31) of the j-th lowest set bit of x, j < popc(x): five halving steps.
+__device__ __forceinline__ int select_set_bit(uint32_t x, int j)
+{
+    int b = 0;
+#pragma unroll
+    for (int w = 16; w >= 1; w >>= 1) {
+        const int c = __popc((x >> b) & ((1u << w) - 1u));
+        if (j >= c) {
+            j -= c;
+            b += w;
+        }
+    }
+    return b;
+}
+
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger()
 {
@@ -455,6 +478,13 @@ cudaError_t launch_attn_wide(const float *q, int64_t n_q, int H_q, int H_kv, flo
                              const void *KV, int64_t n_kv, int64_t ld, const int32_t *pos,
                              const int32_t *n_cells, int64_t max_cells, float *out, float *lse,
                              cudaStream_t st);
+// The same kernel listing each query's cells from its mask row itself (rows of at most
+// attn_wide_mask_max_kv() positions); counts_out (nullable) gets each row's true count.
+int64_t attn_wide_mask_max_kv();
+cudaError_t launch_attn_wide_mask(const float *q, int64_t n_q, int H_q, int H_kv, float scale,
+                                  const void *KV, int64_t n_kv, int64_t ld, const uint8_t *mask,
+                                  int64_t ld_mask, int64_t max_list, int32_t *counts_out,
+                                  float *out, float *lse, cudaStream_t st);
 int attn_num_splits(int64_t n_q, int H_kv, int64_t max_cells);
 size_t attn_smem_bytes_host(int G, int d_k, int d_v, int esize);
 size_t attn_workspace_bytes(int64_t n_q, int H_q, int H_kv, int d_v, int64_t max_cells);

@@ -9,7 +9,8 @@
  *   qsa_pool_update -> qsa_index_score -> qsa_topk_blocks -> qsa_gather_kv
  *                   -> qsa_sparse_attn
  *
- * and the mask-driven variant is qsa_mask_to_list -> qsa_sparse_attn.
+ * and the mask-driven variant is qsa_mask_to_list -> qsa_sparse_attn, or for the latent
+ * shape the single call qsa_mask_sparse_attn.
  *
  * Conventions shared by every entry point
  *   - Every tensor pointer is device memory owned by the caller (except the host buffers
@@ -62,7 +63,8 @@ typedef enum {
 const char *qsa_status_str(qsa_status s);
 
 /* Library ABI version: (major << 16) | minor.  Major 2: pooled-cache dtype arguments,
- * several queries per decode step, the host-fed decode step; minor 1: decode plans. */
+ * several queries per decode step, the host-fed decode step; minor 1: decode plans;
+ * minor 2: qsa_mask_sparse_attn. */
 int qsa_version(void);
 
 /*
@@ -236,7 +238,9 @@ qsa_status qsa_gather_kv(const void *K, const void *V, qsa_dtype dtype, int64_t 
  *   K, V     dtype `dtype`, row strides ld_k, ld_v (V may alias K, e.g. V = K[:, :d_v])
  *   n_cells  [n_q] int32 device counts
  * Requirements: H_q % H_kv == 0, d_k and d_v multiples of 8, ld_k and ld_v multiples
- * of 8, K and V 16-byte aligned (checked: INVALID_ARG otherwise).
+ * of 8, K and V 16-byte aligned; for the latent shape (bf16, d_k 576, d_v 512, 16 query
+ * heads on one KV head, V = K with the same stride) q 8-byte aligned (checked:
+ * INVALID_ARG otherwise).
  */
 qsa_status qsa_sparse_attn(const float *q, int64_t n_q, int H_q, int H_kv, int d_k, int d_v,
                            float scale, const void *K, const void *V, qsa_dtype dtype,
@@ -467,6 +471,39 @@ qsa_status qsa_sparse_attn_noalloc(const float *q, int64_t n_q, int H_q, int H_k
 qsa_status qsa_mask_to_list(const uint8_t *mask, int64_t n_rows, int64_t n_kv, int64_t ld_mask,
                             int64_t max_list, int32_t *pos_out, int32_t *counts_out,
                             uint64_t *bits_out, qsa_stream_t stream);
+
+/*
+ * qsa_mask_sparse_attn -- the mask-driven sparse attention in one call: each query's key
+ * list is taken from its mask row inside the attention kernel instead of a separate
+ * qsa_mask_to_list launch.
+ *
+ * Source: devotd.net, "llama.cpp CDNA sparse attention", sections 2-3 (the attendable
+ * positions listed from the mask, then the sparse kernel over the listed keys); Qiita,
+ * ariera, llama.cpp series part (mask-driven sparse attention), section "sparse MMA
+ * kernel" (16 query columns of one latent KV group, DKQ 576 / d_v 512).
+ *
+ * For query i the list is the ascending set positions of mask row i (nonzero bytes of
+ * mask[i*ld_mask + 0 .. n_kv)), exactly the list qsa_mask_to_list writes, and the result
+ * equals qsa_sparse_attn over that list (same cells per split, same order: bit for bit).
+ * counts_out[i] (nullable) = the true count; a count above max_list gives out = NaN and
+ * lse = NaN for that query (the caller must not use it), as in the two-call path.
+ *
+ *   q       [n_q][H_q][576] fp32, 8-byte aligned;  out [n_q][H_q][512] fp32
+ *   KV      [n_kv] rows of ld_kv bf16 elements (16-byte aligned, ld_kv*2 a multiple of 16):
+ *           the key is a row's first 576 columns, the value its first 512
+ *   mask    [n_q][ld_mask] uint8, nonzero = attend;  lse_out [n_q][H_q] or NULL
+ * Only the latent shape runs here: bf16, d_k 576, d_v 512, H_q = 16 on H_kv = 1
+ * (QSA_ERR_UNSUPPORTED otherwise), n_kv <= 65536 (QSA_ERR_UNSUPPORTED above).
+ * Errors: INVALID_ARG for null q / KV / mask / out, a misaligned q, out, lse_out or
+ * counts_out, n_q < 0, H_q not a multiple of H_kv, ld_kv < H_kv * d_k, ld_mask < n_kv,
+ * max_list < 0, a dtype other than QSA_F32 / QSA_BF16.  No workspace: the splits of a query combine inside a thread-block cluster.
+ * Eligibility (qsa_mask_sparse_eligible) stays the caller's decision.
+ */
+qsa_status qsa_mask_sparse_attn(const float *q, int64_t n_q, int H_q, int H_kv, int d_k,
+                                int d_v, float scale, const void *KV, qsa_dtype dtype,
+                                int64_t n_kv, int64_t ld_kv, const uint8_t *mask, int64_t ld_mask,
+                                int64_t max_list, int32_t *counts_out, float *out, float *lse_out,
+                                qsa_stream_t stream);
 
 /*
  * qsa_mask_sparse_eligible -- host-side check of when the mask-driven sparse path

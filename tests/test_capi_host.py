@@ -32,7 +32,7 @@ def test_status_strings_and_version(lib):
     assert qsa.status_str(1) == "QSA_ERR_INVALID_ARG"
     assert qsa.status_str(4) == "QSA_ERR_TIMEOUT"
     assert lib.qsa_version() >> 16 == 2
-    assert lib.qsa_version() & 0xFFFF >= 1  # decode plans
+    assert lib.qsa_version() & 0xFFFF >= 2  # decode plans, the one-call mask attention
 
 
 def test_pool_update_rejects(lib):
@@ -150,6 +150,30 @@ def test_mask_to_list_rejects(lib):
     assert lib.qsa_mask_to_list(FAKE, 1, 64, 63, 8, FAKE, FAKE, None, s) == 1
     assert lib.qsa_mask_to_list(FAKE, 1, 64, 64, 8, FAKE, FAKE, P(0x10004), s) == 1
     assert lib.qsa_mask_to_list(FAKE, 1, 1 << 31, 1 << 31, 8, FAKE, FAKE, None, s) == 2
+
+
+def test_mask_sparse_attn_rejects(lib):
+    ok = dict(q=FAKE, n_q=4, H_q=16, H_kv=1, d_k=576, d_v=512, scale=0.04, KV=FAKE, dt=1,
+              n_kv=32768, ld_kv=576, mask=FAKE, ld_mask=32768, max_list=2048, counts=FAKE,
+              out=FAKE, lse=None, st=None)
+
+    def call(**kw):
+        v = dict(ok, **kw)
+        return lib.qsa_mask_sparse_attn(*v.values())
+
+    assert call(mask=None) == 1
+    assert call(out=None) == 1
+    assert call(q=P(0x10004)) == 1                       # q not 8-byte aligned
+    assert call(ld_mask=100) == 1                        # ld_mask < n_kv
+    assert call(max_list=-1) == 1
+    assert call(ld_kv=500) == 1                          # ld_kv < d_k
+    assert call(dt=7) == 1                               # no such dtype
+    assert call(H_q=32, H_kv=2, ld_kv=1152) == 2         # one latent KV head only
+    assert call(d_k=128, d_v=128, ld_kv=128) == 2        # not the latent shape
+    assert call(dt=0) == 2                               # fp32 rows
+    assert call(KV=P(0x10008)) == 2                      # rows not 16-byte aligned
+    assert call(n_kv=65537, ld_mask=65537) == 2          # longer than the in-kernel words
+    assert call(n_q=0) == 0                              # nothing to launch
 
 
 def test_mask_sparse_eligibility_rule():

@@ -226,6 +226,64 @@ def test_latent_attention_list_lengths(n_q, lens):
         np.testing.assert_allclose(g_lse[i], want_lse, rtol=1e-5, atol=1e-4)
 
 
+@pytest.mark.parametrize("case", ["32k", "ragged", "unaligned", "overflow", "max_kv", "many"])
+def test_mask_sparse_attn_one_call(case):
+    """qsa_mask_sparse_attn (each query's list built from its mask row inside the attention
+    kernel) against the oracle's list and attention, and bit for bit against the two-call
+    path (qsa_mask_to_list, then qsa_sparse_attn) on the same inputs: rows of whole aligned
+    64-key words, a ragged key count, row strides off the 16-byte grid, a list overflow
+    (NaN result, true count), an empty row, the longest rows (65,536 keys) and 160 queries
+    (one CTA per query, no cluster)."""
+    d_k, d_v, H, max_list = 576, 512, 16, 2048
+    n_q, n_kv, pad, dens = {"32k": (4, 32768, 0, 0.06), "ragged": (3, 5000, 0, 0.1),
+                            "unaligned": (4, 4096, 3, 0.2), "overflow": (2, 5000, 0, 0.6),
+                            "max_kv": (2, 65536, 0, 0.03), "many": (160, 8192, 0, 0.02)}[case]
+    rng = np.random.default_rng(len(case) * 31 + n_kv)
+    KV = qsa_synth.to_bf16_bits(rng.standard_normal((n_kv, d_k)).astype(np.float32))
+    q = rng.standard_normal((n_q, H, d_k)).astype(np.float32)
+    m = (rng.random((n_q, n_kv)) < dens).astype(np.uint8)
+    if case == "ragged":
+        m[1, :] = 0                                    # empty row
+    wide = np.zeros((n_q, n_kv + pad), np.uint8)
+    wide[:, :n_kv] = m * rng.integers(1, 256, size=m.shape).astype(np.uint8)  # any nonzero byte
+    wide[:, n_kv:] = 1                                 # past the row: never listed
+    kv, d_mask, d_q = to_dev(KV), to_dev(wide), to_dev(q)
+    scale = 1.0 / math.sqrt(d_k)
+    out = torch.full((n_q, H, d_v), -5.0, device="cuda")
+    lse = torch.full((n_q, H), -5.0, device="cuda")
+    cnt = torch.full((n_q,), -1, dtype=torch.int32, device="cuda")
+    qsa.mask_sparse_attn(d_q, kv, d_mask, max_list, out, scale, counts_out=cnt, lse=lse,
+                         n_kv=n_kv)
+    # the two-call path
+    pos = torch.zeros((n_q, max_list), dtype=torch.int32, device="cuda")
+    cnt2 = torch.zeros(n_q, dtype=torch.int32, device="cuda")
+    qsa.mask_to_list(d_mask, max_list, pos, cnt2, n_kv=n_kv)
+    out2 = torch.zeros((n_q, H, d_v), device="cuda")
+    lse2 = torch.zeros((n_q, H), device="cuda")
+    ws_n = qsa.sparse_attn_workspace_size(n_q, H, 1, d_v, max_list)
+    ws = torch.empty(max(ws_n // 4, 1), device="cuda")
+    qsa.sparse_attn(d_q, kv, kv, cnt2, max_list, out2, 1, d_k, d_v, scale, pos=pos, lse=lse2,
+                    workspace=ws, ld_k=d_k, ld_v=d_k, n_kv=n_kv)
+    g_out, g_lse, g_cnt = to_host(out), to_host(lse), to_host(cnt)
+    np.testing.assert_array_equal(g_cnt, to_host(cnt2))
+    np.testing.assert_array_equal(g_out.view(np.uint32), to_host(out2).view(np.uint32))
+    np.testing.assert_array_equal(g_lse.view(np.uint32), to_host(lse2).view(np.uint32))
+    for r in range(n_q) if n_q <= 8 else range(0, n_q, 23):
+        w_pos, w_cnt, _ = oracle.mask_to_list(m[r], max_list)
+        assert g_cnt[r] == w_cnt
+        if w_cnt > max_list:
+            assert np.all(np.isnan(g_out[r])) and np.all(np.isnan(g_lse[r]))
+        elif w_cnt == 0:
+            assert np.all(g_out[r] == 0.0) and np.all(np.isneginf(g_lse[r]))
+        else:
+            want, want_lse = oracle.attention(q[r], KV, KV, H, 1, d_k, d_v, d_k, d_k, w_pos,
+                                              scale)
+            np.testing.assert_allclose(g_out[r], want, rtol=0, atol=ATOL_ATTN_BF16)
+            np.testing.assert_allclose(g_lse[r], want_lse, rtol=1e-5, atol=1e-4)
+    if case == "overflow":
+        assert np.all(g_cnt > max_list)
+
+
 def test_dkq576_with_separate_values():
     """DKQ 576 / d_v 512 with a V tensor of its own (not the K row's first columns): the
     general attention kernel, against the oracle."""
