@@ -212,7 +212,7 @@ __device__ __forceinline__ void for_each_key_at_least(const float *__restrict__ 
 
 // The sampled form's candidate pass over a 16-byte aligned row (T > kKeyNegInf): every
 // score >= key_float(T) goes to the candidate list (key, block), slots past cap counted
-// but not stored.  Each round a thread loads U vectors, folds them into a 4U-bit hit mask
+// but not stored, and into hist, the candidates' histogram of the first 12-bit digit.  Each round a thread loads U vectors, folds them into a 4U-bit hit mask
 // and lets them die; a warp scan and one shared atomic per warp reserve the round's slots;
 // the hits are then read again (lines just fetched) and stored.  Keeping the vectors live
 // across the stores (a lambda per hit) measured 9.8 us per 64k-block row against 5.6 us
@@ -220,7 +220,7 @@ __device__ __forceinline__ void for_each_key_at_least(const float *__restrict__ 
 __device__ __forceinline__ void collect_at_least(const float *__restrict__ row, int64_t n,
                                                  uint32_t T, uint32_t *counter,
                                                  uint32_t *cand_key, int32_t *cand_idx,
-                                                 uint32_t cap)
+                                                 uint32_t cap, uint32_t *hist)
 {
     constexpr int U = 8;
     const float lo = key_float(T);
@@ -255,8 +255,10 @@ __device__ __forceinline__ void collect_at_least(const float *__restrict__ row, 
             const int bit = __ffs(hit) - 1;
             hit &= hit - 1;
             const int b = 4 * (b0 + (int)threadIdx.x + (bit >> 2) * NT) + (bit & 3);
+            const uint32_t key = score_key(row[b]);
+            atomicAdd(&hist[key >> (32 - kTopkHistBits)], 1u);
             if (s < cap) {
-                cand_key[s] = score_key(row[b]);
+                cand_key[s] = key;
                 cand_idx[s] = b;
             }
             ++s;
@@ -264,9 +266,11 @@ __device__ __forceinline__ void collect_at_least(const float *__restrict__ row, 
     }
     for (int64_t i = 4 * (int64_t)n4 + threadIdx.x; i < n; i += NT)
         if (row[i] >= lo) {
+            const uint32_t key = score_key(row[i]);
+            atomicAdd(&hist[key >> (32 - kTopkHistBits)], 1u);
             const uint32_t slot = atomicAdd(counter, 1u);
             if (slot < cap) {
-                cand_key[slot] = score_key(row[i]);
+                cand_key[slot] = key;
                 cand_idx[slot] = (int32_t)i;
             }
         }
@@ -493,11 +497,14 @@ __device__ bool topk_query_sampled(const float *srow, int64_t n, int64_t k, int3
     if (r > ns) r = ns;
     find_bucket(hist, kBins1, (uint32_t)r, warp_s, misc);
     const uint32_t T = misc[0] << (32 - kTopkHistBits);
+    for (int i = tid; i < kBins1; i += NT) hist[i] = 0u;  // find_bucket has read it
     __syncthreads();
 
-    // ---- 2. one pass: every key >= T is a candidate
+    // ---- 2. one pass: every key >= T is a candidate, and the candidates' first-digit
+    // histogram
     auto keep = [&](uint32_t key, int64_t i) {
         if (key >= T) {
+            atomicAdd(&hist[key >> (32 - kTopkHistBits)], 1u);
             const uint32_t slot = atomicAdd(&misc[8], 1u);
             if (slot < (uint32_t)cand_cap) {
                 cand_key[slot] = key;
@@ -506,7 +513,7 @@ __device__ bool topk_query_sampled(const float *srow, int64_t n, int64_t k, int3
         }
     };
     if (T > kKeyNegInf && (reinterpret_cast<uintptr_t>(srow) & 15) == 0)
-        collect_at_least(srow, n, T, &misc[8], cand_key, cand_idx, (uint32_t)cand_cap);
+        collect_at_least(srow, n, T, &misc[8], cand_key, cand_idx, (uint32_t)cand_cap, hist);
     else if (T > kKeyNegInf)
         for_each_key_at_least(srow, n, T, keep);
     else
@@ -515,11 +522,7 @@ __device__ bool topk_query_sampled(const float *srow, int64_t n, int64_t k, int3
     const uint32_t m = misc[8];
     if (m < (uint32_t)k || m > (uint32_t)cand_cap) return false;  // uniform
 
-    // ---- 3. first digit over the candidates
-    for (int i = tid; i < kBins1; i += NT) hist[i] = 0u;
-    __syncthreads();
-    for (uint32_t c = tid; c < m; c += NT) atomicAdd(&hist[cand_key[c] >> (32 - kTopkHistBits)], 1u);
-    __syncthreads();
+    // ---- 3. first digit over the candidates (their histogram came with the pass)
     find_bucket(hist, kBins1, (uint32_t)k, warp_s, misc);
     const uint32_t B1 = misc[0];
     const uint32_t k_rem = (uint32_t)k - misc[1];
