@@ -1121,6 +1121,19 @@ size_t attn_workspace_bytes(int64_t n_q, int H_q, int H_kv, int d_v, int64_t max
     return sizeof(float) * (size_t)n_q * H_kv * S * G * (size_t)(d_v + 4);
 }
 
+size_t attn_partials_bytes(qsa_dtype dt, int64_t n_q, int H_q, int H_kv, int d_k, int d_v,
+                           const void *K, const void *V, int64_t ld_k, int64_t ld_v,
+                           const int32_t *pos, int64_t max_cells)
+{
+    if (n_q <= 0 || H_kv <= 0 || H_q % H_kv) return 0;
+    const int G = H_q / H_kv;
+    // the same order of choices as launch_sparse_attn
+    if (attn_uses_rows4(dt, n_q, H_q, H_kv, d_k, d_v, K, V, ld_k, ld_v, pos, max_cells)) return 0;
+    if (H_kv == 1 && attn_uses_wide(dt, d_k, d_v, G, K, V, ld_k, ld_v)) return 0;
+    if (attn_uses_mma(dt, d_k, d_v, G)) return 0;
+    return attn_workspace_bytes(n_q, H_q, H_kv, d_v, max_cells);
+}
+
 cudaError_t launch_sparse_attn(const float *q, int64_t n_q, int H_q, int H_kv, int d_k, int d_v,
                                float scale, const void *K, const void *V, qsa_dtype dt,
                                int64_t n_kv, int64_t ld_k, int64_t ld_v, const int32_t *pos,

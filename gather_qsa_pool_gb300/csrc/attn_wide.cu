@@ -1,9 +1,9 @@
 // attn_wide.cu -- sparse attention of 16 query heads on one latent KV head: DKQ 576,
 // d_v 512, V the first 512 columns of each K row (one row read serves both), bf16.
 //
-// Source: Qiita, ariera, llama.cpp series part (mask-driven sparse attention), section
-// "sparse MMA kernel": the 16 query columns of one KV group attend only over the key
-// positions listed from the mask (DKQ 576 / ncols2 16 on the pages' model).
+// Source: devotd.net, "llama.cpp CDNA sparse attention", sections 2-3: the sparse
+// matrix-op kernel attends the 16 query columns of one KV group only over the key positions
+// listed from the mask (DKQ 576 / ncols2 16 on the pages' model).
 //
 // Grid (S, H_kv, n_q): the S CTAs of one (query, KV head) split the list and, for S > 1,
 // form a thread-block cluster that merges their (o, m, l) states in distributed shared

@@ -6,7 +6,6 @@
 #include <stdlib.h>
 
 #include <atomic>
-#include <mutex>
 
 #include "qsa_internal.cuh"
 
@@ -666,34 +665,12 @@ qsa_status qsa_mask_sparse_eligible(int has_mask, float max_bias, float softcap,
 // ---------------------------------------------------------------------------------
 // Split-K scratch for callers that cannot allocate: one fixed device array per GPU,
 // shared by every call.  Host code must not pass the array's name to a kernel (on the
-// host that name is a stand-in, not a device address): the address is looked up once per
-// device with cudaGetSymbolAddress and kept.
+// host that name is a stand-in, not a device address): every call looks the address up
+// with cudaGetSymbolAddress in the caller's current device and context.  The lookup
+// allocates nothing, and doing it per call (rather than caching it per device ordinal)
+// keeps the address right when the caller switches to another context on the same device
+// or after a device reset has reloaded the module.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[QSA_NOALLOC_SCRATCH_BYTES];
-
-namespace {
-
-constexpr int kNoallocMaxDevices = 64;
-std::mutex g_noalloc_mutex;
-void *g_noalloc_addr[kNoallocMaxDevices] = {};
-
-// Device address of g_noalloc_scratch on the current device (looked up on first use).
-qsa_status noalloc_scratch(void **addr)
-{
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess) return QSA_ERR_CUDA;
-    if (dev < 0 || dev >= kNoallocMaxDevices) return QSA_ERR_UNSUPPORTED;
-    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-    if (g_noalloc_addr[dev] == nullptr) {
-        void *p = nullptr;
-        const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (e != cudaSuccess || p == nullptr) return QSA_ERR_CUDA;
-        g_noalloc_addr[dev] = p;
-    }
-    *addr = g_noalloc_addr[dev];
-    return QSA_OK;
-}
-
-}  // namespace
 
 extern "C" qsa_status qsa_sparse_attn_noalloc(const float *q, int64_t n_q, int H_q, int H_kv,
                                               int d_k, int d_v, float scale, const void *K,
@@ -702,12 +679,16 @@ extern "C" qsa_status qsa_sparse_attn_noalloc(const float *q, int64_t n_q, int H
                                               const int32_t *n_cells, int64_t max_cells,
                                               float *out, float *lse_out, qsa_stream_t stream)
 {
+    // what the path these arguments take really writes (0 for the forms that merge their
+    // splits inside a cluster); the argument checks themselves are qsa_sparse_attn's
     if (n_q >= 0 && H_q >= 1 && H_kv >= 1 && d_v >= 1 && max_cells >= 0 && H_q % H_kv == 0 &&
-        qsa_sparse_attn_workspace_size(n_q, H_q, H_kv, d_v, max_cells) > QSA_NOALLOC_SCRATCH_BYTES)
+        valid_dtype(dtype) &&
+        attn_partials_bytes(dtype, n_q, H_q, H_kv, d_k, d_v, K, V, ld_k, ld_v, pos, max_cells) >
+            QSA_NOALLOC_SCRATCH_BYTES)
         return QSA_ERR_UNSUPPORTED;  // this shape needs more scratch than the fixed array
     void *scratch = nullptr;
-    const qsa_status s = noalloc_scratch(&scratch);
-    if (s != QSA_OK) return s;
+    const cudaError_t e = cudaGetSymbolAddress(&scratch, g_noalloc_scratch);
+    if (e != cudaSuccess || scratch == nullptr) return QSA_ERR_CUDA;
     return qsa_sparse_attn(q, n_q, H_q, H_kv, d_k, d_v, scale, K, V, dtype, n_kv, ld_k, ld_v, pos,
                            n_cells, max_cells, out, lse_out, scratch, QSA_NOALLOC_SCRATCH_BYTES,
                            stream);

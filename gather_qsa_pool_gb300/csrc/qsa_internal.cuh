@@ -488,6 +488,12 @@ cudaError_t launch_attn_wide_mask(const float *q, int64_t n_q, int H_q, int H_kv
 int attn_num_splits(int64_t n_q, int H_kv, int64_t max_cells);
 size_t attn_smem_bytes_host(int G, int d_k, int d_v, int esize);
 size_t attn_workspace_bytes(int64_t n_q, int H_q, int H_kv, int d_v, int64_t max_cells);
+// Split-K scratch the path launch_sparse_attn takes for these arguments really uses: 0 for
+// the forms that merge their splits inside a cluster (rows4, latent, bf16 8-head mma),
+// attn_workspace_bytes() otherwise.
+size_t attn_partials_bytes(qsa_dtype dt, int64_t n_q, int H_q, int H_kv, int d_k, int d_v,
+                           const void *K, const void *V, int64_t ld_k, int64_t ld_v,
+                           const int32_t *pos, int64_t max_cells);
 cudaError_t launch_sparse_attn(const float *q, int64_t n_q, int H_q, int H_kv, int d_k, int d_v,
                                float scale, const void *K, const void *V, qsa_dtype dt,
                                int64_t n_kv, int64_t ld_k, int64_t ld_v, const int32_t *pos,

@@ -249,6 +249,9 @@ qsa_status qsa_sparse_attn(const float *q, int64_t n_q, int H_q, int H_kv, int d
                            float *lse_out, void *workspace, size_t workspace_bytes,
                            qsa_stream_t stream);
 
+/* Workspace bytes of qsa_sparse_attn: the split-K partial records of the general kernels.
+ * It depends on the shape only, so it is an upper bound: the forms that merge their splits
+ * inside a cluster (see qsa_sparse_attn_noalloc) leave the workspace untouched. */
 size_t qsa_sparse_attn_workspace_size(int64_t n_q, int H_q, int H_kv, int d_v,
                                       int64_t max_cells);
 
@@ -429,19 +432,24 @@ size_t qsa_decode_step_host_workspace_size(int64_t n_q, int H_q, int H_kv, int d
  * until the process exits.
  *
  * Arguments, layouts and results are those of qsa_sparse_attn without workspace and
- * workspace_bytes.  The call allocates nothing and calls no allocating routine.  The
- * first call on each device looks the array's device address up (cudaGetSymbolAddress,
- * with that device current) and remembers it; make that first call before any stream
+ * workspace_bytes.  The call allocates nothing and calls no allocating routine.  Every
+ * call looks the array's device address up (cudaGetSymbolAddress, in the caller's current
+ * device and context; the lookup allocates nothing), so calls may come from any context
+ * and survive a device reset; the first lookup in a context loads the library's device
+ * code there if that has not happened yet, so make a first call before any stream
  * capture.  All calls share the one array, which keeps whatever the previous call wrote
  * there; nothing in it has to start at zero, because every call writes each partial
  * record before reading it.  Calls that run at the same time on the GPU (on different
- * streams, or in parallel branches of a graph) race on the array: the caller must
- * order them.
+ * streams, or in parallel branches of a graph) race on the array: the caller must order
+ * them.
  *
- * Errors: those of qsa_sparse_attn, plus QSA_ERR_UNSUPPORTED when the scratch this shape
- * needs -- qsa_sparse_attn_workspace_size(n_q, H_q, H_kv, d_v, max_cells) -- is larger
- * than QSA_NOALLOC_SCRATCH_BYTES (decode shapes fit: 32 query heads, 4 KV heads, d 128,
- * 2051 cells need 1.1 MB), and QSA_ERR_CUDA when the address lookup fails.
+ * Errors: those of qsa_sparse_attn, plus QSA_ERR_UNSUPPORTED when the split-K scratch the
+ * shape's kernel really uses is larger than QSA_NOALLOC_SCRATCH_BYTES, and QSA_ERR_CUDA
+ * when the address lookup fails.  The forms that merge their splits inside a thread-block
+ * cluster use none (bf16 with 8 query heads per KV head and d 128, e.g. the decode shape
+ * 32 / 4 heads; the latent shape; many-query bf16 4 x 8 heads); the others use about
+ * qsa_sparse_attn_workspace_size() bytes (e.g. fp32 K/V, 32 / 4 heads, d 128, 2051 cells:
+ * 0.6 MB), which is an upper bound for every form.
  */
 #define QSA_NOALLOC_SCRATCH_BYTES ((size_t)4 << 20)
 qsa_status qsa_sparse_attn_noalloc(const float *q, int64_t n_q, int H_q, int H_kv, int d_k,
@@ -477,10 +485,10 @@ qsa_status qsa_mask_to_list(const uint8_t *mask, int64_t n_rows, int64_t n_kv, i
  * list is taken from its mask row inside the attention kernel instead of a separate
  * qsa_mask_to_list launch.
  *
- * Source: devotd.net, "llama.cpp CDNA sparse attention", sections 2-3 (the attendable
- * positions listed from the mask, then the sparse kernel over the listed keys); Qiita,
- * ariera, llama.cpp series part (mask-driven sparse attention), section "sparse MMA
- * kernel" (16 query columns of one latent KV group, DKQ 576 / d_v 512).
+ * Source: devotd.net, "llama.cpp CDNA sparse attention", section 2 (the attendable
+ * positions are listed from the mask before the sparse kernel runs) and section 3 (the
+ * sparse matrix-op kernel over the listed keys, for DKQ 576 with 16 query columns per KV
+ * group; here d_v 512 on one latent KV head).
  *
  * For query i the list is the ascending set positions of mask row i (nonzero bytes of
  * mask[i*ld_mask + 0 .. n_kv)), exactly the list qsa_mask_to_list writes, and the result
