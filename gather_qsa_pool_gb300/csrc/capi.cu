@@ -236,9 +236,9 @@ size_t qsa_sparse_attn_workspace_size(int64_t n_q, int H_q, int H_kv, int d_v, i
 
 static qsa_status check_attn(const float *q, int64_t n_q, int H_q, int H_kv, int d_k, int d_v,
                              const void *K, const void *V, qsa_dtype dtype, int64_t n_kv,
-                             int64_t ld_k, int64_t ld_v, const int32_t *n_cells,
-                             int64_t max_cells, float *out, void *workspace,
-                             size_t workspace_bytes)
+                             int64_t ld_k, int64_t ld_v, const int32_t *pos,
+                             const int32_t *n_cells, int64_t max_cells, float *out,
+                             void *workspace, size_t workspace_bytes)
 {
     if (!q || !K || !V || !n_cells || !out) return QSA_ERR_INVALID_ARG;
     if (!valid_dtype(dtype) || n_q < 0 || H_q < 1 || H_kv < 1 || H_q % H_kv || d_k < 8 ||
@@ -252,7 +252,10 @@ static qsa_status check_attn(const float *q, int64_t n_q, int H_q, int H_kv, int
     if (attn_smem_bytes_host(G, d_k, d_v, esize_of(dtype)) > kMaxSmem) return QSA_ERR_UNSUPPORTED;
     if (n_q > 65535 || H_kv > 65535) return QSA_ERR_UNSUPPORTED;
     if (n_kv > 0x7fffffffLL || n_q * max_cells > 0x7fffffffLL) return QSA_ERR_UNSUPPORTED;
-    const size_t need = qsa_sparse_attn_workspace_size(n_q, H_q, H_kv, d_v, max_cells);
+    // the split-K records the kernel these arguments select really writes (none for the
+    // forms that merge in a cluster)
+    const size_t need =
+        attn_partials_bytes(dtype, n_q, H_q, H_kv, d_k, d_v, K, V, ld_k, ld_v, pos, max_cells);
     if (workspace_bytes < need || (need > 0 && !workspace)) return QSA_ERR_INVALID_ARG;
     if (need > 0 && !aligned(workspace, 16)) return QSA_ERR_INVALID_ARG;
     return QSA_OK;
@@ -266,7 +269,7 @@ qsa_status qsa_sparse_attn(const float *q, int64_t n_q, int H_q, int H_kv, int d
                            qsa_stream_t stream)
 {
     const qsa_status v = check_attn(q, n_q, H_q, H_kv, d_k, d_v, K, V, dtype, n_kv, ld_k, ld_v,
-                                    n_cells, max_cells, out, workspace, workspace_bytes);
+                                    pos, n_cells, max_cells, out, workspace, workspace_bytes);
     if (v != QSA_OK) return v;
     // the latent form reads the query in 8-byte pairs
     if (H_kv == 1 && attn_uses_wide(dtype, d_k, d_v, H_q / H_kv, K, V, ld_k, ld_v) &&
@@ -338,7 +341,7 @@ static qsa_status decode_step_impl(const void *raw_k, qsa_dtype raw_dtype, int64
         v = check_gather(K, V, kv_dtype, n_kv, H_kv, d, d, ld_kv, ld_kv, blocks, counts, n_q,
                          k_blk, nullptr, n_ctx, nullptr, nullptr, pos, n_cells, max_cells);
     if (v == QSA_OK)
-        v = check_attn(q, n_q, H_q, H_kv, d, d, K, V, kv_dtype, n_kv, ld_kv, ld_kv, n_cells,
+        v = check_attn(q, n_q, H_q, H_kv, d, d, K, V, kv_dtype, n_kv, ld_kv, ld_kv, pos, n_cells,
                        max_cells, out, workspace, attn_bytes);
     if (v != QSA_OK) return v;
     const cudaStream_t st = (cudaStream_t)stream;

@@ -237,6 +237,10 @@ qsa_status qsa_gather_kv(const void *K, const void *V, qsa_dtype dtype, int64_t 
  *   q        [n_q][H_q][d_k] fp32;  out [n_q][H_q][d_v] fp32;  lse_out [n_q][H_q] or NULL
  *   K, V     dtype `dtype`, row strides ld_k, ld_v (V may alias K, e.g. V = K[:, :d_v])
  *   n_cells  [n_q] int32 device counts
+ *   workspace  caller scratch for the split-K partial records, 16-byte aligned: at least
+ *            the bytes the kernel these arguments select writes (0 for the forms that merge
+ *            their splits inside a thread-block cluster); qsa_sparse_attn_workspace_size()
+ *            is always enough.  INVALID_ARG when smaller than the kernel needs.
  * Requirements: H_q % H_kv == 0, d_k and d_v multiples of 8, ld_k and ld_v multiples
  * of 8, K and V 16-byte aligned; for the latent shape (bf16, d_k 576, d_v 512, 16 query
  * heads on one KV head, V = K with the same stride) q 8-byte aligned (checked:

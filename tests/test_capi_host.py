@@ -136,7 +136,10 @@ def test_sparse_attn_rejects(lib):
     assert call(d_k=100) == 1                # not a multiple of 8
     assert call(ld_k=500) == 1               # ld_k < H_kv*d_k
     assert call(K=P(0x10008)) == 1           # K not 16-byte aligned
-    assert call(ws_bytes=0) == 1             # workspace too small
+    # fp32 K/V: the general kernel writes split-K records, so a workspace is required (the
+    # bf16 8-head form merges in a cluster and needs none; a valid call would launch)
+    assert call(ws_bytes=0, dt=0) == 1       # workspace too small
+    assert call(ws_bytes=64, dt=0) == 1
     assert call(H_q=96) == 2                 # 24 heads per KV head: not built
     assert call(H_q=16, H_kv=1, d_k=576, d_v=512, ld_k=576, ld_v=576, dt=0) == 2  # smem
     need = lib.qsa_sparse_attn_workspace_size(1, 32, 4, 128, 2051)
