@@ -39,10 +39,14 @@ CONTEXTS = {"64k": "decode_64k", "128k": "decode_128k", "256k": "decode_256k"}
 SCORE_SRCS = [os.path.join(ROOT, "gather_qsa_pool_gb300", "csrc", f)
               for f in ("index_score.cu", "score_stream.cuh")]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "score_stream_256k_traffic.txt")
+STEP_SCORE_SRCS = [os.path.join(ROOT, "gather_qsa_pool_gb300", "csrc", f)
+                   for f in ("score_pool.cu", "score_stream.cuh", "qsa_internal.cuh")]
+STEP_TRAFFIC_FILE = os.path.join(ROOT, "profiles", "score_pool_256k_traffic.txt")
 # Kernels one qsa_decode_step launches when it appends a token: the fused pool-update +
 # score scan, the top-k (whose last CTA also writes the cell list) and the attention
 # kernel (split-K with the combine inside its cluster).
 LAUNCHES_PER_DECODE_STEP = 3
+SCORE_POOL_THREADS = 256  # block size of the step's score kernel (score_pool_kernel)
 
 
 def parse_args():
@@ -171,25 +175,24 @@ class ClockSampler:
                 "sm_max_mhz": max(r[2] for r in sel), "reasons": reasons, "samples": len(sel)}
 
 
-def traffic_per_launch(n_rows_primary: int):
-    """DRAM bytes per score launch from the committed ncu summary, if it was taken on the
-    current kernel source (else None)."""
+def traffic_per_launch(path, srcs, n_rows):
+    """DRAM bytes per launch from a committed ncu summary (bytes per pooled row, scaled to
+    n_rows), if it was taken on the current kernel sources ``srcs`` (else None)."""
     try:
         h = hashlib.sha256()
-        for src in SCORE_SRCS:
+        for src in srcs:
             with open(src, "rb") as f:
                 h.update(f.read())
         sha = h.hexdigest()[:16]
         kv = {}
-        with open(TRAFFIC_FILE) as f:
+        with open(path) as f:
             for ln in f:
                 if "=" in ln and not ln.startswith("#"):
                     k, v = ln.split("=", 1)
                     kv[k.strip()] = v.strip()
         if kv.get("kernel_source_sha256_16") != sha:
             return None
-        per_row = float(kv["dram_bytes_per_row"])
-        return per_row * n_rows_primary
+        return float(kv["dram_bytes_per_row"]) * n_rows
     except Exception:
         return None
 
@@ -314,6 +317,29 @@ def run_context(name, args, world, rank, local, want_clocks, pooled="f32", n_q=1
             graph_err = f"{type(e).__name__}: {e}"[:200]
         torch.cuda.synchronize()
 
+    # the step's own score kernel (pool update of the new / open rows + scan of every row +
+    # the top-k histogram), live: each layer set's step captured, all kernels but the score
+    # kernel dropped from the graph, the rest replayed over the rotating layer sets
+    step_score_us, step_score_err = None, None
+    if not light:
+        try:
+            def cap_of(li):
+                def cap(stream_ptr):
+                    layers[li].step_ptr(n_ctx[li] + n_q - 1, q_ptrs[li][0][0], q_ptrs[li][1][0],
+                                        stream_ptr, n_q)
+                return cap
+
+            step_score_us = step_kernel_us([cap_of(li) for li in range(L)], 0,
+                                           SCORE_POOL_THREADS, max(3, K // L), dev)
+        except Exception as e:
+            step_score_err = f"{type(e).__name__}: {e}"[:200]
+        finally:
+            for li in range(L):
+                layers[li].n_valid_full = (n_ctx[li] - 1) // 4
+                # the replays added to the top-k histograms: start the next step from zero
+                layers[li].workspace.zero_()
+            torch.cuda.synchronize()
+
     # score kernel alone, back to back over the rotating layers (its average duration)
     n_rows = [(c + 3) // 4 for c in n_ctx]
 
@@ -380,6 +406,8 @@ def run_context(name, args, world, rank, local, want_clocks, pooled="f32", n_q=1
         "t_e2e": t_e2e, "k_e2e": k_e2e, "host_issue_us": t_issue * 1e6 / K, "h2d": h2d, "d2h": d2h, "clocks": clocks,
         "n_cells": n_cells_last, "shape": shape, "n_ctx_end": max(n_ctx),
         "graph_us": graph_us, "graph_err": graph_err, "pooled": pooled, "n_q": n_q,
+        "step_score_us": step_score_us, "step_score_err": step_score_err,
+        "step_score_rows": sum((c + n_q - 1 + 3) // 4 for c in n_ctx) / L,
     }
     del layers, caches
     torch.cuda.empty_cache()
@@ -413,6 +441,99 @@ def graph_time_us(fns, reps, dev):
     torch.cuda.synchronize()
     del graph
     return a.elapsed_time(b) * 1e3 / reps
+
+
+class _KernelNodeParams(__import__("ctypes").Structure):
+    """CUDA_KERNEL_NODE_PARAMS_v2 of the driver API (the fields read here)."""
+    import ctypes as _ct
+    _fields_ = [("func", _ct.c_void_p), ("gridDimX", _ct.c_uint), ("gridDimY", _ct.c_uint),
+                ("gridDimZ", _ct.c_uint), ("blockDimX", _ct.c_uint), ("blockDimY", _ct.c_uint),
+                ("blockDimZ", _ct.c_uint), ("sharedMemBytes", _ct.c_uint),
+                ("kernelParams", _ct.c_void_p), ("extra", _ct.c_void_p), ("kern", _ct.c_void_p),
+                ("ctx", _ct.c_void_p)]
+
+
+def step_kernel_us(captures, keep, block_x, reps, dev):
+    """Live device time of one kernel of the decode step, as the step runs it: each function
+    of ``captures`` issues one decode step (three kernels) on the stream it is given, which
+    is captured into a CUDA graph through the driver API; a clone of each graph keeps only
+    the kernel at position ``keep`` (checked by its block size, ``block_x``), and the
+    one-kernel graphs are replayed round-robin between CUDA events on one stream (so they
+    run one after another, as inside the steps).  Returns microseconds per kernel.  The kept
+    kernels read and write exactly what they do inside the step."""
+    import ctypes
+
+    import torch
+
+    cu = ctypes.CDLL("libcuda.so.1")
+    V = ctypes.c_void_p
+
+    def ck(r, what):
+        if r != 0:
+            raise RuntimeError(f"{what}: CUresult {r}")
+
+    gs = torch.cuda.Stream(device=dev)
+    gs.wait_stream(torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    h = V(gs.cuda_stream)
+    graphs, execs = [], []
+    try:
+        for capture in captures:
+            graph = V()
+            ck(cu.cuStreamBeginCapture_v2(h, ctypes.c_int(2)), "cuStreamBeginCapture")  # relaxed
+            try:
+                capture(gs.cuda_stream)
+            finally:
+                r_end = cu.cuStreamEndCapture(h, ctypes.byref(graph))
+            ck(r_end, "cuStreamEndCapture")
+            graphs.append(graph)
+            n = ctypes.c_size_t(0)
+            ck(cu.cuGraphGetNodes(graph, None, ctypes.byref(n)), "cuGraphGetNodes")
+            nodes = (V * n.value)()
+            ck(cu.cuGraphGetNodes(graph, nodes, ctypes.byref(n)), "cuGraphGetNodes")
+            kern = []
+            for i in range(n.value):
+                t = ctypes.c_int(-1)
+                ck(cu.cuGraphNodeGetType(V(nodes[i]), ctypes.byref(t)), "cuGraphNodeGetType")
+                if t.value == 0:  # CU_GRAPH_NODE_TYPE_KERNEL
+                    kern.append(nodes[i])
+            if len(kern) != 3:
+                raise RuntimeError(f"{len(kern)} kernel nodes in one step")
+            kept = kern[keep]
+            prm = _KernelNodeParams()
+            ck(cu.cuGraphKernelNodeGetParams_v2(V(kept), ctypes.byref(prm)), "params")
+            if prm.blockDimX != block_x:
+                raise RuntimeError(f"kept kernel has {prm.blockDimX} threads, not {block_x}")
+            clone = V()
+            ck(cu.cuGraphClone(ctypes.byref(clone), graph), "cuGraphClone")
+            graphs.append(clone)
+            for i in range(n.value):
+                if nodes[i] == kept:
+                    continue
+                cn = V()
+                ck(cu.cuGraphNodeFindInClone(ctypes.byref(cn), V(nodes[i]), clone), "find")
+                ck(cu.cuGraphDestroyNode(cn), "cuGraphDestroyNode")
+            ex = V()
+            ck(cu.cuGraphInstantiateWithFlags(ctypes.byref(ex), clone, ctypes.c_ulonglong(0)),
+               "cuGraphInstantiate")
+            execs.append(ex)
+        for ex in execs:
+            ck(cu.cuGraphLaunch(ex, h), "cuGraphLaunch")
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(gs)
+        for _ in range(reps):
+            for ex in execs:
+                ck(cu.cuGraphLaunch(ex, h), "cuGraphLaunch")
+        b.record(gs)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) * 1e3 / (reps * len(execs))
+    finally:
+        torch.cuda.synchronize()
+        for ex in execs:
+            cu.cuGraphExecDestroy(ex)
+        for g in graphs:
+            cu.cuGraphDestroy(g)
 
 
 def run_prefill(args, local, pooled_kind="f32"):
@@ -893,11 +1014,38 @@ def main():
     sh = r["shape"]
     value = sweep[args.primary]["steps_per_s"]
     pes = 2 if args.pooled == "bf16" else 4
-    score_bytes = (r["score_rows"] * sh.H_idx * sh.d_idx * pes
-                   + args.queries * r["score_rows"] * 4)
-    achieved = score_bytes / (r["score_us"] * 1e-6) / 1e9
     default_form = args.pooled == "f32" and args.queries == 1
-    traffic = traffic_per_launch(int(r["score_rows"])) if default_form else None
+
+    def row_bytes(rows):
+        # per pooled row: the row read once, one fp32 score written per query
+        return rows * (sh.H_idx * sh.d_idx * pes + args.queries * 4)
+
+    # the standalone scan (qsa_index_score) and, when it could be timed, the step's own
+    # fused score kernel (the step's dominant kernel)
+    scan_GBps = row_bytes(r["score_rows"]) / (r["score_us"] * 1e-6) / 1e9
+    scan = {"kernel": "score_stream_kernel (qsa_index_score alone)", "us": r["score_us"],
+            "rows": r["score_rows"], "achieved": scan_GBps, "frac": scan_GBps / peak,
+            "traffic": traffic_per_launch(TRAFFIC_FILE, SCORE_SRCS, r["score_rows"])
+            if default_form else None}
+    in_step = None
+    if r.get("step_score_us"):
+        st_GBps = row_bytes(r["step_score_rows"]) / (r["step_score_us"] * 1e-6) / 1e9
+        in_step = {"kernel": "score_pool_kernel (inside qsa_decode_step: open-row update, "
+                             "scan, top-k histogram)",
+                   "us": r["step_score_us"], "rows": r["step_score_rows"], "achieved": st_GBps,
+                   "frac": st_GBps / peak,
+                   "traffic": traffic_per_launch(STEP_TRAFFIC_FILE, STEP_SCORE_SRCS,
+                                                 r["step_score_rows"]) if default_form else None}
+    main_k = in_step or scan
+    peak_src = (f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
+                if peak_kind == "measured" else "fallback 6.8 TB/s")
+    roofline = {"bound": "hbm", "achieved": main_k["achieved"], "peak": peak, "unit": "GB/s",
+                "frac": main_k["frac"], "traffic": main_k["traffic"],
+                "kernel": f"{main_k['kernel']}; {args.pooled} cache, {args.queries} "
+                          f"quer{'y' if args.queries == 1 else 'ies'}",
+                "us_per_launch": main_k["us"], "peak_source": peak_src,
+                "scan_alone": scan, "in_step": in_step,
+                "in_step_err": r.get("step_score_err")}
 
     prefill = None if args.no_prefill else run_prefill(args, local)
     mask = None if args.no_mask else run_mask(args, local)
@@ -931,12 +1079,7 @@ def main():
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded N(0,1) keys/values/queries, 1% of blocks +3 on raw indexer keys)",
         "config": config_for(sh, args.layers, args.pooled, args.queries),
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": traffic,
-                     "kernel": f"score_stream_kernel (qsa_index_score, decode, {args.pooled} "
-                               f"cache, {args.queries} quer{'y' if args.queries == 1 else 'ies'})",
-                     "peak_source": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
-                     if peak_kind == "measured" else "fallback 6.8 TB/s"},
+        "roofline": roofline,
         "e2e": ({"value": sweep[args.primary]["e2e_steps_per_s"], "unit": "steps/s",
                  "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]}
                 if "e2e_steps_per_s" in sweep[args.primary] else None),
