@@ -25,6 +25,8 @@ from ._binding import (  # noqa: F401
     mask_to_list,
     pool_update,
     sparse_attn,
+    sparse_attn_union,
+    sparse_attn_union_workspace_size,
     sparse_attn_workspace_size,
     status_str,
     topk_blocks,

@@ -43,6 +43,9 @@ _SIGNATURES = {
     "qsa_sparse_attn": (_int, [_p, _i64, _int, _int, _int, _int, _f, _p, _p, _int, _i64, _i64,
                                _i64, _p, _p, _i64, _p, _p, _p, _sz, _p]),
     "qsa_sparse_attn_workspace_size": (_sz, [_i64, _int, _int, _int, _i64]),
+    "qsa_sparse_attn_union": (_int, [_p, _i64, _int, _int, _int, _f, _p, _p, _int, _i64, _i64,
+                                     _i64, _p, _p, _i64, _p, _p, _p, _sz, _p]),
+    "qsa_sparse_attn_union_workspace_size": (_sz, [_i64, _i64]),
     "qsa_decode_step": (_int, [_p, _int, _i64, _int, _int, _p, _f, _d, _p, _int, _i64, _i64,
                                _i64, _p, _f, _p, _i64, _p, _p, _p, _p, _int, _i64, _int, _int,
                                _i64, _p, _p, _i64, _p, _int, _f, _p, _p, _p, _sz, _p]),
@@ -223,6 +226,25 @@ def sparse_attn(q, K, V, n_cells, max_cells, out, H_kv, d_k, d_v, scale, pos=Non
         _ptr(q), n_q, H_q, H_kv, d_k, d_v, scale, _ptr(K), _ptr(V), _dtype(K), n_kv, ld_k, ld_v,
         _ptr(pos), _ptr(n_cells), max_cells, _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes,
         _stream(stream)))
+
+
+def sparse_attn_union(q, K, V, n_cells, max_cells, out, H_kv, d, scale, pos, lse=None,
+                      workspace=None, ld_k=None, ld_v=None, n_kv=None, stream=None):
+    """qsa_sparse_attn_union: q [n_q][H_q][d] fp32, groups of 16 consecutive queries over the
+    union of their lists (bf16 K/V, d 128, 8 query heads per KV head)."""
+    n_q, H_q = q.shape[0], q.shape[1]
+    ld_k = _ld(K) if ld_k is None else ld_k
+    ld_v = _ld(V) if ld_v is None else ld_v
+    n_kv = K.shape[0] if n_kv is None else n_kv
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("qsa_sparse_attn_union", load().qsa_sparse_attn_union(
+        _ptr(q), n_q, H_q, H_kv, d, scale, _ptr(K), _ptr(V), _dtype(K), n_kv, ld_k, ld_v,
+        _ptr(pos), _ptr(n_cells), max_cells, _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes,
+        _stream(stream)))
+
+
+def sparse_attn_union_workspace_size(n_q, max_cells) -> int:
+    return int(load().qsa_sparse_attn_union_workspace_size(n_q, max_cells))
 
 
 def decode_step(raw_k, n_ctx, H_idx, d_idx, norm_w, eps, rope_base, pooled, n_valid_full,

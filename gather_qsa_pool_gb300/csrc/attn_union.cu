@@ -1,0 +1,733 @@
+// attn_union.cu -- grouped-union sparse attention for many consecutive queries (a prefill
+// chunk): every group of 16 consecutive queries attends over one dense sequence of K / V
+// tiles, the union of the 4-cell blocks its queries selected, on the tcgen05 tensor cores;
+// each query's rows are masked to that query's own cells.
+//
+// Source: Qiita, ariera, EVO-X2 + Qwen3.8-Flash-Next llama.cpp series part 10, section on
+// profiling the Vulkan build (its r2 / r3 table: "QSA union" OFF 221.44 -> ON 263.28 tok/s
+// of prompt processing, token generation unchanged) and the COMMON-004 results section (r2's
+// grouped-union keeps 128k / 256k prompt processing far ahead of r3, which lacks it).  The
+// pages name grouped-union but do not describe it; the form below is this library's reading:
+// queries of a chunk that share selected blocks read each shared block once.
+//
+// Result: for query i and head h, exactly the attention qsa_sparse_attn computes over the
+// query's own list (softmax over its cells only), up to rounding.
+//
+// Kernel 1, union_build_kernel (one CTA per group): a bitmap over the cache's 4-cell blocks
+// collects every block a listed cell of the group falls in; a block scan of its words ranks
+// the blocks; the union block list is written in ascending order, and for every query one
+// bit per union cell (4 per block) says whether the cell is in that query's list.
+//
+// Kernel 2, attn_union_kernel (one CTA per group and KV head; M = 16 queries x 8 heads =
+// 128 rows): warp 0 stages the union's blocks 16 at a time (a 64-cell tile of K and one of
+// V: one 3-D TMA box of 4 cells x 64 dims per block and half, 128-byte swizzle) into a ring
+// of three stages; warp 1 issues the MMAs -- S = Q K^T (N 64 cells, K 128 dims; the query's
+// bf16 high and low halves, pre-scaled by scale * log2 e) into one of two tensor-memory
+// buffers, then O += P V (N 128 dims, K 64 cells, V read MN-major; P's high and low
+// halves) into a third; warps 2-5 (one thread per row) read S, mask it with the row's
+// membership bits, keep an online maximum that is moved (and O rescaled in tensor memory)
+// only when it grows by more than 2^8, write P to shared memory in the operand layout, and
+// at the end divide O by the row sum.  Every mbarrier wait is bounded: on a timeout the
+// rows of the CTA become NaN, nothing new is issued, what was issued is waited for (bounded)
+// and the tensor memory is returned.
+#include <cuda.h>
+
+#include "attn_union.cuh"
+
+namespace qsa {
+namespace {
+
+constexpr int kUG = kUnionGroup;        // queries per group
+constexpr int kUHeads = 8;              // query heads per KV head
+constexpr int kUM = kUG * kUHeads;      // 128 rows
+constexpr int kUD = 128;                // head dim
+constexpr int kUTB = 16;                // union blocks per tile
+constexpr int kUTC = 4 * kUTB;          // 64 cells per tile
+constexpr int kUStages = 3;
+constexpr int kUThreads = 192;          // warp 0 TMA, warp 1 MMA, warps 2-5 softmax
+constexpr float kURescale = 8.0f;       // move the running maximum past 2^8 growth
+constexpr int kUMaxBlockWords = 8192;   // bitmap words: 2^18 blocks = 2^20 cells
+
+constexpr uint32_t kQHalf = kUM * 128;              // 16 KB: 128 rows x 64 dims bf16
+constexpr uint32_t kQBytes = 2 * kQHalf;            // 32 KB: one of Q's two bf16 halves
+constexpr uint32_t kPBytes = kUM * 128;             // 16 KB: 128 rows x 64 cells bf16
+constexpr uint32_t kTileHalf = kUTC * 128;          // 8 KB: 64 cells x 64 dims bf16
+constexpr uint32_t kTileBytes = 2 * kTileHalf;      // 16 KB: one tensor's 64-cell tile
+constexpr uint32_t kStageBytes = 2 * kTileBytes;    // K and V
+constexpr uint32_t kTmemCols = 256;                 // S[0], S[1] (64 each), O (128)
+
+__host__ __device__ constexpr size_t union_smem_bytes()
+{
+    return 1024 + 2 * (size_t)kQBytes + 2 * (size_t)kPBytes + (size_t)kUStages * kStageBytes +
+           256;
+}
+
+// Union capacity in blocks for lists of up to max_cells cells: a list of whole blocks plus
+// one partial block spans at most ceil(max_cells / 4) + 1 blocks.  Whole tiles.
+__host__ __device__ inline int64_t union_cap_blocks(int64_t max_cells)
+{
+    const int64_t per_q = (max_cells + 3) / 4 + 1;
+    return ((kUG * per_q + kUTB - 1) / kUTB) * kUTB;
+}
+
+// Per-group workspace: [count, pad] int32 x 4 | blocks [cap] int32 | membership
+// [cap / 16 tiles][16 queries][2 words].
+__host__ __device__ inline int64_t union_group_words(int64_t max_cells)
+{
+    const int64_t cap = union_cap_blocks(max_cells);
+    return 4 + cap + (cap / kUTB) * kUG * 2;
+}
+
+// ------------------------------------------------------------------ kernel 1: the unions
+
+__global__ void __launch_bounds__(1024)
+union_build_kernel(const int32_t *__restrict__ pos, const int32_t *__restrict__ n_cells,
+                   int64_t max_cells, int64_t n_q, int64_t n_kv, uint32_t *__restrict__ ws)
+{
+    extern __shared__ __align__(16) uint32_t ush[];
+    const int64_t cap = union_cap_blocks(max_cells);
+    const int mwords = (int)(cap / 8);                 // membership words per query
+    const int nblk = (int)((n_kv + 3) / 4);
+    const int nwords = (nblk + 31) / 32;
+    uint32_t *bits = ush;                              // [nwords]
+    uint32_t *base = bits + nwords;                    // [nwords] exclusive prefix of popcounts
+    uint32_t *mem = base + nwords;                     // [16][mwords]
+    __shared__ uint32_t warp_tot[32];
+
+    pdl_wait();
+    QSA_AFTER_WAIT(pos);
+    QSA_AFTER_WAIT(n_cells);
+    pdl_trigger();
+
+    const int64_t g = blockIdx.x, q0 = g * kUG;
+    const int nq = (int)min((int64_t)kUG, n_q - q0);
+    uint32_t *gw = ws + g * union_group_words(max_cells);
+    const int tid = threadIdx.x, nt = blockDim.x;
+    for (int w = tid; w < nwords; w += nt) bits[w] = 0u;
+    for (int w = tid; w < kUG * mwords; w += nt) mem[w] = 0u;
+    __syncthreads();
+
+    // every valid cell of every (non-truncated) list marks its block
+    for (int li = 0; li < nq; ++li) {
+        const int64_t n = n_cells[q0 + li];
+        if (n < 0 || n > max_cells) continue;
+        const int32_t *pl = pos + (q0 + li) * max_cells;
+        for (int64_t e = tid; e < n; e += nt) {
+            const int32_t c = pl[e];
+            if (c < 0 || c >= n_kv) continue;
+            const int b = c >> 2;
+            atomicOr(&bits[b >> 5], 1u << (b & 31));
+        }
+    }
+    __syncthreads();
+
+    // exclusive scan of the words' popcounts: each thread a contiguous run of words
+    const int per = (nwords + nt - 1) / nt;
+    const int w0 = tid * per, w1 = min(nwords, w0 + per);
+    uint32_t run = 0;
+    for (int w = w0; w < w1; ++w) run += __popc(bits[w]);
+    const int lane = tid & 31, warp = tid >> 5;
+    uint32_t incl = run;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        uint32_t t = lane < (nt >> 5) ? warp_tot[lane] : 0u;
+        uint32_t ti = t;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t v = __shfl_up_sync(0xffffffffu, ti, o);
+            if (lane >= o) ti += v;
+        }
+        warp_tot[lane] = ti - t;  // exclusive prefix of the warps' totals
+    }
+    __syncthreads();
+    uint32_t acc = warp_tot[warp] + incl - run;
+    for (int w = w0; w < w1; ++w) {
+        base[w] = acc;
+        acc += __popc(bits[w]);
+    }
+    __syncthreads();
+    const uint32_t total = nwords ? base[nwords - 1] + __popc(bits[nwords - 1]) : 0u;
+    if ((int64_t)total > cap) {
+        // lists spanning more blocks than the workspace holds: the group's rows become NaN
+        if (tid == 0) gw[0] = 0xffffffffu;
+        return;
+    }
+    // the union's blocks, ascending
+    int32_t *ublk = reinterpret_cast<int32_t *>(gw + 4);
+    for (int w = w0; w < w1; ++w) {
+        uint32_t m = bits[w];
+        uint32_t r = base[w];
+        while (m) {
+            const int bit = __ffs(m) - 1;
+            m &= m - 1;
+            ublk[r++] = w * 32 + bit;
+        }
+    }
+    // membership: bit 4j + (c & 3) of query li's words for cell c of union block j
+    for (int li = 0; li < nq; ++li) {
+        const int64_t n = n_cells[q0 + li];
+        if (n < 0 || n > max_cells) continue;
+        const int32_t *pl = pos + (q0 + li) * max_cells;
+        for (int64_t e = tid; e < n; e += nt) {
+            const int32_t c = pl[e];
+            if (c < 0 || c >= n_kv) continue;
+            const int b = c >> 2;
+            const uint32_t j = base[b >> 5] + __popc(bits[b >> 5] & ((1u << (b & 31)) - 1u));
+            const uint32_t k = 4 * j + (uint32_t)(c & 3);
+            atomicOr(&mem[li * mwords + (k >> 5)], 1u << (k & 31));
+        }
+    }
+    __syncthreads();
+    // out in tile-major order: [tile][query][2 words], 64 cells per tile
+    uint32_t *gm = gw + 4 + cap;
+    const int n_tiles = (int)((total + kUTB - 1) / kUTB);
+    for (int e = tid; e < n_tiles * kUG * 2; e += nt) {
+        const int t = e / (kUG * 2), li = (e / 2) % kUG, k = e & 1;
+        gm[e] = li < nq ? mem[li * mwords + 2 * t + k] : 0u;
+    }
+    if (tid == 0) gw[0] = total;
+}
+
+// ------------------------------------------------------------------ tcgen05 helpers
+
+// K-major operand, 128-byte swizzle: rows of 128 bytes, 8-row groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t desc_kmajor_sw128(uint32_t saddr)
+{
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)(16u >> 4) << 16;       // leading byte offset: unused here
+    d |= (uint64_t)(1024u >> 4) << 32;     // stride byte offset: next 8 rows
+    d |= (uint64_t)1 << 46;                // descriptor version
+    d |= (uint64_t)2 << 61;                // 128-byte swizzle
+    return d;
+}
+
+// MN-major operand, 128-byte swizzle: each 128-byte row holds 64 consecutive N elements of
+// one k; the next 64 N elements start `mn_stride` bytes on (leading byte offset); the next
+// 8 k rows 1024 bytes on (stride byte offset).
+__device__ __forceinline__ uint64_t desc_mnmajor_sw128(uint32_t saddr, uint32_t mn_stride)
+{
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)((mn_stride >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)(1024u >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, M 128, the given N,
+// B MN-major when b_mn.
+__host__ __device__ constexpr uint32_t idesc_m128(int n, bool b_mn)
+{
+    return (1u << 4) | (1u << 7) | (1u << 10) | (b_mn ? (1u << 16) : 0u) |
+           ((uint32_t)(n >> 3) << 17) | ((uint32_t)(kUM >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma_m128(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive on the barrier once every MMA this thread issued so far has completed.
+__device__ __forceinline__ void umma_commit(uint64_t *bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, int x, int y, int z,
+                                            uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float *v)
+{
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float *v)
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+        "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+        "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+        "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+        "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+        "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
+        "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
+        "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+        "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
+        "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
+        "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+        : "memory");
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi)
+{
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// Row r of a K-major 128-byte-swizzled operand whose rows are 128 bytes: 16-byte chunk c
+// of the row sits at chunk c ^ (r & 7) of the row's 128 bytes.
+__device__ __forceinline__ void st_row_sw128(unsigned char *tile, int r, const uint32_t *w)
+{
+    unsigned char *row = tile + (r >> 3) * 1024 + (r & 7) * 128;
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<uint4 *>(row + ((c ^ (r & 7)) << 4)) =
+            make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+}
+
+// ------------------------------------------------------------------ kernel 2: attention
+
+__global__ void __launch_bounds__(kUThreads, 1)
+attn_union_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                  const float *__restrict__ q, int64_t n_q, int H_q, float scale_log2,
+                  const int32_t *__restrict__ n_cells, int64_t max_cells,
+                  const uint32_t *__restrict__ ws, float *__restrict__ out,
+                  float *__restrict__ lse)
+{
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    unsigned char *sb = reinterpret_cast<unsigned char *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    unsigned char *sQh = sb;                         // [2 dim halves][128 rows][128 B]
+    unsigned char *sQl = sQh + kQBytes;
+    unsigned char *sPh = sQl + kQBytes;              // [128 rows][128 B]
+    unsigned char *sPl = sPh + kPBytes;
+    unsigned char *sKV = sPl + kPBytes;              // [stage][K, V][2 halves][64 cells][128 B]
+    uint64_t *kv_full = reinterpret_cast<uint64_t *>(sKV + kUStages * kStageBytes);
+    uint64_t *kv_empty = kv_full + kUStages;
+    uint64_t *s_full = kv_empty + kUStages;          // [2]
+    uint64_t *s_empty = s_full + 2;                  // [2]
+    uint64_t *p_full = s_empty + 2;
+    uint64_t *o_done = p_full + 1;
+    uint64_t *q_ready = o_done + 1;
+    uint64_t *drain = q_ready + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int64_t g = blockIdx.x;
+    const int kvh = blockIdx.y;
+    const int64_t gwords = union_group_words(max_cells);
+    const int64_t cap = union_cap_blocks(max_cells);
+
+    if (tid == 0) {
+        for (int s = 0; s < kUStages; ++s) {
+            mbar_init(&kv_full[s], 1);
+            mbar_init(&kv_empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&s_full[b], 1);
+            mbar_init(&s_empty[b], 4);
+        }
+        mbar_init(p_full, 4);
+        mbar_init(o_done, 1);
+        mbar_init(q_ready, 4);
+        mbar_init(drain, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(tmem_slot)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    pdl_wait();
+    QSA_AFTER_WAIT(q);
+    QSA_AFTER_WAIT(n_cells);
+    QSA_AFTER_WAIT(ws);
+    pdl_trigger();
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    const uint32_t tmem = *tmem_slot;
+
+    const uint32_t *gw = ws + g * gwords;
+    const uint32_t ucount = gw[0];
+    const bool bad_group = ucount == 0xffffffffu;
+    const int n_tiles = bad_group ? 0 : (int)((ucount + kUTB - 1) / kUTB);
+    const int32_t *ublk = reinterpret_cast<const int32_t *>(gw + 4);
+    const uint32_t *gmem = gw + 4 + cap;
+    bool ok = true;
+
+    if (warp == 0) {
+        // ---- producer: lane = 2 * (block in tile) + dim half; K and V boxes of 4 cells
+        const int j = lane >> 1, half = lane & 1;
+        int armed = 0;
+        int32_t blk_next = 0;
+        if (n_tiles > 0) {
+            const int64_t u = j;
+            blk_next = u < ucount ? ublk[u] : ublk[0];
+        }
+        for (int t = 0; t < n_tiles; ++t, ++armed) {
+            const int s = t % kUStages;
+            const int32_t blk = blk_next;
+            if (t + 1 < n_tiles) {  // the next tile's block index, one tile ahead
+                const int64_t u = (int64_t)(t + 1) * kUTB + j;
+                blk_next = u < ucount ? ublk[u] : ublk[0];
+            }
+            // every lane waits; the warp goes on only if all of them saw the stage free
+            const bool freed =
+                t < kUStages || mbar_wait(&kv_empty[s], (uint32_t)((t / kUStages) - 1) & 1u);
+            if (!__all_sync(0xffffffffu, freed)) {
+                ok = false;
+                break;
+            }
+            if (lane == 0) mbar_arrive_expect_tx(&kv_full[s], kStageBytes);
+            __syncwarp();
+            unsigned char *st = sKV + s * kStageBytes;
+            const uint32_t off = half * kTileHalf + j * 512;
+            tma_load_3d(st + off, &tmK, half * 64, kvh, 4 * blk, &kv_full[s]);
+            tma_load_3d(st + kTileBytes + off, &tmV, half * 64, kvh, 4 * blk, &kv_full[s]);
+        }
+        // every armed stage lands before the CTA may leave
+        for (int s = 0; s < kUStages && lane == 0; ++s) {
+            const int uses = armed / kUStages + (s < armed % kUStages ? 1 : 0);
+            if (uses > 0 && !mbar_wait(&kv_full[s], (uint32_t)(uses - 1) & 1u)) ok = false;
+        }
+    } else if (warp == 1) {
+        // ---- MMA issuer (one thread)
+        if (lane == 0) {
+            constexpr uint32_t id_s = idesc_m128(kUTC, false);
+            constexpr uint32_t id_o = idesc_m128(kUD, true);
+            if (n_tiles > 0 && !mbar_wait(q_ready, 0)) ok = false;
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            const uint32_t qh = smem_u32(sQh), ql = smem_u32(sQl);
+            const uint32_t ph = smem_u32(sPh), pl = smem_u32(sPl);
+            for (int t = 0; ok && t <= n_tiles; ++t) {
+                if (t < n_tiles) {
+                    const int s = t % kUStages, b = t & 1;
+                    if (!mbar_wait(&kv_full[s], (uint32_t)(t / kUStages) & 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    if (t >= 2 && !mbar_wait(&s_empty[b], (uint32_t)((t >> 1) - 1) & 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                    const uint32_t kb = smem_u32(sKV + s * kStageBytes);
+                    uint32_t acc = 0;
+#pragma unroll
+                    for (int part = 0; part < 2; ++part) {
+                        const uint32_t qa = part ? ql : qh;
+#pragma unroll
+                        for (int k16 = 0; k16 < kUD / 16; ++k16) {
+                            const uint32_t hf = (uint32_t)(k16 >> 2), ko = (uint32_t)(k16 & 3) * 32;
+                            umma_m128(tmem + (uint32_t)(b * kUTC),
+                                      desc_kmajor_sw128(qa + hf * kQHalf + ko),
+                                      desc_kmajor_sw128(kb + hf * kTileHalf + ko), id_s, acc);
+                            acc = 1;
+                        }
+                    }
+                    umma_commit(&s_full[b]);
+                }
+                if (t >= 1) {
+                    const int tp = t - 1, sp = tp % kUStages;
+                    if (!mbar_wait(p_full, (uint32_t)tp & 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                    const uint32_t vb = smem_u32(sKV + sp * kStageBytes + kTileBytes);
+#pragma unroll
+                    for (int part = 0; part < 2; ++part) {
+                        const uint32_t pa = part ? pl : ph;
+#pragma unroll
+                        for (int k16 = 0; k16 < kUTC / 16; ++k16)
+                            umma_m128(tmem + 128u, desc_kmajor_sw128(pa + k16 * 32),
+                                      desc_mnmajor_sw128(vb + k16 * 2048, kTileHalf), id_o,
+                                      (tp > 0 || part > 0 || k16 > 0) ? 1u : 0u);
+                    }
+                    umma_commit(o_done);
+                    umma_commit(&kv_empty[sp]);
+                }
+            }
+            // every MMA issued has completed before the tensor memory is freed
+            umma_commit(drain);
+            if (!mbar_wait(drain, 0)) ok = false;
+        }
+    } else {
+        // ---- softmax / epilogue: one thread per row (row = 8 * query + head)
+        const int quarter = warp & 3;
+        const int r = quarter * 32 + lane;
+        const int li = r >> 3;
+        const int64_t qi = g * kUG + li;
+        const int h = kvh * kUHeads + (r & 7);
+        const bool live = qi < n_q;
+        int64_t n = live ? (int64_t)n_cells[qi] : 0;
+        const bool trunc = n > max_cells;
+        const uint32_t lrow = (uint32_t)(quarter * 32) << 16;
+        // the row's query, pre-scaled, as bf16 high and low halves in the operand layout
+        {
+            const float *qr = q + (qi * H_q + h) * (int64_t)kUD;
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                uint32_t wh[32], wl[32];
+#pragma unroll
+                for (int e = 0; e < 64; e += 2) {
+                    float x0 = 0.0f, x1 = 0.0f;
+                    if (live) {
+                        const float2 v = *reinterpret_cast<const float2 *>(qr + hf * 64 + e);
+                        x0 = v.x * scale_log2;
+                        x1 = v.y * scale_log2;
+                    }
+                    const float h0 = __bfloat162float(__float2bfloat16_rn(x0));
+                    const float h1 = __bfloat162float(__float2bfloat16_rn(x1));
+                    wh[e / 2] = pack_bf16(h0, h1);
+                    wl[e / 2] = pack_bf16(x0 - h0, x1 - h1);
+                }
+                st_row_sw128(sQh + hf * kQHalf, r, wh);
+                st_row_sw128(sQl + hf * kQHalf, r, wl);
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) mbar_arrive(q_ready);
+        }
+        float m_ref = -INFINITY, l = 0.0f;
+        uint32_t mw0 = 0, mw1 = 0;
+        if (n_tiles > 0) {
+            mw0 = gmem[li * 2];
+            mw1 = gmem[li * 2 + 1];
+        }
+        for (int t = 0; t < n_tiles; ++t) {
+            const int b = t & 1;
+            const uint32_t w0 = mw0, w1 = mw1;
+            if (t + 1 < n_tiles) {  // next tile's membership words, one tile ahead
+                const uint32_t *nm = gmem + ((int64_t)(t + 1) * kUG + li) * 2;
+                mw0 = nm[0];
+                mw1 = nm[1];
+            }
+            // waits are warp-uniform: the tensor-memory loads below need the whole warp
+            if (!__all_sync(0xffffffffu, mbar_wait(&s_full[b], (uint32_t)(t >> 1) & 1u))) {
+                ok = false;
+                break;
+            }
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            float x[kUTC];
+            tmem_ld32(tmem + lrow + (uint32_t)(b * kUTC), x);
+            tmem_ld32(tmem + lrow + (uint32_t)(b * kUTC + 32), x + 32);
+            asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s_empty[b]);
+            float mt = -INFINITY;
+#pragma unroll
+            for (int e = 0; e < kUTC; ++e) {
+                const bool in = ((e < 32 ? w0 >> e : w1 >> (e - 32)) & 1u) && !trunc && live;
+                x[e] = in ? x[e] : -INFINITY;
+                mt = fmaxf(mt, x[e]);
+            }
+            // P(t - 1) has been consumed (and O holds it) before P or O is touched
+            if (t > 0 && !__all_sync(0xffffffffu, mbar_wait(o_done, (uint32_t)(t - 1) & 1u))) {
+                ok = false;
+                break;
+            }
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            float alpha = 1.0f;
+            bool move = false;
+            if (mt > m_ref + kURescale) {  // also the first finite maximum (m_ref = -inf)
+                move = true;
+                alpha = m_ref == -INFINITY ? 0.0f : exp2f(m_ref - mt);
+            }
+            if (__any_sync(0xffffffffu, move && m_ref != -INFINITY)) {
+                // rescale O's row in tensor memory (the warp's 32 rows at once)
+#pragma unroll 1
+                for (int c = 0; c < kUD; c += 32) {
+                    float o[32];
+                    tmem_ld32(tmem + lrow + 128u + (uint32_t)c, o);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) o[e] *= alpha;
+                    tmem_st32(tmem + lrow + 128u + (uint32_t)c, o);
+                }
+            }
+            if (move) {
+                l *= alpha;
+                m_ref = mt;
+            }
+            uint32_t ph_w[32], pl_w[32];
+            float ls = 0.0f;
+#pragma unroll
+            for (int e = 0; e < kUTC; e += 2) {
+                const float p0 = x[e] == -INFINITY ? 0.0f : exp2f(x[e] - m_ref);
+                const float p1 = x[e + 1] == -INFINITY ? 0.0f : exp2f(x[e + 1] - m_ref);
+                ls += p0 + p1;
+                const float h0 = __bfloat162float(__float2bfloat16_rn(p0));
+                const float h1 = __bfloat162float(__float2bfloat16_rn(p1));
+                ph_w[e / 2] = pack_bf16(h0, h1);
+                pl_w[e / 2] = pack_bf16(p0 - h0, p1 - h1);
+            }
+            l += ls;
+            st_row_sw128(sPh, r, ph_w);
+            st_row_sw128(sPl, r, pl_w);
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) mbar_arrive(p_full);
+        }
+        if (ok && n_tiles > 0 &&
+            !__all_sync(0xffffffffu, mbar_wait(o_done, (uint32_t)(n_tiles - 1) & 1u)))
+            ok = false;
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        const bool nan_rows = !ok || bad_group || trunc;
+        const float inv = l > 0.0f ? 1.0f / l : 0.0f;
+#pragma unroll 1
+        for (int c = 0; c < kUD; c += 32) {
+            float o[32];
+            if (n_tiles > 0 && ok) {
+                tmem_ld32(tmem + lrow + 128u + (uint32_t)c, o);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) o[e] = 0.0f;
+            }
+            if (live) {
+                float *dst = out + (qi * H_q + h) * (int64_t)kUD + c;
+#pragma unroll
+                for (int e = 0; e < 32; e += 4)
+                    *reinterpret_cast<float4 *>(dst + e) =
+                        nan_rows ? make_float4(NAN, NAN, NAN, NAN)
+                                 : make_float4(o[e] * inv, o[e + 1] * inv, o[e + 2] * inv,
+                                               o[e + 3] * inv);
+            }
+        }
+        if (live && lse)
+            lse[qi * H_q + h] = nan_rows ? NAN
+                                         : (l > 0.0f ? (m_ref + log2f(l)) * 0.6931471805599453f
+                                                     : -INFINITY);
+    }
+
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    if (warp == 1)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(kTmemCols)
+                     : "memory");
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult qr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &qr) == cudaSuccess &&
+            qr == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+// 3-D map of a bf16 cache [n_kv rows of ld elements][H_kv heads][128 dims]: boxes of 64 dims
+// x 1 head x 4 cells, 128-byte swizzle, zero fill past the last row.
+bool make_kv_map(CUtensorMap *m, const void *base, int64_t n_kv, int H_kv, int64_t ld)
+{
+    EncodeTiledFn fn = encode_tiled_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)kUD, (cuuint64_t)H_kv, (cuuint64_t)n_kv};
+    const cuuint64_t strides[2] = {(cuuint64_t)kUD * 2, (cuuint64_t)ld * 2};
+    const cuuint32_t box[3] = {64, 1, 4};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+int64_t attn_union_max_kv() { return (int64_t)kUMaxBlockWords * 32 * 4; }
+
+size_t attn_union_workspace_bytes(int64_t n_q, int64_t max_cells)
+{
+    if (n_q <= 0 || max_cells < 0) return 0;
+    const int64_t groups = (n_q + kUG - 1) / kUG;
+    return (size_t)groups * (size_t)union_group_words(max_cells) * 4;
+}
+
+bool attn_union_shape_ok(qsa_dtype dt, int H_q, int H_kv, int d_k, int d_v, const void *K,
+                         const void *V, int64_t ld_k, int64_t ld_v)
+{
+    return dt == QSA_BF16 && H_kv >= 1 && H_q == kUHeads * H_kv && d_k == kUD && d_v == kUD &&
+           ld_k % 8 == 0 && ld_v % 8 == 0 && ld_k >= (int64_t)H_kv * kUD &&
+           ld_v >= (int64_t)H_kv * kUD &&
+           ((reinterpret_cast<uintptr_t>(K) | reinterpret_cast<uintptr_t>(V)) & 15) == 0;
+}
+
+qsa_status launch_attn_union(const float *q, int64_t n_q, int H_q, int H_kv, float scale,
+                             const void *K, const void *V, int64_t n_kv, int64_t ld_k,
+                             int64_t ld_v, const int32_t *pos, const int32_t *n_cells,
+                             int64_t max_cells, float *out, float *lse, void *workspace,
+                             cudaStream_t st)
+{
+    if (n_q == 0) return QSA_OK;
+    const int64_t groups = (n_q + kUG - 1) / kUG;
+    const int64_t cap = union_cap_blocks(max_cells);
+    const int nblk = (int)((n_kv + 3) / 4);
+    const int nwords = (nblk + 31) / 32;
+    const size_t bsmem = sizeof(uint32_t) * (2 * (size_t)nwords + (size_t)kUG * (cap / 8));
+    if (bsmem > 227 * 1024) return QSA_ERR_UNSUPPORTED;
+    CUtensorMap tmK, tmV;
+    if (n_kv > 0 && (!make_kv_map(&tmK, K, n_kv, H_kv, ld_k) || !make_kv_map(&tmV, V, n_kv, H_kv, ld_v)))
+        return QSA_ERR_CUDA;
+    if (n_kv == 0) {  // nothing to attend to: the maps are never read
+        memset(&tmK, 0, sizeof tmK);
+        memset(&tmV, 0, sizeof tmV);
+    }
+    uint32_t *ws = static_cast<uint32_t *>(workspace);
+    if (ensure_kernel_attrs<union_build_kernel>(bsmem) != cudaSuccess) return QSA_ERR_CUDA;
+    cudaError_t e = launch(union_build_kernel, dim3((unsigned)groups), dim3(1024), bsmem, st, 1, pos,
+                           n_cells, max_cells, n_q, n_kv, ws);
+    if (e != cudaSuccess) return QSA_ERR_CUDA;
+    if (ensure_kernel_attrs<attn_union_kernel>(union_smem_bytes()) != cudaSuccess)
+        return QSA_ERR_CUDA;
+    e = launch(attn_union_kernel, dim3((unsigned)groups, (unsigned)H_kv), dim3(kUThreads),
+               union_smem_bytes(), st, 1, tmK, tmV, q, n_q, H_q, scale * 1.4426950408889634f,
+               n_cells, max_cells, (const uint32_t *)ws, out, lse);
+    return e == cudaSuccess ? QSA_OK : QSA_ERR_CUDA;
+}
+
+}  // namespace qsa

@@ -7,6 +7,7 @@
 
 #include <atomic>
 
+#include "attn_union.cuh"
 #include "qsa_internal.cuh"
 
 namespace qsa {
@@ -61,7 +62,7 @@ const char *qsa_status_str(qsa_status s)
     return "QSA_ERR_UNKNOWN";
 }
 
-int qsa_version(void) { return (2 << 16) | 2; }
+int qsa_version(void) { return (2 << 16) | 3; }
 
 static qsa_status check_pool_update(const void *raw_k, qsa_dtype raw_dtype, int64_t n_ctx, int H,
                                     int d, const float *norm_w, float eps, double rope_base,
@@ -278,6 +279,37 @@ qsa_status qsa_sparse_attn(const float *q, int64_t n_q, int H_q, int H_kv, int d
     return from_cuda(launch_sparse_attn(q, n_q, H_q, H_kv, d_k, d_v, scale, K, V, dtype, n_kv,
                                         ld_k, ld_v, pos, n_cells, max_cells, out, lse_out,
                                         (float *)workspace, (cudaStream_t)stream));
+}
+
+size_t qsa_sparse_attn_union_workspace_size(int64_t n_q, int64_t max_cells)
+{
+    if (n_q <= 0 || max_cells < 0) return 0;
+    return attn_union_workspace_bytes(n_q, max_cells);
+}
+
+qsa_status qsa_sparse_attn_union(const float *q, int64_t n_q, int H_q, int H_kv, int d,
+                                 float scale, const void *K, const void *V, qsa_dtype dtype,
+                                 int64_t n_kv, int64_t ld_k, int64_t ld_v, const int32_t *pos,
+                                 const int32_t *n_cells, int64_t max_cells, float *out,
+                                 float *lse_out, void *workspace, size_t workspace_bytes,
+                                 qsa_stream_t stream)
+{
+    if (!q || !K || !V || !pos || !n_cells || !out) return QSA_ERR_INVALID_ARG;
+    if (n_q < 0 || H_q < 1 || H_kv < 1 || d < 1 || n_kv < 0 || max_cells < 0 || ld_k < 0 ||
+        ld_v < 0 || !valid_dtype(dtype))
+        return QSA_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(out, 16) || (lse_out && !aligned(lse_out, 4)) ||
+        !aligned(pos, 4) || !aligned(n_cells, 4))
+        return QSA_ERR_INVALID_ARG;
+    if (!attn_union_shape_ok(dtype, H_q, H_kv, d, d, K, V, ld_k, ld_v)) return QSA_ERR_UNSUPPORTED;
+    if (n_kv < 4 || n_kv > attn_union_max_kv() || max_cells > 2100 || H_kv > 65535 ||
+        (n_q + kUnionGroup - 1) / kUnionGroup > 0x7fffffffLL)
+        return QSA_ERR_UNSUPPORTED;
+    if (n_q == 0) return QSA_OK;
+    const size_t need = attn_union_workspace_bytes(n_q, max_cells);
+    if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return QSA_ERR_INVALID_ARG;
+    return launch_attn_union(q, n_q, H_q, H_kv, scale, K, V, n_kv, ld_k, ld_v, pos, n_cells,
+                             max_cells, out, lse_out, workspace, (cudaStream_t)stream);
 }
 
 static size_t align256(size_t b) { return (b + 255) & ~(size_t)255; }

@@ -64,7 +64,7 @@ const char *qsa_status_str(qsa_status s);
 
 /* Library ABI version: (major << 16) | minor.  Major 2: pooled-cache dtype arguments,
  * several queries per decode step, the host-fed decode step; minor 1: decode plans;
- * minor 2: qsa_mask_sparse_attn. */
+ * minor 2: qsa_mask_sparse_attn; minor 3: qsa_sparse_attn_union. */
 int qsa_version(void);
 
 /*
@@ -258,6 +258,47 @@ qsa_status qsa_sparse_attn(const float *q, int64_t n_q, int H_q, int H_kv, int d
  * inside a cluster (see qsa_sparse_attn_noalloc) leave the workspace untouched. */
 size_t qsa_sparse_attn_workspace_size(int64_t n_q, int H_q, int H_kv, int d_v,
                                       int64_t max_cells);
+
+/*
+ * qsa_sparse_attn_union -- qsa_sparse_attn for many consecutive queries (a prefill chunk),
+ * computed group by group over the union of each group's lists.
+ *
+ * Source: same page as qsa_pool_update, section on profiling the Vulkan build (its table of
+ * r2 with "QSA union" off / on: 221.44 -> 263.28 tok/s of prompt processing, token
+ * generation unchanged) and the COMMON-004 results section (r2's grouped-union keeps long
+ * prompt processing ahead).  The pages do not describe the mechanism; here queries of a
+ * chunk that selected the same blocks read each such block once.
+ *
+ * Queries are taken in groups of 16 consecutive ones (the last group may be short).  For a
+ * group, the union of the 4-cell blocks its listed cells fall in is staged once, as dense
+ * tiles, and every query attends over the whole tile sequence with its own cells only (the
+ * others masked).  Result: out[i][h][:] and lse_out[i][h] as qsa_sparse_attn over the same
+ * lists (up to rounding; a cell listed twice in one list counts once here), including the
+ * conventions for empty lists (out 0, lse -inf), truncated lists (n_cells[i] > max_cells:
+ * NaN) and cells outside [0, n_kv) (skipped).  The union wins over qsa_sparse_attn when the
+ * queries of a group share much of their selection; with independent selections it moves
+ * the same bytes and does about 16 times the arithmetic.
+ *
+ *   q, out   [n_q][H_q][128] fp32, 16-byte aligned;  lse_out [n_q][H_q] or NULL
+ *   K, V     bf16 caches, row strides ld_k, ld_v (multiples of 8 elements), 16-byte aligned;
+ *            KV head g of row c at K[c*ld_k + g*128]
+ *   pos      [n_q][max_cells] int32 cell lists;  n_cells [n_q] int32 device counts
+ *   workspace  qsa_sparse_attn_union_workspace_size(n_q, max_cells) bytes, 256-byte aligned
+ * Only this shape runs: bf16, d_k = d_v = 128, H_q = 8 * H_kv (QSA_ERR_UNSUPPORTED
+ * otherwise), 4 <= n_kv <= 2^20 (UNSUPPORTED), max_cells <= 2100 (UNSUPPORTED).  The union of
+ * one group may hold at most 16 * (ceil(max_cells/4) + 1) blocks -- always the case for
+ * lists of whole blocks plus one open block, as qsa_gather_kv writes; a group beyond it gets
+ * NaN outputs.  Errors: INVALID_ARG for null pointers, negative sizes, misaligned pointers or
+ * a short workspace.
+ */
+qsa_status qsa_sparse_attn_union(const float *q, int64_t n_q, int H_q, int H_kv, int d,
+                                 float scale, const void *K, const void *V, qsa_dtype dtype,
+                                 int64_t n_kv, int64_t ld_k, int64_t ld_v, const int32_t *pos,
+                                 const int32_t *n_cells, int64_t max_cells, float *out,
+                                 float *lse_out, void *workspace, size_t workspace_bytes,
+                                 qsa_stream_t stream);
+
+size_t qsa_sparse_attn_union_workspace_size(int64_t n_q, int64_t max_cells);
 
 /*
  * qsa_decode_step -- one decode step of one QSA layer: the five calls above in order,

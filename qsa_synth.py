@@ -331,3 +331,33 @@ def mask_attn_inputs(shape: MaskShape, seed: int):
     q = _normal(rng, (shape.n_q, shape.H_q, shape.d_k))
     KV = to_bf16_bits(_normal(rng, (shape.n_kv, shape.d_k)))
     return {"q": q, "KV": KV}
+
+
+# --------------------------------------------------------------------------- shared selections
+
+def overlap_block_lists(n_cand, k_blk: int, group: int, share: float, seed: int):
+    """Block lists with a stated overlap inside each group of ``group`` consecutive queries,
+    for measuring how attention over a group's union behaves as queries share more blocks.
+
+    n_cand[i] is how many blocks query i may pick from (blocks 0 .. n_cand[i]-1).  Each group
+    draws one common set of k_blk blocks from the blocks every member may pick; each query
+    takes round(share * k) of them (k = min(k_blk, n_cand[i])) and draws the rest uniformly
+    from its other candidates, without repeats.  Returns a list of ascending int32 arrays.
+    Only random draws: nothing of the method's arithmetic."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    n_cand = np.asarray(n_cand, np.int64)
+    out = []
+    for g0 in range(0, n_cand.shape[0], group):
+        members = n_cand[g0:g0 + group]
+        lo = int(members.min())
+        common = rng.choice(lo, size=min(k_blk, lo), replace=False) if lo > 0 else np.zeros(0, np.int64)
+        for nc in members:
+            k = int(min(k_blk, nc))
+            n_sh = min(int(round(share * k)), common.shape[0])
+            mine = rng.choice(common, size=n_sh, replace=False) if n_sh else np.zeros(0, np.int64)
+            taken = np.zeros(int(nc), bool)
+            taken[mine] = True
+            rest = np.flatnonzero(~taken)
+            extra = rng.choice(rest, size=k - n_sh, replace=False) if k > n_sh else np.zeros(0, np.int64)
+            out.append(np.sort(np.concatenate([mine, extra])).astype(np.int32))
+    return out

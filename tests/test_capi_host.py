@@ -147,6 +147,35 @@ def test_sparse_attn_rejects(lib):
     assert lib.qsa_sparse_attn_workspace_size(1024, 32, 4, 128, 2051) == 0  # one split
 
 
+def test_sparse_attn_union_rejects(lib):
+    s = None
+    a = P(0x10000)
+    ws_need = lib.qsa_sparse_attn_union_workspace_size(1024, 2051)
+    assert ws_need > 0
+    assert lib.qsa_sparse_attn_union_workspace_size(0, 2051) == 0
+    ok = dict(q=a, n_q=1024, H_q=32, H_kv=4, d=128, scale=0.1, K=a, V=a, dt=1, n_kv=256205,
+              ld_k=512, ld_v=512, pos=a, n_cells=a, max_cells=2051, out=a, lse=None,
+              ws=P(0x20000), ws_bytes=ws_need, st=s)
+
+    def call(**kw):
+        v = dict(ok, **kw)
+        return lib.qsa_sparse_attn_union(*v.values())
+
+    # every call below fails validation before anything is launched
+    assert call(pos=None) == 1                   # null list
+    assert call(q=P(0x10008)) == 1               # q not 16-byte aligned
+    assert call(n_q=-1) == 1
+    assert call(ws_bytes=ws_need - 1) == 1       # workspace too small
+    assert call(ws=P(0x20010)) == 1              # workspace not 256-byte aligned
+    assert call(dt=0) == 2                       # fp32 K/V: not built
+    assert call(d=64) == 2                       # head dim 64: not built
+    assert call(H_q=16) == 2                     # 4 query heads per KV head: not built
+    assert call(n_kv=(1 << 20) + 4) == 2         # beyond the union builder's bitmap
+    assert call(n_kv=3) == 2
+    assert call(max_cells=2101) == 2
+    assert call(ld_k=500) == 2                   # stride below the row
+
+
 def test_mask_to_list_rejects(lib):
     s = None
     assert lib.qsa_mask_to_list(None, 1, 64, 64, 8, FAKE, FAKE, None, s) == 1
