@@ -622,6 +622,70 @@ def run_prefill(args, local, pooled_kind="f32"):
     return out_d
 
 
+def run_grouped_union(args, local):
+    """Grouped-union attention (qsa_sparse_attn_union) against the per-query kernel
+    (qsa_sparse_attn) on the prefill chunk's shape -- 1024 queries after 255,181 tokens, 512
+    selected blocks each plus the open tail -- over a sweep of how many of its blocks each
+    query shares with the others of its group of 16 (qsa_synth.overlap_block_lists: the
+    share of each query's blocks drawn from one common set per group, the rest drawn
+    independently).  Each call captured in a CUDA graph and replayed; returns microseconds
+    per call, the union's mean size per group and the share from which the union wins."""
+    import torch
+
+    import gather_qsa_pool_gb300 as qsa
+    import qsa_synth
+
+    shape = qsa_synth.CONFIGS["prefill_256k"]
+    dev = torch.device("cuda", local)
+    n_q, n_ctx, d, H_kv, H_q = shape.n_q, shape.n_ctx, shape.d, shape.H_kv, shape.H_q
+    g = torch.Generator(device=dev)
+    g.manual_seed(5150)
+    K = torch.randn(n_ctx, H_kv, d, generator=g, device=dev).to(torch.bfloat16)
+    V = torch.randn(n_ctx, H_kv, d, generator=g, device=dev).to(torch.bfloat16)
+    q = torch.randn(n_q, H_q, d, generator=g, device=dev)
+    q_pos = shape.depth + np.arange(n_q)
+    q_pos_d = torch.from_numpy(q_pos.astype(np.int32)).to(dev)
+    scale = 1.0 / math.sqrt(d)
+    ws = torch.empty(qsa.sparse_attn_union_workspace_size(n_q, shape.max_cells),
+                     dtype=torch.uint8, device=dev)
+    out_u = torch.empty(n_q, H_q, d, device=dev)
+    out_r = torch.empty(n_q, H_q, d, device=dev)
+    pos = torch.empty(n_q, shape.max_cells, dtype=torch.int32, device=dev)
+    n_cells = torch.empty(n_q, dtype=torch.int32, device=dev)
+    rows = []
+    for share in (0.0, 0.5, 0.75, 0.85, 0.9, 0.95, 1.0):
+        blocks = qsa_synth.overlap_block_lists((q_pos + 1) // 4, shape.k_blk, 16, share,
+                                               int(1000 * share) + 7)
+        bl = np.zeros((n_q, shape.k_blk), np.int32)
+        cnt = np.zeros(n_q, np.int32)
+        for i, b in enumerate(blocks):
+            bl[i, :b.shape[0]] = b
+            cnt[i] = b.shape[0]
+        qsa.gather_kv(torch.from_numpy(bl).to(dev), torch.from_numpy(cnt).to(dev), shape.k_blk,
+                      pos, n_cells, shape.max_cells, q_pos=q_pos_d, n_kv=n_ctx)
+        union = float(np.mean([np.unique(np.concatenate(blocks[i:i + 16])).shape[0]
+                               for i in range(0, n_q, 16)]))
+        u_us = graph_time_us([lambda: qsa.sparse_attn_union(q, K, V, n_cells, shape.max_cells,
+                                                            out_u, H_kv, d, scale, pos,
+                                                            workspace=ws)],
+                             args.prefill_reps, dev)
+        r_us = graph_time_us([lambda: qsa.sparse_attn(q, K, V, n_cells, shape.max_cells, out_r,
+                                                      H_kv, d, d, scale, pos=pos)],
+                             args.prefill_reps, dev)
+        diff = float((out_u - out_r).abs().max().item())
+        rows.append({"share": share, "union_blocks_per_group": round(union, 1),
+                     "union_us": round(u_us, 1), "per_query_us": round(r_us, 1),
+                     "max_abs_diff": diff})
+    wins = [r["share"] for r in rows if r["union_us"] < r["per_query_us"]]
+    del K, V, q, ws, out_u, out_r, pos, n_cells
+    torch.cuda.empty_cache()
+    return {"workload": (f"{n_q} queries at positions {shape.depth:,}..{n_ctx - 1:,}, "
+                         f"{shape.k_blk} blocks + tail each, groups of 16, attention "
+                         f"{H_q}/{H_kv}x{d} bf16"),
+            "timing": "cuda graph replay", "sweep": rows,
+            "union_wins_from_share": min(wins) if wins else None}
+
+
 def run_ablation(args, local):
     """The pages' A/B on this GPU at 255,181 tokens: each piece of the QSA decode step next
     to the piece it replaced -- the full pooled-cache rebuild (before the incremental cache),
@@ -1050,6 +1114,7 @@ def main():
     prefill = None if args.no_prefill else run_prefill(args, local)
     mask = None if args.no_mask else run_mask(args, local)
     ablation = None if args.no_ablation else run_ablation(args, local)
+    grouped_union = None if args.no_prefill else run_grouped_union(args, local)
 
     cpu_baseline = None
     cpu_all_cores = None
@@ -1090,6 +1155,7 @@ def main():
         "prefill": prefill,
         "mask": mask,
         "ablation": ablation,
+        "grouped_union": grouped_union,
         "cpu_baseline": cpu_baseline,
         "cpu_baseline_all_cores": cpu_all_cores,
     }

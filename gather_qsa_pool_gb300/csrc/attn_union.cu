@@ -21,13 +21,14 @@
 // Kernel 2, attn_union_kernel (one CTA per group and KV head; M = 16 queries x 8 heads =
 // 128 rows): warp 0 stages the union's blocks 16 at a time (a 64-cell tile of K and one of
 // V: one 3-D TMA box of 4 cells x 64 dims per block and half, 128-byte swizzle) into a ring
-// of three stages; warp 1 issues the MMAs -- S = Q K^T (N 64 cells, K 128 dims; the query's
-// bf16 high and low halves, pre-scaled by scale * log2 e) into one of two tensor-memory
-// buffers, then O += P V (N 128 dims, K 64 cells, V read MN-major; P's high and low
-// halves) into a third; warps 2-5 (one thread per row) read S, mask it with the row's
-// membership bits, keep an online maximum that is moved (and O rescaled in tensor memory)
-// only when it grows by more than 2^8, write P to shared memory in the operand layout, and
-// at the end divide O by the row sum.  Every mbarrier wait is bounded: on a timeout the
+// of six stages; warp 1 issues the MMAs -- S = Q K^T (N 64 cells, K 128 dims; A is the
+// query's bf16 high and low halves, pre-scaled by scale * log2 e, held in tensor memory) into
+// one of two tensor-memory buffers, then O += P V (N 128 dims, K 64 cells, V read MN-major;
+// A is P's high and low halves, in one of two tensor-memory buffers) into a third; warps 2-5
+// (one thread per row) read S, mask it with the row's membership bits, keep an online
+// maximum that is moved (and O rescaled in tensor memory) only when it grows by more than
+// 2^8, write P into tensor memory, and at the end divide O by the row sum.  With two S and
+// two P buffers, the softmax of tile t overlaps the MMAs of tiles t - 1 and t + 1.  Every mbarrier wait is bounded: on a timeout the
 // rows of the CTA become NaN, nothing new is issued, what was issued is waited for (bounded)
 // and the tensor memory is returned.
 #include <cuda.h>
@@ -43,23 +44,24 @@ constexpr int kUM = kUG * kUHeads;      // 128 rows
 constexpr int kUD = 128;                // head dim
 constexpr int kUTB = 16;                // union blocks per tile
 constexpr int kUTC = 4 * kUTB;          // 64 cells per tile
-constexpr int kUStages = 3;
-constexpr int kUThreads = 192;          // warp 0 TMA, warp 1 MMA, warps 2-5 softmax
+constexpr int kUStages = 6;
+constexpr int kUThreads = 320;          // warp 0 TMA, warp 1 MMA, warps 2-9 softmax
+constexpr int kUEpiWarps = 8;           // two per row: one per half of the tile's columns
 constexpr float kURescale = 8.0f;       // move the running maximum past 2^8 growth
 constexpr int kUMaxBlockWords = 8192;   // bitmap words: 2^18 blocks = 2^20 cells
 
-constexpr uint32_t kQHalf = kUM * 128;              // 16 KB: 128 rows x 64 dims bf16
-constexpr uint32_t kQBytes = 2 * kQHalf;            // 32 KB: one of Q's two bf16 halves
-constexpr uint32_t kPBytes = kUM * 128;             // 16 KB: 128 rows x 64 cells bf16
 constexpr uint32_t kTileHalf = kUTC * 128;          // 8 KB: 64 cells x 64 dims bf16
 constexpr uint32_t kTileBytes = 2 * kTileHalf;      // 16 KB: one tensor's 64-cell tile
 constexpr uint32_t kStageBytes = 2 * kTileBytes;    // K and V
-constexpr uint32_t kTmemCols = 256;                 // S[0], S[1] (64 each), O (128)
+// Tensor memory (512 columns, one row per lane): S[0], S[1] fp32 (64 each), O fp32 (128),
+// Q's bf16 high and low halves (64 each: two dims per column), P[0], P[1] as bf16 high and
+// low halves (32 each: two cells per column).
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS = 0, kColO = 128, kColQh = 256, kColQl = 320, kColP = 384;
 
 __host__ __device__ constexpr size_t union_smem_bytes()
 {
-    return 1024 + 2 * (size_t)kQBytes + 2 * (size_t)kPBytes + (size_t)kUStages * kStageBytes +
-           256;
+    return 1024 + (size_t)kUStages * kStageBytes + 256 + 6 * kUM * sizeof(float);
 }
 
 // Union capacity in blocks for lists of up to max_cells cells: a list of whole blocks plus
@@ -230,14 +232,16 @@ __host__ __device__ constexpr uint32_t idesc_m128(int n, bool b_mn)
            ((uint32_t)(n >> 3) << 17) | ((uint32_t)(kUM >> 4) << 24);
 }
 
-__device__ __forceinline__ void umma_m128(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                          uint32_t idesc, uint32_t accumulate)
+// One M128 MMA of this CTA with A read from tensor memory (row i in lane i, two bf16 per
+// 32-bit column, k-contiguous) and B from shared memory.
+__device__ __forceinline__ void umma_m128_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                             uint32_t idesc, uint32_t accumulate)
 {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 
@@ -278,42 +282,65 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float *v)
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float *v)
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t *v)
 {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
         "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
         "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
-        "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
-        "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
-        "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
-        "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
-        "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
-        "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
-        "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
-        "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
-        "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
-        "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
-        "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+        "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+        "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]),
+        "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]),
+        "r"(v[29]), "r"(v[30]), "r"(v[31])
         : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st()
+{
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t *v)
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+        "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+        "r"(v[15])
+        : "memory");
+}
+
+// 2^x by the hardware's approximate exponential (2^-inf = +0).
+__device__ __forceinline__ float ex2_approx(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Barrier of the two softmax warps that own the same 32 rows (named barrier 1 + quarter)
+// that also returns the AND of `v` over their 64 threads: both warps take every decision that
+// follows it the same way (neither may leave a loop the other stays in).
+__device__ __forceinline__ bool pair_and(int quarter, bool v)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, c;\n\t"
+        "setp.ne.u32 c, %1, 0;\n\t"
+        "bar.red.and.pred p, %2, 64, c;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v), "r"(1 + quarter)
+        : "memory");
+    return r != 0;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi)
 {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&v);
-}
-
-// Row r of a K-major 128-byte-swizzled operand whose rows are 128 bytes: 16-byte chunk c
-// of the row sits at chunk c ^ (r & 7) of the row's 128 bytes.
-__device__ __forceinline__ void st_row_sw128(unsigned char *tile, int r, const uint32_t *w)
-{
-    unsigned char *row = tile + (r >> 3) * 1024 + (r & 7) * 128;
-#pragma unroll
-    for (int c = 0; c < 8; ++c)
-        *reinterpret_cast<uint4 *>(row + ((c ^ (r & 7)) << 4)) =
-            make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
 }
 
 // ------------------------------------------------------------------ kernel 2: attention
@@ -326,22 +353,21 @@ attn_union_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
                   float *__restrict__ lse)
 {
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    unsigned char *sb = reinterpret_cast<unsigned char *>(
+    unsigned char *sKV = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-    unsigned char *sQh = sb;                         // [2 dim halves][128 rows][128 B]
-    unsigned char *sQl = sQh + kQBytes;
-    unsigned char *sPh = sQl + kQBytes;              // [128 rows][128 B]
-    unsigned char *sPl = sPh + kPBytes;
-    unsigned char *sKV = sPl + kPBytes;              // [stage][K, V][2 halves][64 cells][128 B]
+    // [stage][K, V][2 dim halves][64 cells][128 B], 128-byte swizzle
     uint64_t *kv_full = reinterpret_cast<uint64_t *>(sKV + kUStages * kStageBytes);
     uint64_t *kv_empty = kv_full + kUStages;
-    uint64_t *s_full = kv_empty + kUStages;          // [2]
-    uint64_t *s_empty = s_full + 2;                  // [2]
-    uint64_t *p_full = s_empty + 2;
-    uint64_t *o_done = p_full + 1;
-    uint64_t *q_ready = o_done + 1;
+    uint64_t *s_full = kv_empty + kUStages;          // [2] S(t) in its buffer
+    uint64_t *s_empty = s_full + 2;                  // [2] S buffer read by the softmax warps
+    uint64_t *p_full = s_empty + 2;                  // [2] P(t) in its buffer
+    uint64_t *o_done = p_full + 2;                   // [2] the P V of a tile using P buffer b done
+    uint64_t *q_ready = o_done + 2;
     uint64_t *drain = q_ready + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+    // row maxima of the two halves of each row, double-buffered by tile parity ([2][2][128]
+    // floats), then the halves' row sums ([2][128]), at 256 bytes past the stage ring
+    float *xch = reinterpret_cast<float *>(sKV + kUStages * kStageBytes + 256);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int64_t g = blockIdx.x;
@@ -356,11 +382,11 @@ attn_union_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&s_full[b], 1);
-            mbar_init(&s_empty[b], 4);
+            mbar_init(&s_empty[b], kUEpiWarps);
+            mbar_init(&p_full[b], kUEpiWarps);
+            mbar_init(&o_done[b], 1);
         }
-        mbar_init(p_full, 4);
-        mbar_init(o_done, 1);
-        mbar_init(q_ready, 4);
+        mbar_init(q_ready, kUEpiWarps);
         mbar_init(drain, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -394,10 +420,7 @@ attn_union_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         const int j = lane >> 1, half = lane & 1;
         int armed = 0;
         int32_t blk_next = 0;
-        if (n_tiles > 0) {
-            const int64_t u = j;
-            blk_next = u < ucount ? ublk[u] : ublk[0];
-        }
+        if (n_tiles > 0) blk_next = (uint32_t)j < ucount ? ublk[j] : ublk[0];
         for (int t = 0; t < n_tiles; ++t, ++armed) {
             const int s = t % kUStages;
             const int32_t blk = blk_next;
@@ -425,14 +448,12 @@ attn_union_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
             if (uses > 0 && !mbar_wait(&kv_full[s], (uint32_t)(uses - 1) & 1u)) ok = false;
         }
     } else if (warp == 1) {
-        // ---- MMA issuer (one thread)
+        // ---- MMA issuer (one thread): S(t) = Q K(t)^T, then O += P(t-1) V(t-1)
         if (lane == 0) {
             constexpr uint32_t id_s = idesc_m128(kUTC, false);
             constexpr uint32_t id_o = idesc_m128(kUD, true);
             if (n_tiles > 0 && !mbar_wait(q_ready, 0)) ok = false;
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-            const uint32_t qh = smem_u32(sQh), ql = smem_u32(sQl);
-            const uint32_t ph = smem_u32(sPh), pl = smem_u32(sPl);
             for (int t = 0; ok && t <= n_tiles; ++t) {
                 if (t < n_tiles) {
                     const int s = t % kUStages, b = t & 1;
@@ -449,36 +470,35 @@ attn_union_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
                     uint32_t acc = 0;
 #pragma unroll
                     for (int part = 0; part < 2; ++part) {
-                        const uint32_t qa = part ? ql : qh;
+                        const uint32_t qa = tmem + (part ? kColQl : kColQh);
 #pragma unroll
                         for (int k16 = 0; k16 < kUD / 16; ++k16) {
                             const uint32_t hf = (uint32_t)(k16 >> 2), ko = (uint32_t)(k16 & 3) * 32;
-                            umma_m128(tmem + (uint32_t)(b * kUTC),
-                                      desc_kmajor_sw128(qa + hf * kQHalf + ko),
-                                      desc_kmajor_sw128(kb + hf * kTileHalf + ko), id_s, acc);
+                            umma_m128_ta(tmem + kColS + (uint32_t)(b * kUTC), qa + (uint32_t)k16 * 8,
+                                         desc_kmajor_sw128(kb + hf * kTileHalf + ko), id_s, acc);
                             acc = 1;
                         }
                     }
                     umma_commit(&s_full[b]);
                 }
                 if (t >= 1) {
-                    const int tp = t - 1, sp = tp % kUStages;
-                    if (!mbar_wait(p_full, (uint32_t)tp & 1u)) {
+                    const int tp = t - 1, sp = tp % kUStages, pb = tp & 1;
+                    if (!mbar_wait(&p_full[pb], (uint32_t)(tp >> 1) & 1u)) {
                         ok = false;
                         break;
                     }
                     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
                     const uint32_t vb = smem_u32(sKV + sp * kStageBytes + kTileBytes);
+                    const uint32_t pcol = tmem + kColP + (uint32_t)pb * 64;
 #pragma unroll
                     for (int part = 0; part < 2; ++part) {
-                        const uint32_t pa = part ? pl : ph;
 #pragma unroll
                         for (int k16 = 0; k16 < kUTC / 16; ++k16)
-                            umma_m128(tmem + 128u, desc_kmajor_sw128(pa + k16 * 32),
-                                      desc_mnmajor_sw128(vb + k16 * 2048, kTileHalf), id_o,
-                                      (tp > 0 || part > 0 || k16 > 0) ? 1u : 0u);
+                            umma_m128_ta(tmem + kColO, pcol + (uint32_t)(part * 32 + k16 * 8),
+                                         desc_mnmajor_sw128(vb + k16 * 2048, kTileHalf), id_o,
+                                         (tp > 0 || part > 0 || k16 > 0) ? 1u : 0u);
                     }
-                    umma_commit(o_done);
+                    umma_commit(&o_done[pb]);
                     umma_commit(&kv_empty[sp]);
                 }
             }
@@ -487,133 +507,154 @@ attn_union_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
             if (!mbar_wait(drain, 0)) ok = false;
         }
     } else {
-        // ---- softmax / epilogue: one thread per row (row = 8 * query + head)
+        // ---- softmax / epilogue: two threads per row (row = 8 * query + head), one per half
+        // of the tile's 64 columns (and of O's 128 dims)
         const int quarter = warp & 3;
+        const int ch = (warp - 2) >> 2;              // column half: warps 2-5 -> 0, 6-9 -> 1
         const int r = quarter * 32 + lane;
         const int li = r >> 3;
         const int64_t qi = g * kUG + li;
         const int h = kvh * kUHeads + (r & 7);
         const bool live = qi < n_q;
-        int64_t n = live ? (int64_t)n_cells[qi] : 0;
+        const int64_t n = live ? (int64_t)n_cells[qi] : 0;
         const bool trunc = n > max_cells;
         const uint32_t lrow = (uint32_t)(quarter * 32) << 16;
-        // the row's query, pre-scaled, as bf16 high and low halves in the operand layout
+        // this half of the row's query (dims 64*ch ..), pre-scaled, as bf16 high and low
+        // halves into tensor memory
         {
-            const float *qr = q + (qi * H_q + h) * (int64_t)kUD;
+            const float *qr = q + (qi * H_q + h) * (int64_t)kUD + ch * 64;
+            uint32_t wh[32], wl[32];
 #pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-                uint32_t wh[32], wl[32];
-#pragma unroll
-                for (int e = 0; e < 64; e += 2) {
-                    float x0 = 0.0f, x1 = 0.0f;
-                    if (live) {
-                        const float2 v = *reinterpret_cast<const float2 *>(qr + hf * 64 + e);
-                        x0 = v.x * scale_log2;
-                        x1 = v.y * scale_log2;
-                    }
-                    const float h0 = __bfloat162float(__float2bfloat16_rn(x0));
-                    const float h1 = __bfloat162float(__float2bfloat16_rn(x1));
-                    wh[e / 2] = pack_bf16(h0, h1);
-                    wl[e / 2] = pack_bf16(x0 - h0, x1 - h1);
+            for (int e = 0; e < 64; e += 2) {
+                float x0 = 0.0f, x1 = 0.0f;
+                if (live) {
+                    const float2 v = *reinterpret_cast<const float2 *>(qr + e);
+                    x0 = v.x * scale_log2;
+                    x1 = v.y * scale_log2;
                 }
-                st_row_sw128(sQh + hf * kQHalf, r, wh);
-                st_row_sw128(sQl + hf * kQHalf, r, wl);
+                const float h0 = __bfloat162float(__float2bfloat16_rn(x0));
+                const float h1 = __bfloat162float(__float2bfloat16_rn(x1));
+                wh[e / 2] = pack_bf16(h0, h1);
+                wl[e / 2] = pack_bf16(x0 - h0, x1 - h1);
             }
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            tmem_st32(tmem + lrow + kColQh + (uint32_t)(ch * 32), wh);
+            tmem_st32(tmem + lrow + kColQl + (uint32_t)(ch * 32), wl);
+            tmem_wait_st();
+            asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
             __syncwarp();
             if (lane == 0) mbar_arrive(q_ready);
         }
         float m_ref = -INFINITY, l = 0.0f;
-        uint32_t mw0 = 0, mw1 = 0;
-        if (n_tiles > 0) {
-            mw0 = gmem[li * 2];
-            mw1 = gmem[li * 2 + 1];
-        }
+        uint32_t mw = 0;
+        if (n_tiles > 0) mw = gmem[li * 2 + ch];
+        // Every iteration passes exactly one pair barrier, which also decides (for both warps
+        // of the pair alike) whether to stop: a warp whose wait gave up skips its tensor-memory
+        // work and stops at the next pair barrier together with its partner.
         for (int t = 0; t < n_tiles; ++t) {
             const int b = t & 1;
-            const uint32_t w0 = mw0, w1 = mw1;
-            if (t + 1 < n_tiles) {  // next tile's membership words, one tile ahead
-                const uint32_t *nm = gmem + ((int64_t)(t + 1) * kUG + li) * 2;
-                mw0 = nm[0];
-                mw1 = nm[1];
-            }
-            // waits are warp-uniform: the tensor-memory loads below need the whole warp
-            if (!__all_sync(0xffffffffu, mbar_wait(&s_full[b], (uint32_t)(t >> 1) & 1u))) {
-                ok = false;
-                break;
-            }
-            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-            float x[kUTC];
-            tmem_ld32(tmem + lrow + (uint32_t)(b * kUTC), x);
-            tmem_ld32(tmem + lrow + (uint32_t)(b * kUTC + 32), x + 32);
-            asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&s_empty[b]);
-            float mt = -INFINITY;
+            const uint32_t w = (live && !trunc) ? mw : 0u;
+            if (t + 1 < n_tiles) mw = gmem[((int64_t)(t + 1) * kUG + li) * 2 + ch];  // ahead
+            // waits are warp-uniform: the tensor-memory accesses below need the whole warp
+            bool good = ok && __all_sync(0xffffffffu, mbar_wait(&s_full[b], (uint32_t)(t >> 1) & 1u));
+            float x[32];
+            float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+            if (good) {
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                tmem_ld32(tmem + lrow + kColS + (uint32_t)(b * kUTC + ch * 32), x);
+                asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&s_empty[b]);
 #pragma unroll
-            for (int e = 0; e < kUTC; ++e) {
-                const bool in = ((e < 32 ? w0 >> e : w1 >> (e - 32)) & 1u) && !trunc && live;
-                x[e] = in ? x[e] : -INFINITY;
-                mt = fmaxf(mt, x[e]);
+                for (int e = 0; e < 32; ++e) {
+                    x[e] = ((w >> e) & 1u) ? x[e] : -INFINITY;
+                    mx[e & 3] = fmaxf(mx[e & 3], x[e]);
+                }
             }
-            // P(t - 1) has been consumed (and O holds it) before P or O is touched
-            if (t > 0 && !__all_sync(0xffffffffu, mbar_wait(o_done, (uint32_t)(t - 1) & 1u))) {
+            // the row's maximum over both halves
+            float *slot = xch + (b * 2) * kUM;
+            slot[ch * kUM + r] = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+            if (!pair_and(quarter, good)) {
                 ok = false;
                 break;
             }
-            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            const float mt = fmaxf(slot[r], slot[kUM + r]);
             float alpha = 1.0f;
             bool move = false;
             if (mt > m_ref + kURescale) {  // also the first finite maximum (m_ref = -inf)
                 move = true;
-                alpha = m_ref == -INFINITY ? 0.0f : exp2f(m_ref - mt);
+                alpha = m_ref == -INFINITY ? 0.0f : ex2_approx(m_ref - mt);
             }
-            if (__any_sync(0xffffffffu, move && m_ref != -INFINITY)) {
-                // rescale O's row in tensor memory (the warp's 32 rows at once)
-#pragma unroll 1
-                for (int c = 0; c < kUD; c += 32) {
-                    float o[32];
-                    tmem_ld32(tmem + lrow + 128u + (uint32_t)c, o);
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) o[e] *= alpha;
-                    tmem_st32(tmem + lrow + 128u + (uint32_t)c, o);
-                }
-            }
+            const bool rescale = __any_sync(0xffffffffu, move && m_ref != -INFINITY);
             if (move) {
                 l *= alpha;
                 m_ref = mt;
             }
-            uint32_t ph_w[32], pl_w[32];
-            float ls = 0.0f;
+            // P(t) relative to the (possibly moved) maximum, before any wait on the MMAs
+            const float mu = m_ref == -INFINITY ? 0.0f : m_ref;
+            uint32_t pw[32];
+            float ls[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-            for (int e = 0; e < kUTC; e += 2) {
-                const float p0 = x[e] == -INFINITY ? 0.0f : exp2f(x[e] - m_ref);
-                const float p1 = x[e + 1] == -INFINITY ? 0.0f : exp2f(x[e + 1] - m_ref);
-                ls += p0 + p1;
-                const float h0 = __bfloat162float(__float2bfloat16_rn(p0));
-                const float h1 = __bfloat162float(__float2bfloat16_rn(p1));
-                ph_w[e / 2] = pack_bf16(h0, h1);
-                pl_w[e / 2] = pack_bf16(p0 - h0, p1 - h1);
+            for (int e = 0; e < 32; e += 2) {
+                const float p0 = ex2_approx(x[e] - mu);
+                const float p1 = ex2_approx(x[e + 1] - mu);
+                ls[(e >> 1) & 3] += p0 + p1;
+                const uint32_t hb = pack_bf16(p0, p1);
+                const float h0 = __uint_as_float(hb << 16), h1 = __uint_as_float(hb & 0xffff0000u);
+                pw[e / 2] = hb;
+                pw[16 + e / 2] = pack_bf16(p0 - h0, p1 - h1);
             }
-            l += ls;
-            st_row_sw128(sPh, r, ph_w);
-            st_row_sw128(sPl, r, pl_w);
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+            // P buffer b was last read by P V(t - 2); O is touched only when rescaling, after
+            // P V(t - 1)
+            const bool w2 = t < 2 || __all_sync(0xffffffffu, mbar_wait(&o_done[b],
+                                                                       (uint32_t)((t - 2) >> 1) & 1u));
+            const bool w3 = !(rescale && t >= 1) ||
+                            __all_sync(0xffffffffu,
+                                       mbar_wait(&o_done[b ^ 1], (uint32_t)((t - 1) >> 1) & 1u));
+            if (!(w2 && w3)) {
+                ok = false;  // stops at the next pair barrier (or the one after the loop)
+                continue;
+            }
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            if (rescale) {
+#pragma unroll 1
+                for (int c = ch * 64; c < ch * 64 + 64; c += 32) {
+                    float o[32];
+                    tmem_ld32(tmem + lrow + kColO + (uint32_t)c, o);
+                    uint32_t ou[32];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) ou[e] = __float_as_uint(o[e] * alpha);
+                    tmem_st32(tmem + lrow + kColO + (uint32_t)c, ou);
+                }
+            }
+            // P(t): high halves in columns 0-31 of the buffer, low halves in 32-63; this
+            // thread's 32 cells are 16 columns of each
+            const uint32_t pcol = tmem + lrow + kColP + (uint32_t)b * 64 + (uint32_t)(ch * 16);
+            tmem_st16(pcol, pw);
+            tmem_st16(pcol + 32, pw + 16);
+            tmem_wait_st();
             asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
             __syncwarp();
-            if (lane == 0) mbar_arrive(p_full);
+            if (lane == 0) mbar_arrive(&p_full[b]);
         }
         if (ok && n_tiles > 0 &&
-            !__all_sync(0xffffffffu, mbar_wait(o_done, (uint32_t)(n_tiles - 1) & 1u)))
+            !__all_sync(0xffffffffu, mbar_wait(&o_done[(n_tiles - 1) & 1],
+                                               (uint32_t)((n_tiles - 1) >> 1) & 1u)))
             ok = false;
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        // the row sum over both halves, and whether both warps of the pair finished (every
+        // warp of a pair arrives here after the same number of pair barriers)
+        float *lsum = xch + 4 * kUM;
+        lsum[ch * kUM + r] = l;
+        ok = pair_and(quarter, ok);
+        const float lt = lsum[r] + lsum[kUM + r];
         const bool nan_rows = !ok || bad_group || trunc;
-        const float inv = l > 0.0f ? 1.0f / l : 0.0f;
+        const float inv = lt > 0.0f ? 1.0f / lt : 0.0f;
 #pragma unroll 1
-        for (int c = 0; c < kUD; c += 32) {
+        for (int c = ch * 64; c < ch * 64 + 64; c += 32) {
             float o[32];
             if (n_tiles > 0 && ok) {
-                tmem_ld32(tmem + lrow + 128u + (uint32_t)c, o);
+                tmem_ld32(tmem + lrow + kColO + (uint32_t)c, o);
             } else {
 #pragma unroll
                 for (int e = 0; e < 32; ++e) o[e] = 0.0f;
@@ -628,10 +669,10 @@ attn_union_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
                                                o[e + 3] * inv);
             }
         }
-        if (live && lse)
+        if (live && lse && ch == 0)
             lse[qi * H_q + h] = nan_rows ? NAN
-                                         : (l > 0.0f ? (m_ref + log2f(l)) * 0.6931471805599453f
-                                                     : -INFINITY);
+                                         : (lt > 0.0f ? (m_ref + log2f(lt)) * 0.6931471805599453f
+                                                      : -INFINITY);
     }
 
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
