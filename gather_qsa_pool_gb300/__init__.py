@@ -9,6 +9,7 @@ from ._binding import (  # noqa: F401
     QSA_F32,
     QSA_PREC_BF16_TC,
     QSA_PREC_F32,
+    QSA_WAIT_DEFAULT_NS,
     QSAError,
     decode_step,
     decode_step_host_layout,
@@ -24,6 +25,7 @@ from ._binding import (  # noqa: F401
     mask_sparse_eligible,
     mask_to_list,
     pool_update,
+    set_wait_options,
     sparse_attn,
     sparse_attn_union,
     sparse_attn_union_workspace_size,

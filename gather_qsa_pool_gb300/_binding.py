@@ -19,6 +19,7 @@ HEADER = os.path.join(os.path.dirname(HERE), "include", "qsa.h")
 QSA_OK, QSA_ERR_INVALID_ARG, QSA_ERR_UNSUPPORTED, QSA_ERR_CUDA, QSA_ERR_TIMEOUT = range(5)
 QSA_F32, QSA_BF16 = 0, 1
 QSA_PREC_F32, QSA_PREC_BF16_TC = 0, 1
+QSA_WAIT_DEFAULT_NS = 2_000_000_000
 
 _p = ctypes.c_void_p
 _i64 = ctypes.c_int64
@@ -30,6 +31,7 @@ _sz = ctypes.c_size_t
 _SIGNATURES = {
     "qsa_status_str": (ctypes.c_char_p, [_int]),
     "qsa_version": (_int, []),
+    "qsa_set_wait_options": (None, [_p, ctypes.c_uint64]),
     "qsa_pool_update": (_int, [_p, _int, _i64, _int, _int, _p, _f, _d, _p, _int, _i64, _i64,
                                _p]),
     "qsa_index_score": (_int, [_p, _i64, _i64, _p, _p, _int, _i64, _int, _int, _f, _p, _i64,
@@ -103,6 +105,13 @@ def load(path: str | None = None) -> ctypes.CDLL:
         fn.argtypes = args
     _lib = lib
     return lib
+
+
+def set_wait_options(status=None, limit_ns=QSA_WAIT_DEFAULT_NS):
+    """qsa_set_wait_options: for later launches from this thread, the int32 device tensor a
+    kernel whose bounded wait gave up stores QSA_ERR_TIMEOUT into (or None), and the limit of
+    the waits inside a kernel's pipeline (0: give up unless already complete)."""
+    load().qsa_set_wait_options(_ptr(status), int(limit_ns))
 
 
 def status_str(status: int) -> str:

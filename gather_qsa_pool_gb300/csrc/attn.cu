@@ -563,7 +563,7 @@ attn_mma_kernel(const float *__restrict__ q, int H_q, int H_kv, float scale_log2
                 const __nv_bfloat16 *__restrict__ K, const __nv_bfloat16 *__restrict__ V,
                 int64_t n_kv, int64_t ld_k, int64_t ld_v, const int32_t *__restrict__ pos,
                 const int32_t *__restrict__ n_cells, int64_t max_cells, float *__restrict__ out,
-                float *__restrict__ lse, int early_q)
+                float *__restrict__ lse, int early_q, const WaitCtl wc)
 {
     constexpr int G = 8, D = 128, TC = 16 * NW, LD = kMmaLd, NT = 32 * NW;
     constexpr int TX = attn_mma_stage_rows<NW, NB>();  // rows of a stage buffer
@@ -632,9 +632,10 @@ attn_mma_kernel(const float *__restrict__ q, int H_q, int H_kv, float scale_log2
         mbar_init(&sbar[1], 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    uint32_t sphase = 0;  // bit b: parity of buffer b's next phase
-    bool lost = false;    // a stage that never completed (its outputs become NaN)
-    uint32_t lost_at = 0;  // buffer | parity << 1 of that stage
+    // phases armed on / seen complete by each stage buffer's barrier (the same in every
+    // thread); a wait that gave up stops the CTA's stage loop (its outputs become NaN)
+    int armed0 = 0, armed1 = 0, done0 = 0, done1 = 0;
+    bool lost = false;
     // A split's cell range is fixed by max_cells, so the positions of its first two stages
     // are loaded together with the list length; entries past the length are dropped once
     // it arrives.  A range a few cells longer than a stage (2,051 cells over 16 splits:
@@ -692,6 +693,8 @@ attn_mma_kernel(const float *__restrict__ q, int H_q, int H_kv, float scale_log2
         }
         const int nv = __syncthreads_count(tid < SC && rb[tid] >= 0);
         if (tid == 0) mbar_arrive_expect_tx(&sbar[buf], (uint32_t)nv * 2u * D * 2u);
+        if (buf) ++armed1;
+        else ++armed0;
         // one thread per row and tensor (NT = 2 * TC); the rows past TC of a wider stage
         // go to the first threads once more
         for (int t = tid; t < 2 * SC; t += NT) {
@@ -706,14 +709,16 @@ attn_mma_kernel(const float *__restrict__ q, int H_q, int H_kv, float scale_log2
             }
         }
     };
-    // Wait for buffer `buf`'s stage (bounded), then make its zero-filled rows visible.
+    // Wait for buffer `buf`'s stage (bounded), then make its zero-filled rows visible; the
+    // CTA agrees on whether any thread's wait gave up.
     auto wait_rows = [&](int buf) {
-        if (!lost && !mbar_wait(&sbar[buf], (sphase >> buf) & 1u)) {
-            lost = true;
-            lost_at = (uint32_t)buf | (((sphase >> buf) & 1u) << 1);
+        const uint32_t par = (uint32_t)((buf ? done1 : done0) & 1);
+        const bool ok_w = !lost && mbar_wait(&sbar[buf], par, wc.limit_ns);
+        lost = __syncthreads_or(lost || !ok_w) != 0;
+        if (!lost) {
+            if (buf) ++done1;
+            else ++done0;
         }
-        sphase ^= 1u << buf;
-        __syncthreads();
     };
 
     if (ntiles > 0) copy_rows(0);
@@ -730,6 +735,7 @@ attn_mma_kernel(const float *__restrict__ q, int H_q, int H_kv, float scale_log2
             copy_rows(0);
         }
         wait_rows(buf);
+        if (lost) break;  // issue nothing more; what was issued is drained below
         const int tc = (int)min((int64_t)SC, c1 - (c0 + (int64_t)it * SC));
         const __nv_bfloat16 *ks = Ks + buf * TX * LD;
         const __nv_bfloat16 *vs = Vs + buf * TX * LD;
@@ -807,8 +813,12 @@ attn_mma_kernel(const float *__restrict__ q, int H_q, int H_kv, float scale_log2
         if (NB == 1 && warp == NW - 1) group(TC);  // the extra rows of a wider stage
         __syncthreads();  // this stage is refilled by the next issue()
     }
-
+    // every copy issued lands before the stage area is reused or the CTA leaves (a buffer is
+    // re-armed only after its previous phase was seen complete: at most one outstanding)
+    if (armed0 > done0) (void)mbar_wait(&sbar[0], (uint32_t)(done0 & 1));
+    if (armed1 > done1) (void)mbar_wait(&sbar[1], (uint32_t)(done1 & 1));
     lost = __syncthreads_or(lost);
+    if (lost && tid == 0) report_timeout(wc);
     // per-warp state -> shared memory: head hr, dims 8j + qc + {0,1}
     float l4 = lsum;
     l4 += __shfl_xor_sync(0xffffffffu, l4, 1);
@@ -866,15 +876,7 @@ attn_mma_kernel(const float *__restrict__ q, int H_q, int H_kv, float scale_log2
             }
         }
     }
-    // a lost stage may still have copies in flight into this CTA's shared memory: give them
-    // one more bounded wait before the CTA retires
-    auto drain = [&]() {
-        if (lost) (void)mbar_wait(&sbar[lost_at & 1u], lost_at >> 1);
-    };
-    if (S == 1) {
-        drain();
-        return;
-    }
+    if (S == 1) return;
 
     // combine the S CTAs of the cluster: CTA s owns outputs [s*per, (s+1)*per) of G*D.
     // Four threads per output, each reading (m, l, o) of a quarter of the remote states in
@@ -934,7 +936,6 @@ attn_mma_kernel(const float *__restrict__ q, int H_q, int H_kv, float scale_log2
         }
     }
     cluster.sync();  // keep this CTA's state alive until every remote read is done
-    drain();
 }
 
 // Combine the S split partials of one (query, head): log-sum-exp weighting.  The split
@@ -1028,7 +1029,7 @@ cudaError_t launch_attn_mma_t(int S, const float *q, int64_t n_q, int H_q, int H
     const dim3 grid((unsigned)S, (unsigned)H_kv, (unsigned)n_q);
     return launch(k, grid, dim3(32 * NW), smem, st, S > 1 ? S : 1, q, H_q, H_kv,
                   scale * kLog2e, (const __nv_bfloat16 *)K, (const __nv_bfloat16 *)V, n_kv, ld_k,
-                  ld_v, pos, n_cells, max_cells, out, lse, early_q ? 1 : 0);
+                  ld_v, pos, n_cells, max_cells, out, lse, early_q ? 1 : 0, current_wait_ctl());
 }
 
 cudaError_t launch_attn_mma(const float *q, int64_t n_q, int H_q, int H_kv, float scale,

@@ -48,7 +48,7 @@ attn_rows4_kernel(const float *__restrict__ q, int H_q, float scale_log2,
                   const __nv_bfloat16 *__restrict__ K, const __nv_bfloat16 *__restrict__ V,
                   int64_t n_kv, int64_t ld_k, int64_t ld_v, const int32_t *__restrict__ pos,
                   const int32_t *__restrict__ n_cells, int64_t max_cells,
-                  float *__restrict__ out, float *__restrict__ lse)
+                  float *__restrict__ out, float *__restrict__ lse, const WaitCtl wc)
 {
     constexpr int G = kRG, D = kRD, TC = kRTC, NS = kRStages, NT = kRNT;
     constexpr int GE = kRGroupElems, SE = kRStageElems;
@@ -117,7 +117,7 @@ attn_rows4_kernel(const float *__restrict__ q, int H_q, float scale_log2,
         for (int it = 0; it < ntiles; ++it, ++armed) {
             const int s = it % NS;
             const uint32_t use = (uint32_t)(it / NS);
-            bool ok = use == 0 || mbar_wait(&empty[s], (use - 1) & 1u);
+            bool ok = use == 0 || mbar_wait(&empty[s], (use - 1) & 1u, wc.limit_ns);
             if (!__all_sync(0xffffffffu, ok)) {
                 lost = true;
                 break;
@@ -157,8 +157,10 @@ attn_rows4_kernel(const float *__restrict__ q, int H_q, float scale_log2,
                 }
             }
         }
-        // copies still in flight after a lost wait must land before the CTA leaves
-        if (lost && lane == 0)
+        // every copy issued lands before the CTA leaves: the last phase armed on each stage
+        // (a stage is re-armed only after every consumer saw its previous phase complete, so
+        // no earlier phase can be outstanding)
+        if (lane == 0)
             for (int s = 0; s < NS && s < armed; ++s) {
                 const int uses = armed / NS + (s < armed % NS ? 1 : 0);
                 (void)mbar_wait(&full[s], (uint32_t)(uses - 1) & 1u);
@@ -198,8 +200,11 @@ attn_rows4_kernel(const float *__restrict__ q, int H_q, float scale_log2,
 
         for (int it = 0; it < ntiles; ++it) {
             const int s = it % NS;
-            const bool ok = lost || mbar_wait(&full[s], (uint32_t)(it / NS) & 1u);
+            const bool ok = !lost && mbar_wait(&full[s], (uint32_t)(it / NS) & 1u, wc.limit_ns);
             if (!__all_sync(0xffffffffu, ok)) lost = true;
+            // a warp that gave up neither reads the stage (copies may still be landing) nor
+            // releases it, so the producer stops too
+            if (lost) continue;
             const __nv_bfloat16 *kst = Ks + (size_t)s * SE + mj * GE + krow;
             const __nv_bfloat16 *vst = Vs + (size_t)s * SE + mj * GE + vrow;
             // two accumulator chains per tile (even / odd k steps) halve the MMA dependency
@@ -283,6 +288,7 @@ attn_rows4_kernel(const float *__restrict__ q, int H_q, float scale_log2,
     }
     if (warp == kRWarps) __syncthreads();  // pairs with the consumers' barrier above
     lost = __syncthreads_or(lost);
+    if (lost && tid == 0) report_timeout(wc);
 
     // the two warps of each KV head merge into the output
     for (int e = tid; e < kRHkv * G * D; e += kRThreads) {
@@ -328,7 +334,7 @@ cudaError_t launch_attn_rows4(const float *q, int64_t n_q, int H_q, float scale,
     if (e != cudaSuccess) return e;
     return launch(attn_rows4_kernel, dim3((unsigned)n_q), dim3(kRThreads), kRSmem, st, 1, q, H_q,
                   scale * kLog2e, (const __nv_bfloat16 *)K, (const __nv_bfloat16 *)V, n_kv, ld_k,
-                  ld_v, pos, n_cells, max_cells, out, lse);
+                  ld_v, pos, n_cells, max_cells, out, lse, current_wait_ctl());
 }
 
 }  // namespace qsa

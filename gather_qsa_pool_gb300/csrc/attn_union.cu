@@ -350,7 +350,7 @@ attn_union_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
                   const float *__restrict__ q, int64_t n_q, int H_q, float scale_log2,
                   const int32_t *__restrict__ n_cells, int64_t max_cells,
                   const uint32_t *__restrict__ ws, float *__restrict__ out,
-                  float *__restrict__ lse)
+                  float *__restrict__ lse, const WaitCtl wc)
 {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     unsigned char *sKV = reinterpret_cast<unsigned char *>(
@@ -430,7 +430,8 @@ attn_union_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
             }
             // every lane waits; the warp goes on only if all of them saw the stage free
             const bool freed =
-                t < kUStages || mbar_wait(&kv_empty[s], (uint32_t)((t / kUStages) - 1) & 1u);
+                t < kUStages ||
+                mbar_wait(&kv_empty[s], (uint32_t)((t / kUStages) - 1) & 1u, wc.limit_ns);
             if (!__all_sync(0xffffffffu, freed)) {
                 ok = false;
                 break;
@@ -452,16 +453,16 @@ attn_union_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         if (lane == 0) {
             constexpr uint32_t id_s = idesc_m128(kUTC, false);
             constexpr uint32_t id_o = idesc_m128(kUD, true);
-            if (n_tiles > 0 && !mbar_wait(q_ready, 0)) ok = false;
+            if (n_tiles > 0 && !mbar_wait(q_ready, 0, wc.limit_ns)) ok = false;
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
             for (int t = 0; ok && t <= n_tiles; ++t) {
                 if (t < n_tiles) {
                     const int s = t % kUStages, b = t & 1;
-                    if (!mbar_wait(&kv_full[s], (uint32_t)(t / kUStages) & 1u)) {
+                    if (!mbar_wait(&kv_full[s], (uint32_t)(t / kUStages) & 1u, wc.limit_ns)) {
                         ok = false;
                         break;
                     }
-                    if (t >= 2 && !mbar_wait(&s_empty[b], (uint32_t)((t >> 1) - 1) & 1u)) {
+                    if (t >= 2 && !mbar_wait(&s_empty[b], (uint32_t)((t >> 1) - 1) & 1u, wc.limit_ns)) {
                         ok = false;
                         break;
                     }
@@ -483,7 +484,7 @@ attn_union_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
                 }
                 if (t >= 1) {
                     const int tp = t - 1, sp = tp % kUStages, pb = tp & 1;
-                    if (!mbar_wait(&p_full[pb], (uint32_t)(tp >> 1) & 1u)) {
+                    if (!mbar_wait(&p_full[pb], (uint32_t)(tp >> 1) & 1u, wc.limit_ns)) {
                         ok = false;
                         break;
                     }
@@ -555,7 +556,8 @@ attn_union_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
             const uint32_t w = (live && !trunc) ? mw : 0u;
             if (t + 1 < n_tiles) mw = gmem[((int64_t)(t + 1) * kUG + li) * 2 + ch];  // ahead
             // waits are warp-uniform: the tensor-memory accesses below need the whole warp
-            bool good = ok && __all_sync(0xffffffffu, mbar_wait(&s_full[b], (uint32_t)(t >> 1) & 1u));
+            bool good = ok && __all_sync(0xffffffffu,
+                                         mbar_wait(&s_full[b], (uint32_t)(t >> 1) & 1u, wc.limit_ns));
             float x[32];
             float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
             if (good) {
@@ -607,10 +609,11 @@ attn_union_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
             // P buffer b was last read by P V(t - 2); O is touched only when rescaling, after
             // P V(t - 1)
             const bool w2 = t < 2 || __all_sync(0xffffffffu, mbar_wait(&o_done[b],
-                                                                       (uint32_t)((t - 2) >> 1) & 1u));
+                                                                       (uint32_t)((t - 2) >> 1) & 1u,
+                                                                       wc.limit_ns));
             const bool w3 = !(rescale && t >= 1) ||
                             __all_sync(0xffffffffu,
-                                       mbar_wait(&o_done[b ^ 1], (uint32_t)((t - 1) >> 1) & 1u));
+                                       mbar_wait(&o_done[b ^ 1], (uint32_t)((t - 1) >> 1) & 1u, wc.limit_ns));
             if (!(w2 && w3)) {
                 ok = false;  // stops at the next pair barrier (or the one after the loop)
                 continue;
@@ -639,7 +642,7 @@ attn_union_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         }
         if (ok && n_tiles > 0 &&
             !__all_sync(0xffffffffu, mbar_wait(&o_done[(n_tiles - 1) & 1],
-                                               (uint32_t)((n_tiles - 1) >> 1) & 1u)))
+                                               (uint32_t)((n_tiles - 1) >> 1) & 1u, wc.limit_ns)))
             ok = false;
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         // the row sum over both halves, and whether both warps of the pair finished (every
@@ -675,6 +678,7 @@ attn_union_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
                                                       : -INFINITY);
     }
 
+    if (!ok) report_timeout(wc);
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncthreads();
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
@@ -767,7 +771,7 @@ qsa_status launch_attn_union(const float *q, int64_t n_q, int H_q, int H_kv, flo
         return QSA_ERR_CUDA;
     e = launch(attn_union_kernel, dim3((unsigned)groups, (unsigned)H_kv), dim3(kUThreads),
                union_smem_bytes(), st, 1, tmK, tmV, q, n_q, H_q, scale * 1.4426950408889634f,
-               n_cells, max_cells, (const uint32_t *)ws, out, lse);
+               n_cells, max_cells, (const uint32_t *)ws, out, lse, current_wait_ctl());
     return e == cudaSuccess ? QSA_OK : QSA_ERR_CUDA;
 }
 

@@ -158,7 +158,7 @@ attn_wide_kernel(const float *__restrict__ q, int H_q, int H_kv, float scale_log
                  const int32_t *__restrict__ pos, const int32_t *__restrict__ n_cells,
                  int64_t max_cells, float *__restrict__ out, float *__restrict__ lse,
                  const uint8_t *__restrict__ mask, int64_t ld_mask,
-                 int32_t *__restrict__ counts_out)
+                 int32_t *__restrict__ counts_out, const WaitCtl wc)
 {
     constexpr int G = kWG, DK = kWDK, DV = kWDV, TC = kWTC, LD = kWLD, NT = kWNT;
     extern __shared__ __align__(16) char smem_raw[];
@@ -226,9 +226,10 @@ attn_wide_kernel(const float *__restrict__ q, int H_q, int H_kv, float scale_log
     }
     __syncthreads();
 
-    uint32_t sphase = 0;
+    // phases armed on / seen complete by each stage buffer's barrier (the same in every
+    // thread); a wait that gave up stops the stage loop (the outputs become NaN)
+    int armed0 = 0, armed1 = 0, done0 = 0, done1 = 0;
     bool lost = false;
-    uint32_t lost_at = 0;
     auto load_rows = [&](int it, int buf) {
         const int64_t base = c0 + (int64_t)it * TC;
         const int tc = (int)min((int64_t)TC, c1 - base);
@@ -255,18 +256,21 @@ attn_wide_kernel(const float *__restrict__ q, int H_q, int H_kv, float scale_log
         }
         const int nv = __syncthreads_count(tid < TC && rb[tid] >= 0);
         if (tid == 0) mbar_arrive_expect_tx(&sbar[buf], (uint32_t)nv * DK * 2u);
+        if (buf) ++armed1;
+        else ++armed0;
         if (tid < TC && rb[tid] >= 0) {
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             bulk_g2s(st + tid * LD, KV + (int64_t)rb[tid] * ld, DK * 2, &sbar[buf]);
         }
     };
     auto wait_rows = [&](int buf) {
-        if (!lost && !mbar_wait(&sbar[buf], (sphase >> buf) & 1u)) {
-            lost = true;
-            lost_at = (uint32_t)buf | (((sphase >> buf) & 1u) << 1);
+        const uint32_t par = (uint32_t)((buf ? done1 : done0) & 1);
+        const bool ok_w = !lost && mbar_wait(&sbar[buf], par, wc.limit_ns);
+        lost = __syncthreads_or(lost || !ok_w) != 0;
+        if (!lost) {
+            if (buf) ++done1;
+            else ++done0;
         }
-        sphase ^= 1u << buf;
-        __syncthreads();
     };
 
     float o[8][4];  // heads hr / hr + 8, dims 64 * warp + 8j + qc + {0, 1}
@@ -304,6 +308,7 @@ attn_wide_kernel(const float *__restrict__ q, int H_q, int H_kv, float scale_log
             copy_rows(buf ^ 1);
         }
         wait_rows(buf);
+        if (lost) break;  // issue nothing more; what was issued is drained below
         const int tc = (int)min((int64_t)TC, c1 - (c0 + (int64_t)it * TC));
         const __nv_bfloat16 *st = St + (size_t)buf * TC * LD;
         const int32_t *rw = rows + buf * TC;
@@ -413,7 +418,12 @@ attn_wide_kernel(const float *__restrict__ q, int H_q, int H_kv, float scale_log
         }
         __syncthreads();  // this stage and P are refilled next
     }
+    // every copy issued lands before the stage area is reused or the CTA leaves (a buffer is
+    // re-armed only after its previous phase was seen complete: at most one outstanding)
+    if (armed0 > done0) (void)mbar_wait(&sbar[0], (uint32_t)(done0 & 1));
+    if (armed1 > done1) (void)mbar_wait(&sbar[1], (uint32_t)(done1 & 1));
     lost = __syncthreads_or(lost);
+    if (lost && tid == 0) report_timeout(wc);
 
     // the CTA's state: unnormalised o (stage area, now free), m and l per head
 #pragma unroll
@@ -426,9 +436,6 @@ attn_wide_kernel(const float *__restrict__ q, int H_q, int H_kv, float scale_log
     }
     if (tid < G && lost) run_l[tid] = -1.0f;  // a negative weight sum marks a lost stage
     __syncthreads();
-    auto drain = [&]() {
-        if (lost) (void)mbar_wait(&sbar[lost_at & 1u], lost_at >> 1);
-    };
     if (S == 1) {
         for (int e = tid; e < G * DV; e += NT) {
             const int h = e / DV, c = e - h * DV;
@@ -440,7 +447,6 @@ attn_wide_kernel(const float *__restrict__ q, int H_q, int H_kv, float scale_log
                 lse[qi * H_q + g * G + h] = (overflow || lost) ? __int_as_float(0x7fc00000)
                                            : (L > 0.0f ? (run_m[h] + log2f(L)) * kLn2 : -INFINITY);
         }
-        drain();
         return;
     }
 
@@ -503,7 +509,6 @@ attn_wide_kernel(const float *__restrict__ q, int H_q, int H_kv, float scale_log
                                        : (L > 0.0f ? (hM[hh] + log2f(L)) * kLn2 : -INFINITY);
     }
     cluster.sync();  // keep this CTA's state alive until every remote read is done
-    drain();
 }
 
 }  // namespace
@@ -538,7 +543,8 @@ cudaError_t launch_attn_wide(const float *q, int64_t n_q, int H_q, int H_kv, flo
     const dim3 grid((unsigned)S, (unsigned)H_kv, (unsigned)n_q);
     return launch(attn_wide_kernel<false>, grid, dim3(kWNT), kWSmem, st, S > 1 ? S : 1, q, H_q,
                   H_kv, scale * kLog2e, (const __nv_bfloat16 *)KV, n_kv, ld, pos, n_cells,
-                  max_cells, out, lse, (const uint8_t *)nullptr, (int64_t)0, (int32_t *)nullptr);
+                  max_cells, out, lse, (const uint8_t *)nullptr, (int64_t)0, (int32_t *)nullptr,
+                  current_wait_ctl());
 }
 
 int64_t attn_wide_mask_max_kv() { return (int64_t)kWMaskWords * 64; }
@@ -555,7 +561,7 @@ cudaError_t launch_attn_wide_mask(const float *q, int64_t n_q, int H_q, int H_kv
     return launch(attn_wide_kernel<true>, grid, dim3(kWNT), kWSmem, st, S > 1 ? S : 1, q, H_q,
                   H_kv, scale * kLog2e, (const __nv_bfloat16 *)KV, n_kv, ld,
                   (const int32_t *)nullptr, (const int32_t *)nullptr, max_list, out, lse, mask,
-                  ld_mask, counts_out);
+                  ld_mask, counts_out, current_wait_ctl());
 }
 
 }  // namespace qsa

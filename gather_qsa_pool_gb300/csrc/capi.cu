@@ -33,6 +33,12 @@ int device_sm_count()
     return sms;
 }
 
+namespace {
+thread_local WaitCtl t_wait_ctl = {nullptr, kWaitLimitNs};
+}  // namespace
+
+WaitCtl current_wait_ctl() { return t_wait_ctl; }
+
 }  // namespace qsa
 
 using namespace qsa;
@@ -62,7 +68,13 @@ const char *qsa_status_str(qsa_status s)
     return "QSA_ERR_UNKNOWN";
 }
 
-int qsa_version(void) { return (2 << 16) | 3; }
+int qsa_version(void) { return (2 << 16) | 4; }
+
+void qsa_set_wait_options(int32_t *status_out, uint64_t pipeline_limit_ns)
+{
+    t_wait_ctl.status = status_out;
+    t_wait_ctl.limit_ns = pipeline_limit_ns;
+}
 
 static qsa_status check_pool_update(const void *raw_k, qsa_dtype raw_dtype, int64_t n_ctx, int H,
                                     int d, const float *norm_w, float eps, double rope_base,

@@ -25,9 +25,9 @@
 //     instead of 48 KB), so the same shared memory keeps 1.5 times the MMA time in flight;
 //   - tiles are ordered query-block-fastest, so the pairs working at the same time share a
 //     pooled tile and all but the first read it from L2;
-//   - every mbarrier wait is bounded (2 s): on a timeout the kernel records an error word,
-//     stops issuing, waits (bounded) for what it already issued, and always returns its
-//     tensor memory.
+//   - every mbarrier wait is bounded (the pipeline's by the caller's limit, the final ones by
+//     2 s): on a timeout the kernel reports it (qsa_set_wait_options), stops issuing, waits
+//     for what either CTA of the pair already issued, and always returns its tensor memory.
 #include <cuda.h>
 
 #include "qsa_internal.cuh"
@@ -48,7 +48,7 @@ constexpr int kEpiWarps = 4;                 // warps 2-5
 
 __host__ __device__ constexpr size_t tc_smem_bytes()
 {
-    return 1024 /* alignment slack */ + (size_t)kStages * (kTileA + kTileB) + 256;
+    return 1024 /* alignment slack */ + (size_t)kStages * (kTileA + kTileB) + 256;  // + barriers
 }
 
 // 64-bit shared-memory matrix descriptor of a K-major tile in the 128-byte swizzle:
@@ -136,6 +136,19 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar)
                  : "memory");
 }
 
+// Complete `bytes` transaction bytes of the barrier's current phase without a copy.
+__device__ __forceinline__ void mbar_complete_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.complete_tx.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+// Store a word into the shared memory of another CTA of the cluster (cluster address).
+__device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v)
+{
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
 __device__ __forceinline__ uint32_t bf16x2(float lo, float hi)
 {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -175,7 +188,7 @@ rows_to_bf16_kernel(const float4 *__restrict__ src, int64_t n4, uint2 *__restric
 __global__ void __launch_bounds__(kTcThreads, 1)
 score_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 int64_t n_q, const int32_t *__restrict__ q_pos, int64_t n_rows, int K,
-                float scale, float *__restrict__ scores, int64_t ld_scores, int *__restrict__ err)
+                float scale, float *__restrict__ scores, int64_t ld_scores, const WaitCtl wc)
 {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     // 1024-byte aligned operand area (the swizzle is a function of address bits 4-9); the
@@ -190,6 +203,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     uint64_t *acce = accf + 2;                             // [2] accumulator drained, leader
     uint64_t *drain = acce + 2;                            // every MMA issued has finished
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+    uint32_t *peer_issued = tmem_slot + 1;                 // leader: k-steps the peer issued
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t rank = cluster_rank();  // 0: the leader, which issues the pair's MMAs
@@ -231,6 +245,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     const int64_t pair = blockIdx.x >> 1, n_pairs = gridDim.x >> 1;
     const int n_k = K / kBK;
     bool ok = true;
+    uint32_t issued = 0;  // producer: k-steps whose copies this CTA issued
 
     if (warp == 0) {
         // ---- producer, in each CTA: its 128 queries and its 128 pooled rows of every stage,
@@ -244,7 +259,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 const int n0 = (int)((u / n_mb) * kBN + rank * (kBN / 2));
                 for (int kb = 0; kb < n_k; ++kb, ++it) {
                     const uint32_t stage = it % kStages, use = it / kStages;
-                    if (use > 0 && !mbar_wait(&empty[stage], (use - 1) & 1u)) {
+                    if (use > 0 && !mbar_wait(&empty[stage], (use - 1) & 1u, wc.limit_ns)) {
                         ok = false;
                         break;
                     }
@@ -254,12 +269,9 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     tma_load_2d_pair(sB + stage * kTileB, &tmB, kb * kBK, n0, fb);
                 }
             }
-            // the leader sees every stage it armed complete: both CTAs' copies have landed
-            if (leader)
-                for (uint32_t s = 0; s < kStages; ++s) {
-                    const uint32_t uses = it / kStages + (s < it % kStages ? 1u : 0u);
-                    if (uses > 0 && !mbar_wait(&full[s], (uses - 1) & 1u)) ok = false;
-                }
+            issued = it;
+            // the peer's count goes to the leader (read there after the cluster barrier below)
+            if (!leader) st_cluster_u32(map_to_rank(peer_issued, 0), it);
         }
     } else if (warp == 1) {
         // ---- MMA issuer: one thread of the leader; accumulators alternate between the two
@@ -270,14 +282,14 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             int64_t t = 0;
             for (int64_t u = pair; u < n_units && ok; u += n_pairs, ++t) {
                 const int j = (int)(t & 1);
-                if (t >= 2 && !mbar_wait(&acce[j], (uint32_t)((t >> 1) - 1) & 1u)) {
+                if (t >= 2 && !mbar_wait(&acce[j], (uint32_t)((t >> 1) - 1) & 1u, wc.limit_ns)) {
                     ok = false;
                     break;
                 }
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
                 for (int kb = 0; kb < n_k; ++kb, ++it) {
                     const uint32_t stage = it % kStages;
-                    if (!mbar_wait(&full[stage], (it / kStages) & 1u)) {
+                    if (!mbar_wait(&full[stage], (it / kStages) & 1u, wc.limit_ns)) {
                         ok = false;
                         break;
                     }
@@ -304,7 +316,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         int64_t t = 0;
         for (int64_t u = pair; u < n_units && ok; u += n_pairs, ++t) {
             const int j = (int)(t & 1);
-            if (!mbar_wait(&accf[j], (uint32_t)(t >> 1) & 1u)) {
+            if (!mbar_wait(&accf[j], (uint32_t)(t >> 1) & 1u, wc.limit_ns)) {
                 ok = false;
                 break;
             }
@@ -354,7 +366,29 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         }
     }
 
-    if (!ok) atomicExch(err, 1);
+    if (!ok) report_timeout(wc);
+    // Every copy either CTA issued completes on the leader's barriers, so the leader sees
+    // them all land before either CTA may leave.  After a wait gave up, the two producers may
+    // have stopped at different k-steps: a phase the leader armed (for both CTAs' bytes) but
+    // the peer never copied into gets the peer's bytes completed by the leader; a phase the
+    // peer copied into but the leader never armed is armed for the peer's bytes alone.  The
+    // producers run at most kStages k-steps apart (each waits for the MMAs to free a stage),
+    // so each stage has at most one such phase, and the phase before it has completed.
+    cluster_sync_all();  // the peer's count is in the leader's shared memory
+    if (warp == 0 && lane == 0 && leader) {
+        const uint32_t L = issued, N = *peer_issued;
+        const uint32_t lo = L < N ? L : N, hi = L < N ? N : L;
+        for (uint32_t x = lo; x < hi; ++x) {
+            const uint32_t stage = x % kStages, use = x / kStages;
+            if (use > 0) (void)mbar_wait(&full[stage], (use - 1) & 1u);
+            if (x < L) mbar_complete_tx(&full[stage], kTileA + kTileB);
+            else mbar_arrive_expect_tx(&full[stage], kTileA + kTileB);
+        }
+        for (uint32_t s = 0; s < kStages; ++s) {
+            const uint32_t uses = hi / kStages + (s < hi % kStages ? 1u : 0u);
+            if (uses > 0 && !mbar_wait(&full[s], (uses - 1) & 1u)) report_timeout(wc);
+        }
+    }
     // neither CTA leaves (or frees its tensor memory) while the pair's MMAs, copies or
     // remote arrivals may still touch it
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -407,11 +441,11 @@ size_t al256(size_t b) { return (b + 255) & ~(size_t)255; }
 
 size_t index_score_tc_workspace(int64_t n_q, int64_t n_rows, int H, int d, qsa_dtype pdt)
 {
-    // bf16 copies of the queries and (for an fp32 cache) of the pooled rows, then one
-    // error word; a bf16 cache is read in place
+    // bf16 copies of the queries and (for an fp32 cache) of the pooled rows; a bf16 cache is
+    // read in place
     const size_t K = (size_t)H * (size_t)d;
     const size_t rows = pdt == QSA_BF16 ? 0 : al256((size_t)n_rows * K * 2);
-    return al256((size_t)n_q * K * 2) + rows + 256;
+    return al256((size_t)n_q * K * 2) + rows;
 }
 
 qsa_status launch_index_score_tc(const float *q, int64_t n_q, int64_t ld_q,
@@ -434,7 +468,6 @@ qsa_status launch_index_score_tc(const float *q, int64_t n_q, int64_t ld_q,
     const __nv_bfloat16 *pb =
         convert_rows ? reinterpret_cast<__nv_bfloat16 *>(ws + al256((size_t)n_q * K * 2))
                      : static_cast<const __nv_bfloat16 *>(pooled);
-    int *err = reinterpret_cast<int *>(ws + need - 256);
     CUtensorMap tmA, tmB;
     if (!make_map(&tmA, qb, n_q, K, kBM) || !make_map(&tmB, pb, n_rows, K, kBN / 2))
         return QSA_ERR_CUDA;
@@ -471,7 +504,7 @@ qsa_status launch_index_score_tc(const float *q, int64_t n_q, int64_t ld_q,
     if (pairs > n_units) pairs = n_units;
     if (pairs < 1) pairs = 1;
     e = launch(score_tc_kernel, dim3((unsigned)(2 * pairs)), dim3(kTcThreads), tc_smem_bytes(), st,
-               2, tmA, tmB, n_q, q_pos, n_rows, K, scale, scores, ld_scores, err);
+               2, tmA, tmB, n_q, q_pos, n_rows, K, scale, scores, ld_scores, current_wait_ctl());
     return e == cudaSuccess ? QSA_OK : QSA_ERR_CUDA;
 }
 

@@ -114,9 +114,11 @@ __device__ __forceinline__ uint64_t global_ns()
 }
 
 // Wait until the barrier's phase with the given parity has completed; false once the wait
-// has lasted kWaitLimitNs (the caller then records an error and winds down).
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
+// has lasted limit_ns (the caller then records an error and winds down).  limit_ns == 0:
+// false at once, without looking (a way to drive the failure path on purpose).
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint64_t limit_ns)
 {
+    if (limit_ns == 0) return false;
     const uint32_t a = smem_u32(bar);
     uint64_t t0 = 0;
     for (uint32_t i = 0;; ++i) {
@@ -132,9 +134,30 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
         if ((i & 1023) == 0) {
             const uint64_t t = global_ns();
             if (t0 == 0) t0 = t;
-            else if (t - t0 > kWaitLimitNs) return false;
+            else if (t - t0 > limit_ns) return false;
         }
     }
+}
+
+// The same with the library's default limit (the drains that let every copy or MMA a kernel
+// issued complete before it exits always use it).
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
+{
+    return mbar_wait(bar, parity, kWaitLimitNs);
+}
+
+// Bounded waits of one launch: where a kernel reports that a wait gave up (nullable) and the
+// limit of the waits inside its pipeline, as qsa_set_wait_options() set them on the launching
+// host thread.
+struct WaitCtl {
+    int32_t *status;
+    uint64_t limit_ns;
+};
+WaitCtl current_wait_ctl();
+
+__device__ __forceinline__ void report_timeout(const WaitCtl &w)
+{
+    if (w.status) atomicExch(reinterpret_cast<int *>(w.status), (int)QSA_ERR_TIMEOUT);
 }
 
 // One plain arrival on the barrier.

@@ -48,7 +48,8 @@ typedef enum {
     QSA_ERR_INVALID_ARG = 1, /* a pointer, size, stride or alignment is invalid */
     QSA_ERR_UNSUPPORTED = 2, /* valid, but outside what this build implements */
     QSA_ERR_CUDA = 3,        /* a CUDA launch or query failed */
-    QSA_ERR_TIMEOUT = 4      /* reserved: a bounded device wait gave up */
+    QSA_ERR_TIMEOUT = 4      /* a bounded device wait gave up (reported in device memory,
+                                see qsa_set_wait_options) */
 } qsa_status;
 
 typedef enum { QSA_F32 = 0, QSA_BF16 = 1 } qsa_dtype;
@@ -64,8 +65,40 @@ const char *qsa_status_str(qsa_status s);
 
 /* Library ABI version: (major << 16) | minor.  Major 2: pooled-cache dtype arguments,
  * several queries per decode step, the host-fed decode step; minor 1: decode plans;
- * minor 2: qsa_mask_sparse_attn; minor 3: qsa_sparse_attn_union. */
+ * minor 2: qsa_mask_sparse_attn; minor 3: qsa_sparse_attn_union; minor 4:
+ * qsa_set_wait_options. */
 int qsa_version(void);
+
+/*
+ * qsa_set_wait_options -- bounded device waits: how long the kernels launched by later calls
+ * from the calling host thread may wait for their own asynchronous work, and where they report
+ * giving up.
+ *
+ * The source pages have no counterpart: it is this library's failure reporting.
+ *
+ * Kernels that stage data with asynchronous copies or run tcgen05 tensor-core work wait on
+ * shared-memory barriers: the attention kernels of qsa_sparse_attn (bf16, 128-dim, 8 query
+ * heads per KV head; the many-query form; the latent form), qsa_sparse_attn_union,
+ * qsa_mask_sparse_attn and qsa_decode_step / its host-fed and plan forms, and the tensor-core
+ * score contraction of qsa_index_score (QSA_PREC_BF16_TC).  No wait is unbounded.  When a
+ * wait inside a kernel's pipeline lasts longer than pipeline_limit_ns, the kernel stores
+ * QSA_ERR_TIMEOUT into *status_out (when status_out is not NULL), stops issuing work, waits
+ * for the copies and MMAs it already issued (bounded by the default limit, which these final
+ * waits always use), returns its tensor memory, and writes NaN to the outputs it could not
+ * finish (scores: the rows of a tile it never stored stay as they were).  The call itself
+ * returned QSA_OK long before: the caller reads the status after synchronising its stream.
+ *
+ *   status_out         device int32 or NULL; the library only ever stores QSA_ERR_TIMEOUT
+ *                      there (clear it before the calls it should cover)
+ *   pipeline_limit_ns  QSA_WAIT_DEFAULT_NS (2 s) is the default; 0 makes every pipeline wait
+ *                      give up at once, without looking (for testing the failure path: every
+ *                      covered kernel then reports QSA_ERR_TIMEOUT and leaves NaN or untouched
+ *                      outputs)
+ * The settings belong to the calling host thread and apply to every later launch from it
+ * (a CUDA graph captured meanwhile keeps the values of its capture) until changed.
+ */
+#define QSA_WAIT_DEFAULT_NS 2000000000ull
+void qsa_set_wait_options(int32_t *status_out, uint64_t pipeline_limit_ns);
 
 /*
  * qsa_pool_update -- incremental pooled-key cache update.
