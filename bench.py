@@ -542,7 +542,10 @@ def run_prefill(args, local, pooled_kind="f32"):
     gathered attention, one at a time and as one chained chunk; returns per-kernel
     microseconds, the chunk's and the score kernel's TFLOP/s.
     pooled_kind "bf16": the pooled cache is stored in bf16 and the contraction reads it in
-    place (no conversion pass)."""
+    place (no conversion pass).  "f32_mirror": an fp32 cache kept together with a bf16 mirror
+    (every pool update also writes the mirror's rows: bit for bit the cache's bf16 rounding),
+    which the contraction reads in place; the chunk's own mirror update (its new rows) is
+    timed as part of the chunk, in place of the rounding pass over the whole cache."""
     import torch
 
     import gather_qsa_pool_gb300 as qsa
@@ -556,10 +559,17 @@ def run_prefill(args, local, pooled_kind="f32"):
     pooled = torch.zeros(n_rows, H * d, dtype=pdt, device=dev)
     qsa.pool_update(inp["raw_k"], shape.n_ctx, H, d, inp["norm_w"], shape.eps, shape.rope_base,
                     pooled, 0)
+    score_src, score_dt = pooled, (qsa.QSA_BF16 if pooled_kind == "bf16" else qsa.QSA_F32)
+    mirror = None
+    if pooled_kind == "f32_mirror":
+        # the mirror as it stood before the chunk; the chunk's rows go in inside the timing
+        mirror = torch.zeros(n_rows, H * d, dtype=torch.bfloat16, device=dev)
+        qsa.pool_update(inp["raw_k"], shape.depth, H, d, inp["norm_w"], shape.eps,
+                        shape.rope_base, mirror, 0)
+        score_src, score_dt = mirror, qsa.QSA_BF16
     scores = torch.empty(n_q, n_rows, device=dev)
     ws = torch.zeros(qsa.index_score_workspace_size(
-        n_q, n_rows, H, d, qsa.QSA_PREC_BF16_TC,
-        qsa.QSA_BF16 if pooled_kind == "bf16" else qsa.QSA_F32), dtype=torch.uint8, device=dev)
+        n_q, n_rows, H, d, qsa.QSA_PREC_BF16_TC, score_dt), dtype=torch.uint8, device=dev)
     blocks = torch.empty(n_q, shape.k_blk, dtype=torch.int32, device=dev)
     counts = torch.empty(n_q, dtype=torch.int32, device=dev)
     pos = torch.empty(n_q, shape.max_cells, dtype=torch.int32, device=dev)
@@ -569,10 +579,16 @@ def run_prefill(args, local, pooled_kind="f32"):
                                                           shape.max_cells) // 4, 1), device=dev)
     scale_idx, scale = 1.0 / math.sqrt(d), 1.0 / math.sqrt(shape.d)
 
-    calls = [
-        ("score_tc", lambda: qsa.index_score(inp["q_idx"], pooled, n_rows, H, d, scale_idx, scores,
-                                              q_pos=inp["q_pos"], precision=qsa.QSA_PREC_BF16_TC,
-                                              workspace=ws)),
+    calls = []
+    if mirror is not None:
+        calls.append(("mirror_update",
+                      lambda: qsa.pool_update(inp["raw_k"], shape.n_ctx, H, d, inp["norm_w"],
+                                              shape.eps, shape.rope_base, mirror,
+                                              shape.depth // 4)))
+    calls += [
+        ("score_tc", lambda: qsa.index_score(inp["q_idx"], score_src, n_rows, H, d, scale_idx,
+                                              scores, q_pos=inp["q_pos"],
+                                              precision=qsa.QSA_PREC_BF16_TC, workspace=ws)),
         ("topk", lambda: qsa.topk_blocks(scores, n_rows, shape.k_blk, blocks, counts,
                                          q_pos=inp["q_pos"])),
         ("cells", lambda: qsa.gather_kv(blocks, counts, shape.k_blk, pos, n_cells, shape.max_cells,
@@ -607,7 +623,8 @@ def run_prefill(args, local, pooled_kind="f32"):
     attn_flops = 2.0 * 2.0 * n_q * shape.H_q * shape.d * float(n_cells.float().mean().item())
     out_d = {
         "workload": (f"prefill chunk: {n_q} queries at positions {shape.depth:,}..{shape.n_ctx - 1:,}, "
-                     f"indexer {H}x{d} ({pooled_kind} pooled cache), top-k {shape.top_k_tokens}, "
+                     f"indexer {H}x{d} ({pooled_kind.replace('_', ' with a bf16 ')} pooled cache), "
+                     f"top-k {shape.top_k_tokens}, "
                      f"attention {shape.H_q}/{shape.H_kv}x{shape.d} bf16"),
         "us": {k: round(v, 1) for k, v in res.items()},
         "chunk_us": round(sum(res.values()), 1),
@@ -617,7 +634,7 @@ def run_prefill(args, local, pooled_kind="f32"):
         "attn_tflops": attn_flops / (res["attn"] * 1e-6) / 1e12,
         "tokens_per_s": n_q / ((chunk_graph or sum(res.values())) * 1e-6),
     }
-    del inp, pooled, scores, ws, pos, out, aws
+    del inp, pooled, mirror, score_src, scores, ws, pos, out, aws
     torch.cuda.empty_cache()
     return out_d
 
@@ -1074,6 +1091,7 @@ def main():
                                    pooled_cache=pooled, queries_per_step=n_q)
         if not args.no_prefill:
             variants["prefill_bf16_pooled"] = run_prefill(args, local, "bf16")
+            variants["prefill_f32_pooled_bf16_mirror"] = run_prefill(args, local, "f32_mirror")
     r = results[args.primary]
     sh = r["shape"]
     value = sweep[args.primary]["steps_per_s"]

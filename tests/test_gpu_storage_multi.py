@@ -398,3 +398,35 @@ def test_plan_steps_with_changing_query_counts():
         assert torch.equal(a.blocks[:n_q], b.blocks[:n_q])
         assert torch.equal(a.n_cells[:n_q], b.n_cells[:n_q])
         assert torch.equal(out_a, b.out[:n_q])
+
+
+def test_bf16_mirror_of_an_fp32_cache_is_its_rounding():
+    """An fp32 pooled cache kept together with a bf16 mirror (every pool update also written
+    into the mirror) for the tensor-core prefill scores: after a rebuild and an incremental
+    chunk of 1,024 tokens, the mirror is bit for bit the fp32 cache rounded to bf16 (nearest
+    even: the update computes one fp32 value per element and rounds it for bf16 storage), so
+    the scores read from the mirror in place equal those of the fp32 cache's own rounding
+    pass."""
+    shape = qsa_synth.shrink(qsa_synth.CONFIGS["prefill_256k"], depth=40_001)
+    inp = qsa_synth.prefill_inputs(shape, seed=4096)
+    H, d, n_q, n_rows, n_ctx = shape.H_idx, shape.d_idx, shape.n_q, shape.n_rows, shape.n_ctx
+    raw, w = to_dev(inp["raw_k"]), to_dev(inp["norm_w"])
+    f32 = torch.zeros(n_rows, H * d, device="cuda")
+    mirror = torch.zeros(n_rows, H * d, dtype=torch.bfloat16, device="cuda")
+    for cache in (f32, mirror):
+        qsa.pool_update(raw, shape.depth, H, d, w, shape.eps, shape.rope_base, cache, 0)
+        qsa.pool_update(raw, n_ctx, H, d, w, shape.eps, shape.rope_base, cache, shape.depth // 4)
+    torch.cuda.synchronize()
+    assert torch.equal(mirror.view(torch.int16), f32.to(torch.bfloat16).view(torch.int16))
+    q_pos = to_dev(inp["q_pos"])
+    q = to_dev(inp["q_idx"])
+    out = []
+    for src, dt in ((f32, qsa.QSA_F32), (mirror, qsa.QSA_BF16)):
+        ws = torch.zeros(qsa.index_score_workspace_size(n_q, n_rows, H, d, qsa.QSA_PREC_BF16_TC,
+                                                        dt), dtype=torch.uint8, device="cuda")
+        sc = torch.empty(n_q, n_rows, device="cuda")
+        qsa.index_score(q, src, n_rows, H, d, 1.0 / math.sqrt(d), sc, q_pos=q_pos,
+                        precision=qsa.QSA_PREC_BF16_TC, workspace=ws)
+        out.append(sc)
+    torch.cuda.synchronize()
+    assert torch.equal(out[0], out[1])
