@@ -563,8 +563,12 @@ attn_mma_kernel(const float *__restrict__ q, int H_q, int H_kv, float scale_log2
                 const __nv_bfloat16 *__restrict__ K, const __nv_bfloat16 *__restrict__ V,
                 int64_t n_kv, int64_t ld_k, int64_t ld_v, const int32_t *__restrict__ pos,
                 const int32_t *__restrict__ n_cells, int64_t max_cells, float *__restrict__ out,
-                float *__restrict__ lse, int early_q, const WaitCtl wc)
+                float *__restrict__ lse, int early_q, const WaitCtl wc,
+                float *__restrict__ out_host, float *__restrict__ lse_host)
 {
+    // out_host / lse_host (nullable): a second copy of out / lse, written in place into the
+    // caller's page-locked host memory (the host-fed decode step), so that no copy kernel
+    // follows this one.
     constexpr int G = 8, D = 128, TC = 16 * NW, LD = kMmaLd, NT = 32 * NW;
     constexpr int TX = attn_mma_stage_rows<NW, NB>();  // rows of a stage buffer
     static_assert(NT == 2 * TC, "one thread per cell of the first two stages");
@@ -863,10 +867,15 @@ attn_mma_kernel(const float *__restrict__ q, int H_q, int H_kv, float scale_log2
         if (S == 1) {
             float v = L > 0.0f ? acc / L : 0.0f;
             if (overflow || lost) v = __int_as_float(0x7fc00000);
-            out[(qi * H_q + (int64_t)g * G + h) * D + c] = v;
-            if (lse && c == 0)
-                lse[qi * H_q + g * G + h] = (overflow || lost) ? __int_as_float(0x7fc00000)
-                                           : (L > 0.0f ? (M + log2f(L)) * kLn2 : -INFINITY);
+            const int64_t oi = (qi * H_q + (int64_t)g * G + h) * D + c;
+            out[oi] = v;
+            if (out_host) out_host[oi] = v;
+            if (lse && c == 0) {
+                const float lv_ = (overflow || lost) ? __int_as_float(0x7fc00000)
+                                  : (L > 0.0f ? (M + log2f(L)) * kLn2 : -INFINITY);
+                lse[qi * H_q + g * G + h] = lv_;
+                if (lse_host) lse_host[qi * H_q + g * G + h] = lv_;
+            }
         } else {
             float *r = cta + h * (D + 2);
             r[c] = acc;
@@ -929,10 +938,15 @@ attn_mma_kernel(const float *__restrict__ q, int H_q, int H_kv, float scale_log2
         if (part == 0 && live) {
             float v = L > 0.0f ? acc / L : 0.0f;
             if (bad) v = __int_as_float(0x7fc00000);
-            out[(qi * H_q + (int64_t)g * G + h) * D + c] = v;
-            if (lse && c == 0)
-                lse[qi * H_q + g * G + h] = bad ? __int_as_float(0x7fc00000)
-                                           : (L > 0.0f ? (M + log2f(L)) * kLn2 : -INFINITY);
+            const int64_t oi = (qi * H_q + (int64_t)g * G + h) * D + c;
+            out[oi] = v;
+            if (out_host) out_host[oi] = v;
+            if (lse && c == 0) {
+                const float lv_ = bad ? __int_as_float(0x7fc00000)
+                                  : (L > 0.0f ? (M + log2f(L)) * kLn2 : -INFINITY);
+                lse[qi * H_q + g * G + h] = lv_;
+                if (lse_host) lse_host[qi * H_q + g * G + h] = lv_;
+            }
         }
     }
     cluster.sync();  // keep this CTA's state alive until every remote read is done
@@ -1020,7 +1034,7 @@ cudaError_t launch_attn_mma_t(int S, const float *q, int64_t n_q, int H_q, int H
                               const void *K, const void *V, int64_t n_kv, int64_t ld_k,
                               int64_t ld_v, const int32_t *pos, const int32_t *n_cells,
                               int64_t max_cells, float *out, float *lse, cudaStream_t st,
-                              bool early_q)
+                              bool early_q, float *out_host, float *lse_host)
 {
     auto k = attn_mma_kernel<NW, NB>;
     const size_t smem = attn_mma_smem<NW, NB>();
@@ -1029,13 +1043,15 @@ cudaError_t launch_attn_mma_t(int S, const float *q, int64_t n_q, int H_q, int H
     const dim3 grid((unsigned)S, (unsigned)H_kv, (unsigned)n_q);
     return launch(k, grid, dim3(32 * NW), smem, st, S > 1 ? S : 1, q, H_q, H_kv,
                   scale * kLog2e, (const __nv_bfloat16 *)K, (const __nv_bfloat16 *)V, n_kv, ld_k,
-                  ld_v, pos, n_cells, max_cells, out, lse, early_q ? 1 : 0, current_wait_ctl());
+                  ld_v, pos, n_cells, max_cells, out, lse, early_q ? 1 : 0, current_wait_ctl(),
+                  out_host, lse_host);
 }
 
 cudaError_t launch_attn_mma(const float *q, int64_t n_q, int H_q, int H_kv, float scale,
                             const void *K, const void *V, int64_t n_kv, int64_t ld_k, int64_t ld_v,
                             const int32_t *pos, const int32_t *n_cells, int64_t max_cells,
-                            float *out, float *lse, cudaStream_t st, bool early_q)
+                            float *out, float *lse, cudaStream_t st, bool early_q,
+                            float *out_host, float *lse_host)
 {
     const int S = attn_mma_splits(n_q, H_kv, max_cells);
     // Several queries per step: n_q * H_kv clusters of S CTAs at one CTA per SM would need a
@@ -1045,9 +1061,11 @@ cudaError_t launch_attn_mma(const float *q, int64_t n_q, int H_q, int H_kv, floa
     const int64_t ctas = n_q * (int64_t)H_kv * S;
     if (S > 1 && ctas > device_sm_count() && ctas <= 2 * (int64_t)device_sm_count())
         return launch_attn_mma_t<kMmaWarps, 1>(S, q, n_q, H_q, H_kv, scale, K, V, n_kv, ld_k, ld_v,
-                                               pos, n_cells, max_cells, out, lse, st, early_q);
+                                               pos, n_cells, max_cells, out, lse, st, early_q,
+                                               out_host, lse_host);
     return launch_attn_mma_t<kMmaWarps, 2>(S, q, n_q, H_q, H_kv, scale, K, V, n_kv, ld_k, ld_v, pos,
-                                           n_cells, max_cells, out, lse, st, early_q);
+                                           n_cells, max_cells, out, lse, st, early_q, out_host,
+                                           lse_host);
 }
 
 template <typename T, int G>
@@ -1135,11 +1153,23 @@ size_t attn_partials_bytes(qsa_dtype dt, int64_t n_q, int H_q, int H_kv, int d_k
     return attn_workspace_bytes(n_q, H_q, H_kv, d_v, max_cells);
 }
 
+bool attn_writes_host(qsa_dtype dt, int64_t n_q, int H_q, int H_kv, int d_k, int d_v,
+                      const void *K, const void *V, int64_t ld_k, int64_t ld_v,
+                      const int32_t *pos, int64_t max_cells)
+{
+    if (H_kv <= 0 || H_q % H_kv) return false;
+    // the same order of choices as launch_sparse_attn
+    return !attn_uses_rows4(dt, n_q, H_q, H_kv, d_k, d_v, K, V, ld_k, ld_v, pos, max_cells) &&
+           !(H_kv == 1 && attn_uses_wide(dt, d_k, d_v, H_q / H_kv, K, V, ld_k, ld_v)) &&
+           attn_uses_mma(dt, d_k, d_v, H_q / H_kv);
+}
+
 cudaError_t launch_sparse_attn(const float *q, int64_t n_q, int H_q, int H_kv, int d_k, int d_v,
                                float scale, const void *K, const void *V, qsa_dtype dt,
                                int64_t n_kv, int64_t ld_k, int64_t ld_v, const int32_t *pos,
                                const int32_t *n_cells, int64_t max_cells, float *out,
-                               float *lse, float *partials, cudaStream_t st, bool early_q)
+                               float *lse, float *partials, cudaStream_t st, bool early_q,
+                               float *out_host, float *lse_host)
 {
     if (n_q == 0) return cudaSuccess;
     const int S = attn_num_splits(n_q, H_kv, max_cells);
@@ -1152,7 +1182,8 @@ cudaError_t launch_sparse_attn(const float *q, int64_t n_q, int H_q, int H_kv, i
                                 out, lse, st);
     if (attn_uses_mma(dt, d_k, d_v, G))
         return launch_attn_mma(q, n_q, H_q, H_kv, scale, K, V, n_kv, ld_k, ld_v, pos, n_cells,
-                               max_cells, out, lse, st, early_q);
+                               max_cells, out, lse, st, early_q, out_host, lse_host);
+    if (out_host || lse_host) return cudaErrorNotSupported;  // only the form above writes them
     if (d_k == 128 && d_v == 128 && G <= 8) {
 #define QSA_ATTN128_CASE(GG)                                                                   \
     case GG:                                                                                   \

@@ -455,13 +455,25 @@ static qsa_status decode_step_impl(const void *raw_k, qsa_dtype raw_dtype, int64
             e = launch_topk(scores, n_q, n_rows, nullptr, n_full, k_blk, blocks, counts, n_ctx, pos,
                             n_cells, max_cells, hist, st, 1);
     }
-    // 4. attention over the listed cells, read in place from the cache
+    // 4. attention over the listed cells, read in place from the cache.  Fed from host
+    // memory, the tensor-core form also writes the outputs straight into mapped page-locked
+    // host buffers (no copy kernel after it).
+    float *ho_direct = nullptr, *hl_direct = nullptr;
+    if (feed && attn_writes_host(kv_dtype, n_q, H_q, H_kv, d, d, K, V, ld_kv, ld_kv, pos,
+                                 max_cells)) {
+        float *ho = static_cast<float *>(mapped_host_view(feed->h_out));
+        float *hl = feed->h_lse ? static_cast<float *>(mapped_host_view(feed->h_lse)) : nullptr;
+        if (ho && aligned(ho, 4) && (!feed->h_lse || (hl && aligned(hl, 4)))) {
+            ho_direct = ho;
+            hl_direct = hl;
+        }
+    }
     if (e == cudaSuccess)
         e = launch_sparse_attn(q, n_q, H_q, H_kv, d, d, scale, K, V, kv_dtype, n_kv, ld_kv, ld_kv,
                                pos, n_cells, max_cells, out, lse_out, (float *)workspace, st,
-                               true);
-    // 5. the outputs back to host memory
-    if (feed && e == cudaSuccess) {
+                               true, ho_direct, hl_direct);
+    // 5. the outputs back to host memory (unless the attention wrote them there)
+    if (feed && e == cudaSuccess && !ho_direct) {
         const int64_t ob = (int64_t)sizeof(float) * n_q * H_q * d;
         const int64_t lb = (int64_t)sizeof(float) * n_q * H_q;
         void *ho = mapped_host_view(feed->h_out);

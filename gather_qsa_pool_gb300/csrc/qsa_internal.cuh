@@ -522,7 +522,13 @@ cudaError_t launch_sparse_attn(const float *q, int64_t n_q, int H_q, int H_kv, i
                                int64_t n_kv, int64_t ld_k, int64_t ld_v, const int32_t *pos,
                                const int32_t *n_cells, int64_t max_cells, float *out,
                                float *lse, float *partials, cudaStream_t st,
-                               bool early_q = false);  // q written before the predecessor
+                               bool early_q = false,  // q written before the predecessor
+                               float *out_host = nullptr, float *lse_host = nullptr);
+// (out_host / lse_host: device views of page-locked host buffers that also receive out /
+// lse; only the bf16 8-head tensor-core form writes them, attn_writes_host() says when.)
+bool attn_writes_host(qsa_dtype dt, int64_t n_q, int H_q, int H_kv, int d_k, int d_v,
+                      const void *K, const void *V, int64_t ld_k, int64_t ld_v,
+                      const int32_t *pos, int64_t max_cells);
 
 cudaError_t launch_mask_to_list(const uint8_t *mask, int64_t n_rows, int64_t n_kv,
                                 int64_t ld_mask, int64_t max_list, int32_t *pos_out,

@@ -410,9 +410,11 @@ size_t qsa_decode_step_workspace_size(int64_t n_q, int H_q, int H_kv, int d, int
  * current device's address space (cudaHostAlloc'd or registered memory on a unified-address
  * system; torch's pin_memory() buffers are), the copy kernel reads it in place over the
  * host link; otherwise one host-to-device copy of h_in (qsa_decode_step_host_layout()
- * bytes) into the staging area comes first.  Likewise mapped h_out / h_lse are written by
- * a kernel after the attention, other host buffers by device-to-host copies.  The call
- * returns without waiting: synchronise the stream before reading h_out or reusing h_in.
+ * bytes) into the staging area comes first.  Likewise mapped h_out / h_lse are written in
+ * place: by the attention kernel itself (bf16 K/V, d 128, 8 query heads per KV head, where
+ * it also writes out / lse_out), else by a copy kernel after it; other host buffers by
+ * device-to-host copies.  The call returns without waiting: synchronise the stream before
+ * reading h_out or reusing h_in.
  *
  *   h_in    packed inputs, sections at the byte offsets qsa_decode_step_host_layout()
  *           reports: [n_q][H_idx*d_idx] raw-key rows (raw_dtype), [n_q][H_kv*d] K rows and
