@@ -256,3 +256,94 @@ def test_prefill_chunk_1024_queries_at_255181_sampled():
         else:
             assert n_band > 0
     assert agree >= len(sample) - 1
+
+
+@pytest.mark.parametrize("store,n_q,steps", [("bf16", 1, 16), ("f32", 3, 6), ("bf16", 3, 6)],
+                         ids=["bf16-pooled", "three-queries", "three-queries-bf16-pooled"])
+def test_decode_255181_tokens_variants_appending(store, n_q, steps):
+    """The benchmarked variants at 255,181 tokens in their launch configuration: a bf16
+    pooled cache (half the scan's bytes) and steps carrying three query tokens (a token and
+    two drafts), appending n_q tokens per step, against the oracle's multi-query step at
+    every step: the recomputed rows (bf16 rows: each stored value a rounding of a value
+    within the kernel's fp32 error of the exact one), 2,000 sampled rows at the first step,
+    every score of every query, each query's selection (the tie band widened, for bf16 rows,
+    by what a rounding the other way can move a score), cell list and output."""
+    shape = qsa_synth.CONFIGS["decode_256k"]
+    inp = qsa_synth.decode_inputs(shape, seed=2551 + n_q, extra_tokens=n_q * steps,
+                                  n_steps=n_q * steps)
+    H, d = shape.H_idx, shape.d_idx
+    scale = 1.0 / math.sqrt(d)
+    raw, w, K, V = (to_dev(inp["raw_k"]), to_dev(inp["norm_w"]), to_dev(inp["K"]),
+                    to_dev(inp["V"]))
+    bf = store == "bf16"
+    lay = qsa.DecodeLayer(cap_tokens=shape.n_ctx + n_q * steps, H_idx=H, d_idx=d,
+                          H_q=shape.H_q, H_kv=shape.H_kv, d=shape.d,
+                          top_k_tokens=shape.top_k_tokens, eps=shape.eps,
+                          rope_base=shape.rope_base,
+                          pooled_dtype=torch.bfloat16 if bf else None, max_queries=n_q)
+    n0 = shape.n_ctx - n_q
+    lay.rebuild(raw, w, n0)
+    o_pooled = np.zeros((lay.cap_rows, H * d), np.uint16 if bf else np.float32)
+    oracle.pool_rows(inp["raw_k"], n0, H, d, inp["norm_w"], shape.eps, shape.rope_base, 0,
+                     (n0 + 3) // 4, o_pooled)
+    o_valid = n0 // 4
+    q_idx_all = inp["q_idx"].reshape(steps, n_q, -1)
+    q_all = inp["q"].reshape(steps, n_q, shape.H_q, shape.d)
+    rng = np.random.default_rng(2551)
+    agree = 0
+    for s in range(steps):
+        n_ctx = n0 + n_q * (s + 1)
+        n_rows = (n_ctx + 3) // 4
+        lay.step(raw, w, K, V, n_ctx, to_dev(q_idx_all[s]), to_dev(q_all[s]))
+        res, o_scores = oracle.decode_step_multi(
+            inp["raw_k"], n_ctx, H, d, inp["norm_w"], shape.eps, shape.rope_base, o_pooled,
+            o_valid, q_idx_all[s], shape.top_k_tokens, q_all[s], inp["K"], inp["V"], shape.H_q,
+            shape.H_kv, shape.d)
+        rows = np.arange(o_valid, n_rows)
+        if s == 0:
+            rows = np.concatenate([rng.choice(o_valid, 2000, replace=False), rows])
+        o_valid = n_ctx // 4
+        g_all = to_host(lay.pooled)
+        if bf:
+            z = pooled_f64(inp, shape, n_ctx, rows)
+            check_bf16_rows(g_all[rows], o_pooled[rows], z, d)
+            g_vals = qsa_synth.bf16_bits_to_f32(g_all[:n_rows])
+        else:
+            np.testing.assert_allclose(g_all[rows], o_pooled[rows], rtol=2e-5,
+                                       atol=2e-6 * float(np.abs(o_pooled[rows]).max()))
+            g_vals = g_all[:n_rows]
+        g_scores = to_host(lay.scores_of(n_q, n_ctx))
+        blocks, counts = to_host(lay.blocks), to_host(lay.counts)
+        pos, n_cells, out = to_host(lay.pos), to_host(lay.n_cells), to_host(lay.out)
+        # the GPU's scores of its own cache against the fp32 summation bound (the bound of
+        # score_tolerance, for all queries at once)
+        g64 = g_vals.astype(np.float64)
+        qs = q_idx_all[s].astype(np.float64).T
+        ref_all = (g64 @ qs).T * scale
+        chain = H * d / 128 + 8
+        tol_all = (2.0 * chain * 2.0 ** -24 * scale * (np.abs(g64) @ np.abs(qs))).T + 1e-30
+        del g64
+        for i in range(n_q):
+            assert np.all(np.abs(g_scores[i] - ref_all[i]) <= tol_all[i]), f"step {s} query {i}"
+            p = n_ctx - n_q + i
+            n_i = min(n_ctx // 4, (p + 1) // 4)
+            band = None
+            if bf:
+                # what a bf16 rounding the other way can move a score, for the rows near the
+                # k-th best oracle score (elsewhere it cannot change the selection)
+                srt = np.sort(np.nan_to_num(o_scores[i][:n_i], nan=-np.inf))[::-1]
+                s_k = srt[shape.k_blk - 1]
+                near = np.flatnonzero(np.abs(o_scores[i][:n_i] - s_k) <= 1e-2 * abs(s_k))
+                band = np.zeros(n_i)
+                band[near] = flip_band(q_idx_all[s][i], pooled_f64(inp, shape, n_ctx, near), d,
+                                       scale)
+            n_band = check_topk(blocks[i], int(counts[i]), o_scores[i], n_i, shape.k_blk,
+                                band_abs=band)
+            o_blocks, o_cells, o_out, _ = res[i]
+            if np.array_equal(blocks[i, :counts[i]], o_blocks):
+                np.testing.assert_array_equal(pos[i, :n_cells[i]], o_cells)
+                np.testing.assert_allclose(out[i], o_out, rtol=0, atol=ATOL_ATTN_BF16)
+                agree += 1
+            else:
+                assert n_band > 0
+    assert agree >= n_q * steps - 2
