@@ -70,6 +70,12 @@ def parse_args():
                     help="pooled-key cache storage of the main sweep")
     ap.add_argument("--queries", type=int, default=1, choices=[1, 2, 3, 4],
                     help="query tokens per decode step of the main sweep")
+    ap.add_argument("--union-only", action="store_true",
+                    help="run only the grouped-union sweep (a profiling case; with "
+                         "--union-queries / --union-depth / --union-shares)")
+    ap.add_argument("--union-queries", type=int, default=1024)
+    ap.add_argument("--union-depth", type=int, default=255181)
+    ap.add_argument("--union-shares", default="0,0.5,0.75,0.85,0.9,0.95,1")
     return ap.parse_args()
 
 
@@ -652,7 +658,8 @@ def run_grouped_union(args, local):
     import gather_qsa_pool_gb300 as qsa
     import qsa_synth
 
-    shape = qsa_synth.CONFIGS["prefill_256k"]
+    shape = qsa_synth.shrink(qsa_synth.CONFIGS["prefill_256k"], n_q=args.union_queries,
+                             depth=args.union_depth)
     dev = torch.device("cuda", local)
     n_q, n_ctx, d, H_kv, H_q = shape.n_q, shape.n_ctx, shape.d, shape.H_kv, shape.H_q
     g = torch.Generator(device=dev)
@@ -670,7 +677,7 @@ def run_grouped_union(args, local):
     pos = torch.empty(n_q, shape.max_cells, dtype=torch.int32, device=dev)
     n_cells = torch.empty(n_q, dtype=torch.int32, device=dev)
     rows = []
-    for share in (0.0, 0.5, 0.75, 0.85, 0.9, 0.95, 1.0):
+    for share in (float(x) for x in args.union_shares.split(",")):
         blocks = qsa_synth.overlap_block_lists((q_pos + 1) // 4, shape.k_blk, 16, share,
                                                int(1000 * share) + 7)
         bl = np.zeros((n_q, shape.k_blk), np.int32)
@@ -1032,6 +1039,16 @@ def main():
     import qsa_synth
 
     primary = qsa_synth.CONFIGS[CONTEXTS[args.primary]]
+
+    if args.union_only:
+        import torch
+
+        torch.cuda.set_device(0)
+        import gather_qsa_pool_gb300 as qsa
+
+        qsa.load()
+        print(json.dumps({"grouped_union": run_grouped_union(args, 0)}))
+        return
 
     if args.impl == "reference":
         world = int(os.environ.get("WORLD_SIZE", "1"))

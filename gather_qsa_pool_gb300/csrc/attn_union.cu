@@ -19,9 +19,12 @@
 // bit per union cell (4 per block) says whether the cell is in that query's list.
 //
 // Kernel 2, attn_union_kernel (one CTA per group and KV head; M = 16 queries x 8 heads =
-// 128 rows): warp 0 stages the union's blocks 16 at a time (a 64-cell tile of K and one of
-// V: one 3-D TMA box of 4 cells x 64 dims per block and half, 128-byte swizzle) into a ring
-// of six stages; warp 1 issues the MMAs -- S = Q K^T (N 64 cells, K 128 dims; A is the
+// 128 rows): warps 0 and 10 stage the union's blocks 16 at a time (a 64-cell tile of K and
+// one of V, each cell's 256-byte head row as sixteen 16-byte asynchronous copies written
+// straight into the 128-byte-swizzled layout the tensor cores read) into a ring of six
+// stages; a stage's barrier completes when the copies of both warps have landed.  (One TMA
+// box per block and dim half, 512 bytes each, ran at about 70 cycles a box: the box count,
+// not the bytes, bounded the kernel.)  Warp 1 issues the MMAs -- S = Q K^T (N 64 cells, K 128 dims; A is the
 // query's bf16 high and low halves, pre-scaled by scale * log2 e, held in tensor memory) into
 // one of two tensor-memory buffers, then O += P V (N 128 dims, K 64 cells, V read MN-major;
 // A is P's high and low halves, in one of two tensor-memory buffers) into a third; warps 2-5
@@ -31,8 +34,6 @@
 // two P buffers, the softmax of tile t overlaps the MMAs of tiles t - 1 and t + 1.  Every mbarrier wait is bounded: on a timeout the
 // rows of the CTA become NaN, nothing new is issued, what was issued is waited for (bounded)
 // and the tensor memory is returned.
-#include <cuda.h>
-
 #include "attn_union.cuh"
 
 namespace qsa {
@@ -45,7 +46,8 @@ constexpr int kUD = 128;                // head dim
 constexpr int kUTB = 16;                // union blocks per tile
 constexpr int kUTC = 4 * kUTB;          // 64 cells per tile
 constexpr int kUStages = 6;
-constexpr int kUThreads = 320;          // warp 0 TMA, warp 1 MMA, warps 2-9 softmax
+constexpr int kUThreads = 352;          // warps 0 and 10 copy, warp 1 MMA, warps 2-9 softmax
+constexpr int kUCopyThreads = 64;       // the two copy warps
 constexpr int kUEpiWarps = 8;           // two per row: one per half of the tile's columns
 constexpr float kURescale = 8.0f;       // move the running maximum past 2^8 growth
 constexpr int kUMaxBlockWords = 8192;   // bitmap words: 2^18 blocks = 2^20 cells
@@ -105,22 +107,43 @@ union_build_kernel(const int32_t *__restrict__ pos, const int32_t *__restrict__ 
     const int nq = (int)min((int64_t)kUG, n_q - q0);
     uint32_t *gw = ws + g * union_group_words(max_cells);
     const int tid = threadIdx.x, nt = blockDim.x;
+    __shared__ int32_t len_s[kUG];  // cells of each list (0 for a truncated one)
+    if (tid < kUG) {
+        int64_t n = tid < nq ? (int64_t)n_cells[q0 + tid] : 0;
+        if (n < 0 || n > max_cells) n = 0;
+        len_s[tid] = (int32_t)n;
+    }
     for (int w = tid; w < nwords; w += nt) bits[w] = 0u;
     for (int w = tid; w < kUG * mwords; w += nt) mem[w] = 0u;
     __syncthreads();
+    // The lists' cells, visited as one flat range (list li at index li * max_cells + e),
+    // kBatch independent loads in flight per thread before any is used.
+    constexpr int kBatch = 8;
+    const int64_t span = (int64_t)nq * max_cells;
+    auto for_each_cell = [&](auto &&f) {
+        for (int64_t base = tid; base < span; base += (int64_t)nt * kBatch) {
+            int32_t c[kBatch];
+            int li_[kBatch];
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                const int64_t t = base + (int64_t)u * nt;
+                const int li = (int)(t / max_cells);
+                const int64_t e = t - (int64_t)li * max_cells;
+                li_[u] = li;
+                c[u] = (t < span && e < len_s[li < kUG ? li : 0]) ? pos[(q0 + li) * max_cells + e]
+                                                                   : -1;
+            }
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u)
+                if (c[u] >= 0 && c[u] < n_kv) f(li_[u], c[u]);
+        }
+    };
 
     // every valid cell of every (non-truncated) list marks its block
-    for (int li = 0; li < nq; ++li) {
-        const int64_t n = n_cells[q0 + li];
-        if (n < 0 || n > max_cells) continue;
-        const int32_t *pl = pos + (q0 + li) * max_cells;
-        for (int64_t e = tid; e < n; e += nt) {
-            const int32_t c = pl[e];
-            if (c < 0 || c >= n_kv) continue;
-            const int b = c >> 2;
-            atomicOr(&bits[b >> 5], 1u << (b & 31));
-        }
-    }
+    for_each_cell([&](int, int32_t c) {
+        const int b = c >> 2;
+        atomicOr(&bits[b >> 5], 1u << (b & 31));
+    });
     __syncthreads();
 
     // exclusive scan of the words' popcounts: each thread a contiguous run of words
@@ -172,19 +195,12 @@ union_build_kernel(const int32_t *__restrict__ pos, const int32_t *__restrict__ 
         }
     }
     // membership: bit 4j + (c & 3) of query li's words for cell c of union block j
-    for (int li = 0; li < nq; ++li) {
-        const int64_t n = n_cells[q0 + li];
-        if (n < 0 || n > max_cells) continue;
-        const int32_t *pl = pos + (q0 + li) * max_cells;
-        for (int64_t e = tid; e < n; e += nt) {
-            const int32_t c = pl[e];
-            if (c < 0 || c >= n_kv) continue;
-            const int b = c >> 2;
-            const uint32_t j = base[b >> 5] + __popc(bits[b >> 5] & ((1u << (b & 31)) - 1u));
-            const uint32_t k = 4 * j + (uint32_t)(c & 3);
-            atomicOr(&mem[li * mwords + (k >> 5)], 1u << (k & 31));
-        }
-    }
+    for_each_cell([&](int li, int32_t c) {
+        const int b = c >> 2;
+        const uint32_t j = base[b >> 5] + __popc(bits[b >> 5] & ((1u << (b & 31)) - 1u));
+        const uint32_t k = 4 * j + (uint32_t)(c & 3);
+        atomicOr(&mem[li * mwords + (k >> 5)], 1u << (k & 31));
+    });
     __syncthreads();
     // out in tile-major order: [tile][query][2 words], 64 cells per tile
     uint32_t *gm = gw + 4 + cap;
@@ -253,14 +269,20 @@ __device__ __forceinline__ void umma_commit(uint64_t *bar)
                  : "memory");
 }
 
-__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, int x, int y, int z,
-                                            uint64_t *bar)
+// 16 bytes from global to shared memory, or zeros when src_bytes is 0 (src is then not read).
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t src_bytes)
 {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
-        : "memory");
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+                 "r"(src_bytes)
+                 : "memory");
+}
+
+// Arrive on the barrier once every cp.async this thread issued so far has landed (the arrival
+// is counted in the barrier's initial count).
+__device__ __forceinline__ void cp_async_arrive(uint64_t *bar)
+{
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
 }
 
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float *v)
@@ -346,8 +368,8 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi)
 // ------------------------------------------------------------------ kernel 2: attention
 
 __global__ void __launch_bounds__(kUThreads, 1)
-attn_union_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                  const float *__restrict__ q, int64_t n_q, int H_q, float scale_log2,
+attn_union_kernel(const __nv_bfloat16 *__restrict__ K, const __nv_bfloat16 *__restrict__ V,
+                  int64_t n_kv, int64_t ld_k, int64_t ld_v, const float *__restrict__ q, int64_t n_q, int H_q, float scale_log2,
                   const int32_t *__restrict__ n_cells, int64_t max_cells,
                   const uint32_t *__restrict__ ws, float *__restrict__ out,
                   float *__restrict__ lse, const WaitCtl wc)
@@ -377,7 +399,7 @@ attn_union_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
 
     if (tid == 0) {
         for (int s = 0; s < kUStages; ++s) {
-            mbar_init(&kv_full[s], 1);
+            mbar_init(&kv_full[s], kUCopyThreads);
             mbar_init(&kv_empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -415,19 +437,28 @@ attn_union_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
     const uint32_t *gmem = gw + 4 + cap;
     bool ok = true;
 
-    if (warp == 0) {
-        // ---- producer: lane = 2 * (block in tile) + dim half; K and V boxes of 4 cells
-        const int j = lane >> 1, half = lane & 1;
+    if (warp == 0 || warp == kUThreads / 32 - 1) {
+        // ---- copies: warp p fills rows 32p .. 32p + 31 (blocks 8p .. 8p + 7) of the tile's
+        // K and V; lane = 16 * (row parity) + 16-byte chunk of the 256-byte head row
+        const int p = warp == 0 ? 0 : 1;
+        const int c = lane & 15, sub = lane >> 4;
+        const uint32_t half_off = (uint32_t)(c >> 3) * kTileHalf;
+        const unsigned char *Kc =
+            reinterpret_cast<const unsigned char *>(K) + (int64_t)kvh * kUD * 2 + c * 16;
+        const unsigned char *Vc =
+            reinterpret_cast<const unsigned char *>(V) + (int64_t)kvh * kUD * 2 + c * 16;
+        const int64_t ldk_b = ld_k * 2, ldv_b = ld_v * 2;
         int armed = 0;
-        int32_t blk_next = 0;
-        if (n_tiles > 0) blk_next = (uint32_t)j < ucount ? ublk[j] : ublk[0];
+        // lanes 0-7 hold the block indices of this warp's eight blocks, one tile ahead
+        auto blk_of = [&](int t) -> int32_t {
+            const int64_t u = (int64_t)t * kUTB + 8 * p + (lane & 7);
+            return u < ucount ? ublk[u] : ublk[0];
+        };
+        int32_t blk_next = n_tiles > 0 ? blk_of(0) : 0;
         for (int t = 0; t < n_tiles; ++t, ++armed) {
             const int s = t % kUStages;
             const int32_t blk = blk_next;
-            if (t + 1 < n_tiles) {  // the next tile's block index, one tile ahead
-                const int64_t u = (int64_t)(t + 1) * kUTB + j;
-                blk_next = u < ucount ? ublk[u] : ublk[0];
-            }
+            if (t + 1 < n_tiles) blk_next = blk_of(t + 1);
             // every lane waits; the warp goes on only if all of them saw the stage free
             const bool freed =
                 t < kUStages ||
@@ -436,14 +467,23 @@ attn_union_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
                 ok = false;
                 break;
             }
-            if (lane == 0) mbar_arrive_expect_tx(&kv_full[s], kStageBytes);
-            __syncwarp();
-            unsigned char *st = sKV + s * kStageBytes;
-            const uint32_t off = half * kTileHalf + j * 512;
-            tma_load_3d(st + off, &tmK, half * 64, kvh, 4 * blk, &kv_full[s]);
-            tma_load_3d(st + kTileBytes + off, &tmV, half * 64, kvh, 4 * blk, &kv_full[s]);
+            const uint32_t st = smem_u32(sKV + s * kStageBytes) + half_off;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int rr = 2 * i + sub;                 // row within this warp's 32
+                const int r = 32 * p + rr;                  // row (cell) of the tile
+                const int32_t b = __shfl_sync(0xffffffffu, blk, i >> 1);
+                const int64_t cell = 4 * (int64_t)b + (rr & 3);
+                const bool in = cell < n_kv;
+                const int64_t row = in ? cell : 0;
+                const uint32_t dst = st + (uint32_t)r * 128 + ((uint32_t)((c & 7) ^ (r & 7)) << 4);
+                cp_async16(dst, Kc + row * ldk_b, in ? 16u : 0u);
+                cp_async16(dst + kTileBytes, Vc + row * ldv_b, in ? 16u : 0u);
+            }
+            cp_async_arrive(&kv_full[s]);
         }
-        // every armed stage lands before the CTA may leave
+        asm volatile("cp.async.wait_all;" ::: "memory");
+        // every armed stage has completed its barrier before the CTA may leave
         for (int s = 0; s < kUStages && lane == 0; ++s) {
             const int uses = armed / kUStages + (s < armed % kUStages ? 1 : 0);
             if (uses > 0 && !mbar_wait(&kv_full[s], (uint32_t)(uses - 1) & 1u)) ok = false;
@@ -462,6 +502,9 @@ attn_union_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
                         ok = false;
                         break;
                     }
+                    // the stage was written by ordinary (generic-proxy) copies; the tensor
+                    // cores read it through the async proxy
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                     if (t >= 2 && !mbar_wait(&s_empty[b], (uint32_t)((t >> 1) - 1) & 1u, wc.limit_ns)) {
                         ok = false;
                         break;
@@ -688,40 +731,6 @@ attn_union_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
                      : "memory");
 }
 
-using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_tiled_fn()
-{
-    static EncodeTiledFn fn = nullptr;
-    if (!fn) {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult qr;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                             &qr) == cudaSuccess &&
-            qr == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(p);
-    }
-    return fn;
-}
-
-// 3-D map of a bf16 cache [n_kv rows of ld elements][H_kv heads][128 dims]: boxes of 64 dims
-// x 1 head x 4 cells, 128-byte swizzle, zero fill past the last row.
-bool make_kv_map(CUtensorMap *m, const void *base, int64_t n_kv, int H_kv, int64_t ld)
-{
-    EncodeTiledFn fn = encode_tiled_fn();
-    if (!fn) return false;
-    const cuuint64_t dims[3] = {(cuuint64_t)kUD, (cuuint64_t)H_kv, (cuuint64_t)n_kv};
-    const cuuint64_t strides[2] = {(cuuint64_t)kUD * 2, (cuuint64_t)ld * 2};
-    const cuuint32_t box[3] = {64, 1, 4};
-    const cuuint32_t estr[3] = {1, 1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
-              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 }  // namespace
 
 int64_t attn_union_max_kv() { return (int64_t)kUMaxBlockWords * 32 * 4; }
@@ -755,13 +764,6 @@ qsa_status launch_attn_union(const float *q, int64_t n_q, int H_q, int H_kv, flo
     const int nwords = (nblk + 31) / 32;
     const size_t bsmem = sizeof(uint32_t) * (2 * (size_t)nwords + (size_t)kUG * (cap / 8));
     if (bsmem > 227 * 1024) return QSA_ERR_UNSUPPORTED;
-    CUtensorMap tmK, tmV;
-    if (n_kv > 0 && (!make_kv_map(&tmK, K, n_kv, H_kv, ld_k) || !make_kv_map(&tmV, V, n_kv, H_kv, ld_v)))
-        return QSA_ERR_CUDA;
-    if (n_kv == 0) {  // nothing to attend to: the maps are never read
-        memset(&tmK, 0, sizeof tmK);
-        memset(&tmV, 0, sizeof tmV);
-    }
     uint32_t *ws = static_cast<uint32_t *>(workspace);
     if (ensure_kernel_attrs<union_build_kernel>(bsmem) != cudaSuccess) return QSA_ERR_CUDA;
     cudaError_t e = launch(union_build_kernel, dim3((unsigned)groups), dim3(1024), bsmem, st, 1, pos,
@@ -770,7 +772,8 @@ qsa_status launch_attn_union(const float *q, int64_t n_q, int H_q, int H_kv, flo
     if (ensure_kernel_attrs<attn_union_kernel>(union_smem_bytes()) != cudaSuccess)
         return QSA_ERR_CUDA;
     e = launch(attn_union_kernel, dim3((unsigned)groups, (unsigned)H_kv), dim3(kUThreads),
-               union_smem_bytes(), st, 1, tmK, tmV, q, n_q, H_q, scale * 1.4426950408889634f,
+               union_smem_bytes(), st, 1, static_cast<const __nv_bfloat16 *>(K),
+               static_cast<const __nv_bfloat16 *>(V), n_kv, ld_k, ld_v, q, n_q, H_q, scale * 1.4426950408889634f,
                n_cells, max_cells, (const uint32_t *)ws, out, lse, current_wait_ctl());
     return e == cudaSuccess ? QSA_OK : QSA_ERR_CUDA;
 }
