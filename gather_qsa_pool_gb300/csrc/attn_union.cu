@@ -24,16 +24,16 @@
 // straight into the 128-byte-swizzled layout the tensor cores read) into a ring of six
 // stages; a stage's barrier completes when the copies of both warps have landed.  (One TMA
 // box per block and dim half, 512 bytes each, ran at about 70 cycles a box: the box count,
-// not the bytes, bounded the kernel.)  Warp 1 issues the MMAs -- S = Q K^T (N 64 cells, K 128 dims; A is the
-// query's bf16 high and low halves, pre-scaled by scale * log2 e, held in tensor memory) into
-// one of two tensor-memory buffers, then O += P V (N 128 dims, K 64 cells, V read MN-major;
-// A is P's high and low halves, in one of two tensor-memory buffers) into a third; warps 2-5
-// (one thread per row) read S, mask it with the row's membership bits, keep an online
-// maximum that is moved (and O rescaled in tensor memory) only when it grows by more than
-// 2^8, write P into tensor memory, and at the end divide O by the row sum.  With two S and
-// two P buffers, the softmax of tile t overlaps the MMAs of tiles t - 1 and t + 1.  Every mbarrier wait is bounded: on a timeout the
-// rows of the CTA become NaN, nothing new is issued, what was issued is waited for (bounded)
-// and the tensor memory is returned.
+// not the bytes, bounded the kernel.)  Warp 1 issues the MMAs -- S = Q K^T (N 64 cells, K
+// 128 dims; A is the query's bf16 high and low halves, pre-scaled by scale * log2 e, held in
+// tensor memory) into one of two tensor-memory buffers, and O += P V (N 128 dims, K 64 cells,
+// V read MN-major; A is P's high and low halves, in one of two tensor-memory buffers) into a
+// third, two tiles behind the S it follows.  Warps 2-9 (two threads per row, one per half of
+// the tile's columns) read S, mask it with the row's membership bits, keep an online maximum
+// that is moved (and O rescaled in tensor memory) only when it grows by more than 2^8, write
+// P into tensor memory, and at the end divide O by the row sum.  Every mbarrier wait is
+// bounded: on a timeout the rows of the CTA become NaN, nothing new is issued, what was
+// issued is waited for (bounded) and the tensor memory is returned.
 #include "attn_union.cuh"
 
 namespace qsa {
@@ -365,6 +365,19 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi)
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
+// A bounded mbarrier wait of a whole warp: lane 0 polls, the warp learns the outcome from it
+// and is ordered after the completed phase by the warp barrier.  (Thirty-two lanes polling
+// the same barrier load the shared-memory pipe that the MMA issue and the tensor-memory
+// accesses of the other warps go through.)
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, uint64_t limit_ns)
+{
+    bool ok = true;
+    if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, limit_ns);
+    ok = __shfl_sync(0xffffffffu, (int)ok, 0) != 0;
+    __syncwarp();
+    return ok;
+}
+
 // ------------------------------------------------------------------ kernel 2: attention
 
 __global__ void __launch_bounds__(kUThreads, 1)
@@ -381,8 +394,7 @@ attn_union_kernel(const __nv_bfloat16 *__restrict__ K, const __nv_bfloat16 *__re
     uint64_t *kv_full = reinterpret_cast<uint64_t *>(sKV + kUStages * kStageBytes);
     uint64_t *kv_empty = kv_full + kUStages;
     uint64_t *s_full = kv_empty + kUStages;          // [2] S(t) in its buffer
-    uint64_t *s_empty = s_full + 2;                  // [2] S buffer read by the softmax warps
-    uint64_t *p_full = s_empty + 2;                  // [2] P(t) in its buffer
+    uint64_t *p_full = s_full + 2;                   // [2] P(t) in its buffer (S(t) read)
     uint64_t *o_done = p_full + 2;                   // [2] the P V of a tile using P buffer b done
     uint64_t *q_ready = o_done + 2;
     uint64_t *drain = q_ready + 1;
@@ -404,7 +416,6 @@ attn_union_kernel(const __nv_bfloat16 *__restrict__ K, const __nv_bfloat16 *__re
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&s_full[b], 1);
-            mbar_init(&s_empty[b], kUEpiWarps);
             mbar_init(&p_full[b], kUEpiWarps);
             mbar_init(&o_done[b], 1);
         }
@@ -459,11 +470,8 @@ attn_union_kernel(const __nv_bfloat16 *__restrict__ K, const __nv_bfloat16 *__re
             const int s = t % kUStages;
             const int32_t blk = blk_next;
             if (t + 1 < n_tiles) blk_next = blk_of(t + 1);
-            // every lane waits; the warp goes on only if all of them saw the stage free
-            const bool freed =
-                t < kUStages ||
-                mbar_wait(&kv_empty[s], (uint32_t)((t / kUStages) - 1) & 1u, wc.limit_ns);
-            if (!__all_sync(0xffffffffu, freed)) {
+            if (t >= kUStages &&
+                !warp_wait(&kv_empty[s], (uint32_t)((t / kUStages) - 1) & 1u, wc.limit_ns)) {
                 ok = false;
                 break;
             }
@@ -489,58 +497,67 @@ attn_union_kernel(const __nv_bfloat16 *__restrict__ K, const __nv_bfloat16 *__re
             if (uses > 0 && !mbar_wait(&kv_full[s], (uint32_t)(uses - 1) & 1u)) ok = false;
         }
     } else if (warp == 1) {
-        // ---- MMA issuer (one thread): S(t) = Q K(t)^T, then O += P(t-1) V(t-1)
+        // ---- MMA issuer (one thread): per tile t one burst, S(t) = Q K(t)^T and then
+        // O += P(t-2) V(t-2), after two waits: K / V(t) landed, and P(t-2) written (so the
+        // softmax warps also read S(t-2), whose buffer S(t) takes).  P V runs two tiles behind
+        // so that S(t + 1) is issued while the softmax of t - 1 still runs.  Each wait or commit
+        // costs this thread over a hundred cycles with the tensor queue draining meanwhile, so a
+        // tile has two waits and three commits.  The issuing thread shares its sub-partition
+        // with two softmax warps, so each MMA costs it one 32-bit add: the descriptors of stage
+        // 0 are built once, and a stage, dim half or k step moves only the start-address field
+        // (bits 0-13, 16-byte units; shared addresses stay below 256 KB, so the add never
+        // carries out of it).
         if (lane == 0) {
             constexpr uint32_t id_s = idesc_m128(kUTC, false);
             constexpr uint32_t id_o = idesc_m128(kUD, true);
+            const uint64_t dk0 = desc_kmajor_sw128(smem_u32(sKV));
+            const uint64_t dv0 = desc_mnmajor_sw128(smem_u32(sKV + kTileBytes), kTileHalf);
+            const uint32_t dk_lo = (uint32_t)dk0, dk_hi = (uint32_t)(dk0 >> 32);
+            const uint32_t dv_lo = (uint32_t)dv0, dv_hi = (uint32_t)(dv0 >> 32);
             if (n_tiles > 0 && !mbar_wait(q_ready, 0, wc.limit_ns)) ok = false;
-            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-            for (int t = 0; ok && t <= n_tiles; ++t) {
+            for (int t = 0; ok && t < n_tiles + 2; ++t) {
+                const int tp = t - 2;
                 if (t < n_tiles) {
-                    const int s = t % kUStages, b = t & 1;
-                    if (!mbar_wait(&kv_full[s], (uint32_t)(t / kUStages) & 1u, wc.limit_ns)) {
+                    if (!mbar_wait(&kv_full[t % kUStages], (uint32_t)(t / kUStages) & 1u, wc.limit_ns)) {
                         ok = false;
                         break;
                     }
                     // the stage was written by ordinary (generic-proxy) copies; the tensor
                     // cores read it through the async proxy
                     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                    if (t >= 2 && !mbar_wait(&s_empty[b], (uint32_t)((t >> 1) - 1) & 1u, wc.limit_ns)) {
-                        ok = false;
-                        break;
-                    }
-                    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                    const uint32_t kb = smem_u32(sKV + s * kStageBytes);
-                    uint32_t acc = 0;
+                }
+                if (tp >= 0 && !mbar_wait(&p_full[tp & 1], (uint32_t)(tp >> 1) & 1u, wc.limit_ns)) {
+                    ok = false;
+                    break;
+                }
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                if (t < n_tiles) {
+                    const int s = t % kUStages, b = t & 1;
+                    const uint32_t ks = dk_lo + (uint32_t)s * (kStageBytes >> 4);
+                    const uint32_t d_s = tmem + kColS + (uint32_t)(b * kUTC);
 #pragma unroll
                     for (int part = 0; part < 2; ++part) {
-                        const uint32_t qa = tmem + (part ? kColQl : kColQh);
 #pragma unroll
                         for (int k16 = 0; k16 < kUD / 16; ++k16) {
-                            const uint32_t hf = (uint32_t)(k16 >> 2), ko = (uint32_t)(k16 & 3) * 32;
-                            umma_m128_ta(tmem + kColS + (uint32_t)(b * kUTC), qa + (uint32_t)k16 * 8,
-                                         desc_kmajor_sw128(kb + hf * kTileHalf + ko), id_s, acc);
-                            acc = 1;
+                            const uint32_t off = ((uint32_t)(k16 >> 2) * kTileHalf + (uint32_t)(k16 & 3) * 32) >> 4;
+                            umma_m128_ta(d_s, tmem + (part ? kColQl : kColQh) + (uint32_t)k16 * 8,
+                                         ((uint64_t)dk_hi << 32) | (ks + off), id_s,
+                                         (part | k16) ? 1u : 0u);
                         }
                     }
                     umma_commit(&s_full[b]);
                 }
-                if (t >= 1) {
-                    const int tp = t - 1, sp = tp % kUStages, pb = tp & 1;
-                    if (!mbar_wait(&p_full[pb], (uint32_t)(tp >> 1) & 1u, wc.limit_ns)) {
-                        ok = false;
-                        break;
-                    }
-                    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                    const uint32_t vb = smem_u32(sKV + sp * kStageBytes + kTileBytes);
+                if (tp >= 0) {
+                    const int sp = tp % kUStages, pb = tp & 1;
+                    const uint32_t vs = dv_lo + (uint32_t)sp * (kStageBytes >> 4);
                     const uint32_t pcol = tmem + kColP + (uint32_t)pb * 64;
 #pragma unroll
                     for (int part = 0; part < 2; ++part) {
 #pragma unroll
                         for (int k16 = 0; k16 < kUTC / 16; ++k16)
                             umma_m128_ta(tmem + kColO, pcol + (uint32_t)(part * 32 + k16 * 8),
-                                         desc_mnmajor_sw128(vb + k16 * 2048, kTileHalf), id_o,
-                                         (tp > 0 || part > 0 || k16 > 0) ? 1u : 0u);
+                                         ((uint64_t)dv_hi << 32) | (vs + (uint32_t)k16 * (2048 >> 4)),
+                                         id_o, (tp | part | k16) ? 1u : 0u);
                     }
                     umma_commit(&o_done[pb]);
                     umma_commit(&kv_empty[sp]);
@@ -599,8 +616,7 @@ attn_union_kernel(const __nv_bfloat16 *__restrict__ K, const __nv_bfloat16 *__re
             const uint32_t w = (live && !trunc) ? mw : 0u;
             if (t + 1 < n_tiles) mw = gmem[((int64_t)(t + 1) * kUG + li) * 2 + ch];  // ahead
             // waits are warp-uniform: the tensor-memory accesses below need the whole warp
-            bool good = ok && __all_sync(0xffffffffu,
-                                         mbar_wait(&s_full[b], (uint32_t)(t >> 1) & 1u, wc.limit_ns));
+            bool good = ok && warp_wait(&s_full[b], (uint32_t)(t >> 1) & 1u, wc.limit_ns);
             float x[32];
             float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
             if (good) {
@@ -608,7 +624,6 @@ attn_union_kernel(const __nv_bfloat16 *__restrict__ K, const __nv_bfloat16 *__re
                 tmem_ld32(tmem + lrow + kColS + (uint32_t)(b * kUTC + ch * 32), x);
                 asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&s_empty[b]);
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
                     x[e] = ((w >> e) & 1u) ? x[e] : -INFINITY;
@@ -651,12 +666,10 @@ attn_union_kernel(const __nv_bfloat16 *__restrict__ K, const __nv_bfloat16 *__re
             l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
             // P buffer b was last read by P V(t - 2); O is touched only when rescaling, after
             // P V(t - 1)
-            const bool w2 = t < 2 || __all_sync(0xffffffffu, mbar_wait(&o_done[b],
-                                                                       (uint32_t)((t - 2) >> 1) & 1u,
-                                                                       wc.limit_ns));
+            const bool w2 = t < 2 || warp_wait(&o_done[b], (uint32_t)((t - 2) >> 1) & 1u,
+                                               wc.limit_ns);
             const bool w3 = !(rescale && t >= 1) ||
-                            __all_sync(0xffffffffu,
-                                       mbar_wait(&o_done[b ^ 1], (uint32_t)((t - 1) >> 1) & 1u, wc.limit_ns));
+                            warp_wait(&o_done[b ^ 1], (uint32_t)((t - 1) >> 1) & 1u, wc.limit_ns);
             if (!(w2 && w3)) {
                 ok = false;  // stops at the next pair barrier (or the one after the loop)
                 continue;
@@ -684,8 +697,7 @@ attn_union_kernel(const __nv_bfloat16 *__restrict__ K, const __nv_bfloat16 *__re
             if (lane == 0) mbar_arrive(&p_full[b]);
         }
         if (ok && n_tiles > 0 &&
-            !__all_sync(0xffffffffu, mbar_wait(&o_done[(n_tiles - 1) & 1],
-                                               (uint32_t)((n_tiles - 1) >> 1) & 1u, wc.limit_ns)))
+            !warp_wait(&o_done[(n_tiles - 1) & 1], (uint32_t)((n_tiles - 1) >> 1) & 1u, wc.limit_ns))
             ok = false;
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         // the row sum over both halves, and whether both warps of the pair finished (every
