@@ -544,9 +544,11 @@ def step_kernel_us(captures, keep, block_x, reps, dev):
 
 def run_prefill(args, local, pooled_kind="f32"):
     """The prefill chunk: 1024 queries after 255,181 tokens.  Times (CUDA-graph replays after a
-    warm-up) the tensor-core score contraction, the per-query top-k, the cell lists and the
-    gathered attention, one at a time and as one chained chunk; returns per-kernel
-    microseconds, the chunk's and the score kernel's TFLOP/s.
+    warm-up) the tensor-core score contraction (which also writes each query's maxima of 32-row
+    groups), the per-query top-k fed by those maxima, the cell lists and the gathered
+    attention, one at a time and as one chained chunk; returns per-kernel microseconds, the
+    chunk's and the score kernel's TFLOP/s, and (outside the chunk) the top-k that scans whole
+    rows on the same scores.
     pooled_kind "bf16": the pooled cache is stored in bf16 and the contraction reads it in
     place (no conversion pass).  "f32_mirror": an fp32 cache kept together with a bf16 mirror
     (every pool update also writes the mirror's rows: bit for bit the cache's bf16 rounding),
@@ -574,6 +576,8 @@ def run_prefill(args, local, pooled_kind="f32"):
                         shape.rope_base, mirror, 0)
         score_src, score_dt = mirror, qsa.QSA_BF16
     scores = torch.empty(n_q, n_rows, device=dev)
+    maxima = torch.empty(n_q, (n_rows + 31) // 32, device=dev)
+    tws = torch.empty(qsa.topk_blocks_maxima_workspace_size(n_q), dtype=torch.uint8, device=dev)
     ws = torch.zeros(qsa.index_score_workspace_size(
         n_q, n_rows, H, d, qsa.QSA_PREC_BF16_TC, score_dt), dtype=torch.uint8, device=dev)
     blocks = torch.empty(n_q, shape.k_blk, dtype=torch.int32, device=dev)
@@ -592,21 +596,26 @@ def run_prefill(args, local, pooled_kind="f32"):
                                               shape.eps, shape.rope_base, mirror,
                                               shape.depth // 4)))
     calls += [
-        ("score_tc", lambda: qsa.index_score(inp["q_idx"], score_src, n_rows, H, d, scale_idx,
-                                              scores, q_pos=inp["q_pos"],
-                                              precision=qsa.QSA_PREC_BF16_TC, workspace=ws)),
-        ("topk", lambda: qsa.topk_blocks(scores, n_rows, shape.k_blk, blocks, counts,
-                                         q_pos=inp["q_pos"])),
+        ("score_tc", lambda: qsa.index_score_maxima(inp["q_idx"], score_src, n_rows, H, d,
+                                                     scale_idx, scores, maxima,
+                                                     q_pos=inp["q_pos"], workspace=ws)),
+        ("topk", lambda: qsa.topk_blocks_maxima(scores, maxima, n_rows, shape.k_blk, blocks,
+                                                counts, tws, q_pos=inp["q_pos"])),
         ("cells", lambda: qsa.gather_kv(blocks, counts, shape.k_blk, pos, n_cells, shape.max_cells,
                                         q_pos=inp["q_pos"], n_kv=shape.n_ctx)),
         ("attn", lambda: qsa.sparse_attn(inp["q"], inp["K"], inp["V"], n_cells, shape.max_cells,
                                          out, shape.H_kv, shape.d, shape.d, scale, pos=pos,
                                          workspace=aws)),
     ]
+    w_blocks, w_counts = torch.empty_like(blocks), torch.empty_like(counts)
+    whole_rows = ("topk_whole_rows", lambda: qsa.topk_blocks(scores, n_rows, shape.k_blk, w_blocks,
+                                                             w_counts, q_pos=inp["q_pos"]))
     for _ in range(2):
         for _, fn in calls:
             fn()
+    whole_rows[1]()
     torch.cuda.synchronize()
+    same_selection = bool(torch.equal(blocks, w_blocks) and torch.equal(counts, w_counts))
     # each kernel's calls captured into a CUDA graph and replayed (device time), then the
     # whole chunk as one graph; plain CUDA events around direct calls if capture fails
     res, timing, chunk_graph = {}, "cuda graph replay", None
@@ -614,6 +623,7 @@ def run_prefill(args, local, pooled_kind="f32"):
         for name, fn in calls:
             res[name] = graph_time_us([fn], args.prefill_reps, dev)
         chunk_graph = graph_time_us([fn for _, fn in calls], args.prefill_reps, dev)
+        whole_us = graph_time_us([whole_rows[1]], args.prefill_reps, dev)
     except Exception as e:  # noqa: BLE001 -- reported in the JSON line
         timing = f"cuda events around direct calls (graph capture failed: {type(e).__name__})"
         torch.cuda.synchronize()
@@ -625,6 +635,7 @@ def run_prefill(args, local, pooled_kind="f32"):
             b.record()
             torch.cuda.synchronize()
             res[name] = a.elapsed_time(b) * 1e3 / args.prefill_reps
+        whole_us = None
     flops = 2.0 * n_q * n_rows * H * d
     attn_flops = 2.0 * 2.0 * n_q * shape.H_q * shape.d * float(n_cells.float().mean().item())
     out_d = {
@@ -635,12 +646,14 @@ def run_prefill(args, local, pooled_kind="f32"):
         "us": {k: round(v, 1) for k, v in res.items()},
         "chunk_us": round(sum(res.values()), 1),
         "chunk_graph_us": None if chunk_graph is None else round(chunk_graph, 1),
+        "topk_whole_rows_us": None if whole_us is None else round(whole_us, 1),
+        "topk_same_selection": same_selection,
         "timing": timing,
         "score_tc_tflops": flops / (res["score_tc"] * 1e-6) / 1e12,
         "attn_tflops": attn_flops / (res["attn"] * 1e-6) / 1e12,
         "tokens_per_s": n_q / ((chunk_graph or sum(res.values())) * 1e-6),
     }
-    del inp, pooled, mirror, score_src, scores, ws, pos, out, aws
+    del inp, pooled, mirror, score_src, scores, maxima, ws, pos, out, aws
     torch.cuda.empty_cache()
     return out_d
 

@@ -19,6 +19,7 @@ from ._binding import (  # noqa: F401
     gather_kv,
     header_functions,
     index_score,
+    index_score_maxima,
     index_score_workspace_size,
     load,
     mask_sparse_attn,
@@ -32,6 +33,8 @@ from ._binding import (  # noqa: F401
     sparse_attn_workspace_size,
     status_str,
     topk_blocks,
+    topk_blocks_maxima,
+    topk_blocks_maxima_workspace_size,
     topk_max_candidates,
 )
 from .decode import DecodeLayer  # noqa: F401

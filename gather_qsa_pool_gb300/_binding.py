@@ -39,6 +39,11 @@ _SIGNATURES = {
     "qsa_index_score_workspace_size": (_sz, [_i64, _i64, _int, _int, _int, _int]),
     "qsa_topk_blocks": (_int, [_p, _i64, _i64, _p, _i64, _i64, _p, _p, _p]),
     "qsa_topk_max_candidates": (_i64, []),
+    "qsa_index_score_maxima": (_int, [_p, _i64, _i64, _p, _p, _int, _i64, _int, _int, _f, _p,
+                                      _i64, _p, _i64, _p, _sz, _p]),
+    "qsa_topk_blocks_maxima": (_int, [_p, _i64, _i64, _p, _i64, _i64, _p, _i64, _p, _p, _p,
+                                      _sz, _p]),
+    "qsa_topk_blocks_maxima_workspace_size": (_sz, [_i64]),
     "qsa_expand_block_scores": (_int, [_p, _i64, _i64, _i64, _p, _i64, _p]),
     "qsa_gather_kv": (_int, [_p, _p, _int, _i64, _int, _int, _int, _i64, _i64, _p, _p, _i64,
                              _i64, _p, _i64, _p, _p, _p, _p, _i64, _p]),
@@ -192,6 +197,37 @@ def topk_blocks(scores, n_full, k_blk, blocks_out, counts_out, q_pos=None, strea
     _check("qsa_topk_blocks", load().qsa_topk_blocks(
         _ptr(scores), n_q, ld, _ptr(q_pos), n_full, k_blk, _ptr(blocks_out), _ptr(counts_out),
         _stream(stream)))
+
+
+def index_score_maxima(q, pooled, n_rows, H, d, scale, scores, maxima, q_pos=None,
+                       workspace=None, stream=None):
+    """qsa_index_score_maxima: the tensor-core scores plus maxima[i][g], the largest score of
+    rows 32g .. 32g+31 of query i (maxima: [n_q][>= ceil(n_rows / 32)] fp32)."""
+    n_q = q.shape[0] if q.dim() > 1 else 1
+    ld_q = _ld(q) if q.dim() > 1 else H * d
+    ld_s = _ld(scores) if scores.dim() > 1 else n_rows
+    ld_m = _ld(maxima) if maxima.dim() > 1 else maxima.numel()
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("qsa_index_score_maxima", load().qsa_index_score_maxima(
+        _ptr(q), n_q, ld_q, _ptr(q_pos), _ptr(pooled), _dtype(pooled), n_rows, H, d, scale,
+        _ptr(scores), ld_s, _ptr(maxima), ld_m, _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def topk_blocks_maxima_workspace_size(n_q) -> int:
+    return int(load().qsa_topk_blocks_maxima_workspace_size(n_q))
+
+
+def topk_blocks_maxima(scores, maxima, n_full, k_blk, blocks_out, counts_out, workspace,
+                       q_pos=None, stream=None):
+    """qsa_topk_blocks_maxima: qsa_topk_blocks fed with the score kernel's group maxima
+    (workspace: topk_blocks_maxima_workspace_size(n_q) bytes of device memory)."""
+    n_q = scores.shape[0] if scores.dim() > 1 else 1
+    ld = _ld(scores)
+    ld_m = _ld(maxima) if maxima.dim() > 1 else maxima.numel()
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check("qsa_topk_blocks_maxima", load().qsa_topk_blocks_maxima(
+        _ptr(scores), n_q, ld, _ptr(q_pos), n_full, k_blk, _ptr(maxima), ld_m,
+        _ptr(blocks_out), _ptr(counts_out), _ptr(workspace), ws_bytes, _stream(stream)))
 
 
 def expand_block_scores(scores, n_full, cell_scores, stream=None):

@@ -8,6 +8,7 @@
 #include <atomic>
 
 #include "attn_union.cuh"
+#include "prefill_select.cuh"
 #include "qsa_internal.cuh"
 
 namespace qsa {
@@ -192,6 +193,45 @@ qsa_status qsa_topk_blocks(const float *scores, int64_t n_q, int64_t ld_scores,
     return from_cuda(launch_topk(scores, n_q, ld_scores, q_pos, n_full, k_blk, blocks_out,
                                  counts_out, 0, nullptr, nullptr, 0, nullptr, (cudaStream_t)stream));
 }
+
+qsa_status qsa_index_score_maxima(const float *q, int64_t n_q, int64_t ld_q,
+                                  const int32_t *q_pos, const void *pooled,
+                                  qsa_dtype pooled_dtype, int64_t n_rows, int H, int d,
+                                  float scale, float *scores, int64_t ld_scores, float *maxima,
+                                  int64_t ld_maxima, void *workspace, size_t workspace_bytes,
+                                  qsa_stream_t stream)
+{
+    const qsa_status v = check_index_score(q, n_q, ld_q, pooled, pooled_dtype, n_rows, H, d,
+                                           scores, ld_scores);
+    if (v != QSA_OK) return v;
+    if (!maxima || !aligned(maxima, 4) || ld_maxima < (n_rows + 31) / 32)
+        return QSA_ERR_INVALID_ARG;
+    const size_t need =
+        qsa_index_score_workspace_size(n_q, n_rows, H, d, pooled_dtype, QSA_PREC_BF16_TC);
+    if (workspace_bytes < need || (need > 0 && !workspace)) return QSA_ERR_INVALID_ARG;
+    return launch_index_score_tc_maxima(q, n_q, ld_q, q_pos, pooled, pooled_dtype, n_rows, H, d,
+                                        scale, scores, ld_scores, maxima, ld_maxima, workspace,
+                                        workspace_bytes, (cudaStream_t)stream);
+}
+
+qsa_status qsa_topk_blocks_maxima(const float *scores, int64_t n_q, int64_t ld_scores,
+                                  const int32_t *q_pos, int64_t n_full, int64_t k_blk,
+                                  const float *maxima, int64_t ld_maxima, int32_t *blocks_out,
+                                  int32_t *counts_out, void *workspace, size_t workspace_bytes,
+                                  qsa_stream_t stream)
+{
+    const qsa_status v = check_topk(scores, n_q, ld_scores, n_full, k_blk, blocks_out, counts_out);
+    if (v != QSA_OK) return v;
+    if (!maxima || !aligned(maxima, 4) || ld_maxima < n_full / 32) return QSA_ERR_INVALID_ARG;
+    const size_t need = topk_maxima_workspace_bytes(n_q);
+    if (workspace_bytes < need || (need > 0 && (!workspace || !aligned(workspace, 256))))
+        return QSA_ERR_INVALID_ARG;
+    return from_cuda(launch_topk_maxima(scores, n_q, ld_scores, q_pos, n_full, k_blk, maxima,
+                                        ld_maxima, blocks_out, counts_out, workspace,
+                                        (cudaStream_t)stream));
+}
+
+size_t qsa_topk_blocks_maxima_workspace_size(int64_t n_q) { return topk_maxima_workspace_bytes(n_q); }
 
 qsa_status qsa_expand_block_scores(const float *scores, int64_t n_q, int64_t ld_scores,
                                    int64_t n_full, float *cell_scores, int64_t ld_cells,

@@ -30,7 +30,7 @@
 //     for what either CTA of the pair already issued, and always returns its tensor memory.
 #include <cuda.h>
 
-#include "qsa_internal.cuh"
+#include "prefill_select.cuh"
 
 namespace qsa {
 namespace {
@@ -188,7 +188,8 @@ rows_to_bf16_kernel(const float4 *__restrict__ src, int64_t n4, uint2 *__restric
 __global__ void __launch_bounds__(kTcThreads, 1)
 score_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 int64_t n_q, const int32_t *__restrict__ q_pos, int64_t n_rows, int K,
-                float scale, float *__restrict__ scores, int64_t ld_scores, const WaitCtl wc)
+                float scale, float *__restrict__ scores, int64_t ld_scores,
+                float *__restrict__ gmax, int64_t ld_gmax, const WaitCtl wc)
 {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     // 1024-byte aligned operand area (the swizzle is a function of address bits 4-9); the
@@ -324,6 +325,13 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             const int64_t m0 = (u % n_mb) * (2 * kBM) + rank * kBM, n0 = (u / n_mb) * kBN;
             const int64_t qi = m0 + quarter * 32 + lane;
             const int64_t p = (qi < n_q && q_pos) ? (int64_t)q_pos[qi] : INT64_MAX;
+            // blocks complete at position p: b with 4b + 3 <= p
+            const int64_t vis_rows = p >= 3 ? (p - 3) / 4 + 1 : 0;
+            // the tile's eight group maxima of this query, shifted in one per chunk (index cc
+            // ends in m8[cc]), stored together after the chunks: two 16-byte stores a tile
+            float m8[kBN / 32];
+#pragma unroll
+            for (int e = 0; e < kBN / 32; ++e) m8[e] = -INFINITY;
 #pragma unroll 1
             for (int cc = 0; cc < kBN / 32; ++cc) {
                 uint32_t v[32];
@@ -344,10 +352,26 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 if (qi < n_q) {
                     float *dst = scores + qi * ld_scores + n0 + cc * 32;
                     const int64_t b0 = n0 + cc * 32;
+                    // rows b0 + e, e < lim, exist and are visible (4b + 3 <= p); the others
+                    // are -inf (those past n_rows are not stored)
+                    const int64_t lim64 = (vis_rows < n_rows ? vis_rows : n_rows) - b0;
+                    const int lim = lim64 < 0 ? 0 : (lim64 > 32 ? 32 : (int)lim64);
                     float o[32];
 #pragma unroll
                     for (int e = 0; e < 32; ++e)
-                        o[e] = 4 * (b0 + e) + 3 <= p ? __uint_as_float(v[e]) * scale : -INFINITY;
+                        o[e] = e < lim ? __uint_as_float(v[e]) * scale : -INFINITY;
+                    if (gmax) {  // the group's largest visible score
+                        float m16[16];
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) m16[e] = fmaxf(o[e], o[e + 16]);
+#pragma unroll
+                        for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+                            for (int e = 0; e < w; ++e) m16[e] = fmaxf(m16[e], m16[e + w]);
+#pragma unroll
+                        for (int e = 0; e + 1 < kBN / 32; ++e) m8[e] = m8[e + 1];
+                        m8[kBN / 32 - 1] = m16[0];
+                    }
                     if (b0 + 32 <= n_rows && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
 #pragma unroll
                         for (int e = 0; e < 32; e += 4)
@@ -358,6 +382,18 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                         for (int e = 0; e < 32; ++e)
                             if (b0 + e < n_rows) dst[e] = o[e];
                     }
+                }
+            }
+            if (gmax && qi < n_q) {  // groups n0 / 32 .. + 7 of this query (those that exist)
+                float *gd = gmax + qi * ld_gmax + (n0 >> 5);
+                const int64_t n_g = (n_rows + 31) / 32 - (n0 >> 5);
+                if (n_g >= kBN / 32 && (reinterpret_cast<uintptr_t>(gd) & 15) == 0) {
+                    *reinterpret_cast<float4 *>(gd) = make_float4(m8[0], m8[1], m8[2], m8[3]);
+                    *reinterpret_cast<float4 *>(gd + 4) = make_float4(m8[4], m8[5], m8[6], m8[7]);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < kBN / 32; ++e)
+                        if (e < n_g) gd[e] = m8[e];
                 }
             }
             asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -448,11 +484,10 @@ size_t index_score_tc_workspace(int64_t n_q, int64_t n_rows, int H, int d, qsa_d
     return al256((size_t)n_q * K * 2) + rows;
 }
 
-qsa_status launch_index_score_tc(const float *q, int64_t n_q, int64_t ld_q,
-                                 const int32_t *q_pos, const void *pooled, qsa_dtype pdt,
-                                 int64_t n_rows, int H, int d, float scale, float *scores,
-                                 int64_t ld_scores, void *workspace, size_t ws_bytes,
-                                 cudaStream_t st)
+static qsa_status score_tc(const float *q, int64_t n_q, int64_t ld_q, const int32_t *q_pos,
+                           const void *pooled, qsa_dtype pdt, int64_t n_rows, int H, int d,
+                           float scale, float *scores, int64_t ld_scores, float *gmax,
+                           int64_t ld_gmax, void *workspace, size_t ws_bytes, cudaStream_t st)
 {
     const int K = H * d;
     if (K % kBK != 0) return QSA_ERR_UNSUPPORTED;
@@ -504,8 +539,30 @@ qsa_status launch_index_score_tc(const float *q, int64_t n_q, int64_t ld_q,
     if (pairs > n_units) pairs = n_units;
     if (pairs < 1) pairs = 1;
     e = launch(score_tc_kernel, dim3((unsigned)(2 * pairs)), dim3(kTcThreads), tc_smem_bytes(), st,
-               2, tmA, tmB, n_q, q_pos, n_rows, K, scale, scores, ld_scores, current_wait_ctl());
+               2, tmA, tmB, n_q, q_pos, n_rows, K, scale, scores, ld_scores, gmax, ld_gmax,
+               current_wait_ctl());
     return e == cudaSuccess ? QSA_OK : QSA_ERR_CUDA;
+}
+
+qsa_status launch_index_score_tc(const float *q, int64_t n_q, int64_t ld_q,
+                                 const int32_t *q_pos, const void *pooled, qsa_dtype pdt,
+                                 int64_t n_rows, int H, int d, float scale, float *scores,
+                                 int64_t ld_scores, void *workspace, size_t ws_bytes,
+                                 cudaStream_t st)
+{
+    return score_tc(q, n_q, ld_q, q_pos, pooled, pdt, n_rows, H, d, scale, scores, ld_scores,
+                    nullptr, 0, workspace, ws_bytes, st);
+}
+
+qsa_status launch_index_score_tc_maxima(const float *q, int64_t n_q, int64_t ld_q,
+                                        const int32_t *q_pos, const void *pooled,
+                                        qsa_dtype pdt, int64_t n_rows, int H, int d, float scale,
+                                        float *scores, int64_t ld_scores, float *maxima,
+                                        int64_t ld_maxima, void *workspace, size_t ws_bytes,
+                                        cudaStream_t st)
+{
+    return score_tc(q, n_q, ld_q, q_pos, pooled, pdt, n_rows, H, d, scale, scores, ld_scores,
+                    maxima, ld_maxima, workspace, ws_bytes, st);
 }
 
 }  // namespace qsa

@@ -35,6 +35,7 @@
 // the block count (a workspace never cleared), or a bucket holding more than 1024
 // candidates, sends the last CTA through the general form instead.
 #include "qsa_internal.cuh"
+#include "prefill_select.cuh"
 
 namespace qsa {
 namespace {
@@ -461,67 +462,16 @@ __device__ void topk_query(const float *srow, int64_t n, int64_t k, int32_t *out
     write_selection(selw, eqw, nw, k_rem, k, out, pout, pvec, warp_s);
 }
 
-// The general form for one query when n is large and no histogram comes with the scores:
-// a strided sample (1024 positions over the row's capacity n_cap, the ones below n kept)
-// sets a threshold T at the 12-bit digit that holds the sample's r-th largest key (r a
-// margin above the k/n share); one pass keeps every key >= T
-// as a candidate (the top k are among them whenever at least k are); the candidates are
-// then selected exactly: first 12-bit digit, second 8-bit digit, and a (key, index) rank
-// inside the last bin.  Returns false (nothing written) when the sample missed -- fewer
-// than k or more than cand_cap candidates -- and the caller runs topk_query instead.
-// smem: the layout of topk_query.
-__device__ bool topk_query_sampled(const float *srow, int64_t n, int64_t k, int32_t *out,
-                                   int32_t *pout, bool pvec, int cand_cap, uint32_t *smem,
-                                   float sample, int64_t n_cap)
+// Steps 3-6 of the candidate forms: the exact top k of the m candidates (cand_key / cand_idx;
+// hist holds their first-digit histogram): first 12-bit digit, second 8-bit digit, a (key,
+// index) rank inside the last bin, then the ordered output.  Returns false (nothing written)
+// when the last bin holds more than kBins1 candidates.  All threads of the CTA call it.
+__device__ bool select_candidates(int64_t k, uint32_t m, uint32_t *hist, uint32_t *warp_s,
+                                  uint32_t *misc, uint32_t *selw, int64_t nw,
+                                  const uint32_t *cand_key, const int32_t *cand_idx,
+                                  int32_t *out, int32_t *pout, bool pvec)
 {
-    uint32_t *hist = smem;
-    uint32_t *warp_s = hist + kBins1;
-    uint32_t *misc = warp_s + 2 * (NT / 32);
-    uint32_t *selw = misc + 32;
-    const int64_t nw = (n + 31) / 32;
-    uint32_t *cand_key = selw + 2 * nw;
-    int32_t *cand_idx = reinterpret_cast<int32_t *>(cand_key + cand_cap);
-    const int tid = threadIdx.x, lane = tid & 31;
-
-    // ---- 1. the sample's histogram and the threshold digit.  sample: this thread's score at
-    // (tid * n_cap) >> 10, loaded by the caller before the query's block count n was known;
-    // the ns samples below n stand for the row (ns >= 1: thread 0 samples block 0).
-    for (int i = tid; i < kBins1; i += NT) hist[i] = 0u;
-    for (int64_t w = tid; w < nw; w += NT) selw[w] = 0u;
-    if (tid == 0) misc[8] = 0u;
-    __syncthreads();
-    const bool in_row = (((int64_t)tid * n_cap) >> 10) < n;
-    if (in_row) atomicAdd(&hist[score_key(sample) >> (32 - kTopkHistBits)], 1u);
-    const int64_t ns = __syncthreads_count(in_row);
-    int64_t r = (k * ns + n - 1) / n + 8;
-    if (r > ns) r = ns;
-    find_bucket(hist, kBins1, (uint32_t)r, warp_s, misc);
-    const uint32_t T = misc[0] << (32 - kTopkHistBits);
-    for (int i = tid; i < kBins1; i += NT) hist[i] = 0u;  // find_bucket has read it
-    __syncthreads();
-
-    // ---- 2. one pass: every key >= T is a candidate, and the candidates' first-digit
-    // histogram
-    auto keep = [&](uint32_t key, int64_t i) {
-        if (key >= T) {
-            atomicAdd(&hist[key >> (32 - kTopkHistBits)], 1u);
-            const uint32_t slot = atomicAdd(&misc[8], 1u);
-            if (slot < (uint32_t)cand_cap) {
-                cand_key[slot] = key;
-                cand_idx[slot] = (int32_t)i;
-            }
-        }
-    };
-    if (T > kKeyNegInf && (reinterpret_cast<uintptr_t>(srow) & 15) == 0)
-        collect_at_least(srow, n, T, &misc[8], cand_key, cand_idx, (uint32_t)cand_cap, hist);
-    else if (T > kKeyNegInf)
-        for_each_key_at_least(srow, n, T, keep);
-    else
-        for_each_key(srow, n, keep);
-    __syncthreads();
-    const uint32_t m = misc[8];
-    if (m < (uint32_t)k || m > (uint32_t)cand_cap) return false;  // uniform
-
+    const int tid = threadIdx.x;
     // ---- 3. first digit over the candidates (their histogram came with the pass)
     find_bucket(hist, kBins1, (uint32_t)k, warp_s, misc);
     const uint32_t B1 = misc[0];
@@ -591,26 +541,85 @@ __device__ bool topk_query_sampled(const float *srow, int64_t n, int64_t k, int3
             __syncthreads();
         }
     }
-    (void)lane;
     // ---- 6. ordered output
     write_selection(selw, nullptr, nw, 0u, k, out, pout, pvec, warp_s);
     return true;
 }
 
-__global__ void __launch_bounds__(NT)
-topk_kernel(const float *__restrict__ scores, int64_t ld, const int32_t *__restrict__ q_pos,
-            int64_t n_full_cap, int k_blk, int32_t *__restrict__ blocks_out,
-            int32_t *__restrict__ counts_out, int64_t n_ctx, int32_t *__restrict__ pos_out,
-            int32_t *__restrict__ n_cells_out, int64_t max_cells, uint32_t *__restrict__ ext_hist,
-            int cand_cap, int64_t p_step)
+// The general form for one query when n is large and no histogram comes with the scores:
+// a strided sample (1024 positions over the row's capacity n_cap, the ones below n kept)
+// sets a threshold T at the 12-bit digit that holds the sample's r-th largest key (r a
+// margin above the k/n share); one pass keeps every key >= T
+// as a candidate (the top k are among them whenever at least k are); the candidates are
+// then selected exactly: first 12-bit digit, second 8-bit digit, and a (key, index) rank
+// inside the last bin.  Returns false (nothing written) when the sample missed -- fewer
+// than k or more than cand_cap candidates -- and the caller runs topk_query instead.
+// smem: the layout of topk_query.
+__device__ bool topk_query_sampled(const float *srow, int64_t n, int64_t k, int32_t *out,
+                                   int32_t *pout, bool pvec, int cand_cap, uint32_t *smem,
+                                   float sample, int64_t n_cap)
 {
-    extern __shared__ __align__(16) uint32_t smem[];
-    const int64_t qi = blockIdx.x;
-    pdl_wait();
-    QSA_AFTER_WAIT(scores);
-    QSA_AFTER_WAIT(q_pos);
-    QSA_AFTER_WAIT(ext_hist);
-    pdl_trigger();
+    uint32_t *hist = smem;
+    uint32_t *warp_s = hist + kBins1;
+    uint32_t *misc = warp_s + 2 * (NT / 32);
+    uint32_t *selw = misc + 32;
+    const int64_t nw = (n + 31) / 32;
+    uint32_t *cand_key = selw + 2 * nw;
+    int32_t *cand_idx = reinterpret_cast<int32_t *>(cand_key + cand_cap);
+    const int tid = threadIdx.x;
+
+    // ---- 1. the sample's histogram and the threshold digit.  sample: this thread's score at
+    // (tid * n_cap) >> 10, loaded by the caller before the query's block count n was known;
+    // the ns samples below n stand for the row (ns >= 1: thread 0 samples block 0).
+    for (int i = tid; i < kBins1; i += NT) hist[i] = 0u;
+    for (int64_t w = tid; w < nw; w += NT) selw[w] = 0u;
+    if (tid == 0) misc[8] = 0u;
+    __syncthreads();
+    const bool in_row = (((int64_t)tid * n_cap) >> 10) < n;
+    if (in_row) atomicAdd(&hist[score_key(sample) >> (32 - kTopkHistBits)], 1u);
+    const int64_t ns = __syncthreads_count(in_row);
+    int64_t r = (k * ns + n - 1) / n + 8;
+    if (r > ns) r = ns;
+    find_bucket(hist, kBins1, (uint32_t)r, warp_s, misc);
+    const uint32_t T = misc[0] << (32 - kTopkHistBits);
+    for (int i = tid; i < kBins1; i += NT) hist[i] = 0u;  // find_bucket has read it
+    __syncthreads();
+
+    // ---- 2. one pass: every key >= T is a candidate, and the candidates' first-digit
+    // histogram
+    auto keep = [&](uint32_t key, int64_t i) {
+        if (key >= T) {
+            atomicAdd(&hist[key >> (32 - kTopkHistBits)], 1u);
+            const uint32_t slot = atomicAdd(&misc[8], 1u);
+            if (slot < (uint32_t)cand_cap) {
+                cand_key[slot] = key;
+                cand_idx[slot] = (int32_t)i;
+            }
+        }
+    };
+    if (T > kKeyNegInf && (reinterpret_cast<uintptr_t>(srow) & 15) == 0)
+        collect_at_least(srow, n, T, &misc[8], cand_key, cand_idx, (uint32_t)cand_cap, hist);
+    else if (T > kKeyNegInf)
+        for_each_key_at_least(srow, n, T, keep);
+    else
+        for_each_key(srow, n, keep);
+    __syncthreads();
+    const uint32_t m = misc[8];
+    if (m < (uint32_t)k || m > (uint32_t)cand_cap) return false;  // uniform
+
+    return select_candidates(k, m, hist, warp_s, misc, selw, nw, cand_key, cand_idx, out, pout,
+                             pvec);
+}
+
+// One query of the general kernel (all threads of a 1024-thread CTA): query qi of n_q.
+__device__ void topk_one(int64_t qi, int64_t n_q, const float *__restrict__ scores, int64_t ld,
+                         const int32_t *__restrict__ q_pos, int64_t n_full_cap, int k_blk,
+                         int32_t *__restrict__ blocks_out, int32_t *__restrict__ counts_out,
+                         int64_t n_ctx, int32_t *__restrict__ pos_out,
+                         int32_t *__restrict__ n_cells_out, int64_t max_cells,
+                         uint32_t *__restrict__ ext_hist, int cand_cap, int64_t p_step,
+                         uint32_t *smem)
+{
     // the sampled form's strided sample over the row's capacity, in flight while the query's
     // position is read (samples past its own block count are dropped there)
     const float sample = (!ext_hist && n_full_cap >= kSampledMinN)
@@ -619,8 +628,7 @@ topk_kernel(const float *__restrict__ scores, int64_t ld, const int32_t *__restr
 
     // the query's position: q_pos[qi], else n_ctx - 1 - p_step * (n_q - 1 - qi) (the last
     // n_q tokens of the context when p_step = 1; every query at n_ctx - 1 when it is 0)
-    const int64_t p = q_pos ? (int64_t)q_pos[qi]
-                            : n_ctx - 1 - p_step * ((int64_t)gridDim.x - 1 - qi);
+    const int64_t p = q_pos ? (int64_t)q_pos[qi] : n_ctx - 1 - p_step * (n_q - 1 - qi);
     int64_t n = n_full_cap;
     if (q_pos || p_step) {
         const int64_t p1 = (p + 1) / 4;
@@ -647,6 +655,45 @@ topk_kernel(const float *__restrict__ scores, int64_t ld, const int32_t *__restr
                            n_full_cap))
         return;
     topk_query(scores + qi * ld, n, k, out, pout, pvec, ehist, cand_cap, smem);
+}
+
+__global__ void __launch_bounds__(NT)
+topk_kernel(const float *__restrict__ scores, int64_t ld, const int32_t *__restrict__ q_pos,
+            int64_t n_full_cap, int k_blk, int32_t *__restrict__ blocks_out,
+            int32_t *__restrict__ counts_out, int64_t n_ctx, int32_t *__restrict__ pos_out,
+            int32_t *__restrict__ n_cells_out, int64_t max_cells, uint32_t *__restrict__ ext_hist,
+            int cand_cap, int64_t p_step)
+{
+    extern __shared__ __align__(16) uint32_t smem[];
+    pdl_wait();
+    QSA_AFTER_WAIT(scores);
+    QSA_AFTER_WAIT(q_pos);
+    QSA_AFTER_WAIT(ext_hist);
+    pdl_trigger();
+    topk_one(blockIdx.x, gridDim.x, scores, ld, q_pos, n_full_cap, k_blk, blocks_out, counts_out,
+             n_ctx, pos_out, n_cells_out, max_cells, ext_hist, cand_cap, p_step, smem);
+}
+
+// The queries listed in list[0 .. *count) (queries the maxima form handed back), each by the
+// general kernel's logic; a persistent grid takes them in turn.
+__global__ void __launch_bounds__(NT)
+topk_listed_kernel(const float *__restrict__ scores, int64_t ld, const int32_t *__restrict__ q_pos,
+                   int64_t n_q, int64_t n_full_cap, int k_blk, int32_t *__restrict__ blocks_out,
+                   int32_t *__restrict__ counts_out, const uint32_t *__restrict__ count,
+                   const int32_t *__restrict__ list, int cand_cap)
+{
+    extern __shared__ __align__(16) uint32_t smem[];
+    pdl_wait();
+    QSA_AFTER_WAIT(scores);
+    QSA_AFTER_WAIT(count);
+    QSA_AFTER_WAIT(list);
+    pdl_trigger();
+    const uint32_t cnt = *count;
+    for (uint32_t j = blockIdx.x; j < cnt; j += gridDim.x) {
+        topk_one(list[j], n_q, scores, ld, q_pos, n_full_cap, k_blk, blocks_out, counts_out, 0,
+                 nullptr, nullptr, 0, nullptr, cand_cap, 0, smem);
+        __syncthreads();  // the next query reuses the shared memory
+    }
 }
 
 // Byte offset of a pointer (the per-query copies of the decode top-k's scratch).
@@ -994,6 +1041,22 @@ cudaError_t launch_topk(const float *scores, int64_t n_q, int64_t ld, const int3
     return launch(topk_kernel, dim3((unsigned)n_q), dim3(NT), smem, st, 1, scores, ld, q_pos,
                   n_full, (int)k_blk, blocks_out, counts_out, n_ctx, pos_out, n_cells_out,
                   max_cells, ext_hist, cand_cap, p_step);
+}
+
+cudaError_t launch_topk_listed(const float *scores, int64_t n_q, int64_t ld, const int32_t *q_pos,
+                               int64_t n_full, int64_t k_blk, int32_t *blocks_out,
+                               int32_t *counts_out, const uint32_t *count, const int32_t *list,
+                               cudaStream_t st)
+{
+    if (n_q == 0) return cudaSuccess;
+    int cand_cap = 0;
+    const size_t smem = topk_smem_bytes(n_full, &cand_cap);
+    cudaError_t e = set_max_smem();
+    if (e == cudaSuccess) e = ensure_kernel_attrs<topk_listed_kernel>(kMaxSmemBytes);
+    if (e != cudaSuccess) return e;
+    const int64_t grid = n_q < device_sm_count() ? n_q : device_sm_count();
+    return launch(topk_listed_kernel, dim3((unsigned)grid), dim3(NT), smem, st, 1, scores, ld,
+                  q_pos, n_q, n_full, (int)k_blk, blocks_out, counts_out, count, list, cand_cap);
 }
 
 }  // namespace qsa

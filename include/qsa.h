@@ -194,6 +194,50 @@ qsa_status qsa_topk_blocks(const float *scores, int64_t n_q, int64_t ld_scores,
 int64_t qsa_topk_max_candidates(void);
 
 /*
+ * qsa_index_score_maxima / qsa_topk_blocks_maxima -- the prefill selection with a per-row
+ * summary written by the score contraction and read by the top-k.
+ *
+ * Source: same page, section "block-domain top-k (COMMON-006)" (the top-k over block
+ * scores) with section "QSA and the QSA indexer" (every query of a prefill chunk scored
+ * against every pooled block).  The pages do not describe how a chunk's top-k is fed; this
+ * library's reading: the score kernel's epilogue, which holds each query's scores of 32
+ * consecutive rows at once, also stores their maximum, and the top-k takes its threshold
+ * from those maxima instead of sampling or scanning the whole row.
+ *
+ * qsa_index_score_maxima is qsa_index_score with precision QSA_PREC_BF16_TC (same
+ * arguments, scores and workspace, same errors) that also writes
+ *   maxima[i][g] = max { scores[i][b] : 32g <= b < min(32g + 32, n_rows) }
+ * for g < ceil(n_rows / 32): -inf when every score of the group is -inf (rows the query
+ * cannot see), NaN scores left out.  maxima: [n_q][ld_maxima] fp32, ld_maxima >=
+ * ceil(n_rows / 32), 4-byte aligned; INVALID_ARG otherwise.
+ *
+ * qsa_topk_blocks_maxima returns exactly what qsa_topk_blocks returns for the same
+ * arguments (same candidates, order, ties and errors), given maxima as written above for
+ * these scores (ld_maxima >= n_full / 32, rounded down; INVALID_ARG otherwise).  For a query
+ * with at least 32 * k_blk candidates (and n_full <= 131,072), the k_blk-th largest maximum
+ * of the groups that hold only candidates bounds its threshold from below, only the groups
+ * whose maximum reaches that bound are read, and four queries share an SM; a query whose
+ * bound leaves more than 2,048 candidates, and every other query, takes the general form.
+ * Maxima that are not those of the scores give an unspecified (but in-bounds) selection.
+ *   workspace  device scratch of qsa_topk_blocks_maxima_workspace_size(n_q) bytes, 256-byte
+ *              aligned (INVALID_ARG when smaller or misaligned)
+ */
+qsa_status qsa_index_score_maxima(const float *q, int64_t n_q, int64_t ld_q,
+                                  const int32_t *q_pos, const void *pooled,
+                                  qsa_dtype pooled_dtype, int64_t n_rows, int H, int d,
+                                  float scale, float *scores, int64_t ld_scores, float *maxima,
+                                  int64_t ld_maxima, void *workspace, size_t workspace_bytes,
+                                  qsa_stream_t stream);
+
+qsa_status qsa_topk_blocks_maxima(const float *scores, int64_t n_q, int64_t ld_scores,
+                                  const int32_t *q_pos, int64_t n_full, int64_t k_blk,
+                                  const float *maxima, int64_t ld_maxima, int32_t *blocks_out,
+                                  int32_t *counts_out, void *workspace, size_t workspace_bytes,
+                                  qsa_stream_t stream);
+
+size_t qsa_topk_blocks_maxima_workspace_size(int64_t n_q);
+
+/*
  * qsa_expand_block_scores -- the selection input of the pages' earlier path, kept for A/B
  * measurement: each full block's score copied to its four cells.
  *

@@ -69,6 +69,43 @@ def test_index_score_rejects(lib):
     assert lib.qsa_index_score_workspace_size(4, 100, 16, 128, 0, 0) == 0
 
 
+def test_maxima_calls_reject(lib):
+    """qsa_index_score_maxima / qsa_topk_blocks_maxima: the checks of the calls they extend,
+    plus a missing or misaligned maxima array and a short maxima stride (nothing launched)."""
+    s = None
+    sa = [FAKE, 1, 256, None, FAKE, 0, 100, 4, 64, 1.0, FAKE, 100, FAKE, 4, None, 0, s]
+
+    def score(**kw):
+        a = list(sa)
+        for i, v in kw.items():
+            a[int(i[1:])] = v
+        return lib.qsa_index_score_maxima(*a)
+
+    assert score(a12=None) == 1          # no maxima
+    assert score(a12=P(0x10002)) == 1    # maxima not 4-byte aligned
+    assert score(a13=3) == 1             # ld_maxima < ceil(100 / 32)
+    assert score(a2=255) == 1            # ld_q < H*d
+    assert score(a11=99) == 1            # ld_scores < n_rows
+    assert score(a15=0) == 1             # workspace smaller than required
+    ws = lib.qsa_topk_blocks_maxima_workspace_size(2)
+    assert ws >= 256 + 8 and lib.qsa_topk_blocks_maxima_workspace_size(0) == 0
+    ta = [FAKE, 2, 70000, None, 70000, 512, FAKE, 2187, FAKE, FAKE, P(0x20000), ws, s]
+
+    def topk(**kw):
+        a = list(ta)
+        for i, v in kw.items():
+            a[int(i[1:])] = v
+        return lib.qsa_topk_blocks_maxima(*a)
+
+    assert topk(a6=None) == 1            # no maxima
+    assert topk(a7=2186) == 1            # ld_maxima < 70000 / 32
+    assert topk(a5=0) == 1               # k_blk < 1
+    assert topk(a2=69999) == 1           # ld_scores < n_full
+    assert topk(a8=None) == 1            # no output
+    assert topk(a11=ws - 1) == 1         # workspace smaller than required
+    assert topk(a10=P(0x20010)) == 1     # workspace not 256-byte aligned
+
+
 def test_decode_step_workspace_and_query_count(lib):
     one = lib.qsa_decode_step_workspace_size(1, 32, 4, 128, 2051, 64000)
     three = lib.qsa_decode_step_workspace_size(3, 32, 4, 128, 2051, 64000)

@@ -258,6 +258,45 @@ def test_prefill_chunk_1024_queries_at_255181_sampled():
     assert agree >= len(sample) - 1
 
 
+def test_prefill_selection_with_maxima_at_255181():
+    """The 1024-query chunk after 255,181 tokens in the benchmark's launch configuration: the
+    score kernel that also writes group maxima gives the same scores bit for bit, and the
+    top-k fed by those maxima the same selection, for every query, as the top-k that scans
+    whole rows (itself exact against the oracle in the tests above and below)."""
+    shape = qsa_synth.CONFIGS["prefill_256k"]
+    inp = qsa_synth.prefill_inputs(shape, seed=1025)
+    H, d, n_q, n_rows, n_ctx = shape.H_idx, shape.d_idx, shape.n_q, shape.n_rows, shape.n_ctx
+    pooled = torch.zeros(n_rows, H * d, device="cuda")
+    qsa.pool_update(to_dev(inp["raw_k"]), n_ctx, H, d, to_dev(inp["norm_w"]), shape.eps,
+                    shape.rope_base, pooled, 0)
+    q_pos, q = to_dev(inp["q_pos"]), to_dev(inp["q_idx"])
+    scale_idx = 1.0 / math.sqrt(d)
+    ws = torch.zeros(qsa.index_score_workspace_size(n_q, n_rows, H, d, qsa.QSA_PREC_BF16_TC),
+                     dtype=torch.uint8, device="cuda")
+    ref = torch.empty(n_q, n_rows, device="cuda")
+    qsa.index_score(q, pooled, n_rows, H, d, scale_idx, ref, q_pos=q_pos,
+                    precision=qsa.QSA_PREC_BF16_TC, workspace=ws)
+    scores = torch.empty(n_q, n_rows, device="cuda")
+    maxima = torch.empty(n_q, (n_rows + 31) // 32, device="cuda")
+    qsa.index_score_maxima(q, pooled, n_rows, H, d, scale_idx, scores, maxima, q_pos=q_pos,
+                           workspace=ws)
+    assert torch.equal(scores, ref)
+    padded = torch.full((n_q, maxima.shape[1] * 32), -math.inf, device="cuda")
+    padded[:, :n_rows] = ref
+    assert torch.equal(maxima, padded.view(n_q, -1, 32).amax(dim=2))
+    blocks = torch.empty(n_q, shape.k_blk, dtype=torch.int32, device="cuda")
+    counts = torch.empty(n_q, dtype=torch.int32, device="cuda")
+    tws = torch.empty(qsa.topk_blocks_maxima_workspace_size(n_q), dtype=torch.uint8,
+                      device="cuda")
+    qsa.topk_blocks_maxima(scores, maxima, n_ctx // 4, shape.k_blk, blocks, counts, tws,
+                           q_pos=q_pos)
+    w_blocks = torch.empty_like(blocks)
+    w_counts = torch.empty_like(counts)
+    qsa.topk_blocks(ref, n_ctx // 4, shape.k_blk, w_blocks, w_counts, q_pos=q_pos)
+    assert torch.equal(counts, w_counts)
+    assert torch.equal(blocks, w_blocks)
+
+
 @pytest.mark.parametrize("store,n_q,steps", [("bf16", 1, 16), ("f32", 3, 6), ("bf16", 3, 6)],
                          ids=["bf16-pooled", "three-queries", "three-queries-bf16-pooled"])
 def test_decode_255181_tokens_variants_appending(store, n_q, steps):
