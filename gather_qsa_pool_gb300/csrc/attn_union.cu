@@ -116,33 +116,46 @@ union_build_kernel(const int32_t *__restrict__ pos, const int32_t *__restrict__ 
     for (int w = tid; w < nwords; w += nt) bits[w] = 0u;
     for (int w = tid; w < kUG * mwords; w += nt) mem[w] = 0u;
     __syncthreads();
-    // The lists' cells, visited as one flat range (list li at index li * max_cells + e),
-    // kBatch independent loads in flight per thread before any is used.
-    constexpr int kBatch = 8;
-    const int64_t span = (int64_t)nq * max_cells;
-    auto for_each_cell = [&](auto &&f) {
-        for (int64_t base = tid; base < span; base += (int64_t)nt * kBatch) {
-            int32_t c[kBatch];
-            int li_[kBatch];
+    // Each list's cells by two warps (16 lists x 2 = the CTA's 32 warps), 32 consecutive cells
+    // per warp load (lane = cell), eight such loads in flight per lane.  A list's cells
+    // ascend, so the lanes' bitmap words never decrease along the warp: a segmented OR scan
+    // over the lanes leaves each word's bits in the last lane holding that word, which alone
+    // issues the shared atomic.
+    constexpr int kU = 8;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int li_w = warp >> 1;
+    const int len_w = li_w < nq ? len_s[li_w] : 0;
+    const int32_t *lp = pos + (q0 + li_w) * max_cells;
+    auto or_lanes = [&](uint32_t *dst, bool valid, int64_t word, uint32_t bit) {
+        const int64_t wk = valid ? word : -1 - (int64_t)lane;  // invalid lanes: own segment
+        uint32_t acc = valid ? bit : 0u;
 #pragma unroll
-            for (int u = 0; u < kBatch; ++u) {
-                const int64_t t = base + (int64_t)u * nt;
-                const int li = (int)(t / max_cells);
-                const int64_t e = t - (int64_t)li * max_cells;
-                li_[u] = li;
-                c[u] = (t < span && e < len_s[li < kUG ? li : 0]) ? pos[(q0 + li) * max_cells + e]
-                                                                   : -1;
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t v = __shfl_up_sync(0xffffffffu, acc, o);
+            const int64_t w2 = __shfl_up_sync(0xffffffffu, wk, o);
+            if (lane >= o && w2 == wk) acc |= v;
+        }
+        const int64_t wn = __shfl_down_sync(0xffffffffu, wk, 1);
+        if (valid && (lane == 31 || wn != wk)) atomicOr(&dst[word], acc);
+    };
+    auto for_each_chunk = [&](auto &&f) {
+        for (int e0 = (warp & 1) * 32; e0 < len_w; e0 += 64 * kU) {  // warp-uniform
+            int32_t c[kU];
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+                const int e = e0 + 64 * u + lane;
+                c[u] = e < len_w ? lp[e] : -1;
             }
 #pragma unroll
-            for (int u = 0; u < kBatch; ++u)
-                if (c[u] >= 0 && c[u] < n_kv) f(li_[u], c[u]);
+            for (int u = 0; u < kU; ++u) f(c[u]);
         }
     };
 
     // every valid cell of every (non-truncated) list marks its block
-    for_each_cell([&](int, int32_t c) {
-        const int b = c >> 2;
-        atomicOr(&bits[b >> 5], 1u << (b & 31));
+    for_each_chunk([&](int32_t c) {
+        const bool valid = c >= 0 && c < n_kv;
+        const int b = valid ? c >> 2 : 0;
+        or_lanes(bits, valid, b >> 5, 1u << (b & 31));
     });
     __syncthreads();
 
@@ -151,7 +164,6 @@ union_build_kernel(const int32_t *__restrict__ pos, const int32_t *__restrict__ 
     const int w0 = tid * per, w1 = min(nwords, w0 + per);
     uint32_t run = 0;
     for (int w = w0; w < w1; ++w) run += __popc(bits[w]);
-    const int lane = tid & 31, warp = tid >> 5;
     uint32_t incl = run;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -195,11 +207,12 @@ union_build_kernel(const int32_t *__restrict__ pos, const int32_t *__restrict__ 
         }
     }
     // membership: bit 4j + (c & 3) of query li's words for cell c of union block j
-    for_each_cell([&](int li, int32_t c) {
-        const int b = c >> 2;
+    for_each_chunk([&](int32_t c) {
+        const bool valid = c >= 0 && c < n_kv;
+        const int b = valid ? c >> 2 : 0;
         const uint32_t j = base[b >> 5] + __popc(bits[b >> 5] & ((1u << (b & 31)) - 1u));
         const uint32_t k = 4 * j + (uint32_t)(c & 3);
-        atomicOr(&mem[li * mwords + (k >> 5)], 1u << (k & 31));
+        or_lanes(mem, valid, (int64_t)li_w * mwords + (k >> 5), 1u << (k & 31));
     });
     __syncthreads();
     // out in tile-major order: [tile][query][2 words], 64 cells per tile
