@@ -21,19 +21,21 @@
 // Kernel 2, attn_union_kernel (one CTA per group and KV head; M = 16 queries x 8 heads =
 // 128 rows): warps 0 and 10 stage the union's blocks 16 at a time (a 64-cell tile of K and
 // one of V, each cell's 256-byte head row as sixteen 16-byte asynchronous copies written
-// straight into the 128-byte-swizzled layout the tensor cores read) into a ring of six
+// straight into the 128-byte-swizzled layout the tensor cores read) into a ring of five
 // stages; a stage's barrier completes when the copies of both warps have landed.  (One TMA
 // box per block and dim half, 512 bytes each, ran at about 70 cycles a box: the box count,
-// not the bytes, bounded the kernel.)  Warp 1 issues the MMAs -- S = Q K^T (N 64 cells, K
-// 128 dims; A is the query's bf16 high and low halves, pre-scaled by scale * log2 e, held in
-// tensor memory) into one of two tensor-memory buffers, and O += P V (N 128 dims, K 64 cells,
-// V read MN-major; A is P's high and low halves, in one of two tensor-memory buffers) into a
-// third, two tiles behind the S it follows.  Warps 2-9 (two threads per row, one per half of
-// the tile's columns) read S, mask it with the row's membership bits, keep an online maximum
-// that is moved (and O rescaled in tensor memory) only when it grows by more than 2^8, write
-// P into tensor memory, and at the end divide O by the row sum.  Every mbarrier wait is
-// bounded: on a timeout the rows of the CTA become NaN, nothing new is issued, what was
-// issued is waited for (bounded) and the tensor memory is returned.
+// not the bytes, bounded the kernel.)  Two softmax groups (warps 2-5 and 6-9, one thread per
+// row and group) take alternate tiles, each with its own S, P and O in tensor memory and its
+// own online maximum and sum, merged at the end.  Lane 0 of warp 1 issues S = Q K^T (N 64
+// cells, K 128 dims; A is the query's bf16 high and low halves, pre-scaled by scale * log2 e,
+// in shared memory) into the tile's group's S; lane 0 of warp 11 issues O_g += P V (N 128
+// dims, K 64 cells; A is P's high and low halves in tensor memory, V read MN-major).  A
+// group's thread reads S, masks it with the row's membership bits, moves its maximum (and
+// rescales its O in tensor memory) only when it grows by more than 2^8, and writes P.  While
+// one group computes, the other's MMAs run; with the S and P V issued by two threads, one
+// issues while the other waits.  Every mbarrier wait is bounded: on a timeout the rows of the
+// CTA become NaN, nothing new is issued, what was issued is waited for (bounded) and the
+// tensor memory is returned.
 #include "attn_union.cuh"
 
 namespace qsa {
@@ -45,25 +47,30 @@ constexpr int kUM = kUG * kUHeads;      // 128 rows
 constexpr int kUD = 128;                // head dim
 constexpr int kUTB = 16;                // union blocks per tile
 constexpr int kUTC = 4 * kUTB;          // 64 cells per tile
-constexpr int kUStages = 6;
-constexpr int kUThreads = 352;          // warps 0 and 10 copy, warp 1 MMA, warps 2-9 softmax
+constexpr int kUStages = 5;
+constexpr int kUThreads = 384;          // warps 0 and 10 copy, 1 and 11 MMA, 2-9 softmax
 constexpr int kUCopyThreads = 64;       // the two copy warps
-constexpr int kUEpiWarps = 8;           // two per row: one per half of the tile's columns
+constexpr int kUGroupWarps = 4;         // softmax warps of a group: one per 32 rows
 constexpr float kURescale = 8.0f;       // move the running maximum past 2^8 growth
 constexpr int kUMaxBlockWords = 8192;   // bitmap words: 2^18 blocks = 2^20 cells
 
 constexpr uint32_t kTileHalf = kUTC * 128;          // 8 KB: 64 cells x 64 dims bf16
 constexpr uint32_t kTileBytes = 2 * kTileHalf;      // 16 KB: one tensor's 64-cell tile
 constexpr uint32_t kStageBytes = 2 * kTileBytes;    // K and V
-// Tensor memory (512 columns, one row per lane): S[0], S[1] fp32 (64 each), O fp32 (128),
-// Q's bf16 high and low halves (64 each: two dims per column), P[0], P[1] as bf16 high and
-// low halves (32 each: two cells per column).
+// Tensor memory (512 columns, one row per lane), per softmax group A / B: S fp32 (64
+// columns), O fp32 (128), P as bf16 high and low halves (32 each: two cells per column).
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0, kColO = 128, kColQh = 256, kColQl = 320, kColP = 384;
+__host__ __device__ constexpr uint32_t col_s(int gi) { return gi ? 64u : 0u; }
+__host__ __device__ constexpr uint32_t col_o(int gi) { return gi ? 256u : 128u; }
+__host__ __device__ constexpr uint32_t col_p(int gi) { return gi ? 448u : 384u; }
+// Q in shared memory: its bf16 high and low halves, each two 64-dim blocks of 128 rows x 128
+// bytes (128-byte swizzle), the A operand of S = Q K^T
+constexpr uint32_t kQTile = kUM * 128;              // 16 KB
+constexpr uint32_t kQBytes = 4 * kQTile;
 
 __host__ __device__ constexpr size_t union_smem_bytes()
 {
-    return 1024 + (size_t)kUStages * kStageBytes + 256 + 6 * kUM * sizeof(float);
+    return 1024 + (size_t)kUStages * kStageBytes + kQBytes + 256;
 }
 
 // Union capacity in blocks for lists of up to max_cells cells: a list of whole blocks plus
@@ -274,6 +281,18 @@ __device__ __forceinline__ void umma_m128_ta(uint32_t d_tmem, uint32_t a_tmem, u
         : "memory");
 }
 
+// One M128 MMA of this CTA with A and B both from shared memory.
+__device__ __forceinline__ void umma_m128_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                             uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Arrive on the barrier once every MMA this thread issued so far has completed.
 __device__ __forceinline__ void umma_commit(uint64_t *bar)
 {
@@ -355,19 +374,18 @@ __device__ __forceinline__ float ex2_approx(float x)
     return y;
 }
 
-// Barrier of the two softmax warps that own the same 32 rows (named barrier 1 + quarter)
-// that also returns the AND of `v` over their 64 threads: both warps take every decision that
-// follows it the same way (neither may leave a loop the other stays in).
-__device__ __forceinline__ bool pair_and(int quarter, bool v)
+// Barrier of the eight softmax warps (named barrier 1) that also returns the AND of `v` over
+// their 256 threads.
+__device__ __forceinline__ bool softmax_and(bool v)
 {
     uint32_t r;
     asm volatile(
         "{\n\t.reg .pred p, c;\n\t"
         "setp.ne.u32 c, %1, 0;\n\t"
-        "bar.red.and.pred p, %2, 64, c;\n\t"
+        "bar.red.and.pred p, 1, 256, c;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(r)
-        : "r"((uint32_t)v), "r"(1 + quarter)
+        : "r"((uint32_t)v)
         : "memory");
     return r != 0;
 }
@@ -403,18 +421,20 @@ attn_union_kernel(const __nv_bfloat16 *__restrict__ K, const __nv_bfloat16 *__re
     extern __shared__ __align__(16) unsigned char smem_raw[];
     unsigned char *sKV = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-    // [stage][K, V][2 dim halves][64 cells][128 B], 128-byte swizzle
-    uint64_t *kv_full = reinterpret_cast<uint64_t *>(sKV + kUStages * kStageBytes);
+    // [stage][K, V][2 dim halves][64 cells][128 B], 128-byte swizzle; then Q
+    unsigned char *sQ = sKV + kUStages * kStageBytes;  // [hi, lo][dim block][128 rows][128 B]
+    uint64_t *kv_full = reinterpret_cast<uint64_t *>(sQ + kQBytes);
     uint64_t *kv_empty = kv_full + kUStages;
-    uint64_t *s_full = kv_empty + kUStages;          // [2] S(t) in its buffer
-    uint64_t *p_full = s_full + 2;                   // [2] P(t) in its buffer (S(t) read)
-    uint64_t *o_done = p_full + 2;                   // [2] the P V of a tile using P buffer b done
+    uint64_t *s_full = kv_empty + kUStages;          // [group] S(t) in the group's buffer
+    uint64_t *s_empty = s_full + 2;                  // [group] the group read S(t)
+    uint64_t *p_full = s_empty + 2;                  // [group] P(t) in the group's buffer
+    uint64_t *o_done = p_full + 2;                   // [group] the group's last P V done
     uint64_t *q_ready = o_done + 2;
-    uint64_t *drain = q_ready + 1;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
-    // row maxima of the two halves of each row, double-buffered by tile parity ([2][2][128]
-    // floats), then the halves' row sums ([2][128]), at 256 bytes past the stage ring
-    float *xch = reinterpret_cast<float *>(sKV + kUStages * kStageBytes + 256);
+    uint64_t *drain = q_ready + 1;                   // [2] each issuing thread's MMAs done
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 2);
+    // each group's row maxima and sums ([2][2][128] floats) for the final merge, over Q's
+    // tiles once every MMA has completed
+    float *xch = reinterpret_cast<float *>(sQ);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int64_t g = blockIdx.x;
@@ -429,11 +449,13 @@ attn_union_kernel(const __nv_bfloat16 *__restrict__ K, const __nv_bfloat16 *__re
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&s_full[b], 1);
-            mbar_init(&p_full[b], kUEpiWarps);
+            mbar_init(&s_empty[b], kUGroupWarps);
+            mbar_init(&p_full[b], kUGroupWarps);
             mbar_init(&o_done[b], 1);
         }
-        mbar_init(q_ready, kUEpiWarps);
-        mbar_init(drain, 1);
+        mbar_init(q_ready, 2 * kUGroupWarps);
+        mbar_init(&drain[0], 1);
+        mbar_init(&drain[1], 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 1) {
@@ -461,7 +483,7 @@ attn_union_kernel(const __nv_bfloat16 *__restrict__ K, const __nv_bfloat16 *__re
     const uint32_t *gmem = gw + 4 + cap;
     bool ok = true;
 
-    if (warp == 0 || warp == kUThreads / 32 - 1) {
+    if (warp == 0 || warp == 10) {
         // ---- copies: warp p fills rows 32p .. 32p + 31 (blocks 8p .. 8p + 7) of the tile's
         // K and V; lane = 16 * (row parity) + 16-byte chunk of the 256-byte head row
         const int p = warp == 0 ? 0 : 1;
@@ -509,82 +531,87 @@ attn_union_kernel(const __nv_bfloat16 *__restrict__ K, const __nv_bfloat16 *__re
             const int uses = armed / kUStages + (s < armed % kUStages ? 1 : 0);
             if (uses > 0 && !mbar_wait(&kv_full[s], (uint32_t)(uses - 1) & 1u)) ok = false;
         }
-    } else if (warp == 1) {
-        // ---- MMA issuer (one thread): per tile t one burst, S(t) = Q K(t)^T and then
-        // O += P(t-2) V(t-2), after two waits: K / V(t) landed, and P(t-2) written (so the
-        // softmax warps also read S(t-2), whose buffer S(t) takes).  P V runs two tiles behind
-        // so that S(t + 1) is issued while the softmax of t - 1 still runs.  Each wait or commit
-        // costs this thread over a hundred cycles with the tensor queue draining meanwhile, so a
-        // tile has two waits and three commits.  The issuing thread shares its sub-partition
-        // with two softmax warps, so each MMA costs it one 32-bit add: the descriptors of stage
-        // 0 are built once, and a stage, dim half or k step moves only the start-address field
-        // (bits 0-13, 16-byte units; shared addresses stay below 256 KB, so the add never
-        // carries out of it).
+    } else if (warp == 1 || warp == 11) {
+        // ---- MMA issuers: lane 0 of warp 1 issues every S, lane 0 of warp 11 every P V, so
+        // that one issues while the other waits (a wait or commit costs its thread over a
+        // hundred cycles, and the tensor queue would drain meanwhile).  Tile t belongs to
+        // softmax group t & 1: S(t) = Q K(t)^T into the group's S once K / V(t) landed and the
+        // group read S(t - 2); O_g += P(t) V(t) once the group wrote P(t), which it does only
+        // after reading S(t), so the stage is free when this P V completes.  The descriptors
+        // of stage 0 and of Q are built once: a stage, dim block or k step moves only their
+        // start-address field (bits 0-13, 16-byte units; shared addresses stay below 256 KB,
+        // so the add never carries out of it).
+        const bool is_s = warp == 1;
         if (lane == 0) {
             constexpr uint32_t id_s = idesc_m128(kUTC, false);
             constexpr uint32_t id_o = idesc_m128(kUD, true);
             const uint64_t dk0 = desc_kmajor_sw128(smem_u32(sKV));
             const uint64_t dv0 = desc_mnmajor_sw128(smem_u32(sKV + kTileBytes), kTileHalf);
+            const uint64_t dq0 = desc_kmajor_sw128(smem_u32(sQ));
             const uint32_t dk_lo = (uint32_t)dk0, dk_hi = (uint32_t)(dk0 >> 32);
             const uint32_t dv_lo = (uint32_t)dv0, dv_hi = (uint32_t)(dv0 >> 32);
-            if (n_tiles > 0 && !mbar_wait(q_ready, 0, wc.limit_ns)) ok = false;
-            for (int t = 0; ok && t < n_tiles + 2; ++t) {
-                const int tp = t - 2;
-                if (t < n_tiles) {
-                    if (!mbar_wait(&kv_full[t % kUStages], (uint32_t)(t / kUStages) & 1u, wc.limit_ns)) {
+            const uint32_t dq_lo = (uint32_t)dq0, dq_hi = (uint32_t)(dq0 >> 32);
+            if (is_s && n_tiles > 0 && !mbar_wait(q_ready, 0, wc.limit_ns)) ok = false;
+            for (int t = 0; ok && t < n_tiles; ++t) {
+                const int s = t % kUStages, b = t & 1;
+                if (is_s) {
+                    if (!mbar_wait(&kv_full[s], (uint32_t)(t / kUStages) & 1u, wc.limit_ns)) {
                         ok = false;
                         break;
                     }
                     // the stage was written by ordinary (generic-proxy) copies; the tensor
                     // cores read it through the async proxy
                     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                }
-                if (tp >= 0 && !mbar_wait(&p_full[tp & 1], (uint32_t)(tp >> 1) & 1u, wc.limit_ns)) {
-                    ok = false;
-                    break;
-                }
-                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                if (t < n_tiles) {
-                    const int s = t % kUStages, b = t & 1;
+                    if (t >= 2 &&
+                        !mbar_wait(&s_empty[b], (uint32_t)((t - 2) >> 1) & 1u, wc.limit_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
                     const uint32_t ks = dk_lo + (uint32_t)s * (kStageBytes >> 4);
-                    const uint32_t d_s = tmem + kColS + (uint32_t)(b * kUTC);
 #pragma unroll
                     for (int part = 0; part < 2; ++part) {
 #pragma unroll
                         for (int k16 = 0; k16 < kUD / 16; ++k16) {
-                            const uint32_t off = ((uint32_t)(k16 >> 2) * kTileHalf + (uint32_t)(k16 & 3) * 32) >> 4;
-                            umma_m128_ta(d_s, tmem + (part ? kColQl : kColQh) + (uint32_t)k16 * 8,
-                                         ((uint64_t)dk_hi << 32) | (ks + off), id_s,
+                            const uint32_t kb = (uint32_t)(k16 >> 2), ko = (uint32_t)(k16 & 3) * 32;
+                            const uint32_t qa = dq_lo + (((uint32_t)part * 2 + kb) * kQTile + ko) / 16;
+                            const uint32_t kd = ks + (kb * kTileHalf + ko) / 16;
+                            umma_m128_ss(tmem + col_s(b), ((uint64_t)dq_hi << 32) | qa,
+                                         ((uint64_t)dk_hi << 32) | kd, id_s,
                                          (part | k16) ? 1u : 0u);
                         }
                     }
                     umma_commit(&s_full[b]);
-                }
-                if (tp >= 0) {
-                    const int sp = tp % kUStages, pb = tp & 1;
-                    const uint32_t vs = dv_lo + (uint32_t)sp * (kStageBytes >> 4);
-                    const uint32_t pcol = tmem + kColP + (uint32_t)pb * 64;
+                } else {
+                    if (!mbar_wait(&p_full[b], (uint32_t)(t >> 1) & 1u, wc.limit_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                    const uint32_t vs = dv_lo + (uint32_t)s * (kStageBytes >> 4);
 #pragma unroll
                     for (int part = 0; part < 2; ++part) {
 #pragma unroll
                         for (int k16 = 0; k16 < kUTC / 16; ++k16)
-                            umma_m128_ta(tmem + kColO, pcol + (uint32_t)(part * 32 + k16 * 8),
-                                         ((uint64_t)dv_hi << 32) | (vs + (uint32_t)k16 * (2048 >> 4)),
-                                         id_o, (tp | part | k16) ? 1u : 0u);
+                            umma_m128_ta(tmem + col_o(b),
+                                         tmem + col_p(b) + (uint32_t)(part * 32 + k16 * 8),
+                                         ((uint64_t)dv_hi << 32) | (vs + (uint32_t)k16 * (2048 / 16)),
+                                         id_o, (t >= 2 || part || k16) ? 1u : 0u);
                     }
-                    umma_commit(&o_done[pb]);
-                    umma_commit(&kv_empty[sp]);
+                    umma_commit(&o_done[b]);
+                    umma_commit(&kv_empty[s]);
                 }
             }
-            // every MMA issued has completed before the tensor memory is freed
-            umma_commit(drain);
-            if (!mbar_wait(drain, 0)) ok = false;
+            // every MMA this thread issued has completed before the tensor memory is freed
+            umma_commit(&drain[is_s ? 0 : 1]);
+            if (!mbar_wait(&drain[is_s ? 0 : 1], 0)) ok = false;
         }
     } else {
-        // ---- softmax / epilogue: two threads per row (row = 8 * query + head), one per half
-        // of the tile's 64 columns (and of O's 128 dims)
+        // ---- softmax, in two groups that take alternate tiles (group gi: warps 2-5 or 6-9,
+        // tiles gi, gi + 2, ...), one thread per row (row = 8 * query + head) and group, all
+        // 64 columns of the group's tiles; each group keeps its own online maximum, sum and O
         const int quarter = warp & 3;
-        const int ch = (warp - 2) >> 2;              // column half: warps 2-5 -> 0, 6-9 -> 1
+        const int gi = (warp - 2) >> 2;
         const int r = quarter * 32 + lane;
         const int li = r >> 3;
         const int64_t qi = g * kUG + li;
@@ -593,64 +620,73 @@ attn_union_kernel(const __nv_bfloat16 *__restrict__ K, const __nv_bfloat16 *__re
         const int64_t n = live ? (int64_t)n_cells[qi] : 0;
         const bool trunc = n > max_cells;
         const uint32_t lrow = (uint32_t)(quarter * 32) << 16;
-        // this half of the row's query (dims 64*ch ..), pre-scaled, as bf16 high and low
-        // halves into tensor memory
+        const uint32_t colS = tmem + lrow + col_s(gi), colP = tmem + lrow + col_p(gi);
+        const uint32_t colO = tmem + lrow + col_o(gi);
+        // dims 64*gi .. of the row's query, pre-scaled, as bf16 high and low halves into Q's
+        // shared-memory tiles (128-byte swizzle: chunk c of row r at chunk c ^ (r % 8))
         {
-            const float *qr = q + (qi * H_q + h) * (int64_t)kUD + ch * 64;
-            uint32_t wh[32], wl[32];
+            const float *qr = q + (qi * H_q + h) * (int64_t)kUD + gi * 64;
 #pragma unroll
-            for (int e = 0; e < 64; e += 2) {
-                float x0 = 0.0f, x1 = 0.0f;
+            for (int c = 0; c < 8; ++c) {
+                float x[8];
                 if (live) {
-                    const float2 v = *reinterpret_cast<const float2 *>(qr + e);
-                    x0 = v.x * scale_log2;
-                    x1 = v.y * scale_log2;
+                    const float4 a = *reinterpret_cast<const float4 *>(qr + 8 * c);
+                    const float4 b = *reinterpret_cast<const float4 *>(qr + 8 * c + 4);
+                    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+                    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) x[e] = 0.0f;
                 }
-                const float h0 = __bfloat162float(__float2bfloat16_rn(x0));
-                const float h1 = __bfloat162float(__float2bfloat16_rn(x1));
-                wh[e / 2] = pack_bf16(h0, h1);
-                wl[e / 2] = pack_bf16(x0 - h0, x1 - h1);
+                uint32_t wh[4], wl[4];
+#pragma unroll
+                for (int e = 0; e < 8; e += 2) {
+                    const float x0 = x[e] * scale_log2, x1 = x[e + 1] * scale_log2;
+                    const float h0 = __bfloat162float(__float2bfloat16_rn(x0));
+                    const float h1 = __bfloat162float(__float2bfloat16_rn(x1));
+                    wh[e / 2] = pack_bf16(h0, h1);
+                    wl[e / 2] = pack_bf16(x0 - h0, x1 - h1);
+                }
+                const uint32_t off = (uint32_t)r * 128 + ((uint32_t)(c ^ (r & 7)) << 4);
+                *reinterpret_cast<uint4 *>(sQ + (uint32_t)gi * kQTile + off) =
+                    make_uint4(wh[0], wh[1], wh[2], wh[3]);
+                *reinterpret_cast<uint4 *>(sQ + (uint32_t)(2 + gi) * kQTile + off) =
+                    make_uint4(wl[0], wl[1], wl[2], wl[3]);
             }
-            tmem_st32(tmem + lrow + kColQh + (uint32_t)(ch * 32), wh);
-            tmem_st32(tmem + lrow + kColQl + (uint32_t)(ch * 32), wl);
-            tmem_wait_st();
-            asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+            // written by this thread (generic proxy), read by the tensor cores (async proxy)
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             __syncwarp();
             if (lane == 0) mbar_arrive(q_ready);
         }
         float m_ref = -INFINITY, l = 0.0f;
-        uint32_t mw = 0;
-        if (n_tiles > 0) mw = gmem[li * 2 + ch];
-        // Every iteration passes exactly one pair barrier, which also decides (for both warps
-        // of the pair alike) whether to stop: a warp whose wait gave up skips its tensor-memory
-        // work and stops at the next pair barrier together with its partner.
-        for (int t = 0; t < n_tiles; ++t) {
-            const int b = t & 1;
-            const uint32_t w = (live && !trunc) ? mw : 0u;
-            if (t + 1 < n_tiles) mw = gmem[((int64_t)(t + 1) * kUG + li) * 2 + ch];  // ahead
+        const int n_mine = n_tiles > gi ? (n_tiles - gi + 1) / 2 : 0;
+        uint2 mw = make_uint2(0u, 0u);
+        if (n_mine > 0) mw = *reinterpret_cast<const uint2 *>(gmem + ((int64_t)gi * kUG + li) * 2);
+        for (int j = 0; j < n_mine; ++j) {
+            const int t = gi + 2 * j;
+            const uint2 w = (live && !trunc) ? mw : make_uint2(0u, 0u);
+            if (j + 1 < n_mine)  // the next tile's membership words, ahead
+                mw = *reinterpret_cast<const uint2 *>(gmem + ((int64_t)(t + 2) * kUG + li) * 2);
             // waits are warp-uniform: the tensor-memory accesses below need the whole warp
-            bool good = ok && warp_wait(&s_full[b], (uint32_t)(t >> 1) & 1u, wc.limit_ns);
-            float x[32];
-            float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-            if (good) {
-                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                tmem_ld32(tmem + lrow + kColS + (uint32_t)(b * kUTC + ch * 32), x);
-                asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-                __syncwarp();
-#pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    x[e] = ((w >> e) & 1u) ? x[e] : -INFINITY;
-                    mx[e & 3] = fmaxf(mx[e & 3], x[e]);
-                }
-            }
-            // the row's maximum over both halves
-            float *slot = xch + (b * 2) * kUM;
-            slot[ch * kUM + r] = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-            if (!pair_and(quarter, good)) {
+            if (!(ok && warp_wait(&s_full[gi], (uint32_t)j & 1u, wc.limit_ns))) {
                 ok = false;
                 break;
             }
-            const float mt = fmaxf(slot[r], slot[kUM + r]);
+            float x[64];
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            tmem_ld32(colS, x);
+            tmem_ld32(colS + 32, x + 32);
+            asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s_empty[gi]);
+            float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+                x[e] = ((w.x >> e) & 1u) ? x[e] : -INFINITY;
+                x[32 + e] = ((w.y >> e) & 1u) ? x[32 + e] : -INFINITY;
+                mx[e & 3] = fmaxf(mx[e & 3], fmaxf(x[e], x[32 + e]));
+            }
+            const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
             float alpha = 1.0f;
             bool move = false;
             if (mt > m_ref + kURescale) {  // also the first finite maximum (m_ref = -inf)
@@ -662,87 +698,107 @@ attn_union_kernel(const __nv_bfloat16 *__restrict__ K, const __nv_bfloat16 *__re
                 l *= alpha;
                 m_ref = mt;
             }
-            // P(t) relative to the (possibly moved) maximum, before any wait on the MMAs
             const float mu = m_ref == -INFINITY ? 0.0f : m_ref;
-            uint32_t pw[32];
-            float ls[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-            for (int e = 0; e < 32; e += 2) {
-                const float p0 = ex2_approx(x[e] - mu);
-                const float p1 = ex2_approx(x[e + 1] - mu);
-                ls[(e >> 1) & 3] += p0 + p1;
-                const uint32_t hb = pack_bf16(p0, p1);
-                const float h0 = __uint_as_float(hb << 16), h1 = __uint_as_float(hb & 0xffff0000u);
-                pw[e / 2] = hb;
-                pw[16 + e / 2] = pack_bf16(p0 - h0, p1 - h1);
-            }
-            l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-            // P buffer b was last read by P V(t - 2); O is touched only when rescaling, after
-            // P V(t - 1)
-            const bool w2 = t < 2 || warp_wait(&o_done[b], (uint32_t)((t - 2) >> 1) & 1u,
-                                               wc.limit_ns);
-            const bool w3 = !(rescale && t >= 1) ||
-                            warp_wait(&o_done[b ^ 1], (uint32_t)((t - 1) >> 1) & 1u, wc.limit_ns);
-            if (!(w2 && w3)) {
-                ok = false;  // stops at the next pair barrier (or the one after the loop)
-                continue;
+            // the group's P buffer and O are free once its P V(t - 2) is done
+            if (j >= 1 && !warp_wait(&o_done[gi], (uint32_t)(j - 1) & 1u, wc.limit_ns)) {
+                ok = false;
+                break;
             }
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
             if (rescale) {
 #pragma unroll 1
-                for (int c = ch * 64; c < ch * 64 + 64; c += 32) {
+                for (int c = 0; c < (int)kUD; c += 32) {
                     float o[32];
-                    tmem_ld32(tmem + lrow + kColO + (uint32_t)c, o);
+                    tmem_ld32(colO + (uint32_t)c, o);
                     uint32_t ou[32];
 #pragma unroll
                     for (int e = 0; e < 32; ++e) ou[e] = __float_as_uint(o[e] * alpha);
-                    tmem_st32(tmem + lrow + kColO + (uint32_t)c, ou);
+                    tmem_st32(colO + (uint32_t)c, ou);
                 }
             }
-            // P(t): high halves in columns 0-31 of the buffer, low halves in 32-63; this
-            // thread's 32 cells are 16 columns of each
-            const uint32_t pcol = tmem + lrow + kColP + (uint32_t)b * 64 + (uint32_t)(ch * 16);
-            tmem_st16(pcol, pw);
-            tmem_st16(pcol + 32, pw + 16);
+            // P(t) relative to the (possibly moved) maximum: high halves in columns 0-31 of
+            // the group's P, low halves in 32-63, two cells per column; in two halves of 32
+            // cells
+            float ls[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                uint32_t ph[16], pl[16];
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) {
+                    const float p0 = ex2_approx(x[32 * hf + e] - mu);
+                    const float p1 = ex2_approx(x[32 * hf + e + 1] - mu);
+                    ls[(e >> 1) & 3] += p0 + p1;
+                    const uint32_t hb = pack_bf16(p0, p1);
+                    const float h0 = __uint_as_float(hb << 16), h1 = __uint_as_float(hb & 0xffff0000u);
+                    ph[e / 2] = hb;
+                    pl[e / 2] = pack_bf16(p0 - h0, p1 - h1);
+                }
+                tmem_st16(colP + (uint32_t)(16 * hf), ph);
+                tmem_st16(colP + 32 + (uint32_t)(16 * hf), pl);
+            }
+            l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
             tmem_wait_st();
             asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
             __syncwarp();
-            if (lane == 0) mbar_arrive(&p_full[b]);
+            if (lane == 0) mbar_arrive(&p_full[gi]);
         }
-        if (ok && n_tiles > 0 &&
-            !warp_wait(&o_done[(n_tiles - 1) & 1], (uint32_t)((n_tiles - 1) >> 1) & 1u, wc.limit_ns))
+        // the group's O is final once its last P V is done
+        if (ok && n_mine > 0 &&
+            !warp_wait(&o_done[gi], (uint32_t)(n_mine - 1) & 1u, wc.limit_ns))
             ok = false;
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        // the row sum over both halves, and whether both warps of the pair finished (every
-        // warp of a pair arrives here after the same number of pair barriers)
-        float *lsum = xch + 4 * kUM;
-        lsum[ch * kUM + r] = l;
-        ok = pair_and(quarter, ok);
-        const float lt = lsum[r] + lsum[kUM + r];
+        // merge the two groups' states: m = max(m_A, m_B), each O and sum scaled by 2^(m_g - m).
+        // Every softmax warp arrives at each of these barriers once, after its loop; past the
+        // first, both groups saw their last P V done (so every S, which precedes the P V of
+        // its tile, too), or gave up waiting and the rows are NaN
+        ok = softmax_and(ok);
+        if (ok) {
+            xch[(2 * gi) * kUM + r] = m_ref;
+            xch[(2 * gi + 1) * kUM + r] = l;
+        }
+        asm volatile("bar.sync 1, 256;" ::: "memory");
+        const float mA = ok ? xch[r] : 0.0f, lA = ok ? xch[kUM + r] : 0.0f;
+        const float mB = ok ? xch[2 * kUM + r] : 0.0f, lB = ok ? xch[3 * kUM + r] : 0.0f;
+        const float mm = fmaxf(mA, mB);
+        const float sA = mA == -INFINITY ? 0.0f : ex2_approx(mA - mm);
+        const float sB = mB == -INFINITY ? 0.0f : ex2_approx(mB - mm);
+        const float lt = lA * sA + lB * sB;
         const bool nan_rows = !ok || bad_group || trunc;
         const float inv = lt > 0.0f ? 1.0f / lt : 0.0f;
+        // a group that took no tile has no O (tensor memory never written)
+        const bool has_a = ok && n_tiles > 0, has_b = ok && n_tiles > 1;
 #pragma unroll 1
-        for (int c = ch * 64; c < ch * 64 + 64; c += 32) {
-            float o[32];
-            if (n_tiles > 0 && ok) {
-                tmem_ld32(tmem + lrow + kColO + (uint32_t)c, o);
+        for (int c = 64 * gi; c < 64 * gi + 64; c += 32) {
+            float oa[32], ob[32];
+            if (has_a) {
+                tmem_ld32(tmem + lrow + col_o(0) + (uint32_t)c, oa);
             } else {
 #pragma unroll
-                for (int e = 0; e < 32; ++e) o[e] = 0.0f;
+                for (int e = 0; e < 32; ++e) oa[e] = 0.0f;
+            }
+            if (has_b) {
+                tmem_ld32(tmem + lrow + col_o(1) + (uint32_t)c, ob);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) ob[e] = 0.0f;
             }
             if (live) {
                 float *dst = out + (qi * H_q + h) * (int64_t)kUD + c;
 #pragma unroll
-                for (int e = 0; e < 32; e += 4)
+                for (int e = 0; e < 32; e += 4) {
+                    float4 v;
+                    v.x = (oa[e] * sA + ob[e] * sB) * inv;
+                    v.y = (oa[e + 1] * sA + ob[e + 1] * sB) * inv;
+                    v.z = (oa[e + 2] * sA + ob[e + 2] * sB) * inv;
+                    v.w = (oa[e + 3] * sA + ob[e + 3] * sB) * inv;
                     *reinterpret_cast<float4 *>(dst + e) =
-                        nan_rows ? make_float4(NAN, NAN, NAN, NAN)
-                                 : make_float4(o[e] * inv, o[e + 1] * inv, o[e + 2] * inv,
-                                               o[e + 3] * inv);
+                        nan_rows ? make_float4(NAN, NAN, NAN, NAN) : v;
+                }
             }
         }
-        if (live && lse && ch == 0)
+        if (live && lse && gi == 0)
             lse[qi * H_q + h] = nan_rows ? NAN
-                                         : (lt > 0.0f ? (m_ref + log2f(lt)) * 0.6931471805599453f
+                                         : (lt > 0.0f ? (mm + log2f(lt)) * 0.6931471805599453f
                                                       : -INFINITY);
     }
 
