@@ -125,25 +125,26 @@ union_build_kernel(const int32_t *__restrict__ pos, const int32_t *__restrict__ 
     __syncthreads();
     // Each list's cells by two warps (16 lists x 2 = the CTA's 32 warps), 32 consecutive cells
     // per warp load (lane = cell), eight such loads in flight per lane.  A list's cells
-    // ascend, so the lanes' bitmap words never decrease along the warp: a segmented OR scan
-    // over the lanes leaves each word's bits in the last lane holding that word, which alone
-    // issues the shared atomic.
+    // ascend, so the lanes' bitmap words never decrease along the warp.
     constexpr int kU = 8;
     const int warp = tid >> 5, lane = tid & 31;
     const int li_w = warp >> 1;
     const int len_w = li_w < nq ? len_s[li_w] : 0;
     const int32_t *lp = pos + (q0 + li_w) * max_cells;
-    auto or_lanes = [&](uint32_t *dst, bool valid, int64_t word, uint32_t bit) {
-        const int64_t wk = valid ? word : -1 - (int64_t)lane;  // invalid lanes: own segment
+    auto or_lanes = [&](uint32_t *dst, bool valid, uint32_t word, uint32_t bit) {
+        // a block's four cells sit in four consecutive lanes and set bits of one word: within
+        // each quad of lanes, the first lane of every run of one word collects the run's bits
+        // (the words never decrease along the warp) and alone issues the atomic
+        const uint32_t wk = valid ? word : 0xffffffffu - (uint32_t)lane;  // invalid: own run
         uint32_t acc = valid ? bit : 0u;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t v = __shfl_up_sync(0xffffffffu, acc, o);
-            const int64_t w2 = __shfl_up_sync(0xffffffffu, wk, o);
-            if (lane >= o && w2 == wk) acc |= v;
-        }
-        const int64_t wn = __shfl_down_sync(0xffffffffu, wk, 1);
-        if (valid && (lane == 31 || wn != wk)) atomicOr(&dst[word], acc);
+        uint32_t wo = __shfl_xor_sync(0xffffffffu, wk, 1);
+        uint32_t ao = __shfl_xor_sync(0xffffffffu, acc, 1);
+        if (wo == wk) acc |= ao;
+        wo = __shfl_xor_sync(0xffffffffu, wk, 2);
+        ao = __shfl_xor_sync(0xffffffffu, acc, 2);
+        if (wo == wk) acc |= ao;
+        const uint32_t wp = __shfl_up_sync(0xffffffffu, wk, 1);
+        if (valid && ((lane & 3) == 0 || wp != wk)) atomicOr(&dst[word], acc);
     };
     auto for_each_chunk = [&](auto &&f) {
         for (int e0 = (warp & 1) * 32; e0 < len_w; e0 += 64 * kU) {  // warp-uniform
@@ -162,7 +163,7 @@ union_build_kernel(const int32_t *__restrict__ pos, const int32_t *__restrict__ 
     for_each_chunk([&](int32_t c) {
         const bool valid = c >= 0 && c < n_kv;
         const int b = valid ? c >> 2 : 0;
-        or_lanes(bits, valid, b >> 5, 1u << (b & 31));
+        or_lanes(bits, valid, (uint32_t)(b >> 5), 1u << (b & 31));
     });
     __syncthreads();
 
@@ -219,7 +220,7 @@ union_build_kernel(const int32_t *__restrict__ pos, const int32_t *__restrict__ 
         const int b = valid ? c >> 2 : 0;
         const uint32_t j = base[b >> 5] + __popc(bits[b >> 5] & ((1u << (b & 31)) - 1u));
         const uint32_t k = 4 * j + (uint32_t)(c & 3);
-        or_lanes(mem, valid, (int64_t)li_w * mwords + (k >> 5), 1u << (k & 31));
+        or_lanes(mem, valid, (uint32_t)(li_w * mwords) + (k >> 5), 1u << (k & 31));
     });
     __syncthreads();
     // out in tile-major order: [tile][query][2 words], 64 cells per tile
