@@ -176,3 +176,25 @@ def test_decode_step_gives_up_and_recovers(status):
     (w_out, w_blk), (g_out, g_blk) = _gave_up_then_recovers(run, status, [lay.out, lay.blocks])
     np.testing.assert_array_equal(g_blk, w_blk)
     assert _rows_nan_or_equal(g_out, w_out) == 1.0
+
+
+def test_tensor_core_scores_with_maxima_give_up_and_recover(status):
+    """The score contraction that also writes the group maxima: when it gives up, neither
+    scores nor maxima are stored (both keep the NaN they were filled with); afterwards the
+    normal result, maxima included, comes back bit for bit."""
+    rng = np.random.default_rng(18)
+    n_q, n_rows, H, d = 300, 5000, 16, 128
+    q = to_dev(rng.standard_normal((n_q, H * d)).astype(np.float32))
+    pooled = to_dev(rng.standard_normal((n_rows, H * d)).astype(np.float32))
+    scores = torch.empty(n_q, n_rows, device="cuda")
+    maxima = torch.empty(n_q, (n_rows + 31) // 32, device="cuda")
+    ws = torch.zeros(qsa.index_score_workspace_size(n_q, n_rows, H, d, qsa.QSA_PREC_BF16_TC),
+                     dtype=torch.uint8, device="cuda")
+
+    def run():
+        qsa.index_score_maxima(q, pooled, n_rows, H, d, 1 / math.sqrt(d), scores, maxima,
+                               workspace=ws)
+
+    (w_sc, w_mx), (g_sc, g_mx) = _gave_up_then_recovers(run, status, [scores, maxima])
+    assert np.isnan(g_sc).all() and np.isnan(g_mx).all()
+    assert np.isfinite(w_mx).all()
