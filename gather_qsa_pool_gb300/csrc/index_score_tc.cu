@@ -20,7 +20,9 @@
 //     barrier; the leader's warp 1 issues the MMAs (four per stage) into one of two
 //     256-column accumulators held in both CTAs' tensor memory and frees each stage in both
 //     CTAs with a multicast commit; warps 2-5 of each CTA drain the other accumulator
-//     (tcgen05.ld, scale, causal mask, store) while the next tile computes.  Against one
+//     (tcgen05.ld, scale, causal mask, store: each warp turns its 32 x 32 chunks through
+//     shared memory so that every store writes whole 128-byte lines) while the next tile
+//     computes.  Against one
 //     CTA per M 128 tile this halves the pooled bytes each SM stages per MMA (32 KB a stage
 //     instead of 48 KB), so the same shared memory keeps 1.5 times the MMA time in flight;
 //   - tiles are ordered query-block-fastest, so the pairs working at the same time share a
@@ -46,9 +48,16 @@ constexpr int kTileB = (kBN / 2) * kBK * 2;  // 16 KB: this CTA's 128 pooled row
 constexpr uint32_t kTmemCols = 512;          // two accumulators of 256 columns
 constexpr int kEpiWarps = 4;                 // warps 2-5
 
+// Each epilogue warp's staging buffer: its 32 rows x 32 columns of a chunk, rows padded to
+// 36 floats (16-byte aligned, banks spread), through which the chunk is turned so that every
+// store instruction writes whole 128-byte lines of four rows.
+constexpr int kEpRow = 36;
+constexpr size_t kEpBytes = (size_t)kEpiWarps * 32 * kEpRow * sizeof(float);
+
 __host__ __device__ constexpr size_t tc_smem_bytes()
 {
-    return 1024 /* alignment slack */ + (size_t)kStages * (kTileA + kTileB) + 256;  // + barriers
+    return 1024 /* alignment slack */ + (size_t)kStages * (kTileA + kTileB) + 256 /* barriers */ +
+           kEpBytes;
 }
 
 // 64-bit shared-memory matrix descriptor of a K-major tile in the 128-byte swizzle:
@@ -205,6 +214,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     uint64_t *drain = acce + 2;                            // every MMA issued has finished
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
     uint32_t *peer_issued = tmem_slot + 1;                 // leader: k-steps the peer issued
+    float *ep_buf = reinterpret_cast<float *>(sB + kStages * kTileB + 256);  // [warp][32][36]
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t rank = cluster_rank();  // 0: the leader, which issues the pair's MMAs
@@ -327,6 +337,9 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             const int64_t p = (qi < n_q && q_pos) ? (int64_t)q_pos[qi] : INT64_MAX;
             // blocks complete at position p: b with 4b + 3 <= p
             const int64_t vis_rows = p >= 3 ? (p - 3) / 4 + 1 : 0;
+            // every row of the scores starts on a 16-byte boundary (the transposed stores)
+            const bool rows_vec =
+                ld_scores % 4 == 0 && (reinterpret_cast<uintptr_t>(scores) & 15) == 0;
             // the tile's eight group maxima of this query, shifted in one per chunk (index cc
             // ends in m8[cc]), stored together after the chunks: two 16-byte stores a tile
             float m8[kBN / 32];
@@ -349,39 +362,51 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                       "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
                     : "r"(taddr));
                 asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-                if (qi < n_q) {
-                    float *dst = scores + qi * ld_scores + n0 + cc * 32;
-                    const int64_t b0 = n0 + cc * 32;
-                    // rows b0 + e, e < lim, exist and are visible (4b + 3 <= p); the others
-                    // are -inf (those past n_rows are not stored)
-                    const int64_t lim64 = (vis_rows < n_rows ? vis_rows : n_rows) - b0;
-                    const int lim = lim64 < 0 ? 0 : (lim64 > 32 ? 32 : (int)lim64);
-                    float o[32];
+                const int64_t b0 = n0 + cc * 32;
+                // rows b0 + e, e < lim, exist and are visible (4b + 3 <= p); the others are
+                // -inf (those past n_rows are not stored)
+                const int64_t lim64 = (vis_rows < n_rows ? vis_rows : n_rows) - b0;
+                const int lim = lim64 < 0 ? 0 : (lim64 > 32 ? 32 : (int)lim64);
+                float o[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e)
+                    o[e] = e < lim ? __uint_as_float(v[e]) * scale : -INFINITY;
+                if (gmax) {  // the group's largest visible score
+                    float m16[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) m16[e] = fmaxf(o[e], o[e + 16]);
+#pragma unroll
+                    for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+                        for (int e = 0; e < w; ++e) m16[e] = fmaxf(m16[e], m16[e + w]);
+#pragma unroll
+                    for (int e = 0; e + 1 < kBN / 32; ++e) m8[e] = m8[e + 1];
+                    m8[kBN / 32 - 1] = m16[0];
+                }
+                if (b0 + 32 <= n_rows && rows_vec) {
+                    // a whole chunk (warp-uniform): each lane's row into the warp's buffer,
+                    // then four rows of 32 scores per store instruction (eight lanes a row)
+                    float *buf = ep_buf + (warp - 2) * 32 * kEpRow;
+#pragma unroll
+                    for (int e = 0; e < 32; e += 4)
+                        *reinterpret_cast<float4 *>(buf + lane * kEpRow + e) =
+                            make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
+                    __syncwarp();
+                    const int c4 = (lane & 7) * 4;
+#pragma unroll
+                    for (int pass = 0; pass < 8; ++pass) {
+                        const int rr = pass * 4 + (lane >> 3);
+                        const int64_t qr = m0 + quarter * 32 + rr;
+                        const float4 val = *reinterpret_cast<const float4 *>(buf + rr * kEpRow + c4);
+                        if (qr < n_q)
+                            *reinterpret_cast<float4 *>(scores + qr * ld_scores + b0 + c4) = val;
+                    }
+                    __syncwarp();  // the buffer is rewritten by the next chunk
+                } else if (qi < n_q) {
+                    float *dst = scores + qi * ld_scores + b0;
 #pragma unroll
                     for (int e = 0; e < 32; ++e)
-                        o[e] = e < lim ? __uint_as_float(v[e]) * scale : -INFINITY;
-                    if (gmax) {  // the group's largest visible score
-                        float m16[16];
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) m16[e] = fmaxf(o[e], o[e + 16]);
-#pragma unroll
-                        for (int w = 8; w >= 1; w >>= 1)
-#pragma unroll
-                            for (int e = 0; e < w; ++e) m16[e] = fmaxf(m16[e], m16[e + w]);
-#pragma unroll
-                        for (int e = 0; e + 1 < kBN / 32; ++e) m8[e] = m8[e + 1];
-                        m8[kBN / 32 - 1] = m16[0];
-                    }
-                    if (b0 + 32 <= n_rows && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
-#pragma unroll
-                        for (int e = 0; e < 32; e += 4)
-                            *reinterpret_cast<float4 *>(dst + e) =
-                                make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < 32; ++e)
-                            if (b0 + e < n_rows) dst[e] = o[e];
-                    }
+                        if (b0 + e < n_rows) dst[e] = o[e];
                 }
             }
             if (gmax && qi < n_q) {  // groups n0 / 32 .. + 7 of this query (those that exist)
