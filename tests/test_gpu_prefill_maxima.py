@@ -190,3 +190,42 @@ def test_topk_with_maxima_many_queries_handed_back():
     g_b = to_host(blocks)
     for i in (0, 1, 7, 299):
         np.testing.assert_array_equal(g_b[i], oracle.topk(s[i].astype(np.float64), n_full, k))
+
+
+@pytest.mark.parametrize("n_q,depth", [(130, 3001), (300, 10000)])
+def test_aligned_row_scores_against_oracle(n_q, depth):
+    """Score rows 16 bytes apart (the epilogue's whole-line transposed stores): every score
+    of partial query and row tiles against the oracle's bf16-operand scores, columns past
+    n_rows untouched (n_rows % 4 == 3 and 1 here), and the same scores through a stride
+    that breaks the alignment (the per-lane stores)."""
+    from gpu_helpers import score_tolerance
+    H, d = 16, 128
+    shape = qsa_synth.PrefillShape("tma", depth, n_q, H, d, 8, 2, 128, 256, dtype="bf16")
+    inp = qsa_synth.prefill_inputs(shape, seed=55 + n_q)
+    n_rows = shape.n_rows
+    o_pooled = oracle.pool_rows(inp["raw_k"], shape.n_ctx, H, d, inp["norm_w"], shape.eps,
+                                shape.rope_base, 0, n_rows)
+    scale = 1.0 / math.sqrt(d)
+    ws = torch.zeros(qsa.index_score_workspace_size(n_q, n_rows, H, d, qsa.QSA_PREC_BF16_TC),
+                     dtype=torch.uint8, device="cuda")
+    q, q_pos, pooled = to_dev(inp["q_idx"]), to_dev(inp["q_pos"]), to_dev(o_pooled)
+    ld = (n_rows + 3) // 4 * 4 + 8
+    scores = torch.full((n_q, ld), 7.0, device="cuda")
+    maxima = torch.empty(n_q, (n_rows + 31) // 32, device="cuda")
+    qsa.index_score_maxima(q, pooled, n_rows, H, d, scale, scores, maxima, q_pos=q_pos,
+                           workspace=ws)
+    odd = torch.full((n_q, n_rows + 1), 7.0, device="cuda")
+    qsa.index_score(q, pooled, n_rows, H, d, scale, odd, q_pos=q_pos,
+                    precision=qsa.QSA_PREC_BF16_TC, workspace=ws)
+    got = to_host(scores)
+    assert np.all(got[:, n_rows:] == 7.0)
+    np.testing.assert_array_equal(got[:, :n_rows], to_host(odd)[:, :n_rows])
+    want = oracle.scores(inp["q_idx"], o_pooled, n_rows, H, d, scale, q_pos=inp["q_pos"],
+                         round_bf16_operands=True)
+    qb = np.array([oracle.round_bf16(float(x)) for x in inp["q_idx"].reshape(-1)],
+                  np.float32).reshape(n_q, -1)
+    for i in range(n_q):
+        vis = np.isfinite(want[i])
+        assert np.array_equal(np.isneginf(got[i, :n_rows]), ~vis)
+        tol = score_tolerance(qb[i], o_pooled, n_rows, scale, chain=H * d)[vis]
+        assert np.all(np.abs(got[i, :n_rows][vis] - want[i][vis]) <= tol)
