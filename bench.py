@@ -205,11 +205,13 @@ def traffic_per_launch(path, srcs, n_rows):
 
 # ----------------------------------------------------------------------------- GPU arm
 
-def run_context(name, args, world, rank, local, want_clocks, pooled="f32", n_q=1, light=False):
+def run_context(name, args, world, rank, local, want_clocks, pooled="f32", n_q=1, light=False,
+                winners=False):
     """Decode steps at one context length over ``args.layers`` rotating layer sets.
     pooled: storage of the pooled-key cache ("f32" or "bf16"); n_q: query tokens per step
     (a token and its drafts, each step appending n_q tokens); light: skip the CUDA-graph
-    replay and the end-to-end loop."""
+    replay and the end-to-end loop; winners: scores with clear winners (1% of the completed
+    pooled rows leaning toward the queries' common direction, qsa_synth.clear_winners_torch)."""
     import torch
 
     import gather_qsa_pool_gb300 as qsa
@@ -226,7 +228,7 @@ def run_context(name, args, world, rank, local, want_clocks, pooled="f32", n_q=1
     n_q_pool = 32
     pdt = torch.bfloat16 if pooled == "bf16" else torch.float32
 
-    layers, caches = [], []
+    layers, caches, win_rows = [], [], []
     for li in range(L):
         inp = qsa_synth.decode_inputs_torch(shape, seed=1000 * (rank + 1) + li, device=dev,
                                             extra_tokens=extra, n_steps=n_q_pool)
@@ -236,6 +238,13 @@ def run_context(name, args, world, rank, local, want_clocks, pooled="f32", n_q=1
                               rope_base=shape.rope_base, pooled_dtype=pdt, max_queries=n_q,
                               device=dev)
         lay.rebuild(inp["raw_k"], inp["norm_w"], shape.n_ctx - 1)
+        if winners:
+            cw = qsa_synth.clear_winners_torch((shape.n_ctx - 1) // 4, shape.H_idx * shape.d_idx,
+                                               n_q_pool, seed=77 + 1000 * (rank + 1) + li,
+                                               device=dev)
+            lay.pooled[cw["rows"]] = (lay.pooled[cw["rows"]].float() + cw["add"]).to(pdt)
+            inp["q_idx"] = cw["q_idx"]
+            win_rows.append(cw["rows"])
         if not light:
             lay.enable_host_feed(inp["raw_k"].dtype, inp["K"].dtype)
         lay.bind(inp["raw_k"], inp["norm_w"], inp["K"], inp["V"])
@@ -407,6 +416,11 @@ def run_context(name, args, world, rank, local, want_clocks, pooled="f32", n_q=1
 
     splits = qsa._binding.load()  # noqa: F841  (library already loaded)
     n_cells_last = int(layers[(s - 1) % L].n_cells[0].item())
+    winner_share = None
+    if winners:  # of the blocks the last step selected, the share that are leaning rows
+        lw = layers[(s - 1) % L]
+        sel = lw.blocks[0, :int(lw.counts[0].item())].long()
+        winner_share = float(torch.isin(sel, win_rows[(s - 1) % L]).float().mean().item())
     res = {
         "ms": ms_max, "K": K, "W": W, "score_us": score_us, "score_rows": score_rows,
         "t_e2e": t_e2e, "k_e2e": k_e2e, "host_issue_us": t_issue * 1e6 / K, "h2d": h2d, "d2h": d2h, "clocks": clocks,
@@ -414,6 +428,7 @@ def run_context(name, args, world, rank, local, want_clocks, pooled="f32", n_q=1
         "graph_us": graph_us, "graph_err": graph_err, "pooled": pooled, "n_q": n_q,
         "step_score_us": step_score_us, "step_score_err": step_score_err,
         "step_score_rows": sum((c + n_q - 1 + 3) // 4 for c in n_ctx) / L,
+        "winner_share": winner_share,
     }
     del layers, caches
     torch.cuda.empty_cache()
@@ -905,6 +920,8 @@ def summarize(r, world, layers, peak):
         out["query_tokens_per_s"] = n_q * steps_s
     if r["k_e2e"]:
         out["e2e_steps_per_s"] = world * r["k_e2e"] / r["t_e2e"]
+    if r.get("winner_share") is not None:
+        out["selected_winner_share"] = r["winner_share"]
     if r["graph_us"] is not None:
         out["graph_us_per_step"] = r["graph_us"]
     elif r["graph_err"] and r["graph_err"] != "not run":
@@ -1110,15 +1127,20 @@ def main():
     # and steps carrying a token with two drafts (three queries, one scan).
     variants = {}
     if not args.no_variants:
-        for label, ctx, pooled, n_q in (("bf16_pooled_64k", "64k", "bf16", 1),
-                                        ("bf16_pooled_128k", "128k", "bf16", 1),
-                                        ("bf16_pooled_256k", "256k", "bf16", 1),
-                                        ("three_queries_256k", "256k", "f32", 3),
-                                        ("three_queries_bf16_pooled_256k", "256k", "bf16", 3)):
+        for label, ctx, pooled, n_q, win in (("bf16_pooled_64k", "64k", "bf16", 1, False),
+                                             ("bf16_pooled_128k", "128k", "bf16", 1, False),
+                                             ("bf16_pooled_256k", "256k", "bf16", 1, False),
+                                             ("three_queries_256k", "256k", "f32", 3, False),
+                                             ("three_queries_bf16_pooled_256k", "256k", "bf16", 3,
+                                              False),
+                                             ("clear_winners_256k", "256k", "f32", 1, True)):
             rv = run_context(ctx, args, world, rank, local, want_clocks=False, pooled=pooled,
-                             n_q=n_q, light=True)
+                             n_q=n_q, light=True, winners=win)
             variants[label] = dict(summarize(rv, world, args.layers, peak),
                                    pooled_cache=pooled, queries_per_step=n_q)
+            if win:
+                variants[label]["scores"] = ("1% of the completed pooled rows lean toward the "
+                                             "queries' common direction (+3 sd)")
         if not args.no_prefill:
             variants["prefill_bf16_pooled"] = run_prefill(args, local, "bf16")
             variants["prefill_f32_pooled_bf16_mirror"] = run_prefill(args, local, "f32_mirror")

@@ -253,6 +253,30 @@ def decode_inputs_torch(shape: DecodeShape, seed: int, device, extra_tokens: int
     return {"raw_k": raw, "norm_w": w, "K": K, "V": V, "q_idx": q_idx, "q": q}
 
 
+def clear_winners_torch(n_rows: int, width: int, n_steps: int, seed: int, device,
+                        frac: float = 0.01, sigma: float = 3.0):
+    """A decode workload whose block scores have clear winners (a timing variant).
+
+    The keys' bias cannot be lined up with the queries in the raw keys without the
+    method's own normalisation and rotation, so this draw acts on the completed rows of
+    the pooled-key cache, which a decode step takes as given: a direction u ~ N(0,1)^width,
+    queries N(0,1) + u, and a random ``frac`` of the rows [0, n_rows) receive lean * u with
+    lean = sigma * sqrt(2 / width).  Against rows of unit-variance entries, the raw dot
+    product with such a query has standard deviation sqrt(2 * width) and the lean adds
+    about lean * width = sigma of those deviations to a chosen row.
+    Returns {"q_idx": [n_steps][width], "rows": sorted row indices, "add": [width] the vector
+    to add to each chosen row}."""
+    import torch
+
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    u = torch.randn(width, generator=g, device=device, dtype=torch.float32)
+    q_idx = torch.randn(n_steps, width, generator=g, device=device, dtype=torch.float32) + u
+    n = int(round(frac * n_rows))
+    rows = torch.randperm(n_rows, generator=g, device=device)[:n].sort().values
+    return {"q_idx": q_idx, "rows": rows, "add": (sigma * (2.0 / width) ** 0.5) * u}
+
+
 # --------------------------------------------------------------------------- prefill
 
 def prefill_inputs(shape: PrefillShape, seed: int, n_tok: int | None = None):
