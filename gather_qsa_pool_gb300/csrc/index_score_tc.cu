@@ -25,8 +25,14 @@
 //     computes.  Against one
 //     CTA per M 128 tile this halves the pooled bytes each SM stages per MMA (32 KB a stage
 //     instead of 48 KB), so the same shared memory keeps 1.5 times the MMA time in flight;
-//   - tiles are ordered query-block-fastest, so the pairs working at the same time share a
-//     pooled tile and all but the first read it from L2;
+//   - when the query blocks of 256 pair up, clusters of four CTAs run two pairs on adjacent
+//     query blocks against the same pooled tile: each CTA stages a quarter (64 rows) of the
+//     half its pair position needs and multicasts it into the CTA of the same position in
+//     both pairs, so a pooled tile leaves L2 once per two query blocks (the stage is freed
+//     by both pairs' commits); this cuts the operands each SM pulls from L2 by a quarter,
+//     which is what bounds the contraction once the scores are stored as well;
+//   - tiles are ordered query-block-fastest, so the clusters working at the same time share
+//     a pooled tile and all but the first read it from L2;
 //   - every mbarrier wait is bounded (the pipeline's by the caller's limit, the final ones by
 //     2 s): on a timeout the kernel reports it (qsa_set_wait_options), stops issuing, waits
 //     for what either CTA of the pair already issued, and always returns its tensor memory.
@@ -138,6 +144,19 @@ __device__ __forceinline__ void tma_load_2d_pair(void *dst, const CUtensorMap *m
         : "memory");
 }
 
+// The same load multicast into every CTA of `mask` (the same shared-memory offset in each),
+// each destination's bytes completing on the barrier at bar's offset in the leader of that
+// destination's pair (bar: the issuing CTA's pair leader's barrier, even rank).
+__device__ __forceinline__ void tma_load_2d_pair_mc(void *dst, const CUtensorMap *map, int x,
+                                                    int y, uint32_t bar, uint16_t mask)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::"
+        "bytes.multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "h"(mask)
+        : "memory");
+}
+
 // Remote (or local) arrival on a barrier given by its cluster address.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar)
 {
@@ -194,6 +213,10 @@ rows_to_bf16_kernel(const float4 *__restrict__ src, int64_t n4, uint2 *__restric
     }
 }
 
+// CL: CTAs per cluster.  2: one CTA pair.  4: two pairs working on adjacent query blocks
+// against the same pooled tile, each CTA staging a quarter (64 rows) of the tile's half its
+// pair position needs and multicasting it into both pairs.
+template <int CL>
 __global__ void __launch_bounds__(kTcThreads, 1)
 score_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 int64_t n_q, const int32_t *__restrict__ q_pos, int64_t n_rows, int K,
@@ -213,12 +236,17 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     uint64_t *acce = accf + 2;                             // [2] accumulator drained, leader
     uint64_t *drain = acce + 2;                            // every MMA issued has finished
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
-    uint32_t *peer_issued = tmem_slot + 1;                 // leader: k-steps the peer issued
+    uint32_t *issued_all = tmem_slot + 1;                  // leader: k-steps each CTA issued
     float *ep_buf = reinterpret_cast<float *>(sB + kStages * kTileB + 256);  // [warp][32][36]
 
+    static_assert(CL == 2 || CL == 4, "one pair or two");
+    constexpr int kPairs = CL / 2;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const uint32_t rank = cluster_rank();  // 0: the leader, which issues the pair's MMAs
-    const bool leader = rank == 0;
+    const uint32_t rank = cluster_rank();
+    const uint32_t lrank = rank & ~1u;  // the pair's leader (even rank), which issues its MMAs
+    const bool leader = rank == lrank;
+    const uint32_t half = rank & 1u;    // which 128 queries (and pooled rows) of the pair
+    const uint32_t pq = rank >> 1;      // the pair's place in the cluster
 
     pdl_wait();
     QSA_AFTER_WAIT(q_pos);
@@ -227,7 +255,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
+            mbar_init(&empty[s], kPairs);  // a commit from each pair's MMAs
         }
         for (int j = 0; j < 2; ++j) {
             mbar_init(&accf[j], 1);
@@ -250,24 +278,30 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     const uint32_t tmem = *tmem_slot;
 
+    // unit u: pooled tile u / n_mg against query blocks (u % n_mg) * kPairs + (0 .. kPairs-1),
+    // one per pair (a block past the queries reads zeros and stores nothing)
     const int64_t n_mb = (n_q + 2 * kBM - 1) / (2 * kBM);
+    const int64_t n_mg = (n_mb + kPairs - 1) / kPairs;
     const int64_t n_nb = (n_rows + kBN - 1) / kBN;
-    const int64_t n_units = n_mb * n_nb;
-    const int64_t pair = blockIdx.x >> 1, n_pairs = gridDim.x >> 1;
+    const int64_t n_units = n_mg * n_nb;
+    const int64_t grp = blockIdx.x / CL, n_grp = gridDim.x / CL;
     const int n_k = K / kBK;
     bool ok = true;
     uint32_t issued = 0;  // producer: k-steps whose copies this CTA issued
 
     if (warp == 0) {
-        // ---- producer, in each CTA: its 128 queries and its 128 pooled rows of every stage,
-        // both completing on the leader's barrier of the stage
+        // ---- producer, in each CTA: its 128 queries and its share of the pooled rows of
+        // every stage (with one pair its 128 rows; with two, a quarter of them, multicast
+        // into the CTA of the same half in both pairs), all completing on the barriers of the
+        // pair leaders
         if (lane == 0) {
             // k-step `it` of this CTA's sequence uses stage it % kStages for the
-            // (it / kStages)-th time; both CTAs of the pair run the same sequence
+            // (it / kStages)-th time; every CTA of the cluster runs the same sequence
             uint32_t it = 0;
-            for (int64_t u = pair; u < n_units && ok; u += n_pairs) {
-                const int m0 = (int)((u % n_mb) * (2 * kBM) + rank * kBM);
-                const int n0 = (int)((u / n_mb) * kBN + rank * (kBN / 2));
+            for (int64_t u = grp; u < n_units && ok; u += n_grp) {
+                const int m0 = (int)(((u % n_mg) * kPairs + pq) * (2 * kBM) + half * kBM);
+                const int n0 = (int)((u / n_mg) * kBN + half * (kBN / 2) +
+                                     (CL == 4 ? pq * (kBN / 4) : 0));
                 for (int kb = 0; kb < n_k; ++kb, ++it) {
                     const uint32_t stage = it % kStages, use = it / kStages;
                     if (use > 0 && !mbar_wait(&empty[stage], (use - 1) & 1u, wc.limit_ns)) {
@@ -275,14 +309,20 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                         break;
                     }
                     if (leader) mbar_arrive_expect_tx(&full[stage], 2 * (kTileA + kTileB));
-                    const uint32_t fb = map_to_rank(&full[stage], 0);
+                    const uint32_t fb = map_to_rank(&full[stage], lrank);
                     tma_load_2d_pair(sA + stage * kTileA, &tmA, kb * kBK, m0, fb);
-                    tma_load_2d_pair(sB + stage * kTileB, &tmB, kb * kBK, n0, fb);
+                    if constexpr (CL == 4)
+                        tma_load_2d_pair_mc(sB + stage * kTileB + pq * (kTileB / 2), &tmB,
+                                            kb * kBK, n0, fb, (uint16_t)((1u << half) | (4u << half)));
+                    else
+                        tma_load_2d_pair(sB + stage * kTileB, &tmB, kb * kBK, n0, fb);
                 }
             }
             issued = it;
-            // the peer's count goes to the leader (read there after the cluster barrier below)
-            if (!leader) st_cluster_u32(map_to_rank(peer_issued, 0), it);
+            // this CTA's count goes to every pair leader (read there after the cluster
+            // barrier below)
+#pragma unroll
+            for (int l = 0; l < CL; l += 2) st_cluster_u32(map_to_rank(issued_all + rank, l), it);
         }
     } else if (warp == 1) {
         // ---- MMA issuer: one thread of the leader; accumulators alternate between the two
@@ -291,7 +331,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             constexpr uint32_t idesc = idesc_bf16_m256_n256();
             uint32_t it = 0;
             int64_t t = 0;
-            for (int64_t u = pair; u < n_units && ok; u += n_pairs, ++t) {
+            for (int64_t u = grp; u < n_units && ok; u += n_grp, ++t) {
                 const int j = (int)(t & 1);
                 if (t >= 2 && !mbar_wait(&acce[j], (uint32_t)((t >> 1) - 1) & 1u, wc.limit_ns)) {
                     ok = false;
@@ -311,28 +351,31 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     for (int k16 = 0; k16 < kBK / 16; ++k16)
                         umma_bf16_pair(tmem + (uint32_t)(j * kBN), sw128_desc(a0 + k16 * 32),
                                        sw128_desc(b0 + k16 * 32), idesc, (kb | k16) ? 1u : 0u);
-                    umma_commit_pair(&empty[stage], 0x3);  // the stage is free in both CTAs
+                    // the stage is free (as far as this pair is concerned) in every CTA
+                    umma_commit_pair(&empty[stage], (uint16_t)((1u << CL) - 1u));
                 }
                 if (!ok) break;
-                umma_commit_pair(&accf[j], 0x3);
+                umma_commit_pair(&accf[j], (uint16_t)(3u << lrank));
             }
-            umma_commit_pair(drain, 0x1);
+            umma_commit_pair(drain, (uint16_t)(1u << lrank));
             if (!mbar_wait(drain, 0)) ok = false;
         }
     } else {
         // ---- epilogue, in each CTA: warp w reads tensor-memory lanes 32*(w%4) .. +31 (its
         // queries), then reports the accumulator half drained to the leader
         const int quarter = warp & 3;
-        const uint32_t acce_leader[2] = {map_to_rank(&acce[0], 0), map_to_rank(&acce[1], 0)};
+        const uint32_t acce_leader[2] = {map_to_rank(&acce[0], lrank),
+                                         map_to_rank(&acce[1], lrank)};
         int64_t t = 0;
-        for (int64_t u = pair; u < n_units && ok; u += n_pairs, ++t) {
+        for (int64_t u = grp; u < n_units && ok; u += n_grp, ++t) {
             const int j = (int)(t & 1);
             if (!mbar_wait(&accf[j], (uint32_t)(t >> 1) & 1u, wc.limit_ns)) {
                 ok = false;
                 break;
             }
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-            const int64_t m0 = (u % n_mb) * (2 * kBM) + rank * kBM, n0 = (u / n_mb) * kBN;
+            const int64_t m0 = ((u % n_mg) * kPairs + pq) * (2 * kBM) + half * kBM;
+            const int64_t n0 = (u / n_mg) * kBN;
             const int64_t qi = m0 + quarter * 32 + lane;
             const int64_t p = (qi < n_q && q_pos) ? (int64_t)q_pos[qi] : INT64_MAX;
             // blocks complete at position p: b with 4b + 3 <= p
@@ -428,22 +471,37 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     }
 
     if (!ok) report_timeout(wc);
-    // Every copy either CTA issued completes on the leader's barriers, so the leader sees
-    // them all land before either CTA may leave.  After a wait gave up, the two producers may
-    // have stopped at different k-steps: a phase the leader armed (for both CTAs' bytes) but
-    // the peer never copied into gets the peer's bytes completed by the leader; a phase the
-    // peer copied into but the leader never armed is armed for the peer's bytes alone.  The
-    // producers run at most kStages k-steps apart (each waits for the MMAs to free a stage),
-    // so each stage has at most one such phase, and the phase before it has completed.
-    cluster_sync_all();  // the peer's count is in the leader's shared memory
+    // Every copy lands on the barrier of the leader of the pair it lands in, so each leader
+    // sees all of its pair's bytes land before any CTA of the cluster may leave.  After a wait
+    // gave up, the producers may have stopped at different k-steps: a phase the leader armed
+    // (for the whole stage) gets the bytes of the copies never issued completed by the
+    // leader; a phase copied into but never armed is armed for the bytes that did land.  The
+    // producers run at most kStages k-steps apart (each waits for every pair's MMAs to free
+    // a stage), so each stage has at most one such phase, and the phase before it completed.
+    cluster_sync_all();  // every CTA's count is in each leader's shared memory
     if (warp == 0 && lane == 0 && leader) {
-        const uint32_t L = issued, N = *peer_issued;
-        const uint32_t lo = L < N ? L : N, hi = L < N ? N : L;
+        uint32_t lo = issued, hi = issued;
+        for (int c = 0; c < CL; ++c) {
+            const uint32_t n = issued_all[c];
+            lo = n < lo ? n : lo;
+            hi = n > hi ? n : hi;
+        }
         for (uint32_t x = lo; x < hi; ++x) {
             const uint32_t stage = x % kStages, use = x / kStages;
             if (use > 0) (void)mbar_wait(&full[stage], (use - 1) & 1u);
-            if (x < L) mbar_complete_tx(&full[stage], kTileA + kTileB);
-            else mbar_arrive_expect_tx(&full[stage], kTileA + kTileB);
+            // bytes of k-step x that landed in this pair: each CTA's query tile lands in its
+            // own CTA, its pooled rows in the CTA(s) of its half
+            uint32_t landed = 0;
+            for (int c = 0; c < CL; ++c)
+                if (x < issued_all[c])
+                    landed += ((uint32_t)c >> 1 == pq ? (uint32_t)kTileA : 0u) +
+                              (uint32_t)(kTileB / kPairs);
+            if (x < issued) {
+                if (landed < 2u * (kTileA + kTileB))
+                    mbar_complete_tx(&full[stage], 2u * (kTileA + kTileB) - landed);
+            } else {
+                mbar_arrive_expect_tx(&full[stage], landed);
+            }
         }
         for (uint32_t s = 0; s < kStages; ++s) {
             const uint32_t uses = hi / kStages + (s < hi % kStages ? 1u : 0u);
@@ -509,6 +567,44 @@ size_t index_score_tc_workspace(int64_t n_q, int64_t n_rows, int H, int d, qsa_d
     return al256((size_t)n_q * K * 2) + rows;
 }
 
+// Persistent launch of the score kernel in clusters of CL CTAs: as many clusters as fit on
+// the GPU at once (one CTA per SM), at most one per unit of work.
+template <int CL>
+static cudaError_t launch_score_tc(const CUtensorMap &tmA, const CUtensorMap &tmB, int64_t n_q,
+                                  const int32_t *q_pos, int64_t n_rows, int K, float scale,
+                                  float *scores, int64_t ld_scores, float *gmax, int64_t ld_gmax,
+                                  cudaStream_t st)
+{
+    cudaError_t e = ensure_kernel_attrs<score_tc_kernel<CL>>(tc_smem_bytes());
+    if (e != cudaSuccess) return e;
+    const int64_t n_mb = (n_q + 2 * kBM - 1) / (2 * kBM);
+    const int64_t n_units = ((n_mb + CL / 2 - 1) / (CL / 2)) * ((n_rows + kBN - 1) / kBN);
+    int64_t groups = device_sm_count() / CL;
+    {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)(CL * groups));
+        cfg.blockDim = dim3(kTcThreads);
+        cfg.dynamicSmemBytes = tc_smem_bytes();
+        cudaLaunchAttribute a;
+        a.id = cudaLaunchAttributeClusterDimension;
+        a.val.clusterDim.x = CL;
+        a.val.clusterDim.y = 1;
+        a.val.clusterDim.z = 1;
+        cfg.attrs = &a;
+        cfg.numAttrs = 1;
+        int resident = 0;
+        if (cudaOccupancyMaxActiveClusters(&resident, score_tc_kernel<CL>, &cfg) != cudaSuccess)
+            (void)cudaGetLastError();
+        else if (resident > 0 && resident < groups)
+            groups = resident;
+    }
+    if (groups > n_units) groups = n_units;
+    if (groups < 1) groups = 1;
+    return launch(score_tc_kernel<CL>, dim3((unsigned)(CL * groups)), dim3(kTcThreads),
+                  tc_smem_bytes(), st, CL, tmA, tmB, n_q, q_pos, n_rows, K, scale, scores,
+                  ld_scores, gmax, ld_gmax, current_wait_ctl());
+}
+
 static qsa_status score_tc(const float *q, int64_t n_q, int64_t ld_q, const int32_t *q_pos,
                            const void *pooled, qsa_dtype pdt, int64_t n_rows, int H, int d,
                            float scale, float *scores, int64_t ld_scores, float *gmax,
@@ -528,8 +624,12 @@ static qsa_status score_tc(const float *q, int64_t n_q, int64_t ld_q, const int3
     const __nv_bfloat16 *pb =
         convert_rows ? reinterpret_cast<__nv_bfloat16 *>(ws + al256((size_t)n_q * K * 2))
                      : static_cast<const __nv_bfloat16 *>(pooled);
+    // two CTA pairs share each pooled tile when the query blocks of 256 pair up exactly
+    const int64_t n_mb = (n_q + 2 * kBM - 1) / (2 * kBM);
+    const int cl = n_mb % 2 == 0 ? 4 : 2;
     CUtensorMap tmA, tmB;
-    if (!make_map(&tmA, qb, n_q, K, kBM) || !make_map(&tmB, pb, n_rows, K, kBN / 2))
+    if (!make_map(&tmA, qb, n_q, K, kBM) ||
+        !make_map(&tmB, pb, n_rows, K, cl == 4 ? kBN / 4 : kBN / 2))
         return QSA_ERR_CUDA;
     cudaError_t e = launch(q_to_bf16_kernel, dim3(1024), dim3(256), 0, st, 1, q, n_q, ld_q, K, qb);
     if (e == cudaSuccess && convert_rows) {
@@ -539,33 +639,10 @@ static qsa_status score_tc(const float *q, int64_t n_q, int64_t ld_q, const int3
                    reinterpret_cast<uint2 *>(const_cast<__nv_bfloat16 *>(pb)));
     }
     if (e != cudaSuccess) return QSA_ERR_CUDA;
-    if (ensure_kernel_attrs<score_tc_kernel>(tc_smem_bytes()) != cudaSuccess) return QSA_ERR_CUDA;
-    // CTA pairs (clusters of two), persistent: as many pairs as fit on the GPU at once
-    const int64_t n_units = ((n_q + 2 * kBM - 1) / (2 * kBM)) * ((n_rows + kBN - 1) / kBN);
-    int64_t pairs = device_sm_count() / 2;
-    {
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3((unsigned)(2 * pairs));
-        cfg.blockDim = dim3(kTcThreads);
-        cfg.dynamicSmemBytes = tc_smem_bytes();
-        cudaLaunchAttribute a;
-        a.id = cudaLaunchAttributeClusterDimension;
-        a.val.clusterDim.x = 2;
-        a.val.clusterDim.y = 1;
-        a.val.clusterDim.z = 1;
-        cfg.attrs = &a;
-        cfg.numAttrs = 1;
-        int resident = 0;
-        if (cudaOccupancyMaxActiveClusters(&resident, score_tc_kernel, &cfg) != cudaSuccess)
-            (void)cudaGetLastError();
-        else if (resident > 0 && resident < pairs)
-            pairs = resident;
-    }
-    if (pairs > n_units) pairs = n_units;
-    if (pairs < 1) pairs = 1;
-    e = launch(score_tc_kernel, dim3((unsigned)(2 * pairs)), dim3(kTcThreads), tc_smem_bytes(), st,
-               2, tmA, tmB, n_q, q_pos, n_rows, K, scale, scores, ld_scores, gmax, ld_gmax,
-               current_wait_ctl());
+    e = cl == 4 ? launch_score_tc<4>(tmA, tmB, n_q, q_pos, n_rows, K, scale, scores, ld_scores,
+                                     gmax, ld_gmax, st)
+                : launch_score_tc<2>(tmA, tmB, n_q, q_pos, n_rows, K, scale, scores, ld_scores,
+                                     gmax, ld_gmax, st);
     return e == cudaSuccess ? QSA_OK : QSA_ERR_CUDA;
 }
 

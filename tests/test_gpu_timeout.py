@@ -136,11 +136,13 @@ def test_latent_mask_attention_gives_up_and_recovers(status):
     assert _rows_nan_or_equal(g_out, w_out) == 1.0
 
 
-def test_tensor_core_scores_give_up_and_recover(status):
-    """The CTA-pair tcgen05 score contraction: no tile is stored, so every score keeps the
-    NaN it was filled with."""
+@pytest.mark.parametrize("n_q", [512, 200])
+def test_tensor_core_scores_give_up_and_recover(status, n_q):
+    """The tcgen05 score contraction, in clusters of two CTA pairs sharing each pooled tile
+    (512 queries: two query blocks of 256) and of one pair (200 queries): no tile is stored,
+    so every score keeps the NaN it was filled with."""
     rng = np.random.default_rng(16)
-    n_q, n_rows, H, d = 512, 6000, 16, 128
+    n_rows, H, d = 6000, 16, 128
     q = to_dev(rng.standard_normal((n_q, H * d)).astype(np.float32))
     pooled = to_dev(rng.standard_normal((n_rows, H * d)).astype(np.float32))
     scores = torch.empty(n_q, n_rows, device="cuda")
