@@ -214,8 +214,8 @@ rows_to_bf16_kernel(const float4 *__restrict__ src, int64_t n4, uint2 *__restric
 }
 
 // CL: CTAs per cluster.  2: one CTA pair.  4: two pairs working on adjacent query blocks
-// against the same pooled tile, each CTA staging a quarter (64 rows) of the tile's half its
-// pair position needs and multicasting it into both pairs.
+// against the same pooled tile, each CTA staging a 1/(CL/2) share (64 rows) of the tile's
+// half its pair position needs and multicasting it into every pair.
 template <int CL>
 __global__ void __launch_bounds__(kTcThreads, 1)
 score_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -300,8 +300,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             uint32_t it = 0;
             for (int64_t u = grp; u < n_units && ok; u += n_grp) {
                 const int m0 = (int)(((u % n_mg) * kPairs + pq) * (2 * kBM) + half * kBM);
-                const int n0 = (int)((u / n_mg) * kBN + half * (kBN / 2) +
-                                     (CL == 4 ? pq * (kBN / 4) : 0));
+                const int n0 = (int)((u / n_mg) * kBN + half * (kBN / 2) + pq * (kBN / CL));
                 for (int kb = 0; kb < n_k; ++kb, ++it) {
                     const uint32_t stage = it % kStages, use = it / kStages;
                     if (use > 0 && !mbar_wait(&empty[stage], (use - 1) & 1u, wc.limit_ns)) {
@@ -311,9 +310,10 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     if (leader) mbar_arrive_expect_tx(&full[stage], 2 * (kTileA + kTileB));
                     const uint32_t fb = map_to_rank(&full[stage], lrank);
                     tma_load_2d_pair(sA + stage * kTileA, &tmA, kb * kBK, m0, fb);
-                    if constexpr (CL == 4)
-                        tma_load_2d_pair_mc(sB + stage * kTileB + pq * (kTileB / 2), &tmB,
-                                            kb * kBK, n0, fb, (uint16_t)((1u << half) | (4u << half)));
+                    if constexpr (CL > 2)
+                        tma_load_2d_pair_mc(sB + stage * kTileB + pq * (kTileB / kPairs), &tmB,
+                                            kb * kBK, n0, fb,
+                                            (uint16_t)((0x5555u & ((1u << CL) - 1u)) << half));
                     else
                         tma_load_2d_pair(sB + stage * kTileB, &tmB, kb * kBK, n0, fb);
                 }
@@ -628,8 +628,7 @@ static qsa_status score_tc(const float *q, int64_t n_q, int64_t ld_q, const int3
     const int64_t n_mb = (n_q + 2 * kBM - 1) / (2 * kBM);
     const int cl = n_mb % 2 == 0 ? 4 : 2;
     CUtensorMap tmA, tmB;
-    if (!make_map(&tmA, qb, n_q, K, kBM) ||
-        !make_map(&tmB, pb, n_rows, K, cl == 4 ? kBN / 4 : kBN / 2))
+    if (!make_map(&tmA, qb, n_q, K, kBM) || !make_map(&tmB, pb, n_rows, K, (uint32_t)(kBN / cl)))
         return QSA_ERR_CUDA;
     cudaError_t e = launch(q_to_bf16_kernel, dim3(1024), dim3(256), 0, st, 1, q, n_q, ld_q, K, qb);
     if (e == cudaSuccess && convert_rows) {
