@@ -116,6 +116,56 @@ def test_decode_61789_tokens_full_oracle():
             assert n_band > 0
 
 
+def test_decode_clear_winners_61789_full_oracle():
+    """Scores with clear winners (the benchmark's clear-winners workload: 1% of the completed
+    pooled rows leaning toward the queries' common direction, about three standard
+    deviations up), over two appending steps at 61,789 tokens: the step takes the leaned
+    cache as given (the same rows on both sides), and every score, the histogram-fed
+    selection on these peaked rows (against the oracle's scores, tie band), the cell list
+    and the attention output are compared with the oracle; most of the selection must be
+    leaning rows, or the workload would not be peaked."""
+    shape = qsa_synth.CONFIGS["decode_64k"]
+    steps = 2
+    inp = qsa_synth.decode_inputs(shape, seed=64, extra_tokens=steps, n_steps=steps)
+    H, d = shape.H_idx, shape.d_idx
+    raw, w, K, V = (to_dev(inp["raw_k"]), to_dev(inp["norm_w"]), to_dev(inp["K"]),
+                    to_dev(inp["V"]))
+    n0 = shape.n_ctx - 1
+    o_valid = n0 // 4
+    cw = qsa_synth.clear_winners_torch(o_valid, H * d, steps, seed=65, device="cpu")
+    q_idx = cw["q_idx"].numpy()
+    lean_rows = cw["rows"].numpy()
+    lay = _layer(shape, steps)
+    lay.rebuild(raw, w, n0)
+    o_pooled = np.zeros((lay.cap_rows, H * d), np.float32)
+    oracle.pool_rows(inp["raw_k"], n0, H, d, inp["norm_w"], shape.eps, shape.rope_base, 0,
+                     (n0 + 3) // 4, o_pooled)
+    o_pooled[lean_rows] += cw["add"].numpy()
+    lay.pooled[:o_valid].copy_(torch.from_numpy(o_pooled[:o_valid]))
+    for s in range(steps):
+        n_ctx = n0 + 1 + s
+        out = lay.step(raw, w, K, V, n_ctx, to_dev(q_idx[s]), to_dev(inp["q"][s]))
+        blocks, cells, o_out, _, o_scores = oracle.decode_step(
+            inp["raw_k"], n_ctx, H, d, inp["norm_w"], shape.eps, shape.rope_base, o_pooled,
+            o_valid, q_idx[s], shape.top_k_tokens, inp["q"][s], inp["K"], inp["V"],
+            shape.H_q, shape.H_kv, shape.d)
+        o_valid = n_ctx // 4
+        n_rows = (n_ctx + 3) // 4
+        g_scores = to_host(lay.scores)[:n_rows]
+        tol = score_tolerance(q_idx[s], o_pooled, n_rows, 1.0 / math.sqrt(d))
+        assert np.all(np.abs(g_scores - o_scores) <= tol)
+        g_count = int(to_host(lay.counts)[0])
+        g_blocks = to_host(lay.blocks)[0]
+        n_band = check_topk(g_blocks, g_count, o_scores, n_ctx // 4, shape.k_blk)
+        assert np.isin(g_blocks[:g_count], lean_rows).mean() > 0.5
+        if np.array_equal(g_blocks[:g_count], blocks):
+            nc = int(to_host(lay.n_cells)[0])
+            np.testing.assert_array_equal(to_host(lay.pos)[0, :nc], cells)
+            np.testing.assert_allclose(to_host(out)[0], o_out, rtol=0, atol=ATOL_ATTN_BF16)
+        else:
+            assert n_band > 0
+
+
 @pytest.mark.parametrize("name", ["decode_128k", "decode_256k"])
 def test_decode_appending_256_steps_full_oracle(name):
     """The decode sweep at 126,253 and 255,181 tokens: 256 consecutive steps, each appending
