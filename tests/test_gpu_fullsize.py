@@ -122,8 +122,9 @@ def test_decode_clear_winners_61789_full_oracle():
     deviations up), over two appending steps at 61,789 tokens: the step takes the leaned
     cache as given (the same rows on both sides), and every score, the histogram-fed
     selection on these peaked rows (against the oracle's scores, tie band), the cell list
-    and the attention output are compared with the oracle; most of the selection must be
-    leaning rows, or the workload would not be peaked."""
+    and the attention output are compared with the oracle; most leaning rows must be
+    selected (with scores of no preference a row is selected with probability k / n, 3%
+    here), or the workload would not be peaked."""
     shape = qsa_synth.CONFIGS["decode_64k"]
     steps = 2
     inp = qsa_synth.decode_inputs(shape, seed=64, extra_tokens=steps, n_steps=steps)
@@ -157,7 +158,7 @@ def test_decode_clear_winners_61789_full_oracle():
         g_count = int(to_host(lay.counts)[0])
         g_blocks = to_host(lay.blocks)[0]
         n_band = check_topk(g_blocks, g_count, o_scores, n_ctx // 4, shape.k_blk)
-        assert np.isin(g_blocks[:g_count], lean_rows).mean() > 0.5
+        assert np.isin(lean_rows, g_blocks[:g_count]).mean() > 0.6
         if np.array_equal(g_blocks[:g_count], blocks):
             nc = int(to_host(lay.n_cells)[0])
             np.testing.assert_array_equal(to_host(lay.pos)[0, :nc], cells)
