@@ -39,7 +39,7 @@ constexpr int kRStageElems = kRGroups * kRGroupElems;     // one tensor's stage
 constexpr size_t kRStageBytes = (size_t)kRStageElems * 2;
 constexpr int kRMaxList = 4096;        // the query's whole position list stays in shared memory
 constexpr size_t kRSmem = 2 * kRStages * kRStageBytes + (size_t)kRMaxList * 4;
-static_assert((size_t)kRWarps * kRG * (kRD + 2) * 4 <= 2 * kRStages * kRStageBytes,
+static_assert((size_t)kRHkv * kRG * (kRD + 2) * 4 <= 2 * kRStages * kRStageBytes,
               "merge area fits the stages");
 static_assert(kRMaxList % kRNT == 0, "the list is read in whole rounds");
 
@@ -55,7 +55,7 @@ attn_rows4_kernel(const float *__restrict__ q, int H_q, float scale_log2,
     extern __shared__ __align__(16) char smem_raw[];
     __nv_bfloat16 *Ks = reinterpret_cast<__nv_bfloat16 *>(smem_raw);       // [NS][8][GE]
     __nv_bfloat16 *Vs = Ks + (size_t)NS * SE;                               // [NS][8][GE]
-    float *mrg = reinterpret_cast<float *>(smem_raw);  // [warps][G][D + 2], after the loop
+    float *mrg = reinterpret_cast<float *>(smem_raw);  // [KV heads][G][D + 2], after the loop
     int32_t *plist_s = reinterpret_cast<int32_t *>(smem_raw + 2 * NS * kRStageBytes);  // [4096]
     __shared__ __align__(8) uint64_t full[NS];
     __shared__ __align__(8) uint64_t empty[NS];
@@ -270,45 +270,58 @@ attn_rows4_kernel(const float *__restrict__ q, int H_q, float scale_log2,
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);  // this warp is done with the stage
         }
-        // per-warp state, kept in registers until every warp has left the ring
+        // per-warp state, kept in registers until every warp has left the ring; the second
+        // warp of each KV head leaves its state in shared memory, the first merges it with
+        // its own in registers and writes the head group's outputs
         __syncthreads();
         float l4 = lsum;
         l4 += __shfl_xor_sync(0xffffffffu, l4, 1);
         l4 += __shfl_xor_sync(0xffffffffu, l4, 2);
-        float *mw = mrg + ((size_t)warp * G + hr) * (D + 2);
+        float *mw = mrg + ((size_t)g * G + hr) * (D + 2);
+        if (half == 1) {
 #pragma unroll
-        for (int jj = 0; jj < 16; ++jj) {
-            mw[8 * jj + qc] = o[jj][0] + o[jj][2];
-            mw[8 * jj + qc + 1] = o[jj][1] + o[jj][3];
+            for (int jj = 0; jj < 16; ++jj) {
+                mw[8 * jj + qc] = o[jj][0] + o[jj][2];
+                mw[8 * jj + qc + 1] = o[jj][1] + o[jj][3];
+            }
+            if ((lane & 3) == 0) {
+                mw[D] = m;
+                mw[D + 1] = l4;
+            }
         }
-        if ((lane & 3) == 0) {
-            mw[D] = m;
-            mw[D + 1] = l4;
+        lost = __syncthreads_or(lost);  // also orders those writes before the reads below
+        if (half == 0) {
+            const float m1 = mw[D], l1 = mw[D + 1];
+            const float M = fmaxf(m, m1);
+            float f0 = 0.0f, f1 = 0.0f, L = 0.0f;
+            if (M != -INFINITY) {
+                f0 = exp2f(m - M);
+                f1 = exp2f(m1 - M);
+                L = fmaf(f0, l4, f1 * l1);
+            }
+            const int64_t hq = qi * H_q + (int64_t)g * G + hr;
+            float *orow = out + hq * D;
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) {
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const float r0 = o[jj][u] + o[jj][u + 2];
+                    const float acc =
+                        M != -INFINITY ? fmaf(f0, r0, f1 * mw[8 * jj + qc + u]) : 0.0f;
+                    float v = L > 0.0f ? acc / L : 0.0f;
+                    if (overflow || lost) v = __int_as_float(0x7fc00000);
+                    orow[8 * jj + qc + u] = v;
+                }
+            }
+            if (lse && (lane & 3) == 0)
+                lse[hq] = (overflow || lost) ? __int_as_float(0x7fc00000)
+                          : (L > 0.0f ? (M + log2f(L)) * kLn2 : -INFINITY);
         }
     }
-    if (warp == kRWarps) __syncthreads();  // pairs with the consumers' barrier above
-    lost = __syncthreads_or(lost);
-    if (lost && tid == 0) report_timeout(wc);
-
-    // the two warps of each KV head merge into the output
-    for (int e = tid; e < kRHkv * G * D; e += kRThreads) {
-        const int hq = e / D, c = e - hq * D;  // query head of this query, dim
-        const int gg = hq / G, h = hq - gg * G;
-        const float *r0 = mrg + ((size_t)(2 * gg) * G + h) * (D + 2);
-        const float *r1 = mrg + ((size_t)(2 * gg + 1) * G + h) * (D + 2);
-        const float M = fmaxf(r0[D], r1[D]);
-        float acc = 0.0f, L = 0.0f;
-        if (M != -INFINITY) {
-            const float f0 = exp2f(r0[D] - M), f1 = exp2f(r1[D] - M);
-            acc = fmaf(f0, r0[c], f1 * r1[c]);
-            L = fmaf(f0, r0[D + 1], f1 * r1[D + 1]);
-        }
-        float v = L > 0.0f ? acc / L : 0.0f;
-        if (overflow || lost) v = __int_as_float(0x7fc00000);
-        out[(qi * H_q + hq) * (int64_t)D + c] = v;
-        if (lse && c == 0)
-            lse[qi * H_q + hq] = (overflow || lost) ? __int_as_float(0x7fc00000)
-                                 : (L > 0.0f ? (M + log2f(L)) * kLn2 : -INFINITY);
+    if (warp == kRWarps) {
+        __syncthreads();                // pairs with the consumers' two barriers above
+        lost = __syncthreads_or(lost);
+        if (lost && lane == 0) report_timeout(wc);
     }
 }
 
