@@ -22,9 +22,9 @@
 //     CTAs with a multicast commit; warps 2-5 of each CTA drain the other accumulator
 //     (tcgen05.ld, scale, causal mask, store: each warp turns its 32 x 32 chunks through
 //     shared memory so that every store writes whole 128-byte lines) while the next tile
-//     computes.  Against one
-//     CTA per M 128 tile this halves the pooled bytes each SM stages per MMA (32 KB a stage
-//     instead of 48 KB), so the same shared memory keeps 1.5 times the MMA time in flight;
+//     computes.  Against one CTA per M 128 tile this halves the pooled bytes each SM stages
+//     per MMA (32 KB a stage instead of 48 KB), so the same shared memory keeps 1.5 times
+//     the MMA time in flight;
 //   - when the query blocks of 256 pair up, clusters of four CTAs run two pairs on adjacent
 //     query blocks against the same pooled tile: each CTA stages a quarter (64 rows) of the
 //     half its pair position needs and multicasts it into the CTA of the same position in
@@ -35,7 +35,8 @@
 //     a pooled tile and all but the first read it from L2;
 //   - every mbarrier wait is bounded (the pipeline's by the caller's limit, the final ones by
 //     2 s): on a timeout the kernel reports it (qsa_set_wait_options), stops issuing, waits
-//     for what either CTA of the pair already issued, and always returns its tensor memory.
+//     for what every CTA of the cluster already issued, and always returns its tensor
+//     memory.
 #include <cuda.h>
 
 #include "prefill_select.cuh"
