@@ -184,19 +184,28 @@ __device__ __forceinline__ uint32_t bf16x2(float lo, float hi)
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
-// Prologue: q (fp32, row stride ld_q) -> bf16 rows of K elements, nearest even.
+// Prologue: q (fp32, row stride ld_q) -> bf16 rows of K elements, nearest even.  One CTA
+// per row at a time; four elements per thread and step when every row starts on a 16-byte
+// boundary (vec), else one.
 __global__ void __launch_bounds__(256)
 q_to_bf16_kernel(const float *__restrict__ q, int64_t n_q, int64_t ld_q, int K,
-                 __nv_bfloat16 *__restrict__ qb)
+                 __nv_bfloat16 *__restrict__ qb, int vec)
 {
     pdl_wait();
     QSA_AFTER_WAIT(q);
     pdl_trigger();
-    const int64_t total = n_q * (int64_t)K;
-    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
-         e += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t i = e / K, k = e - i * K;
-        qb[e] = __float2bfloat16_rn(q[i * ld_q + k]);
+    for (int64_t i = blockIdx.x; i < n_q; i += gridDim.x) {
+        const float *src = q + i * ld_q;
+        __nv_bfloat16 *dst = qb + i * (int64_t)K;
+        if (vec) {
+            for (int k4 = threadIdx.x; k4 < K / 4; k4 += blockDim.x) {
+                const float4 v = reinterpret_cast<const float4 *>(src)[k4];
+                reinterpret_cast<uint2 *>(dst)[k4] =
+                    make_uint2(bf16x2(v.x, v.y), bf16x2(v.z, v.w));
+            }
+        } else {
+            for (int k = threadIdx.x; k < K; k += blockDim.x) dst[k] = __float2bfloat16_rn(src[k]);
+        }
     }
 }
 
@@ -631,7 +640,10 @@ static qsa_status score_tc(const float *q, int64_t n_q, int64_t ld_q, const int3
     CUtensorMap tmA, tmB;
     if (!make_map(&tmA, qb, n_q, K, kBM) || !make_map(&tmB, pb, n_rows, K, (uint32_t)(kBN / cl)))
         return QSA_ERR_CUDA;
-    cudaError_t e = launch(q_to_bf16_kernel, dim3(1024), dim3(256), 0, st, 1, q, n_q, ld_q, K, qb);
+    const int qvec = ld_q % 4 == 0 && (reinterpret_cast<uintptr_t>(q) & 15) == 0;
+    const int64_t qgrid = n_q < (int64_t)device_sm_count() * 8 ? n_q : (int64_t)device_sm_count() * 8;
+    cudaError_t e = launch(q_to_bf16_kernel, dim3((unsigned)qgrid), dim3(256), 0, st, 1, q, n_q,
+                           ld_q, K, qb, qvec);
     if (e == cudaSuccess && convert_rows) {
         const int64_t n4 = n_rows * (int64_t)K / 4;
         e = launch(rows_to_bf16_kernel, dim3((unsigned)(device_sm_count() * 8)), dim3(256), 0, st,

@@ -229,3 +229,27 @@ def test_aligned_row_scores_against_oracle(n_q, depth):
         assert np.array_equal(np.isneginf(got[i, :n_rows]), ~vis)
         tol = score_tolerance(qb[i], o_pooled, n_rows, scale, chain=H * d)[vis]
         assert np.all(np.abs(got[i, :n_rows][vis] - want[i][vis]) <= tol)
+
+
+@pytest.mark.parametrize("pad,shift", [(1, 0), (3, 1)])
+def test_tensor_core_scores_with_strided_queries(pad, shift):
+    """Query rows whose starts are not all on a 16-byte boundary (a row stride of H*d + 1,
+    or rows of H*d + 4 starting one float in) are rounded to bf16 element by element: the
+    tensor-core scores equal those of the contiguous queries bit for bit."""
+    H, d, n_q, n_rows = 16, 128, 130, 700
+    rng = np.random.default_rng(70 + pad)
+    qh = rng.standard_normal((n_q, H * d)).astype(np.float32)
+    pooled = to_dev(rng.standard_normal((n_rows, H * d)).astype(np.float32))
+    ws = torch.zeros(qsa.index_score_workspace_size(n_q, n_rows, H, d, qsa.QSA_PREC_BF16_TC),
+                     dtype=torch.uint8, device="cuda")
+    q = to_dev(qh)
+    big = torch.zeros(n_q, H * d + pad + shift, device="cuda")
+    big[:, shift:shift + H * d] = q
+    qs = big[:, shift:shift + H * d]
+    want = torch.empty(n_q, n_rows, device="cuda")
+    got = torch.empty(n_q, n_rows, device="cuda")
+    qsa.index_score(q, pooled, n_rows, H, d, 0.125, want, precision=qsa.QSA_PREC_BF16_TC,
+                    workspace=ws)
+    qsa.index_score(qs, pooled, n_rows, H, d, 0.125, got, precision=qsa.QSA_PREC_BF16_TC,
+                    workspace=ws)
+    np.testing.assert_array_equal(to_host(got), to_host(want))
