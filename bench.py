@@ -1087,12 +1087,12 @@ def main():
         rank = int(os.environ.get("RANK", "0"))
         if rank != 0:
             return
-        # W untimed warm-up steps (at least three), then up to K timed ones on the same
-        # appending context, bounded to ~90 s
+        # W untimed warm-up steps (at least three; bounded to ~30 s), then up to K timed
+        # ones on the same appending context, bounded to ~90 s
         W = max(args.warmup, 3)
         K = max(1, args.steps)
         inp, pooled = oracle_prepare(primary, W + K)
-        oracle_steps(primary, inp, pooled, W, budget_s=float("inf"))
+        W, _ = oracle_steps(primary, inp, pooled, W, budget_s=30.0)
         n_done, t = oracle_steps(primary, inp, pooled, K, budget_s=90.0, first_q=W, start=W)
         steps = n_done
         value = n_done / t
