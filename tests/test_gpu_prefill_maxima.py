@@ -192,7 +192,7 @@ def test_topk_with_maxima_many_queries_handed_back():
         np.testing.assert_array_equal(g_b[i], oracle.topk(s[i].astype(np.float64), n_full, k))
 
 
-@pytest.mark.parametrize("n_q,depth", [(130, 3001), (300, 10000)])
+@pytest.mark.parametrize("n_q,depth", [(130, 3001), (300, 10000), (600, 6003), (1000, 5002)])
 def test_aligned_row_scores_against_oracle(n_q, depth):
     """Score rows 16 bytes apart (the epilogue's whole-line transposed stores): every score
     of partial query and row tiles against the oracle's bf16-operand scores, columns past
