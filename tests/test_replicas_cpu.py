@@ -75,3 +75,7 @@ def test_reference_arm_rank0_prints_one_line():
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["unit"] == "steps/s"
     assert d["value"] > 0 and d["cpu_baseline"]["kind"] == "oracle"
     assert d["e2e"]["h2d_bytes_per_step"] == 0
+    # at least three untimed warm-up steps even when fewer are asked for; the value and the
+    # time per step cover the timed steps only
+    assert d["warmup"] >= 3 and d["steps"] == 1
+    assert abs(d["value"] * d["ms_per_step"] - 1e3) < 1e-6 * 1e3
