@@ -192,11 +192,14 @@ def test_topk_with_maxima_many_queries_handed_back():
         np.testing.assert_array_equal(g_b[i], oracle.topk(s[i].astype(np.float64), n_full, k))
 
 
-@pytest.mark.parametrize("n_q,depth", [(130, 3001), (300, 10000), (600, 6003), (1000, 5002)])
+@pytest.mark.parametrize("n_q,depth", [(130, 3001), (300, 10000), (600, 6003), (1000, 5002),
+                                       (512, 17), (1, 900), (257, 1000)])
 def test_aligned_row_scores_against_oracle(n_q, depth):
     """Score rows 16 bytes apart (the epilogue's whole-line transposed stores): every score
-    of partial query and row tiles against the oracle's bf16-operand scores, columns past
-    n_rows untouched (n_rows % 4 == 3 and 1 here), and the same scores through a stride
+    of partial query and row tiles against the oracle's bf16-operand scores (one query; a
+    second pair of 256 queries holding one live row; a context shorter than one row tile),
+    columns past n_rows untouched (n_rows % 4 == 3 and 1 among them), and the same scores
+    through a stride
     that breaks the alignment (the per-lane stores)."""
     from gpu_helpers import score_tolerance
     H, d = 16, 128
