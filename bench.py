@@ -742,8 +742,10 @@ def run_ablation(args, local):
     """The pages' A/B on this GPU at 255,181 tokens: each piece of the QSA decode step next
     to the piece it replaced -- the full pooled-cache rebuild (before the incremental cache),
     the block score expanded to cells and a cell-level top-k (before the block-domain
-    top-k), attention over every cell of the context (before the selected-K/V gather).
-    CUDA events over a few repetitions after a warm-up call; returns microseconds."""
+    top-k), attention over every cell of the context (before the selected-K/V gather) -- and
+    the gather itself as the pages run it (the listed K/V rows copied into a compact buffer,
+    then attention over that buffer), which the decode step replaces by reading the rows in
+    place.  CUDA events over a few repetitions after a warm-up call; returns microseconds."""
     import torch
 
     import gather_qsa_pool_gb300 as qsa
@@ -772,6 +774,11 @@ def run_ablation(args, local):
     ws = torch.zeros(max(qsa.sparse_attn_workspace_size(1, shape.H_q, shape.H_kv, shape.d, n_ctx)
                          // 4, 1), device=dev)
     scale_idx, scale = 1.0 / math.sqrt(d), 1.0 / math.sqrt(shape.d)
+    mc = lay.max_cells
+    Kc = torch.empty(mc, shape.H_kv, shape.d, dtype=K.dtype, device=dev)
+    Vc = torch.empty(mc, shape.H_kv, shape.d, dtype=V.dtype, device=dev)
+    g_pos = torch.empty(1, mc, dtype=torch.int32, device=dev)
+    g_n = torch.empty(1, dtype=torch.int32, device=dev)
     pieces = [
         ("pool_full_rebuild", lambda: qsa.pool_update(raw, n_ctx, H, d, w, shape.eps,
                                                       shape.rope_base, lay.pooled, 0)),
@@ -787,11 +794,19 @@ def run_ablation(args, local):
                                                       pos=lay.pos[:1], workspace=lay.workspace)),
         ("attn_full_kv", lambda: qsa.sparse_attn(q, K, V, all_n, n_ctx, out, shape.H_kv, shape.d,
                                                  shape.d, scale, pos=all_pos, workspace=ws)),
+        ("gather_rows", lambda: qsa.gather_kv(blocks, counts, k_blk, g_pos, g_n, mc, n_ctx=n_ctx,
+                                              K=K, V=V, K_out=Kc, V_out=Vc, H_kv=shape.H_kv,
+                                              d_k=shape.d, d_v=shape.d)),
+        ("attn_gathered_rows", lambda: qsa.sparse_attn(q, Kc, Vc, g_n, mc, out, shape.H_kv,
+                                                       shape.d, shape.d, scale,
+                                                       workspace=lay.workspace)),
     ]
     # each piece captured (reps calls) into a CUDA graph and replayed, so the device time is
     # measured rather than the Python wrapper's issue time
     res = {name: round(graph_time_us([fn], 5, dev), 1) for name, fn in pieces}
     n_listed = int(lay.n_cells[0].item())
+    n_gathered = int(g_n[0].item())
+    gather_bytes = 2 * n_gathered * shape.H_kv * shape.d * K.element_size() * 2  # read + write
     out_d = {
         "workload": (f"one layer at {n_ctx:,} tokens: {n_rows:,} pooled rows, {n_listed} listed "
                      f"cells of {n_ctx:,}"),
@@ -800,11 +815,16 @@ def run_ablation(args, local):
                              + res["cell_topk"] + res["attn_full_kv"], 1),
         "qsa_pieces_us": round(res["pool_incremental"] + res["score_scan"] + res["block_topk"]
                                + res["attn_listed_cells"], 1),
+        "gather_rows_GBps": round(gather_bytes / res["gather_rows"] / 1e3, 1),
+        "gather_then_attend_us": round(res["gather_rows"] + res["attn_gathered_rows"], 1),
         "note": ("pieces timed one at a time from CUDA-graph replays (the fused decode step "
                  "overlaps them and uses the histogram-fed top-k); the old path is the sum of "
-                 "the pieces it ran"),
+                 "the pieces it ran; gather_rows copies the selected blocks' K and V rows (and "
+                 "the open tail) into a compact buffer, gather_then_attend_us adds the "
+                 "attention over that buffer, against attn_listed_cells reading the rows in "
+                 "place"),
     }
-    del lay, inp, cells, ws
+    del lay, inp, cells, ws, Kc, Vc
     torch.cuda.empty_cache()
     return out_d
 
