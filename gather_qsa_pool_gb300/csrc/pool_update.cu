@@ -50,6 +50,79 @@ pool_update_kernel(const T *__restrict__ raw, int64_t n_ctx, int H, int d,
              pooled + b * (int64_t)(H * d));
 }
 
+// Many rows (a rebuild, a prefill chunk's new rows): one warp per row, the row's H*D values
+// in registers -- value e (of the row's H*D) on lane e % 32 as value e / 32 -- so no shared
+// memory or block barrier is needed and a CTA's eight rows are in flight together.  Every
+// value is formed as in pool_row, in the same order (the 4-token mean; per head the sum of
+// squares over values lane, lane + 32, ... then the warp reduction; the rotation of the
+// pair (i, i + D/2), both on one lane), so the two forms write the same bits.
+constexpr int kWarpRowThreads = 256;
+
+template <typename T, typename TP, int D, int NH>
+__global__ void __launch_bounds__(kWarpRowThreads)
+pool_rows_warp_kernel(const T *__restrict__ raw, int64_t n_ctx, const float *__restrict__ w,
+                      float eps, const RopeTable tab, TP *__restrict__ pooled, int64_t row0,
+                      int64_t row1, uint32_t *__restrict__ zero_hist)
+{
+    constexpr int HD = NH * D, PER = HD / 32, PH = D / 32, HALF = D / 2, MH = HALF / 32;
+    static_assert(D % 64 == 0 && PER <= 64, "two rotation partners per lane, <= 64 values");
+    pdl_wait();
+    QSA_AFTER_WAIT(raw);
+    QSA_AFTER_WAIT(w);
+    pdl_trigger();
+    if (zero_hist && blockIdx.x == 0)
+        for (int i = threadIdx.x; i < (1 << kTopkHistBits); i += kWarpRowThreads) zero_hist[i] = 0u;
+    const int lane = threadIdx.x & 31;
+    const int64_t b = row0 + (int64_t)blockIdx.x * (kWarpRowThreads / 32) + (threadIdx.x >> 5);
+    if (b >= row1) return;
+    const int64_t t0 = 4 * b;
+    const int c = (int)min((int64_t)4, n_ctx - t0);  // tokens present in this block (1..4)
+    const float inv_c = 1.0f / (float)c;
+    const T *rb = raw + t0 * HD;
+    float p[PER];
+#pragma unroll
+    for (int k = 0; k < PER; ++k) {
+        const int e = lane + 32 * k;
+        float v[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) v[t] = t < c ? to_f32(rb[(int64_t)t * HD + e]) : 0.0f;
+        p[k] = ((v[0] + v[1]) + (v[2] + v[3])) * inv_c;
+    }
+    float cs[MH], sn[MH], wa[MH], wb[MH];
+#pragma unroll
+    for (int m = 0; m < MH; ++m) {
+        const int i = lane + 32 * m;
+        // the angle 4b * theta_i, formed and reduced modulo 2 pi in fp64; fp32 sincos of
+        // the reduced angle (|r| <= pi)
+        const double phi = (4.0 * (double)b) * tab.theta[i];
+        const double k = rint(phi * kInvTwoPi);
+        const float r = (float)fma(-k, kTwoPi, phi);
+        sincosf(r, &sn[m], &cs[m]);
+        wa[m] = w[i];
+        wb[m] = w[i + HALF];
+    }
+    TP *out_row = pooled + b * (int64_t)HD;
+#pragma unroll
+    for (int h = 0; h < NH; ++h) {
+        float ss = 0.0f;
+#pragma unroll
+        for (int j = 0; j < PH; ++j) ss = fmaf(p[h * PH + j], p[h * PH + j], ss);
+        ss = warp_sum(ss);
+        const float inv = 1.0f / sqrtf(ss / (float)D + eps);
+        TP *o = out_row + (int64_t)h * D;
+#pragma unroll
+        for (int m = 0; m < MH; ++m) {
+            const int i = lane + 32 * m;
+            const float ya = p[h * PH + m] * inv * wa[m];
+            const float yb = p[h * PH + m + MH] * inv * wb[m];
+            const float za = ya * cs[m] - yb * sn[m];
+            const float zb = ya * sn[m] + yb * cs[m];
+            store_pooled(o + i, za);
+            store_pooled(o + i + HALF, zb);
+        }
+    }
+}
+
 }  // namespace
 
 void make_rope_table(RopeTable *tab, int d, double base)
@@ -64,6 +137,17 @@ cudaError_t launch_pool_typed(const void *raw_k, int64_t n_ctx, int H, int d,
                               int64_t row0, int64_t row1, uint32_t *zero_hist, int64_t n,
                               cudaStream_t st)
 {
+    // many rows of the usual shapes: one warp per row
+    if (n >= 64 && ((d == 128 && H == 16) || (d == 64 && H == 4))) {
+        const unsigned grid = (unsigned)((n + kWarpRowThreads / 32 - 1) / (kWarpRowThreads / 32));
+        if (d == 128)
+            return launch(pool_rows_warp_kernel<T, TP, 128, 16>, dim3(grid), dim3(kWarpRowThreads),
+                          0, st, 1, (const T *)raw_k, n_ctx, norm_w, eps, tab, (TP *)pooled, row0,
+                          row1, zero_hist);
+        return launch(pool_rows_warp_kernel<T, TP, 64, 4>, dim3(grid), dim3(kWarpRowThreads), 0,
+                      st, 1, (const T *)raw_k, n_ctx, norm_w, eps, tab, (TP *)pooled, row0, row1,
+                      zero_hist);
+    }
     const size_t smem = sizeof(float) * ((size_t)H * d + (size_t)d);
     auto k = pool_update_kernel<T, TP>;
     const cudaError_t e = ensure_kernel_attrs<pool_update_kernel<T, TP>>(smem);
