@@ -137,14 +137,12 @@ cudaError_t launch_pool_typed(const void *raw_k, int64_t n_ctx, int H, int d,
                               int64_t row0, int64_t row1, uint32_t *zero_hist, int64_t n,
                               cudaStream_t st)
 {
-    // many rows of the usual shapes: one warp per row
-    if (n >= 64 && ((d == 128 && H == 16) || (d == 64 && H == 4))) {
+    // enough rows of the indexer's shape to fill the GPU (16 rows in flight per SM): one warp
+    // per row; fewer rows finish sooner as one CTA each, whose 512 threads shorten a row's
+    // chain of loads
+    if (n >= 2048 && d == 128 && H == 16) {
         const unsigned grid = (unsigned)((n + kWarpRowThreads / 32 - 1) / (kWarpRowThreads / 32));
-        if (d == 128)
-            return launch(pool_rows_warp_kernel<T, TP, 128, 16>, dim3(grid), dim3(kWarpRowThreads),
-                          0, st, 1, (const T *)raw_k, n_ctx, norm_w, eps, tab, (TP *)pooled, row0,
-                          row1, zero_hist);
-        return launch(pool_rows_warp_kernel<T, TP, 64, 4>, dim3(grid), dim3(kWarpRowThreads), 0,
+        return launch(pool_rows_warp_kernel<T, TP, 128, 16>, dim3(grid), dim3(kWarpRowThreads), 0,
                       st, 1, (const T *)raw_k, n_ctx, norm_w, eps, tab, (TP *)pooled, row0, row1,
                       zero_hist);
     }
